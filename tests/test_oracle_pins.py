@@ -1,0 +1,374 @@
+"""Pins of the fp64 oracle against facts that do not come from the oracle itself.
+
+Each test fixes one piece of the oracle against something independent: a
+published value (golden files with citations), a closed form, a library routine,
+an invariant, or brute force over exact rationals on tiny inputs.
+"""
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _golden_lines(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return [ln.split("#")[0].strip() for ln in f if ln.split("#")[0].strip()]
+
+
+# ------------------------------------------------------------------ generator
+
+
+def test_splitmix64_published_vectors():
+    for ln in _golden_lines("splitmix64_vectors.txt"):
+        state, i, out = ln.split()
+        assert oracle.splitmix64_at(int(state), int(i)) == int(out, 16)
+        assert synth.mix64_int(int(state) + (int(i) + 1) * synth.G) == int(out, 16)
+
+
+def test_counter_mode_two_implementations_agree():
+    for seed, stream, i in [(0, 0, 0), (1, 7, 12345), (2**63 + 5, 2**40, 2**33), (1001, 1791, 99)]:
+        assert oracle.u64(seed, stream, i) == synth.u64_int(seed, stream, i)
+    arr = synth.u64_array(3, 9, 100, 50)
+    assert [int(v) for v in arr] == [oracle.u64(3, 9, 100 + j) for j in range(50)]
+
+
+def test_generated_expert_bytes_follow_the_recipe():
+    H, I = 64, 32
+    codes, scales = oracle.gen_expert(1, 5, H, I)
+    assert codes.size == 3 * H * I // 2 and scales.size == 3 * H * I // 32
+    for b in [0, 1, 7, 8, 100, codes.size - 1]:
+        r = synth.u64_int(1, 10, b // 8)
+        assert codes[b] == (r >> (8 * (b % 8))) & 0xFF
+    for j in [0, 3, scales.size - 1]:
+        assert scales[j] == 118 + (synth.u64_int(1, 11, j) >> 32) % 5
+    big_c, big_s = oracle.gen_expert(7, 3, 1024, 512)
+    assert set(np.unique(big_s)) == {118, 119, 120, 121, 122}
+    nib = np.concatenate([big_c & 15, big_c >> 4])
+    hist = np.bincount(nib, minlength=16) / nib.size
+    assert np.all(np.abs(hist - 1 / 16) < 0.002)
+
+
+# ----------------------------------------------------------------- MX formats
+
+
+def test_e2m1_table_from_spec_and_bitfields():
+    rows = [ln.split() for ln in _golden_lines("e2m1_e8m0.txt")]
+    for r in rows:
+        if r[0] == "e8m0":
+            b, v = int(r[1]), float(r[2])
+            assert oracle.e8m0_value(b) == v
+            continue
+        code, v = int(r[0]), float(r[1])
+        got = oracle.e2m1_value(code)
+        assert got == v and math.copysign(1, got) == math.copysign(1, v)
+        s, e, m = code >> 3, (code >> 1) & 3, code & 1
+        bits = (m * 0.5) if e == 0 else 2.0 ** (e - 1) * (1 + m / 2)
+        assert got == (-bits if s else bits)
+
+
+def test_e8m0_all_bytes():
+    for b in range(255):
+        assert oracle.e8m0_value(b) == math.ldexp(1.0, b - 127)
+    assert math.isnan(oracle.e8m0_value(255))
+
+
+def test_e4m3_values_match_torch():
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    tv = codes.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    for c in range(256):
+        v = oracle.e4m3_value(c)
+        if math.isnan(tv[c]):
+            assert math.isnan(v)
+        else:
+            assert v == tv[c]
+
+
+def test_e4m3_encode_round_trip_midpoints_and_saturation():
+    finite = [c for c in range(127)]
+    vals = [oracle.e4m3_value(c) for c in finite]
+    for c, v in zip(finite, vals):
+        assert oracle.e4m3_encode(v) == c
+        assert oracle.e4m3_encode(-v) == (c | 0x80)
+    for c in range(126):                        # exact midpoints go to the even code
+        mid = (vals[c] + vals[c + 1]) / 2
+        want = c if c % 2 == 0 else c + 1
+        assert oracle.e4m3_encode(mid) == want
+        # just off the midpoint goes to the nearer neighbour
+        eps = (vals[c + 1] - vals[c]) * 1e-6
+        assert oracle.e4m3_encode(mid - eps) == c
+        assert oracle.e4m3_encode(mid + eps) == c + 1
+    for big in [448.0, 449.0, 464.0, 480.0, 1e6, 1e300]:
+        assert oracle.e4m3_encode(big) == 0x7E
+        assert oracle.e4m3_encode(-big) == 0xFE
+
+
+def test_e4m3_encode_matches_torch_in_range():
+    rng = np.random.default_rng(0)
+    v = rng.standard_normal(4000) * np.exp2(rng.integers(-12, 8, size=4000))
+    v = v[np.abs(v) < 440].astype(np.float32).astype(np.float64)   # fp32-exact, in range
+    t = torch.from_numpy(v.astype(np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    for a, c in zip(v, t):
+        assert oracle.e4m3_encode(a) == c
+
+
+def test_mxfp8_block_rule():
+    # amax 1.0 -> X = floor(log2 1) - 8 = -8 (byte 119); 1.0 -> 256 -> code exact
+    v = np.zeros(64)
+    v[0] = 1.0
+    v[5] = -0.75
+    v[32] = 500.0         # X = 8 - 8 = 0; 500 saturates to 448
+    v[33] = 3.0
+    codes, sb, deq = oracle.quant_mxfp8(v)
+    assert list(sb) == [119, 127]
+    assert deq[0] == 1.0 and deq[5] == -0.75
+    assert deq[32] == 448.0 and deq[33] == 3.0
+    z = oracle.quant_mxfp8(np.zeros(32))
+    assert z[1][0] == 0 and np.all(z[2] == 0)
+
+
+def test_mxfp8_error_bound_on_bf16_inputs():
+    # every element of a block is within half an E4M3 step of its value, the step
+    # being 2^(X + e - 3) for element exponent e >= -6 (relative 2^-4 at most)
+    x = synth.bf16_bits_to_f64(synth.tokens_bf16(0, 0, 4, 1024)).ravel()
+    _, sb, deq = oracle.quant_mxfp8(x)
+    for b in range(0, x.size, 32):
+        X = int(sb[b // 32]) - 127
+        amax = np.max(np.abs(x[b:b + 32]))
+        assert 256 <= amax / 2.0 ** X < 512
+        err = np.abs(deq[b:b + 32] - x[b:b + 32])
+        bound = np.maximum(np.abs(x[b:b + 32]) * 2.0 ** -4, 2.0 ** (X - 10))
+        small = np.abs(x[b:b + 32]) / 2.0 ** X <= 448
+        assert np.all(err[small] <= bound[small])
+
+
+def test_bf16_round_against_fp32_path():
+    rng = np.random.default_rng(1)
+    v = (rng.standard_normal(3000) * np.exp2(rng.integers(-140, 120, size=3000))).astype(np.float32)
+    v = v.astype(np.float64)                    # fp32-exact values: one rounding either way
+    got = oracle.bf16_round(v)
+    want = torch.from_numpy(v.astype(np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(got, want)
+    assert oracle.bf16_round(np.array([1.0 + 2.0 ** -8]))[0] == 0x3F80       # tie -> even
+    assert oracle.bf16_round(np.array([1.0 + 3 * 2.0 ** -8]))[0] == 0x3F82   # tie -> even (up)
+    assert oracle.bf16_round(np.array([1e39]))[0] == 0x7F80
+
+
+# -------------------------------------------------------------------- routing
+
+
+def _bf16(rng, shape, scale=1.0):
+    return synth.bf16_bits_from_f64(rng.standard_normal(shape) * scale)
+
+
+def _brute_route(x_bits, W_bits, k, skew=None):
+    """Exact logits as rationals, sort by (-value, index)."""
+    x = [Fraction(float(v)) for v in synth.bf16_bits_to_f64(x_bits)]
+    out = []
+    for e in range(W_bits.shape[0]):
+        w = [Fraction(float(v)) for v in synth.bf16_bits_to_f64(W_bits[e])]
+        s = sum(a * b for a, b in zip(x, w))
+        if skew is not None:
+            s += Fraction(float(skew[e]))
+        out.append(s)
+    order = sorted(range(len(out)), key=lambda e: (-out[e], e))
+    return order[:k], out
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2, 3])
+def test_route_matches_exact_rationals(seed):
+    rng = np.random.default_rng(seed)
+    E, H = 24, 48
+    x = _bf16(rng, (3, H))
+    W = _bf16(rng, (E, H), 1 / np.sqrt(H))
+    skew = (rng.standard_normal(E) * 0.1).astype(np.float32) if seed % 2 else None
+    for k in (1, 5, 16, E):
+        idx, w, logits = oracle.route(x, W, k, skew)
+        for m in range(3):
+            want, exact = _brute_route(x[m], W, k, skew)
+            assert list(idx[m]) == want
+            # logits are the exact values rounded once to double
+            assert all(logits[m, e] == float(exact[e]) for e in range(E))
+            z = [math.exp(float(exact[e]) - float(exact[want[0]])) for e in want]
+            assert np.allclose(w[m], np.array(z) / sum(z), rtol=1e-14, atol=0)
+
+
+def test_route_planted_ties_and_near_ties():
+    rng = np.random.default_rng(7)
+    E, H = 20, 64
+    x = _bf16(rng, (1, H))
+    W = _bf16(rng, (E, H), 1 / np.sqrt(H))
+    # make experts 3, 11, 17 the clear winners and exactly equal: 11 is 3 with its
+    # elements permuted in pairs of equal x (same multiset of products) -> exact tie
+    W[3] = synth.bf16_bits_from_f64(np.sign(synth.bf16_bits_to_f64(x[0])) * 0.5)
+    W[11] = W[3]
+    W[17] = W[3]
+    # expert 5: expert 3 with one element nudged by one bf16 ulp -> near tie
+    W[5] = W[3]
+    W[5, 10] = W[5, 10] + 1 if synth.bf16_bits_to_f64(x[0, 10]) > 0 else W[5, 10] - 1
+    idx, w, logits = oracle.route(x, W, 6)
+    want, exact = _brute_route(x[0], W, 6)
+    assert list(idx[0]) == want
+    assert exact[3] == exact[11] == exact[17] and exact[5] != exact[3]
+    pos = list(idx[0])
+    assert pos.index(3) < pos.index(11) < pos.index(17)     # ties -> lower index first
+    assert w[0, pos.index(3)] == w[0, pos.index(11)]
+
+
+def test_route_weights_sum_to_one_and_are_monotone():
+    x = synth.tokens_bf16(0, 0, 5, 1024)
+    W = synth.router_bf16(2, 64, 1024)
+    idx, w, logits = oracle.route(x, W, 16)
+    assert np.all(np.abs(w.sum(axis=1) - 1.0) < 1e-15)
+    for m in range(5):
+        l = logits[m, idx[m]]
+        assert np.all(np.diff(l) <= 0) and np.all(np.diff(w[m]) <= 0)
+
+
+# ------------------------------------------------------------------ the expert
+
+
+def _dequant(codes, scales, rows, K):
+    """Dense matrix from logical MXFP4 bytes, by the OCP bit-field definition."""
+    c = np.asarray(codes, dtype=np.uint8).reshape(rows, K // 2)
+    nib = np.empty((rows, K), dtype=np.int64)
+    nib[:, 0::2] = c & 15
+    nib[:, 1::2] = c >> 4
+    s, e, m = nib >> 3, (nib >> 1) & 3, nib & 1
+    mag = np.where(e == 0, m * 0.5, np.exp2(e - 1.0) * (1 + m / 2))
+    val = np.where(s == 1, -mag, mag)
+    sc = np.exp2(np.asarray(scales, dtype=np.float64).reshape(rows, K // 32) - 127)
+    return val * np.repeat(sc, 32, axis=1)
+
+
+def _split(codes, scales, H, I):
+    n1, n2 = I * H // 2, 2 * I * H // 2
+    s1, s2 = I * H // 32, 2 * I * H // 32
+    return ((codes[:n1], scales[:s1]), (codes[n1:n2], scales[s1:s2]), (codes[n2:], scales[s2:]))
+
+
+def test_zero_code_expert_contributes_zero():
+    H, I = 256, 128
+    codes = np.zeros(3 * H * I // 2, dtype=np.uint8)
+    scales = np.full(3 * H * I // 32, 120, dtype=np.uint8)
+    x = synth.bf16_bits_to_f64(synth.tokens_bf16(0, 0, 2, H))
+    y, h = oracle.expert_forward(codes, scales, H, I, x)
+    assert np.all(y == 0.0) and np.all(h == 0.0)
+    codes8 = np.full_like(codes, 0x88)          # -0 codes
+    y, h = oracle.expert_forward(codes8, scales, H, I, x)
+    assert np.all(y == 0.0)
+
+
+def test_all_ones_closed_form():
+    # every code 2 (value 1.0), every scale byte 127 (2^0): each gate and up row is
+    # s = sum(x), h = silu(s) * s for every i, and every output is I * h
+    H, I = 512, 256
+    codes = np.full(3 * H * I // 2, 0x22, dtype=np.uint8)
+    scales = np.full(3 * H * I // 32, 127, dtype=np.uint8)
+    x = synth.bf16_bits_to_f64(synth.tokens_bf16(0, 3, 1, H)) / 8
+    s = math.fsum(x[0])
+    hval = s / (1 + math.exp(-s)) * s
+    y, h = oracle.expert_forward(codes, scales, H, I, x)
+    assert np.allclose(h, hval, rtol=1e-13, atol=0)
+    assert np.allclose(y, I * hval, rtol=1e-13, atol=0)
+
+
+def test_expert_matches_dense_dequantised_matmul():
+    H, I = 128, 64
+    codes, scales = oracle.gen_expert(11, 2, H, I)
+    (cg, sg), (cu, su), (cd, sd) = _split(codes, scales, H, I)
+    Wg, Wu, Wd = _dequant(cg, sg, I, H), _dequant(cu, su, I, H), _dequant(cd, sd, H, I)
+    x = synth.bf16_bits_to_f64(synth.tokens_bf16(4, 0, 3, H))
+    g, u = x @ Wg.T, x @ Wu.T
+    h_ref = g / (1 + np.exp(-g)) * u
+    y_ref = h_ref @ Wd.T
+    y, h = oracle.expert_forward(codes, scales, H, I, x)
+    assert np.allclose(h, h_ref, rtol=1e-12, atol=1e-12 * np.abs(h_ref).max())
+    assert np.allclose(y, y_ref, rtol=1e-12, atol=1e-12 * np.abs(y_ref).max())
+
+
+def test_power_of_two_linearity_of_down_scales():
+    H, I = 128, 64
+    codes, scales = oracle.gen_expert(5, 1, H, I)
+    x = synth.bf16_bits_to_f64(synth.tokens_bf16(0, 0, 1, H))
+    y1, h1 = oracle.expert_forward(codes, scales, H, I, x)
+    s2 = scales.copy()
+    s2[2 * I * H // 32:] += 1                  # every down scale doubled
+    y2, h2 = oracle.expert_forward(codes, s2, H, I, x)
+    assert np.array_equal(h1, h2) and np.array_equal(y2, 2 * y1)
+
+
+def test_dense_k_equals_E_is_softmax_moe():
+    E, H, I = 8, 64, 32
+    pool = oracle.SyntheticPool(21, E, H, I)
+    x = synth.tokens_bf16(0, 0, 2, H)
+    Wr = synth.router_bf16(22, E, H)
+    d = oracle.decode_layer(pool, x, Wr, E)
+    xf = synth.bf16_bits_to_f64(x)
+    logits = xf @ synth.bf16_bits_to_f64(Wr).T           # fp64 sum: fine for weights
+    p = np.exp(logits - logits.max(axis=1, keepdims=True))
+    p /= p.sum(axis=1, keepdims=True)
+    y = np.zeros((2, H))
+    for e in range(E):
+        codes, scales = pool(e)
+        (cg, sg), (cu, su), (cd, sd) = _split(codes, scales, H, I)
+        g = xf @ _dequant(cg, sg, I, H).T
+        u = xf @ _dequant(cu, su, I, H).T
+        y += p[:, e:e + 1] * ((g / (1 + np.exp(-g)) * u) @ _dequant(cd, sd, H, I).T)
+    assert np.allclose(d["y"], y, rtol=1e-10, atol=1e-10 * np.abs(y).max())
+
+
+# ------------------------------------------------------------------- prefill
+
+
+def test_sort_pairs_is_the_stable_expert_major_order():
+    rng = np.random.default_rng(3)
+    T, k, E = 37, 4, 11
+    idx = np.stack([rng.choice(E, size=k, replace=False) for _ in range(T)]).astype(np.int32)
+    perm, inv, offsets = oracle.sort_pairs(idx, E)
+    pairs = sorted(range(T * k), key=lambda p: (idx[p // k, p % k], p))
+    assert list(perm) == pairs
+    assert sorted(perm) == list(range(T * k))
+    assert all(inv[perm[r]] == r for r in range(T * k))
+    for e in range(E):
+        seg = perm[offsets[e]:offsets[e + 1]]
+        assert all(idx[p // k, p % k] == e for p in seg)
+    assert offsets[-1] == T * k
+
+
+# --------------------------------------------------------------- stacked glue
+
+
+def test_prescale_is_exact_power_of_two():
+    x = synth.tokens_bf16(10, 0, 3, 1024)
+    x[1] = synth.bf16_bits_from_f64(synth.bf16_bits_to_f64(x[1]) * 37.0)
+    xh = oracle.prescale(x)
+    for r in range(3):
+        a, b = synth.bf16_bits_to_f64(x[r]), synth.bf16_bits_to_f64(xh[r])
+        amax = np.abs(b).max()
+        assert 4 <= amax < 8
+        ratio = a[a != 0] / b[a != 0]
+        assert np.all(ratio == ratio[0]) and math.log2(ratio[0]).is_integer()
+
+
+# --------------------------------------------------------------- byte counts
+
+
+def test_expert_record_size_matches_the_pages():
+    facts = {ln.split()[0]: float(ln.split()[1]) for ln in _golden_lines("page_facts.txt")}
+    E = facts["routed_experts_total"] / facts["moe_layers"]
+    assert E == synth.FULL.E == 896
+    per_expert = synth.expert_code_bytes(7168, 1600) + synth.expert_scale_bytes(7168, 1600)
+    assert per_expert == 18_278_400
+    assert synth.expert_code_bytes(1024, 512) + synth.expert_scale_bytes(1024, 512) == 835_584
+    mib = per_expert / 2**20
+    assert abs(mib - facts["expert_record_mib"]) / facts["expert_record_mib"] < 0.005
+    per_token = facts["experts_selected_per_layer"] * facts["moe_layers"] * mib / 1000
+    assert abs(per_token - facts["expert_data_per_token_gb"]) / facts["expert_data_per_token_gb"] < 0.01
