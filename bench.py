@@ -1,0 +1,291 @@
+"""Benchmark of the routed-expert MXFP4 MoE layer on GB300.
+
+Default workload: the full-size decode layer (E=896 experts, hidden 7168,
+intermediate 1600, top-16), 1000 seeded synthetic tokens decoded one at a time.
+One step = route + expert forward of all 1000 tokens (2 library calls, 5 kernels
+per token), captured once in a CUDA graph and replayed.  value = layer-tokens/s.
+
+    python bench.py [--steps K] [--warmup W] [--impl ours|reference] [--gpus N]
+
+--impl reference times the fp64 CPU oracle (the only baseline this workload has)
+on a bounded sample of the same tokens.  Under torchrun every rank runs an
+independent replica (the layer does not shard); rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "MoE-layer decode layer-tokens/s and expert-weight HBM GB/s (% of peak); prefill tok/s"
+WORKLOAD = "full-size decode layer: E=896, H=7168, I=1600, top-16, M=1, 1000 seeded tokens one at a time"
+NTOK = 1000
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def expert_bytes(H, I):
+    return synth.expert_code_bytes(H, I) + synth.expert_scale_bytes(H, I)
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index=0):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.out = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out = ""
+
+    def summary(self):
+        rows = [r.split(",") for r in self.out.strip().splitlines() if r.count(",") >= 7]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm = [float(r[0]) for r in rows if r[0].strip().replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if "Active" in r[4 + i] and "Not" not in r[4 + i]})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# --------------------------------------------------------------- reference arm
+
+
+def oracle_sample(ntok, threads=None):
+    """Time the fp64 oracle on `ntok` tokens of the workload (route + experts),
+    with the experts pre-generated outside the timed region."""
+    import oracle
+    s = synth.FULL
+    xb = synth.tokens_bf16(synth.TOKENS_SEED["full"], 0, ntok, s.H)
+    Wrb = synth.router_bf16(synth.router_seed(0), s.E, s.H)
+    idx, _, _ = oracle.route(xb, Wrb, s.k)
+    pool = oracle.SyntheticPool(synth.pool_seed(0), s.E, s.H, s.I, cache=ntok * s.k)
+    for e in sorted(set(int(v) for v in idx.ravel())):
+        pool(e)
+    t0 = time.perf_counter()
+    oracle.decode_layer(pool, xb, Wrb, s.k)
+    return time.perf_counter() - t0
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    ntok = args.ref_tokens
+    for _ in range(args.warmup if args.warmup < 1 else 1):
+        oracle_sample(1)
+    times = [oracle_sample(ntok) for _ in range(args.steps)]
+    tot = sum(times)
+    v = args.steps * ntok / tot
+    cb = {"value": v, "unit": "layer-tokens/s", "cores": cores, "kind": "oracle",
+          "sample": f"{ntok} tokens of the workload per step (route exact + 16 experts fp64), experts pre-generated"}
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "layer-tokens/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * tot / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "sample_tokens_per_step": ntok},
+        "cpu_baseline": cb,
+        "e2e": {"value": v, "unit": "layer-tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}))
+
+
+# ---------------------------------------------------------------------- ours
+
+
+def run_ours(args):
+    import torch
+    import mxfp4_routed_expert_topk_gb300 as moe
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    moe.build()
+
+    s = synth.FULL
+    pool = moe.Pool(s.E, s.H, s.I, device=dev)
+    moe.moe_pool_fill_synthetic(pool, synth.pool_seed(0))
+    Wrb = synth.router_bf16(synth.router_seed(0), s.E, s.H)
+    Wr = torch.from_numpy(Wrb.view(np.int16)).to(dev).view(torch.bfloat16)
+    xb = synth.tokens_bf16(synth.TOKENS_SEED["full"], 0, NTOK, s.H)
+    x_host = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).pin_memory()
+    x = x_host.to(dev)
+    y = torch.empty((NTOK, s.H), dtype=torch.bfloat16, device=dev)
+    y_host = torch.empty((NTOK, s.H), dtype=torch.bfloat16).pin_memory()
+    idx = torch.empty((NTOK, s.k), dtype=torch.int32, device=dev)
+    w = torch.empty((NTOK, s.k), dtype=torch.float32, device=dev)
+    ws_r = moe.workspace(moe.moe_workspace_size(moe.MOE_OP_ROUTE, s.E, s.H, s.I, 1, s.k), dev)
+    ws_d = moe.workspace(moe.moe_workspace_size(moe.MOE_OP_DECODE, s.E, s.H, s.I, 1, s.k), dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    def step():
+        for t in range(NTOK):
+            moe.moe_route_topk(x[t:t + 1], Wr, s.k, ws=ws_r, idx=idx[t:t + 1], w=w[t:t + 1])
+            moe.moe_expert_forward_decode(pool, x[t:t + 1], idx[t:t + 1], w[t:t + 1], ws=ws_d, y=y[t:t + 1])
+
+    with torch.cuda.stream(stream):
+        step()                                   # eager once (sets kernel attributes)
+        torch.cuda.synchronize()
+        assert moe.moe_check_status(ws_d) == 0 and moe.moe_check_status(ws_r) == 0
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            step()
+    torch.cuda.synchronize()
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(args.warmup):
+        graph.replay()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(args.steps):
+                graph.replay()
+            e1.record(stream)
+        barrier()
+    ms = e0.elapsed_time(e1)
+    if dist is not None:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_step = ms / args.steps
+    value = world * NTOK / (ms_step / 1000.0)
+
+    # end to end through the public API: pinned host x in, host y out, every step
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            x.copy_(x_host, non_blocking=True)
+            graph.replay()
+            y_host.copy_(y, non_blocking=True)
+        barrier()
+        e2, e3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e2.record(stream)
+        for _ in range(args.steps):
+            x.copy_(x_host, non_blocking=True)
+            graph.replay()
+            y_host.copy_(y, non_blocking=True)
+        e3.record(stream)
+        barrier()
+    e2e_ms = e2.elapsed_time(e3) / args.steps
+    h2d = x_host.numel() * 2
+    d2h = y_host.numel() * 2
+
+    # per-kernel device time over one more pass of the timed region (eager launches)
+    kern = {}
+    for name in ("decode_gateup", "decode_down", "route_logits", "route_select", "decode_prep"):
+        moe.moe_trace_begin(name)
+        with torch.cuda.stream(stream):
+            step()
+        n, tot = moe.moe_trace_end()
+        kern[name] = tot / max(n, 1)
+    hbm, peak_kind = peaks()
+    gu_bytes = s.k * (2 * s.I * s.H // 2 + 2 * s.I * s.H // 32)
+    dn_bytes = s.k * (s.H * s.I // 2 + s.H * s.I // 32)
+    layer_bytes = s.k * expert_bytes(s.H, s.I) + s.E * s.H * 2
+    achieved = gu_bytes / (kern["decode_gateup"] / 1000.0) / 1e9
+    layer_gbs = layer_bytes / (ms_step / 1000.0 / NTOK) / 1e9
+    traffic = None
+    tfile = os.path.join(ROOT, "profiles", "decode_gateup_traffic.json")
+    if os.path.exists(tfile):
+        traffic = json.load(open(tfile)).get("bytes_per_launch")
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+        secs = oracle_sample(args.ref_tokens)
+        cpu = {"value": args.ref_tokens / secs, "unit": "layer-tokens/s", "cores": cores, "kind": "oracle",
+               "sample": f"{args.ref_tokens} tokens of the workload (exact route + 16 experts, fp64), "
+                         "experts pre-generated outside the timing"}
+    launches = 5 * NTOK * args.steps
+    if rank == 0:
+        print(json.dumps({
+            "metric": METRIC, "value": value, "unit": "layer-tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "mxfp4(e2m1)xbf16, f16x2 block MAC, fp32 accumulate",
+            "data": "synthetic",
+            "config": {"workload": WORKLOAD, "parallelism": f"replicas x{world}",
+                       "l2": "inputs larger than L2: 16.6 GB resident pool, 16 fresh experts per token",
+                       "graph": "one CUDA graph per step (1000 tokens)"},
+            "expert_weight_hbm_gbs": layer_gbs, "hbm_frac_layer": layer_gbs / hbm,
+            "roofline": {"bound": "hbm", "kernel": "decode_gateup", "achieved": achieved, "peak": hbm,
+                         "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / hbm, "traffic": traffic,
+                         "algorithmic_bytes_per_launch": gu_bytes},
+            "kernel_ms": kern,
+            "cpu_baseline": cpu,
+            "e2e": {"value": NTOK / (e2e_ms / 1000.0) * world, "unit": "layer-tokens/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": launches,
+            "clocks": clk.summary(),
+        }))
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--ref-tokens", type=int, default=16)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

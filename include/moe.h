@@ -1,0 +1,192 @@
+/*
+ * moe.h -- C ABI of the GB300 (sm_103a) routed-expert MXFP4 MoE layer.
+ *
+ * The layer follows the Deltafin pages' problem statement: a token's hidden state
+ * goes in, the router picks 16 routed experts per layer ("Deltafin：在Apple Silicon
+ * Mac上运行Kimi K3", section 工作原理), the experts come from a resident pool of
+ * per-(layer, expert) MXFP4 records ("Deltafin 在配备四个 SSD 的 MacBook Pro 上…",
+ * section Deltafin 的功能), several rows can be verified in one pass (same page,
+ * section 可选的 Qwen 扩展) and prefill reads each expert once for all its rows
+ * (same page, section 作者仍需帮助的事项).  The layer math, which the pages do not
+ * spell out, is: router logits l = W_r x (+ skew), top-k by l with ties to the
+ * lower expert index, softmax over the k selected logits, per expert
+ * h = silu(W_g x) * (W_u x), o = W_d h, and y = sum_j w_j o_j (+ residual).
+ *
+ * Conventions (all entry points):
+ *  - Every pointer argument named *_dev, and every tensor argument unless stated
+ *    otherwise, is a DEVICE pointer owned by the caller.  The library never
+ *    allocates device memory, and keeps no reference after the call returns
+ *    (except the pool view, which refers to caller memory until destroyed).
+ *  - bf16 tensors are passed as uint16_t bit patterns.  Matrices are row-major
+ *    with the hidden dimension contiguous.
+ *  - `stream` is a cudaStream_t.  Calls are asynchronous on that stream; the
+ *    return value reports host-side validation and launch errors only.
+ *  - Errors the GPU detects (an expert index out of range, a non-finite router
+ *    logit, a bounded device wait that expired) are recorded in a status word at
+ *    the start of the workspace `ws` and returned by moe_check_status().  Kernels
+ *    never trap; a bad expert index makes its (token, slot) pair contribute zero.
+ *  - Supported shapes: 1 <= k <= 32, k <= E <= 65536, H a multiple of 128,
+ *    I a multiple of 32 (decode) or of 64 (prefill), H, I <= 32768.
+ */
+#ifndef MOE_H
+#define MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,       /* null pointer, negative size, k > E, ... */
+    MOE_ERR_UNSUPPORTED_SHAPE = 2, /* shape outside the supported set above */
+    MOE_ERR_WORKSPACE = 3,         /* ws smaller than moe_workspace_size() */
+    MOE_ERR_CUDA = 4,              /* a CUDA runtime call or launch failed */
+    MOE_ERR_BAD_INDEX = 5,         /* device: an expert index outside [0, E) */
+    MOE_ERR_TIMEOUT = 6,           /* device: a bounded wait gave up */
+    MOE_ERR_NONFINITE = 7          /* device: non-finite router input or logit */
+} moe_status;
+
+typedef void *moe_stream_t;        /* a cudaStream_t */
+typedef struct moe_pool moe_pool;  /* host-side view of a resident expert pool */
+
+/* Operation codes for moe_workspace_size(). */
+enum { MOE_OP_ROUTE = 0, MOE_OP_DECODE = 1, MOE_OP_GROUPED = 2 };
+
+/* Activation formats of the expert-major (grouped) path. */
+enum { MOE_ACT_MXFP8 = 1 };
+
+/* Element types of the grouped path's partial outputs. */
+enum { MOE_PARTIAL_F32 = 0, MOE_PARTIAL_BF16 = 1 };
+
+/* ------------------------------------------------------------ expert pool
+ * One record per expert (the pages' per-(layer, expert) MXFP4 file, 17.5 MiB at
+ * the full shape), resident in device memory the caller allocates.  A record
+ * holds W_gu = the gate and up rows interleaved in groups of 16 (rows 32q..32q+15
+ * are gate rows 16q..16q+15, rows 32q+16..32q+31 the matching up rows), shape
+ * [2I][H], and W_d [H][I], as packed E2M1 codes (two per byte, element 2j in
+ * the low nibble, K contiguous) followed by their E8M0 scale bytes (one per 32
+ * consecutive K elements, row-major).  Rows of W_d are padded with zero codes and
+ * zero scale bytes to a multiple of 128 elements. */
+
+/* Bytes one pool of E experts needs (a multiple of 1024 per record); 0 when the
+ * shape is unsupported. */
+size_t moe_pool_bytes(int E, int H, int I);
+
+/* Bytes of one expert record. */
+size_t moe_pool_record_bytes(int H, int I);
+
+/* Create a view of a pool over caller memory `dev_mem` of `bytes` bytes (at
+ * least moe_pool_bytes(E,H,I), 1024-byte aligned).  Contents are undefined until
+ * filled.  *out receives a host object freed by moe_pool_destroy(). */
+moe_status moe_pool_create(moe_pool **out, void *dev_mem, size_t bytes, int E, int H, int I);
+void moe_pool_destroy(moe_pool *pool);
+
+/* Fill experts [e_lo, e_hi) with synthetic data drawn on the device from the
+ * counter-based SplitMix64 definition (codes of expert e: byte b is byte b%8 of
+ * u64(seed, 2e, b/8) in the logical row-major order gate, up, down; scale byte j
+ * is 118 + (u64(seed, 2e+1, j) >> 32) % 5, i.e. exponents -9..-5), where
+ * u64(seed, s, i) = mix(key + (i+1) G), key = mix(mix(seed + G) ^ mix(s + 2G)),
+ * G = 0x9E3779B97F4A7C15, mix = the SplitMix64 finaliser. */
+moe_status moe_pool_fill_synthetic(moe_pool *pool, uint64_t seed, int e_lo, int e_hi,
+                                   moe_stream_t stream);
+
+/* Pack expert e from its logical row-major form (device buffers):
+ * codes_dev [3*H*I/2] = gate [I][H/2] | up [I][H/2] | down [H][I/2],
+ * scales_dev [3*H*I/32] = gate [I][H/32] | up [I][H/32] | down [H][I/32]. */
+moe_status moe_pool_upload_expert(moe_pool *pool, int e, const uint8_t *codes_dev,
+                                  const uint8_t *scales_dev, moe_stream_t stream);
+
+/* Inverse of moe_pool_upload_expert (for inspection and tests). */
+moe_status moe_pool_download_expert(const moe_pool *pool, int e, uint8_t *codes_dev,
+                                    uint8_t *scales_dev, moe_stream_t stream);
+
+/* ------------------------------------------------------------- workspace */
+
+/* Workspace bytes of operation `op` (MOE_OP_*) for M (decode) or T (prefill)
+ * rows.  The workspace is caller-owned device memory, 256-byte aligned; its
+ * first 256 bytes hold the device status word. */
+moe_status moe_workspace_size(int op, int E, int H, int I, int rows, int k, size_t *bytes);
+
+/* Clear the status word of `ws` (asynchronously, on `stream`). */
+moe_status moe_clear_status(void *ws, moe_stream_t stream);
+
+/* Synchronise `stream`, return the first device-detected error recorded in
+ * `ws` since it was last cleared (MOE_OK if none), and clear it. */
+moe_status moe_check_status(void *ws, moe_stream_t stream);
+
+const char *moe_status_string(moe_status s);
+
+/* ---------------------------------------------------------------- routing
+ * Router top-k with softmax ("工作原理": 16 experts per layer per token).
+ * x [M][H] bf16, Wr [E][H] bf16, skew [E] fp32 or NULL (added to the logits).
+ * Out: idx [M][k] int32, the k experts of largest exact logit
+ * sum_h x_h Wr[e,h] (+ skew_e) in descending order, ties to the lower index;
+ * w [M][k] fp32 = softmax over those k logits.  The selection is exact: fp32
+ * logits carry a rigorous error bound and any order the bound cannot decide is
+ * settled with exact integer arithmetic.  ws: MOE_OP_ROUTE bytes. */
+moe_status moe_route_topk(const uint16_t *x, int M, int H, const uint16_t *Wr, int E,
+                          const float *skew, int k, int32_t *idx, float *w,
+                          void *ws, size_t ws_bytes, moe_stream_t stream);
+
+/* ------------------------------------------------------- decode / verify
+ * Expert forward for M (1..32) rows that were routed by moe_route_topk: each
+ * distinct selected expert is read from the pool once and applied to every row
+ * routed to it (the pages' speculative-verify batch, "可选的 Qwen 扩展").
+ * x [M][H] bf16, idx/w [M][k] as from moe_route_topk, residual [M][H] bf16 or
+ * NULL.  Out: y [M][H] bf16 = sum_j w[m,j] * expert_{idx[m,j]}(x[m]) (+ residual),
+ * fp32 accumulation, rounded to nearest-even.  ws: MOE_OP_DECODE bytes. */
+moe_status moe_expert_forward_decode(const moe_pool *pool, const uint16_t *x, int M,
+                                     const int32_t *idx, const float *w, int k,
+                                     const uint16_t *residual, uint16_t *y,
+                                     void *ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Exact power-of-two pre-scale of layer inputs (stacked layers): for each row,
+ * out = x * 2^-p with p = floor(log2(max|x|)) - 2, so max|out| lies in [4, 8);
+ * an all-zero row is copied.  x, out [M][H] bf16. */
+moe_status moe_prescale(const uint16_t *x, int M, int H, uint16_t *out, moe_stream_t stream);
+
+/* ---------------------------------------------------- expert-major prefill
+ * Expert-major forward of T rows ("作者仍需帮助的事项": each expert read once per
+ * layer for all rows routed to it).  The T*k (token, slot) pairs p = t*k + j are
+ * stably sorted by expert: perm [T*k] (sorted position -> pair), inv_perm [T*k]
+ * (pair -> sorted position), offsets [E+1] (first sorted position of each
+ * expert).  With act_mode MOE_ACT_MXFP8 the rows are quantised to MXFP8 (E4M3
+ * elements, one E8M0 scale per 32, shared exponent floor(log2 amax) - 8,
+ * round-to-nearest-even with saturation) before W_g/W_u, and h likewise before
+ * W_d; the contractions run on the tensor cores as block-scaled MMAs.
+ * Out: partial [T*k][H] (partial_dtype MOE_PARTIAL_*), row r = o of pair perm[r]
+ * (unweighted).  ws: MOE_OP_GROUPED bytes. */
+moe_status moe_expert_forward_grouped(const moe_pool *pool, const uint16_t *x, int T,
+                                      const int32_t *idx, int k, int act_mode,
+                                      int32_t *perm, int32_t *inv_perm, int32_t *offsets,
+                                      void *partial, int partial_dtype,
+                                      void *ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Weighted combine of the grouped path: y[t] = sum_{j<k} w[t,j] *
+ * partial[inv_perm[t*k+j]] (+ residual[t]), summed in slot order j in fp32 and
+ * rounded to bf16.  No atomics: the result is deterministic. */
+moe_status moe_combine(const void *partial, int partial_dtype, const int32_t *inv_perm,
+                       const float *w, int T, int k, int H, const uint16_t *residual,
+                       uint16_t *y, moe_stream_t stream);
+
+/* ----------------------------------------------------------------- tracing
+ * Between moe_trace_begin(name) and moe_trace_end(), every launch of the named
+ * kernel ("route_logits", "route_select", "decode_prep", "decode_gateup",
+ * "decode_down", "sort_rank", "sort_scan", "sort_scatter", "gather_quant",
+ * "gemm_gateup", "gemm_down", "combine", "prescale") is bracketed by CUDA events
+ * on its stream (at most 65536 launches are recorded).  moe_trace_end()
+ * synchronises the device and returns the number of recorded launches and their
+ * summed device time in milliseconds.  Tracing is process-wide and not
+ * thread-safe; it creates CUDA events on first use but allocates no device
+ * memory. */
+moe_status moe_trace_begin(const char *kernel_name);
+moe_status moe_trace_end(int *launches, double *total_ms);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_H */

@@ -1,0 +1,288 @@
+"""ctypes binding of libmoe.so: argument marshalling only.
+
+Every function here forwards to the entry point of the same name in
+include/moe.h.  Tensors are PyTorch CUDA tensors (device memory and streams
+come from PyTorch); all computation happens in the library's CUDA kernels.  If
+the library has not been built the first call raises, there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmoe.so")
+
+MOE_OK = 0
+MOE_ERR_INVALID_ARG = 1
+MOE_ERR_UNSUPPORTED_SHAPE = 2
+MOE_ERR_WORKSPACE = 3
+MOE_ERR_CUDA = 4
+MOE_ERR_BAD_INDEX = 5
+MOE_ERR_TIMEOUT = 6
+MOE_ERR_NONFINITE = 7
+
+MOE_OP_ROUTE, MOE_OP_DECODE, MOE_OP_GROUPED = 0, 1, 2
+MOE_ACT_MXFP8 = 1
+MOE_PARTIAL_F32, MOE_PARTIAL_BF16 = 0, 1
+
+EXPORTED = [
+    "moe_pool_bytes", "moe_pool_record_bytes", "moe_pool_create", "moe_pool_destroy",
+    "moe_pool_fill_synthetic", "moe_pool_upload_expert", "moe_pool_download_expert",
+    "moe_workspace_size", "moe_clear_status", "moe_check_status", "moe_status_string",
+    "moe_route_topk", "moe_expert_forward_decode", "moe_prescale",
+    "moe_expert_forward_grouped", "moe_combine", "moe_trace_begin", "moe_trace_end",
+]
+
+
+class MoeError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {status_string(code)} ({code})")
+
+
+_lib = None
+_vp, _sz, _i, _u64 = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_uint64
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"libmoe.so is not built ({LIB_PATH}); run __graft_entry__.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        sig = {
+            "moe_pool_bytes": (_sz, [_i, _i, _i]),
+            "moe_pool_record_bytes": (_sz, [_i, _i]),
+            "moe_pool_create": (_i, [ctypes.POINTER(_vp), _vp, _sz, _i, _i, _i]),
+            "moe_pool_destroy": (None, [_vp]),
+            "moe_pool_fill_synthetic": (_i, [_vp, _u64, _i, _i, _vp]),
+            "moe_pool_upload_expert": (_i, [_vp, _i, _vp, _vp, _vp]),
+            "moe_pool_download_expert": (_i, [_vp, _i, _vp, _vp, _vp]),
+            "moe_workspace_size": (_i, [_i, _i, _i, _i, _i, _i, ctypes.POINTER(_sz)]),
+            "moe_clear_status": (_i, [_vp, _vp]),
+            "moe_check_status": (_i, [_vp, _vp]),
+            "moe_status_string": (ctypes.c_char_p, [_i]),
+            "moe_route_topk": (_i, [_vp, _i, _i, _vp, _i, _vp, _i, _vp, _vp, _vp, _sz, _vp]),
+            "moe_expert_forward_decode": (_i, [_vp, _vp, _i, _vp, _vp, _i, _vp, _vp, _vp, _sz, _vp]),
+            "moe_prescale": (_i, [_vp, _i, _i, _vp, _vp]),
+            "moe_expert_forward_grouped": (_i, [_vp, _vp, _i, _vp, _i, _i, _vp, _vp, _vp, _vp, _i, _vp, _sz,
+                                                _vp]),
+            "moe_combine": (_i, [_vp, _i, _vp, _vp, _i, _i, _i, _vp, _vp, _vp]),
+            "moe_trace_begin": (_i, [ctypes.c_char_p]),
+            "moe_trace_end": (_i, [ctypes.POINTER(_i), ctypes.POINTER(ctypes.c_double)]),
+        }
+        for name, (res, args) in sig.items():
+            f = getattr(L, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = L
+    return _lib
+
+
+def status_string(code: int) -> str:
+    return lib().moe_status_string(code).decode()
+
+
+def _check(code: int, where: str):
+    if code != MOE_OK:
+        raise MoeError(code, where)
+
+
+def _stream(stream=None):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _need(t, dtype, name):
+    if not (t.is_cuda and t.dtype == dtype and t.is_contiguous()):
+        raise ValueError(f"{name}: expected a contiguous CUDA {dtype} tensor")
+
+
+# ------------------------------------------------------------------ pool
+
+
+def moe_pool_bytes(E: int, H: int, I: int) -> int:
+    return int(lib().moe_pool_bytes(E, H, I))
+
+
+def moe_pool_record_bytes(H: int, I: int) -> int:
+    return int(lib().moe_pool_record_bytes(H, I))
+
+
+class Pool:
+    """A resident expert pool in a caller-owned (PyTorch) device buffer."""
+
+    def __init__(self, E: int, H: int, I: int, device="cuda", buffer: torch.Tensor | None = None):
+        self.E, self.H, self.I = E, H, I
+        nbytes = moe_pool_bytes(E, H, I)
+        if nbytes == 0:
+            raise MoeError(MOE_ERR_UNSUPPORTED_SHAPE, "moe_pool_bytes")
+        if buffer is None:
+            buffer = torch.empty(nbytes + 1024, dtype=torch.uint8, device=device)
+        self.buffer = buffer
+        off = (-buffer.data_ptr()) % 1024
+        self.mem = buffer[off:off + nbytes]
+        h = ctypes.c_void_p()
+        _check(lib().moe_pool_create(ctypes.byref(h), _ptr(self.mem), nbytes, E, H, I), "moe_pool_create")
+        self.handle = h
+
+    def __del__(self):
+        h = getattr(self, "handle", None)
+        if h is not None and _lib is not None:
+            _lib.moe_pool_destroy(h)
+            self.handle = None
+
+
+def moe_pool_fill_synthetic(pool: Pool, seed: int, e_lo: int = 0, e_hi: int | None = None, stream=None):
+    e_hi = pool.E if e_hi is None else e_hi
+    _check(lib().moe_pool_fill_synthetic(pool.handle, seed, e_lo, e_hi, _stream(stream)),
+           "moe_pool_fill_synthetic")
+
+
+def moe_pool_upload_expert(pool: Pool, e: int, codes: torch.Tensor, scales: torch.Tensor, stream=None):
+    _need(codes, torch.uint8, "codes")
+    _need(scales, torch.uint8, "scales")
+    _check(lib().moe_pool_upload_expert(pool.handle, e, _ptr(codes), _ptr(scales), _stream(stream)),
+           "moe_pool_upload_expert")
+
+
+def moe_pool_download_expert(pool: Pool, e: int, stream=None):
+    codes = torch.empty(3 * pool.H * pool.I // 2, dtype=torch.uint8, device=pool.mem.device)
+    scales = torch.empty(3 * pool.H * pool.I // 32, dtype=torch.uint8, device=pool.mem.device)
+    _check(lib().moe_pool_download_expert(pool.handle, e, _ptr(codes), _ptr(scales), _stream(stream)),
+           "moe_pool_download_expert")
+    return codes, scales
+
+
+# ------------------------------------------------------------- workspace
+
+
+def moe_workspace_size(op: int, E: int, H: int, I: int, rows: int, k: int) -> int:
+    n = ctypes.c_size_t()
+    _check(lib().moe_workspace_size(op, E, H, I, rows, k, ctypes.byref(n)), "moe_workspace_size")
+    return int(n.value)
+
+
+def workspace(nbytes: int, device="cuda") -> torch.Tensor:
+    """A zeroed workspace buffer (status word cleared), 256-byte aligned."""
+    buf = torch.zeros(nbytes + 256, dtype=torch.uint8, device=device)
+    off = (-buf.data_ptr()) % 256
+    return buf[off:off + nbytes]
+
+
+def moe_clear_status(ws: torch.Tensor, stream=None):
+    _check(lib().moe_clear_status(_ptr(ws), _stream(stream)), "moe_clear_status")
+
+
+def moe_check_status(ws: torch.Tensor, stream=None) -> int:
+    return int(lib().moe_check_status(_ptr(ws), _stream(stream)))
+
+
+def exact_fallbacks(ws: torch.Tensor) -> int:
+    """Router diagnostic: tokens that needed exact re-evaluation (status word slot 2)."""
+    return int(ws[8:12].view(torch.int32).item())
+
+
+# ---------------------------------------------------------------- layer
+
+
+def moe_route_topk(x: torch.Tensor, Wr: torch.Tensor, k: int, skew: torch.Tensor | None = None,
+                   ws: torch.Tensor | None = None, idx: torch.Tensor | None = None,
+                   w: torch.Tensor | None = None, stream=None):
+    _need(x, torch.bfloat16, "x")
+    _need(Wr, torch.bfloat16, "Wr")
+    M, H = x.shape
+    E = Wr.shape[0]
+    if skew is not None:
+        _need(skew, torch.float32, "skew")
+    if ws is None:
+        ws = workspace(moe_workspace_size(MOE_OP_ROUTE, E, H, 32, M, k), x.device)
+    idx = torch.empty((M, k), dtype=torch.int32, device=x.device) if idx is None else idx
+    w = torch.empty((M, k), dtype=torch.float32, device=x.device) if w is None else w
+    _check(lib().moe_route_topk(_ptr(x), M, H, _ptr(Wr), E, _ptr(skew), k, _ptr(idx), _ptr(w), _ptr(ws),
+                                ws.numel(), _stream(stream)), "moe_route_topk")
+    return idx, w
+
+
+def moe_expert_forward_decode(pool: Pool, x: torch.Tensor, idx: torch.Tensor, w: torch.Tensor,
+                              residual: torch.Tensor | None = None, ws: torch.Tensor | None = None,
+                              y: torch.Tensor | None = None, stream=None):
+    _need(x, torch.bfloat16, "x")
+    _need(idx, torch.int32, "idx")
+    _need(w, torch.float32, "w")
+    M, k = idx.shape
+    if residual is not None:
+        _need(residual, torch.bfloat16, "residual")
+    if ws is None:
+        ws = workspace(moe_workspace_size(MOE_OP_DECODE, pool.E, pool.H, pool.I, M, k), x.device)
+    y = torch.empty((M, pool.H), dtype=torch.bfloat16, device=x.device) if y is None else y
+    _check(lib().moe_expert_forward_decode(pool.handle, _ptr(x), M, _ptr(idx), _ptr(w), k, _ptr(residual),
+                                           _ptr(y), _ptr(ws), ws.numel(), _stream(stream)),
+           "moe_expert_forward_decode")
+    return y
+
+
+def moe_prescale(x: torch.Tensor, out: torch.Tensor | None = None, stream=None):
+    _need(x, torch.bfloat16, "x")
+    M, H = x.shape
+    out = torch.empty_like(x) if out is None else out
+    _check(lib().moe_prescale(_ptr(x), M, H, _ptr(out), _stream(stream)), "moe_prescale")
+    return out
+
+
+def moe_expert_forward_grouped(pool: Pool, x: torch.Tensor, idx: torch.Tensor, act_mode: int = MOE_ACT_MXFP8,
+                               partial_dtype: int = MOE_PARTIAL_F32, ws: torch.Tensor | None = None,
+                               out: dict | None = None, stream=None):
+    _need(x, torch.bfloat16, "x")
+    _need(idx, torch.int32, "idx")
+    T, k = idx.shape
+    dev = x.device
+    if ws is None:
+        ws = workspace(moe_workspace_size(MOE_OP_GROUPED, pool.E, pool.H, pool.I, T, k), dev)
+    if out is None:
+        pdt = torch.float32 if partial_dtype == MOE_PARTIAL_F32 else torch.bfloat16
+        out = {"perm": torch.empty(T * k, dtype=torch.int32, device=dev),
+               "inv_perm": torch.empty(T * k, dtype=torch.int32, device=dev),
+               "offsets": torch.empty(pool.E + 1, dtype=torch.int32, device=dev),
+               "partial": torch.empty((T * k, pool.H), dtype=pdt, device=dev)}
+    _check(lib().moe_expert_forward_grouped(pool.handle, _ptr(x), T, _ptr(idx), k, act_mode, _ptr(out["perm"]),
+                                            _ptr(out["inv_perm"]), _ptr(out["offsets"]), _ptr(out["partial"]),
+                                            partial_dtype, _ptr(ws), ws.numel(), _stream(stream)),
+           "moe_expert_forward_grouped")
+    return out
+
+
+def moe_combine(partial: torch.Tensor, inv_perm: torch.Tensor, w: torch.Tensor, residual: torch.Tensor | None = None,
+                y: torch.Tensor | None = None, stream=None):
+    _need(inv_perm, torch.int32, "inv_perm")
+    _need(w, torch.float32, "w")
+    T, k = w.shape
+    H = partial.shape[1]
+    pdt = MOE_PARTIAL_F32 if partial.dtype == torch.float32 else MOE_PARTIAL_BF16
+    y = torch.empty((T, H), dtype=torch.bfloat16, device=partial.device) if y is None else y
+    _check(lib().moe_combine(_ptr(partial), pdt, _ptr(inv_perm), _ptr(w), T, k, H, _ptr(residual), _ptr(y),
+                             _stream(stream)), "moe_combine")
+    return y
+
+
+# --------------------------------------------------------------- tracing
+
+
+def moe_trace_begin(kernel_name: str):
+    _check(lib().moe_trace_begin(kernel_name.encode()), "moe_trace_begin")
+
+
+def moe_trace_end():
+    """(launches, total device milliseconds) of the traced kernel since moe_trace_begin."""
+    n = ctypes.c_int()
+    ms = ctypes.c_double()
+    _check(lib().moe_trace_end(ctypes.byref(n), ctypes.byref(ms)), "moe_trace_end")
+    return int(n.value), float(ms.value)

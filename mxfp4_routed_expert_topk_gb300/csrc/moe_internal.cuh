@@ -1,0 +1,145 @@
+// Internal declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_fp16.h>
+#include <cuda_bf16.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+constexpr int kMaxK = 32;      // slots per row
+constexpr int kMaxDecodeRows = 32;
+constexpr int kGroupRows = 16; // gate/up interleave granularity in W_gu
+
+// Device-side view of a resident pool (all offsets in bytes within a record).
+struct PoolView {
+    uint8_t *base;
+    uint64_t rec;       // bytes per expert record
+    int E, H, I;
+    int Ip;             // I rounded up to a multiple of 128 (W_d row length in elements)
+    uint64_t off_d;     // W_d codes
+    uint64_t off_sgu;   // W_gu scales
+    uint64_t off_sd;    // W_d scales
+    int ld_gu;          // bytes per W_gu code row  = H/2
+    int ld_d;           // bytes per W_d code row   = Ip/2
+    int lds_gu;         // scale bytes per W_gu row = H/32
+    int lds_d;          // scale bytes per W_d row  = Ip/32
+};
+
+}  // namespace moe
+
+struct moe_pool {
+    moe::PoolView v;
+    size_t bytes;
+};
+
+namespace moe {
+
+// ------------------------------------------------------------ status word
+// The first 256 bytes of every workspace: [0] first error code, [1] detail,
+// [2] count of exact-arithmetic fallbacks taken by the router (diagnostic).
+struct StatusWord {
+    unsigned int code;
+    unsigned int detail;
+    unsigned int exact_fallbacks;
+    unsigned int pad[61];
+};
+
+__device__ __forceinline__ void set_status(StatusWord *s, unsigned int code, unsigned int detail) {
+    if (s == nullptr) return;
+    if (atomicCAS(&s->code, 0u, code) == 0u) s->detail = detail;
+}
+
+__host__ __device__ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// ---------------------------------------------------------- small helpers
+
+__device__ __forceinline__ float bf16_bits_to_float(uint16_t b) {
+    return __uint_as_float(((unsigned int)b) << 16);
+}
+
+// E8M0 byte -> 2^(b-127) as fp32 (b = 0 gives the subnormal 2^-127, b = 255 NaN).
+__device__ __forceinline__ float e8m0_to_float(unsigned int b) {
+    float v = __uint_as_float(b << 23);
+    v = (b == 0u) ? __uint_as_float(0x00400000u) : v;
+    v = (b == 255u) ? __uint_as_float(0x7fc00000u) : v;
+    return v;
+}
+
+// Four packed bytes of E2M1 pairs -> four f16x2 (low nibble -> low half).
+__device__ __forceinline__ void e2m1x8_to_f16x2x4(unsigned int q, unsigned int &h0, unsigned int &h1,
+                                                   unsigned int &h2, unsigned int &h3) {
+    asm("{\n\t.reg .b8 a0, a1, a2, a3;\n\t"
+        "mov.b32 {a0, a1, a2, a3}, %4;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %0, a0;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %1, a1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %2, a2;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %3, a3;\n\t}"
+        : "=r"(h0), "=r"(h1), "=r"(h2), "=r"(h3)
+        : "r"(q));
+}
+
+__device__ __forceinline__ unsigned int hfma2_u32(unsigned int a, unsigned int b, unsigned int c) {
+    unsigned int d;
+    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+__device__ __forceinline__ float f16x2_sum_to_float(unsigned int v) {
+    __half2 h = *reinterpret_cast<__half2 *>(&v);
+    return __low2float(h) + __high2float(h);
+}
+
+// 16-byte streaming load that does not allocate in L1.
+__device__ __forceinline__ uint4 ldg_stream16(const void *p) {
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+
+__device__ __forceinline__ unsigned char ldg_stream_u8(const void *p) {
+    unsigned short r;
+    asm volatile("ld.global.nc.L1::no_allocate.u8 %0, [%1];" : "=h"(r) : "l"(p));
+    return (unsigned char)r;
+}
+
+// Kernel tracing (api.cu): bracket one launch of kernel `name` with events.
+void trace_pre(const char *name, cudaStream_t st);
+void trace_post(const char *name, cudaStream_t st);
+
+struct TraceScope {
+    const char *name;
+    cudaStream_t st;
+    TraceScope(const char *n, cudaStream_t s) : name(n), st(s) { trace_pre(name, st); }
+    ~TraceScope() { trace_post(name, st); }
+};
+
+// Launch helpers implemented per translation unit.
+cudaError_t launch_pool_kernel(const PoolView &v, int mode, uint64_t seed, int e_lo, int e_hi,
+                               const uint8_t *codes, const uint8_t *scales, uint8_t *out_codes,
+                               uint8_t *out_scales, cudaStream_t st);
+
+size_t route_workspace_bytes(int E, int M, int k);
+cudaError_t launch_route(const uint16_t *x, int M, int H, const uint16_t *Wr, int E, const float *skew,
+                         int k, int32_t *idx, float *w, void *ws, cudaStream_t st);
+
+size_t decode_workspace_bytes(int E, int H, int I, int M, int k);
+cudaError_t launch_decode(const PoolView &v, const uint16_t *x, int M, const int32_t *idx, const float *w,
+                          int k, const uint16_t *residual, uint16_t *y, void *ws, cudaStream_t st);
+
+cudaError_t launch_prescale(const uint16_t *x, int M, int H, uint16_t *out, cudaStream_t st);
+
+size_t grouped_workspace_bytes(int E, int H, int I, int T, int k);
+cudaError_t launch_grouped(const PoolView &v, const uint16_t *x, int T, const int32_t *idx, int k,
+                           int act_mode, int32_t *perm, int32_t *inv_perm, int32_t *offsets,
+                           void *partial, int partial_dtype, void *ws, cudaStream_t st);
+cudaError_t launch_combine(const void *partial, int partial_dtype, const int32_t *inv_perm, const float *w,
+                           int T, int k, int H, const uint16_t *residual, uint16_t *y, cudaStream_t st);
+
+}  // namespace moe

@@ -1,0 +1,225 @@
+// Expert-major prefill path ("作者仍需帮助的事项" on the four-SSD page: read each
+// expert once per layer and process all of its routed rows together).
+//
+//   sort_rank_kernel / sort_scan_kernel / sort_scatter_kernel
+//        stable counting sort of the pairs p = t*k + j by expert (bit-exact perm)
+//   gather_quant_kernel
+//        rows of x in sorted order, quantised to MXFP8 (E4M3 + E8M0 per 32)
+//   grouped GEMMs (tcgen05, block-scaled)               -- gemm.cu
+//   combine_kernel
+//        y[t] = sum_j w[t,j] partial[inv_perm[t*k+j]] (+ residual), slot order
+#include "moe_internal.cuh"
+#include "prefill_internal.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kSortBlock = 1024;  // pairs per block of the counting sort
+
+// Block b: local rank of each of its pairs among the block's pairs of the same
+// expert (in pair order), and the block's per-expert counts cnt[b][e].
+__global__ void __launch_bounds__(kSortBlock) sort_rank_kernel(const int32_t *__restrict__ idx, int P, int E,
+                                                               int *__restrict__ local_rank, int *__restrict__ cnt,
+                                                               StatusWord *st) {
+    __shared__ int es[kSortBlock];
+    __shared__ int hist[kMaxSortE];
+    const int b = blockIdx.x, tid = threadIdx.x;
+    const int p = b * kSortBlock + tid;
+    for (int e = tid; e < E; e += blockDim.x) hist[e] = 0;
+    int e = -1;
+    if (p < P) {
+        e = idx[p];
+        if (e < 0 || e >= E) {
+            set_status(st, MOE_ERR_BAD_INDEX, (unsigned)p);
+            e = -1;
+        }
+    }
+    es[tid] = e;
+    __syncthreads();
+    if (e >= 0) {
+        int r = 0;
+        for (int q = 0; q < tid; q++) r += (es[q] == e);
+        local_rank[p] = r;
+        atomicAdd(&hist[e], 1);
+    }
+    __syncthreads();
+    for (int x = tid; x < E; x += blockDim.x) cnt[(size_t)b * E + x] = hist[x];
+}
+
+// One CTA: prior[b][e] = sum_{b'<b} cnt[b'][e]; offsets = exclusive scan of totals.
+__global__ void __launch_bounds__(1024) sort_scan_kernel(int nblocks, int E, const int *__restrict__ cnt,
+                                                         int *__restrict__ prior, int32_t *__restrict__ offsets) {
+    __shared__ int tot[kMaxSortE];
+    __shared__ int warp_sum[32];
+    const int tid = threadIdx.x;
+    for (int e = tid; e < E; e += blockDim.x) {
+        int run = 0;
+        for (int b = 0; b < nblocks; b++) {
+            prior[(size_t)b * E + e] = run;
+            run += cnt[(size_t)b * E + e];
+        }
+        tot[e] = run;
+    }
+    __syncthreads();
+    // exclusive scan of tot[0..E) with 1024 threads, each owning a contiguous chunk
+    const int per = (E + blockDim.x - 1) / blockDim.x;
+    const int lo = tid * per, hi = min(E, lo + per);
+    int s = 0;
+    for (int e = lo; e < hi; e++) s += tot[e];
+    // block-wide exclusive scan of s
+    const int lane = tid & 31, warp = tid >> 5;
+    int incl = s;
+    for (int off = 1; off < 32; off <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += v;
+    }
+    if (lane == 31) warp_sum[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        int w = warp_sum[lane];
+        for (int off = 1; off < 32; off <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, w, off);
+            if (lane >= off) w += v;
+        }
+        warp_sum[lane] = w;  // inclusive over warps
+    }
+    __syncthreads();
+    int base = incl - s + (warp > 0 ? warp_sum[warp - 1] : 0);
+    for (int e = lo; e < hi; e++) {
+        offsets[e] = base;
+        base += tot[e];
+    }
+    if (tid == blockDim.x - 1) offsets[E] = base;
+}
+
+__global__ void sort_scatter_kernel(const int32_t *__restrict__ idx, int P, int E, const int *__restrict__ local_rank,
+                                    const int *__restrict__ prior, const int32_t *__restrict__ offsets,
+                                    int32_t *__restrict__ perm, int32_t *__restrict__ inv_perm) {
+    const int p = blockIdx.x * blockDim.x + threadIdx.x;
+    if (p >= P) return;
+    const int e = idx[p];
+    if (e < 0 || e >= E) {
+        inv_perm[p] = -1;
+        return;
+    }
+    const int b = p / kSortBlock;
+    const int pos = offsets[e] + prior[(size_t)b * E + e] + local_rank[p];
+    perm[pos] = p;
+    inv_perm[p] = pos;
+}
+
+// Sorted row r (one warp per row): Xs[r] = MXFP8(x[perm[r] / k]).  Shared exponent
+// X = floor(log2 amax) - 8 per 32-block (clamped to [-127, 127]); codes are
+// RNE(x / 2^X) to E4M3 with saturation.  x / 2^X is exact for bf16 input.
+__global__ void gather_quant_kernel(const uint16_t *__restrict__ x, int H, int k, int nrows,
+                                    const int32_t *__restrict__ perm, uint8_t *__restrict__ xq,
+                                    uint8_t *__restrict__ xs) {
+    const int lane = threadIdx.x & 31;
+    const int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    if (r >= nrows) return;
+    const int t = perm[r] / k;
+    const uint16_t *xr = x + (size_t)t * H;
+    uint8_t *qr = xq + (size_t)r * H;
+    for (int b0 = 0; b0 < H; b0 += 32) {
+        const float v = bf16_bits_to_float(xr[b0 + lane]);
+        float a = fabsf(v);
+        for (int off = 16; off > 0; off >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, off));
+        int X = -127;
+        if (a > 0.f) {
+            int ex;
+            frexpf(a, &ex);
+            X = max(-127, min(127, ex - 1 - 8));
+        }
+        const float sv = ldexpf(v, -X);
+        unsigned short pair;
+        asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(pair) : "f"(0.f), "f"(sv));
+        qr[b0 + lane] = (uint8_t)(pair & 0xFF);
+        if (lane == 0) xs[(size_t)r * (H / 32) + b0 / 32] = (uint8_t)(X + 127);
+    }
+}
+
+template <typename PT>
+__device__ __forceinline__ float load_partial(const PT *p);
+template <>
+__device__ __forceinline__ float load_partial<float>(const float *p) { return *p; }
+template <>
+__device__ __forceinline__ float load_partial<__nv_bfloat16>(const __nv_bfloat16 *p) { return __bfloat162float(*p); }
+
+// Block per token; threads over the hidden dimension.  Slot order j, fp32.
+template <typename PT>
+__global__ void combine_kernel(const PT *__restrict__ partial, const int32_t *__restrict__ inv_perm,
+                               const float *__restrict__ w, int k, int H, const uint16_t *__restrict__ residual,
+                               uint16_t *__restrict__ y) {
+    __shared__ int rows[kMaxK];
+    __shared__ float ws[kMaxK];
+    const int t = blockIdx.x;
+    if (threadIdx.x < k) {
+        rows[threadIdx.x] = inv_perm[(size_t)t * k + threadIdx.x];
+        ws[threadIdx.x] = w[(size_t)t * k + threadIdx.x];
+    }
+    __syncthreads();
+    for (int o = threadIdx.x; o < H; o += blockDim.x) {
+        float acc = 0.f;
+        for (int j = 0; j < k; j++) {
+            const int r = rows[j];
+            if (r >= 0) acc = fmaf(ws[j], load_partial<PT>(partial + (size_t)r * H + o), acc);
+        }
+        if (residual != nullptr) acc += bf16_bits_to_float(residual[(size_t)t * H + o]);
+        const __nv_bfloat16 b = __float2bfloat16_rn(acc);
+        y[(size_t)t * H + o] = *reinterpret_cast<const uint16_t *>(&b);
+    }
+}
+
+}  // namespace
+
+size_t grouped_workspace_bytes(int E, int H, int I, int T, int k) {
+    return grouped_ws_layout(nullptr, E, H, I, T, k).end;
+}
+
+cudaError_t launch_grouped(const PoolView &v, const uint16_t *x, int T, const int32_t *idx, int k, int act_mode,
+                           int32_t *perm, int32_t *inv_perm, int32_t *offsets, void *partial, int partial_dtype,
+                           void *ws, cudaStream_t st) {
+    (void)act_mode;
+    if (v.E > kMaxSortE) return cudaErrorNotSupported;
+    const GroupedWs g = grouped_ws_layout(ws, v.E, v.H, v.I, T, k);
+    StatusWord *stw = reinterpret_cast<StatusWord *>(ws);
+    const int P = T * k;
+    if (P == 0) {
+        cudaMemsetAsync(offsets, 0, (size_t)(v.E + 1) * sizeof(int32_t), st);
+        return cudaGetLastError();
+    }
+    const int nblocks = (P + kSortBlock - 1) / kSortBlock;
+    {
+        TraceScope trace_scope("sort_rank", st);
+        sort_rank_kernel<<<nblocks, kSortBlock, 0, st>>>(idx, P, v.E, g.local_rank, g.cnt, stw);
+    }
+    {
+        TraceScope trace_scope("sort_scan", st);
+        sort_scan_kernel<<<1, 1024, 0, st>>>(nblocks, v.E, g.cnt, g.prior, offsets);
+    }
+    {
+        TraceScope trace_scope("sort_scatter", st);
+        sort_scatter_kernel<<<(P + 255) / 256, 256, 0, st>>>(idx, P, v.E, g.local_rank, g.prior, offsets, perm, inv_perm);
+    }
+    {
+        TraceScope trace_scope("gather_quant", st);
+        gather_quant_kernel<<<(P * 32 + 255) / 256, 256, 0, st>>>(x, v.H, k, P, perm, g.xq, g.xs);
+    }
+    cudaError_t e = launch_grouped_gemms(v, T, k, offsets, g, partial, partial_dtype, stw, st);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const void *partial, int partial_dtype, const int32_t *inv_perm, const float *w, int T, int k,
+                           int H, const uint16_t *residual, uint16_t *y, cudaStream_t st) {
+    if (T == 0) return cudaSuccess;
+    TraceScope trace_scope("combine", st);
+    if (partial_dtype == MOE_PARTIAL_F32)
+        combine_kernel<float><<<T, 256, 0, st>>>((const float *)partial, inv_perm, w, k, H, residual, y);
+    else
+        combine_kernel<__nv_bfloat16><<<T, 256, 0, st>>>((const __nv_bfloat16 *)partial, inv_perm, w, k, H, residual,
+                                                         y);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

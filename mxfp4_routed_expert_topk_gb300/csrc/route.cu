@@ -1,0 +1,539 @@
+// Router: logits, exact top-k and softmax over the selected logits.
+//
+// The pages ("工作原理" on the Apple Silicon page) say the router picks 16 of each
+// layer's routed experts per token.  Selection here is EXACT: expert e ranks by
+// the real number
+//   l_e = sum_h x_h W_r[e,h] (+ skew_e),  ties broken to the lower index,
+// and the k winners are returned in descending order.
+//
+// route_logits_kernel computes l~_e in fp32 with a rigorous bound
+// |l~_e - l_e| <= b_e.  A product of two bf16 is exact in fp32, so the only
+// errors are the roundings of the additions: every product passes through at most
+// d of them (d follows from the summation tree below), hence
+//   |l~ - l| <= gamma_d * (sum_h |x_h W_r[e,h]| + |skew_e|),  gamma_d = d u / (1 - d u),
+// plus at most 2^-150 per product lost to underflow.
+//
+// route_select_kernel (one CTA per token) sorts by (l~ desc, index asc) and
+// certifies the order with the intervals [l~ - b, l~ + b]: an outsider can only
+// enter the top k if its interval reaches the lowest lower bound of the winners,
+// and two experts can only swap if their intervals meet.  Clusters of meeting
+// intervals that touch the top k are re-evaluated with exact integer arithmetic
+// (every term is an integer multiple of 2^-268) and ordered by exact value.
+#include "moe_internal.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kLogitTokens = 8;    // tokens per CTA in the logit kernel
+constexpr int kLogitExperts = 4;   // experts per CTA (two warps each, one per half of H)
+constexpr int kSelectThreads = 512;
+constexpr int kMaxE = 4096;
+constexpr int kMaxCand = 256;      // experts that may still enter the top k
+constexpr int kMaxExact = 64;      // experts evaluated exactly per token
+constexpr int kLimbs = 20;         // base-2^32 digits of an exact logit, unit 2^-268
+constexpr int kBins = 512;         // exponent bins of the exact evaluation
+
+struct RouteWs {
+    float *logit;  // [M][E]
+    float *bound;  // [M][E]
+};
+
+__host__ __device__ inline RouteWs route_ws(void *ws, int M, int E) {
+    RouteWs r;
+    char *p = (char *)ws + 256;
+    r.logit = (float *)p;
+    r.bound = (float *)(p + align_up((size_t)M * E * sizeof(float), 256));
+    return r;
+}
+
+// depth of the summation tree of route_logits_kernel for a given H
+__host__ __device__ inline int logit_tree_depth(int H) {
+    const int hmid = ((H / 2) + 7) / 8 * 8;
+    const int longest = hmid > H - hmid ? hmid : H - hmid;
+    const int chunks = (longest + 255) / 256;
+    return 3 /* pairwise 8 */ + chunks /* lane running sum */ + 5 /* warp */ + 1 /* halves */ + 1 /* skew */;
+}
+
+__device__ __forceinline__ void unpack_bf16x8(const uint4 &v, float f[8]) {
+    const unsigned int u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+        f[2 * i] = __uint_as_float(u[i] << 16);
+        f[2 * i + 1] = __uint_as_float(u[i] & 0xffff0000u);
+    }
+}
+
+// grid (ceil(E/4), ceil(M/8)), 256 threads.  Warp w handles expert 4*bx + w/2 over
+// one half of H for up to 8 tokens; lanes take 8 consecutive elements per step.
+__global__ void __launch_bounds__(256) route_logits_kernel(const uint16_t *__restrict__ x, int M, int H,
+                                                           const uint16_t *__restrict__ Wr, int E,
+                                                           const float *__restrict__ skew,
+                                                           float *__restrict__ logit, float *__restrict__ bound) {
+    extern __shared__ __align__(16) uint16_t xs[];  // [nt][H]
+    __shared__ float red_l[8][kLogitTokens], red_s[8][kLogitTokens];
+    const int m0 = blockIdx.y * kLogitTokens;
+    const int nt = min(kLogitTokens, M - m0);
+    const int nvec = nt * H / 8;
+    const uint4 *xg = reinterpret_cast<const uint4 *>(x + (size_t)m0 * H);
+    for (int i = threadIdx.x; i < nvec; i += blockDim.x) reinterpret_cast<uint4 *>(xs)[i] = xg[i];
+    __syncthreads();
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int e = blockIdx.x * kLogitExperts + (warp >> 1);
+    const int hmid = ((H / 2) + 7) / 8 * 8;
+    const int h0 = (warp & 1) ? hmid : 0, h1 = (warp & 1) ? H : hmid;
+    float acc[kLogitTokens], accs[kLogitTokens];
+#pragma unroll
+    for (int t = 0; t < kLogitTokens; t++) acc[t] = accs[t] = 0.f;
+    if (e < E) {
+        const uint16_t *wrow = Wr + (size_t)e * H;
+        for (int h = h0 + lane * 8; h < h1; h += 256) {
+            float wf[8];
+            unpack_bf16x8(__ldg(reinterpret_cast<const uint4 *>(wrow + h)), wf);
+#pragma unroll
+            for (int t = 0; t < kLogitTokens; t++) {
+                if (t < nt) {
+                    float xf[8], p[8];
+                    unpack_bf16x8(*reinterpret_cast<const uint4 *>(xs + (size_t)t * H + h), xf);
+#pragma unroll
+                    for (int i = 0; i < 8; i++) p[i] = xf[i] * wf[i];  // exact
+                    const float s = ((p[0] + p[1]) + (p[2] + p[3])) + ((p[4] + p[5]) + (p[6] + p[7]));
+                    const float a = ((fabsf(p[0]) + fabsf(p[1])) + (fabsf(p[2]) + fabsf(p[3]))) +
+                                    ((fabsf(p[4]) + fabsf(p[5])) + (fabsf(p[6]) + fabsf(p[7])));
+                    acc[t] += s;
+                    accs[t] += a;
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int t = 0; t < kLogitTokens; t++) {
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            acc[t] += __shfl_xor_sync(0xffffffffu, acc[t], off);
+            accs[t] += __shfl_xor_sync(0xffffffffu, accs[t], off);
+        }
+        if (lane == 0) {
+            red_l[warp][t] = acc[t];
+            red_s[warp][t] = accs[t];
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x < kLogitExperts * nt) {
+        const int q = threadIdx.x / nt, t = threadIdx.x % nt;
+        const int eq = blockIdx.x * kLogitExperts + q;
+        if (eq < E) {
+            float l = red_l[2 * q][t] + red_l[2 * q + 1][t];
+            float S = red_s[2 * q][t] + red_s[2 * q + 1][t];
+            if (skew != nullptr) {
+                const float sk = skew[eq];
+                l = l + sk;
+                S = S + fabsf(sk);
+            }
+            const int d = logit_tree_depth(H);
+            // (d+1) u S covers gamma_d S; the factor 1 + 2^-10 covers the rounding of S
+            // itself and of this expression; 2^-148 per product covers underflow.
+            float b = (float)(d + 1) * 5.9604645e-8f * S * (1.0f + 9.765625e-4f);
+            b = b + (float)H * 2.8025969e-45f;
+            logit[(size_t)(m0 + t) * E + eq] = l;
+            bound[(size_t)(m0 + t) * E + eq] = b;
+        }
+    }
+}
+
+// ------------------------------------------------------------ exact logits
+
+__device__ __forceinline__ bool bf16_parts(uint16_t b, int &neg, unsigned int &m, int &ep) {
+    const int E = (b >> 7) & 0xFF;
+    neg = (b >> 15) & 1;
+    m = (b & 0x7Fu) | (E ? 0x80u : 0u);
+    ep = E ? E : 1;
+    return E != 0xFF;
+}
+
+__device__ void limbs_add_shifted(long long *limbs, __int128 v, int o) {
+    const bool neg = v < 0;
+    unsigned __int128 mag = neg ? (unsigned __int128)(-v) : (unsigned __int128)v;
+    const int li = o / 32, sh = o % 32;
+    const unsigned __int128 s = mag << sh;  // |v| < 2^95, so s < 2^127
+#pragma unroll
+    for (int q = 0; q < 4; q++) {
+        const long long c = (long long)((unsigned long long)(s >> (32 * q)) & 0xffffffffull);
+        limbs[li + q] += neg ? -c : c;
+    }
+}
+
+__device__ void limbs_normalise(long long *d) {
+    for (int i = 0; i < kLimbs - 1; i++) {
+        const long long c = d[i] >> 32;  // floor division by 2^32
+        d[i] -= c * (1ll << 32);
+        d[i + 1] += c;
+    }
+}
+
+// -1, 0, +1 for a < b, a == b, a > b (normalised limbs)
+__device__ int limbs_cmp(const long long *a, const long long *b) {
+    if (a[kLimbs - 1] != b[kLimbs - 1]) return a[kLimbs - 1] < b[kLimbs - 1] ? -1 : 1;
+    for (int i = kLimbs - 2; i >= 0; i--)
+        if (a[i] != b[i]) return a[i] < b[i] ? -1 : 1;
+    return 0;
+}
+
+__device__ __forceinline__ __int128 shfl_xor_i128(__int128 v, int off) {
+    unsigned long long lo = (unsigned long long)v, hi = (unsigned long long)((unsigned __int128)v >> 64);
+    lo = __shfl_xor_sync(0xffffffffu, lo, off);
+    hi = __shfl_xor_sync(0xffffffffu, hi, off);
+    return (__int128)(((unsigned __int128)hi << 64) | lo);
+}
+
+struct ExactScratch {
+    long long bins[kBins];
+    __int128 part[kSelectThreads / 32];
+    int tmax[kSelectThreads / 32];
+    int T0;
+    int bad;
+};
+
+// The exact logit of expert e for token row xr, as normalised limbs (thread 0 writes out).
+// Terms inside the 64-bit window below the largest exponent are summed in 128-bit
+// registers; any term further down goes to a per-exponent bin.  Whole CTA.
+__device__ void exact_logit(const uint16_t *xr, const uint16_t *wr, int H, const float *skew_e,
+                            ExactScratch &sc, long long *out) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    for (int i = tid; i < kBins; i += blockDim.x) sc.bins[i] = 0;
+    if (tid == 0) sc.bad = 0;
+    // skew term: fp32 = m * 2^(E'-150) = m * 2^(E'+118-268)
+    int sk_neg = 0, sk_t = -1;
+    unsigned int sk_m = 0;
+    if (skew_e != nullptr) {
+        const unsigned int u = __float_as_uint(*skew_e);
+        const int Es = (u >> 23) & 0xFF;
+        sk_neg = u >> 31;
+        sk_m = (u & 0x7FFFFFu) | (Es ? 0x800000u : 0u);
+        sk_t = sk_m ? (Es ? Es : 1) + 118 : -1;
+        if (Es == 0xFF && tid == 0) sc.bad = 1;
+    }
+    int tmax = (tid == 0) ? sk_t : -1;
+    for (int h = tid; h < H; h += blockDim.x) {
+        int n1, n2, e1, e2;
+        unsigned int m1, m2;
+        const bool ok = bf16_parts(xr[h], n1, m1, e1) & bf16_parts(wr[h], n2, m2, e2);
+        if (!ok) sc.bad = 1;
+        if (m1 && m2) tmax = max(tmax, e1 + e2);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) tmax = max(tmax, __shfl_xor_sync(0xffffffffu, tmax, off));
+    if (lane == 0) sc.tmax[warp] = tmax;
+    __syncthreads();
+    if (tid == 0) {
+        int t = -1;
+        for (int w = 0; w < (int)(blockDim.x / 32); w++) t = max(t, sc.tmax[w]);
+        sc.T0 = t;
+    }
+    __syncthreads();
+    const int lo = max(sc.T0 - 63, 0);
+    __int128 acc = 0;
+    for (int h = tid; h < H; h += blockDim.x) {
+        int n1, n2, e1, e2;
+        unsigned int m1, m2;
+        bf16_parts(xr[h], n1, m1, e1);
+        bf16_parts(wr[h], n2, m2, e2);
+        if (!(m1 && m2)) continue;
+        const int t = e1 + e2;
+        const long long p = (long long)(m1 * m2);
+        if (t >= lo) {
+            const __int128 v = (__int128)p << (t - lo);
+            acc += (n1 ^ n2) ? -v : v;
+        } else {
+            atomicAdd(reinterpret_cast<unsigned long long *>(&sc.bins[t]),
+                      (unsigned long long)((n1 ^ n2) ? -p : p));
+        }
+    }
+    if (tid == 0 && sk_t >= 0) {
+        if (sk_t >= lo) {
+            const __int128 v = (__int128)sk_m << (sk_t - lo);
+            acc += sk_neg ? -v : v;
+        } else {
+            atomicAdd(reinterpret_cast<unsigned long long *>(&sc.bins[sk_t]),
+                      (unsigned long long)(sk_neg ? -(long long)sk_m : (long long)sk_m));
+        }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) acc += shfl_xor_i128(acc, off);
+    if (lane == 0) sc.part[warp] = acc;
+    __syncthreads();
+    if (tid == 0) {
+        __int128 tot = 0;
+        for (int w = 0; w < (int)(blockDim.x / 32); w++) tot += sc.part[w];
+        for (int i = 0; i < kLimbs; i++) out[i] = 0;
+        if (sc.T0 >= 0) {
+            limbs_add_shifted(out, tot, lo);
+            for (int t = 0; t < lo; t++)
+                if (sc.bins[t] != 0) limbs_add_shifted(out, (__int128)sc.bins[t], t);
+        }
+        limbs_normalise(out);
+    }
+    __syncthreads();
+}
+
+// ------------------------------------------------------------- selection
+
+__device__ __forceinline__ unsigned int orderable(float f) {
+    const unsigned int u = __float_as_uint(f);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+struct SelectShared {
+    unsigned long long keys[kMaxE];
+    int cand[kMaxCand];          // sorted positions >= k that may still enter
+    int ncand;
+    int nonfinite;
+    int uncertain;
+    // slow path
+    int aexp[kMaxCand + kMaxK];  // experts of the candidate set, ordered by upper bound
+    int comp[kMaxCand + kMaxK];  // component id
+    int xlist[kMaxExact];        // experts evaluated exactly
+    int nx;
+    long long exact[kMaxExact][kLimbs];
+    int final_idx[kMaxK];
+    int overflow;
+    ExactScratch sc;
+};
+
+__global__ void __launch_bounds__(kSelectThreads) route_select_kernel(
+    const uint16_t *__restrict__ x, int H, const uint16_t *__restrict__ Wr, int E, const float *__restrict__ skew,
+    int k, const float *__restrict__ logit, const float *__restrict__ bound, int32_t *__restrict__ idx_out,
+    float *__restrict__ w_out, StatusWord *st) {
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    SelectShared &s = *reinterpret_cast<SelectShared *>(smem_raw);
+    const int m = blockIdx.x, tid = threadIdx.x;
+    const float *lm = logit + (size_t)m * E;
+    const float *bm = bound + (size_t)m * E;
+    int P = 2;
+    while (P < E) P <<= 1;
+    if (tid == 0) {
+        s.ncand = 0;
+        s.nonfinite = 0;
+        s.uncertain = 0;
+        s.overflow = 0;
+        s.nx = 0;
+    }
+    __syncthreads();
+    for (int i = tid; i < P; i += blockDim.x) {
+        unsigned long long key = 0ull;
+        if (i < E) {
+            const float l = lm[i], b = bm[i];
+            if (!isfinite(l) || !isfinite(b)) s.nonfinite = 1;
+            key = ((unsigned long long)orderable(l) << 32) | (unsigned long long)(0xFFFFFFFFu - (unsigned)i);
+        }
+        s.keys[i] = key;
+    }
+    __syncthreads();
+    // bitonic sort, descending
+    for (int size = 2; size <= P; size <<= 1) {
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            for (int i = tid; i < P / 2; i += blockDim.x) {
+                const int lo = 2 * i - (i & (stride - 1));
+                const int hi = lo + stride;
+                const bool desc = (lo & size) == 0;
+                const unsigned long long a = s.keys[lo], b = s.keys[hi];
+                if ((a < b) == desc) {
+                    s.keys[lo] = b;
+                    s.keys[hi] = a;
+                }
+            }
+            __syncthreads();
+        }
+    }
+    auto expert_at = [&](int pos) { return (int)(0xFFFFFFFFu - (unsigned)(s.keys[pos] & 0xFFFFFFFFull)); };
+
+    // lowest lower bound among the k winners
+    float myL = __int_as_float(0x7f800000);
+    for (int p = tid; p < k; p += blockDim.x) {
+        const int e = expert_at(p);
+        myL = fminf(myL, __fsub_rd(lm[e], bm[e]));
+    }
+    for (int off = 16; off > 0; off >>= 1) myL = fminf(myL, __shfl_xor_sync(0xffffffffu, myL, off));
+    // float min through an orderable integer min
+    __shared__ unsigned int Lord;
+    if (tid == 0) Lord = 0xFFFFFFFFu;
+    __syncthreads();
+    if ((tid & 31) == 0) atomicMin(&Lord, orderable(myL));
+    __syncthreads();
+    const unsigned int Lo = Lord;
+    // outsiders whose upper bound reaches L; adjacent winners whose intervals meet
+    for (int p = k + tid; p < E; p += blockDim.x) {
+        const int e = expert_at(p);
+        if (orderable(__fadd_ru(lm[e], bm[e])) >= Lo) {
+            const int slot = atomicAdd(&s.ncand, 1);
+            if (slot < kMaxCand) s.cand[slot] = p;
+            else s.overflow = 1;
+        }
+    }
+    for (int p = tid; p + 1 < k; p += blockDim.x) {
+        const int a = expert_at(p), b = expert_at(p + 1);
+        if (!(__fsub_rd(lm[a], bm[a]) > __fadd_ru(lm[b], bm[b]))) s.uncertain = 1;
+    }
+    __syncthreads();
+    if (s.nonfinite) {
+        if (tid == 0) set_status(st, MOE_ERR_NONFINITE, (unsigned)m);
+        for (int j = tid; j < k; j += blockDim.x) s.final_idx[j] = expert_at(j);
+        __syncthreads();
+    } else if (s.ncand == 0 && !s.uncertain) {
+        for (int j = tid; j < k; j += blockDim.x) s.final_idx[j] = expert_at(j);
+        __syncthreads();
+    } else {
+        // ---- slow path: interval clusters, exact evaluation where needed
+        if (tid == 0) {
+            atomicAdd(&st->exact_fallbacks, 1u);
+            const int nc = min(s.ncand, kMaxCand);
+            int n = 0;
+            for (int p = 0; p < k; p++) s.aexp[n++] = expert_at(p);
+            for (int c = 0; c < nc; c++) s.aexp[n++] = expert_at(s.cand[c]);
+            // insertion sort by upper bound descending (ties: lower bound descending, then index)
+            for (int i = 1; i < n; i++) {
+                const int e = s.aexp[i];
+                const float ue = __fadd_ru(lm[e], bm[e]);
+                int j = i - 1;
+                while (j >= 0) {
+                    const int f = s.aexp[j];
+                    const float uf = __fadd_ru(lm[f], bm[f]);
+                    if (uf > ue || (uf == ue && f < e)) break;
+                    s.aexp[j + 1] = f;
+                    j--;
+                }
+                s.aexp[j + 1] = e;
+            }
+            // connected components of the interval graph, in order
+            int cid = 0;
+            float run_lo = __fsub_rd(lm[s.aexp[0]], bm[s.aexp[0]]);
+            s.comp[0] = 0;
+            for (int i = 1; i < n; i++) {
+                const int e = s.aexp[i];
+                if (__fadd_ru(lm[e], bm[e]) >= run_lo) {
+                    run_lo = fminf(run_lo, __fsub_rd(lm[e], bm[e]));
+                } else {
+                    cid++;
+                    run_lo = __fsub_rd(lm[e], bm[e]);
+                }
+                s.comp[i] = cid;
+            }
+            // members of multi-expert components that start inside the top k
+            int pos = 0, nx = 0;
+            for (int i = 0; i < n && pos < k;) {
+                int j = i;
+                while (j < n && s.comp[j] == s.comp[i]) j++;
+                if (j - i > 1) {
+                    for (int q = i; q < j; q++) {
+                        if (nx < kMaxExact) s.xlist[nx++] = s.aexp[q];
+                        else s.overflow = 1;
+                    }
+                }
+                pos += j - i;
+                i = j;
+            }
+            s.nx = nx;
+            s.ncand = n;  // now the size of aexp
+        }
+        __syncthreads();
+        const uint16_t *xr = x + (size_t)m * H;
+        for (int q = 0; q < s.nx; q++) {
+            const int e = s.xlist[q];
+            exact_logit(xr, Wr + (size_t)e * H, H, skew ? skew + e : nullptr, s.sc, s.exact[q]);
+            if (tid == 0 && s.sc.bad) s.nonfinite = 1;
+            __syncthreads();
+        }
+        if (tid == 0) {
+            if (s.nonfinite) set_status(st, MOE_ERR_NONFINITE, (unsigned)m);
+            if (s.overflow) set_status(st, MOE_ERR_UNSUPPORTED_SHAPE, (unsigned)m);
+            const int n = s.ncand;
+            int pos = 0;
+            for (int i = 0; i < n && pos < k;) {
+                int j = i;
+                while (j < n && s.comp[j] == s.comp[i]) j++;
+                if (j - i == 1) {
+                    s.final_idx[pos++] = s.aexp[i];
+                } else {
+                    // order the component by exact value (desc), ties to the lower index
+                    int order[kMaxCand + kMaxK];
+                    int cnt = 0;
+                    for (int q = i; q < j; q++) order[cnt++] = s.aexp[q];
+                    auto xi = [&](int e) {
+                        for (int q = 0; q < s.nx; q++)
+                            if (s.xlist[q] == e) return q;
+                        return -1;
+                    };
+                    for (int a = 1; a < cnt; a++) {
+                        const int e = order[a];
+                        const int qe = xi(e);
+                        int b = a - 1;
+                        while (b >= 0) {
+                            const int f = order[b];
+                            const int qf = xi(f);
+                            int c;
+                            if (qe >= 0 && qf >= 0) c = limbs_cmp(s.exact[qf], s.exact[qe]);
+                            else c = (lm[f] > lm[e]) ? 1 : ((lm[f] < lm[e]) ? -1 : 0);  // only on overflow
+                            if (c > 0 || (c == 0 && f < e)) break;
+                            order[b + 1] = f;
+                            b--;
+                        }
+                        order[b + 1] = e;
+                    }
+                    for (int q = 0; q < cnt && pos < k; q++) s.final_idx[pos++] = order[q];
+                }
+                i = j;
+            }
+        }
+        __syncthreads();
+    }
+    // softmax over the k selected fp32 logits
+    if (tid < 32) {
+        const int j = tid;
+        const float l = (j < k) ? lm[s.final_idx[j]] : -__int_as_float(0x7f800000);
+        float mx = l;
+        for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+        const float ex = (j < k) ? expf(l - mx) : 0.f;
+        float z = ex;
+        for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
+        if (j < k) {
+            idx_out[(size_t)m * k + j] = s.final_idx[j];
+            w_out[(size_t)m * k + j] = ex / z;
+        }
+    }
+}
+
+}  // namespace
+
+size_t route_workspace_bytes(int E, int M, int k) {
+    (void)k;
+    return 256 + 2 * align_up((size_t)M * E * sizeof(float), 256);
+}
+
+cudaError_t launch_route(const uint16_t *x, int M, int H, const uint16_t *Wr, int E, const float *skew, int k,
+                         int32_t *idx, float *w, void *ws, cudaStream_t st) {
+    if (M == 0) return cudaSuccess;
+    RouteWs r = route_ws(ws, M, E);
+    const int nt = M < kLogitTokens ? M : kLogitTokens;
+    if ((size_t)nt * H * sizeof(uint16_t) > 200 * 1024) return cudaErrorInvalidValue;
+    const size_t smem1 = (size_t)nt * H * sizeof(uint16_t);
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaFuncSetAttribute(route_logits_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+        cudaFuncSetAttribute(route_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)sizeof(SelectShared));
+        attr_set = true;
+    }
+    dim3 g1((E + kLogitExperts - 1) / kLogitExperts, (M + kLogitTokens - 1) / kLogitTokens);
+    {
+        TraceScope trace_scope("route_logits", st);
+        route_logits_kernel<<<g1, 256, smem1, st>>>(x, M, H, Wr, E, skew, r.logit, r.bound);
+    }
+    {
+        TraceScope trace_scope("route_select", st);
+        route_select_kernel<<<M, kSelectThreads, sizeof(SelectShared), st>>>(
+            x, H, Wr, E, skew, k, r.logit, r.bound, idx, w, reinterpret_cast<StatusWord *>(ws));
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,265 @@
+"""GPU parity of the pool, the router and the decode/verify path against the
+fp64 oracle: bit-exact bytes and routing indices, float tolerance on outputs."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from tests._util import bf16_to_bits, bf16_to_f64, check_close, to_dev_bf16
+
+pytestmark = pytest.mark.gpu
+
+moe = pytest.importorskip("mxfp4_routed_expert_topk_gb300")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    moe.build()
+    oracle.build()
+
+
+def make_pool(shape, seed):
+    pool = moe.Pool(shape.E, shape.H, shape.I)
+    moe.moe_pool_fill_synthetic(pool, seed)
+    return pool
+
+
+@pytest.fixture(scope="module")
+def tiny():
+    s = synth.TINY
+    pool = make_pool(s, synth.pool_seed(0))
+    Wrb = synth.router_bf16(synth.router_seed(0), s.E, s.H)
+    return s, pool, Wrb, to_dev_bf16(Wrb)
+
+
+@pytest.fixture(scope="module")
+def full():
+    s = synth.FULL
+    pool = make_pool(s, synth.pool_seed(0))
+    Wrb = synth.router_bf16(synth.router_seed(0), s.E, s.H)
+    return s, pool, Wrb, to_dev_bf16(Wrb)
+
+
+# ------------------------------------------------------------------ pool
+
+
+def test_generator_agreement_tiny(tiny):
+    s, pool, _, _ = tiny
+    for e in range(s.E):
+        c, sc = moe.moe_pool_download_expert(pool, e)
+        rc, rs = oracle.gen_expert(synth.pool_seed(0), e, s.H, s.I)
+        assert np.array_equal(c.cpu().numpy(), rc), e
+        assert np.array_equal(sc.cpu().numpy(), rs), e
+
+
+def test_generator_agreement_full_sampled(full):
+    s, pool, _, _ = full
+    for e in (0, 1, 447, 895):
+        c, sc = moe.moe_pool_download_expert(pool, e)
+        rc, rs = oracle.gen_expert(synth.pool_seed(0), e, s.H, s.I)
+        assert np.array_equal(c.cpu().numpy(), rc), e
+        assert np.array_equal(sc.cpu().numpy(), rs), e
+
+
+@pytest.mark.parametrize("H,I", [(1024, 512), (384, 96), (256, 160)])
+def test_upload_download_roundtrip(H, I):
+    pool = moe.Pool(3, H, I)
+    rng = np.random.default_rng(H + I)
+    for e in range(3):
+        c = rng.integers(0, 256, size=3 * H * I // 2, dtype=np.uint8)
+        sc = rng.integers(110, 130, size=3 * H * I // 32, dtype=np.uint8)
+        moe.moe_pool_upload_expert(pool, e, torch.from_numpy(c).cuda(), torch.from_numpy(sc).cuda())
+        c2, s2 = moe.moe_pool_download_expert(pool, e)
+        assert np.array_equal(c2.cpu().numpy(), c) and np.array_equal(s2.cpu().numpy(), sc)
+
+
+# ---------------------------------------------------------------- router
+
+
+def _route_check(xb, Wrb, Wr, k, skew=None):
+    x = to_dev_bf16(xb)
+    sk = None if skew is None else torch.from_numpy(skew).cuda()
+    ws = moe.workspace(moe.moe_workspace_size(moe.MOE_OP_ROUTE, Wrb.shape[0], xb.shape[1], 32, xb.shape[0], k))
+    idx, w = moe.moe_route_topk(x, Wr, k, sk, ws=ws)
+    torch.cuda.synchronize()
+    nfb = moe.exact_fallbacks(ws)
+    assert moe.moe_check_status(ws) == moe.MOE_OK
+    ridx, rw, _ = oracle.route(xb, Wrb, k, skew)
+    assert np.array_equal(idx.cpu().numpy(), ridx)
+    assert np.max(np.abs(w.cpu().numpy() - rw)) < 2e-6
+    return nfb
+
+
+def test_route_tiny_bit_exact(tiny):
+    s, _, Wrb, Wr = tiny
+    xb = synth.tokens_bf16(synth.TOKENS_SEED["tiny"], 0, 200, s.H)
+    _route_check(xb, Wrb, Wr, s.k)
+
+
+def test_route_full_bit_exact(full):
+    s, _, Wrb, Wr = full
+    xb = synth.tokens_bf16(synth.TOKENS_SEED["full"], 0, 48, s.H)
+    _route_check(xb, Wrb, Wr, s.k)
+
+
+def test_route_with_zipf_skew(full):
+    s, _, Wrb, Wr = full
+    xb = synth.tokens_bf16(synth.TOKENS_SEED["stacked"], 0, 24, s.H)
+    _route_check(xb, Wrb, Wr, s.k, synth.zipf_skew_f32(synth.skew_seed(0), s.E))
+
+
+@pytest.mark.parametrize("k", [1, 2, 16, 32])
+def test_route_k_values(tiny, k):
+    s, _, Wrb, Wr = tiny
+    xb = synth.tokens_bf16(5, 0, 40, s.H)
+    _route_check(xb, Wrb, Wr, k)
+
+
+def test_route_planted_ties_take_exact_path(tiny):
+    s, _, Wrb0, _ = tiny
+    Wrb = Wrb0.copy()
+    xb = synth.tokens_bf16(7, 0, 16, s.H)
+    # exact duplicates (ties -> lower index), and one-ulp near ties of a strong row
+    strong = synth.bf16_bits_from_f64(np.sign(synth.bf16_bits_to_f64(xb[0])) * 0.05)
+    for e in (3, 20, 41):
+        Wrb[e] = strong
+    Wrb[9] = strong
+    Wrb[9, 100] += 1
+    Wrb[50] = Wrb[17]
+    Wrb[63] = Wrb[17]
+    nfb = _route_check(xb, Wrb, to_dev_bf16(Wrb), s.k)
+    assert nfb > 0
+
+
+def test_route_large_dynamic_range(tiny):
+    s, _, Wrb0, _ = tiny
+    rng = np.random.default_rng(11)
+    xb = synth.bf16_bits_from_f64(rng.standard_normal((8, s.H)) * np.exp2(rng.integers(-60, 60, size=(8, s.H))))
+    Wrb = synth.bf16_bits_from_f64(rng.standard_normal((s.E, s.H)) * np.exp2(rng.integers(-40, 30, size=(s.E, s.H))))
+    _route_check(xb, Wrb, to_dev_bf16(Wrb), s.k)
+
+
+# ---------------------------------------------------------------- decode
+
+
+def _decode_check(s, pool, Wrb, Wr, xb, seed, residual=None):
+    x = to_dev_bf16(xb)
+    idx, w = moe.moe_route_topk(x, Wr, s.k)
+    ws = moe.workspace(moe.moe_workspace_size(moe.MOE_OP_DECODE, s.E, s.H, s.I, xb.shape[0], s.k))
+    res = None if residual is None else to_dev_bf16(residual)
+    y = moe.moe_expert_forward_decode(pool, x, idx, w, residual=res, ws=ws)
+    assert moe.moe_check_status(ws) == moe.MOE_OK
+    ref = oracle.decode_layer(oracle.SyntheticPool(seed, s.E, s.H, s.I), xb, Wrb, s.k, residual_bits=residual)
+    assert np.array_equal(idx.cpu().numpy(), ref["idx"])
+    return check_close(bf16_to_f64(y), ref["y"])
+
+
+def test_decode_tiny_single_tokens(tiny):
+    s, pool, Wrb, Wr = tiny
+    for t in range(6):
+        xb = synth.tokens_bf16(synth.TOKENS_SEED["tiny"], t, 1, s.H)
+        _decode_check(s, pool, Wrb, Wr, xb, synth.pool_seed(0))
+
+
+@pytest.mark.parametrize("M", [2, 5, 9, 17, 32])
+def test_decode_verify_tiny(tiny, M):
+    s, pool, Wrb, Wr = tiny
+    xb = synth.verify_batch_bf16(synth.TOKENS_SEED["verify"], M, M, s.H)
+    _decode_check(s, pool, Wrb, Wr, xb, synth.pool_seed(0))
+
+
+def test_decode_full_single_tokens(full):
+    s, pool, Wrb, Wr = full
+    for t in (0, 1):
+        xb = synth.tokens_bf16(synth.TOKENS_SEED["full"], t, 1, s.H)
+        _decode_check(s, pool, Wrb, Wr, xb, synth.pool_seed(0))
+
+
+def test_decode_full_verify_batch(full):
+    s, pool, Wrb, Wr = full
+    xb = synth.verify_batch_bf16(synth.TOKENS_SEED["verify"], 0, 5, s.H)
+    _decode_check(s, pool, Wrb, Wr, xb, synth.pool_seed(0))
+
+
+@pytest.mark.parametrize("E,H,I,k,M", [(40, 384, 96, 8, 3), (20, 256, 160, 4, 7), (33, 640, 224, 32, 2)])
+def test_decode_ragged_shapes(E, H, I, k, M):
+    s = synth.Shape(E=E, H=H, I=I, k=k)
+    pool = make_pool(s, 77)
+    Wrb = synth.router_bf16(78, E, H)
+    xb = synth.tokens_bf16(79, 0, M, H)
+    _decode_check(s, pool, Wrb, to_dev_bf16(Wrb), xb, 77)
+
+
+def test_decode_residual(tiny):
+    s, pool, Wrb, Wr = tiny
+    xb = synth.tokens_bf16(3, 0, 3, s.H)
+    res = synth.tokens_bf16(4, 0, 3, s.H)
+    _decode_check(s, pool, Wrb, Wr, xb, synth.pool_seed(0), residual=res)
+
+
+def test_decode_deterministic(full):
+    s, pool, Wrb, Wr = full
+    x = to_dev_bf16(synth.verify_batch_bf16(1, 1, 9, s.H))
+    idx, w = moe.moe_route_topk(x, Wr, s.k)
+    y1 = moe.moe_expert_forward_decode(pool, x, idx, w)
+    y2 = moe.moe_expert_forward_decode(pool, x, idx, w)
+    assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
+
+
+def test_zero_and_closed_form_experts():
+    H, I, k = 256, 128, 4
+    pool = moe.Pool(8, H, I)
+    zc = torch.zeros(3 * H * I // 2, dtype=torch.uint8, device="cuda")
+    ones = torch.full((3 * H * I // 2,), 0x22, dtype=torch.uint8, device="cuda")
+    s127 = torch.full((3 * H * I // 32,), 127, dtype=torch.uint8, device="cuda")
+    for e in range(4):
+        moe.moe_pool_upload_expert(pool, e, zc, s127)
+    for e in range(4, 8):
+        moe.moe_pool_upload_expert(pool, e, ones, s127)
+    xb = synth.bf16_bits_from_f64(synth.bf16_bits_to_f64(synth.tokens_bf16(9, 0, 1, H)) / 16)
+    x = to_dev_bf16(xb)
+    w = torch.full((1, k), 1.0 / k, dtype=torch.float32, device="cuda")
+    y0 = moe.moe_expert_forward_decode(pool, x, torch.tensor([[0, 1, 2, 3]], dtype=torch.int32, device="cuda"), w)
+    assert torch.count_nonzero(y0.float()) == 0
+    y1 = moe.moe_expert_forward_decode(pool, x, torch.tensor([[4, 5, 6, 7]], dtype=torch.int32, device="cuda"), w)
+    s_ = float(np.sum(synth.bf16_bits_to_f64(xb)))
+    want = I * (s_ / (1 + np.exp(-s_)) * s_)
+    check_close(bf16_to_f64(y1), np.full((1, H), want))
+
+
+def test_bad_index_sets_status(tiny):
+    s, pool, _, _ = tiny
+    x = to_dev_bf16(synth.tokens_bf16(0, 0, 1, s.H))
+    idx = torch.arange(s.k, dtype=torch.int32, device="cuda").view(1, -1).clone()
+    idx[0, 3] = 10_000
+    w = torch.full((1, s.k), 1.0 / s.k, dtype=torch.float32, device="cuda")
+    ws = moe.workspace(moe.moe_workspace_size(moe.MOE_OP_DECODE, s.E, s.H, s.I, 1, s.k))
+    y = moe.moe_expert_forward_decode(pool, x, idx, w, ws=ws)
+    assert moe.moe_check_status(ws) == moe.MOE_ERR_BAD_INDEX
+    assert torch.isfinite(y.float()).all()
+    assert moe.moe_check_status(ws) == moe.MOE_OK      # cleared by the first check
+
+
+def test_stacked_layers_oracle_forced(tiny):
+    """Per layer on the oracle's own layer input: pre-scale bit-exact, routing bit-exact,
+    layer output within tolerance."""
+    s = synth.TINY
+    L = 4
+    pools = [oracle.SyntheticPool(synth.pool_seed(l), s.E, s.H, s.I) for l in range(L)]
+    gpools = [make_pool(s, synth.pool_seed(l)) for l in range(L)]
+    routers = [synth.router_bf16(synth.router_seed(l), s.E, s.H) for l in range(L)]
+    skews = [synth.zipf_skew_f32(synth.skew_seed(l), s.E) for l in range(L)]
+    xb = synth.tokens_bf16(synth.TOKENS_SEED["stacked"], 0, 1, s.H)
+    layers, _ = oracle.stacked_step(pools, routers, skews, xb, s.k)
+    for l, ly in enumerate(layers):
+        x = to_dev_bf16(ly["x"])
+        xh = moe.moe_prescale(x)
+        assert np.array_equal(bf16_to_bits(xh), ly["x_hat"])
+        idx, w = moe.moe_route_topk(xh, to_dev_bf16(routers[l]), s.k, torch.from_numpy(skews[l]).cuda())
+        assert np.array_equal(idx.cpu().numpy(), ly["idx"])
+        y = moe.moe_expert_forward_decode(gpools[l], xh, idx, w, residual=x)
+        ref = synth.bf16_bits_to_f64(ly["x"]) + ly["y"]
+        check_close(bf16_to_f64(y) - synth.bf16_bits_to_f64(ly["x"]), ref - synth.bf16_bits_to_f64(ly["x"]))
