@@ -313,7 +313,6 @@ cudaError_t launch_decode(const PoolView &v, const uint16_t *x, int M, const int
         int dev = 0;
         cudaGetDevice(&dev);
         cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev);
-        cudaFuncSetAttribute(decode_down_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
     }
     DecodeWs d = decode_ws(ws, v.H, v.I, M, k);
     StatusWord *stw = reinterpret_cast<StatusWord *>(ws);
@@ -340,6 +339,9 @@ cudaError_t launch_decode(const PoolView &v, const uint16_t *x, int M, const int
     if (group > fit) group = fit;
     if (group < 1) return cudaErrorInvalidValue;
     const size_t smem = (size_t)group * v.Ip * 2 + (size_t)M * rows * 4;
+    static int smem_down = 0;
+    cudaError_t e = ensure_dynamic_smem(decode_down_kernel, smem, smem_down);
+    if (e != cudaSuccess) return e;
     {
         TraceScope trace_scope("decode_down", st);
         decode_down_kernel<<<(v.H + rows - 1) / rows, kThreads, smem, st>>>(v, M, k, rows, group, w, residual, y, d,

@@ -120,6 +120,16 @@ struct TraceScope {
     ~TraceScope() { trace_post(name, st); }
 };
 
+// Raise a kernel's dynamic shared memory limit to `bytes` if needed (per kernel,
+// remembered in `cur`).  Returns the error of the attribute call.
+template <typename K>
+inline cudaError_t ensure_dynamic_smem(K kernel, size_t bytes, int &cur) {
+    if ((int)bytes <= cur || bytes <= 48 * 1024) return cudaSuccess;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    if (e == cudaSuccess) cur = (int)bytes;
+    return e;
+}
+
 // Launch helpers implemented per translation unit.
 cudaError_t launch_pool_kernel(const PoolView &v, int mode, uint64_t seed, int e_lo, int e_hi,
                                const uint8_t *codes, const uint8_t *scales, uint8_t *out_codes,

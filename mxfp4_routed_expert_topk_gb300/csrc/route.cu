@@ -516,13 +516,11 @@ cudaError_t launch_route(const uint16_t *x, int M, int H, const uint16_t *Wr, in
     const int nt = M < kLogitTokens ? M : kLogitTokens;
     if ((size_t)nt * H * sizeof(uint16_t) > 200 * 1024) return cudaErrorInvalidValue;
     const size_t smem1 = (size_t)nt * H * sizeof(uint16_t);
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaFuncSetAttribute(route_logits_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-        cudaFuncSetAttribute(route_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)sizeof(SelectShared));
-        attr_set = true;
-    }
+    static int smem_logits = 0, smem_select = 0;
+    cudaError_t e = ensure_dynamic_smem(route_logits_kernel, smem1, smem_logits);
+    if (e != cudaSuccess) return e;
+    e = ensure_dynamic_smem(route_select_kernel, sizeof(SelectShared), smem_select);
+    if (e != cudaSuccess) return e;
     dim3 g1((E + kLogitExperts - 1) / kLogitExperts, (M + kLogitTokens - 1) / kLogitTokens);
     {
         TraceScope trace_scope("route_logits", st);
