@@ -272,6 +272,25 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+def run_profile_case(args):
+    """A small case of the same kernels for ncu captures: full H and I, a 64-expert
+    pool (1.2 GB, larger than L2), a few single-token calls."""
+    import torch
+    import mxfp4_routed_expert_topk_gb300 as moe
+    moe.build()
+    s = synth.Shape(E=64, H=synth.FULL.H, I=synth.FULL.I, k=16)
+    pool = moe.Pool(s.E, s.H, s.I)
+    moe.moe_pool_fill_synthetic(pool, synth.pool_seed(0))
+    Wr = torch.from_numpy(synth.router_bf16(synth.router_seed(0), s.E, s.H).view(np.int16)).cuda().view(torch.bfloat16)
+    xb = synth.tokens_bf16(synth.TOKENS_SEED["full"], 0, 4, s.H)
+    x = torch.from_numpy(xb.view(np.int16)).cuda().view(torch.bfloat16)
+    for t in range(4):
+        idx, w = moe.moe_route_topk(x[t:t + 1], Wr, s.k)
+        moe.moe_expert_forward_decode(pool, x[t:t + 1], idx, w)
+    torch.cuda.synchronize()
+    print("profile case done")
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -280,8 +299,12 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--ref-tokens", type=int, default=16)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile", choices=["decode"], default=None,
+                    help="run a small case of the kernels for an ncu capture (no JSON line)")
     args = ap.parse_args()
-    if args.impl == "reference":
+    if args.profile:
+        run_profile_case(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

@@ -11,5 +11,5 @@ from ._lib import moe_trace_begin, moe_trace_end  # noqa: F401
 
 def build(verbose: bool = False) -> str:
     """Compile libmoe.so in-tree for sm_103a."""
-    from .build import build as _build
+    from .nvcc_build import build as _build
     return _build(verbose=verbose)
