@@ -131,6 +131,26 @@ moe_status moe_route_topk(const uint16_t *x, int M, int H, const uint16_t *Wr, i
                           const float *skew, int k, int32_t *idx, float *w,
                           void *ws, size_t ws_bytes, moe_stream_t stream);
 
+/* Router variant that allocates nothing and takes no workspace.  The pages have
+ * no counterpart to this entry point; it exists for callers that cannot call
+ * cudaMalloc or hand over a workspace -- code running while a caching allocator
+ * or a host framework owns all device memory, plugins whose host provides no
+ * scratch buffers, and latency-critical threads that must not risk the
+ * device-wide synchronisation cudaMalloc/cudaFree can cause.
+ * Same arguments, kernels and results as moe_route_topk, but the scratch (status
+ * word, fp32 logits and their bounds) lives in one static device array of the
+ * library, 1 MiB + 256 B, that every GPU which loads the library keeps until the
+ * process exits.  Limit: M * E <= 131072 (else MOE_ERR_UNSUPPORTED_SHAPE).
+ * The first call on a device looks up the array's device address (with that
+ * device current), so make that first call before any stream capture.  All calls
+ * share the array: calls that overlap on the GPU (other streams, other threads)
+ * race and must be serialised by the caller.  The status word is cleared at the
+ * start of every call; device-detected errors are recorded there but not
+ * returned -- use moe_route_topk with a workspace to read them. */
+moe_status moe_route_topk_static(const uint16_t *x, int M, int H, const uint16_t *Wr, int E,
+                                 const float *skew, int k, int32_t *idx, float *w,
+                                 moe_stream_t stream);
+
 /* ------------------------------------------------------- decode / verify
  * Expert forward for M (1..32) rows that were routed by moe_route_topk: each
  * distinct selected expert is read from the pool once and applied to every row
