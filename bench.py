@@ -2,7 +2,7 @@
 
 Default workload: the full-size decode layer (E=896 experts, hidden 7168,
 intermediate 1600, top-16), 1000 seeded synthetic tokens decoded one at a time.
-One step = route + expert forward of all 1000 tokens (2 library calls, 5 kernels
+One step = route + expert forward of all 1000 tokens (2 library calls, 2 kernels
 per token), captured once in a CUDA graph and replayed.  value = layer-tokens/s.
 
     python bench.py [--steps K] [--warmup W] [--impl ours|reference] [--gpus N]
@@ -221,20 +221,21 @@ def run_ours(args):
 
     # per-kernel device time over one more pass of the timed region (eager launches)
     kern = {}
-    for name in ("decode_gateup", "decode_down", "route_logits", "route_select", "decode_prep"):
+    for name in ("decode_fused", "route_single"):
         moe.moe_trace_begin(name)
         with torch.cuda.stream(stream):
             step()
         n, tot = moe.moe_trace_end()
         kern[name] = tot / max(n, 1)
     hbm, peak_kind = peaks()
-    gu_bytes = s.k * (2 * s.I * s.H // 2 + 2 * s.I * s.H // 32)
-    dn_bytes = s.k * (s.H * s.I // 2 + s.H * s.I // 32)
+    # dominant kernel: the fused expert kernel streams the 16 selected experts' MXFP4
+    # codes and scales (18,278,400 B each at this shape)
+    kern_bytes = s.k * expert_bytes(s.H, s.I)
     layer_bytes = s.k * expert_bytes(s.H, s.I) + s.E * s.H * 2
-    achieved = gu_bytes / (kern["decode_gateup"] / 1000.0) / 1e9
+    achieved = kern_bytes / (kern["decode_fused"] / 1000.0) / 1e9
     layer_gbs = layer_bytes / (ms_step / 1000.0 / NTOK) / 1e9
     traffic = None
-    tfile = os.path.join(ROOT, "profiles", "decode_gateup_traffic.json")
+    tfile = os.path.join(ROOT, "profiles", "decode_fused_traffic.json")
     if os.path.exists(tfile):
         traffic = json.load(open(tfile)).get("bytes_per_launch")
 
@@ -247,7 +248,7 @@ def run_ours(args):
         cpu = {"value": args.ref_tokens / secs, "unit": "layer-tokens/s", "cores": cores, "kind": "oracle",
                "sample": f"{args.ref_tokens} tokens of the workload (exact route + 16 experts, fp64), "
                          "experts pre-generated outside the timing"}
-    launches = 5 * NTOK * args.steps
+    launches = 2 * NTOK * args.steps      # route_single + decode_fused per token
     if rank == 0:
         print(json.dumps({
             "metric": METRIC, "value": value, "unit": "layer-tokens/s", "n_gpus": world, "steps": args.steps,
@@ -258,9 +259,9 @@ def run_ours(args):
                        "l2": "inputs larger than L2: 16.6 GB resident pool, 16 fresh experts per token",
                        "graph": "one CUDA graph per step (1000 tokens)"},
             "expert_weight_hbm_gbs": layer_gbs, "hbm_frac_layer": layer_gbs / hbm,
-            "roofline": {"bound": "hbm", "kernel": "decode_gateup", "achieved": achieved, "peak": hbm,
+            "roofline": {"bound": "hbm", "kernel": "decode_fused", "achieved": achieved, "peak": hbm,
                          "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / hbm, "traffic": traffic,
-                         "algorithmic_bytes_per_launch": gu_bytes},
+                         "algorithmic_bytes_per_launch": kern_bytes},
             "kernel_ms": kern,
             "cpu_baseline": cpu,
             "e2e": {"value": NTOK / (e2e_ms / 1000.0) * world, "unit": "layer-tokens/s",

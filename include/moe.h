@@ -107,7 +107,9 @@ moe_status moe_pool_download_expert(const moe_pool *pool, int e, uint8_t *codes_
 
 /* Workspace bytes of operation `op` (MOE_OP_*) for M (decode) or T (prefill)
  * rows.  The workspace is caller-owned device memory, 256-byte aligned; its
- * first 256 bytes hold the device status word. */
+ * first 256 bytes hold the device status word and the kernels' own counters.
+ * They must be zero before the first call on a workspace (moe_clear_status, or a
+ * zero-filled allocation); the kernels leave them zero again after each call. */
 moe_status moe_workspace_size(int op, int E, int H, int I, int rows, int k, size_t *bytes);
 
 /* Clear the status word of `ws` (asynchronously, on `stream`). */

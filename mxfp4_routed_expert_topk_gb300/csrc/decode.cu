@@ -314,6 +314,10 @@ cudaError_t launch_decode(const PoolView &v, const uint16_t *x, int M, const int
         cudaGetDevice(&dev);
         cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev);
     }
+    if (M == 1) {
+        const cudaError_t e = launch_decode_fused(v, x, idx, w, k, residual, y, ws, st);
+        if (e != cudaErrorNotSupported) return e;
+    }
     DecodeWs d = decode_ws(ws, v.H, v.I, M, k);
     StatusWord *stw = reinterpret_cast<StatusWord *>(ws);
     {

@@ -1,0 +1,446 @@
+// Single-token decode of the routed-expert layer in one cooperative persistent
+// kernel, one CTA per SM (the memory-bound path of the layer: each of the 16
+// selected experts' packed MXFP4 weights is streamed from HBM exactly once).
+//
+//   phase A  g = W_g x, u = W_u x, h = silu(g) * u for every (slot, index) item;
+//            each CTA owns a contiguous range of the k*I items
+//   grid barrier (h complete in global memory)
+//   phase B  y[o] = sum_j w_j (W_d,j h_j)[o] (+ residual) for this CTA's block of
+//            output rows, summed in a fixed order (deterministic, no atomics)
+//
+// A producer warp streams weight rows and their scale rows with bulk copies into a
+// ring of shared-memory slots (evict-first in L2); W_d rows of phase B are fetched
+// while phase A finishes and while CTAs wait at the grid barrier.  Consumer warps
+// dequantise in registers: E2M1 pairs -> f16x2 (cvt), packed f16 FMAs over one
+// 32-element scale block against the token held in registers as f16 scaled by a
+// power of two, then the block sum is scaled by its E8M0 factor in fp32.
+#include "moe_internal.cuh"
+#include "sm100_async.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kCW = 8;                        // consumer warps
+constexpr int kThreadsF = (kCW + 1) * 32;     // + one producer warp
+constexpr int kSlots = 3;
+constexpr int kMaxJ = 7;                      // H <= 32 lanes * 32 elements * 7
+constexpr int kMaxKF = 16;                    // two pairs per consumer warp in phase B
+constexpr int kMaxR = 4;                      // output rows per phase-B stage
+constexpr int kMaxRowsCta = 64;               // output rows per CTA
+
+struct FusedArgs {
+    PoolView v;
+    int k;
+    int G;
+    const uint16_t *x;
+    const int32_t *idx;
+    const float *w;
+    const uint16_t *residual;
+    uint16_t *y;
+    float *h;            // [k][I] workspace
+    StatusWord *st;      // pad[1]: grid barrier, pad[2]: exit counter, pad[8+p]: max |h| of pair p
+    uint32_t slot_bytes;
+    int R;
+    uint32_t sb_stride;  // bytes per pair of phase-B scale rows in a slot
+};
+
+// 32 E2M1 elements (16 bytes) times the matching f16x2 input block: 16 packed f16
+// FMAs in one chain, then the two halves summed in fp32.
+__device__ __forceinline__ float block_dot1(const uint4 &q, const uint4 *xb) {
+    const unsigned int words[4] = {q.x, q.y, q.z, q.w};
+    unsigned int acc = 0u;
+#pragma unroll
+    for (int wd = 0; wd < 4; wd++) {
+        unsigned int w0, w1, w2, w3;
+        e2m1x8_to_f16x2x4(words[wd], w0, w1, w2, w3);
+        const uint4 xv = xb[wd];
+        acc = hfma2_u32(w0, xv.x, acc);
+        acc = hfma2_u32(w1, xv.y, acc);
+        acc = hfma2_u32(w2, xv.z, acc);
+        acc = hfma2_u32(w3, xv.w, acc);
+    }
+    return f16x2_sum_to_float(acc);
+}
+
+// E8M0 byte -> 2^(b-127) with one shift: byte 0 gives 0 instead of 2^-127 (far
+// below anything it scales), byte 255 (NaN) gives +inf (non-finite either way).
+__device__ __forceinline__ float e8m0_fast(unsigned int b) { return __uint_as_float(b << 23); }
+
+__device__ __forceinline__ unsigned int pack_half2(float lo, float hi) {
+    const __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const unsigned int *>(&h);
+}
+
+__global__ void __launch_bounds__(kThreadsF, 1) decode_fused_kernel(const FusedArgs a) {
+    extern __shared__ __align__(1024) unsigned char smem[];
+    const PoolView &v = a.v;
+    uint8_t *slots = smem;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)kSlots * a.slot_bytes);
+    uint64_t *empty = full + kSlots;
+    float *red = reinterpret_cast<float *>(empty + kSlots);     // [kCW][kMaxRowsCta]
+    int *sidx = reinterpret_cast<int *>(red + kCW * kMaxRowsCta);  // [kMaxKF]
+    int *abort_flag = sidx + kMaxKF;
+    unsigned int *samax = reinterpret_cast<unsigned int *>(abort_flag + 1);  // [kMaxKF] max |h| per pair
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int b = blockIdx.x, G = a.G, k = a.k;
+    const int NA = k * v.I;
+    const int n_lo = (int)((long long)b * NA / G), n_hi = (int)((long long)(b + 1) * NA / G);
+    const int nitems = n_hi - n_lo;
+    const int nstageA = (nitems + kCW - 1) / kCW;
+    const int o_lo = (int)((long long)b * v.H / G), o_hi = (int)((long long)(b + 1) * v.H / G);
+    const int rows = o_hi - o_lo;
+    const int nstageB = (rows + a.R - 1) / a.R;
+    const int nkb = v.H / 32, nkbd = v.I / 32;
+    const int ldg = v.ld_gu, lsg = v.lds_gu;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kSlots; s++) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kCW);
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (threadIdx.x < kMaxKF) samax[threadIdx.x] = 0u;
+    if (threadIdx.x < k) {
+        const int e = a.idx[threadIdx.x];
+        const bool ok = e >= 0 && e < v.E;
+        sidx[threadIdx.x] = ok ? e : -1;
+        if (!ok && b == 0) set_status(a.st, MOE_ERR_BAD_INDEX, (unsigned)threadIdx.x);
+    }
+    __syncthreads();
+
+    if (warp == kCW) {
+        // -------------------------------------------------------------- producer
+        if (lane == 0) {
+            const uint64_t pol = policy_evict_first();
+            int issued = 0;
+            for (int s = 0; s < nstageA + nstageB; s++) {
+                const int slot = s % kSlots;
+                const uint32_t ph = (uint32_t)(s / kSlots) & 1u;
+                if (!mbar_wait(&empty[slot], ph ^ 1u, a.st, 0x100u + slot)) {
+                    *abort_flag = 1;
+                    break;
+                }
+                if (*(volatile int *)abort_flag) break;
+                uint8_t *dst = slots + (size_t)slot * a.slot_bytes;
+                if (s < nstageA) {
+                    const int n0 = n_lo + kCW * s;
+                    const int cnt = min(kCW, n_hi - n0);
+                    mbar_arrive_expect_tx(&full[slot], (uint32_t)(cnt * 2 * (ldg + lsg)));
+                    // runs of consecutive items within one expert and one group of 16
+                    // rows are contiguous in the pool: 4 copies per run
+                    for (int j = 0; j < cnt;) {
+                        const int n = n0 + j;
+                        const int p = n / v.I, i = n % v.I;
+                        const int len = min(min(cnt - j, kGroupRows - i % kGroupRows), v.I - i);
+                        const int e = max(sidx[p], 0);  // invalid pairs: read expert 0, result discarded
+                        const uint8_t *rec = v.base + (uint64_t)e * v.rec;
+                        const int rg = 32 * (i / kGroupRows) + (i % kGroupRows);
+                        bulk_g2s(dst + (size_t)j * ldg, rec + (uint64_t)rg * ldg, (uint32_t)(len * ldg), &full[slot],
+                                 pol);
+                        bulk_g2s(dst + (size_t)(kCW + j) * ldg, rec + (uint64_t)(rg + kGroupRows) * ldg,
+                                 (uint32_t)(len * ldg), &full[slot], pol);
+                        const uint8_t *sr = rec + v.off_sgu;
+                        uint8_t *ds = dst + (size_t)2 * kCW * ldg;
+                        bulk_g2s(ds + (size_t)j * lsg, sr + (uint64_t)rg * lsg, (uint32_t)(len * lsg), &full[slot],
+                                 pol);
+                        bulk_g2s(ds + (size_t)(kCW + j) * lsg, sr + (uint64_t)(rg + kGroupRows) * lsg,
+                                 (uint32_t)(len * lsg), &full[slot], pol);
+                        j += len;
+                    }
+                } else {
+                    const int r0 = (s - nstageA) * a.R, nr = min(a.R, rows - r0);
+                    // scale rows: the 16-byte aligned span covering rows o_lo+r0 .. +nr
+                    const uint64_t s_lo = (uint64_t)(o_lo + r0) * v.lds_d / 16 * 16;
+                    const uint64_t s_hi = ((uint64_t)(o_lo + r0 + nr) * v.lds_d + 15) / 16 * 16;
+                    const uint32_t sbytes = (uint32_t)(s_hi - s_lo);
+                    mbar_arrive_expect_tx(&full[slot], (uint32_t)(k * (nr * v.ld_d + sbytes)));
+                    for (int p = 0; p < k; p++) {
+                        const int e = max(sidx[p], 0);
+                        const uint8_t *rec = v.base + (uint64_t)e * v.rec;
+                        bulk_g2s(dst + (size_t)p * a.R * v.ld_d, rec + v.off_d + (uint64_t)(o_lo + r0) * v.ld_d,
+                                 (uint32_t)(nr * v.ld_d), &full[slot], pol);
+                        bulk_g2s(dst + (size_t)k * a.R * v.ld_d + (size_t)p * a.sb_stride, rec + v.off_sd + s_lo,
+                                 sbytes, &full[slot], pol);
+                    }
+                }
+                issued = s + 1;
+            }
+            // copies still in flight must land before this CTA can exit
+            for (int s = max(0, issued - kSlots); s < issued; s++)
+                mbar_wait(&full[s % kSlots], (uint32_t)(s / kSlots) & 1u, a.st, 0x180u);
+        }
+        return;
+    }
+
+    // ------------------------------------------------------------------ consumers
+    // the token's max |x| (16-byte loads spread over the consumer threads)
+    float xa = 0.f;
+    for (int c = threadIdx.x; c < v.H / 8; c += kCW * 32) {
+        const uint4 raw = __ldg(reinterpret_cast<const uint4 *>(a.x) + c);
+        const unsigned int u[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+        for (int t = 0; t < 4; t++)
+            xa = fmaxf(xa, fmaxf(fabsf(__uint_as_float(u[t] << 16)), fabsf(__uint_as_float(u[t] & 0xffff0000u))));
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) xa = fmaxf(xa, __shfl_xor_sync(0xffffffffu, xa, off));
+    if (lane == 0) red[warp] = xa;
+    named_barrier(1, kCW * 32);
+    float amax_x = 0.f;
+    for (int ww = 0; ww < kCW; ww++) amax_x = fmaxf(amax_x, red[ww]);
+    named_barrier(1, kCW * 32);  // red[] is reused in phase B
+    // the token as f16 scaled by 2^-sx, max|x 2^-sx| in [128, 256) (exact for bf16),
+    // kept in registers: lane holds blocks lane + 32 j of 32 elements
+    int sx = 0;
+    if (amax_x > 0.f) {
+        int ex;
+        frexpf(amax_x, &ex);
+        sx = ex - 1 - 7;
+    }
+    uint4 xr[kMaxJ][4];
+#pragma unroll
+    for (int j = 0; j < kMaxJ; j++) {
+        const int kb = lane + 32 * j;
+        const uint4 *xp = reinterpret_cast<const uint4 *>(a.x + (size_t)kb * 32);
+#pragma unroll
+        for (int q = 0; q < 4; q++) {
+            unsigned int hw[4] = {0u, 0u, 0u, 0u};
+            if (kb < nkb) {
+                const uint4 raw = __ldg(xp + q);
+                const unsigned int u[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+                for (int t = 0; t < 4; t++)
+                    hw[t] = pack_half2(ldexpf(__uint_as_float(u[t] << 16), -sx),
+                                       ldexpf(__uint_as_float(u[t] & 0xffff0000u), -sx));
+            }
+            xr[j][q] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+        }
+    }
+
+    bool ok = true;
+    int s = 0;
+    // ---- phase A: one (gate row, up row) pair per warp per stage
+    for (; s < nstageA; s++) {
+        const int slot = s % kSlots;
+        const uint32_t ph = (uint32_t)(s / kSlots) & 1u;
+        const int n = n_lo + kCW * s + warp;
+        int p = 0, i = 0;
+        bool valid = false;
+        if (n < n_hi) {
+            p = n / v.I;
+            i = n % v.I;
+            valid = sidx[p] >= 0;
+        }
+        ok = !*(volatile int *)abort_flag && mbar_wait(&full[slot], ph, a.st, 0x200u + slot);
+        if (!ok) *abort_flag = 1;
+        float ag = 0.f, au = 0.f;
+        if (ok && valid) {
+            const uint8_t *base = slots + (size_t)slot * a.slot_bytes;
+            const uint8_t *cg = base + (size_t)warp * ldg;
+            const uint8_t *cu = base + (size_t)(kCW + warp) * ldg;
+            const uint8_t *sgp = base + (size_t)2 * kCW * ldg + (size_t)warp * lsg;
+            const uint8_t *sup = base + (size_t)2 * kCW * ldg + (size_t)(kCW + warp) * lsg;
+#pragma unroll
+            for (int j = 0; j < kMaxJ; j++) {
+                const int kb = lane + 32 * j;
+                if (kb < nkb) {
+                    const uint4 qg = *reinterpret_cast<const uint4 *>(cg + kb * 16);
+                    const uint4 qu = *reinterpret_cast<const uint4 *>(cu + kb * 16);
+                    ag = fmaf(block_dot1(qg, xr[j]), e8m0_fast(sgp[kb]), ag);
+                    au = fmaf(block_dot1(qu, xr[j]), e8m0_fast(sup[kb]), au);
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[slot]);
+        if (ok && valid) {
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) {
+                ag += __shfl_xor_sync(0xffffffffu, ag, off);
+                au += __shfl_xor_sync(0xffffffffu, au, off);
+            }
+            if (lane == 0) {
+                const float gv = ldexpf(ag, sx), uv = ldexpf(au, sx);
+                const float hval = gv / (1.f + expf(-gv)) * uv;
+                a.h[(size_t)p * v.I + i] = hval;
+                atomicMax(&samax[p], __float_as_uint(fabsf(hval)));
+            }
+        }
+    }
+    // this CTA's share of each pair's max |h| (non-negative floats order as integers)
+    named_barrier(1, kCW * 32);
+    if (threadIdx.x < k && samax[threadIdx.x] != 0u) atomicMax(&a.st->pad[8 + threadIdx.x], samax[threadIdx.x]);
+    // every consumer warp takes part, aborted or not, so the named barriers match
+    ok = grid_barrier(&a.st->pad[1], (unsigned)G, 1, kCW * 32, a.st, 0x300u, abort_flag);
+
+    // ---- phase B: the warp owns pairs warp and warp + 8, their h in registers as
+    // f16 scaled by a per-pair power of two (found from the loaded values)
+    uint4 hr[2][2][4];
+    float wsc[2] = {0.f, 0.f};
+    bool pv[2] = {false, false};
+    if (ok) {
+#pragma unroll
+        for (int pi = 0; pi < 2; pi++) {
+            const int p = warp + kCW * pi;
+            pv[pi] = p < k && sidx[p] >= 0;
+            int sp = 0;
+            if (pv[pi]) {
+                const float ha = __uint_as_float(__ldcg(&a.st->pad[8 + p]));
+                if (ha > 0.f && isfinite(ha)) {
+                    int ex;
+                    frexpf(ha, &ex);
+                    sp = ex - 1 - 7;
+                }
+                wsc[pi] = ldexpf(a.w[p], sp);
+            }
+#pragma unroll
+            for (int blk = 0; blk < 2; blk++) {
+                const int kb = lane + 32 * blk;
+#pragma unroll
+                for (int q = 0; q < 4; q++) {
+                    unsigned int hw[4] = {0u, 0u, 0u, 0u};
+                    if (pv[pi] && kb < nkbd) {
+                        const float4 *hp = reinterpret_cast<const float4 *>(a.h + (size_t)p * v.I + kb * 32 + q * 8);
+                        const float4 f0 = __ldcg(hp), f1 = __ldcg(hp + 1);
+                        hw[0] = pack_half2(ldexpf(f0.x, -sp), ldexpf(f0.y, -sp));
+                        hw[1] = pack_half2(ldexpf(f0.z, -sp), ldexpf(f0.w, -sp));
+                        hw[2] = pack_half2(ldexpf(f1.x, -sp), ldexpf(f1.y, -sp));
+                        hw[3] = pack_half2(ldexpf(f1.z, -sp), ldexpf(f1.w, -sp));
+                    }
+                    hr[pi][blk][q] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                }
+            }
+        }
+        for (int sb = 0; sb < nstageB; sb++, s++) {
+            const int slot = s % kSlots;
+            const uint32_t ph = (uint32_t)(s / kSlots) & 1u;
+            const int r0 = sb * a.R, nr = min(a.R, rows - r0);
+            const int soff = (int)((uint64_t)(o_lo + r0) * v.lds_d % 16);  // first scale row in the span
+            ok = !*(volatile int *)abort_flag && mbar_wait(&full[slot], ph, a.st, 0x400u + slot);
+            if (!ok) *abort_flag = 1;
+            float part[kMaxR] = {0.f, 0.f, 0.f, 0.f};
+            if (ok) {
+                const uint8_t *base = slots + (size_t)slot * a.slot_bytes;
+#pragma unroll
+                for (int pi = 0; pi < 2; pi++) {
+                    if (!pv[pi]) continue;
+                    const int p = warp + kCW * pi;
+#pragma unroll
+                    for (int r = 0; r < kMaxR; r++) {
+                        if (r >= nr) continue;
+                        const uint8_t *row = base + ((size_t)p * a.R + r) * v.ld_d;
+                        const uint8_t *srow =
+                            base + (size_t)k * a.R * v.ld_d + (size_t)p * a.sb_stride + soff + (size_t)r * v.lds_d;
+                        float dsum = 0.f;
+#pragma unroll
+                        for (int blk = 0; blk < 2; blk++) {
+                            const int kb = lane + 32 * blk;
+                            if (kb < nkbd) {
+                                const uint4 q = *reinterpret_cast<const uint4 *>(row + kb * 16);
+                                dsum = fmaf(block_dot1(q, hr[pi][blk]), e8m0_fast(srow[kb]), dsum);
+                            }
+                        }
+                        part[r] = fmaf(wsc[pi], dsum, part[r]);
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[slot]);
+#pragma unroll
+            for (int r = 0; r < kMaxR; r++) {
+                float t = part[r];
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) t += __shfl_xor_sync(0xffffffffu, t, off);
+                if (lane == 0 && r < nr) red[warp * kMaxRowsCta + r0 + r] = t;
+            }
+        }
+    }
+    named_barrier(1, kCW * 32);
+    if (ok && !*(volatile int *)abort_flag) {
+        for (int t = threadIdx.x; t < rows; t += kCW * 32) {
+            float acc = 0.f;
+            for (int ww = 0; ww < kCW; ww++) acc += red[ww * kMaxRowsCta + t];
+            const int o = o_lo + t;
+            if (a.residual != nullptr) acc += bf16_bits_to_float(a.residual[o]);
+            const __nv_bfloat16 bv = __float2bfloat16_rn(acc);
+            a.y[o] = *reinterpret_cast<const uint16_t *>(&bv);
+        }
+    }
+    // every CTA is past the grid barrier: the last one here resets both counters
+    if (threadIdx.x == 0) {
+        __threadfence();
+        if (atomicAdd(&a.st->pad[2], 1u) == (unsigned)G - 1u) {
+            for (int p = 0; p < kMaxKF; p++) atomicExch(&a.st->pad[8 + p], 0u);
+            atomicExch(&a.st->pad[1], 0u);
+            atomicExch(&a.st->pad[2], 0u);
+        }
+    }
+}
+
+int g_sms = 0;
+int g_grid = -1;   // co-resident CTAs of the fused kernel (0: unusable)
+int g_smem_set = 0;
+
+}  // namespace
+
+// Launch the fused kernel if the shape allows it; cudaErrorNotSupported otherwise
+// (the caller then uses the general decode kernels).
+cudaError_t launch_decode_fused(const PoolView &v, const uint16_t *x, const int32_t *idx, const float *w, int k,
+                                const uint16_t *residual, uint16_t *y, void *ws, cudaStream_t st) {
+    if (!(k <= kMaxKF && v.H <= 32 * 32 * kMaxJ && v.H % 512 == 0 && v.I <= 64 * 32))
+        return cudaErrorNotSupported;
+    if (g_sms == 0) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&g_sms, cudaDevAttrMultiProcessorCount, dev);
+    }
+    FusedArgs fa;
+    fa.v = v;
+    fa.k = k;
+    fa.x = x;
+    fa.idx = idx;
+    fa.w = w;
+    fa.residual = residual;
+    fa.y = y;
+    fa.h = reinterpret_cast<float *>((char *)ws + 256);
+    fa.st = reinterpret_cast<StatusWord *>(ws);
+    const uint32_t slotA = (uint32_t)(2 * kCW * (v.ld_gu + v.lds_gu));
+    // phase-B stage: R rows of W_d per pair plus a 16-byte aligned span of their scale rows
+    auto sb_of = [&](int r) { return (uint32_t)((r * v.lds_d + 15) / 16 * 16 + 32); };
+    auto stageB = [&](int r) { return (uint32_t)k * ((uint32_t)r * v.ld_d + sb_of(r)); };
+    int R = kMaxR;
+    while (R > 1 && stageB(R) > slotA) R--;
+    fa.R = R;
+    fa.sb_stride = sb_of(R);
+    const uint32_t slot_need = slotA > stageB(R) ? slotA : stageB(R);
+    fa.slot_bytes = (slot_need + 127) / 128 * 128;
+    const size_t smem = (size_t)kSlots * fa.slot_bytes + 2 * kSlots * sizeof(uint64_t) +
+                        (size_t)kCW * kMaxRowsCta * sizeof(float) + (2 * kMaxKF + 4) * sizeof(int);
+    cudaError_t e = ensure_dynamic_smem(decode_fused_kernel, smem, g_smem_set);
+    if (e != cudaSuccess) return e;
+    if (g_grid < 0) {
+        int per_sm = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_fused_kernel, kThreadsF, smem);
+        if (e != cudaSuccess) return e;
+        g_grid = per_sm >= 1 ? g_sms : 0;
+    }
+    fa.G = g_grid;
+    if (fa.G <= 0 || (v.H + fa.G - 1) / fa.G > kMaxRowsCta) return cudaErrorNotSupported;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(fa.G);
+    cfg.blockDim = dim3(kThreadsF);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;  // all CTAs co-resident: the grid barrier needs it
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    TraceScope trace_scope("decode_fused", st);
+    e = cudaLaunchKernelEx(&cfg, decode_fused_kernel, fa);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+}  // namespace moe

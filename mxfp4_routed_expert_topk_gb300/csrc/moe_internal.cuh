@@ -143,6 +143,10 @@ size_t decode_workspace_bytes(int E, int H, int I, int M, int k);
 cudaError_t launch_decode(const PoolView &v, const uint16_t *x, int M, const int32_t *idx, const float *w,
                           int k, const uint16_t *residual, uint16_t *y, void *ws, cudaStream_t st);
 
+// Single-token fused decode; cudaErrorNotSupported when the shape does not allow it.
+cudaError_t launch_decode_fused(const PoolView &v, const uint16_t *x, const int32_t *idx, const float *w, int k,
+                                const uint16_t *residual, uint16_t *y, void *ws, cudaStream_t st);
+
 cudaError_t launch_prescale(const uint16_t *x, int M, int H, uint16_t *out, cudaStream_t st);
 
 size_t grouped_workspace_bytes(int E, int H, int I, int T, int k);

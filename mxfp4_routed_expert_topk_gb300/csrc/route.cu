@@ -26,7 +26,6 @@ namespace {
 
 constexpr int kLogitTokens = 8;    // tokens per CTA in the logit kernel
 constexpr int kLogitExperts = 4;   // experts per CTA (two warps each, one per half of H)
-constexpr int kSelectThreads = 512;
 constexpr int kMaxE = 4096;
 constexpr int kMaxCand = 256;      // experts that may still enter the top k
 constexpr int kMaxExact = 64;      // experts evaluated exactly per token
@@ -63,12 +62,12 @@ __device__ __forceinline__ void unpack_bf16x8(const uint4 &v, float f[8]) {
     }
 }
 
-// grid (ceil(E/4), ceil(M/8)), 256 threads.  Warp w handles expert 4*bx + w/2 over
-// one half of H for up to 8 tokens; lanes take 8 consecutive elements per step.
-__global__ void __launch_bounds__(256) route_logits_kernel(const uint16_t *__restrict__ x, int M, int H,
-                                                           const uint16_t *__restrict__ Wr, int E,
-                                                           const float *__restrict__ skew,
-                                                           float *__restrict__ logit, float *__restrict__ bound) {
+// Block (bx, by): experts 4*bx .. 4*bx+3 for tokens 8*by .. 8*by+7.  Warp w handles
+// expert 4*bx + w/2 over one half of H; lanes take 8 consecutive elements per step.
+// Used with 256 threads; x rows staged in dynamic shared memory.
+__device__ void logits_block(const uint16_t *__restrict__ x, int M, int H, const uint16_t *__restrict__ Wr, int E,
+                             const float *__restrict__ skew, float *__restrict__ logit,
+                             float *__restrict__ bound) {
     extern __shared__ __align__(16) uint16_t xs[];  // [nt][H]
     __shared__ float red_l[8][kLogitTokens], red_s[8][kLogitTokens];
     const int m0 = blockIdx.y * kLogitTokens;
@@ -141,6 +140,13 @@ __global__ void __launch_bounds__(256) route_logits_kernel(const uint16_t *__res
     }
 }
 
+__global__ void __launch_bounds__(256) route_logits_kernel(const uint16_t *__restrict__ x, int M, int H,
+                                                           const uint16_t *__restrict__ Wr, int E,
+                                                           const float *__restrict__ skew,
+                                                           float *__restrict__ logit, float *__restrict__ bound) {
+    logits_block(x, M, H, Wr, E, skew, logit, bound);
+}
+
 // ------------------------------------------------------------ exact logits
 
 __device__ __forceinline__ bool bf16_parts(uint16_t b, int &neg, unsigned int &m, int &ep) {
@@ -188,8 +194,8 @@ __device__ __forceinline__ __int128 shfl_xor_i128(__int128 v, int off) {
 
 struct ExactScratch {
     long long bins[kBins];
-    __int128 part[kSelectThreads / 32];
-    int tmax[kSelectThreads / 32];
+    __int128 part[32];
+    int tmax[32];
     int T0;
     int bad;
 };
@@ -278,109 +284,148 @@ __device__ void exact_logit(const uint16_t *xr, const uint16_t *wr, int H, const
 
 // ------------------------------------------------------------- selection
 
+constexpr int kRouteThreads = 256;
+constexpr int kRouteWarps = kRouteThreads / 32;
+constexpr int kKeysPerThread = kMaxE / kRouteThreads;  // 16
+
 __device__ __forceinline__ unsigned int orderable(float f) {
     const unsigned int u = __float_as_uint(f);
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+// Sort key of expert e: larger logit first, then lower index (keys are unique).
+__device__ __forceinline__ unsigned long long route_key(float l, int e) {
+    return ((unsigned long long)orderable(l) << 32) | (unsigned long long)(0xFFFFFFFFu - (unsigned)e);
+}
+
+__device__ __forceinline__ int key_expert(unsigned long long key) {
+    return (int)(0xFFFFFFFFu - (unsigned)(key & 0xFFFFFFFFull));
+}
+
+// The warp's k largest keys in descending order into out[0..k) (0 = none): k rounds
+// of a warp max; the lane holding the winner drops it and rescans its own keys.
+template <int J>
+__device__ void warp_topk(unsigned long long (&key)[J], int k, unsigned long long *out) {
+    const int lane = threadIdx.x & 31;
+    unsigned long long best = 0ull;
+#pragma unroll
+    for (int j = 0; j < J; j++) best = key[j] > best ? key[j] : best;
+    for (int r = 0; r < k; r++) {
+        unsigned long long m = best;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            const unsigned long long o = __shfl_xor_sync(0xffffffffu, m, off);
+            m = o > m ? o : m;
+        }
+        if (lane == 0) out[r] = m;
+        if (m != 0ull && best == m) {
+            best = 0ull;
+#pragma unroll
+            for (int j = 0; j < J; j++) {
+                if (key[j] == m) key[j] = 0ull;
+                best = key[j] > best ? key[j] : best;
+            }
+        }
+    }
+}
+
 struct SelectShared {
-    unsigned long long keys[kMaxE];
-    int cand[kMaxCand];          // sorted positions >= k that may still enter
+    unsigned long long wtop[kRouteWarps][kMaxK];  // each warp's top k
+    unsigned long long top[kMaxK];                // the token's top k by fp32 logit
+    unsigned int Lord;
+    int cand[kMaxCand];                           // outsiders that may still enter
     int ncand;
     int nonfinite;
     int uncertain;
-    // slow path
-    int aexp[kMaxCand + kMaxK];  // experts of the candidate set, ordered by upper bound
-    int comp[kMaxCand + kMaxK];  // component id
-    int xlist[kMaxExact];        // experts evaluated exactly
+    int overflow;
     int nx;
+    int aexp[kMaxCand + kMaxK];                   // candidate set ordered by upper bound
+    int comp[kMaxCand + kMaxK];                   // interval-cluster id
+    int xlist[kMaxExact];                         // experts evaluated exactly
     long long exact[kMaxExact][kLimbs];
     int final_idx[kMaxK];
-    int overflow;
     ExactScratch sc;
 };
 
-__global__ void __launch_bounds__(kSelectThreads) route_select_kernel(
-    const uint16_t *__restrict__ x, int H, const uint16_t *__restrict__ Wr, int E, const float *__restrict__ skew,
-    int k, const float *__restrict__ logit, const float *__restrict__ bound, int32_t *__restrict__ idx_out,
-    float *__restrict__ w_out, StatusWord *st) {
-    extern __shared__ __align__(16) unsigned char smem_raw[];
-    SelectShared &s = *reinterpret_cast<SelectShared *>(smem_raw);
-    const int m = blockIdx.x, tid = threadIdx.x;
-    const float *lm = logit + (size_t)m * E;
-    const float *bm = bound + (size_t)m * E;
-    int P = 2;
-    while (P < E) P <<= 1;
+// Exact top-k and softmax of one token (whole CTA of kRouteThreads threads).
+// lm / bm: the token's fp32 logits and bounds (read through L2: they may have
+// been written by other CTAs of the same kernel).
+__device__ void select_token(int m, const uint16_t *__restrict__ x, int H, const uint16_t *__restrict__ Wr, int E,
+                             const float *__restrict__ skew, int k, const float *lm, const float *bm,
+                             int32_t *__restrict__ idx_out, float *__restrict__ w_out, StatusWord *st,
+                             SelectShared &s) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     if (tid == 0) {
         s.ncand = 0;
         s.nonfinite = 0;
         s.uncertain = 0;
         s.overflow = 0;
         s.nx = 0;
+        s.Lord = 0xFFFFFFFFu;
     }
-    __syncthreads();
-    for (int i = tid; i < P; i += blockDim.x) {
-        unsigned long long key = 0ull;
-        if (i < E) {
-            const float l = lm[i], b = bm[i];
-            if (!isfinite(l) || !isfinite(b)) s.nonfinite = 1;
-            key = ((unsigned long long)orderable(l) << 32) | (unsigned long long)(0xFFFFFFFFu - (unsigned)i);
-        }
-        s.keys[i] = key;
-    }
-    __syncthreads();
-    // bitonic sort, descending
-    for (int size = 2; size <= P; size <<= 1) {
-        for (int stride = size >> 1; stride > 0; stride >>= 1) {
-            for (int i = tid; i < P / 2; i += blockDim.x) {
-                const int lo = 2 * i - (i & (stride - 1));
-                const int hi = lo + stride;
-                const bool desc = (lo & size) == 0;
-                const unsigned long long a = s.keys[lo], b = s.keys[hi];
-                if ((a < b) == desc) {
-                    s.keys[lo] = b;
-                    s.keys[hi] = a;
-                }
-            }
-            __syncthreads();
+    unsigned long long key[kKeysPerThread];
+    float lv[kKeysPerThread], bv[kKeysPerThread];
+    bool bad = false;
+#pragma unroll
+    for (int j = 0; j < kKeysPerThread; j++) {
+        const int e = tid + kRouteThreads * j;
+        key[j] = 0ull;
+        lv[j] = 0.f;
+        bv[j] = 0.f;
+        if (e < E) {
+            lv[j] = __ldcg(lm + e);
+            bv[j] = __ldcg(bm + e);
+            if (!isfinite(lv[j]) || !isfinite(bv[j])) bad = true;
+            key[j] = route_key(lv[j], e);
         }
     }
-    auto expert_at = [&](int pos) { return (int)(0xFFFFFFFFu - (unsigned)(s.keys[pos] & 0xFFFFFFFFull)); };
-
+    __syncthreads();
+    if (bad) s.nonfinite = 1;
+    warp_topk<kKeysPerThread>(key, k, s.wtop[warp]);
+    __syncthreads();
+    if (warp == 0) {
+        constexpr int JW = kRouteWarps * kMaxK / 32;
+        unsigned long long wk[JW];
+#pragma unroll
+        for (int j = 0; j < JW; j++) {
+            const int q = lane + 32 * j;
+            const int ww = q / kMaxK, r = q % kMaxK;
+            wk[j] = (r < k) ? s.wtop[ww][r] : 0ull;
+        }
+        warp_topk<JW>(wk, k, s.top);
+    }
+    __syncthreads();
+    const unsigned long long kth = s.top[k - 1];
     // lowest lower bound among the k winners
-    float myL = __int_as_float(0x7f800000);
-    for (int p = tid; p < k; p += blockDim.x) {
-        const int e = expert_at(p);
-        myL = fminf(myL, __fsub_rd(lm[e], bm[e]));
+    if (tid < k) {
+        const int e = key_expert(s.top[tid]);
+        atomicMin(&s.Lord, orderable(__fsub_rd(__ldcg(lm + e), __ldcg(bm + e))));
     }
-    for (int off = 16; off > 0; off >>= 1) myL = fminf(myL, __shfl_xor_sync(0xffffffffu, myL, off));
-    // float min through an orderable integer min
-    __shared__ unsigned int Lord;
-    if (tid == 0) Lord = 0xFFFFFFFFu;
     __syncthreads();
-    if ((tid & 31) == 0) atomicMin(&Lord, orderable(myL));
-    __syncthreads();
-    const unsigned int Lo = Lord;
-    // outsiders whose upper bound reaches L; adjacent winners whose intervals meet
-    for (int p = k + tid; p < E; p += blockDim.x) {
-        const int e = expert_at(p);
-        if (orderable(__fadd_ru(lm[e], bm[e])) >= Lo) {
+    const unsigned int Lo = s.Lord;
+    // outsiders whose upper bound reaches it; adjacent winners whose intervals meet
+#pragma unroll
+    for (int j = 0; j < kKeysPerThread; j++) {
+        const int e = tid + kRouteThreads * j;
+        if (e < E && route_key(lv[j], e) < kth && orderable(__fadd_ru(lv[j], bv[j])) >= Lo) {
             const int slot = atomicAdd(&s.ncand, 1);
-            if (slot < kMaxCand) s.cand[slot] = p;
+            if (slot < kMaxCand) s.cand[slot] = e;
             else s.overflow = 1;
         }
     }
-    for (int p = tid; p + 1 < k; p += blockDim.x) {
-        const int a = expert_at(p), b = expert_at(p + 1);
-        if (!(__fsub_rd(lm[a], bm[a]) > __fadd_ru(lm[b], bm[b]))) s.uncertain = 1;
+    if (tid + 1 < k) {
+        const int a = key_expert(s.top[tid]), b = key_expert(s.top[tid + 1]);
+        if (!(__fsub_rd(__ldcg(lm + a), __ldcg(bm + a)) > __fadd_ru(__ldcg(lm + b), __ldcg(bm + b)))) s.uncertain = 1;
     }
     __syncthreads();
+    auto L_ = [&](int e) { return __ldcg(lm + e); };
+    auto B_ = [&](int e) { return __ldcg(bm + e); };
     if (s.nonfinite) {
         if (tid == 0) set_status(st, MOE_ERR_NONFINITE, (unsigned)m);
-        for (int j = tid; j < k; j += blockDim.x) s.final_idx[j] = expert_at(j);
+        if (tid < k) s.final_idx[tid] = key_expert(s.top[tid]);
         __syncthreads();
     } else if (s.ncand == 0 && !s.uncertain) {
-        for (int j = tid; j < k; j += blockDim.x) s.final_idx[j] = expert_at(j);
+        if (tid < k) s.final_idx[tid] = key_expert(s.top[tid]);
         __syncthreads();
     } else {
         // ---- slow path: interval clusters, exact evaluation where needed
@@ -388,16 +433,16 @@ __global__ void __launch_bounds__(kSelectThreads) route_select_kernel(
             atomicAdd(&st->exact_fallbacks, 1u);
             const int nc = min(s.ncand, kMaxCand);
             int n = 0;
-            for (int p = 0; p < k; p++) s.aexp[n++] = expert_at(p);
-            for (int c = 0; c < nc; c++) s.aexp[n++] = expert_at(s.cand[c]);
-            // insertion sort by upper bound descending (ties: lower bound descending, then index)
+            for (int p = 0; p < k; p++) s.aexp[n++] = key_expert(s.top[p]);
+            for (int c = 0; c < nc; c++) s.aexp[n++] = s.cand[c];
+            // insertion sort by upper bound descending (ties: lower index first)
             for (int i = 1; i < n; i++) {
                 const int e = s.aexp[i];
-                const float ue = __fadd_ru(lm[e], bm[e]);
+                const float ue = __fadd_ru(L_(e), B_(e));
                 int j = i - 1;
                 while (j >= 0) {
                     const int f = s.aexp[j];
-                    const float uf = __fadd_ru(lm[f], bm[f]);
+                    const float uf = __fadd_ru(L_(f), B_(f));
                     if (uf > ue || (uf == ue && f < e)) break;
                     s.aexp[j + 1] = f;
                     j--;
@@ -406,15 +451,15 @@ __global__ void __launch_bounds__(kSelectThreads) route_select_kernel(
             }
             // connected components of the interval graph, in order
             int cid = 0;
-            float run_lo = __fsub_rd(lm[s.aexp[0]], bm[s.aexp[0]]);
+            float run_lo = __fsub_rd(L_(s.aexp[0]), B_(s.aexp[0]));
             s.comp[0] = 0;
             for (int i = 1; i < n; i++) {
                 const int e = s.aexp[i];
-                if (__fadd_ru(lm[e], bm[e]) >= run_lo) {
-                    run_lo = fminf(run_lo, __fsub_rd(lm[e], bm[e]));
+                if (__fadd_ru(L_(e), B_(e)) >= run_lo) {
+                    run_lo = fminf(run_lo, __fsub_rd(L_(e), B_(e)));
                 } else {
                     cid++;
-                    run_lo = __fsub_rd(lm[e], bm[e]);
+                    run_lo = __fsub_rd(L_(e), B_(e));
                 }
                 s.comp[i] = cid;
             }
@@ -472,7 +517,7 @@ __global__ void __launch_bounds__(kSelectThreads) route_select_kernel(
                             const int qf = xi(f);
                             int c;
                             if (qe >= 0 && qf >= 0) c = limbs_cmp(s.exact[qf], s.exact[qe]);
-                            else c = (lm[f] > lm[e]) ? 1 : ((lm[f] < lm[e]) ? -1 : 0);  // only on overflow
+                            else c = (L_(f) > L_(e)) ? 1 : ((L_(f) < L_(e)) ? -1 : 0);  // only on overflow
                             if (c > 0 || (c == 0 && f < e)) break;
                             order[b + 1] = f;
                             b--;
@@ -489,7 +534,7 @@ __global__ void __launch_bounds__(kSelectThreads) route_select_kernel(
     // softmax over the k selected fp32 logits
     if (tid < 32) {
         const int j = tid;
-        const float l = (j < k) ? lm[s.final_idx[j]] : -__int_as_float(0x7f800000);
+        const float l = (j < k) ? L_(s.final_idx[j]) : -__int_as_float(0x7f800000);
         float mx = l;
         for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
         const float ex = (j < k) ? expf(l - mx) : 0.f;
@@ -500,6 +545,38 @@ __global__ void __launch_bounds__(kSelectThreads) route_select_kernel(
             w_out[(size_t)m * k + j] = ex / z;
         }
     }
+}
+
+// One CTA per token.
+__global__ void __launch_bounds__(kRouteThreads) route_select_kernel(
+    const uint16_t *__restrict__ x, int H, const uint16_t *__restrict__ Wr, int E, const float *__restrict__ skew,
+    int k, const float *__restrict__ logit, const float *__restrict__ bound, int32_t *__restrict__ idx_out,
+    float *__restrict__ w_out, StatusWord *st) {
+    __shared__ SelectShared s;
+    const int m = blockIdx.x;
+    select_token(m, x, H, Wr, E, skew, k, logit + (size_t)m * E, bound + (size_t)m * E, idx_out, w_out, st, s);
+}
+
+// Single token: logits of 4 experts per CTA as in route_logits_kernel, then the
+// last CTA to finish (ticket in the status word, reset after use) selects.
+__global__ void __launch_bounds__(kRouteThreads) route_single_kernel(
+    const uint16_t *__restrict__ x, int H, const uint16_t *__restrict__ Wr, int E, const float *__restrict__ skew,
+    int k, float *__restrict__ logit, float *__restrict__ bound, int32_t *__restrict__ idx_out,
+    float *__restrict__ w_out, StatusWord *st) {
+    __shared__ SelectShared s;
+    __shared__ int last;
+    logits_block(x, 1, H, Wr, E, skew, logit, bound);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        const unsigned int t = atomicAdd(&st->pad[0], 1u);
+        last = (t == gridDim.x - 1);
+    }
+    __syncthreads();
+    if (!last) return;
+    __threadfence();
+    select_token(0, x, H, Wr, E, skew, k, logit, bound, idx_out, w_out, st, s);
+    if (threadIdx.x == 0) st->pad[0] = 0u;
 }
 
 }  // namespace
@@ -516,20 +593,25 @@ cudaError_t launch_route(const uint16_t *x, int M, int H, const uint16_t *Wr, in
     const int nt = M < kLogitTokens ? M : kLogitTokens;
     if ((size_t)nt * H * sizeof(uint16_t) > 200 * 1024) return cudaErrorInvalidValue;
     const size_t smem1 = (size_t)nt * H * sizeof(uint16_t);
-    static int smem_logits = 0, smem_select = 0;
+    static int smem_logits = 0, smem_single = 0;
     cudaError_t e = ensure_dynamic_smem(route_logits_kernel, smem1, smem_logits);
     if (e != cudaSuccess) return e;
-    e = ensure_dynamic_smem(route_select_kernel, sizeof(SelectShared), smem_select);
+    e = ensure_dynamic_smem(route_single_kernel, smem1, smem_single);
     if (e != cudaSuccess) return e;
+    StatusWord *stw = reinterpret_cast<StatusWord *>(ws);
     dim3 g1((E + kLogitExperts - 1) / kLogitExperts, (M + kLogitTokens - 1) / kLogitTokens);
+    if (M == 1) {
+        TraceScope trace_scope("route_single", st);
+        route_single_kernel<<<g1.x, kRouteThreads, smem1, st>>>(x, H, Wr, E, skew, k, r.logit, r.bound, idx, w, stw);
+        return cudaGetLastError();
+    }
     {
         TraceScope trace_scope("route_logits", st);
         route_logits_kernel<<<g1, 256, smem1, st>>>(x, M, H, Wr, E, skew, r.logit, r.bound);
     }
     {
         TraceScope trace_scope("route_select", st);
-        route_select_kernel<<<M, kSelectThreads, sizeof(SelectShared), st>>>(
-            x, H, Wr, E, skew, k, r.logit, r.bound, idx, w, reinterpret_cast<StatusWord *>(ws));
+        route_select_kernel<<<M, kRouteThreads, 0, st>>>(x, H, Wr, E, skew, k, r.logit, r.bound, idx, w, stw);
     }
     return cudaGetLastError();
 }
