@@ -1,12 +1,518 @@
-// Grouped block-scaled GEMMs of the prefill path (tcgen05).  Not built yet.
+// Grouped block-scaled GEMMs of the expert-major prefill path on the 5th-generation
+// tensor cores (tcgen05, kind::mxf8f6f4): weights are the MMA's A operand (E2M1,
+// one E8M0 scale per 32 along K, 128 rows per tile), the expert's sorted token rows
+// are B (E4M3 with E8M0 scales, up to BN rows per tile), fp32 accumulators in TMEM.
+//
+//   GEMM 1 (gate/up): A = W_gu (2I rows, K = H), B = MXFP8 x rows; epilogue
+//            h = silu(g) * u from the interleaved gate/up rows, quantised to MXFP8
+//            along I (the same rule as x) -> hq, hs
+//   GEMM 2 (down):    A = W_d (H rows, K = I, zero padded to 128), B = MXFP8 h rows;
+//            epilogue writes the unweighted expert output rows (fp32 or bf16)
+//
+// One CTA per (expert, 128-row tile of A), 4 warps: warp 0 issues the tensor
+// copies of A and B, warp 1 stages the scale factors in shared memory in the
+// 32x16-byte layout tcgen05.cp expects, warp 2 owns TMEM and issues the MMAs,
+// and all four warps run the epilogue (warp w reads TMEM lanes 32w..32w+31).
+// Every wait is bounded (MOE_ERR_TIMEOUT), and nothing exits with copies or MMAs
+// in flight.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include "prefill_internal.cuh"
+#include "sm100_async.cuh"
 
 namespace moe {
+namespace {
+
+constexpr int kStages = 4;
+constexpr int kTileM = 128;
+constexpr int kTileK = 128;   // elements (bytes in shared memory for both operands)
+constexpr int kBoxN = 16;     // rows per tensor copy of B
+constexpr int kGemmThreads = 128;
+constexpr int kMaxBN = 256;
+
+struct GemmArgs {
+    int mode;            // 1: gate/up + SwiGLU + MXFP8, 2: down
+    int E;
+    int Kel;             // K elements (H for gate/up, I for down)
+    int nkt;             // K tiles of 128
+    int nkb_a;           // scale blocks per A row present in the pool (H/32 or Ip/32)
+    int nkb_b;           // valid scale blocks per B row (H/32 or I/32)
+    int lds_a;           // bytes per A scale row
+    int lds_b;           // bytes per B scale row
+    uint64_t a_scale_off;  // offset of A's scale plane in a record
+    const uint8_t *pool;
+    uint64_t rec;
+    const int32_t *offsets;
+    const uint8_t *bscale;   // xs or hs, [P][lds_b]
+    int BN;              // columns of the accumulator tile (multiple of 16)
+    uint32_t tmem_cols;
+    // epilogue outputs
+    int I;               // intermediate size (gate/up epilogue)
+    int H;               // hidden size (down epilogue)
+    uint8_t *hq;         // [P][I]
+    uint8_t *hs;         // [P][lds_hs]
+    int lds_hs;
+    void *partial;       // [P][H]
+    int partial_dtype;
+    StatusWord *st;
+};
+
+// ---------------------------------------------------------------- PTX helpers
+
+__device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, int c0, int c1, int c2, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(
+            smem_u32(dst)),
+        "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int c0, int c1, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+            smem_u32(dst)),
+        "l"(map), "r"(c0), "r"(c1), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// Shared-memory matrix descriptor of tcgen05: start address, leading / stride
+// byte offsets (16-byte units), fixed version bits 46..48 = 0b001, swizzle mode.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo, uint32_t swizzle) {
+    uint64_t d = 0;
+    d |= (uint64_t)((addr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)(swizzle & 7u) << 61;
+    return d;
+}
+constexpr uint32_t kSwizzle128B = 2;
+constexpr uint32_t kSwizzleNone = 0;
+
+// Instruction descriptor of kind::mxf8f6f4: A = E2M1 (5), B = E4M3 (0), both
+// K-major, M = 128, N = n, E8M0 scales, scale-factor ids for A and B.
+__device__ __forceinline__ uint32_t idesc_mxf8f6f4(int n, int sf_id) {
+    uint32_t d = 0;
+    d |= (uint32_t)(sf_id & 3) << 4;     // B scale factor id
+    d |= 5u << 7;                        // A format: E2M1
+    d |= 0u << 10;                       // B format: E4M3
+    d |= (uint32_t)(n >> 3) << 17;       // N / 8
+    d |= 1u << 23;                       // scale format: UE8M0
+    d |= (uint32_t)(kTileM >> 4) << 24;  // M / 16
+    d |= (uint32_t)(sf_id & 3) << 29;    // A scale factor id
+    return d;
+}
+
+__device__ __forceinline__ void tmem_alloc(uint32_t *dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tc_cp_sf(uint32_t taddr, uint64_t sdesc) {
+    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t sfa,
+                                       uint32_t sfb, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+            d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_commit(uint64_t *bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 16; i++) v[i] = __uint_as_float(r[i]);
+}
+
+// ------------------------------------------------------------------- kernel
+
+struct GemmSmemLayout {
+    uint32_t a, b, sfa, sfb, bars, misc, total;
+    __host__ __device__ GemmSmemLayout(int BN) {
+        const uint32_t nsfb = (uint32_t)((BN + 127) / 128);
+        a = 0;                                            // kStages x 16 KB (1024-aligned)
+        b = a + kStages * kTileM * kTileK;                // kStages x BN*128
+        sfa = b + kStages * (uint32_t)BN * kTileK;        // kStages x 512
+        sfb = sfa + kStages * 512;                        // kStages x nsfb*512
+        bars = sfb + kStages * 512 * nsfb;                // full[], empty[], done
+        misc = bars + (2 * kStages + 1) * 8;              // tmem addr, abort, amax[4][16]
+        total = misc + 16 + 4 * 16 * 4;
+    }
+};
+
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                        const GemmArgs a) {
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    // the tensor copies with 128-byte swizzling need 1024-byte aligned tiles
+    unsigned char *smem = (unsigned char *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    const GemmSmemLayout L(a.BN);
+    uint8_t *sA = smem + L.a, *sB = smem + L.b, *sSFA = smem + L.sfa, *sSFB = smem + L.sfb;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.bars);
+    uint64_t *empty = full + kStages;
+    uint64_t *done = empty + kStages;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L.misc);
+    int *abort_flag = reinterpret_cast<int *>(smem + L.misc + 4);
+    float *amax_x = reinterpret_cast<float *>(smem + L.misc + 16);  // [4 warps][16 columns]
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int mt = blockIdx.x, e = blockIdx.y;
+    const int row0 = a.offsets[e], nrows = a.offsets[e + 1] - row0;
+    if (nrows <= 0) return;
+    const int nsfb = (a.BN + 127) / 128;
+    const int ntile = (nrows + a.BN - 1) / a.BN;
+
+    // The unpacked E2M1 copies write 8 of every 16 bytes of an A tile; keep the
+    // other 8 (which the MMA format pads with) zero for the whole kernel.
+    for (int i = threadIdx.x; i < kStages * kTileM * kTileK / 16; i += kGemmThreads)
+        reinterpret_cast<uint4 *>(sA)[i] = make_uint4(0u, 0u, 0u, 0u);
+    fence_proxy_async_smem();
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; s++) {
+            mbar_init(&full[s], 2);   // producer's expect-tx arrival + scale-factor warp
+            mbar_init(&empty[s], 1);  // MMA commit
+        }
+        mbar_init(done, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 2) tmem_alloc(tmem_slot, a.tmem_cols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t sf_col0 = (uint32_t)a.BN;  // scale factors after the accumulator columns
+
+    int it_issued = 0;   // producer: stages issued
+    for (int nt = 0; nt < ntile; nt++) {
+        const int n0 = nt * a.BN;
+        const int nn = min(a.BN, nrows - n0);      // valid columns
+        const int nmma = (nn + 15) / 16 * 16;      // MMA N
+        if (warp == 0) {
+            if (lane == 0) {
+                for (int kt = 0; kt < a.nkt; kt++) {
+                    const int it = nt * a.nkt + kt, s = it % kStages;
+                    const uint32_t ph = (uint32_t)(it / kStages) & 1u;
+                    if (*(volatile int *)abort_flag || !mbar_wait(&empty[s], ph ^ 1u, a.st, 0x500u + s)) {
+                        *abort_flag = 1;
+                        break;
+                    }
+                    const int nbox = (nmma + kBoxN - 1) / kBoxN;
+                    // A arrives unpacked (16 E2M1 values in each 16 bytes, 8 of them data) and
+                    // counts its packed bytes; B counts one byte per element
+                    mbar_arrive_expect_tx(&full[s], (uint32_t)(kTileM * kTileK / 2 + nbox * kBoxN * kTileK));
+                    tma_load_3d(sA + (size_t)s * kTileM * kTileK, &tmA, kt * kTileK, mt * kTileM, e, &full[s]);
+                    for (int j = 0; j < nbox; j++)
+                        tma_load_2d(sB + (size_t)s * a.BN * kTileK + (size_t)j * kBoxN * kTileK, &tmB, kt * kTileK,
+                                    row0 + n0 + j * kBoxN, &full[s]);
+                    it_issued = it + 1;
+                }
+            }
+            __syncwarp();  // the epilogue's tensor-memory loads need the whole warp
+        } else if (warp == 1) {
+            for (int kt = 0; kt < a.nkt; kt++) {
+                const int it = nt * a.nkt + kt, s = it % kStages;
+                const uint32_t ph = (uint32_t)(it / kStages) & 1u;
+                int okl = 0;
+                if (lane == 0) okl = !*(volatile int *)abort_flag && mbar_wait(&empty[s], ph ^ 1u, a.st, 0x600u + s);
+                const bool ok = __shfl_sync(0xffffffffu, okl, 0) != 0;  // warp-uniform
+                if (!ok && lane == 0) *abort_flag = 1;
+                if (ok) {
+                    // A: rows mt*128 + lane + 32 q, scale blocks 4kt .. 4kt+3
+                    const uint8_t *sa = a.pool + (uint64_t)e * a.rec + a.a_scale_off;
+                    uint32_t wa[4];
+#pragma unroll
+                    for (int q = 0; q < 4; q++) {
+                        const uint64_t r = (uint64_t)(mt * kTileM + lane + 32 * q);
+                        wa[q] = (4 * kt + 3 < a.nkb_a) ? *reinterpret_cast<const uint32_t *>(sa + r * a.lds_a + 4 * kt)
+                                                       : 0u;
+                    }
+                    *reinterpret_cast<uint4 *>(sSFA + (size_t)s * 512 + lane * 16) = make_uint4(wa[0], wa[1], wa[2], wa[3]);
+                    // B: columns n0 + lane + 32 q of this tile
+                    for (int at = 0; at < nsfb; at++) {
+                        uint32_t wb[4];
+#pragma unroll
+                        for (int q = 0; q < 4; q++) {
+                            const int c = at * 128 + lane + 32 * q;
+                            uint32_t w = 0u;
+                            if (c < nn) {
+                                const uint8_t *rowp = a.bscale + (uint64_t)(row0 + n0 + c) * a.lds_b;
+#pragma unroll
+                                for (int t = 0; t < 4; t++) {
+                                    const int kb = 4 * kt + t;
+                                    if (kb < a.nkb_b) w |= (uint32_t)rowp[kb] << (8 * t);
+                                }
+                            }
+                            wb[q] = w;
+                        }
+                        *reinterpret_cast<uint4 *>(sSFB + ((size_t)s * nsfb + at) * 512 + lane * 16) =
+                            make_uint4(wb[0], wb[1], wb[2], wb[3]);
+                    }
+                    fence_proxy_async_smem();
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&full[s]);
+                if (!ok) break;
+            }
+        } else if (warp == 2) {
+            if (lane == 0) {
+                bool ok = true;
+                for (int kt = 0; kt < a.nkt; kt++) {
+                    const int it = nt * a.nkt + kt, s = it % kStages;
+                    const uint32_t ph = (uint32_t)(it / kStages) & 1u;
+                    ok = !*(volatile int *)abort_flag && mbar_wait(&full[s], ph, a.st, 0x700u + s);
+                    if (!ok) {
+                        *abort_flag = 1;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sfa_t = tmem + sf_col0 + (uint32_t)s * (4u + 4u * nsfb);
+                    const uint32_t sfb_t = sfa_t + 4u;
+                    tc_cp_sf(sfa_t, smem_desc(smem_u32(sSFA + (size_t)s * 512), 128, 128, kSwizzleNone));
+                    for (int at = 0; at < nsfb; at++)
+                        tc_cp_sf(sfb_t + 4u * at,
+                                 smem_desc(smem_u32(sSFB + ((size_t)s * nsfb + at) * 512), 128, 128, kSwizzleNone));
+                    const uint32_t a_base = smem_u32(sA + (size_t)s * kTileM * kTileK);
+                    const uint32_t b_base = smem_u32(sB + (size_t)s * a.BN * kTileK);
+#pragma unroll
+                    for (int ks = 0; ks < kTileK / 32; ks++) {
+                        const uint64_t ad = smem_desc(a_base + 32 * ks, 16, 1024, kSwizzle128B);
+                        const uint64_t bd = smem_desc(b_base + 32 * ks, 16, 1024, kSwizzle128B);
+                        tc_mma(tmem, ad, bd, idesc_mxf8f6f4(nmma, ks), sfa_t, sfb_t, (kt > 0 || ks > 0) ? 1u : 0u);
+                    }
+                    tc_commit(&empty[s]);  // frees the stage when these MMAs have read it
+                }
+                tc_commit(done);           // accumulator complete (or as far as it got)
+            }
+            __syncwarp();
+        }
+
+        // ------------------------------------------------------------ epilogue
+        const bool okl = mbar_wait(done, (uint32_t)nt & 1u, a.st, 0x800u) && !*(volatile int *)abort_flag;
+        const bool ok = __all_sync(0xffffffffu, okl);  // warp-uniform for the .sync.aligned loads
+        tc_fence_after();
+        const uint32_t lane_base = tmem + ((uint32_t)(32 * warp) << 16);
+        for (int c0 = 0; c0 < nmma; c0 += 16) {
+            float v[16];
+#pragma unroll
+            for (int j = 0; j < 16; j++) v[j] = 0.f;
+            if (ok) tmem_ld16(lane_base + (uint32_t)c0, v);
+            if (a.mode == 1) {
+                // lanes 0-15: gate rows, 16-31: up rows of the same 16 intermediate indices
+                const int i = (4 * mt + warp) * 16 + (lane & 15);
+                float hv[16];
+                float am[16];
+#pragma unroll
+                for (int j = 0; j < 16; j++) {
+                    const float u = __shfl_down_sync(0xffffffffu, v[j], 16);
+                    const float g = v[j];
+                    hv[j] = (lane < 16) ? g / (1.f + expf(-g)) * u : 0.f;
+                    float m = fabsf(hv[j]);
+#pragma unroll
+                    for (int off = 8; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+                    am[j] = m;
+                }
+                if (lane == 0) {
+#pragma unroll
+                    for (int j = 0; j < 16; j++) amax_x[warp * 16 + j] = am[j];
+                }
+                named_barrier(2, kGemmThreads);
+#pragma unroll
+                for (int j = 0; j < 16; j++) {
+                    const int n = c0 + j;
+                    const float amax = fmaxf(amax_x[warp * 16 + j], amax_x[(warp ^ 1) * 16 + j]);
+                    int X = -127;
+                    if (amax > 0.f) {
+                        int ex;
+                        frexpf(amax, &ex);
+                        X = max(-127, min(127, ex - 1 - 8));
+                    }
+                    if (ok && n < nn && lane < 16) {
+                        const uint64_t r = (uint64_t)(row0 + n0 + n);
+                        unsigned short pair;
+                        asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;"
+                            : "=h"(pair)
+                            : "f"(0.f), "f"(ldexpf(hv[j], -X)));
+                        a.hq[r * a.I + i] = (uint8_t)(pair & 0xFF);
+                        if (lane == 0 && (warp & 1) == 0) a.hs[r * a.lds_hs + i / 32] = (uint8_t)(X + 127);
+                    }
+                }
+                named_barrier(2, kGemmThreads);
+            } else {
+                const int o = mt * kTileM + 32 * warp + lane;
+#pragma unroll
+                for (int j = 0; j < 16; j++) {
+                    const int n = c0 + j;
+                    if (ok && n < nn && o < a.H) {
+                        const uint64_t r = (uint64_t)(row0 + n0 + n);
+                        if (a.partial_dtype == MOE_PARTIAL_F32)
+                            reinterpret_cast<float *>(a.partial)[r * a.H + o] = v[j];
+                        else
+                            reinterpret_cast<__nv_bfloat16 *>(a.partial)[r * a.H + o] = __float2bfloat16_rn(v[j]);
+                    }
+                }
+            }
+        }
+        tc_fence_before();
+        __syncthreads();
+    }
+    // nothing may still be in flight when TMEM is released and the CTA exits
+    if (warp == 0 && lane == 0) {
+        for (int it = max(0, it_issued - kStages); it < it_issued; it++)
+            mbar_wait(&full[it % kStages], (uint32_t)(it / kStages) & 1u, a.st, 0x900u);
+    }
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 2) tmem_dealloc(tmem, a.tmem_cols);
+}
+
+// ------------------------------------------------------------- tensor maps
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+cudaError_t get_encoder() {
+    if (g_encode) return cudaSuccess;
+    void *fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || fn == nullptr) return cudaErrorNotSupported;
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    return cudaSuccess;
+}
+
+// A: packed E2M1 weights of all experts, [E][rows][K] with the given strides,
+// unpacked by the copy to 16 elements per 16 bytes (the f8f6f4 operand format).
+cudaError_t make_map_a(CUtensorMap *m, const void *base, int K, int rows, int E, uint64_t row_stride,
+                       uint64_t rec) {
+    cuuint64_t dims[3] = {(cuuint64_t)K, (cuuint64_t)rows, (cuuint64_t)E};
+    cuuint64_t strides[2] = {row_stride, rec};
+    cuuint32_t box[3] = {kTileK, kTileM, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 3, const_cast<void *>(base), dims, strides, box, es,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+// B: E4M3 rows [P][K] (one byte per element), boxes of 16 rows.
+cudaError_t make_map_b(CUtensorMap *m, const void *base, int K, int P) {
+    cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)P};
+    cuuint64_t strides[1] = {(cuuint64_t)K};
+    cuuint32_t box[2] = {kTileK, kBoxN};
+    cuuint32_t es[2] = {1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, es,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+uint32_t pow2_at_least(uint32_t v) {
+    uint32_t p = 32;
+    while (p < v) p <<= 1;
+    return p;
+}
+
+int g_gemm_smem = 0;
+
+}  // namespace
 
 cudaError_t launch_grouped_gemms(const PoolView &v, int T, int k, const int32_t *offsets, const GroupedWs &g,
                                  void *partial, int partial_dtype, StatusWord *st, cudaStream_t stream) {
-    (void)v; (void)T; (void)k; (void)offsets; (void)g; (void)partial; (void)partial_dtype; (void)st; (void)stream;
-    return cudaErrorNotSupported;
+    const int P = T * k;
+    if (P == 0) return cudaSuccess;
+    cudaError_t e = get_encoder();
+    if (e != cudaSuccess) return e;
+    // accumulator columns per tile: about twice the mean rows per expert, 32..256
+    const int mean = (P + v.E - 1) / v.E;
+    int BN = (2 * mean + 16 + 31) / 32 * 32;
+    BN = BN < 32 ? 32 : (BN > kMaxBN ? kMaxBN : BN);
+    const int nsfb = (BN + 127) / 128;
+    const uint32_t tmem_cols = pow2_at_least((uint32_t)(BN + kStages * (4 + 4 * nsfb)));
+    if (tmem_cols > 512) return cudaErrorNotSupported;
+    const GemmSmemLayout L(BN);
+    const size_t smem = L.total + 1024;  // alignment slack
+    e = ensure_dynamic_smem(grouped_gemm_kernel, smem, g_gemm_smem);
+    if (e != cudaSuccess) return e;
+
+    GemmArgs ga;
+    ga.E = v.E;
+    ga.pool = v.base;
+    ga.rec = v.rec;
+    ga.offsets = offsets;
+    ga.BN = BN;
+    ga.tmem_cols = tmem_cols;
+    ga.I = v.I;
+    ga.H = v.H;
+    ga.hq = g.hq;
+    ga.hs = g.hs;
+    ga.lds_hs = v.Ip / 32;
+    ga.partial = partial;
+    ga.partial_dtype = partial_dtype;
+    ga.st = st;
+
+    // GEMM 1: gate/up
+    CUtensorMap mA, mB;
+    if ((e = make_map_a(&mA, v.base, v.H, 2 * v.I, v.E, (uint64_t)v.ld_gu, v.rec)) != cudaSuccess) return e;
+    if ((e = make_map_b(&mB, g.xq, v.H, P)) != cudaSuccess) return e;
+    ga.mode = 1;
+    ga.Kel = v.H;
+    ga.nkt = v.H / kTileK;
+    ga.nkb_a = v.H / 32;
+    ga.nkb_b = v.H / 32;
+    ga.lds_a = v.lds_gu;
+    ga.lds_b = v.H / 32;
+    ga.a_scale_off = v.off_sgu;
+    ga.bscale = g.xs;
+    {
+        TraceScope trace_scope("gemm_gateup", stream);
+        grouped_gemm_kernel<<<dim3(2 * v.I / kTileM, v.E), kGemmThreads, smem, stream>>>(mA, mB, ga);
+    }
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+
+    // GEMM 2: down
+    if ((e = make_map_a(&mA, v.base + v.off_d, v.Ip, v.H, v.E, (uint64_t)v.ld_d, v.rec)) != cudaSuccess) return e;
+    if ((e = make_map_b(&mB, g.hq, v.I, P)) != cudaSuccess) return e;
+    ga.mode = 2;
+    ga.Kel = v.I;
+    ga.nkt = v.Ip / kTileK;
+    ga.nkb_a = v.Ip / 32;
+    ga.nkb_b = v.I / 32;
+    ga.lds_a = v.lds_d;
+    ga.lds_b = v.Ip / 32;
+    ga.a_scale_off = v.off_sd;
+    ga.bscale = g.hs;
+    {
+        TraceScope trace_scope("gemm_down", stream);
+        grouped_gemm_kernel<<<dim3(v.H / kTileM, v.E), kGemmThreads, smem, stream>>>(mA, mB, ga);
+    }
+    return cudaGetLastError();
 }
 
 }  // namespace moe

@@ -15,7 +15,7 @@ struct GroupedWs {
     uint8_t *xq;      // [P][H]    E4M3 rows of x in sorted order
     uint8_t *xs;      // [P][H/32] their E8M0 scales
     uint8_t *hq;      // [P][I]    E4M3 rows of h in sorted order
-    uint8_t *hs;      // [P][I/32]
+    uint8_t *hs;      // [P][Ip/32], Ip = I rounded up to 128 (tail bytes unused)
     size_t end;       // total bytes
 };
 
@@ -31,7 +31,7 @@ __host__ __device__ inline GroupedWs grouped_ws_layout(void *ws, int E, int H, i
     g.xq = (uint8_t *)(base + o);      o += align_up(P * H, 1024);
     g.xs = (uint8_t *)(base + o);      o += align_up(P * (H / 32), 1024);
     g.hq = (uint8_t *)(base + o);      o += align_up(P * I, 1024);
-    g.hs = (uint8_t *)(base + o);      o += align_up(P * (I / 32), 1024);
+    g.hs = (uint8_t *)(base + o);      o += align_up(P * (((size_t)I + 127) / 128 * 4), 1024);
     g.end = o;
     return g;
 }

@@ -86,21 +86,34 @@ __device__ void logits_block(const uint16_t *__restrict__ x, int M, int H, const
     for (int t = 0; t < kLogitTokens; t++) acc[t] = accs[t] = 0.f;
     if (e < E) {
         const uint16_t *wrow = Wr + (size_t)e * H;
-        for (int h = h0 + lane * 8; h < h1; h += 256) {
-            float wf[8];
-            unpack_bf16x8(__ldg(reinterpret_cast<const uint4 *>(wrow + h)), wf);
+        // batches of 8 chunks: all loads of a batch issued before any arithmetic;
+        // chunks are still summed in increasing h (the order the bound assumes)
+        for (int hb = h0 + lane * 8; hb < h1; hb += 256 * 8) {
+            uint4 wv[8];
 #pragma unroll
-            for (int t = 0; t < kLogitTokens; t++) {
-                if (t < nt) {
-                    float xf[8], p[8];
-                    unpack_bf16x8(*reinterpret_cast<const uint4 *>(xs + (size_t)t * H + h), xf);
+            for (int c = 0; c < 8; c++) {
+                const int h = hb + 256 * c;
+                wv[c] = h < h1 ? __ldg(reinterpret_cast<const uint4 *>(wrow + h)) : make_uint4(0u, 0u, 0u, 0u);
+            }
 #pragma unroll
-                    for (int i = 0; i < 8; i++) p[i] = xf[i] * wf[i];  // exact
-                    const float s = ((p[0] + p[1]) + (p[2] + p[3])) + ((p[4] + p[5]) + (p[6] + p[7]));
-                    const float a = ((fabsf(p[0]) + fabsf(p[1])) + (fabsf(p[2]) + fabsf(p[3]))) +
-                                    ((fabsf(p[4]) + fabsf(p[5])) + (fabsf(p[6]) + fabsf(p[7])));
-                    acc[t] += s;
-                    accs[t] += a;
+            for (int c = 0; c < 8; c++) {
+                const int h = hb + 256 * c;
+                if (h >= h1) break;
+                float wf[8];
+                unpack_bf16x8(wv[c], wf);
+#pragma unroll
+                for (int t = 0; t < kLogitTokens; t++) {
+                    if (t < nt) {
+                        float xf[8], p[8];
+                        unpack_bf16x8(*reinterpret_cast<const uint4 *>(xs + (size_t)t * H + h), xf);
+#pragma unroll
+                        for (int i = 0; i < 8; i++) p[i] = xf[i] * wf[i];  // exact
+                        const float s = ((p[0] + p[1]) + (p[2] + p[3])) + ((p[4] + p[5]) + (p[6] + p[7]));
+                        const float a = ((fabsf(p[0]) + fabsf(p[1])) + (fabsf(p[2]) + fabsf(p[3]))) +
+                                        ((fabsf(p[4]) + fabsf(p[5])) + (fabsf(p[6]) + fabsf(p[7])));
+                        acc[t] += s;
+                        accs[t] += a;
+                    }
                 }
             }
         }

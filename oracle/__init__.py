@@ -83,6 +83,11 @@ def lib():
         L.orc_expert_forward.restype = None
         L.orc_expert_forward.argtypes = [_u8p, _u8p, ctypes.c_int, ctypes.c_int, _f64p, ctypes.c_int,
                                          _f64p, ctypes.c_void_p, ctypes.c_int]
+        L.orc_mxfp8_ambiguity.restype = None
+        L.orc_mxfp8_ambiguity.argtypes = [_f64p, _f64p, ctypes.c_int, _f64p]
+        L.orc_expert_ambiguity.restype = None
+        L.orc_expert_ambiguity.argtypes = [_u8p, _u8p, ctypes.c_int, ctypes.c_int, _f64p, ctypes.c_int,
+                                           ctypes.c_double, _f64p]
         L.orc_prescale_exponent.restype = ctypes.c_int
         L.orc_prescale_exponent.argtypes = [_u16p, ctypes.c_int]
         L.orc_prescale.restype = None
@@ -182,6 +187,21 @@ def expert_forward(codes: np.ndarray, scales: np.ndarray, H: int, I: int, x: np.
     return y, h
 
 
+# Error model of the fp32 h of the tensor-core path, relative to the sums of
+# |products| of its dot products (a few fp32 ulps per term, with a wide margin).
+MXFP8_AMBIGUITY_EPS = 2.0 ** -16
+
+
+def mxfp8_ambiguity(v: np.ndarray, radius) -> np.ndarray:
+    """delta[i]: change an alternative MXFP8 rounding may make when v[i] is known
+    only to within radius[i] (absolute)."""
+    v = np.ascontiguousarray(v, dtype=np.float64)
+    r = np.ascontiguousarray(np.broadcast_to(radius, v.shape), dtype=np.float64)
+    d = np.empty_like(v)
+    lib().orc_mxfp8_ambiguity(v, r, v.size, d)
+    return d
+
+
 def prescale(x_bits: np.ndarray) -> np.ndarray:
     """Row-wise exact power-of-two pre-scale (bf16 bits in, bf16 bits out)."""
     x = np.ascontiguousarray(np.atleast_2d(x_bits), dtype=np.uint16)
@@ -214,6 +234,19 @@ class SyntheticPool:
         if len(self._cache) > self._cap:
             self._cache.popitem(last=False)
         return v
+
+
+def pair_outputs(experts, H: int, I: int, x: np.ndarray, idx: np.ndarray, h_mode: int = 0) -> np.ndarray:
+    """Unweighted expert outputs o[m, j] = expert_{idx[m,j]}(x[m]) (fp64 [M, k, H])."""
+    M, k = idx.shape
+    o = np.zeros((M, k, H), dtype=np.float64)
+    for e in sorted(set(int(v) for v in idx.ravel())):
+        rows = [(m, j) for m in range(M) for j in range(k) if idx[m, j] == e]
+        codes, scales = experts(e)
+        ye, _ = expert_forward(codes, scales, H, I, np.stack([x[m] for m, _ in rows]), h_mode)
+        for r, (m, j) in enumerate(rows):
+            o[m, j] = ye[r]
+    return o
 
 
 def combine_rows(experts, H: int, I: int, x: np.ndarray, idx: np.ndarray, w: np.ndarray,
@@ -265,6 +298,32 @@ def sort_pairs(idx: np.ndarray, E: int):
     return perm, inv, offsets
 
 
+def pair_ambiguity(experts, H: int, I: int, x: np.ndarray, idx: np.ndarray,
+                   eps: float = MXFP8_AMBIGUITY_EPS) -> np.ndarray:
+    """amb[m, j, o]: the largest change of expert_{idx[m,j]}(x[m])[o] that an
+    alternative (equally correct) MXFP8 rounding of its h could make."""
+    M, k = idx.shape
+    amb = np.zeros((M, k, H), dtype=np.float64)
+    for e in sorted(set(int(v) for v in idx.ravel())):
+        rows = [(m, j) for m in range(M) for j in range(k) if idx[m, j] == e]
+        codes, scales = experts(e)
+        xe = np.ascontiguousarray(np.stack([x[m] for m, _ in rows]), dtype=np.float64)
+        ya = np.empty((len(rows), H), dtype=np.float64)
+        lib().orc_expert_ambiguity(np.ascontiguousarray(codes), np.ascontiguousarray(scales), H, I, xe, len(rows),
+                                   eps, ya)
+        for r, (m, j) in enumerate(rows):
+            amb[m, j] = ya[r]
+    return amb
+
+
+def combine_ambiguity(experts, H: int, I: int, x: np.ndarray, idx: np.ndarray, w: np.ndarray,
+                      eps: float = MXFP8_AMBIGUITY_EPS) -> np.ndarray:
+    """Per output, sum_j |w_j| * pair_ambiguity: the part of the difference between
+    two correct MXFP8-h layer outputs that rounding choices can explain."""
+    amb = pair_ambiguity(experts, H, I, x, idx, eps)
+    return np.einsum("mj,mjh->mh", np.abs(w), amb)
+
+
 def quant_rows_mxfp8(x: np.ndarray) -> np.ndarray:
     """Rows of x (fp64) replaced by their MXFP8-dequantised values."""
     out = np.empty_like(x, dtype=np.float64)
@@ -287,8 +346,9 @@ def prefill_layer(experts, x_bits: np.ndarray, Wr_bits: np.ndarray, k: int, act_
     if act_mode == 1:
         xs = quant_rows_mxfp8(xs)
     y = combine_rows(experts, H, experts.I, xs, idx[toks], w[toks], h_mode=act_mode)
+    amb = combine_ambiguity(experts, H, experts.I, xs, idx[toks], w[toks]) if act_mode == 1 else np.zeros_like(y)
     return {"idx": idx, "w": w, "perm": perm, "inv_perm": inv, "offsets": offsets,
-            "tokens": toks, "y": y}
+            "tokens": toks, "y": y, "y_amb": amb}
 
 
 def stacked_step(pools, routers, skews, x_bits: np.ndarray, k: int):

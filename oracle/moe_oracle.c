@@ -351,6 +351,112 @@ void orc_expert_forward(const uint8_t *codes, const uint8_t *scales, int H, int 
     free(qs);
 }
 
+/* ------------------------------------------------- MXFP8 rounding ambiguity
+ * Test support for the tensor-core prefill path, whose h is computed in fp32:
+ * h_i carries an error of up to radius[i] there, so a value within radius[i] of an
+ * E4M3 rounding midpoint may legitimately round to either neighbour, and a block
+ * whose max |h| lies within its radius of a power of two may take either shared
+ * exponent.  delta[i] = the largest change of the dequantised value such an
+ * alternative choice makes (0 when the choice is clear).  The quantised values
+ * themselves are those of orc_quant_mxfp8. */
+void orc_mxfp8_ambiguity(const double *v, const double *radius, int n, double *delta) {
+    for (int b0 = 0; b0 < n; b0 += 32) {
+        int b1 = b0 + 32 < n ? b0 + 32 : n;
+        double amax = 0.0, rmax = 0.0;
+        for (int i = b0; i < b1; i++) {
+            if (fabs(v[i]) > amax) amax = fabs(v[i]);
+            if (radius[i] > rmax) rmax = radius[i];
+        }
+        int X = -127, Xalt = 1000;
+        if (amax > 0.0) {
+            int ex;
+            frexp(amax, &ex);
+            X = (ex - 1) - 8;
+            if (X < -127) X = -127;
+            if (X > 127) X = 127;
+            if (amax + rmax >= ldexp(1.0, X + 9) && X < 127) Xalt = X + 1;
+            else if (amax - rmax < ldexp(1.0, X + 8) && X > -127) Xalt = X - 1;
+        }
+        for (int i = b0; i < b1; i++) {
+            double t = ldexp(v[i], -X), a = fabs(t), rt = ldexp(radius[i], -X);
+            double q = ldexp(orc_e4m3_value(orc_e4m3_encode(t)), X);
+            double d = 0.0;
+            if (a < 448.0) {
+                double lo = 0.0, hi = 448.0;           /* neighbours of a among E4M3 values */
+                for (unsigned c = 0; c < 0x7F; c++) {
+                    double vc = orc_e4m3_value(c);
+                    if (vc <= a && vc > lo) lo = vc;
+                    if (vc >= a && vc < hi) hi = vc;
+                }
+                if (fabs(a - 0.5 * (lo + hi)) <= rt) d = ldexp(hi - lo, X);
+            }
+            if (Xalt != 1000) {
+                double q2 = ldexp(orc_e4m3_value(orc_e4m3_encode(ldexp(v[i], -Xalt))), Xalt);
+                if (fabs(q2 - q) > d) d = fabs(q2 - q);
+            }
+            delta[i] = d;
+        }
+    }
+}
+
+/* |dot| of an MXFP4 row with v: sum_j |w_j v_j| (the scale of fp32 rounding error). */
+static double mx_row_absdot(const uint8_t *codes, const uint8_t *scales, size_t row, int K, const double *v) {
+    const uint8_t *c = codes + row * (size_t)(K / 2);
+    const uint8_t *s = scales + row * (size_t)(K / 32);
+    double acc = 0.0;
+    for (int b = 0; b < K / 32; b++) {
+        double sc = orc_e8m0_value(s[b]), part = 0.0;
+        for (int j = 32 * b; j < 32 * b + 32; j++) {
+            unsigned code = (j & 1) ? (c[j / 2] >> 4) : (c[j / 2] & 15);
+            part += fabs(orc_e2m1_value(code) * v[j]);
+        }
+        acc += sc * part;
+    }
+    return acc;
+}
+
+/* Per output row o of one expert applied to the rows x [n][H] with MXFP8 h:
+ * yamb[o] = sum_i |W_d[o][i]| * delta_i (orc_mxfp8_ambiguity).  The error radius
+ * of h_i = silu(g) u is modelled as rel * (S_g |u| + |g| S_u) + rel * |h|, with
+ * S = the sum of |products| of each dot product (fp32 accumulation with some
+ * ulps per term; rel = 2^-16 leaves a wide margin). */
+void orc_expert_ambiguity(const uint8_t *codes, const uint8_t *scales, int H, int I,
+                          const double *x, int n, double rel, double *yamb) {
+    const uint8_t *cg = codes, *cu = codes + (size_t)I * H / 2, *cd = codes + (size_t)I * H;
+    const uint8_t *sg = scales, *su = scales + (size_t)I * H / 32, *sd = scales + (size_t)I * H / 16;
+    double *hv = (double *)malloc(sizeof(double) * (size_t)I);
+    double *rd = (double *)malloc(sizeof(double) * (size_t)I);
+    double *dl = (double *)malloc(sizeof(double) * (size_t)I);
+    for (int r = 0; r < n; r++) {
+        const double *xr = x + (size_t)r * H;
+        #pragma omp parallel for schedule(static)
+        for (int i = 0; i < I; i++) {
+            double g = mx_row_dot(cg, sg, (size_t)i, H, xr);
+            double u = mx_row_dot(cu, su, (size_t)i, H, xr);
+            double Sg = mx_row_absdot(cg, sg, (size_t)i, H, xr);
+            double Su = mx_row_absdot(cu, su, (size_t)i, H, xr);
+            hv[i] = silu(g) * u;
+            rd[i] = rel * (Sg * fabs(u) + fabs(g) * Su) + rel * fabs(hv[i]);
+        }
+        orc_mxfp8_ambiguity(hv, rd, I, dl);
+        #pragma omp parallel for schedule(static)
+        for (int o = 0; o < H; o++) {
+            const uint8_t *c = cd + (size_t)o * (I / 2);
+            const uint8_t *sc = sd + (size_t)o * (I / 32);
+            double acc = 0.0;
+            for (int i = 0; i < I; i++) {
+                if (dl[i] == 0.0) continue;
+                unsigned code = (i & 1) ? (c[i / 2] >> 4) : (c[i / 2] & 15);
+                acc += fabs(orc_e2m1_value(code)) * orc_e8m0_value(sc[i / 32]) * dl[i];
+            }
+            yamb[(size_t)r * H + o] = acc;
+        }
+    }
+    free(hv);
+    free(rd);
+    free(dl);
+}
+
 /* ------------------------------------------------------------- stacked-layer glue
  * Pre-scale of the MoE input (exact): x_hat = x * 2^-p with p = floor(log2(amax|x|)) - 2,
  * so amax|x_hat| lies in [4, 8).  amax == 0 gives p = 0.  Result rounded to bf16

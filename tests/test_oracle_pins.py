@@ -372,3 +372,19 @@ def test_expert_record_size_matches_the_pages():
     assert abs(mib - facts["expert_record_mib"]) / facts["expert_record_mib"] < 0.005
     per_token = facts["experts_selected_per_layer"] * facts["moe_layers"] * mib / 1000
     assert abs(per_token - facts["expert_data_per_token_gb"]) / facts["expert_data_per_token_gb"] < 0.01
+
+
+def test_mxfp8_ambiguity_marks_only_near_decisions():
+    v = np.zeros(64)
+    v[0] = 300.0                      # block amax well inside [256, 512): X = 0 (clear)
+    v[1] = 1.0625                     # exact midpoint of 1.0 and 1.125 -> ambiguous
+    v[2] = 1.0625 * (1 + 1e-6)        # within eps of it -> ambiguous
+    v[3] = 1.03                       # far from a midpoint -> clear
+    v[32] = 511.99                    # block max just below 2^9 -> the exponent may go up
+    v[33] = 3.0
+    d = oracle.mxfp8_ambiguity(v, 1e-4 * np.abs(v))
+    assert d[0] == 0.0 and d[3] == 0.0
+    assert d[1] == 0.125 and d[2] == 0.125
+    assert d[32] > 0.0                # scale alternative 2^1 changes 511.99 -> 512 vs 448
+    q = oracle.quant_mxfp8(v)[2]
+    assert q[3] == 1.0 and q[1] == 1.0  # midpoint rounds to even (1.0)
