@@ -131,6 +131,50 @@ def run_reference(args):
 # ---------------------------------------------------------------------- ours
 
 
+def measure_prefill(moe, torch, pool, Wr, dev, T, iters=3):
+    """Expert-major prefill of T tokens on the full-size layer: route, sort,
+    MXFP8 gather, grouped gate/up and down GEMMs, combine.  Returns timings."""
+    s = synth.FULL
+    xb = synth.tokens_bf16(synth.TOKENS_SEED["prefill"], 0, T, s.H)
+    x = torch.from_numpy(xb.view(np.int16)).to(dev).view(torch.bfloat16)
+    ws_r = moe.workspace(moe.moe_workspace_size(moe.MOE_OP_ROUTE, s.E, s.H, s.I, T, s.k), dev)
+    ws_g = moe.workspace(moe.moe_workspace_size(moe.MOE_OP_GROUPED, s.E, s.H, s.I, T, s.k), dev)
+    idx = torch.empty((T, s.k), dtype=torch.int32, device=dev)
+    w = torch.empty((T, s.k), dtype=torch.float32, device=dev)
+    out = {"perm": torch.empty(T * s.k, dtype=torch.int32, device=dev),
+           "inv_perm": torch.empty(T * s.k, dtype=torch.int32, device=dev),
+           "offsets": torch.empty(s.E + 1, dtype=torch.int32, device=dev),
+           "partial": torch.empty((T * s.k, s.H), dtype=torch.float32, device=dev)}
+    y = torch.empty((T, s.H), dtype=torch.bfloat16, device=dev)
+
+    def once():
+        moe.moe_route_topk(x, Wr, s.k, ws=ws_r, idx=idx, w=w)
+        moe.moe_expert_forward_grouped(pool, x, idx, ws=ws_g, out=out)
+        moe.moe_combine(out["partial"], out["inv_perm"], w, y=y)
+
+    once()
+    torch.cuda.synchronize()
+    assert moe.moe_check_status(ws_g) == 0 and moe.moe_check_status(ws_r) == 0
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(iters):
+        once()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / iters
+    kern = {}
+    for name in ("route_logits", "route_select", "gemm_gateup", "gemm_down", "combine", "gather_quant"):
+        moe.moe_trace_begin(name)
+        once()
+        n, tot = moe.moe_trace_end()
+        kern[name] = tot / max(n, 1)
+    wbytes = s.E * expert_bytes(s.H, s.I)
+    flops = 2.0 * 3 * s.H * s.I * T * s.k
+    return {"tok_s": T / (ms / 1000.0), "ms": ms, "kernel_ms": kern,
+            "gemm_weight_gbs": wbytes / ((kern["gemm_gateup"] + kern["gemm_down"]) / 1000.0) / 1e9,
+            "gemm_tflops": flops / ((kern["gemm_gateup"] + kern["gemm_down"]) / 1000.0) / 1e12}
+
+
 def run_ours(args):
     import torch
     import mxfp4_routed_expert_topk_gb300 as moe
@@ -249,6 +293,10 @@ def run_ours(args):
                "sample": f"{args.ref_tokens} tokens of the workload (exact route + 16 experts, fp64), "
                          "experts pre-generated outside the timing"}
     launches = 2 * NTOK * args.steps      # route_single + decode_fused per token
+    prefill = {}
+    if not args.no_prefill:
+        for T in synth.PREFILL_T:
+            prefill[str(T)] = measure_prefill(moe, torch, pool, Wr, dev, T)
     if rank == 0:
         print(json.dumps({
             "metric": METRIC, "value": value, "unit": "layer-tokens/s", "n_gpus": world, "steps": args.steps,
@@ -267,6 +315,7 @@ def run_ours(args):
             "e2e": {"value": NTOK / (e2e_ms / 1000.0) * world, "unit": "layer-tokens/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": launches,
+            "prefill": prefill,
             "clocks": clk.summary(),
         }))
     if dist is not None:
@@ -275,7 +324,8 @@ def run_ours(args):
 
 def run_profile_case(args):
     """A small case of the same kernels for ncu captures: full H and I, a 64-expert
-    pool (1.2 GB, larger than L2), a few single-token calls."""
+    pool (1.2 GB, larger than L2); a few single-token calls (decode) or one
+    64-token expert-major call (prefill)."""
     import torch
     import mxfp4_routed_expert_topk_gb300 as moe
     moe.build()
@@ -283,6 +333,16 @@ def run_profile_case(args):
     pool = moe.Pool(s.E, s.H, s.I)
     moe.moe_pool_fill_synthetic(pool, synth.pool_seed(0))
     Wr = torch.from_numpy(synth.router_bf16(synth.router_seed(0), s.E, s.H).view(np.int16)).cuda().view(torch.bfloat16)
+    if args.profile == "prefill":
+        xb = synth.tokens_bf16(synth.TOKENS_SEED["prefill"], 0, 64, s.H)
+        x = torch.from_numpy(xb.view(np.int16)).cuda().view(torch.bfloat16)
+        for _ in range(2):
+            idx, w = moe.moe_route_topk(x, Wr, s.k)
+            out = moe.moe_expert_forward_grouped(pool, x, idx)
+            moe.moe_combine(out["partial"], out["inv_perm"], w)
+        torch.cuda.synchronize()
+        print("profile case done")
+        return
     xb = synth.tokens_bf16(synth.TOKENS_SEED["full"], 0, 4, s.H)
     x = torch.from_numpy(xb.view(np.int16)).cuda().view(torch.bfloat16)
     for t in range(4):
@@ -300,7 +360,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--ref-tokens", type=int, default=16)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--profile", choices=["decode"], default=None,
+    ap.add_argument("--no-prefill", action="store_true", help="skip the expert-major prefill measurements")
+    ap.add_argument("--profile", choices=["decode", "prefill"], default=None,
                     help="run a small case of the kernels for an ncu capture (no JSON line)")
     args = ap.parse_args()
     if args.profile:
