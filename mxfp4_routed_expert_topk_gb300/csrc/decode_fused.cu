@@ -12,19 +12,22 @@
 // ring of shared-memory slots (evict-first in L2); W_d rows of phase B are fetched
 // while phase A finishes and while CTAs wait at the grid barrier.  Consumer warps
 // dequantise in registers: E2M1 pairs -> f16x2 (cvt), packed f16 FMAs over one
-// 32-element scale block against the token held in registers as f16 scaled by a
-// power of two, then the block sum is scaled by its E8M0 factor in fp32.
+// 32-element scale block against the token (f16 in shared memory, scaled by a
+// power of two; in phase B the warp's h in registers), then the block sum is
+// scaled by its E8M0 factor in fp32.  Phase A gives each (gate row, up row) item
+// to a pair of warps, phase B each selected expert to one warp.
 #include "moe_internal.cuh"
 #include "sm100_async.cuh"
 
 namespace moe {
 namespace {
 
-constexpr int kCW = 8;                        // consumer warps
+constexpr int kCW = 16;                       // consumer warps
+constexpr int kItems = 8;                     // phase-A items per stage (a warp pair each)
 constexpr int kThreadsF = (kCW + 1) * 32;     // + one producer warp
 constexpr int kSlots = 3;
 constexpr int kMaxJ = 7;                      // H <= 32 lanes * 32 elements * 7
-constexpr int kMaxKF = 16;                    // two pairs per consumer warp in phase B
+constexpr int kMaxKF = 16;                    // one pair per consumer warp in phase B
 constexpr int kMaxR = 4;                      // output rows per phase-B stage
 constexpr int kMaxRowsCta = 64;               // output rows per CTA
 
@@ -77,8 +80,11 @@ __global__ void __launch_bounds__(kThreadsF, 1) decode_fused_kernel(const FusedA
     uint8_t *slots = smem;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)kSlots * a.slot_bytes);
     uint64_t *empty = full + kSlots;
-    float *red = reinterpret_cast<float *>(empty + kSlots);     // [kCW][kMaxRowsCta]
-    int *sidx = reinterpret_cast<int *>(red + kCW * kMaxRowsCta);  // [kMaxKF]
+    // (slots are a multiple of 128 bytes; every region below starts 16-byte aligned)
+    float *red = reinterpret_cast<float *>(empty + kSlots);             // [kCW][kMaxRowsCta]
+    uint4 *xsm = reinterpret_cast<uint4 *>(red + kCW * kMaxRowsCta);    // the token, f16: [4][H/32] x 8
+    float2 *pairsum = reinterpret_cast<float2 *>(xsm + v.H / 8);        // [2][kItems][2] half sums
+    int *sidx = reinterpret_cast<int *>(pairsum + 2 * kItems * 2);      // [kMaxKF]
     int *abort_flag = sidx + kMaxKF;
     unsigned int *samax = reinterpret_cast<unsigned int *>(abort_flag + 1);  // [kMaxKF] max |h| per pair
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -86,7 +92,7 @@ __global__ void __launch_bounds__(kThreadsF, 1) decode_fused_kernel(const FusedA
     const int NA = k * v.I;
     const int n_lo = (int)((long long)b * NA / G), n_hi = (int)((long long)(b + 1) * NA / G);
     const int nitems = n_hi - n_lo;
-    const int nstageA = (nitems + kCW - 1) / kCW;
+    const int nstageA = (nitems + kItems - 1) / kItems;
     const int o_lo = (int)((long long)b * v.H / G), o_hi = (int)((long long)(b + 1) * v.H / G);
     const int rows = o_hi - o_lo;
     const int nstageB = (rows + a.R - 1) / a.R;
@@ -124,8 +130,8 @@ __global__ void __launch_bounds__(kThreadsF, 1) decode_fused_kernel(const FusedA
                 if (*(volatile int *)abort_flag) break;
                 uint8_t *dst = slots + (size_t)slot * a.slot_bytes;
                 if (s < nstageA) {
-                    const int n0 = n_lo + kCW * s;
-                    const int cnt = min(kCW, n_hi - n0);
+                    const int n0 = n_lo + kItems * s;
+                    const int cnt = min(kItems, n_hi - n0);
                     mbar_arrive_expect_tx(&full[slot], (uint32_t)(cnt * 2 * (ldg + lsg)));
                     // runs of consecutive items within one expert and one group of 16
                     // rows are contiguous in the pool: 4 copies per run
@@ -138,13 +144,13 @@ __global__ void __launch_bounds__(kThreadsF, 1) decode_fused_kernel(const FusedA
                         const int rg = 32 * (i / kGroupRows) + (i % kGroupRows);
                         bulk_g2s(dst + (size_t)j * ldg, rec + (uint64_t)rg * ldg, (uint32_t)(len * ldg), &full[slot],
                                  pol);
-                        bulk_g2s(dst + (size_t)(kCW + j) * ldg, rec + (uint64_t)(rg + kGroupRows) * ldg,
+                        bulk_g2s(dst + (size_t)(kItems + j) * ldg, rec + (uint64_t)(rg + kGroupRows) * ldg,
                                  (uint32_t)(len * ldg), &full[slot], pol);
                         const uint8_t *sr = rec + v.off_sgu;
-                        uint8_t *ds = dst + (size_t)2 * kCW * ldg;
+                        uint8_t *ds = dst + (size_t)2 * kItems * ldg;
                         bulk_g2s(ds + (size_t)j * lsg, sr + (uint64_t)rg * lsg, (uint32_t)(len * lsg), &full[slot],
                                  pol);
-                        bulk_g2s(ds + (size_t)(kCW + j) * lsg, sr + (uint64_t)(rg + kGroupRows) * lsg,
+                        bulk_g2s(ds + (size_t)(kItems + j) * lsg, sr + (uint64_t)(rg + kGroupRows) * lsg,
                                  (uint32_t)(len * lsg), &full[slot], pol);
                         j += len;
                     }
@@ -191,40 +197,34 @@ __global__ void __launch_bounds__(kThreadsF, 1) decode_fused_kernel(const FusedA
     for (int ww = 0; ww < kCW; ww++) amax_x = fmaxf(amax_x, red[ww]);
     named_barrier(1, kCW * 32);  // red[] is reused in phase B
     // the token as f16 scaled by 2^-sx, max|x 2^-sx| in [128, 256) (exact for bf16),
-    // kept in registers: lane holds blocks lane + 32 j of 32 elements
+    // staged in shared memory for all consumer warps
     int sx = 0;
     if (amax_x > 0.f) {
         int ex;
         frexpf(amax_x, &ex);
         sx = ex - 1 - 7;
     }
-    uint4 xr[kMaxJ][4];
+    for (int c = threadIdx.x; c < v.H / 8; c += kCW * 32) {
+        const uint4 raw = __ldg(reinterpret_cast<const uint4 *>(a.x) + c);
+        const unsigned int u[4] = {raw.x, raw.y, raw.z, raw.w};
+        unsigned int hw[4];
 #pragma unroll
-    for (int j = 0; j < kMaxJ; j++) {
-        const int kb = lane + 32 * j;
-        const uint4 *xp = reinterpret_cast<const uint4 *>(a.x + (size_t)kb * 32);
-#pragma unroll
-        for (int q = 0; q < 4; q++) {
-            unsigned int hw[4] = {0u, 0u, 0u, 0u};
-            if (kb < nkb) {
-                const uint4 raw = __ldg(xp + q);
-                const unsigned int u[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-                for (int t = 0; t < 4; t++)
-                    hw[t] = pack_half2(ldexpf(__uint_as_float(u[t] << 16), -sx),
-                                       ldexpf(__uint_as_float(u[t] & 0xffff0000u), -sx));
-            }
-            xr[j][q] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-        }
+        for (int t = 0; t < 4; t++)
+            hw[t] = pack_half2(ldexpf(__uint_as_float(u[t] << 16), -sx), ldexpf(__uint_as_float(u[t] & 0xffff0000u), -sx));
+        // eighth q of 32-block kb at [q][kb]: a warp's lanes read consecutive 16 bytes
+        xsm[(c & 3) * nkb + (c >> 2)] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
     }
+    named_barrier(1, kCW * 32);
 
     bool ok = true;
     int s = 0;
-    // ---- phase A: one (gate row, up row) pair per warp per stage
+    // ---- phase A: item j of a stage (gate row + up row) is shared by warps 2j and
+    // 2j+1, which take the even and the odd 32-block columns of the lane's blocks
+    const int item = warp >> 1, half = warp & 1;
     for (; s < nstageA; s++) {
         const int slot = s % kSlots;
         const uint32_t ph = (uint32_t)(s / kSlots) & 1u;
-        const int n = n_lo + kCW * s + warp;
+        const int n = n_lo + kItems * s + item;
         int p = 0, i = 0;
         bool valid = false;
         if (n < n_hi) {
@@ -237,35 +237,41 @@ __global__ void __launch_bounds__(kThreadsF, 1) decode_fused_kernel(const FusedA
         float ag = 0.f, au = 0.f;
         if (ok && valid) {
             const uint8_t *base = slots + (size_t)slot * a.slot_bytes;
-            const uint8_t *cg = base + (size_t)warp * ldg;
-            const uint8_t *cu = base + (size_t)(kCW + warp) * ldg;
-            const uint8_t *sgp = base + (size_t)2 * kCW * ldg + (size_t)warp * lsg;
-            const uint8_t *sup = base + (size_t)2 * kCW * ldg + (size_t)(kCW + warp) * lsg;
+            const uint8_t *cg = base + (size_t)item * ldg;
+            const uint8_t *cu = base + (size_t)(kItems + item) * ldg;
+            const uint8_t *sgp = base + (size_t)2 * kItems * ldg + (size_t)item * lsg;
+            const uint8_t *sup = base + (size_t)2 * kItems * ldg + (size_t)(kItems + item) * lsg;
 #pragma unroll
-            for (int j = 0; j < kMaxJ; j++) {
+            for (int jj = 0; jj < (kMaxJ + 1) / 2; jj++) {
+                const int j = 2 * jj + half;
                 const int kb = lane + 32 * j;
-                if (kb < nkb) {
+                if (j < kMaxJ && kb < nkb) {
+                    uint4 xb[4];
+#pragma unroll
+                    for (int q = 0; q < 4; q++) xb[q] = xsm[q * nkb + kb];
                     const uint4 qg = *reinterpret_cast<const uint4 *>(cg + kb * 16);
                     const uint4 qu = *reinterpret_cast<const uint4 *>(cu + kb * 16);
-                    ag = fmaf(block_dot1(qg, xr[j]), e8m0_fast(sgp[kb]), ag);
-                    au = fmaf(block_dot1(qu, xr[j]), e8m0_fast(sup[kb]), au);
+                    ag = fmaf(block_dot1(qg, xb), e8m0_fast(sgp[kb]), ag);
+                    au = fmaf(block_dot1(qu, xb), e8m0_fast(sup[kb]), au);
                 }
             }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[slot]);
-        if (ok && valid) {
 #pragma unroll
-            for (int off = 16; off > 0; off >>= 1) {
-                ag += __shfl_xor_sync(0xffffffffu, ag, off);
-                au += __shfl_xor_sync(0xffffffffu, au, off);
-            }
-            if (lane == 0) {
-                const float gv = ldexpf(ag, sx), uv = ldexpf(au, sx);
-                const float hval = gv / (1.f + expf(-gv)) * uv;
-                a.h[(size_t)p * v.I + i] = hval;
-                atomicMax(&samax[p], __float_as_uint(fabsf(hval)));
-            }
+        for (int off = 16; off > 0; off >>= 1) {
+            ag += __shfl_xor_sync(0xffffffffu, ag, off);
+            au += __shfl_xor_sync(0xffffffffu, au, off);
+        }
+        float2 *ps = pairsum + (size_t)(s & 1) * kItems * 2;
+        if (lane == 0) ps[item * 2 + half] = make_float2(ag, au);
+        named_barrier(2 + item, 64);  // the two warps of this item
+        if (ok && valid && half == 0 && lane == 0) {
+            const float2 lo = ps[item * 2], hi = ps[item * 2 + 1];
+            const float gv = ldexpf(lo.x + hi.x, sx), uv = ldexpf(lo.y + hi.y, sx);
+            const float hval = gv / (1.f + expf(-gv)) * uv;
+            a.h[(size_t)p * v.I + i] = hval;
+            atomicMax(&samax[p], __float_as_uint(fabsf(hval)));
         }
     }
     // this CTA's share of each pair's max |h| (non-negative floats order as integers)
@@ -274,42 +280,38 @@ __global__ void __launch_bounds__(kThreadsF, 1) decode_fused_kernel(const FusedA
     // every consumer warp takes part, aborted or not, so the named barriers match
     ok = grid_barrier(&a.st->pad[1], (unsigned)G, 1, kCW * 32, a.st, 0x300u, abort_flag);
 
-    // ---- phase B: the warp owns pairs warp and warp + 8, their h in registers as
-    // f16 scaled by a per-pair power of two (found from the loaded values)
-    uint4 hr[2][2][4];
-    float wsc[2] = {0.f, 0.f};
-    bool pv[2] = {false, false};
+    // ---- phase B: warp w owns pair w; its h in registers as f16 scaled by a
+    // per-pair power of two (from the max |h| gathered in phase A)
+    uint4 hr[2][4];
+    float wsc = 0.f;
+    const int p = warp;
+    const bool pv = ok && p < k && sidx[p] >= 0;
     if (ok) {
-#pragma unroll
-        for (int pi = 0; pi < 2; pi++) {
-            const int p = warp + kCW * pi;
-            pv[pi] = p < k && sidx[p] >= 0;
-            int sp = 0;
-            if (pv[pi]) {
-                const float ha = __uint_as_float(__ldcg(&a.st->pad[8 + p]));
-                if (ha > 0.f && isfinite(ha)) {
-                    int ex;
-                    frexpf(ha, &ex);
-                    sp = ex - 1 - 7;
-                }
-                wsc[pi] = ldexpf(a.w[p], sp);
+        int sp = 0;
+        if (pv) {
+            const float ha = __uint_as_float(__ldcg(&a.st->pad[8 + p]));
+            if (ha > 0.f && isfinite(ha)) {
+                int ex;
+                frexpf(ha, &ex);
+                sp = ex - 1 - 7;
             }
+            wsc = ldexpf(a.w[p], sp);
+        }
 #pragma unroll
-            for (int blk = 0; blk < 2; blk++) {
-                const int kb = lane + 32 * blk;
+        for (int blk = 0; blk < 2; blk++) {
+            const int kb = lane + 32 * blk;
 #pragma unroll
-                for (int q = 0; q < 4; q++) {
-                    unsigned int hw[4] = {0u, 0u, 0u, 0u};
-                    if (pv[pi] && kb < nkbd) {
-                        const float4 *hp = reinterpret_cast<const float4 *>(a.h + (size_t)p * v.I + kb * 32 + q * 8);
-                        const float4 f0 = __ldcg(hp), f1 = __ldcg(hp + 1);
-                        hw[0] = pack_half2(ldexpf(f0.x, -sp), ldexpf(f0.y, -sp));
-                        hw[1] = pack_half2(ldexpf(f0.z, -sp), ldexpf(f0.w, -sp));
-                        hw[2] = pack_half2(ldexpf(f1.x, -sp), ldexpf(f1.y, -sp));
-                        hw[3] = pack_half2(ldexpf(f1.z, -sp), ldexpf(f1.w, -sp));
-                    }
-                    hr[pi][blk][q] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+            for (int q = 0; q < 4; q++) {
+                unsigned int hw[4] = {0u, 0u, 0u, 0u};
+                if (pv && kb < nkbd) {
+                    const float4 *hp = reinterpret_cast<const float4 *>(a.h + (size_t)p * v.I + kb * 32 + q * 8);
+                    const float4 f0 = __ldcg(hp), f1 = __ldcg(hp + 1);
+                    hw[0] = pack_half2(ldexpf(f0.x, -sp), ldexpf(f0.y, -sp));
+                    hw[1] = pack_half2(ldexpf(f0.z, -sp), ldexpf(f0.w, -sp));
+                    hw[2] = pack_half2(ldexpf(f1.x, -sp), ldexpf(f1.y, -sp));
+                    hw[3] = pack_half2(ldexpf(f1.z, -sp), ldexpf(f1.w, -sp));
                 }
+                hr[blk][q] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
             }
         }
         for (int sb = 0; sb < nstageB; sb++, s++) {
@@ -320,29 +322,24 @@ __global__ void __launch_bounds__(kThreadsF, 1) decode_fused_kernel(const FusedA
             ok = !*(volatile int *)abort_flag && mbar_wait(&full[slot], ph, a.st, 0x400u + slot);
             if (!ok) *abort_flag = 1;
             float part[kMaxR] = {0.f, 0.f, 0.f, 0.f};
-            if (ok) {
+            if (ok && pv) {
                 const uint8_t *base = slots + (size_t)slot * a.slot_bytes;
 #pragma unroll
-                for (int pi = 0; pi < 2; pi++) {
-                    if (!pv[pi]) continue;
-                    const int p = warp + kCW * pi;
+                for (int r = 0; r < kMaxR; r++) {
+                    if (r >= nr) continue;
+                    const uint8_t *row = base + ((size_t)p * a.R + r) * v.ld_d;
+                    const uint8_t *srow =
+                        base + (size_t)k * a.R * v.ld_d + (size_t)p * a.sb_stride + soff + (size_t)r * v.lds_d;
+                    float dsum = 0.f;
 #pragma unroll
-                    for (int r = 0; r < kMaxR; r++) {
-                        if (r >= nr) continue;
-                        const uint8_t *row = base + ((size_t)p * a.R + r) * v.ld_d;
-                        const uint8_t *srow =
-                            base + (size_t)k * a.R * v.ld_d + (size_t)p * a.sb_stride + soff + (size_t)r * v.lds_d;
-                        float dsum = 0.f;
-#pragma unroll
-                        for (int blk = 0; blk < 2; blk++) {
-                            const int kb = lane + 32 * blk;
-                            if (kb < nkbd) {
-                                const uint4 q = *reinterpret_cast<const uint4 *>(row + kb * 16);
-                                dsum = fmaf(block_dot1(q, hr[pi][blk]), e8m0_fast(srow[kb]), dsum);
-                            }
+                    for (int blk = 0; blk < 2; blk++) {
+                        const int kb = lane + 32 * blk;
+                        if (kb < nkbd) {
+                            const uint4 q = *reinterpret_cast<const uint4 *>(row + kb * 16);
+                            dsum = fmaf(block_dot1(q, hr[blk]), e8m0_fast(srow[kb]), dsum);
                         }
-                        part[r] = fmaf(wsc[pi], dsum, part[r]);
                     }
+                    part[r] = wsc * dsum;
                 }
             }
             __syncwarp();
@@ -405,7 +402,7 @@ cudaError_t launch_decode_fused(const PoolView &v, const uint16_t *x, const int3
     fa.y = y;
     fa.h = reinterpret_cast<float *>((char *)ws + 256);
     fa.st = reinterpret_cast<StatusWord *>(ws);
-    const uint32_t slotA = (uint32_t)(2 * kCW * (v.ld_gu + v.lds_gu));
+    const uint32_t slotA = (uint32_t)(2 * kItems * (v.ld_gu + v.lds_gu));
     // phase-B stage: R rows of W_d per pair plus a 16-byte aligned span of their scale rows
     auto sb_of = [&](int r) { return (uint32_t)((r * v.lds_d + 15) / 16 * 16 + 32); };
     auto stageB = [&](int r) { return (uint32_t)k * ((uint32_t)r * v.ld_d + sb_of(r)); };
@@ -416,7 +413,8 @@ cudaError_t launch_decode_fused(const PoolView &v, const uint16_t *x, const int3
     const uint32_t slot_need = slotA > stageB(R) ? slotA : stageB(R);
     fa.slot_bytes = (slot_need + 127) / 128 * 128;
     const size_t smem = (size_t)kSlots * fa.slot_bytes + 2 * kSlots * sizeof(uint64_t) +
-                        (size_t)kCW * kMaxRowsCta * sizeof(float) + (2 * kMaxKF + 4) * sizeof(int);
+                        (size_t)kCW * kMaxRowsCta * sizeof(float) + (size_t)v.H * 2 +
+                        2 * kItems * 2 * sizeof(float2) + (2 * kMaxKF + 4) * sizeof(int);
     cudaError_t e = ensure_dynamic_smem(decode_fused_kernel, smem, g_smem_set);
     if (e != cudaSuccess) return e;
     if (g_grid < 0) {

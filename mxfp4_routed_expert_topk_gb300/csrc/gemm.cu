@@ -237,49 +237,65 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             }
             __syncwarp();  // the epilogue's tensor-memory loads need the whole warp
         } else if (warp == 1) {
+            // Scale factors of K-tile kt: A rows mt*128 + lane + 32 q, B columns
+            // n0 + at*128 + lane + 32 q, scale blocks 4kt .. 4kt+3 (4 bytes each).  They are
+            // fetched two K-tiles ahead into registers so their global latency overlaps
+            // the wait for a free stage.
+            const uint8_t *sa = a.pool + (uint64_t)e * a.rec + a.a_scale_off;
+            auto load_sf = [&](int kt, uint32_t (&wa)[4], uint32_t (&wb)[2][4]) {
+#pragma unroll
+                for (int q = 0; q < 4; q++) {
+                    const uint64_t r = (uint64_t)(mt * kTileM + lane + 32 * q);
+                    wa[q] = (kt < a.nkt && 4 * kt + 3 < a.nkb_a)
+                                ? __ldg(reinterpret_cast<const uint32_t *>(sa + r * a.lds_a + 4 * kt))
+                                : 0u;
+                }
+                const uint32_t keep = (4 * kt + 4 <= a.nkb_b) ? 0xFFFFFFFFu
+                                      : (4 * kt >= a.nkb_b)    ? 0u
+                                                               : (0xFFFFFFFFu >> (8 * (4 * kt + 4 - a.nkb_b)));
+#pragma unroll
+                for (int at = 0; at < 2; at++)
+#pragma unroll
+                    for (int q = 0; q < 4; q++) {
+                        const int c = at * 128 + lane + 32 * q;
+                        uint32_t w = 0u;
+                        if (at < nsfb && c < nn && kt < a.nkt && keep != 0u)
+                            w = __ldg(reinterpret_cast<const uint32_t *>(a.bscale + (uint64_t)(row0 + n0 + c) * a.lds_b +
+                                                                        4 * kt)) & keep;
+                        wb[at][q] = w;
+                    }
+            };
+            uint32_t wa0[4], wb0[2][4], wa1[4], wb1[2][4], wa2[4], wb2[2][4];
+            load_sf(0, wa0, wb0);
+            load_sf(1, wa1, wb1);
             for (int kt = 0; kt < a.nkt; kt++) {
                 const int it = nt * a.nkt + kt, s = it % kStages;
                 const uint32_t ph = (uint32_t)(it / kStages) & 1u;
+                load_sf(kt + 2, wa2, wb2);
                 int okl = 0;
                 if (lane == 0) okl = !*(volatile int *)abort_flag && mbar_wait(&empty[s], ph ^ 1u, a.st, 0x600u + s);
                 const bool ok = __shfl_sync(0xffffffffu, okl, 0) != 0;  // warp-uniform
                 if (!ok && lane == 0) *abort_flag = 1;
                 if (ok) {
-                    // A: rows mt*128 + lane + 32 q, scale blocks 4kt .. 4kt+3
-                    const uint8_t *sa = a.pool + (uint64_t)e * a.rec + a.a_scale_off;
-                    uint32_t wa[4];
-#pragma unroll
-                    for (int q = 0; q < 4; q++) {
-                        const uint64_t r = (uint64_t)(mt * kTileM + lane + 32 * q);
-                        wa[q] = (4 * kt + 3 < a.nkb_a) ? *reinterpret_cast<const uint32_t *>(sa + r * a.lds_a + 4 * kt)
-                                                       : 0u;
-                    }
-                    *reinterpret_cast<uint4 *>(sSFA + (size_t)s * 512 + lane * 16) = make_uint4(wa[0], wa[1], wa[2], wa[3]);
-                    // B: columns n0 + lane + 32 q of this tile
-                    for (int at = 0; at < nsfb; at++) {
-                        uint32_t wb[4];
-#pragma unroll
-                        for (int q = 0; q < 4; q++) {
-                            const int c = at * 128 + lane + 32 * q;
-                            uint32_t w = 0u;
-                            if (c < nn) {
-                                const uint8_t *rowp = a.bscale + (uint64_t)(row0 + n0 + c) * a.lds_b;
-#pragma unroll
-                                for (int t = 0; t < 4; t++) {
-                                    const int kb = 4 * kt + t;
-                                    if (kb < a.nkb_b) w |= (uint32_t)rowp[kb] << (8 * t);
-                                }
-                            }
-                            wb[q] = w;
-                        }
+                    *reinterpret_cast<uint4 *>(sSFA + (size_t)s * 512 + lane * 16) =
+                        make_uint4(wa0[0], wa0[1], wa0[2], wa0[3]);
+                    for (int at = 0; at < nsfb; at++)
                         *reinterpret_cast<uint4 *>(sSFB + ((size_t)s * nsfb + at) * 512 + lane * 16) =
-                            make_uint4(wb[0], wb[1], wb[2], wb[3]);
-                    }
+                            make_uint4(wb0[at][0], wb0[at][1], wb0[at][2], wb0[at][3]);
                     fence_proxy_async_smem();
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&full[s]);
                 if (!ok) break;
+#pragma unroll
+                for (int q = 0; q < 4; q++) {
+                    wa0[q] = wa1[q];
+                    wa1[q] = wa2[q];
+                    wb0[0][q] = wb1[0][q];
+                    wb0[1][q] = wb1[1][q];
+                    wb1[0][q] = wb2[0][q];
+                    wb1[1][q] = wb2[1][q];
+                }
             }
         } else if (warp == 2) {
             if (lane == 0) {
