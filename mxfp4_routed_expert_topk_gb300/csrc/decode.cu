@@ -303,7 +303,10 @@ int g_num_sms = 0;
 
 size_t decode_workspace_bytes(int E, int H, int I, int M, int k) {
     (void)E;
-    return decode_ws_end(H, I, M, k);
+    const size_t general = decode_ws_end(H, I, M, k);
+    if (M != 1) return general;
+    const size_t fused = decode_fused_workspace_bytes(I, k);
+    return fused > general ? fused : general;
 }
 
 cudaError_t launch_decode(const PoolView &v, const uint16_t *x, int M, const int32_t *idx, const float *w, int k,

@@ -40,8 +40,9 @@ struct FusedArgs {
     const float *w;
     const uint16_t *residual;
     uint16_t *y;
-    float *h;            // [k][I] workspace
-    StatusWord *st;      // pad[1]: grid barrier, pad[2]: exit counter, pad[8+p]: max |h| of pair p
+    float *h;            // [k][8][I/32] float4 workspace (see h_slot)
+    float *hmax;         // [kMaxKF][G] workspace: each CTA's max |h| per pair
+    StatusWord *st;      // grid barrier and exit counters
     uint32_t slot_bytes;
     int R;
     uint32_t sb_stride;  // bytes per pair of phase-B scale rows in a slot
@@ -65,9 +66,27 @@ __device__ __forceinline__ float block_dot1(const uint4 &q, const uint4 *xb) {
     return f16x2_sum_to_float(acc);
 }
 
+// Position of h[p][i] in the workspace: float4 (p, e8, kb) at (p*8 + e8)*(I/32) + kb
+// for 32-block kb = i/32 and eighth e8 = (i%32)/4, so that in phase B the lanes of
+// a warp, one 32-block each, read 512 contiguous bytes per load instruction.
+__device__ __forceinline__ size_t h_slot(int p, int i, int nkbd) {
+    return ((size_t)(p * 8 + ((i & 31) >> 2)) * nkbd + (i >> 5)) * 4 + (i & 3);
+}
+
 // E8M0 byte -> 2^(b-127) with one shift: byte 0 gives 0 instead of 2^-127 (far
 // below anything it scales), byte 255 (NaN) gives +inf (non-finite either way).
 __device__ __forceinline__ float e8m0_fast(unsigned int b) { return __uint_as_float(b << 23); }
+
+// f * 2^n for n in [-126, 254], exact unless the result is subnormal (then one
+// rounding, as a single multiplication by 2^n would give): a scale-up above 2^127
+// is split into two exact steps.
+__device__ __forceinline__ float mul_pow2(float f, int n) {
+    if (n > 127) {
+        f *= __uint_as_float((uint32_t)(n - 127 + 127) << 23);
+        n = 127;
+    }
+    return f * __uint_as_float((uint32_t)(n + 127) << 23);
+}
 
 __device__ __forceinline__ unsigned int pack_half2(float lo, float hi) {
     const __half2 h = __floats2half2_rn(lo, hi);
@@ -180,11 +199,14 @@ __global__ void __launch_bounds__(kThreadsF, 1) decode_fused_kernel(const FusedA
     }
 
     // ------------------------------------------------------------------ consumers
-    // the token's max |x| (16-byte loads spread over the consumer threads)
+    // the token (at most two 16-byte chunks per consumer thread) and its max |x|
+    uint4 xraw[2];
     float xa = 0.f;
-    for (int c = threadIdx.x; c < v.H / 8; c += kCW * 32) {
-        const uint4 raw = __ldg(reinterpret_cast<const uint4 *>(a.x) + c);
-        const unsigned int u[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+    for (int r = 0; r < 2; r++) {
+        const int c = threadIdx.x + r * kCW * 32;
+        xraw[r] = c < v.H / 8 ? __ldg(reinterpret_cast<const uint4 *>(a.x) + c) : make_uint4(0u, 0u, 0u, 0u);
+        const unsigned int u[4] = {xraw[r].x, xraw[r].y, xraw[r].z, xraw[r].w};
 #pragma unroll
         for (int t = 0; t < 4; t++)
             xa = fmaxf(xa, fmaxf(fabsf(__uint_as_float(u[t] << 16)), fabsf(__uint_as_float(u[t] & 0xffff0000u))));
@@ -195,7 +217,6 @@ __global__ void __launch_bounds__(kThreadsF, 1) decode_fused_kernel(const FusedA
     named_barrier(1, kCW * 32);
     float amax_x = 0.f;
     for (int ww = 0; ww < kCW; ww++) amax_x = fmaxf(amax_x, red[ww]);
-    named_barrier(1, kCW * 32);  // red[] is reused in phase B
     // the token as f16 scaled by 2^-sx, max|x 2^-sx| in [128, 256) (exact for bf16),
     // staged in shared memory for all consumer warps
     int sx = 0;
@@ -204,17 +225,21 @@ __global__ void __launch_bounds__(kThreadsF, 1) decode_fused_kernel(const FusedA
         frexpf(amax_x, &ex);
         sx = ex - 1 - 7;
     }
-    for (int c = threadIdx.x; c < v.H / 8; c += kCW * 32) {
-        const uint4 raw = __ldg(reinterpret_cast<const uint4 *>(a.x) + c);
-        const unsigned int u[4] = {raw.x, raw.y, raw.z, raw.w};
-        unsigned int hw[4];
 #pragma unroll
-        for (int t = 0; t < 4; t++)
-            hw[t] = pack_half2(ldexpf(__uint_as_float(u[t] << 16), -sx), ldexpf(__uint_as_float(u[t] & 0xffff0000u), -sx));
-        // eighth q of 32-block kb at [q][kb]: a warp's lanes read consecutive 16 bytes
-        xsm[(c & 3) * nkb + (c >> 2)] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+    for (int r = 0; r < 2; r++) {
+        const int c = threadIdx.x + r * kCW * 32;
+        if (c < v.H / 8) {
+            const unsigned int u[4] = {xraw[r].x, xraw[r].y, xraw[r].z, xraw[r].w};
+            unsigned int hw[4];
+#pragma unroll
+            for (int t = 0; t < 4; t++)
+                hw[t] = pack_half2(mul_pow2(__uint_as_float(u[t] << 16), -sx),
+                                   mul_pow2(__uint_as_float(u[t] & 0xffff0000u), -sx));
+            // eighth q of 32-block kb at [q][kb]: a warp's lanes read consecutive 16 bytes
+            xsm[(c & 3) * nkb + (c >> 2)] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+        }
     }
-    named_barrier(1, kCW * 32);
+    named_barrier(1, kCW * 32);  // also orders the reads of red[] before its reuse in phase B
 
     bool ok = true;
     int s = 0;
@@ -270,15 +295,15 @@ __global__ void __launch_bounds__(kThreadsF, 1) decode_fused_kernel(const FusedA
             const float2 lo = ps[item * 2], hi = ps[item * 2 + 1];
             const float gv = ldexpf(lo.x + hi.x, sx), uv = ldexpf(lo.y + hi.y, sx);
             const float hval = gv / (1.f + expf(-gv)) * uv;
-            a.h[(size_t)p * v.I + i] = hval;
+            a.h[h_slot(p, i, nkbd)] = hval;
             atomicMax(&samax[p], __float_as_uint(fabsf(hval)));
         }
     }
-    // this CTA's share of each pair's max |h| (non-negative floats order as integers)
+    // this CTA's max |h| per pair (plain stores: one column of the [pair][CTA] table)
     named_barrier(1, kCW * 32);
-    if (threadIdx.x < k && samax[threadIdx.x] != 0u) atomicMax(&a.st->pad[8 + threadIdx.x], samax[threadIdx.x]);
+    if (threadIdx.x < kMaxKF) a.hmax[threadIdx.x * G + b] = __uint_as_float(samax[threadIdx.x]);
     // every consumer warp takes part, aborted or not, so the named barriers match
-    ok = grid_barrier(&a.st->pad[1], (unsigned)G, 1, kCW * 32, a.st, 0x300u, abort_flag);
+    ok = grid_barrier(&a.st->pad[kStGridBarrier], (unsigned)G, 1, kCW * 32, a.st, 0x300u, abort_flag);
 
     // ---- phase B: warp w owns pair w; its h in registers as f16 scaled by a
     // per-pair power of two (from the max |h| gathered in phase A)
@@ -287,33 +312,44 @@ __global__ void __launch_bounds__(kThreadsF, 1) decode_fused_kernel(const FusedA
     const int p = warp;
     const bool pv = ok && p < k && sidx[p] >= 0;
     if (ok) {
-        int sp = 0;
+        // every load issued before any use: one L2 round trip.  The pair's max |h|
+        // is the max over its row of the [pair][CTA] table.
+        float ha = 0.f, wp = 0.f;
+        float4 hv[2][4][2];
         if (pv) {
-            const float ha = __uint_as_float(__ldcg(&a.st->pad[8 + p]));
-            if (ha > 0.f && isfinite(ha)) {
-                int ex;
-                frexpf(ha, &ex);
-                sp = ex - 1 - 7;
-            }
-            wsc = ldexpf(a.w[p], sp);
+            wp = __ldg(a.w + p);
+            for (int c = lane; c < G; c += 32) ha = fmaxf(ha, __ldcg(a.hmax + p * G + c));
         }
 #pragma unroll
         for (int blk = 0; blk < 2; blk++) {
             const int kb = lane + 32 * blk;
+            const bool in = pv && kb < nkbd;
+            const float4 *hp = reinterpret_cast<const float4 *>(a.h) + (size_t)(in ? p : 0) * 8 * nkbd + (in ? kb : 0);
 #pragma unroll
-            for (int q = 0; q < 4; q++) {
-                unsigned int hw[4] = {0u, 0u, 0u, 0u};
-                if (pv && kb < nkbd) {
-                    const float4 *hp = reinterpret_cast<const float4 *>(a.h + (size_t)p * v.I + kb * 32 + q * 8);
-                    const float4 f0 = __ldcg(hp), f1 = __ldcg(hp + 1);
-                    hw[0] = pack_half2(ldexpf(f0.x, -sp), ldexpf(f0.y, -sp));
-                    hw[1] = pack_half2(ldexpf(f0.z, -sp), ldexpf(f0.w, -sp));
-                    hw[2] = pack_half2(ldexpf(f1.x, -sp), ldexpf(f1.y, -sp));
-                    hw[3] = pack_half2(ldexpf(f1.z, -sp), ldexpf(f1.w, -sp));
-                }
-                hr[blk][q] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+            for (int q = 0; q < 8; q++) {
+                const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+                hv[blk][q >> 1][q & 1] = in ? __ldcg(hp + (size_t)q * nkbd) : z;
             }
         }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) ha = fmaxf(ha, __shfl_xor_sync(0xffffffffu, ha, off));
+        int sp = 0;
+        if (ha > 0.f && isfinite(ha)) {
+            int ex;
+            frexpf(ha, &ex);
+            sp = ex - 1 - 7;
+        }
+        if (pv) wsc = ldexpf(wp, sp);
+#pragma unroll
+        for (int blk = 0; blk < 2; blk++)
+#pragma unroll
+            for (int q = 0; q < 4; q++) {
+                const float4 f0 = hv[blk][q][0], f1 = hv[blk][q][1];
+                hr[blk][q] = make_uint4(pack_half2(mul_pow2(f0.x, -sp), mul_pow2(f0.y, -sp)),
+                                        pack_half2(mul_pow2(f0.z, -sp), mul_pow2(f0.w, -sp)),
+                                        pack_half2(mul_pow2(f1.x, -sp), mul_pow2(f1.y, -sp)),
+                                        pack_half2(mul_pow2(f1.z, -sp), mul_pow2(f1.w, -sp)));
+            }
         for (int sb = 0; sb < nstageB; sb++, s++) {
             const int slot = s % kSlots;
             const uint32_t ph = (uint32_t)(s / kSlots) & 1u;
@@ -367,10 +403,9 @@ __global__ void __launch_bounds__(kThreadsF, 1) decode_fused_kernel(const FusedA
     // every CTA is past the grid barrier: the last one here resets both counters
     if (threadIdx.x == 0) {
         __threadfence();
-        if (atomicAdd(&a.st->pad[2], 1u) == (unsigned)G - 1u) {
-            for (int p = 0; p < kMaxKF; p++) atomicExch(&a.st->pad[8 + p], 0u);
-            atomicExch(&a.st->pad[1], 0u);
-            atomicExch(&a.st->pad[2], 0u);
+        if (atomicAdd(&a.st->pad[kStExitCount], 1u) == (unsigned)G - 1u) {
+            atomicExch(&a.st->pad[kStGridBarrier], 0u);
+            atomicExch(&a.st->pad[kStExitCount], 0u);
         }
     }
 }
@@ -401,6 +436,7 @@ cudaError_t launch_decode_fused(const PoolView &v, const uint16_t *x, const int3
     fa.residual = residual;
     fa.y = y;
     fa.h = reinterpret_cast<float *>((char *)ws + 256);
+    fa.hmax = reinterpret_cast<float *>((char *)ws + 256 + align_up((size_t)k * v.I * sizeof(float), 256));
     fa.st = reinterpret_cast<StatusWord *>(ws);
     const uint32_t slotA = (uint32_t)(2 * kItems * (v.ld_gu + v.lds_gu));
     // phase-B stage: R rows of W_d per pair plus a 16-byte aligned span of their scale rows
@@ -424,7 +460,7 @@ cudaError_t launch_decode_fused(const PoolView &v, const uint16_t *x, const int3
         g_grid = per_sm >= 1 ? g_sms : 0;
     }
     fa.G = g_grid;
-    if (fa.G <= 0 || (v.H + fa.G - 1) / fa.G > kMaxRowsCta) return cudaErrorNotSupported;
+    if (fa.G <= 0 || fa.G > kMaxFusedGrid || (v.H + fa.G - 1) / fa.G > kMaxRowsCta) return cudaErrorNotSupported;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(fa.G);
     cfg.blockDim = dim3(kThreadsF);

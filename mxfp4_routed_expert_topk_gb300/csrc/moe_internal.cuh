@@ -46,8 +46,13 @@ struct StatusWord {
     unsigned int code;
     unsigned int detail;
     unsigned int exact_fallbacks;
-    unsigned int pad[61];
+    unsigned int pad[61];  // kernel counters: see the kSt* slots
 };
+// Counter slots in StatusWord::pad.  The grid barrier's counter, polled by every
+// CTA, sits alone in the second 128-byte line of the word.
+constexpr int kStRouteTicket = 0;   // route_single: CTAs done with their logits
+constexpr int kStExitCount = 2;     // decode_fused: CTAs past the grid barrier
+constexpr int kStGridBarrier = 32;  // decode_fused: grid barrier arrivals (byte 140)
 
 __device__ __forceinline__ void set_status(StatusWord *s, unsigned int code, unsigned int detail) {
     if (s == nullptr) return;
@@ -140,6 +145,12 @@ cudaError_t launch_route(const uint16_t *x, int M, int H, const uint16_t *Wr, in
                          int k, int32_t *idx, float *w, void *ws, cudaStream_t st);
 
 size_t decode_workspace_bytes(int E, int H, int I, int M, int k);
+// The single-token fused decode runs at most this many CTAs; its workspace holds
+// h [k][I] and a [16][grid] table of per-CTA max |h| after the status word.
+constexpr int kMaxFusedGrid = 1024;
+inline size_t decode_fused_workspace_bytes(int I, int k) {
+    return 256 + align_up((size_t)k * I * sizeof(float), 256) + (size_t)16 * kMaxFusedGrid * sizeof(float);
+}
 cudaError_t launch_decode(const PoolView &v, const uint16_t *x, int M, const int32_t *idx, const float *w,
                           int k, const uint16_t *residual, uint16_t *y, void *ws, cudaStream_t st);
 

@@ -582,14 +582,14 @@ __global__ void __launch_bounds__(kRouteThreads) route_single_kernel(
     __syncthreads();
     if (threadIdx.x == 0) {
         __threadfence();
-        const unsigned int t = atomicAdd(&st->pad[0], 1u);
+        const unsigned int t = atomicAdd(&st->pad[kStRouteTicket], 1u);
         last = (t == gridDim.x - 1);
     }
     __syncthreads();
     if (!last) return;
     __threadfence();
     select_token(0, x, H, Wr, E, skew, k, logit, bound, idx_out, w_out, st, s);
-    if (threadIdx.x == 0) st->pad[0] = 0u;
+    if (threadIdx.x == 0) st->pad[kStRouteTicket] = 0u;
 }
 
 }  // namespace
