@@ -342,9 +342,27 @@ __device__ void warp_topk(unsigned long long (&key)[J], int k, unsigned long lon
     }
 }
 
+// Maximum of a 64-bit key over the warp: two single-instruction reductions, the
+// high halves first, then the low halves of the lanes holding the highest one.
+__device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long v) {
+    const unsigned int hi = (unsigned int)(v >> 32);
+    const unsigned int mhi = __reduce_max_sync(0xffffffffu, hi);
+    const unsigned int lo = hi == mhi ? (unsigned int)v : 0u;
+    const unsigned int mlo = __reduce_max_sync(0xffffffffu, lo);
+    return ((unsigned long long)mhi << 32) | mlo;
+}
+
+constexpr int kMaxTopCand = 512;  // keys at or above the filter threshold ranked directly
+
 struct SelectShared {
-    unsigned long long wtop[kRouteWarps][kMaxK];  // each warp's top k
+    unsigned long long wtop[kRouteWarps][kMaxK];  // each warp's top keys
     unsigned long long top[kMaxK];                // the token's top k by fp32 logit
+    float top_l[kMaxK], top_b[kMaxK];             // their fp32 logits and bounds
+    float final_l[kMaxK];                         // fp32 logits of the final selection
+    unsigned long long ckey[kMaxTopCand];         // keys at or above the threshold
+    float cl[kMaxTopCand], cb[kMaxTopCand];
+    unsigned long long thr;
+    int nc;
     unsigned int Lord;
     int cand[kMaxCand];                           // outsiders that may still enter
     int ncand;
@@ -394,26 +412,95 @@ __device__ void select_token(int m, const uint16_t *__restrict__ x, int H, const
     }
     __syncthreads();
     if (bad) s.nonfinite = 1;
-    warp_topk<kKeysPerThread>(key, k, s.wtop[warp]);
-    __syncthreads();
-    if (warp == 0) {
-        constexpr int JW = kRouteWarps * kMaxK / 32;
-        unsigned long long wk[JW];
+    // (1) each warp's top q keys, q = ceil(k / warps): these 8q keys are distinct, so
+    // at least k keys lie at or above the smallest of them (0 if a warp has fewer)
+    const int q = (k + kRouteWarps - 1) / kRouteWarps;
+    {
+        unsigned long long best = 0ull;
 #pragma unroll
-        for (int j = 0; j < JW; j++) {
-            const int q = lane + 32 * j;
-            const int ww = q / kMaxK, r = q % kMaxK;
-            wk[j] = (r < k) ? s.wtop[ww][r] : 0ull;
+        for (int j = 0; j < kKeysPerThread; j++) best = key[j] > best ? key[j] : best;
+        for (int r = 0; r < q; r++) {
+            const unsigned long long mx = warp_max_u64(best);
+            if (lane == 0) s.wtop[warp][r] = mx;
+            if (mx != 0ull && best == mx) {
+                best = 0ull;
+#pragma unroll
+                for (int j = 0; j < kKeysPerThread; j++) {
+                    if (key[j] == mx) key[j] = 0ull;
+                    best = key[j] > best ? key[j] : best;
+                }
+            }
         }
-        warp_topk<JW>(wk, k, s.top);
+    }
+    __syncthreads();
+    if (tid == 0) {
+        unsigned long long t = ~0ull;
+        for (int ww = 0; ww < kRouteWarps; ww++)
+            for (int r = 0; r < q; r++) t = s.wtop[ww][r] < t ? s.wtop[ww][r] : t;
+        s.thr = t;
+        s.nc = 0;
+    }
+    __syncthreads();
+    // (2) gather every key at or above the threshold (slots by warp ballot)
+    const unsigned long long thr = s.thr;
+#pragma unroll
+    for (int j = 0; j < kKeysPerThread; j++) {
+        const int e = tid + kRouteThreads * j;
+        key[j] = e < E ? route_key(lv[j], e) : 0ull;  // restore what (1) cleared
+        const bool take = key[j] != 0ull && key[j] >= thr;
+        const unsigned int bal = __ballot_sync(0xffffffffu, take);
+        if (bal != 0u) {
+            int base = 0;
+            if (lane == __ffs(bal) - 1) base = atomicAdd(&s.nc, __popc(bal));
+            base = __shfl_sync(0xffffffffu, base, __ffs(bal) - 1);
+            const int slot = base + __popc(bal & ((1u << lane) - 1u));
+            if (take && slot < kMaxTopCand) {
+                s.ckey[slot] = key[j];
+                s.cl[slot] = lv[j];
+                s.cb[slot] = bv[j];
+            }
+        }
+    }
+    __syncthreads();
+    const int nc = s.nc;
+    if (nc <= kMaxTopCand) {
+        // (3) a candidate's place is the number of larger candidates (keys are unique)
+        for (int c = tid; c < nc; c += kRouteThreads) {
+            const unsigned long long kc = s.ckey[c];
+            int r = 0;
+            for (int d = 0; d < nc; d++) r += s.ckey[d] > kc;
+            if (r < k) {
+                s.top[r] = kc;
+                s.top_l[r] = s.cl[c];
+                s.top_b[r] = s.cb[c];
+            }
+        }
+    } else {
+        // many keys at the threshold: k rounds of warp maxima, then over the warps
+        warp_topk<kKeysPerThread>(key, k, s.wtop[warp]);
+        __syncthreads();
+        if (warp == 0) {
+            constexpr int JW = kRouteWarps * kMaxK / 32;
+            unsigned long long wk[JW];
+#pragma unroll
+            for (int j = 0; j < JW; j++) {
+                const int qq = lane + 32 * j;
+                const int ww = qq / kMaxK, r = qq % kMaxK;
+                wk[j] = (r < k) ? s.wtop[ww][r] : 0ull;
+            }
+            warp_topk<JW>(wk, k, s.top);
+        }
+        __syncthreads();
+        if (tid < k) {
+            const int e = key_expert(s.top[tid]);
+            s.top_l[tid] = __ldcg(lm + e);
+            s.top_b[tid] = __ldcg(bm + e);
+        }
     }
     __syncthreads();
     const unsigned long long kth = s.top[k - 1];
     // lowest lower bound among the k winners
-    if (tid < k) {
-        const int e = key_expert(s.top[tid]);
-        atomicMin(&s.Lord, orderable(__fsub_rd(__ldcg(lm + e), __ldcg(bm + e))));
-    }
+    if (tid < k) atomicMin(&s.Lord, orderable(__fsub_rd(s.top_l[tid], s.top_b[tid])));
     __syncthreads();
     const unsigned int Lo = s.Lord;
     // outsiders whose upper bound reaches it; adjacent winners whose intervals meet
@@ -427,18 +514,23 @@ __device__ void select_token(int m, const uint16_t *__restrict__ x, int H, const
         }
     }
     if (tid + 1 < k) {
-        const int a = key_expert(s.top[tid]), b = key_expert(s.top[tid + 1]);
-        if (!(__fsub_rd(__ldcg(lm + a), __ldcg(bm + a)) > __fadd_ru(__ldcg(lm + b), __ldcg(bm + b)))) s.uncertain = 1;
+        if (!(__fsub_rd(s.top_l[tid], s.top_b[tid]) > __fadd_ru(s.top_l[tid + 1], s.top_b[tid + 1]))) s.uncertain = 1;
     }
     __syncthreads();
     auto L_ = [&](int e) { return __ldcg(lm + e); };
     auto B_ = [&](int e) { return __ldcg(bm + e); };
     if (s.nonfinite) {
         if (tid == 0) set_status(st, MOE_ERR_NONFINITE, (unsigned)m);
-        if (tid < k) s.final_idx[tid] = key_expert(s.top[tid]);
+        if (tid < k) {
+            s.final_idx[tid] = key_expert(s.top[tid]);
+            s.final_l[tid] = s.top_l[tid];
+        }
         __syncthreads();
     } else if (s.ncand == 0 && !s.uncertain) {
-        if (tid < k) s.final_idx[tid] = key_expert(s.top[tid]);
+        if (tid < k) {
+            s.final_idx[tid] = key_expert(s.top[tid]);
+            s.final_l[tid] = s.top_l[tid];
+        }
         __syncthreads();
     } else {
         // ---- slow path: interval clusters, exact evaluation where needed
@@ -543,11 +635,13 @@ __device__ void select_token(int m, const uint16_t *__restrict__ x, int H, const
             }
         }
         __syncthreads();
+        if (tid < k) s.final_l[tid] = L_(s.final_idx[tid]);
+        __syncthreads();
     }
     // softmax over the k selected fp32 logits
     if (tid < 32) {
         const int j = tid;
-        const float l = (j < k) ? L_(s.final_idx[j]) : -__int_as_float(0x7f800000);
+        const float l = (j < k) ? s.final_l[j] : -__int_as_float(0x7f800000);
         float mx = l;
         for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
         const float ex = (j < k) ? expf(l - mx) : 0.f;

@@ -134,6 +134,24 @@ def test_route_planted_ties_take_exact_path(tiny):
     assert nfb > 0
 
 
+@pytest.mark.parametrize("M", [1, 3])
+def test_route_threshold_fallback(full, M):
+    # The experts of the select CTA's last warp (e mod 256 in 224..255) get strongly
+    # negative logits for token 0: the filter threshold (the smallest per-warp
+    # runner-up) then sits among them and more than 512 keys pass it, so the
+    # selection takes its round-by-round branch.  Token 0 of M=1 runs the
+    # single-kernel router; M=3 repeats the token (the planted rows are identical,
+    # so for other tokens they would form one 96-way exact tie).
+    s, _, Wrb0, _ = full
+    Wrb = Wrb0.copy()
+    xb = np.repeat(synth.tokens_bf16(synth.TOKENS_SEED["full"], 100, 1, s.H), M, axis=0)
+    neg = synth.bf16_bits_from_f64(-0.05 * np.sign(synth.bf16_bits_to_f64(xb[0])))
+    for e in range(s.E):
+        if (e % 256) // 32 == 7:
+            Wrb[e] = neg
+    _route_check(xb, Wrb, to_dev_bf16(Wrb), s.k)
+
+
 def test_route_large_dynamic_range(tiny):
     s, _, Wrb0, _ = tiny
     rng = np.random.default_rng(11)
