@@ -106,6 +106,8 @@ __global__ void __launch_bounds__(kThreadsF, 1) decode_fused_kernel(const FusedA
     int *sidx = reinterpret_cast<int *>(pairsum + 2 * kItems * 2);      // [kMaxKF]
     int *abort_flag = sidx + kMaxKF;
     unsigned int *samax = reinterpret_cast<unsigned int *>(abort_flag + 1);  // [kMaxKF] max |h| per pair
+    int *s_sp = reinterpret_cast<int *>(samax + kMaxKF);                     // [kMaxKF] h scale exponent per pair
+    float *s_wsc = reinterpret_cast<float *>(s_sp + kMaxKF);                 // [kMaxKF] w_p * 2^sp
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int b = blockIdx.x, G = a.G, k = a.k;
     const int NA = k * v.I;
@@ -244,8 +246,11 @@ __global__ void __launch_bounds__(kThreadsF, 1) decode_fused_kernel(const FusedA
     bool ok = true;
     int s = 0;
     // ---- phase A: item j of a stage (gate row + up row) is shared by warps 2j and
-    // 2j+1, which take the even and the odd 32-block columns of the lane's blocks
-    const int item = warp >> 1, half = warp & 1;
+    // 2j+1, which take alternate 32-block columns of the row.  Warp w issues on
+    // scheduler w mod 4; which warp of the pair takes the even columns (one more
+    // when the row has an odd number of columns) alternates every two items, so
+    // the four schedulers get equal work.
+    const int item = warp >> 1, half = (warp & 1) ^ ((item >> 1) & 1);
     for (; s < nstageA; s++) {
         const int slot = s % kSlots;
         const uint32_t ph = (uint32_t)(s / kSlots) & 1u;
@@ -305,51 +310,73 @@ __global__ void __launch_bounds__(kThreadsF, 1) decode_fused_kernel(const FusedA
     // every consumer warp takes part, aborted or not, so the named barriers match
     ok = grid_barrier(&a.st->pad[kStGridBarrier], (unsigned)G, 1, kCW * 32, a.st, 0x300u, abort_flag);
 
-    // ---- phase B: warp w owns pair w; its h in registers as f16 scaled by a
-    // per-pair power of two (from the max |h| gathered in phase A)
+    // ---- phase B: each lane owns up to two (pair, 32-block) combinations of h, in
+    // registers as f16 scaled by a per-pair power of two (from the max |h| of the
+    // pair gathered in phase A), and for every output row of a stage adds
+    //   w_pair * (W_d,pair row block . h block) * scale
+    // for each.  Combination 0: pair = warp, block = lane (blocks 0..31).
+    // Combination 1: the tail blocks 32..I/32-1 of every pair, packed densely into
+    // the lanes of as few warps as possible, starting after the warps of
+    // combination 0, so that no warp instruction runs with idle lanes it could
+    // have avoided.
+    const int T1 = nkbd > 32 ? nkbd - 32 : 0;
+    const int g = warp * 32 + lane;
+    const int c1 = (g - (k * 32) % (kCW * 32) + kCW * 32) % (kCW * 32);
+    const int pb[2] = {warp, T1 > 0 ? c1 / T1 : 0};
+    const int kbs[2] = {lane, T1 > 0 ? 32 + c1 % T1 : 0};
+    const bool pv[2] = {ok && warp < k && lane < nkbd && sidx[warp] >= 0,
+                        ok && T1 > 0 && c1 < k * T1 && sidx[pb[1]] >= 0};
     uint4 hr[2][4];
-    float wsc = 0.f;
-    const int p = warp;
-    const bool pv = ok && p < k && sidx[p] >= 0;
-    if (ok) {
-        // every load issued before any use: one L2 round trip.  The pair's max |h|
-        // is the max over its row of the [pair][CTA] table.
-        float ha = 0.f, wp = 0.f;
-        float4 hv[2][4][2];
-        if (pv) {
-            wp = __ldg(a.w + p);
-            for (int c = lane; c < G; c += 32) ha = fmaxf(ha, __ldcg(a.hmax + p * G + c));
-        }
+    float wsc[2] = {0.f, 0.f};
+    // the lanes' h blocks first (their latency overlaps the rest of the setup)
+    float4 hv[2][4][2];
+    {
 #pragma unroll
-        for (int blk = 0; blk < 2; blk++) {
-            const int kb = lane + 32 * blk;
-            const bool in = pv && kb < nkbd;
-            const float4 *hp = reinterpret_cast<const float4 *>(a.h) + (size_t)(in ? p : 0) * 8 * nkbd + (in ? kb : 0);
+        for (int u = 0; u < 2; u++) {
+            const float4 *hp =
+                reinterpret_cast<const float4 *>(a.h) + (size_t)(pv[u] ? pb[u] : 0) * 8 * nkbd + (pv[u] ? kbs[u] : 0);
 #pragma unroll
             for (int q = 0; q < 8; q++) {
                 const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-                hv[blk][q >> 1][q & 1] = in ? __ldcg(hp + (size_t)q * nkbd) : z;
+                hv[u][q >> 1][q & 1] = pv[u] ? __ldcg(hp + (size_t)q * nkbd) : z;
             }
         }
+    }
+    // warp p: max |h| of pair p over its row of the [pair][CTA] table, then the
+    // pair's f16 scale exponent and scaled routing weight for all warps
+    {
+        if (ok && warp < k) {
+            float ha = 0.f;
+            for (int c = lane; c < G; c += 32) ha = fmaxf(ha, __ldcg(a.hmax + warp * G + c));
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) ha = fmaxf(ha, __shfl_xor_sync(0xffffffffu, ha, off));
-        int sp = 0;
-        if (ha > 0.f && isfinite(ha)) {
-            int ex;
-            frexpf(ha, &ex);
-            sp = ex - 1 - 7;
+            for (int off = 16; off > 0; off >>= 1) ha = fmaxf(ha, __shfl_xor_sync(0xffffffffu, ha, off));
+            int sp = 0;
+            if (ha > 0.f && isfinite(ha)) {
+                int ex;
+                frexpf(ha, &ex);
+                sp = ex - 1 - 7;
+            }
+            if (lane == 0) {
+                s_sp[warp] = sp;
+                s_wsc[warp] = sidx[warp] >= 0 ? ldexpf(__ldg(a.w + warp), sp) : 0.f;
+            }
         }
-        if (pv) wsc = ldexpf(wp, sp);
+    }
+    named_barrier(1, kCW * 32);  // every consumer warp, aborted or not
+    if (ok) {
 #pragma unroll
-        for (int blk = 0; blk < 2; blk++)
+        for (int u = 0; u < 2; u++) {
+            const int sp = pv[u] ? s_sp[pb[u]] : 0;
+            if (pv[u]) wsc[u] = s_wsc[pb[u]];
 #pragma unroll
             for (int q = 0; q < 4; q++) {
-                const float4 f0 = hv[blk][q][0], f1 = hv[blk][q][1];
-                hr[blk][q] = make_uint4(pack_half2(mul_pow2(f0.x, -sp), mul_pow2(f0.y, -sp)),
-                                        pack_half2(mul_pow2(f0.z, -sp), mul_pow2(f0.w, -sp)),
-                                        pack_half2(mul_pow2(f1.x, -sp), mul_pow2(f1.y, -sp)),
-                                        pack_half2(mul_pow2(f1.z, -sp), mul_pow2(f1.w, -sp)));
+                const float4 f0 = hv[u][q][0], f1 = hv[u][q][1];
+                hr[u][q] = make_uint4(pack_half2(mul_pow2(f0.x, -sp), mul_pow2(f0.y, -sp)),
+                                      pack_half2(mul_pow2(f0.z, -sp), mul_pow2(f0.w, -sp)),
+                                      pack_half2(mul_pow2(f1.x, -sp), mul_pow2(f1.y, -sp)),
+                                      pack_half2(mul_pow2(f1.z, -sp), mul_pow2(f1.w, -sp)));
             }
+        }
         for (int sb = 0; sb < nstageB; sb++, s++) {
             const int slot = s % kSlots;
             const uint32_t ph = (uint32_t)(s / kSlots) & 1u;
@@ -358,24 +385,19 @@ __global__ void __launch_bounds__(kThreadsF, 1) decode_fused_kernel(const FusedA
             ok = !*(volatile int *)abort_flag && mbar_wait(&full[slot], ph, a.st, 0x400u + slot);
             if (!ok) *abort_flag = 1;
             float part[kMaxR] = {0.f, 0.f, 0.f, 0.f};
-            if (ok && pv) {
+            if (ok) {
                 const uint8_t *base = slots + (size_t)slot * a.slot_bytes;
 #pragma unroll
-                for (int r = 0; r < kMaxR; r++) {
-                    if (r >= nr) continue;
-                    const uint8_t *row = base + ((size_t)p * a.R + r) * v.ld_d;
-                    const uint8_t *srow =
-                        base + (size_t)k * a.R * v.ld_d + (size_t)p * a.sb_stride + soff + (size_t)r * v.lds_d;
-                    float dsum = 0.f;
+                for (int u = 0; u < 2; u++) {
+                    if (!pv[u]) continue;
+                    const uint8_t *row = base + (size_t)pb[u] * a.R * v.ld_d + kbs[u] * 16;
+                    const uint8_t *srow = base + (size_t)k * a.R * v.ld_d + (size_t)pb[u] * a.sb_stride + soff + kbs[u];
 #pragma unroll
-                    for (int blk = 0; blk < 2; blk++) {
-                        const int kb = lane + 32 * blk;
-                        if (kb < nkbd) {
-                            const uint4 q = *reinterpret_cast<const uint4 *>(row + kb * 16);
-                            dsum = fmaf(block_dot1(q, hr[blk]), e8m0_fast(srow[kb]), dsum);
-                        }
+                    for (int r = 0; r < kMaxR; r++) {
+                        if (r >= nr) continue;
+                        const uint4 q = *reinterpret_cast<const uint4 *>(row + (size_t)r * v.ld_d);
+                        part[r] = fmaf(wsc[u] * block_dot1(q, hr[u]), e8m0_fast(srow[(size_t)r * v.lds_d]), part[r]);
                     }
-                    part[r] = wsc * dsum;
                 }
             }
             __syncwarp();
@@ -450,7 +472,7 @@ cudaError_t launch_decode_fused(const PoolView &v, const uint16_t *x, const int3
     fa.slot_bytes = (slot_need + 127) / 128 * 128;
     const size_t smem = (size_t)kSlots * fa.slot_bytes + 2 * kSlots * sizeof(uint64_t) +
                         (size_t)kCW * kMaxRowsCta * sizeof(float) + (size_t)v.H * 2 +
-                        2 * kItems * 2 * sizeof(float2) + (2 * kMaxKF + 4) * sizeof(int);
+                        2 * kItems * 2 * sizeof(float2) + (4 * kMaxKF + 4) * sizeof(int);
     cudaError_t e = ensure_dynamic_smem(decode_fused_kernel, smem, g_smem_set);
     if (e != cudaSuccess) return e;
     if (g_grid < 0) {
