@@ -263,11 +263,13 @@ def run_ours(args):
     h2d = x_host.numel() * 2
     d2h = y_host.numel() * 2
 
-    # per-kernel device time over one more pass of the timed region (eager launches)
+    # per-kernel device time over one more pass of the timed region (eager launches
+    # queued behind a bounded sleep kernel, so the GPU never waits on the host)
     kern = {}
     for name in ("decode_fused", "route_single"):
         moe.moe_trace_begin(name)
         with torch.cuda.stream(stream):
+            torch.cuda._sleep(200_000_000)
             step()
         n, tot = moe.moe_trace_end()
         kern[name] = tot / max(n, 1)
@@ -329,6 +331,18 @@ def run_profile_case(args):
     import torch
     import mxfp4_routed_expert_topk_gb300 as moe
     moe.build()
+    if args.profile == "route":
+        # the router alone at the full shape (E=896, H=7168): 12.8 MB of W_r
+        s = synth.FULL
+        Wr = torch.from_numpy(synth.router_bf16(synth.router_seed(0), s.E, s.H).view(np.int16)).cuda()
+        Wr = Wr.view(torch.bfloat16)
+        xb = synth.tokens_bf16(synth.TOKENS_SEED["full"], 0, 4, s.H)
+        x = torch.from_numpy(xb.view(np.int16)).cuda().view(torch.bfloat16)
+        for t in range(4):
+            moe.moe_route_topk(x[t:t + 1], Wr, s.k)
+        torch.cuda.synchronize()
+        print("profile case done")
+        return
     s = synth.Shape(E=64, H=synth.FULL.H, I=synth.FULL.I, k=16)
     pool = moe.Pool(s.E, s.H, s.I)
     moe.moe_pool_fill_synthetic(pool, synth.pool_seed(0))
@@ -361,7 +375,7 @@ def main():
     ap.add_argument("--ref-tokens", type=int, default=16)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true", help="skip the expert-major prefill measurements")
-    ap.add_argument("--profile", choices=["decode", "prefill"], default=None,
+    ap.add_argument("--profile", choices=["decode", "prefill", "route"], default=None,
                     help="run a small case of the kernels for an ncu capture (no JSON line)")
     args = ap.parse_args()
     if args.profile:

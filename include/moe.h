@@ -109,7 +109,9 @@ moe_status moe_pool_download_expert(const moe_pool *pool, int e, uint8_t *codes_
  * rows.  The workspace is caller-owned device memory, 256-byte aligned; its
  * first 256 bytes hold the device status word and the kernels' own counters.
  * They must be zero before the first call on a workspace (moe_clear_status, or a
- * zero-filled allocation); the kernels leave them zero again after each call. */
+ * zero-filled allocation); the kernels leave them zero again after each call
+ * that succeeds.  After a call that recorded a device error (a bounded wait that
+ * expired, for instance) moe_check_status or moe_clear_status resets them. */
 moe_status moe_workspace_size(int op, int E, int H, int I, int rows, int k, size_t *bytes);
 
 /* Clear the status word of `ws` (asynchronously, on `stream`). */

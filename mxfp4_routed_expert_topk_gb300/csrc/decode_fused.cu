@@ -3,7 +3,7 @@
 // selected experts' packed MXFP4 weights is streamed from HBM exactly once).
 //
 //   phase A  g = W_g x, u = W_u x, h = silu(g) * u for every (slot, index) item;
-//            each CTA owns a contiguous range of the k*I items
+//            each CTA owns a contiguous range of units of 8 items (one stage each)
 //   grid barrier (h complete in global memory)
 //   phase B  y[o] = sum_j w_j (W_d,j h_j)[o] (+ residual) for this CTA's block of
 //            output rows, summed in a fixed order (deterministic, no atomics)
@@ -110,10 +110,10 @@ __global__ void __launch_bounds__(kThreadsF, 1) decode_fused_kernel(const FusedA
     float *s_wsc = reinterpret_cast<float *>(s_sp + kMaxKF);                 // [kMaxKF] w_p * 2^sp
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int b = blockIdx.x, G = a.G, k = a.k;
-    const int NA = k * v.I;
-    const int n_lo = (int)((long long)b * NA / G), n_hi = (int)((long long)(b + 1) * NA / G);
-    const int nitems = n_hi - n_lo;
-    const int nstageA = (nitems + kItems - 1) / kItems;
+    // I % 32 == 0: a unit of 8 items never straddles a pair or a 16-row group
+    const int nunits = k * v.I / kItems;
+    const int u_lo = (int)((long long)b * nunits / G), u_hi = (int)((long long)(b + 1) * nunits / G);
+    const int nstageA = u_hi - u_lo;
     const int o_lo = (int)((long long)b * v.H / G), o_hi = (int)((long long)(b + 1) * v.H / G);
     const int rows = o_hi - o_lo;
     const int nstageB = (rows + a.R - 1) / a.R;
@@ -138,65 +138,64 @@ __global__ void __launch_bounds__(kThreadsF, 1) decode_fused_kernel(const FusedA
 
     if (warp == kCW) {
         // -------------------------------------------------------------- producer
-        if (lane == 0) {
-            const uint64_t pol = policy_evict_first();
-            int issued = 0;
-            for (int s = 0; s < nstageA + nstageB; s++) {
-                const int slot = s % kSlots;
-                const uint32_t ph = (uint32_t)(s / kSlots) & 1u;
-                if (!mbar_wait(&empty[slot], ph ^ 1u, a.st, 0x100u + slot)) {
+        // Lane 0 waits for a free slot and posts the stage's byte count; the copies
+        // of the stage are then issued by several lanes at once (one per run in
+        // phase A, one per pair in phase B).
+        const uint64_t pol = policy_evict_first();
+        int issued = 0;
+        for (int s = 0; s < nstageA + nstageB; s++) {
+            const int slot = s % kSlots;
+            const uint32_t ph = (uint32_t)(s / kSlots) & 1u;
+            uint8_t *dst = slots + (size_t)slot * a.slot_bytes;
+            const bool isA = s < nstageA;
+            const int r0 = isA ? 0 : (s - nstageA) * a.R, nr = isA ? 0 : min(a.R, rows - r0);
+            // phase B scale rows: the 16-byte aligned span covering rows o_lo+r0 .. +nr
+            const uint64_t s_lo = (uint64_t)(o_lo + r0) * v.lds_d / 16 * 16;
+            const uint64_t s_hi = ((uint64_t)(o_lo + r0 + nr) * v.lds_d + 15) / 16 * 16;
+            const uint32_t sbytes = (uint32_t)(s_hi - s_lo);
+            int go = 1;
+            if (lane == 0) {
+                if (!mbar_wait(&empty[slot], ph ^ 1u, a.st, 0x100u + slot) || *(volatile int *)abort_flag) {
                     *abort_flag = 1;
-                    break;
-                }
-                if (*(volatile int *)abort_flag) break;
-                uint8_t *dst = slots + (size_t)slot * a.slot_bytes;
-                if (s < nstageA) {
-                    const int n0 = n_lo + kItems * s;
-                    const int cnt = min(kItems, n_hi - n0);
-                    mbar_arrive_expect_tx(&full[slot], (uint32_t)(cnt * 2 * (ldg + lsg)));
-                    // runs of consecutive items within one expert and one group of 16
-                    // rows are contiguous in the pool: 4 copies per run
-                    for (int j = 0; j < cnt;) {
-                        const int n = n0 + j;
-                        const int p = n / v.I, i = n % v.I;
-                        const int len = min(min(cnt - j, kGroupRows - i % kGroupRows), v.I - i);
-                        const int e = max(sidx[p], 0);  // invalid pairs: read expert 0, result discarded
-                        const uint8_t *rec = v.base + (uint64_t)e * v.rec;
-                        const int rg = 32 * (i / kGroupRows) + (i % kGroupRows);
-                        bulk_g2s(dst + (size_t)j * ldg, rec + (uint64_t)rg * ldg, (uint32_t)(len * ldg), &full[slot],
-                                 pol);
-                        bulk_g2s(dst + (size_t)(kItems + j) * ldg, rec + (uint64_t)(rg + kGroupRows) * ldg,
-                                 (uint32_t)(len * ldg), &full[slot], pol);
-                        const uint8_t *sr = rec + v.off_sgu;
-                        uint8_t *ds = dst + (size_t)2 * kItems * ldg;
-                        bulk_g2s(ds + (size_t)j * lsg, sr + (uint64_t)rg * lsg, (uint32_t)(len * lsg), &full[slot],
-                                 pol);
-                        bulk_g2s(ds + (size_t)(kItems + j) * lsg, sr + (uint64_t)(rg + kGroupRows) * lsg,
-                                 (uint32_t)(len * lsg), &full[slot], pol);
-                        j += len;
-                    }
+                    go = 0;
                 } else {
-                    const int r0 = (s - nstageA) * a.R, nr = min(a.R, rows - r0);
-                    // scale rows: the 16-byte aligned span covering rows o_lo+r0 .. +nr
-                    const uint64_t s_lo = (uint64_t)(o_lo + r0) * v.lds_d / 16 * 16;
-                    const uint64_t s_hi = ((uint64_t)(o_lo + r0 + nr) * v.lds_d + 15) / 16 * 16;
-                    const uint32_t sbytes = (uint32_t)(s_hi - s_lo);
-                    mbar_arrive_expect_tx(&full[slot], (uint32_t)(k * (nr * v.ld_d + sbytes)));
-                    for (int p = 0; p < k; p++) {
-                        const int e = max(sidx[p], 0);
-                        const uint8_t *rec = v.base + (uint64_t)e * v.rec;
-                        bulk_g2s(dst + (size_t)p * a.R * v.ld_d, rec + v.off_d + (uint64_t)(o_lo + r0) * v.ld_d,
-                                 (uint32_t)(nr * v.ld_d), &full[slot], pol);
-                        bulk_g2s(dst + (size_t)k * a.R * v.ld_d + (size_t)p * a.sb_stride, rec + v.off_sd + s_lo,
-                                 sbytes, &full[slot], pol);
-                    }
+                    mbar_arrive_expect_tx(&full[slot], isA ? (uint32_t)(kItems * 2 * (ldg + lsg))
+                                                           : (uint32_t)(k * (nr * v.ld_d + sbytes)));
                 }
-                issued = s + 1;
             }
-            // copies still in flight must land before this CTA can exit
-            for (int s = max(0, issued - kSlots); s < issued; s++)
-                mbar_wait(&full[s % kSlots], (uint32_t)(s / kSlots) & 1u, a.st, 0x180u);
+            if (__shfl_sync(0xffffffffu, go, 0) == 0) break;
+            if (isA) {
+                if (lane < 4) {
+                    // 8 consecutive gate rows (lane 0), the matching up rows (1) and
+                    // their scale runs (2, 3)
+                    const int n0 = (u_lo + s) * kItems;
+                    const int p = n0 / v.I, i = n0 % v.I;
+                    const int e = max(sidx[p], 0);  // invalid pairs: read expert 0, result discarded
+                    const uint8_t *rec = v.base + (uint64_t)e * v.rec;
+                    const int rg = 32 * (i / kGroupRows) + (i % kGroupRows) + (lane & 1) * kGroupRows;
+                    if (lane < 2)
+                        bulk_g2s(dst + (size_t)(lane & 1) * kItems * ldg, rec + (uint64_t)rg * ldg,
+                                 (uint32_t)(kItems * ldg), &full[slot], pol);
+                    else
+                        bulk_g2s(dst + (size_t)2 * kItems * ldg + (size_t)(lane & 1) * kItems * lsg,
+                                 rec + v.off_sgu + (uint64_t)rg * lsg, (uint32_t)(kItems * lsg), &full[slot], pol);
+                }
+            } else if (lane < k) {
+                const int p = lane;
+                const int e = max(sidx[p], 0);
+                const uint8_t *rec = v.base + (uint64_t)e * v.rec;
+                bulk_g2s(dst + (size_t)p * a.R * v.ld_d, rec + v.off_d + (uint64_t)(o_lo + r0) * v.ld_d,
+                         (uint32_t)(nr * v.ld_d), &full[slot], pol);
+                bulk_g2s(dst + (size_t)k * a.R * v.ld_d + (size_t)p * a.sb_stride, rec + v.off_sd + s_lo, sbytes,
+                         &full[slot], pol);
+            }
+            issued = s + 1;
         }
+        // copies still in flight must land before this CTA can exit
+        if (lane == 0)
+            for (int t = max(0, issued - kSlots); t < issued; t++)
+                mbar_wait(&full[t % kSlots], (uint32_t)(t / kSlots) & 1u, a.st, 0x180u);
+        __syncwarp();
         return;
     }
 
@@ -254,14 +253,9 @@ __global__ void __launch_bounds__(kThreadsF, 1) decode_fused_kernel(const FusedA
     for (; s < nstageA; s++) {
         const int slot = s % kSlots;
         const uint32_t ph = (uint32_t)(s / kSlots) & 1u;
-        const int n = n_lo + kItems * s + item;
-        int p = 0, i = 0;
-        bool valid = false;
-        if (n < n_hi) {
-            p = n / v.I;
-            i = n % v.I;
-            valid = sidx[p] >= 0;
-        }
+        const int n = (u_lo + s) * kItems + item;
+        const int p = n / v.I, i = n % v.I;
+        const bool valid = sidx[p] >= 0;
         ok = !*(volatile int *)abort_flag && mbar_wait(&full[slot], ph, a.st, 0x200u + slot);
         if (!ok) *abort_flag = 1;
         float ag = 0.f, au = 0.f;
