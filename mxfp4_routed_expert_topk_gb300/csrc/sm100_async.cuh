@@ -98,17 +98,26 @@ __device__ __forceinline__ unsigned int ld_acquire_gpu(const unsigned int *p) {
     return v;
 }
 
+__device__ __forceinline__ void red_release_gpu_add(unsigned int *p, unsigned int v) {
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
 // Grid-wide barrier among the CTAs of a cooperative launch, for the `nthreads`
 // threads of the calling CTA that take part (named barrier `bar_id`; thread 0 of
 // the CTA must be one of them).  The counter is zero before the launch; each of
 // the G CTAs adds 1.  A CTA that has aborted does not arrive; the others then give
 // up after kWaitLimitNs.  Returns false if this CTA aborted or timed out.
+//
+// Ordering: the CTA's writes before the barrier precede thread 0's release add
+// (CTA barrier, then release at GPU scope); thread 0's acquire load that sees the
+// full count precedes the CTA's reads after the barrier (acquire, then CTA
+// barrier).  Data written by other CTAs before the barrier must be read through
+// L2 afterwards (ld.global.cg or stronger), not through a possibly stale L1 line.
 __device__ __forceinline__ bool grid_barrier(unsigned int *counter, unsigned int G, int bar_id, int nthreads,
                                              StatusWord *st, unsigned where, int *abort_flag) {
     named_barrier(bar_id, nthreads);
     if (threadIdx.x == 0 && *(volatile int *)abort_flag == 0) {
-        __threadfence();
-        atomicAdd(counter, 1u);
+        red_release_gpu_add(counter, 1u);
         const uint64_t t0 = global_timer_ns();
         while (ld_acquire_gpu(counter) < G) {
             if (global_timer_ns() - t0 > kWaitLimitNs) {
@@ -117,7 +126,6 @@ __device__ __forceinline__ bool grid_barrier(unsigned int *counter, unsigned int
                 break;
             }
         }
-        __threadfence();
     }
     named_barrier(bar_id, nthreads);
     return (*(volatile int *)abort_flag) == 0;
