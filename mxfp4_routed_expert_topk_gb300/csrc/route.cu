@@ -64,7 +64,9 @@ __device__ __forceinline__ void unpack_bf16x8(const uint4 &v, float f[8]) {
 
 // Block (bx, by): experts 4*bx .. 4*bx+3 for tokens 8*by .. 8*by+7.  Warp w handles
 // expert 4*bx + w/2 over one half of H; lanes take 8 consecutive elements per step.
-// Used with 256 threads; x rows staged in dynamic shared memory.
+// Used with 256 threads; x rows staged in dynamic shared memory.  NB chunks of
+// W_r are loaded per batch (one batch covers H/2 = 4096 with NB = 16).
+template <int NB>
 __device__ void logits_block(const uint16_t *__restrict__ x, int M, int H, const uint16_t *__restrict__ Wr, int E,
                              const float *__restrict__ skew, float *__restrict__ logit,
                              float *__restrict__ bound) {
@@ -86,17 +88,17 @@ __device__ void logits_block(const uint16_t *__restrict__ x, int M, int H, const
     for (int t = 0; t < kLogitTokens; t++) acc[t] = accs[t] = 0.f;
     if (e < E) {
         const uint16_t *wrow = Wr + (size_t)e * H;
-        // batches of 8 chunks: all loads of a batch issued before any arithmetic;
+        // batches of NB chunks: all loads of a batch issued before any arithmetic;
         // chunks are still summed in increasing h (the order the bound assumes)
-        for (int hb = h0 + lane * 8; hb < h1; hb += 256 * 8) {
-            uint4 wv[8];
+        for (int hb = h0 + lane * 8; hb < h1; hb += 256 * NB) {
+            uint4 wv[NB];
 #pragma unroll
-            for (int c = 0; c < 8; c++) {
+            for (int c = 0; c < NB; c++) {
                 const int h = hb + 256 * c;
                 wv[c] = h < h1 ? __ldg(reinterpret_cast<const uint4 *>(wrow + h)) : make_uint4(0u, 0u, 0u, 0u);
             }
 #pragma unroll
-            for (int c = 0; c < 8; c++) {
+            for (int c = 0; c < NB; c++) {
                 const int h = hb + 256 * c;
                 if (h >= h1) break;
                 float wf[8];
@@ -157,7 +159,7 @@ __global__ void __launch_bounds__(256) route_logits_kernel(const uint16_t *__res
                                                            const uint16_t *__restrict__ Wr, int E,
                                                            const float *__restrict__ skew,
                                                            float *__restrict__ logit, float *__restrict__ bound) {
-    logits_block(x, M, H, Wr, E, skew, logit, bound);
+    logits_block<8>(x, M, H, Wr, E, skew, logit, bound);
 }
 
 // ------------------------------------------------------------ exact logits
@@ -299,7 +301,9 @@ __device__ void exact_logit(const uint16_t *xr, const uint16_t *wr, int H, const
 
 constexpr int kRouteThreads = 256;
 constexpr int kRouteWarps = kRouteThreads / 32;
-constexpr int kKeysPerThread = kMaxE / kRouteThreads;  // 16
+// Selection kernels are instantiated for J = 4, 8, 16 keys per thread (E up to
+// 1024, 2048, 4096).
+static_assert(16 * kRouteThreads == kMaxE, "the largest selection covers kMaxE experts");
 
 __device__ __forceinline__ unsigned int orderable(float f) {
     const unsigned int u = __float_as_uint(f);
@@ -381,6 +385,7 @@ struct SelectShared {
 // Exact top-k and softmax of one token (whole CTA of kRouteThreads threads).
 // lm / bm: the token's fp32 logits and bounds (read through L2: they may have
 // been written by other CTAs of the same kernel).
+template <int J>
 __device__ void select_token(int m, const uint16_t *__restrict__ x, int H, const uint16_t *__restrict__ Wr, int E,
                              const float *__restrict__ skew, int k, const float *lm, const float *bm,
                              int32_t *__restrict__ idx_out, float *__restrict__ w_out, StatusWord *st,
@@ -394,11 +399,11 @@ __device__ void select_token(int m, const uint16_t *__restrict__ x, int H, const
         s.nx = 0;
         s.Lord = 0xFFFFFFFFu;
     }
-    unsigned long long key[kKeysPerThread];
-    float lv[kKeysPerThread], bv[kKeysPerThread];
+    unsigned long long key[J];
+    float lv[J], bv[J];
     bool bad = false;
 #pragma unroll
-    for (int j = 0; j < kKeysPerThread; j++) {
+    for (int j = 0; j < J; j++) {
         const int e = tid + kRouteThreads * j;
         key[j] = 0ull;
         lv[j] = 0.f;
@@ -418,14 +423,14 @@ __device__ void select_token(int m, const uint16_t *__restrict__ x, int H, const
     {
         unsigned long long best = 0ull;
 #pragma unroll
-        for (int j = 0; j < kKeysPerThread; j++) best = key[j] > best ? key[j] : best;
+        for (int j = 0; j < J; j++) best = key[j] > best ? key[j] : best;
         for (int r = 0; r < q; r++) {
             const unsigned long long mx = warp_max_u64(best);
             if (lane == 0) s.wtop[warp][r] = mx;
             if (mx != 0ull && best == mx) {
                 best = 0ull;
 #pragma unroll
-                for (int j = 0; j < kKeysPerThread; j++) {
+                for (int j = 0; j < J; j++) {
                     if (key[j] == mx) key[j] = 0ull;
                     best = key[j] > best ? key[j] : best;
                 }
@@ -444,7 +449,7 @@ __device__ void select_token(int m, const uint16_t *__restrict__ x, int H, const
     // (2) gather every key at or above the threshold (slots by warp ballot)
     const unsigned long long thr = s.thr;
 #pragma unroll
-    for (int j = 0; j < kKeysPerThread; j++) {
+    for (int j = 0; j < J; j++) {
         const int e = tid + kRouteThreads * j;
         key[j] = e < E ? route_key(lv[j], e) : 0ull;  // restore what (1) cleared
         const bool take = key[j] != 0ull && key[j] >= thr;
@@ -477,7 +482,7 @@ __device__ void select_token(int m, const uint16_t *__restrict__ x, int H, const
         }
     } else {
         // many keys at the threshold: k rounds of warp maxima, then over the warps
-        warp_topk<kKeysPerThread>(key, k, s.wtop[warp]);
+        warp_topk<J>(key, k, s.wtop[warp]);
         __syncthreads();
         if (warp == 0) {
             constexpr int JW = kRouteWarps * kMaxK / 32;
@@ -505,7 +510,7 @@ __device__ void select_token(int m, const uint16_t *__restrict__ x, int H, const
     const unsigned int Lo = s.Lord;
     // outsiders whose upper bound reaches it; adjacent winners whose intervals meet
 #pragma unroll
-    for (int j = 0; j < kKeysPerThread; j++) {
+    for (int j = 0; j < J; j++) {
         const int e = tid + kRouteThreads * j;
         if (e < E && route_key(lv[j], e) < kth && orderable(__fadd_ru(lv[j], bv[j])) >= Lo) {
             const int slot = atomicAdd(&s.ncand, 1);
@@ -655,35 +660,61 @@ __device__ void select_token(int m, const uint16_t *__restrict__ x, int H, const
 }
 
 // One CTA per token.
+template <int J>
 __global__ void __launch_bounds__(kRouteThreads) route_select_kernel(
     const uint16_t *__restrict__ x, int H, const uint16_t *__restrict__ Wr, int E, const float *__restrict__ skew,
     int k, const float *__restrict__ logit, const float *__restrict__ bound, int32_t *__restrict__ idx_out,
     float *__restrict__ w_out, StatusWord *st) {
     __shared__ SelectShared s;
     const int m = blockIdx.x;
-    select_token(m, x, H, Wr, E, skew, k, logit + (size_t)m * E, bound + (size_t)m * E, idx_out, w_out, st, s);
+    select_token<J>(m, x, H, Wr, E, skew, k, logit + (size_t)m * E, bound + (size_t)m * E, idx_out, w_out, st, s);
 }
 
 // Single token: logits of 4 experts per CTA as in route_logits_kernel, then the
 // last CTA to finish (ticket in the status word, reset after use) selects.
+template <int J>
 __global__ void __launch_bounds__(kRouteThreads) route_single_kernel(
     const uint16_t *__restrict__ x, int H, const uint16_t *__restrict__ Wr, int E, const float *__restrict__ skew,
     int k, float *__restrict__ logit, float *__restrict__ bound, int32_t *__restrict__ idx_out,
     float *__restrict__ w_out, StatusWord *st) {
     __shared__ SelectShared s;
     __shared__ int last;
-    logits_block(x, 1, H, Wr, E, skew, logit, bound);
+    logits_block<16>(x, 1, H, Wr, E, skew, logit, bound);
     __syncthreads();
     if (threadIdx.x == 0) {
-        __threadfence();
-        const unsigned int t = atomicAdd(&st->pad[kStRouteTicket], 1u);
+        // release: this CTA's logits (ordered by the CTA barrier) before the
+        // ticket; acquire: every earlier CTA's logits after it
+        unsigned int t;
+        asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(t) : "l"(&st->pad[kStRouteTicket]) : "memory");
         last = (t == gridDim.x - 1);
     }
     __syncthreads();
     if (!last) return;
-    __threadfence();
-    select_token(0, x, H, Wr, E, skew, k, logit, bound, idx_out, w_out, st, s);
+    select_token<J>(0, x, H, Wr, E, skew, k, logit, bound, idx_out, w_out, st, s);
     if (threadIdx.x == 0) st->pad[kStRouteTicket] = 0u;
+}
+
+template <int J>
+cudaError_t launch_route_j(const uint16_t *x, int M, int H, const uint16_t *Wr, int E, const float *skew, int k,
+                           int32_t *idx, float *w, const RouteWs &r, size_t smem1, StatusWord *stw, cudaStream_t st) {
+    static int smem_single = 0;
+    dim3 g1((E + kLogitExperts - 1) / kLogitExperts, (M + kLogitTokens - 1) / kLogitTokens);
+    if (M == 1) {
+        cudaError_t e = ensure_dynamic_smem(route_single_kernel<J>, smem1, smem_single);
+        if (e != cudaSuccess) return e;
+        TraceScope trace_scope("route_single", st);
+        route_single_kernel<J><<<g1.x, kRouteThreads, smem1, st>>>(x, H, Wr, E, skew, k, r.logit, r.bound, idx, w, stw);
+        return cudaGetLastError();
+    }
+    {
+        TraceScope trace_scope("route_logits", st);
+        route_logits_kernel<<<g1, 256, smem1, st>>>(x, M, H, Wr, E, skew, r.logit, r.bound);
+    }
+    {
+        TraceScope trace_scope("route_select", st);
+        route_select_kernel<J><<<M, kRouteThreads, 0, st>>>(x, H, Wr, E, skew, k, r.logit, r.bound, idx, w, stw);
+    }
+    return cudaGetLastError();
 }
 
 }  // namespace
@@ -700,27 +731,13 @@ cudaError_t launch_route(const uint16_t *x, int M, int H, const uint16_t *Wr, in
     const int nt = M < kLogitTokens ? M : kLogitTokens;
     if ((size_t)nt * H * sizeof(uint16_t) > 200 * 1024) return cudaErrorInvalidValue;
     const size_t smem1 = (size_t)nt * H * sizeof(uint16_t);
-    static int smem_logits = 0, smem_single = 0;
+    static int smem_logits = 0;
     cudaError_t e = ensure_dynamic_smem(route_logits_kernel, smem1, smem_logits);
     if (e != cudaSuccess) return e;
-    e = ensure_dynamic_smem(route_single_kernel, smem1, smem_single);
-    if (e != cudaSuccess) return e;
     StatusWord *stw = reinterpret_cast<StatusWord *>(ws);
-    dim3 g1((E + kLogitExperts - 1) / kLogitExperts, (M + kLogitTokens - 1) / kLogitTokens);
-    if (M == 1) {
-        TraceScope trace_scope("route_single", st);
-        route_single_kernel<<<g1.x, kRouteThreads, smem1, st>>>(x, H, Wr, E, skew, k, r.logit, r.bound, idx, w, stw);
-        return cudaGetLastError();
-    }
-    {
-        TraceScope trace_scope("route_logits", st);
-        route_logits_kernel<<<g1, 256, smem1, st>>>(x, M, H, Wr, E, skew, r.logit, r.bound);
-    }
-    {
-        TraceScope trace_scope("route_select", st);
-        route_select_kernel<<<M, kRouteThreads, 0, st>>>(x, H, Wr, E, skew, k, r.logit, r.bound, idx, w, stw);
-    }
-    return cudaGetLastError();
+    if (E <= 4 * kRouteThreads) return launch_route_j<4>(x, M, H, Wr, E, skew, k, idx, w, r, smem1, stw, st);
+    if (E <= 8 * kRouteThreads) return launch_route_j<8>(x, M, H, Wr, E, skew, k, idx, w, r, smem1, stw, st);
+    return launch_route_j<16>(x, M, H, Wr, E, skew, k, idx, w, r, smem1, stw, st);
 }
 
 }  // namespace moe
