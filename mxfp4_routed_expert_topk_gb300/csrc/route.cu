@@ -213,6 +213,9 @@ struct ExactScratch {
     int tmax[32];
     int T0;
     int bad;
+    int any_bin;          // some term fell below the 128-bit window
+    int nnz;              // number of non-empty bins
+    short nzl[kBins];     // their exponents
 };
 
 // The exact logit of expert e for token row xr, as normalised limbs (thread 0 writes out).
@@ -222,7 +225,11 @@ __device__ void exact_logit(const uint16_t *xr, const uint16_t *wr, int H, const
                             ExactScratch &sc, long long *out) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     for (int i = tid; i < kBins; i += blockDim.x) sc.bins[i] = 0;
-    if (tid == 0) sc.bad = 0;
+    if (tid == 0) {
+        sc.bad = 0;
+        sc.any_bin = 0;
+        sc.nnz = 0;
+    }
     // skew term: fp32 = m * 2^(E'-150) = m * 2^(E'+118-268)
     int sk_neg = 0, sk_t = -1;
     unsigned int sk_m = 0;
@@ -234,14 +241,27 @@ __device__ void exact_logit(const uint16_t *xr, const uint16_t *wr, int H, const
         sk_t = sk_m ? (Es ? Es : 1) + 118 : -1;
         if (Es == 0xFF && tid == 0) sc.bad = 1;
     }
+    // rows read 4 elements (8 bytes) at a time: H % 8 == 0 and the rows start on
+    // 16-byte boundaries
+    const uint2 *xv = reinterpret_cast<const uint2 *>(xr);
+    const uint2 *wv = reinterpret_cast<const uint2 *>(wr);
+    const int H4 = H / 4;
     int tmax = (tid == 0) ? sk_t : -1;
-    for (int h = tid; h < H; h += blockDim.x) {
-        int n1, n2, e1, e2;
-        unsigned int m1, m2;
-        const bool ok = bf16_parts(xr[h], n1, m1, e1) & bf16_parts(wr[h], n2, m2, e2);
-        if (!ok) sc.bad = 1;
-        if (m1 && m2) tmax = max(tmax, e1 + e2);
+    bool bad = false;
+    for (int h4 = tid; h4 < H4; h4 += blockDim.x) {
+        const uint2 a = xv[h4], b = wv[h4];
+        const unsigned int av[4] = {a.x & 0xffffu, a.x >> 16, a.y & 0xffffu, a.y >> 16};
+        const unsigned int bv[4] = {b.x & 0xffffu, b.x >> 16, b.y & 0xffffu, b.y >> 16};
+#pragma unroll
+        for (int q = 0; q < 4; q++) {
+            int n1, n2, e1, e2;
+            unsigned int m1, m2;
+            const bool ok = bf16_parts((uint16_t)av[q], n1, m1, e1) & bf16_parts((uint16_t)bv[q], n2, m2, e2);
+            if (!ok) bad = true;
+            if (m1 && m2) tmax = max(tmax, e1 + e2);
+        }
     }
+    if (bad) sc.bad = 1;
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) tmax = max(tmax, __shfl_xor_sync(0xffffffffu, tmax, off));
     if (lane == 0) sc.tmax[warp] = tmax;
@@ -254,20 +274,28 @@ __device__ void exact_logit(const uint16_t *xr, const uint16_t *wr, int H, const
     __syncthreads();
     const int lo = max(sc.T0 - 63, 0);
     __int128 acc = 0;
-    for (int h = tid; h < H; h += blockDim.x) {
-        int n1, n2, e1, e2;
-        unsigned int m1, m2;
-        bf16_parts(xr[h], n1, m1, e1);
-        bf16_parts(wr[h], n2, m2, e2);
-        if (!(m1 && m2)) continue;
-        const int t = e1 + e2;
-        const long long p = (long long)(m1 * m2);
-        if (t >= lo) {
-            const __int128 v = (__int128)p << (t - lo);
-            acc += (n1 ^ n2) ? -v : v;
-        } else {
-            atomicAdd(reinterpret_cast<unsigned long long *>(&sc.bins[t]),
-                      (unsigned long long)((n1 ^ n2) ? -p : p));
+    bool binned = false;
+    for (int h4 = tid; h4 < H4; h4 += blockDim.x) {
+        const uint2 a = xv[h4], b = wv[h4];
+        const unsigned int av[4] = {a.x & 0xffffu, a.x >> 16, a.y & 0xffffu, a.y >> 16};
+        const unsigned int bv[4] = {b.x & 0xffffu, b.x >> 16, b.y & 0xffffu, b.y >> 16};
+#pragma unroll
+        for (int q = 0; q < 4; q++) {
+            int n1, n2, e1, e2;
+            unsigned int m1, m2;
+            bf16_parts((uint16_t)av[q], n1, m1, e1);
+            bf16_parts((uint16_t)bv[q], n2, m2, e2);
+            if (!(m1 && m2)) continue;
+            const int t = e1 + e2;
+            const long long p = (long long)(m1 * m2);
+            if (t >= lo) {
+                const __int128 v = (__int128)p << (t - lo);
+                acc += (n1 ^ n2) ? -v : v;
+            } else {
+                atomicAdd(reinterpret_cast<unsigned long long *>(&sc.bins[t]),
+                          (unsigned long long)((n1 ^ n2) ? -p : p));
+                binned = true;
+            }
         }
     }
     if (tid == 0 && sk_t >= 0) {
@@ -277,11 +305,20 @@ __device__ void exact_logit(const uint16_t *xr, const uint16_t *wr, int H, const
         } else {
             atomicAdd(reinterpret_cast<unsigned long long *>(&sc.bins[sk_t]),
                       (unsigned long long)(sk_neg ? -(long long)sk_m : (long long)sk_m));
+            binned = true;
         }
     }
+    if (binned) sc.any_bin = 1;
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) acc += shfl_xor_i128(acc, off);
     if (lane == 0) sc.part[warp] = acc;
+    __syncthreads();
+    // the non-empty bins below the window, found in parallel (exact integer sums:
+    // the order they are added in does not matter)
+    if (sc.any_bin) {
+        for (int t = tid; t < lo; t += blockDim.x)
+            if (sc.bins[t] != 0) sc.nzl[atomicAdd(&sc.nnz, 1)] = (short)t;
+    }
     __syncthreads();
     if (tid == 0) {
         __int128 tot = 0;
@@ -289,8 +326,10 @@ __device__ void exact_logit(const uint16_t *xr, const uint16_t *wr, int H, const
         for (int i = 0; i < kLimbs; i++) out[i] = 0;
         if (sc.T0 >= 0) {
             limbs_add_shifted(out, tot, lo);
-            for (int t = 0; t < lo; t++)
-                if (sc.bins[t] != 0) limbs_add_shifted(out, (__int128)sc.bins[t], t);
+            for (int q = 0; q < sc.nnz; q++) {
+                const int t = sc.nzl[q];
+                limbs_add_shifted(out, (__int128)sc.bins[t], t);
+            }
         }
         limbs_normalise(out);
     }
@@ -375,6 +414,7 @@ struct SelectShared {
     int overflow;
     int nx;
     int aexp[kMaxCand + kMaxK];                   // candidate set ordered by upper bound
+    float aup[kMaxCand + kMaxK], alo[kMaxCand + kMaxK];  // its interval ends (staged)
     int comp[kMaxCand + kMaxK];                   // interval-cluster id
     int xlist[kMaxExact];                         // experts evaluated exactly
     long long exact[kMaxExact][kLimbs];
@@ -545,31 +585,46 @@ __device__ void select_token(int m, const uint16_t *__restrict__ x, int H, const
             int n = 0;
             for (int p = 0; p < k; p++) s.aexp[n++] = key_expert(s.top[p]);
             for (int c = 0; c < nc; c++) s.aexp[n++] = s.cand[c];
+            s.ncand = n;  // from here on the size of aexp
+        }
+        __syncthreads();
+        // every candidate's interval ends, staged in shared memory by all threads
+        for (int i = tid; i < s.ncand; i += kRouteThreads) {
+            const int e = s.aexp[i];
+            s.aup[i] = __fadd_ru(L_(e), B_(e));
+            s.alo[i] = __fsub_rd(L_(e), B_(e));
+        }
+        __syncthreads();
+        if (tid == 0) {
+            const int n = s.ncand;
             // insertion sort by upper bound descending (ties: lower index first)
             for (int i = 1; i < n; i++) {
                 const int e = s.aexp[i];
-                const float ue = __fadd_ru(L_(e), B_(e));
+                const float ue = s.aup[i], le = s.alo[i];
                 int j = i - 1;
                 while (j >= 0) {
                     const int f = s.aexp[j];
-                    const float uf = __fadd_ru(L_(f), B_(f));
+                    const float uf = s.aup[j];
                     if (uf > ue || (uf == ue && f < e)) break;
                     s.aexp[j + 1] = f;
+                    s.aup[j + 1] = uf;
+                    s.alo[j + 1] = s.alo[j];
                     j--;
                 }
                 s.aexp[j + 1] = e;
+                s.aup[j + 1] = ue;
+                s.alo[j + 1] = le;
             }
             // connected components of the interval graph, in order
             int cid = 0;
-            float run_lo = __fsub_rd(L_(s.aexp[0]), B_(s.aexp[0]));
+            float run_lo = s.alo[0];
             s.comp[0] = 0;
             for (int i = 1; i < n; i++) {
-                const int e = s.aexp[i];
-                if (__fadd_ru(L_(e), B_(e)) >= run_lo) {
-                    run_lo = fminf(run_lo, __fsub_rd(L_(e), B_(e)));
+                if (s.aup[i] >= run_lo) {
+                    run_lo = fminf(run_lo, s.alo[i]);
                 } else {
                     cid++;
-                    run_lo = __fsub_rd(L_(e), B_(e));
+                    run_lo = s.alo[i];
                 }
                 s.comp[i] = cid;
             }
@@ -588,7 +643,6 @@ __device__ void select_token(int m, const uint16_t *__restrict__ x, int H, const
                 i = j;
             }
             s.nx = nx;
-            s.ncand = n;  // now the size of aexp
         }
         __syncthreads();
         const uint16_t *xr = x + (size_t)m * H;
