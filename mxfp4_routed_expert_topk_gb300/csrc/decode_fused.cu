@@ -16,6 +16,8 @@
 // power of two; in phase B the warp's h in registers), then the block sum is
 // scaled by its E8M0 factor in fp32.  Phase A gives each (gate row, up row) item
 // to a pair of warps, phase B each selected expert to one warp.
+#include <algorithm>
+
 #include "moe_internal.cuh"
 #include "sm100_async.cuh"
 
@@ -46,6 +48,9 @@ struct FusedArgs {
     uint32_t slot_bytes;
     int R;
     uint32_t sb_stride;  // bytes per pair of phase-B scale rows in a slot
+    uint32_t sp_stride;  // != 0: all of a CTA's W_d scale rows are preloaded once, this
+                         // many bytes per pair (else each phase-B stage carries its own)
+    uint32_t tail_bytes; // the token / preloaded-scale region (a multiple of 16)
 };
 
 // 32 E2M1 elements (16 bytes) times the matching f16x2 input block: 16 packed f16
@@ -99,10 +104,15 @@ __global__ void __launch_bounds__(kThreadsF, 1) decode_fused_kernel(const FusedA
     uint8_t *slots = smem;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)kSlots * a.slot_bytes);
     uint64_t *empty = full + kSlots;
+    uint64_t *fullS = empty + kSlots;  // the preloaded W_d scale rows (8 barriers: 64 bytes)
     // (slots are a multiple of 128 bytes; every region below starts 16-byte aligned)
-    float *red = reinterpret_cast<float *>(empty + kSlots);             // [kCW][kMaxRowsCta]
-    uint4 *xsm = reinterpret_cast<uint4 *>(red + kCW * kMaxRowsCta);    // the token, f16: [4][H/32] x 8
-    float2 *pairsum = reinterpret_cast<float2 *>(xsm + v.H / 8);        // [2][kItems][2] half sums
+    float *red = reinterpret_cast<float *>(full + 8);                   // [kCW][kMaxRowsCta]
+    // phase A: the token, f16 [4][H/32] x 8; phase B (once the last phase-A stage has
+    // been released): the preloaded W_d scale rows, [pair][sp_stride]
+    uint8_t *tail = reinterpret_cast<uint8_t *>(red + kCW * kMaxRowsCta);
+    uint4 *xsm = reinterpret_cast<uint4 *>(tail);
+    const uint8_t *spre = tail;
+    float2 *pairsum = reinterpret_cast<float2 *>(tail + a.tail_bytes);  // [2][kItems][2] half sums
     int *sidx = reinterpret_cast<int *>(pairsum + 2 * kItems * 2);      // [kMaxKF]
     int *abort_flag = sidx + kMaxKF;
     unsigned int *samax = reinterpret_cast<unsigned int *>(abort_flag + 1);  // [kMaxKF] max |h| per pair
@@ -124,6 +134,7 @@ __global__ void __launch_bounds__(kThreadsF, 1) decode_fused_kernel(const FusedA
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], kCW);
         }
+        mbar_init(fullS, 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -143,58 +154,96 @@ __global__ void __launch_bounds__(kThreadsF, 1) decode_fused_kernel(const FusedA
         // phase A, one per pair in phase B).
         const uint64_t pol = policy_evict_first();
         int issued = 0;
-        for (int s = 0; s < nstageA + nstageB; s++) {
+        bool run = true;
+        // phase A: one unit (8 gate rows, 8 up rows, their scale runs) per stage
+        for (int s = 0; s < nstageA; s++) {
             const int slot = s % kSlots;
             const uint32_t ph = (uint32_t)(s / kSlots) & 1u;
-            uint8_t *dst = slots + (size_t)slot * a.slot_bytes;
-            const bool isA = s < nstageA;
-            const int r0 = isA ? 0 : (s - nstageA) * a.R, nr = isA ? 0 : min(a.R, rows - r0);
-            // phase B scale rows: the 16-byte aligned span covering rows o_lo+r0 .. +nr
-            const uint64_t s_lo = (uint64_t)(o_lo + r0) * v.lds_d / 16 * 16;
-            const uint64_t s_hi = ((uint64_t)(o_lo + r0 + nr) * v.lds_d + 15) / 16 * 16;
-            const uint32_t sbytes = (uint32_t)(s_hi - s_lo);
             int go = 1;
             if (lane == 0) {
                 if (!mbar_wait(&empty[slot], ph ^ 1u, a.st, 0x100u + slot) || *(volatile int *)abort_flag) {
                     *abort_flag = 1;
                     go = 0;
                 } else {
-                    mbar_arrive_expect_tx(&full[slot], isA ? (uint32_t)(kItems * 2 * (ldg + lsg))
-                                                           : (uint32_t)(k * (nr * v.ld_d + sbytes)));
+                    mbar_arrive_expect_tx(&full[slot], (uint32_t)(kItems * 2 * (ldg + lsg)));
+                }
+            }
+            if (__shfl_sync(0xffffffffu, go, 0) == 0) {
+                run = false;
+                break;
+            }
+            if (lane < 4) {
+                // 8 consecutive gate rows (lane 0), the matching up rows (1) and
+                // their scale runs (2, 3)
+                uint8_t *dst = slots + (size_t)slot * a.slot_bytes;
+                const int n0 = (u_lo + s) * kItems;
+                const int p = n0 / v.I, i = n0 % v.I;
+                const int e = max(sidx[p], 0);  // invalid pairs: read expert 0, result discarded
+                const uint8_t *rec = v.base + (uint64_t)e * v.rec;
+                const int rg = 32 * (i / kGroupRows) + (i % kGroupRows) + (lane & 1) * kGroupRows;
+                if (lane < 2)
+                    bulk_g2s(dst + (size_t)(lane & 1) * kItems * ldg, rec + (uint64_t)rg * ldg,
+                             (uint32_t)(kItems * ldg), &full[slot], pol);
+                else
+                    bulk_g2s(dst + (size_t)2 * kItems * ldg + (size_t)(lane & 1) * kItems * lsg,
+                             rec + v.off_sgu + (uint64_t)rg * lsg, (uint32_t)(kItems * lsg), &full[slot], pol);
+            }
+            issued = s + 1;
+        }
+        // phase B: R rows of W_d of every pair per stage.  The scale rows of all this
+        // CTA's output rows are preloaded with stage 2 (or the last one if there are
+        // fewer): by then the last phase-A stage, the last reader of the token
+        // region they overwrite, has been released.
+        const int spre_at = a.sp_stride != 0 ? min(2, nstageB - 1) : -1;
+        const uint64_t p_lo = (uint64_t)o_lo * v.lds_d / 16 * 16;
+        const uint32_t pbytes = (uint32_t)(((uint64_t)o_hi * v.lds_d + 15) / 16 * 16 - p_lo);
+        for (int sb = 0; run && sb < nstageB; sb++) {
+            const int s = nstageA + sb;
+            const int slot = s % kSlots;
+            const uint32_t ph = (uint32_t)(s / kSlots) & 1u;
+            const int r0 = sb * a.R, nr = min(a.R, rows - r0);
+            // per-stage scale rows: the 16-byte aligned span covering rows o_lo+r0 .. +nr
+            const uint64_t s_lo = (uint64_t)(o_lo + r0) * v.lds_d / 16 * 16;
+            const uint64_t s_hi = ((uint64_t)(o_lo + r0 + nr) * v.lds_d + 15) / 16 * 16;
+            const uint32_t sbytes = a.sp_stride != 0 ? 0u : (uint32_t)(s_hi - s_lo);
+            const bool pre = sb == spre_at;
+            int go = 1;
+            if (lane == 0) {
+                bool okw = mbar_wait(&empty[slot], ph ^ 1u, a.st, 0x100u + slot);
+                if (okw && pre && nstageA > 0) {
+                    const int sl = nstageA - 1;  // nothing has reused its slot yet
+                    okw = mbar_wait(&empty[sl % kSlots], (uint32_t)(sl / kSlots) & 1u, a.st, 0x140u);
+                }
+                if (!okw || *(volatile int *)abort_flag) {
+                    *abort_flag = 1;
+                    go = 0;
+                } else {
+                    if (pre) mbar_arrive_expect_tx(fullS, (uint32_t)k * pbytes);
+                    mbar_arrive_expect_tx(&full[slot], (uint32_t)(k * (nr * v.ld_d + sbytes)));
                 }
             }
             if (__shfl_sync(0xffffffffu, go, 0) == 0) break;
-            if (isA) {
-                if (lane < 4) {
-                    // 8 consecutive gate rows (lane 0), the matching up rows (1) and
-                    // their scale runs (2, 3)
-                    const int n0 = (u_lo + s) * kItems;
-                    const int p = n0 / v.I, i = n0 % v.I;
-                    const int e = max(sidx[p], 0);  // invalid pairs: read expert 0, result discarded
-                    const uint8_t *rec = v.base + (uint64_t)e * v.rec;
-                    const int rg = 32 * (i / kGroupRows) + (i % kGroupRows) + (lane & 1) * kGroupRows;
-                    if (lane < 2)
-                        bulk_g2s(dst + (size_t)(lane & 1) * kItems * ldg, rec + (uint64_t)rg * ldg,
-                                 (uint32_t)(kItems * ldg), &full[slot], pol);
-                    else
-                        bulk_g2s(dst + (size_t)2 * kItems * ldg + (size_t)(lane & 1) * kItems * lsg,
-                                 rec + v.off_sgu + (uint64_t)rg * lsg, (uint32_t)(kItems * lsg), &full[slot], pol);
-                }
-            } else if (lane < k) {
+            if (lane < k) {
                 const int p = lane;
                 const int e = max(sidx[p], 0);
                 const uint8_t *rec = v.base + (uint64_t)e * v.rec;
+                if (pre) bulk_g2s(tail + (size_t)p * a.sp_stride, rec + v.off_sd + p_lo, pbytes, fullS, pol);
+                uint8_t *dst = slots + (size_t)slot * a.slot_bytes;
                 bulk_g2s(dst + (size_t)p * a.R * v.ld_d, rec + v.off_d + (uint64_t)(o_lo + r0) * v.ld_d,
                          (uint32_t)(nr * v.ld_d), &full[slot], pol);
-                bulk_g2s(dst + (size_t)k * a.R * v.ld_d + (size_t)p * a.sb_stride, rec + v.off_sd + s_lo, sbytes,
-                         &full[slot], pol);
+                if (sbytes != 0)
+                    bulk_g2s(dst + (size_t)k * a.R * v.ld_d + (size_t)p * a.sb_stride, rec + v.off_sd + s_lo, sbytes,
+                             &full[slot], pol);
             }
             issued = s + 1;
         }
         // copies still in flight must land before this CTA can exit
-        if (lane == 0)
+        if (lane == 0) {
             for (int t = max(0, issued - kSlots); t < issued; t++)
                 mbar_wait(&full[t % kSlots], (uint32_t)(t / kSlots) & 1u, a.st, 0x180u);
+            if (a.sp_stride != 0 && nstageB > 0 && issued - nstageA > min(2, nstageB - 1))
+                mbar_wait(fullS, 0u, a.st, 0x1a0u);
+        }
         __syncwarp();
         return;
     }
@@ -371,7 +420,13 @@ __global__ void __launch_bounds__(kThreadsF, 1) decode_fused_kernel(const FusedA
                                       pack_half2(mul_pow2(f1.z, -sp), mul_pow2(f1.w, -sp)));
             }
         }
-        for (int sb = 0; sb < nstageB; sb++, s++) {
+        // the preloaded scale rows (one wait per launch)
+        if (a.sp_stride != 0 && nstageB > 0) {
+            ok = !*(volatile int *)abort_flag && mbar_wait(fullS, 0u, a.st, 0x3a0u);
+            if (!ok) *abort_flag = 1;
+        }
+        const int soffP = (int)((uint64_t)o_lo * v.lds_d % 16);
+        for (int sb = 0; sb < nstageB; sb++, s++) {  // every lane runs every stage (warp shuffles below)
             const int slot = s % kSlots;
             const uint32_t ph = (uint32_t)(s / kSlots) & 1u;
             const int r0 = sb * a.R, nr = min(a.R, rows - r0);
@@ -385,7 +440,9 @@ __global__ void __launch_bounds__(kThreadsF, 1) decode_fused_kernel(const FusedA
                 for (int u = 0; u < 2; u++) {
                     if (!pv[u]) continue;
                     const uint8_t *row = base + (size_t)pb[u] * a.R * v.ld_d + kbs[u] * 16;
-                    const uint8_t *srow = base + (size_t)k * a.R * v.ld_d + (size_t)pb[u] * a.sb_stride + soff + kbs[u];
+                    const uint8_t *srow = a.sp_stride != 0
+                                              ? spre + (size_t)pb[u] * a.sp_stride + soffP + (size_t)r0 * v.lds_d + kbs[u]
+                                              : base + (size_t)k * a.R * v.ld_d + (size_t)pb[u] * a.sb_stride + soff + kbs[u];
 #pragma unroll
                     for (int r = 0; r < kMaxR; r++) {
                         if (r >= nr) continue;
@@ -427,6 +484,7 @@ __global__ void __launch_bounds__(kThreadsF, 1) decode_fused_kernel(const FusedA
 }
 
 int g_sms = 0;
+int g_smem_max = 0;
 int g_grid = -1;   // co-resident CTAs of the fused kernel (0: unusable)
 int g_smem_set = 0;
 
@@ -464,9 +522,22 @@ cudaError_t launch_decode_fused(const PoolView &v, const uint16_t *x, const int3
     fa.sb_stride = sb_of(R);
     const uint32_t slot_need = slotA > stageB(R) ? slotA : stageB(R);
     fa.slot_bytes = (slot_need + 127) / 128 * 128;
-    const size_t smem = (size_t)kSlots * fa.slot_bytes + 2 * kSlots * sizeof(uint64_t) +
-                        (size_t)kCW * kMaxRowsCta * sizeof(float) + (size_t)v.H * 2 +
+    if (g_smem_max == 0) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&g_smem_max, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    }
+    // everything but the token / preloaded-scale region
+    const size_t head = (size_t)kSlots * fa.slot_bytes + 8 * sizeof(uint64_t) + (size_t)kCW * kMaxRowsCta * sizeof(float) +
                         2 * kItems * 2 * sizeof(float2) + (4 * kMaxKF + 4) * sizeof(int);
+    // the W_d scale rows of a CTA's output rows (at most ceil(H / SMs) of them), one
+    // 16-byte aligned span per pair, if they fit in shared memory
+    const int rows_max = (v.H + g_sms - 1) / g_sms;
+    const uint32_t sp = (uint32_t)((rows_max * v.lds_d + 15) / 16 * 16 + 32);
+    const size_t tok = (size_t)v.H * 2;
+    fa.sp_stride = head + std::max(tok, (size_t)k * sp) <= (size_t)g_smem_max ? sp : 0u;
+    fa.tail_bytes = (uint32_t)std::max(tok, (size_t)k * fa.sp_stride);
+    const size_t smem = head + fa.tail_bytes;
     cudaError_t e = ensure_dynamic_smem(decode_fused_kernel, smem, g_smem_set);
     if (e != cudaSuccess) return e;
     if (g_grid < 0) {
