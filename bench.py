@@ -175,6 +175,119 @@ def measure_prefill(moe, torch, pool, Wr, dev, T, iters=3):
             "gemm_tflops": flops / ((kern["gemm_gateup"] + kern["gemm_down"]) / 1000.0) / 1e12}
 
 
+def measure_verify(moe, torch, pool, Wr, dev, M, nbatch=50, iters=3):
+    """Multi-token verify on the full-size layer: nbatch seeded batches of M correlated
+    rows, each routed and run through the experts (every distinct selected expert
+    read once and applied to all its rows).  One CUDA graph over all batches."""
+    s = synth.FULL
+    xb = np.stack([synth.verify_batch_bf16(synth.TOKENS_SEED["verify"], b, M, s.H) for b in range(nbatch)])
+    x = torch.from_numpy(xb.view(np.int16)).to(dev).view(torch.bfloat16)
+    idx = torch.empty((nbatch, M, s.k), dtype=torch.int32, device=dev)
+    w = torch.empty((nbatch, M, s.k), dtype=torch.float32, device=dev)
+    y = torch.empty((nbatch, M, s.H), dtype=torch.bfloat16, device=dev)
+    ws_r = moe.workspace(moe.moe_workspace_size(moe.MOE_OP_ROUTE, s.E, s.H, s.I, M, s.k), dev)
+    ws_d = moe.workspace(moe.moe_workspace_size(moe.MOE_OP_DECODE, s.E, s.H, s.I, M, s.k), dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    def step():
+        for b in range(nbatch):
+            moe.moe_route_topk(x[b], Wr, s.k, ws=ws_r, idx=idx[b], w=w[b])
+            moe.moe_expert_forward_decode(pool, x[b], idx[b], w[b], ws=ws_d, y=y[b])
+
+    with torch.cuda.stream(stream):
+        step()
+        torch.cuda.synchronize()
+        sd, sr = moe.moe_check_status(ws_d), moe.moe_check_status(ws_r)
+        if sd != 0 or sr != 0:
+            raise RuntimeError(f"verify M={M}: decode status {moe.status_string(sd)}, route status {moe.status_string(sr)}")
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            step()
+    torch.cuda.synchronize()
+    union = float(np.mean([len(np.unique(a)) for a in idx.cpu().numpy().reshape(nbatch, -1)]))
+    graph.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(iters):
+            graph.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1000.0 / (iters * nbatch)
+    kern = {}
+    for name in ("route_logits", "route_select", "sort_small", "gather_split", "gemm_gateup", "gemm_down",
+                 "combine"):
+        moe.moe_trace_begin(name)
+        with torch.cuda.stream(stream):
+            torch.cuda._sleep(50_000_000)
+            step()
+        n, tot = moe.moe_trace_end()
+        torch.cuda.synchronize()  # the side stream's work is done before its tensors are freed
+        if n:
+            kern[name] = tot / n
+    nbytes = union * expert_bytes(s.H, s.I) + s.E * s.H * 2
+    hbm, _ = peaks()
+    return {"us_per_batch": us, "rows_per_s": M / (us * 1e-6), "mean_union_experts": union,
+            "bytes_per_batch": nbytes, "hbm_gbs": nbytes / (us * 1e-6) / 1e9,
+            "hbm_frac": nbytes / (us * 1e-6) / 1e9 / hbm, "kernel_ms": kern}
+
+
+def measure_stacked(moe, torch, pool0, dev, ntok=64, L=8, iters=2):
+    """Eight stacked layers (each its own pool, router and Zipf skew), one token at a
+    time: per layer x_hat = prescale(x), route(x_hat), x = x + MoE(x_hat).  Reports
+    layer-tokens/s.  Allocates L - 1 more full-size pools."""
+    s = synth.FULL
+    pools = [pool0]
+    for l in range(1, L):
+        p = moe.Pool(s.E, s.H, s.I, device=dev)
+        moe.moe_pool_fill_synthetic(p, synth.pool_seed(l))
+        pools.append(p)
+    Wrs = [torch.from_numpy(synth.router_bf16(synth.router_seed(l), s.E, s.H).view(np.int16)).to(dev)
+           .view(torch.bfloat16) for l in range(L)]
+    skews = [torch.from_numpy(synth.zipf_skew_f32(synth.skew_seed(l), s.E)).to(dev) for l in range(L)]
+    xb = synth.tokens_bf16(synth.TOKENS_SEED["stacked"], 0, ntok, s.H)
+    xs = [torch.from_numpy(xb.view(np.int16)).to(dev).view(torch.bfloat16)]
+    xs += [torch.empty_like(xs[0]) for _ in range(L)]
+    xh = torch.empty((1, s.H), dtype=torch.bfloat16, device=dev)
+    idx = torch.empty((1, s.k), dtype=torch.int32, device=dev)
+    w = torch.empty((1, s.k), dtype=torch.float32, device=dev)
+    ws_r = moe.workspace(moe.moe_workspace_size(moe.MOE_OP_ROUTE, s.E, s.H, s.I, 1, s.k), dev)
+    ws_d = moe.workspace(moe.moe_workspace_size(moe.MOE_OP_DECODE, s.E, s.H, s.I, 1, s.k), dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    def step():
+        for t in range(ntok):
+            for l in range(L):
+                moe.moe_prescale(xs[l][t:t + 1], out=xh)
+                moe.moe_route_topk(xh, Wrs[l], s.k, skews[l], ws=ws_r, idx=idx, w=w)
+                moe.moe_expert_forward_decode(pools[l], xh, idx, w, residual=xs[l][t:t + 1], ws=ws_d,
+                                              y=xs[l + 1][t:t + 1])
+
+    with torch.cuda.stream(stream):
+        step()
+        torch.cuda.synchronize()
+        assert moe.moe_check_status(ws_d) == 0 and moe.moe_check_status(ws_r) == 0
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            step()
+    torch.cuda.synchronize()
+    graph.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(iters):
+            graph.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    sec = e0.elapsed_time(e1) / 1000.0 / iters
+    per_layer = s.k * expert_bytes(s.H, s.I) + s.E * s.H * 2
+    del pools[1:]
+    return {"tokens": ntok, "layers": L, "layer_tokens_per_s": ntok * L / sec,
+            "us_per_layer_token": sec * 1e6 / (ntok * L), "hbm_gbs": ntok * L * per_layer / sec / 1e9}
+
+
 def run_ours(args):
     import torch
     import mxfp4_routed_expert_topk_gb300 as moe
@@ -299,6 +412,11 @@ def run_ours(args):
     if not args.no_prefill:
         for T in synth.PREFILL_T:
             prefill[str(T)] = measure_prefill(moe, torch, pool, Wr, dev, T)
+    verify, stacked = {}, None
+    if not args.no_extra:
+        for M in synth.VERIFY_M:
+            verify[str(M)] = measure_verify(moe, torch, pool, Wr, dev, M)
+        stacked = measure_stacked(moe, torch, pool, dev)
     if rank == 0:
         print(json.dumps({
             "metric": METRIC, "value": value, "unit": "layer-tokens/s", "n_gpus": world, "steps": args.steps,
@@ -318,6 +436,8 @@ def run_ours(args):
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": launches,
             "prefill": prefill,
+            "verify": verify,
+            "stacked_8_layers": stacked,
             "clocks": clk.summary(),
         }))
     if dist is not None:
@@ -375,6 +495,8 @@ def main():
     ap.add_argument("--ref-tokens", type=int, default=16)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true", help="skip the expert-major prefill measurements")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the multi-token verify and 8-layer stacked measurements")
     ap.add_argument("--profile", choices=["decode", "prefill", "route"], default=None,
                     help="run a small case of the kernels for an ncu capture (no JSON line)")
     args = ap.parse_args()

@@ -161,7 +161,13 @@ moe_status moe_route_topk_static(const uint16_t *x, int M, int H, const uint16_t
  * routed to it (the pages' speculative-verify batch, "可选的 Qwen 扩展").
  * x [M][H] bf16, idx/w [M][k] as from moe_route_topk, residual [M][H] bf16 or
  * NULL.  Out: y [M][H] bf16 = sum_j w[m,j] * expert_{idx[m,j]}(x[m]) (+ residual),
- * fp32 accumulation, rounded to nearest-even.  ws: MOE_OP_DECODE bytes. */
+ * fp32 accumulation, rounded to nearest-even.  ws: MOE_OP_DECODE bytes.
+ * M = 1 runs on the CUDA cores (E2M1 -> f16 dequantisation, f16 products summed
+ * per 32-element block, then fp32).  M > 1 runs on the tensor cores when I is a
+ * multiple of 64: each activation block is written as the sum of three E4M3
+ * parts with their own E8M0 scales (exact for bf16 elements within about 20
+ * binades of their block's max), multiplied with the E2M1 weights in
+ * block-scaled MMAs with fp32 accumulation; h is split the same way for W_d. */
 moe_status moe_expert_forward_decode(const moe_pool *pool, const uint16_t *x, int M,
                                      const int32_t *idx, const float *w, int k,
                                      const uint16_t *residual, uint16_t *y,
@@ -198,9 +204,10 @@ moe_status moe_combine(const void *partial, int partial_dtype, const int32_t *in
 
 /* ----------------------------------------------------------------- tracing
  * Between moe_trace_begin(name) and moe_trace_end(), every launch of the named
- * kernel ("route_logits", "route_select", "decode_prep", "decode_gateup",
- * "decode_down", "sort_rank", "sort_scan", "sort_scatter", "gather_quant",
- * "gemm_gateup", "gemm_down", "combine", "prescale") is bracketed by CUDA events
+ * kernel ("route_single", "route_logits", "route_select", "decode_fused",
+ * "decode_prep", "decode_gateup", "decode_down", "sort_rank", "sort_scan",
+ * "sort_scatter", "sort_small", "gather_quant", "gather_split", "gemm_gateup", "gemm_down",
+ * "combine", "prescale") is bracketed by CUDA events
  * on its stream (at most 65536 launches are recorded).  moe_trace_end()
  * synchronises the device and returns the number of recorded launches and their
  * summed device time in milliseconds.  Tracing is process-wide and not

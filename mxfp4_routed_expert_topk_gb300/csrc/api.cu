@@ -86,8 +86,9 @@ moe_status moe_trace_end(int *launches, double *total_ms) {
     g_trace.on = false;
     *launches = g_trace.n;
     *total_ms = 0.0;
-    if (g_trace.n == 0) return MOE_OK;
+    // always: on return, all work issued while tracing has finished
     if (cudaDeviceSynchronize() != cudaSuccess) return MOE_ERR_CUDA;
+    if (g_trace.n == 0) return MOE_OK;
     double tot = 0.0;
     for (int i = 0; i < g_trace.n; i++) {
         float ms = 0.f;

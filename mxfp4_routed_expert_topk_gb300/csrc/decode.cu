@@ -11,6 +11,7 @@
 // times a scaled f16 input is exact in f16; the 16-term block sum is rounded in
 // f16), then the block sum is scaled by its E8M0 factor and accumulated in fp32.
 #include "moe_internal.cuh"
+#include "prefill_internal.cuh"
 
 namespace moe {
 namespace {
@@ -302,11 +303,10 @@ int g_num_sms = 0;
 }  // namespace
 
 size_t decode_workspace_bytes(int E, int H, int I, int M, int k) {
-    (void)E;
     const size_t general = decode_ws_end(H, I, M, k);
-    if (M != 1) return general;
-    const size_t fused = decode_fused_workspace_bytes(I, k);
-    return fused > general ? fused : general;
+    // M = 1: the fused kernel; M > 1: the grouped GEMMs when the shape allows
+    const size_t special = M == 1 ? decode_fused_workspace_bytes(I, k) : decode_multi_workspace_bytes(E, H, I, M, k);
+    return special > general ? special : general;
 }
 
 cudaError_t launch_decode(const PoolView &v, const uint16_t *x, int M, const int32_t *idx, const float *w, int k,
@@ -319,6 +319,9 @@ cudaError_t launch_decode(const PoolView &v, const uint16_t *x, int M, const int
     }
     if (M == 1) {
         const cudaError_t e = launch_decode_fused(v, x, idx, w, k, residual, y, ws, st);
+        if (e != cudaErrorNotSupported) return e;
+    } else {
+        const cudaError_t e = launch_decode_multi(v, x, M, idx, w, k, residual, y, ws, st);
         if (e != cudaErrorNotSupported) return e;
     }
     DecodeWs d = decode_ws(ws, v.H, v.I, M, k);

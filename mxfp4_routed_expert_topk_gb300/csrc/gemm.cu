@@ -44,6 +44,8 @@ struct GemmArgs {
     const uint8_t *pool;
     uint64_t rec;
     const int32_t *offsets;
+    const int32_t *uexp;     // experts with pairs (grid.y indexes this list)
+    const int32_t *n_union;
     const uint8_t *bscale;   // xs or hs, [P][lds_b]
     int BN;              // columns of the accumulator tile (multiple of 16)
     uint32_t tmem_cols;
@@ -55,6 +57,7 @@ struct GemmArgs {
     int lds_hs;
     void *partial;       // [P][H]
     int partial_dtype;
+    int nparts;          // activation rows per pair (1, or 3 for the exact split)
     StatusWord *st;
 };
 
@@ -151,6 +154,75 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
     for (int i = 0; i < 16; i++) v[i] = __uint_as_float(r[i]);
 }
 
+// Epilogue of the three-part activations: 16 pairs (48 accumulator columns) at a
+// time, each pair's value the sum of its three columns in part order.  Gate/up:
+// h = silu(g) * u, written as three E4M3 parts per 32-block along I (split_part);
+// down: the unweighted expert output row in fp32.
+__device__ __forceinline__ void epilogue_split3(const GemmArgs &a, uint32_t lane_base, bool ok, int nn, int nmma, int mt,
+                                                int row0, int n0, int warp, int lane, float *amax_x) {
+    for (int c0 = 0; c0 < nmma; c0 += 48) {
+        float v0[16], v1[16], v2[16];
+#pragma unroll
+        for (int j = 0; j < 16; j++) v0[j] = v1[j] = v2[j] = 0.f;
+        if (ok) {
+            tmem_ld16(lane_base + (uint32_t)c0, v0);
+            tmem_ld16(lane_base + (uint32_t)c0 + 16, v1);
+            tmem_ld16(lane_base + (uint32_t)c0 + 32, v2);
+        }
+        auto col = [&](int c) { return c < 16 ? v0[c] : (c < 32 ? v1[c - 16] : v2[c - 32]); };
+        float pv[16];
+#pragma unroll
+        for (int j = 0; j < 16; j++) pv[j] = (col(3 * j) + col(3 * j + 1)) + col(3 * j + 2);
+        // sorted pair of column group j: (row0 + n0 + c0) / 3 + j
+        const int pair0 = (row0 + n0 + c0) / 3;
+        const int npair = min(16, (nn - c0) / 3);  // pairs of this group with all three columns
+        if (a.mode == 1) {
+            // lanes 0-15: gate rows, 16-31: up rows of the same 16 intermediate indices
+            const int i = (4 * mt + warp) * 16 + (lane & 15);
+            float hv[16];
+#pragma unroll
+            for (int j = 0; j < 16; j++) {
+                const float u = __shfl_down_sync(0xffffffffu, pv[j], 16);
+                hv[j] = (lane < 16) ? pv[j] / (1.f + expf(-pv[j])) * u : 0.f;
+            }
+#pragma unroll 1
+            for (int q = 0; q < 3; q++) {
+                // max |remainder| of each pair's 32-block along I (warps 2w and 2w+1)
+                float am[16];
+#pragma unroll
+                for (int j = 0; j < 16; j++) {
+                    float m = fabsf(hv[j]);
+#pragma unroll
+                    for (int off = 8; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+                    am[j] = m;
+                }
+                if (lane == 0) {
+#pragma unroll
+                    for (int j = 0; j < 16; j++) amax_x[warp * 16 + j] = am[j];
+                }
+                named_barrier(2, kGemmThreads);
+#pragma unroll
+                for (int j = 0; j < 16; j++) {
+                    const int X = split_exp(fmaxf(amax_x[warp * 16 + j], amax_x[(warp ^ 1) * 16 + j]));
+                    const uint8_t code = split_part(hv[j], X);
+                    if (ok && j < npair && lane < 16) {
+                        const uint64_t r = (uint64_t)3 * (pair0 + j) + q;
+                        a.hq[r * a.I + i] = code;
+                        if (lane == 0 && (warp & 1) == 0) a.hs[r * a.lds_hs + i / 32] = (uint8_t)(X + 127);
+                    }
+                }
+                named_barrier(2, kGemmThreads);
+            }
+        } else {
+            const int o = mt * kTileM + 32 * warp + lane;
+#pragma unroll
+            for (int j = 0; j < 16; j++)
+                if (ok && j < npair && o < a.H)
+                    reinterpret_cast<float *>(a.partial)[(uint64_t)(pair0 + j) * a.H + o] = pv[j];
+        }
+    }
+}
+
 // ------------------------------------------------------------------- kernel
 
 struct GemmSmemLayout {
@@ -183,8 +255,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     float *amax_x = reinterpret_cast<float *>(smem + L.misc + 16);  // [4 warps][16 columns]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int mt = blockIdx.x, e = blockIdx.y;
-    const int row0 = a.offsets[e], nrows = a.offsets[e + 1] - row0;
+    const int mt = blockIdx.x;
+    if ((int)blockIdx.y >= *a.n_union) return;
+    const int e = a.uexp[blockIdx.y];
+    // B rows of this expert: nparts per sorted pair (row nparts*r + q = part q of pair r)
+    const int row0 = a.nparts * a.offsets[e], nrows = a.nparts * (a.offsets[e + 1] - a.offsets[e]);
     if (nrows <= 0) return;
     const int nsfb = (a.BN + 127) / 128;
     const int ntile = (nrows + a.BN - 1) / a.BN;
@@ -335,6 +410,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const bool ok = __all_sync(0xffffffffu, okl);  // warp-uniform for the .sync.aligned loads
         tc_fence_after();
         const uint32_t lane_base = tmem + ((uint32_t)(32 * warp) << 16);
+        if (a.nparts == 3) {
+            epilogue_split3(a, lane_base, ok, nn, nmma, mt, row0, n0, warp, lane, amax_x);
+        } else {
         for (int c0 = 0; c0 < nmma; c0 += 16) {
             float v[16];
 #pragma unroll
@@ -395,6 +473,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     }
                 }
             }
+        }
         }
         tc_fence_before();
         __syncthreads();
@@ -460,15 +539,24 @@ int g_gemm_smem = 0;
 }  // namespace
 
 cudaError_t launch_grouped_gemms(const PoolView &v, int T, int k, const int32_t *offsets, const GroupedWs &g,
-                                 void *partial, int partial_dtype, StatusWord *st, cudaStream_t stream) {
+                                 void *partial, int partial_dtype, StatusWord *st, cudaStream_t stream, int nparts) {
     const int P = T * k;
     if (P == 0) return cudaSuccess;
+    if (nparts != 1 && nparts != 3) return cudaErrorInvalidValue;
     cudaError_t e = get_encoder();
     if (e != cudaSuccess) return e;
-    // accumulator columns per tile: about twice the mean rows per expert, 32..256
-    const int mean = (P + v.E - 1) / v.E;
-    int BN = (2 * mean + 16 + 31) / 32 * 32;
-    BN = BN < 32 ? 32 : (BN > kMaxBN ? kMaxBN : BN);
+    int BN;
+    if (nparts == 3) {
+        // one expert has at most T pairs (distinct slots of a row): 3T columns, in
+        // whole groups of 16 pairs (48 columns), one tile
+        BN = (3 * T + 47) / 48 * 48;
+        if (BN > kMaxBN) return cudaErrorNotSupported;
+    } else {
+        // accumulator columns per tile: about twice the mean rows per expert, 32..256
+        const int mean = (P + v.E - 1) / v.E;
+        BN = (2 * mean + 16 + 31) / 32 * 32;
+        BN = BN < 32 ? 32 : (BN > kMaxBN ? kMaxBN : BN);
+    }
     const int nsfb = (BN + 127) / 128;
     const uint32_t tmem_cols = pow2_at_least((uint32_t)(BN + kStages * (4 + 4 * nsfb)));
     if (tmem_cols > 512) return cudaErrorNotSupported;
@@ -482,6 +570,9 @@ cudaError_t launch_grouped_gemms(const PoolView &v, int T, int k, const int32_t 
     ga.pool = v.base;
     ga.rec = v.rec;
     ga.offsets = offsets;
+    ga.uexp = g.uexp;
+    ga.n_union = g.n_union;
+    const int ngy = P < v.E ? P : v.E;  // at most this many experts have pairs
     ga.BN = BN;
     ga.tmem_cols = tmem_cols;
     ga.I = v.I;
@@ -491,12 +582,13 @@ cudaError_t launch_grouped_gemms(const PoolView &v, int T, int k, const int32_t 
     ga.lds_hs = v.Ip / 32;
     ga.partial = partial;
     ga.partial_dtype = partial_dtype;
+    ga.nparts = nparts;
     ga.st = st;
 
     // GEMM 1: gate/up
     CUtensorMap mA, mB;
     if ((e = make_map_a(&mA, v.base, v.H, 2 * v.I, v.E, (uint64_t)v.ld_gu, v.rec)) != cudaSuccess) return e;
-    if ((e = make_map_b(&mB, g.xq, v.H, P)) != cudaSuccess) return e;
+    if ((e = make_map_b(&mB, g.xq, v.H, nparts * P)) != cudaSuccess) return e;
     ga.mode = 1;
     ga.Kel = v.H;
     ga.nkt = v.H / kTileK;
@@ -508,13 +600,13 @@ cudaError_t launch_grouped_gemms(const PoolView &v, int T, int k, const int32_t 
     ga.bscale = g.xs;
     {
         TraceScope trace_scope("gemm_gateup", stream);
-        grouped_gemm_kernel<<<dim3(2 * v.I / kTileM, v.E), kGemmThreads, smem, stream>>>(mA, mB, ga);
+        grouped_gemm_kernel<<<dim3(2 * v.I / kTileM, ngy), kGemmThreads, smem, stream>>>(mA, mB, ga);
     }
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
     // GEMM 2: down
     if ((e = make_map_a(&mA, v.base + v.off_d, v.Ip, v.H, v.E, (uint64_t)v.ld_d, v.rec)) != cudaSuccess) return e;
-    if ((e = make_map_b(&mB, g.hq, v.I, P)) != cudaSuccess) return e;
+    if ((e = make_map_b(&mB, g.hq, v.I, nparts * P)) != cudaSuccess) return e;
     ga.mode = 2;
     ga.Kel = v.I;
     ga.nkt = v.Ip / kTileK;
@@ -526,7 +618,7 @@ cudaError_t launch_grouped_gemms(const PoolView &v, int T, int k, const int32_t 
     ga.bscale = g.hs;
     {
         TraceScope trace_scope("gemm_down", stream);
-        grouped_gemm_kernel<<<dim3(v.H / kTileM, v.E), kGemmThreads, smem, stream>>>(mA, mB, ga);
+        grouped_gemm_kernel<<<dim3(v.H / kTileM, ngy), kGemmThreads, smem, stream>>>(mA, mB, ga);
     }
     return cudaGetLastError();
 }

@@ -46,9 +46,62 @@ __global__ void __launch_bounds__(kSortBlock) sort_rank_kernel(const int32_t *__
     for (int x = tid; x < E; x += blockDim.x) cnt[(size_t)b * E + x] = hist[x];
 }
 
-// One CTA: prior[b][e] = sum_{b'<b} cnt[b'][e]; offsets = exclusive scan of totals.
+// Exclusive scan over the 1024 threads of a CTA (total in *total); warp_sum is
+// shared scratch of 32 ints.
+__device__ int block_exclusive_scan(int s, int *warp_sum, int *total) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    int incl = s;
+    for (int off = 1; off < 32; off <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += v;
+    }
+    __syncthreads();
+    if (lane == 31) warp_sum[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        int w = warp_sum[lane];
+        for (int off = 1; off < 32; off <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, w, off);
+            if (lane >= off) w += v;
+        }
+        warp_sum[lane] = w;  // inclusive over warps
+    }
+    __syncthreads();
+    *total = warp_sum[31];
+    return incl - s + (warp > 0 ? warp_sum[warp - 1] : 0);
+}
+
+// From the per-expert totals tot[0..E) (shared): offsets = their exclusive scan,
+// uexp / n_union = the experts with a non-zero total, ascending.  1024 threads.
+__device__ void offsets_and_union(const int *tot, int E, int *warp_sum, int32_t *offsets, int32_t *uexp,
+                                  int32_t *n_union) {
+    const int tid = threadIdx.x;
+    const int per = (E + blockDim.x - 1) / blockDim.x;
+    const int lo = tid * per, hi = min(E, lo + per);
+    int s = 0, nz = 0;
+    for (int e = lo; e < hi; e++) {
+        s += tot[e];
+        nz += tot[e] > 0;
+    }
+    int total;
+    int base = block_exclusive_scan(s, warp_sum, &total);
+    for (int e = lo; e < hi; e++) {
+        offsets[e] = base;
+        base += tot[e];
+    }
+    if (tid == 0) offsets[E] = total;
+    int nu;
+    int ub = block_exclusive_scan(nz, warp_sum, &nu);
+    for (int e = lo; e < hi; e++)
+        if (tot[e] > 0) uexp[ub++] = e;
+    if (tid == 0) *n_union = nu;
+}
+
+// One CTA: prior[b][e] = sum_{b'<b} cnt[b'][e]; offsets = exclusive scan of totals;
+// the list of experts that have pairs.
 __global__ void __launch_bounds__(1024) sort_scan_kernel(int nblocks, int E, const int *__restrict__ cnt,
-                                                         int *__restrict__ prior, int32_t *__restrict__ offsets) {
+                                                         int *__restrict__ prior, int32_t *__restrict__ offsets,
+                                                         int32_t *__restrict__ uexp, int32_t *__restrict__ n_union) {
     __shared__ int tot[kMaxSortE];
     __shared__ int warp_sum[32];
     const int tid = threadIdx.x;
@@ -61,35 +114,47 @@ __global__ void __launch_bounds__(1024) sort_scan_kernel(int nblocks, int E, con
         tot[e] = run;
     }
     __syncthreads();
-    // exclusive scan of tot[0..E) with 1024 threads, each owning a contiguous chunk
-    const int per = (E + blockDim.x - 1) / blockDim.x;
-    const int lo = tid * per, hi = min(E, lo + per);
-    int s = 0;
-    for (int e = lo; e < hi; e++) s += tot[e];
-    // block-wide exclusive scan of s
-    const int lane = tid & 31, warp = tid >> 5;
-    int incl = s;
-    for (int off = 1; off < 32; off <<= 1) {
-        const int v = __shfl_up_sync(0xffffffffu, incl, off);
-        if (lane >= off) incl += v;
-    }
-    if (lane == 31) warp_sum[warp] = incl;
-    __syncthreads();
-    if (warp == 0) {
-        int w = warp_sum[lane];
-        for (int off = 1; off < 32; off <<= 1) {
-            const int v = __shfl_up_sync(0xffffffffu, w, off);
-            if (lane >= off) w += v;
+    offsets_and_union(tot, E, warp_sum, offsets, uexp, n_union);
+}
+
+// The whole sort in one CTA of 1024 threads for P <= 1024 pairs (multi-token
+// decode): per-expert counts, offsets, the list of experts with pairs, and the
+// stable scatter (a pair's place among its expert's pairs is the number of earlier
+// pairs of the same expert).
+__global__ void __launch_bounds__(1024) sort_small_kernel(const int32_t *__restrict__ idx, int P, int E,
+                                                          int32_t *__restrict__ offsets, int32_t *__restrict__ uexp,
+                                                          int32_t *__restrict__ n_union, int32_t *__restrict__ perm,
+                                                          int32_t *__restrict__ inv_perm, StatusWord *st) {
+    __shared__ int tot[kMaxSortE];
+    __shared__ int es[1024];
+    __shared__ int warp_sum[32];
+    const int tid = threadIdx.x;
+    for (int e = tid; e < E; e += blockDim.x) tot[e] = 0;
+    int e = -1;
+    if (tid < P) {
+        e = idx[tid];
+        if (e < 0 || e >= E) {
+            set_status(st, MOE_ERR_BAD_INDEX, (unsigned)tid);
+            e = -1;
         }
-        warp_sum[lane] = w;  // inclusive over warps
     }
+    es[tid] = e;
     __syncthreads();
-    int base = incl - s + (warp > 0 ? warp_sum[warp - 1] : 0);
-    for (int e = lo; e < hi; e++) {
-        offsets[e] = base;
-        base += tot[e];
+    if (e >= 0) atomicAdd(&tot[e], 1);
+    __syncthreads();
+    offsets_and_union(tot, E, warp_sum, offsets, uexp, n_union);
+    __syncthreads();  // offsets[] of this CTA's threads are visible to the others
+    if (tid < P) {
+        if (e < 0) {
+            inv_perm[tid] = -1;
+        } else {
+            int r = 0;
+            for (int q = 0; q < tid; q++) r += (es[q] == e);
+            const int pos = offsets[e] + r;
+            perm[pos] = tid;
+            inv_perm[tid] = pos;
+        }
     }
-    if (tid == blockDim.x - 1) offsets[E] = base;
 }
 
 __global__ void sort_scatter_kernel(const int32_t *__restrict__ idx, int P, int E, const int *__restrict__ local_rank,
@@ -138,6 +203,32 @@ __global__ void gather_quant_kernel(const uint16_t *__restrict__ x, int H, int k
     }
 }
 
+// Row r of the sorted pairs: x[perm[r] / k] as three E4M3 parts (rows 3r, 3r+1,
+// 3r+2) with one E8M0 scale per part and 32-block (split_part).  One warp per row.
+__global__ void gather_split3_kernel(const uint16_t *__restrict__ x, int H, int k, int nrows,
+                                     const int32_t *__restrict__ perm, uint8_t *__restrict__ xq,
+                                     uint8_t *__restrict__ xs) {
+    // warp = (row, group of 8 blocks of 32)
+    const int lane = threadIdx.x & 31;
+    const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int ngrp = (H / 32 + 7) / 8;
+    const int r = gw / ngrp, grp = gw % ngrp;
+    if (r >= nrows) return;
+    const int t = perm[r] / k;
+    const uint16_t *xr = x + (size_t)t * H;
+    for (int b0 = grp * 256; b0 < min(H, grp * 256 + 256); b0 += 32) {
+        float v = bf16_bits_to_float(xr[b0 + lane]);
+#pragma unroll
+        for (int q = 0; q < 3; q++) {
+            float a = fabsf(v);
+            for (int off = 16; off > 0; off >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, off));
+            const int X = split_exp(a);
+            xq[((size_t)3 * r + q) * H + b0 + lane] = split_part(v, X);
+            if (lane == 0) xs[((size_t)3 * r + q) * (H / 32) + b0 / 32] = (uint8_t)(X + 127);
+        }
+    }
+}
+
 template <typename PT>
 __device__ __forceinline__ float load_partial(const PT *p);
 template <>
@@ -149,16 +240,17 @@ __device__ __forceinline__ float load_partial<__nv_bfloat16>(const __nv_bfloat16
 template <typename PT>
 __global__ void combine_kernel(const PT *__restrict__ partial, const int32_t *__restrict__ inv_perm,
                                const float *__restrict__ w, int k, int H, const uint16_t *__restrict__ residual,
-                               uint16_t *__restrict__ y) {
+                               uint16_t *__restrict__ y, int chunk) {
     __shared__ int rows[kMaxK];
     __shared__ float ws[kMaxK];
     const int t = blockIdx.x;
+    const int o_lo = blockIdx.y * chunk, o_hi = min(H, o_lo + chunk);
     if (threadIdx.x < k) {
         rows[threadIdx.x] = inv_perm[(size_t)t * k + threadIdx.x];
         ws[threadIdx.x] = w[(size_t)t * k + threadIdx.x];
     }
     __syncthreads();
-    for (int o = threadIdx.x; o < H; o += blockDim.x) {
+    for (int o = o_lo + threadIdx.x; o < o_hi; o += blockDim.x) {
         float acc = 0.f;
         for (int j = 0; j < k; j++) {
             const int r = rows[j];
@@ -195,7 +287,7 @@ cudaError_t launch_grouped(const PoolView &v, const uint16_t *x, int T, const in
     }
     {
         TraceScope trace_scope("sort_scan", st);
-        sort_scan_kernel<<<1, 1024, 0, st>>>(nblocks, v.E, g.cnt, g.prior, offsets);
+        sort_scan_kernel<<<1, 1024, 0, st>>>(nblocks, v.E, g.cnt, g.prior, offsets, g.uexp, g.n_union);
     }
     {
         TraceScope trace_scope("sort_scatter", st);
@@ -210,15 +302,49 @@ cudaError_t launch_grouped(const PoolView &v, const uint16_t *x, int T, const in
     return cudaGetLastError();
 }
 
+size_t decode_multi_workspace_bytes(int E, int H, int I, int M, int k) {
+    return decode_multi_ws_layout((void *)0, E, H, I, M, k).end;
+}
+
+cudaError_t launch_decode_multi(const PoolView &v, const uint16_t *x, int M, const int32_t *idx, const float *w, int k,
+                                const uint16_t *residual, uint16_t *y, void *ws, cudaStream_t st) {
+    if (v.E > kMaxSortE || v.I % 64 != 0 || v.H % 128 != 0 || 3 * M > 96) return cudaErrorNotSupported;
+    const DecodeMultiWs d = decode_multi_ws_layout(ws, v.E, v.H, v.I, M, k);
+    StatusWord *stw = reinterpret_cast<StatusWord *>(ws);
+    const int P = M * k;
+    if (P > 1024) return cudaErrorNotSupported;
+    {
+        TraceScope trace_scope("sort_small", st);
+        sort_small_kernel<<<1, 1024, 0, st>>>(idx, P, v.E, d.offsets, d.g.uexp, d.g.n_union, d.perm, d.inv_perm, stw);
+    }
+    {
+        TraceScope trace_scope("gather_split", st);
+        const int ngrp = (v.H / 32 + 7) / 8;
+        gather_split3_kernel<<<(P * ngrp * 32 + 255) / 256, 256, 0, st>>>(x, v.H, k, P, d.perm, d.g.xq, d.g.xs);
+    }
+    cudaError_t e = launch_grouped_gemms(v, M, k, d.offsets, d.g, d.partial, MOE_PARTIAL_F32, stw, st, 3);
+    if (e != cudaSuccess) return e;
+    {
+        TraceScope trace_scope("combine", st);
+        const int chunk = 256;  // few rows: one output per thread, (row, chunk) grid
+        combine_kernel<float><<<dim3(M, (v.H + chunk - 1) / chunk), 256, 0, st>>>(d.partial, d.inv_perm, w, k, v.H,
+                                                                                   residual, y, chunk);
+    }
+    return cudaGetLastError();
+}
+
 cudaError_t launch_combine(const void *partial, int partial_dtype, const int32_t *inv_perm, const float *w, int T, int k,
                            int H, const uint16_t *residual, uint16_t *y, cudaStream_t st) {
     if (T == 0) return cudaSuccess;
     TraceScope trace_scope("combine", st);
+    // one CTA per row over all of H, or (row, chunk) CTAs when there are few rows
+    const int chunk = T < 152 ? 256 : H;
+    const dim3 grid(T, (H + chunk - 1) / chunk);
     if (partial_dtype == MOE_PARTIAL_F32)
-        combine_kernel<float><<<T, 256, 0, st>>>((const float *)partial, inv_perm, w, k, H, residual, y);
+        combine_kernel<float><<<grid, 256, 0, st>>>((const float *)partial, inv_perm, w, k, H, residual, y, chunk);
     else
-        combine_kernel<__nv_bfloat16><<<T, 256, 0, st>>>((const __nv_bfloat16 *)partial, inv_perm, w, k, H, residual,
-                                                         y);
+        combine_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>((const __nv_bfloat16 *)partial, inv_perm, w, k, H, residual,
+                                                            y, chunk);
     return cudaGetLastError();
 }
 
