@@ -9,12 +9,19 @@
 //   GEMM 2 (down):    A = W_d (H rows, K = I, zero padded to 128), B = MXFP8 h rows;
 //            epilogue writes the unweighted expert output rows (fp32 or bf16)
 //
-// One CTA per (expert, 128-row tile of A), 4 warps: warp 0 issues the tensor
+// Persistent: one CTA per SM walks the (expert with pairs, 128-row tile of A) items
+// with a stride of the grid, with as many pipeline stages as shared memory holds
+// (the stream of K steps runs on across items).  8 warps: warp 0 issues the tensor
 // copies of A and B, warp 1 stages the scale factors in shared memory in the
-// 32x16-byte layout tcgen05.cp expects, warp 2 owns TMEM and issues the MMAs,
-// and all four warps run the epilogue (warp w reads TMEM lanes 32w..32w+31).
-// Every wait is bounded (MOE_ERR_TIMEOUT), and nothing exits with copies or MMAs
-// in flight.
+// 32x16-byte layout tcgen05.cp expects, warp 2 owns TMEM and issues the MMAs into
+// one of two accumulators, and warps 4-7 run the epilogue of the other
+// accumulator (warp 4+w reads TMEM lanes 32w..32w+31), so a tile's epilogue
+// overlaps the next tile's MMAs.  With three-part activations (nparts = 3, the
+// multi-token decode) each sorted pair has three B rows whose columns the
+// epilogue sums.  Every wait is bounded (MOE_ERR_TIMEOUT), and nothing exits with
+// copies or MMAs in flight.
+#include <algorithm>
+
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -24,12 +31,13 @@
 namespace moe {
 namespace {
 
-constexpr int kStages = 4;
+constexpr int kMaxStages = 12;
 constexpr int kTileM = 128;
 constexpr int kTileK = 128;   // elements (bytes in shared memory for both operands)
-constexpr int kBoxN = 16;     // rows per tensor copy of B
-constexpr int kGemmThreads = 128;
-constexpr int kMaxBN = 256;
+
+constexpr int kGemmThreads = 256;  // warps: 0 copies, 1 scale factors, 2 MMA, 4-7 epilogue
+constexpr int kEpiThreads = 128;
+constexpr int kMaxBN = 192;        // two accumulators + scale factors fit in 512 TMEM columns
 
 struct GemmArgs {
     int mode;            // 1: gate/up + SwiGLU + MXFP8, 2: down
@@ -48,6 +56,10 @@ struct GemmArgs {
     const int32_t *n_union;
     const uint8_t *bscale;   // xs or hs, [P][lds_b]
     int BN;              // columns of the accumulator tile (multiple of 16)
+    int ns;              // pipeline stages
+    int nmt;             // 128-row tiles of A per expert
+    int tpi;             // 128-row tiles per work item (1, or 2: one 256-row tensor copy of A)
+    int nrows_a;         // rows of A per expert (2I or H)
     uint32_t tmem_cols;
     // epilogue outputs
     int I;               // intermediate size (gate/up epilogue)
@@ -120,6 +132,18 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
 
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// 4-byte asynchronous copy global -> shared; bytes past src_bytes (0..4) are zero.
+__device__ __forceinline__ void cp_async4(void *dst, const void *src, uint32_t src_bytes) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(src_bytes)
+                 : "memory");
+}
+
+// Arrive on `bar` once this thread's earlier cp.async copies have landed (the
+// arrival is one of the barrier's expected arrivals).
+__device__ __forceinline__ void cp_async_arrive(uint64_t *bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
 
 __device__ __forceinline__ void tc_cp_sf(uint32_t taddr, uint64_t sdesc) {
     asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
@@ -200,7 +224,7 @@ __device__ __forceinline__ void epilogue_split3(const GemmArgs &a, uint32_t lane
 #pragma unroll
                     for (int j = 0; j < 16; j++) amax_x[warp * 16 + j] = am[j];
                 }
-                named_barrier(2, kGemmThreads);
+                named_barrier(2, kEpiThreads);
 #pragma unroll
                 for (int j = 0; j < 16; j++) {
                     const int X = split_exp(fmaxf(amax_x[warp * 16 + j], amax_x[(warp ^ 1) * 16 + j]));
@@ -211,7 +235,7 @@ __device__ __forceinline__ void epilogue_split3(const GemmArgs &a, uint32_t lane
                         if (lane == 0 && (warp & 1) == 0) a.hs[r * a.lds_hs + i / 32] = (uint8_t)(X + 127);
                     }
                 }
-                named_barrier(2, kGemmThreads);
+                named_barrier(2, kEpiThreads);
             }
         } else {
             const int o = mt * kTileM + 32 * warp + lane;
@@ -225,17 +249,117 @@ __device__ __forceinline__ void epilogue_split3(const GemmArgs &a, uint32_t lane
 
 // ------------------------------------------------------------------- kernel
 
+// One-part (MXFP8) epilogue of a tile's 16-column groups: gate/up -> h = silu(g) * u
+// quantised to MXFP8 along I (OCP rule); down -> expert output rows.  ew = warp
+// index within the epilogue warpgroup (TMEM lanes 32ew..32ew+31).
+__device__ __forceinline__ void epilogue_mx1(const GemmArgs &a, uint32_t lane_base, bool ok, int nn, int nmma, int mt,
+                                             int row0, int n0, int ew, int lane, float *amax_x) {
+    for (int c0 = 0; c0 < nmma; c0 += 16) {
+        float v[16];
+#pragma unroll
+        for (int j = 0; j < 16; j++) v[j] = 0.f;
+        if (ok) tmem_ld16(lane_base + (uint32_t)c0, v);
+        if (a.mode == 1) {
+            // lanes 0-15: gate rows, 16-31: up rows of the same 16 intermediate indices
+            const int i = (4 * mt + ew) * 16 + (lane & 15);
+            float hv[16];
+            float am[16];
+#pragma unroll
+            for (int j = 0; j < 16; j++) {
+                const float u = __shfl_down_sync(0xffffffffu, v[j], 16);
+                const float g = v[j];
+                hv[j] = (lane < 16) ? g / (1.f + expf(-g)) * u : 0.f;
+                float m = fabsf(hv[j]);
+#pragma unroll
+                for (int off = 8; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+                am[j] = m;
+            }
+            if (lane == 0) {
+#pragma unroll
+                for (int j = 0; j < 16; j++) amax_x[ew * 16 + j] = am[j];
+            }
+            named_barrier(2, kEpiThreads);
+#pragma unroll
+            for (int j = 0; j < 16; j++) {
+                const int n = c0 + j;
+                const float amax = fmaxf(amax_x[ew * 16 + j], amax_x[(ew ^ 1) * 16 + j]);
+                int X = -127;
+                if (amax > 0.f) {
+                    int ex;
+                    frexpf(amax, &ex);
+                    X = max(-127, min(127, ex - 1 - 8));
+                }
+                if (ok && n < nn && lane < 16) {
+                    const uint64_t r = (uint64_t)(row0 + n0 + n);
+                    unsigned short pair;
+                    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(pair) : "f"(0.f), "f"(ldexpf(hv[j], -X)));
+                    a.hq[r * a.I + i] = (uint8_t)(pair & 0xFF);
+                    if (lane == 0 && (ew & 1) == 0) a.hs[r * a.lds_hs + i / 32] = (uint8_t)(X + 127);
+                }
+            }
+            named_barrier(2, kEpiThreads);
+        } else {
+            const int o = mt * kTileM + 32 * ew + lane;
+#pragma unroll
+            for (int j = 0; j < 16; j++) {
+                const int n = c0 + j;
+                if (ok && n < nn && o < a.H) {
+                    const uint64_t r = (uint64_t)(row0 + n0 + n);
+                    if (a.partial_dtype == MOE_PARTIAL_F32)
+                        reinterpret_cast<float *>(a.partial)[r * a.H + o] = v[j];
+                    else
+                        reinterpret_cast<__nv_bfloat16 *>(a.partial)[r * a.H + o] = __float2bfloat16_rn(v[j]);
+                }
+            }
+        }
+    }
+}
+
+// Shared memory of the persistent kernel for BN accumulator columns and ns stages.
 struct GemmSmemLayout {
     uint32_t a, b, sfa, sfb, bars, misc, total;
-    __host__ __device__ GemmSmemLayout(int BN) {
+    __host__ __device__ GemmSmemLayout(int BN, int ns, int tpi) {
         const uint32_t nsfb = (uint32_t)((BN + 127) / 128);
-        a = 0;                                            // kStages x 16 KB (1024-aligned)
-        b = a + kStages * kTileM * kTileK;                // kStages x BN*128
-        sfa = b + kStages * (uint32_t)BN * kTileK;        // kStages x 512
-        sfb = sfa + kStages * 512;                        // kStages x nsfb*512
-        bars = sfb + kStages * 512 * nsfb;                // full[], empty[], done
-        misc = bars + (2 * kStages + 1) * 8;              // tmem addr, abort, amax[4][16]
+        a = 0;                                            // ns x tpi x 16 KB (1024-aligned)
+        b = a + (uint32_t)(ns * tpi) * kTileM * kTileK;   // ns x BN*128
+        sfa = b + (uint32_t)ns * (uint32_t)BN * kTileK;   // ns x tpi x 512
+        sfb = sfa + (uint32_t)(ns * tpi) * 512;           // ns x nsfb*512
+        bars = sfb + (uint32_t)ns * 512 * nsfb;           // full[], empty[], acc_full[2], acc_empty[2]
+        misc = bars + (2 * kMaxStages + 4) * 8;           // tmem addr, abort, amax[4][16]
         total = misc + 16 + 4 * 16 * 4;
+    }
+};
+
+// The work of a CTA: items i = blockIdx.x, +gridDim.x, ... of the n_union * nmt
+// (expert of the union, 128-row tile of A) items; each item's columns in tiles of
+// BN.  Every role walks this same sequence.
+struct JobIter {
+    const GemmArgs &a;
+    int nu, i, nt, ntile, e, mt, row0, nrows;
+    __device__ JobIter(const GemmArgs &args, int nu_) : a(args), nu(nu_), i((int)blockIdx.x), nt(0), ntile(0) { load(); }
+    __device__ void load() {
+        ntile = 0;
+        const int nwi = (a.nmt + a.tpi - 1) / a.tpi;  // items per expert
+        while (i < nu * nwi) {
+            const int u = i / nwi;
+            mt = (i % nwi) * a.tpi;  // first 128-row tile of the item
+            e = a.uexp[u];
+            row0 = a.nparts * a.offsets[e];
+            nrows = a.nparts * (a.offsets[e + 1] - a.offsets[e]);
+            ntile = (nrows + a.BN - 1) / a.BN;
+            if (ntile > 0) break;
+            i += (int)gridDim.x;
+        }
+        nt = 0;
+    }
+    __device__ bool valid() const { return i < nu * ((a.nmt + a.tpi - 1) / a.tpi) && ntile > 0; }
+    __device__ int n0() const { return nt * a.BN; }
+    __device__ int nn() const { return min(a.BN, nrows - nt * a.BN); }
+    __device__ void next() {
+        if (++nt >= ntile) {
+            i += (int)gridDim.x;
+            load();
+        }
     }
 };
 
@@ -245,36 +369,37 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     // the tensor copies with 128-byte swizzling need 1024-byte aligned tiles
     unsigned char *smem = (unsigned char *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    const GemmSmemLayout L(a.BN);
+    const int ns = a.ns;
+    const int tpi = a.tpi;
+    const GemmSmemLayout L(a.BN, ns, tpi);
     uint8_t *sA = smem + L.a, *sB = smem + L.b, *sSFA = smem + L.sfa, *sSFB = smem + L.sfb;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.bars);
-    uint64_t *empty = full + kStages;
-    uint64_t *done = empty + kStages;
+    uint64_t *empty = full + kMaxStages;
+    uint64_t *acc_full = empty + kMaxStages;
+    uint64_t *acc_empty = acc_full + 2;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L.misc);
     int *abort_flag = reinterpret_cast<int *>(smem + L.misc + 4);
-    float *amax_x = reinterpret_cast<float *>(smem + L.misc + 16);  // [4 warps][16 columns]
+    float *amax_x = reinterpret_cast<float *>(smem + L.misc + 16);  // [4 epilogue warps][16 columns]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int mt = blockIdx.x;
-    if ((int)blockIdx.y >= *a.n_union) return;
-    const int e = a.uexp[blockIdx.y];
-    // B rows of this expert: nparts per sorted pair (row nparts*r + q = part q of pair r)
-    const int row0 = a.nparts * a.offsets[e], nrows = a.nparts * (a.offsets[e + 1] - a.offsets[e]);
-    if (nrows <= 0) return;
+    const int nu = *a.n_union;
+    if ((int)blockIdx.x >= nu * ((a.nmt + tpi - 1) / tpi)) return;  // the whole CTA, before any barrier
     const int nsfb = (a.BN + 127) / 128;
-    const int ntile = (nrows + a.BN - 1) / a.BN;
 
     // The unpacked E2M1 copies write 8 of every 16 bytes of an A tile; keep the
     // other 8 (which the MMA format pads with) zero for the whole kernel.
-    for (int i = threadIdx.x; i < kStages * kTileM * kTileK / 16; i += kGemmThreads)
+    for (int i = threadIdx.x; i < ns * tpi * kTileM * kTileK / 16; i += kGemmThreads)
         reinterpret_cast<uint4 *>(sA)[i] = make_uint4(0u, 0u, 0u, 0u);
     fence_proxy_async_smem();
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; s++) {
-            mbar_init(&full[s], 2);   // producer's expect-tx arrival + scale-factor warp
+        for (int s = 0; s < ns; s++) {
+            mbar_init(&full[s], 33);  // producer's expect-tx arrival + 32 scale-factor lanes' copies
             mbar_init(&empty[s], 1);  // MMA commit
         }
-        mbar_init(done, 1);
+        for (int b = 0; b < 2; b++) {
+            mbar_init(&acc_full[b], 1);   // MMA commit after a tile's last K step
+            mbar_init(&acc_empty[b], 4);  // the four epilogue warps
+        }
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -283,205 +408,171 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t sf_col0 = (uint32_t)a.BN;  // scale factors after the accumulator columns
+    const uint32_t sf_col0 = 2u * (uint32_t)(tpi * a.BN);  // scale factors after the two accumulators
+    const uint32_t sf_stage = 4u * (uint32_t)tpi + 4u * (uint32_t)nsfb;  // TMEM columns per stage
 
-    int it_issued = 0;   // producer: stages issued
-    for (int nt = 0; nt < ntile; nt++) {
-        const int n0 = nt * a.BN;
-        const int nn = min(a.BN, nrows - n0);      // valid columns
-        const int nmma = (nn + 15) / 16 * 16;      // MMA N
-        if (warp == 0) {
-            if (lane == 0) {
-                for (int kt = 0; kt < a.nkt; kt++) {
-                    const int it = nt * a.nkt + kt, s = it % kStages;
-                    const uint32_t ph = (uint32_t)(it / kStages) & 1u;
+    int it_issued = 0;  // producer: stages issued
+    if (warp == 0) {
+        // ------------------------------------------------------- tensor copies
+        if (lane == 0) {
+            int it = 0;
+            bool run = true;
+            for (JobIter J(a, nu); run && J.valid(); J.next()) {
+                const int nmma = (J.nn() + 15) / 16 * 16;
+                for (int kt = 0; kt < a.nkt; kt++, it++) {
+                    const int s = it % ns;
+                    const uint32_t ph = (uint32_t)(it / ns) & 1u;
                     if (*(volatile int *)abort_flag || !mbar_wait(&empty[s], ph ^ 1u, a.st, 0x500u + s)) {
                         *abort_flag = 1;
+                        run = false;
                         break;
                     }
-                    const int nbox = (nmma + kBoxN - 1) / kBoxN;
                     // A arrives unpacked (16 E2M1 values in each 16 bytes, 8 of them data) and
                     // counts its packed bytes; B counts one byte per element
-                    mbar_arrive_expect_tx(&full[s], (uint32_t)(kTileM * kTileK / 2 + nbox * kBoxN * kTileK));
-                    tma_load_3d(sA + (size_t)s * kTileM * kTileK, &tmA, kt * kTileK, mt * kTileM, e, &full[s]);
-                    for (int j = 0; j < nbox; j++)
-                        tma_load_2d(sB + (size_t)s * a.BN * kTileK + (size_t)j * kBoxN * kTileK, &tmB, kt * kTileK,
-                                    row0 + n0 + j * kBoxN, &full[s]);
+                    // B: one copy of BN rows (rows past this tile's nmma belong to other
+                    // experts or are out of range and zero; the MMA does not read them)
+                    mbar_arrive_expect_tx(&full[s], (uint32_t)(tpi * kTileM * kTileK / 2 + a.BN * kTileK));
+                    tma_load_3d(sA + (size_t)s * tpi * kTileM * kTileK, &tmA, kt * kTileK, J.mt * kTileM, J.e, &full[s]);
+                    tma_load_2d(sB + (size_t)s * a.BN * kTileK, &tmB, kt * kTileK, J.row0 + J.n0(), &full[s]);
                     it_issued = it + 1;
                 }
             }
-            __syncwarp();  // the epilogue's tensor-memory loads need the whole warp
-        } else if (warp == 1) {
-            // Scale factors of K-tile kt: A rows mt*128 + lane + 32 q, B columns
-            // n0 + at*128 + lane + 32 q, scale blocks 4kt .. 4kt+3 (4 bytes each).  They are
-            // fetched two K-tiles ahead into registers so their global latency overlaps
-            // the wait for a free stage.
-            const uint8_t *sa = a.pool + (uint64_t)e * a.rec + a.a_scale_off;
-            auto load_sf = [&](int kt, uint32_t (&wa)[4], uint32_t (&wb)[2][4]) {
-#pragma unroll
-                for (int q = 0; q < 4; q++) {
-                    const uint64_t r = (uint64_t)(mt * kTileM + lane + 32 * q);
-                    wa[q] = (kt < a.nkt && 4 * kt + 3 < a.nkb_a)
-                                ? __ldg(reinterpret_cast<const uint32_t *>(sa + r * a.lds_a + 4 * kt))
-                                : 0u;
-                }
-                const uint32_t keep = (4 * kt + 4 <= a.nkb_b) ? 0xFFFFFFFFu
-                                      : (4 * kt >= a.nkb_b)    ? 0u
-                                                               : (0xFFFFFFFFu >> (8 * (4 * kt + 4 - a.nkb_b)));
-#pragma unroll
-                for (int at = 0; at < 2; at++)
-#pragma unroll
-                    for (int q = 0; q < 4; q++) {
-                        const int c = at * 128 + lane + 32 * q;
-                        uint32_t w = 0u;
-                        if (at < nsfb && c < nn && kt < a.nkt && keep != 0u)
-                            w = __ldg(reinterpret_cast<const uint32_t *>(a.bscale + (uint64_t)(row0 + n0 + c) * a.lds_b +
-                                                                        4 * kt)) & keep;
-                        wb[at][q] = w;
-                    }
-            };
-            uint32_t wa0[4], wb0[2][4], wa1[4], wb1[2][4], wa2[4], wb2[2][4];
-            load_sf(0, wa0, wb0);
-            load_sf(1, wa1, wb1);
-            for (int kt = 0; kt < a.nkt; kt++) {
-                const int it = nt * a.nkt + kt, s = it % kStages;
-                const uint32_t ph = (uint32_t)(it / kStages) & 1u;
-                load_sf(kt + 2, wa2, wb2);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------- scale factors
+        // Of K-tile kt: A rows mt*128 + lane + 32 q and B columns n0 + at*128 + lane + 32 q,
+        // scale blocks 4kt .. 4kt+3 (4 bytes each), copied asynchronously into the stage
+        // in the layout tcgen05.cp expects (row r at (r % 32) * 16 + (r / 32) * 4).  Each
+        // lane's arrival on full[s] waits for its own copies, so the warp runs as many
+        // stages ahead as the pipeline allows.
+        int it = 0;
+        bool run = true;
+        for (JobIter J(a, nu); run && J.valid(); J.next()) {
+            const uint8_t *sa = a.pool + (uint64_t)J.e * a.rec + a.a_scale_off;
+            const int nn = J.nn(), base_row = J.row0 + J.n0();
+            for (int kt = 0; kt < a.nkt; kt++, it++) {
+                const int s = it % ns;
+                const uint32_t ph = (uint32_t)(it / ns) & 1u;
                 int okl = 0;
                 if (lane == 0) okl = !*(volatile int *)abort_flag && mbar_wait(&empty[s], ph ^ 1u, a.st, 0x600u + s);
                 const bool ok = __shfl_sync(0xffffffffu, okl, 0) != 0;  // warp-uniform
-                if (!ok && lane == 0) *abort_flag = 1;
-                if (ok) {
-                    *reinterpret_cast<uint4 *>(sSFA + (size_t)s * 512 + lane * 16) =
-                        make_uint4(wa0[0], wa0[1], wa0[2], wa0[3]);
-                    for (int at = 0; at < nsfb; at++)
-                        *reinterpret_cast<uint4 *>(sSFB + ((size_t)s * nsfb + at) * 512 + lane * 16) =
-                            make_uint4(wb0[at][0], wb0[at][1], wb0[at][2], wb0[at][3]);
-                    fence_proxy_async_smem();
+                if (!ok) {
+                    if (lane == 0) *abort_flag = 1;
+                    run = false;
+                    break;
                 }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&full[s]);
-                if (!ok) break;
+                uint8_t *dA = sSFA + (size_t)s * tpi * 512;
+                const uint32_t a_bytes = 4 * kt + 3 < a.nkb_a ? 4u : 0u;
+                for (int q = 0; q < 4 * tpi; q++) {
+                    // row of A; rows past the expert's A rows (the copy zero-fills them) get zero scales
+                    const int r = J.mt * kTileM + lane + 32 * q;
+                    const bool in = r < a.nrows_a && a_bytes != 0;
+                    cp_async4(dA + (q >> 2) * 512 + lane * 16 + (q & 3) * 4,
+                              sa + (uint64_t)(in ? r : 0) * a.lds_a + (in ? 4 * kt : 0), in ? a_bytes : 0u);
+                }
+                // valid scale bytes of B in this K-tile (the rest of the word is zero)
+                const int vb = min(4, max(0, a.nkb_b - 4 * kt));
+                for (int at = 0; at < nsfb; at++) {
+                    uint8_t *dB = sSFB + ((size_t)s * nsfb + at) * 512;
 #pragma unroll
-                for (int q = 0; q < 4; q++) {
-                    wa0[q] = wa1[q];
-                    wa1[q] = wa2[q];
-                    wb0[0][q] = wb1[0][q];
-                    wb0[1][q] = wb1[1][q];
-                    wb1[0][q] = wb2[0][q];
-                    wb1[1][q] = wb2[1][q];
+                    for (int q = 0; q < 4; q++) {
+                        const int c = at * 128 + lane + 32 * q;
+                        const bool in = c < nn && vb > 0;
+                        cp_async4(dB + lane * 16 + q * 4,
+                                  a.bscale + (uint64_t)(in ? base_row + c : base_row) * a.lds_b + (in ? 4 * kt : 0),
+                                  in ? (uint32_t)vb : 0u);
+                    }
                 }
+                cp_async_arrive(&full[s]);
             }
-        } else if (warp == 2) {
-            if (lane == 0) {
-                bool ok = true;
-                for (int kt = 0; kt < a.nkt; kt++) {
-                    const int it = nt * a.nkt + kt, s = it % kStages;
-                    const uint32_t ph = (uint32_t)(it / kStages) & 1u;
-                    ok = !*(volatile int *)abort_flag && mbar_wait(&full[s], ph, a.st, 0x700u + s);
-                    if (!ok) {
+        }
+    } else if (warp == 2) {
+        // ------------------------------------------------------- MMA issue
+        if (lane == 0) {
+            int it = 0, jb = 0;
+            bool run = true;
+            for (JobIter J(a, nu); run && J.valid(); J.next(), jb++) {
+                const int nmma = (J.nn() + 15) / 16 * 16;
+                const int buf = jb & 1;
+                // the epilogue has finished with this accumulator (two tiles ago)
+                if (*(volatile int *)abort_flag ||
+                    !mbar_wait(&acc_empty[buf], ((uint32_t)(jb >> 1) & 1u) ^ 1u, a.st, 0x680u + buf)) {
+                    *abort_flag = 1;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t acc = tmem + (uint32_t)(buf * tpi * a.BN);
+                for (int kt = 0; kt < a.nkt; kt++, it++) {
+                    const int s = it % ns;
+                    const uint32_t ph = (uint32_t)(it / ns) & 1u;
+                    if (*(volatile int *)abort_flag || !mbar_wait(&full[s], ph, a.st, 0x700u + s)) {
                         *abort_flag = 1;
+                        run = false;
                         break;
                     }
+                    // the scale factors were written by the generic proxy (cp.async);
+                    // tcgen05.cp reads them through the async proxy
+                    fence_proxy_async_smem();
                     tc_fence_after();
-                    const uint32_t sfa_t = tmem + sf_col0 + (uint32_t)s * (4u + 4u * nsfb);
-                    const uint32_t sfb_t = sfa_t + 4u;
-                    tc_cp_sf(sfa_t, smem_desc(smem_u32(sSFA + (size_t)s * 512), 128, 128, kSwizzleNone));
+                    const uint32_t sfa_t = tmem + sf_col0 + (uint32_t)s * sf_stage;  // + 4t for tile t
+                    const uint32_t sfb_t = sfa_t + 4u * (uint32_t)tpi;
+                    for (int t = 0; t < tpi; t++)
+                        tc_cp_sf(sfa_t + 4u * t,
+                                 smem_desc(smem_u32(sSFA + ((size_t)s * tpi + t) * 512), 128, 128, kSwizzleNone));
                     for (int at = 0; at < nsfb; at++)
                         tc_cp_sf(sfb_t + 4u * at,
                                  smem_desc(smem_u32(sSFB + ((size_t)s * nsfb + at) * 512), 128, 128, kSwizzleNone));
-                    const uint32_t a_base = smem_u32(sA + (size_t)s * kTileM * kTileK);
                     const uint32_t b_base = smem_u32(sB + (size_t)s * a.BN * kTileK);
+                    for (int t = 0; t < tpi; t++) {
+                        // tile t: rows 128t.. of the stage's A (16 KB apart), accumulator columns t*BN..
+                        const uint32_t a_base = smem_u32(sA + ((size_t)s * tpi + t) * kTileM * kTileK);
 #pragma unroll
-                    for (int ks = 0; ks < kTileK / 32; ks++) {
-                        const uint64_t ad = smem_desc(a_base + 32 * ks, 16, 1024, kSwizzle128B);
-                        const uint64_t bd = smem_desc(b_base + 32 * ks, 16, 1024, kSwizzle128B);
-                        tc_mma(tmem, ad, bd, idesc_mxf8f6f4(nmma, ks), sfa_t, sfb_t, (kt > 0 || ks > 0) ? 1u : 0u);
+                        for (int ks = 0; ks < kTileK / 32; ks++) {
+                            const uint64_t ad = smem_desc(a_base + 32 * ks, 16, 1024, kSwizzle128B);
+                            const uint64_t bd = smem_desc(b_base + 32 * ks, 16, 1024, kSwizzle128B);
+                            tc_mma(acc + (uint32_t)(t * a.BN), ad, bd, idesc_mxf8f6f4(nmma, ks), sfa_t + 4u * t, sfb_t,
+                                   (kt > 0 || ks > 0) ? 1u : 0u);
+                        }
                     }
                     tc_commit(&empty[s]);  // frees the stage when these MMAs have read it
                 }
-                tc_commit(done);           // accumulator complete (or as far as it got)
+                tc_commit(&acc_full[buf]);  // the accumulator is complete (or as far as it got)
             }
+        }
+        __syncwarp();
+    } else if (warp >= 4) {
+        // ------------------------------------------------------- epilogue
+        const int ew = warp - 4;
+        int jb = 0;
+        for (JobIter J(a, nu); J.valid(); J.next(), jb++) {
+            const int buf = jb & 1;
+            const int nn = J.nn(), nmma = (nn + 15) / 16 * 16;
+            bool okl = !*(volatile int *)abort_flag &&
+                       mbar_wait(&acc_full[buf], (uint32_t)(jb >> 1) & 1u, a.st, 0x800u + buf);
+            if (!okl) *abort_flag = 1;
+            const bool ok = __all_sync(0xffffffffu, okl);  // warp-uniform for the .sync.aligned loads
+            tc_fence_after();
+            for (int t = 0; t < tpi; t++) {
+                if (J.mt + t >= a.nmt) break;  // a half item past the expert's A rows (uniform)
+                const uint32_t lane_base =
+                    tmem + (uint32_t)((buf * tpi + t) * a.BN) + ((uint32_t)(32 * ew) << 16);
+                if (a.nparts == 3)
+                    epilogue_split3(a, lane_base, ok, nn, nmma, J.mt + t, J.row0, J.n0(), ew, lane, amax_x);
+                else
+                    epilogue_mx1(a, lane_base, ok, nn, nmma, J.mt + t, J.row0, J.n0(), ew, lane, amax_x);
+            }
+            tc_fence_before();
             __syncwarp();
+            if (lane == 0) mbar_arrive(&acc_empty[buf]);
+            // no early exit: after an abort the waits are skipped, and all four warps
+            // run the same sequence of named barriers to the end
         }
-
-        // ------------------------------------------------------------ epilogue
-        const bool okl = mbar_wait(done, (uint32_t)nt & 1u, a.st, 0x800u) && !*(volatile int *)abort_flag;
-        const bool ok = __all_sync(0xffffffffu, okl);  // warp-uniform for the .sync.aligned loads
-        tc_fence_after();
-        const uint32_t lane_base = tmem + ((uint32_t)(32 * warp) << 16);
-        if (a.nparts == 3) {
-            epilogue_split3(a, lane_base, ok, nn, nmma, mt, row0, n0, warp, lane, amax_x);
-        } else {
-        for (int c0 = 0; c0 < nmma; c0 += 16) {
-            float v[16];
-#pragma unroll
-            for (int j = 0; j < 16; j++) v[j] = 0.f;
-            if (ok) tmem_ld16(lane_base + (uint32_t)c0, v);
-            if (a.mode == 1) {
-                // lanes 0-15: gate rows, 16-31: up rows of the same 16 intermediate indices
-                const int i = (4 * mt + warp) * 16 + (lane & 15);
-                float hv[16];
-                float am[16];
-#pragma unroll
-                for (int j = 0; j < 16; j++) {
-                    const float u = __shfl_down_sync(0xffffffffu, v[j], 16);
-                    const float g = v[j];
-                    hv[j] = (lane < 16) ? g / (1.f + expf(-g)) * u : 0.f;
-                    float m = fabsf(hv[j]);
-#pragma unroll
-                    for (int off = 8; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-                    am[j] = m;
-                }
-                if (lane == 0) {
-#pragma unroll
-                    for (int j = 0; j < 16; j++) amax_x[warp * 16 + j] = am[j];
-                }
-                named_barrier(2, kGemmThreads);
-#pragma unroll
-                for (int j = 0; j < 16; j++) {
-                    const int n = c0 + j;
-                    const float amax = fmaxf(amax_x[warp * 16 + j], amax_x[(warp ^ 1) * 16 + j]);
-                    int X = -127;
-                    if (amax > 0.f) {
-                        int ex;
-                        frexpf(amax, &ex);
-                        X = max(-127, min(127, ex - 1 - 8));
-                    }
-                    if (ok && n < nn && lane < 16) {
-                        const uint64_t r = (uint64_t)(row0 + n0 + n);
-                        unsigned short pair;
-                        asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;"
-                            : "=h"(pair)
-                            : "f"(0.f), "f"(ldexpf(hv[j], -X)));
-                        a.hq[r * a.I + i] = (uint8_t)(pair & 0xFF);
-                        if (lane == 0 && (warp & 1) == 0) a.hs[r * a.lds_hs + i / 32] = (uint8_t)(X + 127);
-                    }
-                }
-                named_barrier(2, kGemmThreads);
-            } else {
-                const int o = mt * kTileM + 32 * warp + lane;
-#pragma unroll
-                for (int j = 0; j < 16; j++) {
-                    const int n = c0 + j;
-                    if (ok && n < nn && o < a.H) {
-                        const uint64_t r = (uint64_t)(row0 + n0 + n);
-                        if (a.partial_dtype == MOE_PARTIAL_F32)
-                            reinterpret_cast<float *>(a.partial)[r * a.H + o] = v[j];
-                        else
-                            reinterpret_cast<__nv_bfloat16 *>(a.partial)[r * a.H + o] = __float2bfloat16_rn(v[j]);
-                    }
-                }
-            }
-        }
-        }
-        tc_fence_before();
-        __syncthreads();
     }
     // nothing may still be in flight when TMEM is released and the CTA exits
     if (warp == 0 && lane == 0) {
-        for (int it = max(0, it_issued - kStages); it < it_issued; it++)
-            mbar_wait(&full[it % kStages], (uint32_t)(it / kStages) & 1u, a.st, 0x900u);
+        for (int it = max(0, it_issued - ns); it < it_issued; it++)
+            mbar_wait(&full[it % ns], (uint32_t)(it / ns) & 1u, a.st, 0x900u);
     }
     __syncthreads();
     tc_fence_after();
@@ -505,10 +596,10 @@ cudaError_t get_encoder() {
 // A: packed E2M1 weights of all experts, [E][rows][K] with the given strides,
 // unpacked by the copy to 16 elements per 16 bytes (the f8f6f4 operand format).
 cudaError_t make_map_a(CUtensorMap *m, const void *base, int K, int rows, int E, uint64_t row_stride,
-                       uint64_t rec) {
+                       uint64_t rec, int box_rows) {
     cuuint64_t dims[3] = {(cuuint64_t)K, (cuuint64_t)rows, (cuuint64_t)E};
     cuuint64_t strides[2] = {row_stride, rec};
-    cuuint32_t box[3] = {kTileK, kTileM, 1};
+    cuuint32_t box[3] = {kTileK, (cuuint32_t)box_rows, 1};
     cuuint32_t es[3] = {1, 1, 1};
     CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 3, const_cast<void *>(base), dims, strides, box, es,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -516,11 +607,11 @@ cudaError_t make_map_a(CUtensorMap *m, const void *base, int K, int rows, int E,
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-// B: E4M3 rows [P][K] (one byte per element), boxes of 16 rows.
-cudaError_t make_map_b(CUtensorMap *m, const void *base, int K, int P) {
+// B: E4M3 rows [P][K] (one byte per element), boxes of box_rows rows.
+cudaError_t make_map_b(CUtensorMap *m, const void *base, int K, int P, int box_rows) {
     cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)P};
     cuuint64_t strides[1] = {(cuuint64_t)K};
-    cuuint32_t box[2] = {kTileK, kBoxN};
+    cuuint32_t box[2] = {kTileK, (cuuint32_t)box_rows};
     cuuint32_t es[2] = {1, 1};
     CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, es,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -535,6 +626,8 @@ uint32_t pow2_at_least(uint32_t v) {
 }
 
 int g_gemm_smem = 0;
+int g_smem_max = 0;
+int g_sms = 0;
 
 }  // namespace
 
@@ -552,15 +645,28 @@ cudaError_t launch_grouped_gemms(const PoolView &v, int T, int k, const int32_t 
         BN = (3 * T + 47) / 48 * 48;
         if (BN > kMaxBN) return cudaErrorNotSupported;
     } else {
-        // accumulator columns per tile: about twice the mean rows per expert, 32..256
+        // accumulator columns per tile: about twice the mean rows per expert, 32..192
         const int mean = (P + v.E - 1) / v.E;
         BN = (2 * mean + 16 + 31) / 32 * 32;
         BN = BN < 32 ? 32 : (BN > kMaxBN ? kMaxBN : BN);
     }
     const int nsfb = (BN + 127) / 128;
-    const uint32_t tmem_cols = pow2_at_least((uint32_t)(BN + kStages * (4 + 4 * nsfb)));
+    if (g_smem_max == 0) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&g_smem_max, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+        cudaDeviceGetAttribute(&g_sms, cudaDevAttrMultiProcessorCount, dev);
+    }
+    // Work items of two 128-row tiles (one 256-row tensor copy of A, 16 KB, which the
+    // copy engine streams at about twice the rate of 8 KB copies) while their four
+    // accumulators fit in TMEM, else single tiles.
+    const int tpi = BN <= 96 ? 2 : 1;
+    // as many pipeline stages as fit (one CTA per SM)
+    int ns = kMaxStages;
+    while (ns > 2 && GemmSmemLayout(BN, ns, tpi).total + 1024 > (uint32_t)g_smem_max) ns--;
+    const uint32_t tmem_cols = pow2_at_least((uint32_t)(2 * tpi * BN + ns * (4 * tpi + 4 * nsfb)));
     if (tmem_cols > 512) return cudaErrorNotSupported;
-    const GemmSmemLayout L(BN);
+    const GemmSmemLayout L(BN, ns, tpi);
     const size_t smem = L.total + 1024;  // alignment slack
     e = ensure_dynamic_smem(grouped_gemm_kernel, smem, g_gemm_smem);
     if (e != cudaSuccess) return e;
@@ -572,8 +678,10 @@ cudaError_t launch_grouped_gemms(const PoolView &v, int T, int k, const int32_t 
     ga.offsets = offsets;
     ga.uexp = g.uexp;
     ga.n_union = g.n_union;
-    const int ngy = P < v.E ? P : v.E;  // at most this many experts have pairs
+    const int nexp = P < v.E ? P : v.E;  // at most this many experts have pairs
     ga.BN = BN;
+    ga.ns = ns;
+    ga.tpi = tpi;
     ga.tmem_cols = tmem_cols;
     ga.I = v.I;
     ga.H = v.H;
@@ -587,8 +695,8 @@ cudaError_t launch_grouped_gemms(const PoolView &v, int T, int k, const int32_t 
 
     // GEMM 1: gate/up
     CUtensorMap mA, mB;
-    if ((e = make_map_a(&mA, v.base, v.H, 2 * v.I, v.E, (uint64_t)v.ld_gu, v.rec)) != cudaSuccess) return e;
-    if ((e = make_map_b(&mB, g.xq, v.H, nparts * P)) != cudaSuccess) return e;
+    if ((e = make_map_a(&mA, v.base, v.H, 2 * v.I, v.E, (uint64_t)v.ld_gu, v.rec, tpi * kTileM)) != cudaSuccess) return e;
+    if ((e = make_map_b(&mB, g.xq, v.H, nparts * P, BN)) != cudaSuccess) return e;
     ga.mode = 1;
     ga.Kel = v.H;
     ga.nkt = v.H / kTileK;
@@ -600,13 +708,17 @@ cudaError_t launch_grouped_gemms(const PoolView &v, int T, int k, const int32_t 
     ga.bscale = g.xs;
     {
         TraceScope trace_scope("gemm_gateup", stream);
-        grouped_gemm_kernel<<<dim3(2 * v.I / kTileM, ngy), kGemmThreads, smem, stream>>>(mA, mB, ga);
+        ga.nmt = 2 * v.I / kTileM;
+        ga.nrows_a = 2 * v.I;
+        grouped_gemm_kernel<<<std::min(g_sms, nexp * ((ga.nmt + tpi - 1) / tpi)), kGemmThreads, smem, stream>>>(mA, mB,
+                                                                                                            ga);
     }
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
     // GEMM 2: down
-    if ((e = make_map_a(&mA, v.base + v.off_d, v.Ip, v.H, v.E, (uint64_t)v.ld_d, v.rec)) != cudaSuccess) return e;
-    if ((e = make_map_b(&mB, g.hq, v.I, nparts * P)) != cudaSuccess) return e;
+    if ((e = make_map_a(&mA, v.base + v.off_d, v.Ip, v.H, v.E, (uint64_t)v.ld_d, v.rec, tpi * kTileM)) != cudaSuccess)
+        return e;
+    if ((e = make_map_b(&mB, g.hq, v.I, nparts * P, BN)) != cudaSuccess) return e;
     ga.mode = 2;
     ga.Kel = v.I;
     ga.nkt = v.Ip / kTileK;
@@ -618,7 +730,10 @@ cudaError_t launch_grouped_gemms(const PoolView &v, int T, int k, const int32_t 
     ga.bscale = g.hs;
     {
         TraceScope trace_scope("gemm_down", stream);
-        grouped_gemm_kernel<<<dim3(v.H / kTileM, ngy), kGemmThreads, smem, stream>>>(mA, mB, ga);
+        ga.nmt = v.H / kTileM;
+        ga.nrows_a = v.H;
+        grouped_gemm_kernel<<<std::min(g_sms, nexp * ((ga.nmt + tpi - 1) / tpi)), kGemmThreads, smem, stream>>>(mA, mB,
+                                                                                                            ga);
     }
     return cudaGetLastError();
 }
