@@ -69,7 +69,10 @@ enum { MOE_PARTIAL_F32 = 0, MOE_PARTIAL_BF16 = 1 };
  * [2I][H], and W_d [H][I], as packed E2M1 codes (two per byte, element 2j in
  * the low nibble, K contiguous) followed by their E8M0 scale bytes (one per 32
  * consecutive K elements, row-major).  Rows of W_d are padded with zero codes and
- * zero scale bytes to a multiple of 128 elements. */
+ * zero scale bytes to a multiple of 128 elements.  The record ends with the same
+ * scale bytes once more, reordered for the tensor-core path (for each K tile of 128
+ * elements and 128-row tile, one 512-byte block: row 128mt + 32q + l keeps the
+ * tile's 4 scale bytes at 16l + 4q); the pool functions write both copies. */
 
 /* Bytes one pool of E experts needs (a multiple of 1024 per record); 0 when the
  * shape is unsupported. */

@@ -31,7 +31,13 @@ PoolView make_view(uint8_t *base, int E, int H, int I) {
     v.off_d = gu_codes;
     v.off_sgu = gu_codes + d_codes;
     v.off_sd = v.off_sgu + gu_scales;
-    v.rec = (gu_codes + d_codes + gu_scales + d_scales + 1023) / 1024 * 1024;
+    v.nmt_gu = (2 * I + 127) / 128;
+    v.nmt_d = H / 128;
+    const uint64_t gu_mma = (uint64_t)(H / 128) * v.nmt_gu * 512;
+    const uint64_t d_mma = (uint64_t)(v.Ip / 128) * v.nmt_d * 512;
+    v.off_sgu_mma = align_up(v.off_sd + d_scales, 1024);
+    v.off_sd_mma = v.off_sgu_mma + align_up(gu_mma, 1024);
+    v.rec = align_up(v.off_sd_mma + d_mma, 1024);
     return v;
 }
 

@@ -11,12 +11,13 @@
 //
 // Persistent: one CTA per SM walks the (expert with pairs, 128-row tile of A) items
 // with a stride of the grid, with as many pipeline stages as shared memory holds
-// (the stream of K steps runs on across items).  8 warps: warp 0 issues the tensor
-// copies of A and B, warp 1 stages the scale factors in shared memory in the
-// 32x16-byte layout tcgen05.cp expects, warp 2 owns TMEM and issues the MMAs into
-// one of two accumulators, and warps 4-7 run the epilogue of the other
-// accumulator (warp 4+w reads TMEM lanes 32w..32w+31), so a tile's epilogue
-// overlaps the next tile's MMAs.  With three-part activations (nparts = 3, the
+// (the stream of K steps runs on across items).  8 warps: warp 0 issues a stage's
+// four copies (the tensor copies of A and B, and one bulk copy each of their scale
+// factors, which both operands keep in memory already in the 32x16-byte layout
+// tcgen05.cp expects: the pool's tensor-core scale planes and the tile-ordered
+// activation scales), warp 2 owns TMEM and issues the MMAs into one of two
+// accumulators, and warps 4-7 run the epilogue of the other accumulator (warp 4+w
+// reads TMEM lanes 32w..32w+31), so a tile's epilogue overlaps the next tile's MMAs.  With three-part activations (nparts = 3, the
 // multi-token decode) each sorted pair has three B rows whose columns the
 // epilogue sums.  Every wait is bounded (MOE_ERR_TIMEOUT), and nothing exits with
 // copies or MMAs in flight.
@@ -35,38 +36,33 @@ constexpr int kMaxStages = 12;
 constexpr int kTileM = 128;
 constexpr int kTileK = 128;   // elements (bytes in shared memory for both operands)
 
-constexpr int kGemmThreads = 256;  // warps: 0 copies, 1 scale factors, 2 MMA, 4-7 epilogue
+constexpr int kGemmThreads = 256;  // warps: 0 copies, 2 MMA, 4-7 epilogue (1 and 3 idle)
 constexpr int kEpiThreads = 128;
-constexpr int kMaxBN = 192;        // two accumulators + scale factors fit in 512 TMEM columns
 
 struct GemmArgs {
     int mode;            // 1: gate/up + SwiGLU + MXFP8, 2: down
     int E;
-    int Kel;             // K elements (H for gate/up, I for down)
     int nkt;             // K tiles of 128
-    int nkb_a;           // scale blocks per A row present in the pool (H/32 or Ip/32)
-    int nkb_b;           // valid scale blocks per B row (H/32 or I/32)
-    int lds_a;           // bytes per A scale row
-    int lds_b;           // bytes per B scale row
-    uint64_t a_scale_off;  // offset of A's scale plane in a record
+    uint64_t a_sf_off;   // offset in a record of A's scale factors in tensor-core order [nkt][nmt][512]
     const uint8_t *pool;
     uint64_t rec;
     const int32_t *offsets;
-    const int32_t *uexp;     // experts with pairs (grid.y indexes this list)
+    const int32_t *tile_off;  // first column tile of each expert
+    const int32_t *uexp;      // experts with pairs
     const int32_t *n_union;
-    const uint8_t *bscale;   // xs or hs, [P][lds_b]
+    const uint8_t *bscale;    // xs or hs in tile order (sf_tile_word), nkt K tiles
     int BN;              // columns of the accumulator tile (multiple of 16)
+    int nsfb;            // 512-byte scale atoms of B per K tile = ceil(BN / 128)
     int ns;              // pipeline stages
     int nmt;             // 128-row tiles of A per expert
     int tpi;             // 128-row tiles per work item (1, or 2: one 256-row tensor copy of A)
-    int nrows_a;         // rows of A per expert (2I or H)
     uint32_t tmem_cols;
     // epilogue outputs
     int I;               // intermediate size (gate/up epilogue)
     int H;               // hidden size (down epilogue)
     uint8_t *hq;         // [P][I]
-    uint8_t *hs;         // [P][lds_hs]
-    int lds_hs;
+    uint8_t *hs;         // tile order, nkt_h K tiles
+    int nkt_h;           // Ip / 128
     void *partial;       // [P][H]
     int partial_dtype;
     int nparts;          // activation rows per pair (1, or 3 for the exact split)
@@ -133,16 +129,21 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-// 4-byte asynchronous copy global -> shared; bytes past src_bytes (0..4) are zero.
-__device__ __forceinline__ void cp_async4(void *dst, const void *src, uint32_t src_bytes) {
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(src_bytes)
+// Bulk copy global -> shared without a cache hint (16-byte aligned, size a
+// multiple of 16), completion counted in bytes on `bar`.
+__device__ __forceinline__ void bulk_g2s_l2(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_u32(dst)),
+                 "l"(src), "r"(bytes), "r"(smem_u32(bar))
                  : "memory");
 }
 
-// Arrive on `bar` once this thread's earlier cp.async copies have landed (the
-// arrival is one of the barrier's expected arrivals).
-__device__ __forceinline__ void cp_async_arrive(uint64_t *bar) {
-    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+// True in one lane of the converged warp (the lowest active lane, lane 0 in the
+// roles below, so a thread's tcgen05 operations and their commits stay together).
+__device__ __forceinline__ bool elect_one() {
+    uint32_t p;
+    asm volatile("{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\tselp.u32 %0, 1, 0, e;\n\t}" : "=r"(p));
+    return p != 0;
 }
 
 __device__ __forceinline__ void tc_cp_sf(uint32_t taddr, uint64_t sdesc) {
@@ -183,7 +184,7 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
 // h = silu(g) * u, written as three E4M3 parts per 32-block along I (split_part);
 // down: the unweighted expert output row in fp32.
 __device__ __forceinline__ void epilogue_split3(const GemmArgs &a, uint32_t lane_base, bool ok, int nn, int nmma, int mt,
-                                                int row0, int n0, int warp, int lane, float *amax_x) {
+                                                int row0, int n0, int tile, int warp, int lane, float *amax_x) {
     for (int c0 = 0; c0 < nmma; c0 += 48) {
         float v0[16], v1[16], v2[16];
 #pragma unroll
@@ -232,7 +233,10 @@ __device__ __forceinline__ void epilogue_split3(const GemmArgs &a, uint32_t lane
                     if (ok && j < npair && lane < 16) {
                         const uint64_t r = (uint64_t)3 * (pair0 + j) + q;
                         a.hq[r * a.I + i] = code;
-                        if (lane == 0 && (warp & 1) == 0) a.hs[r * a.lds_hs + i / 32] = (uint8_t)(X + 127);
+                        // column of row r in the tile: c0 + 3j + q (row0 + n0 is a multiple of 3)
+                        if (lane == 0 && (warp & 1) == 0)
+                            a.hs[sf_tile_word(tile, a.nkt_h, a.nsfb, i >> 7, c0 + 3 * j + q) + ((i >> 5) & 3)] =
+                                (uint8_t)(X + 127);
                     }
                 }
                 named_barrier(2, kEpiThreads);
@@ -253,7 +257,7 @@ __device__ __forceinline__ void epilogue_split3(const GemmArgs &a, uint32_t lane
 // quantised to MXFP8 along I (OCP rule); down -> expert output rows.  ew = warp
 // index within the epilogue warpgroup (TMEM lanes 32ew..32ew+31).
 __device__ __forceinline__ void epilogue_mx1(const GemmArgs &a, uint32_t lane_base, bool ok, int nn, int nmma, int mt,
-                                             int row0, int n0, int ew, int lane, float *amax_x) {
+                                             int row0, int n0, int tile, int ew, int lane, float *amax_x) {
     for (int c0 = 0; c0 < nmma; c0 += 16) {
         float v[16];
 #pragma unroll
@@ -294,7 +298,8 @@ __device__ __forceinline__ void epilogue_mx1(const GemmArgs &a, uint32_t lane_ba
                     unsigned short pair;
                     asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(pair) : "f"(0.f), "f"(ldexpf(hv[j], -X)));
                     a.hq[r * a.I + i] = (uint8_t)(pair & 0xFF);
-                    if (lane == 0 && (ew & 1) == 0) a.hs[r * a.lds_hs + i / 32] = (uint8_t)(X + 127);
+                    if (lane == 0 && (ew & 1) == 0)
+                        a.hs[sf_tile_word(tile, a.nkt_h, a.nsfb, i >> 7, n) + ((i >> 5) & 3)] = (uint8_t)(X + 127);
                 }
             }
             named_barrier(2, kEpiThreads);
@@ -335,7 +340,7 @@ struct GemmSmemLayout {
 // BN.  Every role walks this same sequence.
 struct JobIter {
     const GemmArgs &a;
-    int nu, i, nt, ntile, e, mt, row0, nrows;
+    int nu, i, nt, ntile, e, mt, row0, nrows, tile0;
     __device__ JobIter(const GemmArgs &args, int nu_) : a(args), nu(nu_), i((int)blockIdx.x), nt(0), ntile(0) { load(); }
     __device__ void load() {
         ntile = 0;
@@ -347,6 +352,7 @@ struct JobIter {
             row0 = a.nparts * a.offsets[e];
             nrows = a.nparts * (a.offsets[e + 1] - a.offsets[e]);
             ntile = (nrows + a.BN - 1) / a.BN;
+            tile0 = a.tile_off[e];
             if (ntile > 0) break;
             i += (int)gridDim.x;
         }
@@ -354,6 +360,7 @@ struct JobIter {
     }
     __device__ bool valid() const { return i < nu * ((a.nmt + a.tpi - 1) / a.tpi) && ntile > 0; }
     __device__ int n0() const { return nt * a.BN; }
+    __device__ int tile() const { return tile0 + nt; }
     __device__ int nn() const { return min(a.BN, nrows - nt * a.BN); }
     __device__ void next() {
         if (++nt >= ntile) {
@@ -384,16 +391,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nu = *a.n_union;
     if ((int)blockIdx.x >= nu * ((a.nmt + tpi - 1) / tpi)) return;  // the whole CTA, before any barrier
-    const int nsfb = (a.BN + 127) / 128;
+    const int nsfb = a.nsfb;
 
     // The unpacked E2M1 copies write 8 of every 16 bytes of an A tile; keep the
-    // other 8 (which the MMA format pads with) zero for the whole kernel.
+    // other 8 (which the MMA format pads with) zero for the whole kernel.  The
+    // scale-factor areas start at zero too (the second tile of an item past the
+    // expert's last row tile gets no copy and reads whatever is there).
     for (int i = threadIdx.x; i < ns * tpi * kTileM * kTileK / 16; i += kGemmThreads)
         reinterpret_cast<uint4 *>(sA)[i] = make_uint4(0u, 0u, 0u, 0u);
+    for (int i = threadIdx.x; i < ns * (tpi + nsfb) * 512 / 16; i += kGemmThreads)
+        reinterpret_cast<uint4 *>(sSFA)[i] = make_uint4(0u, 0u, 0u, 0u);  // sSFB follows sSFA
     fence_proxy_async_smem();
     if (threadIdx.x == 0) {
         for (int s = 0; s < ns; s++) {
-            mbar_init(&full[s], 33);  // producer's expect-tx arrival + 32 scale-factor lanes' copies
+            mbar_init(&full[s], 1);   // producer's expect-tx arrival
             mbar_init(&empty[s], 1);  // MMA commit
         }
         for (int b = 0; b < 2; b++) {
@@ -412,124 +423,94 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const uint32_t sf_stage = 4u * (uint32_t)tpi + 4u * (uint32_t)nsfb;  // TMEM columns per stage
 
     int it_issued = 0;  // producer: stages issued
+    // The copy and MMA roles run their loops with the whole warp converged (waits
+    // polled by lane 0 and broadcast), so the addresses, coordinates and descriptors
+    // are warp-uniform values; one elected lane issues the asynchronous operations.
     if (warp == 0) {
         // ------------------------------------------------------- tensor copies
-        if (lane == 0) {
-            int it = 0;
-            bool run = true;
-            for (JobIter J(a, nu); run && J.valid(); J.next()) {
-                const int nmma = (J.nn() + 15) / 16 * 16;
-                for (int kt = 0; kt < a.nkt; kt++, it++) {
-                    const int s = it % ns;
-                    const uint32_t ph = (uint32_t)(it / ns) & 1u;
-                    if (*(volatile int *)abort_flag || !mbar_wait(&empty[s], ph ^ 1u, a.st, 0x500u + s)) {
-                        *abort_flag = 1;
-                        run = false;
-                        break;
-                    }
-                    // A arrives unpacked (16 E2M1 values in each 16 bytes, 8 of them data) and
-                    // counts its packed bytes; B counts one byte per element
-                    // B: one copy of BN rows (rows past this tile's nmma belong to other
-                    // experts or are out of range and zero; the MMA does not read them)
-                    mbar_arrive_expect_tx(&full[s], (uint32_t)(tpi * kTileM * kTileK / 2 + a.BN * kTileK));
-                    tma_load_3d(sA + (size_t)s * tpi * kTileM * kTileK, &tmA, kt * kTileK, J.mt * kTileM, J.e, &full[s]);
-                    tma_load_2d(sB + (size_t)s * a.BN * kTileK, &tmB, kt * kTileK, J.row0 + J.n0(), &full[s]);
-                    it_issued = it + 1;
-                }
-            }
-        }
-        __syncwarp();
-    } else if (warp == 1) {
-        // ------------------------------------------------------- scale factors
-        // Of K-tile kt: A rows mt*128 + lane + 32 q and B columns n0 + at*128 + lane + 32 q,
-        // scale blocks 4kt .. 4kt+3 (4 bytes each), copied asynchronously into the stage
-        // in the layout tcgen05.cp expects (row r at (r % 32) * 16 + (r / 32) * 4).  Each
-        // lane's arrival on full[s] waits for its own copies, so the warp runs as many
-        // stages ahead as the pipeline allows.
-        int it = 0;
+        int it = 0, s = 0;  // stages issued; slot of stage it
+        uint32_t ph = 0;    // phase parity of slot s's use by stage it
         bool run = true;
         for (JobIter J(a, nu); run && J.valid(); J.next()) {
-            const uint8_t *sa = a.pool + (uint64_t)J.e * a.rec + a.a_scale_off;
-            const int nn = J.nn(), base_row = J.row0 + J.n0();
             for (int kt = 0; kt < a.nkt; kt++, it++) {
-                const int s = it % ns;
-                const uint32_t ph = (uint32_t)(it / ns) & 1u;
-                int okl = 0;
-                if (lane == 0) okl = !*(volatile int *)abort_flag && mbar_wait(&empty[s], ph ^ 1u, a.st, 0x600u + s);
-                const bool ok = __shfl_sync(0xffffffffu, okl, 0) != 0;  // warp-uniform
-                if (!ok) {
+                int okl = 1;
+                if (lane == 0) okl = !*(volatile int *)abort_flag && mbar_wait(&empty[s], ph ^ 1u, a.st, 0x500u + s);
+                if (!__shfl_sync(0xffffffffu, okl, 0)) {
                     if (lane == 0) *abort_flag = 1;
                     run = false;
                     break;
                 }
-                uint8_t *dA = sSFA + (size_t)s * tpi * 512;
-                const uint32_t a_bytes = 4 * kt + 3 < a.nkb_a ? 4u : 0u;
-                for (int q = 0; q < 4 * tpi; q++) {
-                    // row of A; rows past the expert's A rows (the copy zero-fills them) get zero scales
-                    const int r = J.mt * kTileM + lane + 32 * q;
-                    const bool in = r < a.nrows_a && a_bytes != 0;
-                    cp_async4(dA + (q >> 2) * 512 + lane * 16 + (q & 3) * 4,
-                              sa + (uint64_t)(in ? r : 0) * a.lds_a + (in ? 4 * kt : 0), in ? a_bytes : 0u);
+                // A arrives unpacked (16 E2M1 values in each 16 bytes, 8 of them data) and
+                // counts its packed bytes; B counts one byte per element
+                // B: one copy of BN rows (rows past this tile's nmma belong to other
+                // experts or are out of range and zero; the MMA does not read them)
+                // scale factors: the item's row tiles of A (adjacent in the plane) and
+                // the column tile's atoms of B, each one contiguous block
+                const uint32_t a_tiles = (uint32_t)min(tpi, a.nmt - J.mt);
+                const uint32_t tx = (uint32_t)(tpi * kTileM * kTileK / 2 + a.BN * kTileK) + (a_tiles + (uint32_t)nsfb) * 512u;
+                const uint8_t *sfa_src = a.pool + (uint64_t)J.e * a.rec + a.a_sf_off + ((uint64_t)kt * a.nmt + J.mt) * 512;
+                const uint8_t *sfb_src = a.bscale + sf_tile_word(J.tile(), a.nkt, nsfb, kt, 0);
+                const int brow = J.row0 + J.n0();
+                if (elect_one()) {
+                    mbar_arrive_expect_tx(&full[s], tx);
+                    tma_load_3d(sA + (size_t)s * tpi * kTileM * kTileK, &tmA, kt * kTileK, J.mt * kTileM, J.e, &full[s]);
+                    tma_load_2d(sB + (size_t)s * a.BN * kTileK, &tmB, kt * kTileK, brow, &full[s]);
+                    bulk_g2s_l2(sSFA + (size_t)s * tpi * 512, sfa_src, a_tiles * 512u, &full[s]);
+                    bulk_g2s_l2(sSFB + (size_t)s * nsfb * 512, sfb_src, (uint32_t)nsfb * 512u, &full[s]);
                 }
-                // valid scale bytes of B in this K-tile (the rest of the word is zero)
-                const int vb = min(4, max(0, a.nkb_b - 4 * kt));
-                for (int at = 0; at < nsfb; at++) {
-                    uint8_t *dB = sSFB + ((size_t)s * nsfb + at) * 512;
-#pragma unroll
-                    for (int q = 0; q < 4; q++) {
-                        const int c = at * 128 + lane + 32 * q;
-                        const bool in = c < nn && vb > 0;
-                        cp_async4(dB + lane * 16 + q * 4,
-                                  a.bscale + (uint64_t)(in ? base_row + c : base_row) * a.lds_b + (in ? 4 * kt : 0),
-                                  in ? (uint32_t)vb : 0u);
-                    }
+                __syncwarp();
+                it_issued = it + 1;
+                if (++s == ns) {
+                    s = 0;
+                    ph ^= 1u;
                 }
-                cp_async_arrive(&full[s]);
             }
         }
     } else if (warp == 2) {
         // ------------------------------------------------------- MMA issue
-        if (lane == 0) {
-            int it = 0, jb = 0;
-            bool run = true;
-            for (JobIter J(a, nu); run && J.valid(); J.next(), jb++) {
-                const int nmma = (J.nn() + 15) / 16 * 16;
-                const int buf = jb & 1;
-                // the epilogue has finished with this accumulator (two tiles ago)
-                if (*(volatile int *)abort_flag ||
-                    !mbar_wait(&acc_empty[buf], ((uint32_t)(jb >> 1) & 1u) ^ 1u, a.st, 0x680u + buf)) {
-                    *abort_flag = 1;
+        int jb = 0, s = 0;  // tiles; slot of the next stage
+        uint32_t ph = 0;    // its phase parity
+        bool run = true;
+        for (JobIter J(a, nu); run && J.valid(); J.next(), jb++) {
+            const int nmma = (J.nn() + 15) / 16 * 16;
+            const int buf = jb & 1;
+            // the epilogue has finished with this accumulator (two tiles ago)
+            int okl = 1;
+            if (lane == 0)
+                okl = !*(volatile int *)abort_flag &&
+                      mbar_wait(&acc_empty[buf], ((uint32_t)(jb >> 1) & 1u) ^ 1u, a.st, 0x680u + buf);
+            if (!__shfl_sync(0xffffffffu, okl, 0)) {
+                if (lane == 0) *abort_flag = 1;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t acc = tmem + (uint32_t)(buf * tpi * a.BN);
+            for (int kt = 0; kt < a.nkt; kt++) {
+                okl = 1;
+                if (lane == 0) okl = !*(volatile int *)abort_flag && mbar_wait(&full[s], ph, a.st, 0x700u + s);
+                if (!__shfl_sync(0xffffffffu, okl, 0)) {
+                    if (lane == 0) *abort_flag = 1;
+                    run = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t acc = tmem + (uint32_t)(buf * tpi * a.BN);
-                for (int kt = 0; kt < a.nkt; kt++, it++) {
-                    const int s = it % ns;
-                    const uint32_t ph = (uint32_t)(it / ns) & 1u;
-                    if (*(volatile int *)abort_flag || !mbar_wait(&full[s], ph, a.st, 0x700u + s)) {
-                        *abort_flag = 1;
-                        run = false;
-                        break;
-                    }
-                    // the scale factors were written by the generic proxy (cp.async);
-                    // tcgen05.cp reads them through the async proxy
-                    fence_proxy_async_smem();
-                    tc_fence_after();
-                    const uint32_t sfa_t = tmem + sf_col0 + (uint32_t)s * sf_stage;  // + 4t for tile t
-                    const uint32_t sfb_t = sfa_t + 4u * (uint32_t)tpi;
+                const uint32_t sfa_t = tmem + sf_col0 + (uint32_t)s * sf_stage;  // + 4t for tile t
+                const uint32_t sfb_t = sfa_t + 4u * (uint32_t)tpi;
+                const uint32_t sfa_s = smem_u32(sSFA + (size_t)s * tpi * 512);
+                const uint32_t sfb_s = smem_u32(sSFB + (size_t)s * nsfb * 512);
+                const uint32_t a_base = smem_u32(sA + (size_t)s * tpi * kTileM * kTileK);
+                const uint32_t b_base = smem_u32(sB + (size_t)s * a.BN * kTileK);
+                if (elect_one()) {
                     for (int t = 0; t < tpi; t++)
-                        tc_cp_sf(sfa_t + 4u * t,
-                                 smem_desc(smem_u32(sSFA + ((size_t)s * tpi + t) * 512), 128, 128, kSwizzleNone));
+                        tc_cp_sf(sfa_t + 4u * t, smem_desc(sfa_s + 512u * t, 128, 128, kSwizzleNone));
                     for (int at = 0; at < nsfb; at++)
-                        tc_cp_sf(sfb_t + 4u * at,
-                                 smem_desc(smem_u32(sSFB + ((size_t)s * nsfb + at) * 512), 128, 128, kSwizzleNone));
-                    const uint32_t b_base = smem_u32(sB + (size_t)s * a.BN * kTileK);
+                        tc_cp_sf(sfb_t + 4u * at, smem_desc(sfb_s + 512u * at, 128, 128, kSwizzleNone));
                     for (int t = 0; t < tpi; t++) {
                         // tile t: rows 128t.. of the stage's A (16 KB apart), accumulator columns t*BN..
-                        const uint32_t a_base = smem_u32(sA + ((size_t)s * tpi + t) * kTileM * kTileK);
 #pragma unroll
                         for (int ks = 0; ks < kTileK / 32; ks++) {
-                            const uint64_t ad = smem_desc(a_base + 32 * ks, 16, 1024, kSwizzle128B);
+                            const uint64_t ad = smem_desc(a_base + (uint32_t)(t * kTileM * kTileK) + 32 * ks, 16, 1024,
+                                                          kSwizzle128B);
                             const uint64_t bd = smem_desc(b_base + 32 * ks, 16, 1024, kSwizzle128B);
                             tc_mma(acc + (uint32_t)(t * a.BN), ad, bd, idesc_mxf8f6f4(nmma, ks), sfa_t + 4u * t, sfb_t,
                                    (kt > 0 || ks > 0) ? 1u : 0u);
@@ -537,10 +518,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     }
                     tc_commit(&empty[s]);  // frees the stage when these MMAs have read it
                 }
-                tc_commit(&acc_full[buf]);  // the accumulator is complete (or as far as it got)
+                __syncwarp();
+                if (++s == ns) {
+                    s = 0;
+                    ph ^= 1u;
+                }
             }
+            if (elect_one()) tc_commit(&acc_full[buf]);  // the accumulator is complete (or as far as it got)
+            __syncwarp();
         }
-        __syncwarp();
     } else if (warp >= 4) {
         // ------------------------------------------------------- epilogue
         const int ew = warp - 4;
@@ -558,9 +544,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 const uint32_t lane_base =
                     tmem + (uint32_t)((buf * tpi + t) * a.BN) + ((uint32_t)(32 * ew) << 16);
                 if (a.nparts == 3)
-                    epilogue_split3(a, lane_base, ok, nn, nmma, J.mt + t, J.row0, J.n0(), ew, lane, amax_x);
+                    epilogue_split3(a, lane_base, ok, nn, nmma, J.mt + t, J.row0, J.n0(), J.tile(), ew, lane, amax_x);
                 else
-                    epilogue_mx1(a, lane_base, ok, nn, nmma, J.mt + t, J.row0, J.n0(), ew, lane, amax_x);
+                    epilogue_mx1(a, lane_base, ok, nn, nmma, J.mt + t, J.row0, J.n0(), J.tile(), ew, lane, amax_x);
             }
             tc_fence_before();
             __syncwarp();
@@ -638,19 +624,13 @@ cudaError_t launch_grouped_gemms(const PoolView &v, int T, int k, const int32_t 
     if (nparts != 1 && nparts != 3) return cudaErrorInvalidValue;
     cudaError_t e = get_encoder();
     if (e != cudaSuccess) return e;
-    int BN;
-    if (nparts == 3) {
-        // one expert has at most T pairs (distinct slots of a row): 3T columns, in
-        // whole groups of 16 pairs (48 columns), one tile
-        BN = (3 * T + 47) / 48 * 48;
-        if (BN > kMaxBN) return cudaErrorNotSupported;
-    } else {
-        // accumulator columns per tile: about twice the mean rows per expert, 32..192
-        const int mean = (P + v.E - 1) / v.E;
-        BN = (2 * mean + 16 + 31) / 32 * 32;
-        BN = BN < 32 ? 32 : (BN > kMaxBN ? kMaxBN : BN);
-    }
-    const int nsfb = (BN + 127) / 128;
+    // one expert has at most T pairs (distinct slots of a row), so with three parts
+    // all of its 3T columns fit one tile; the sort laid out the activation scales
+    // for this BN
+    const int BN = grouped_bn(P, v.E, T, nparts);
+    if (BN == 0) return cudaErrorNotSupported;
+    if (BN != g.BN) return cudaErrorInvalidValue;
+    const int nsfb = g.nsfb;
     if (g_smem_max == 0) {
         int dev = 0;
         cudaGetDevice(&dev);
@@ -676,10 +656,12 @@ cudaError_t launch_grouped_gemms(const PoolView &v, int T, int k, const int32_t 
     ga.pool = v.base;
     ga.rec = v.rec;
     ga.offsets = offsets;
+    ga.tile_off = g.tile_off;
     ga.uexp = g.uexp;
     ga.n_union = g.n_union;
     const int nexp = P < v.E ? P : v.E;  // at most this many experts have pairs
     ga.BN = BN;
+    ga.nsfb = nsfb;
     ga.ns = ns;
     ga.tpi = tpi;
     ga.tmem_cols = tmem_cols;
@@ -687,7 +669,7 @@ cudaError_t launch_grouped_gemms(const PoolView &v, int T, int k, const int32_t 
     ga.H = v.H;
     ga.hq = g.hq;
     ga.hs = g.hs;
-    ga.lds_hs = v.Ip / 32;
+    ga.nkt_h = v.Ip / kTileK;
     ga.partial = partial;
     ga.partial_dtype = partial_dtype;
     ga.nparts = nparts;
@@ -698,18 +680,12 @@ cudaError_t launch_grouped_gemms(const PoolView &v, int T, int k, const int32_t 
     if ((e = make_map_a(&mA, v.base, v.H, 2 * v.I, v.E, (uint64_t)v.ld_gu, v.rec, tpi * kTileM)) != cudaSuccess) return e;
     if ((e = make_map_b(&mB, g.xq, v.H, nparts * P, BN)) != cudaSuccess) return e;
     ga.mode = 1;
-    ga.Kel = v.H;
     ga.nkt = v.H / kTileK;
-    ga.nkb_a = v.H / 32;
-    ga.nkb_b = v.H / 32;
-    ga.lds_a = v.lds_gu;
-    ga.lds_b = v.H / 32;
-    ga.a_scale_off = v.off_sgu;
+    ga.a_sf_off = v.off_sgu_mma;
     ga.bscale = g.xs;
     {
         TraceScope trace_scope("gemm_gateup", stream);
-        ga.nmt = 2 * v.I / kTileM;
-        ga.nrows_a = 2 * v.I;
+        ga.nmt = v.nmt_gu;
         grouped_gemm_kernel<<<std::min(g_sms, nexp * ((ga.nmt + tpi - 1) / tpi)), kGemmThreads, smem, stream>>>(mA, mB,
                                                                                                             ga);
     }
@@ -720,18 +696,12 @@ cudaError_t launch_grouped_gemms(const PoolView &v, int T, int k, const int32_t 
         return e;
     if ((e = make_map_b(&mB, g.hq, v.I, nparts * P, BN)) != cudaSuccess) return e;
     ga.mode = 2;
-    ga.Kel = v.I;
     ga.nkt = v.Ip / kTileK;
-    ga.nkb_a = v.Ip / 32;
-    ga.nkb_b = v.I / 32;
-    ga.lds_a = v.lds_d;
-    ga.lds_b = v.Ip / 32;
-    ga.a_scale_off = v.off_sd;
+    ga.a_sf_off = v.off_sd_mma;
     ga.bscale = g.hs;
     {
         TraceScope trace_scope("gemm_down", stream);
-        ga.nmt = v.H / kTileM;
-        ga.nrows_a = v.H;
+        ga.nmt = v.nmt_d;
         grouped_gemm_kernel<<<std::min(g_sms, nexp * ((ga.nmt + tpi - 1) / tpi)), kGemmThreads, smem, stream>>>(mA, mB,
                                                                                                             ga);
     }

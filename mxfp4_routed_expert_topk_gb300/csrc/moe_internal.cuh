@@ -28,6 +28,13 @@ struct PoolView {
     int ld_d;           // bytes per W_d code row   = Ip/2
     int lds_gu;         // scale bytes per W_gu row = H/32
     int lds_d;          // scale bytes per W_d row  = Ip/32
+    // the same scale bytes once more in the order of the tensor-core path: for each
+    // K tile kt of 128 elements and 128-row tile mt, 512 bytes in which row
+    // mt*128 + 32q + l keeps its blocks 4kt..4kt+3 at bytes 16l + 4q + 0..3
+    uint64_t off_sgu_mma;  // W_gu: [H/128][nmt_gu][512]
+    uint64_t off_sd_mma;   // W_d:  [Ip/128][nmt_d][512]
+    int nmt_gu;         // 128-row tiles of W_gu = ceil(2I/128)
+    int nmt_d;          // 128-row tiles of W_d  = H/128
 };
 
 }  // namespace moe

@@ -6,8 +6,14 @@
 //   W_d  codes  [H][Ip/2]     Ip = I rounded up to 128 (zero padded)
 //   W_gu scales [2I][H/32]    E8M0, one per 32 elements along K
 //   W_d  scales [H][Ip/32]
-// K is contiguous everywhere, so the decode kernels stream whole rows and the
-// prefill kernels cut 128-element K tiles with the tensor-memory-accelerator.
+//   W_gu scales again, [H/128][ceil(2I/128)][512], in tensor-core order
+//   W_d  scales again, [Ip/128][H/128][512],      in tensor-core order
+// K is contiguous in the codes and the first two scale planes, so the decode
+// kernels stream whole rows and the prefill kernels cut 128-element K tiles with
+// the tensor-memory-accelerator.  The last two planes (derived from the first two
+// whenever a record is written) give the grouped GEMMs each stage's weight scale
+// factors as one contiguous 512-byte block per 128-row tile, the layout tcgen05.cp
+// copies into tensor memory, instead of 4 bytes from each of 128 rows.
 #include "moe_internal.cuh"
 
 namespace moe {
@@ -110,6 +116,31 @@ __global__ void pool_pad_kernel(PoolView v, int e_lo) {
     }
 }
 
+// The tensor-core copies of the scale planes: byte w of the 512-byte block of (K tile
+// kt, row tile mt) is scale block 4kt + w % 4 of row mt*128 + 32 ((w / 4) % 4) + w / 16
+// (0 past the matrix's rows).
+__global__ void pool_mma_scales_kernel(PoolView v, int e_lo) {
+    const int e = e_lo + blockIdx.y;
+    uint8_t *rec = v.base + (uint64_t)e * v.rec;
+    const uint64_t n_gu = (uint64_t)(v.H / 128) * v.nmt_gu * 512;
+    const uint64_t n_d = (uint64_t)(v.Ip / 128) * v.nmt_d * 512;
+    for (uint64_t j = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; j < n_gu + n_d;
+         j += (uint64_t)gridDim.x * blockDim.x) {
+        const bool gu = j < n_gu;
+        const uint64_t jj = gu ? j : j - n_gu;
+        const int nmt = gu ? v.nmt_gu : v.nmt_d;
+        const uint64_t kt = jj / ((uint64_t)nmt * 512);
+        const int mt = (int)((jj / 512) % (uint64_t)nmt);
+        const int w = (int)(jj % 512);
+        const int row = mt * 128 + ((w >> 2) & 3) * 32 + (w >> 4);
+        const uint64_t blk = 4 * kt + (uint64_t)(w & 3);
+        uint8_t val = 0;
+        if (gu && row < 2 * v.I) val = rec[v.off_sgu + (uint64_t)row * v.lds_gu + blk];
+        if (!gu && row < v.H) val = rec[v.off_sd + (uint64_t)row * v.lds_d + blk];
+        rec[(gu ? v.off_sgu_mma : v.off_sd_mma) + jj] = val;
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_pool_kernel(const PoolView &v, int mode, uint64_t seed, int e_lo, int e_hi,
@@ -128,6 +159,11 @@ cudaError_t launch_pool_kernel(const PoolView &v, int mode, uint64_t seed, int e
         pool_scales_kernel<<<dim3(gs, n), 256, 0, st>>>(v, mode, seed, e0, scales, out_scales);
         if (mode != kUnpack && v.Ip != v.I)
             pool_pad_kernel<<<dim3((v.H + 255) / 256, n), 256, 0, st>>>(v, e0);
+        if (mode != kUnpack) {
+            const uint64_t nm = ((uint64_t)(v.H / 128) * v.nmt_gu + (uint64_t)(v.Ip / 128) * v.nmt_d) * 512;
+            const unsigned gm = (unsigned)((nm + 255) / 256 < 2048 ? (nm + 255) / 256 : 2048);
+            pool_mma_scales_kernel<<<dim3(gm, n), 256, 0, st>>>(v, e0);
+        }
     }
     return cudaGetLastError();
 }

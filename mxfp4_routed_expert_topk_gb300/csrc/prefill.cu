@@ -72,16 +72,18 @@ __device__ int block_exclusive_scan(int s, int *warp_sum, int *total) {
 }
 
 // From the per-expert totals tot[0..E) (shared): offsets = their exclusive scan,
-// uexp / n_union = the experts with a non-zero total, ascending.  1024 threads.
+// uexp / n_union = the experts with a non-zero total, ascending, and tile_off = the
+// exclusive scan of each expert's column tiles ceil(nparts * tot[e] / BN).  1024 threads.
 __device__ void offsets_and_union(const int *tot, int E, int *warp_sum, int32_t *offsets, int32_t *uexp,
-                                  int32_t *n_union) {
+                                  int32_t *n_union, int32_t *tile_off, int BN, int nparts) {
     const int tid = threadIdx.x;
     const int per = (E + blockDim.x - 1) / blockDim.x;
     const int lo = tid * per, hi = min(E, lo + per);
-    int s = 0, nz = 0;
+    int s = 0, nz = 0, nt = 0;
     for (int e = lo; e < hi; e++) {
         s += tot[e];
         nz += tot[e] > 0;
+        nt += (nparts * tot[e] + BN - 1) / BN;
     }
     int total;
     int base = block_exclusive_scan(s, warp_sum, &total);
@@ -95,13 +97,21 @@ __device__ void offsets_and_union(const int *tot, int E, int *warp_sum, int32_t 
     for (int e = lo; e < hi; e++)
         if (tot[e] > 0) uexp[ub++] = e;
     if (tid == 0) *n_union = nu;
+    int ntiles;
+    int tb = block_exclusive_scan(nt, warp_sum, &ntiles);
+    for (int e = lo; e < hi; e++) {
+        tile_off[e] = tb;
+        tb += (nparts * tot[e] + BN - 1) / BN;
+    }
+    if (tid == 0) tile_off[E] = ntiles;
 }
 
 // One CTA: prior[b][e] = sum_{b'<b} cnt[b'][e]; offsets = exclusive scan of totals;
 // the list of experts that have pairs.
 __global__ void __launch_bounds__(1024) sort_scan_kernel(int nblocks, int E, const int *__restrict__ cnt,
                                                          int *__restrict__ prior, int32_t *__restrict__ offsets,
-                                                         int32_t *__restrict__ uexp, int32_t *__restrict__ n_union) {
+                                                         int32_t *__restrict__ uexp, int32_t *__restrict__ n_union,
+                                                         int32_t *__restrict__ tile_off, int BN, int nparts) {
     __shared__ int tot[kMaxSortE];
     __shared__ int warp_sum[32];
     const int tid = threadIdx.x;
@@ -114,7 +124,7 @@ __global__ void __launch_bounds__(1024) sort_scan_kernel(int nblocks, int E, con
         tot[e] = run;
     }
     __syncthreads();
-    offsets_and_union(tot, E, warp_sum, offsets, uexp, n_union);
+    offsets_and_union(tot, E, warp_sum, offsets, uexp, n_union, tile_off, BN, nparts);
 }
 
 // The whole sort in one CTA of 1024 threads for P <= 1024 pairs (multi-token
@@ -124,7 +134,8 @@ __global__ void __launch_bounds__(1024) sort_scan_kernel(int nblocks, int E, con
 __global__ void __launch_bounds__(1024) sort_small_kernel(const int32_t *__restrict__ idx, int P, int E,
                                                           int32_t *__restrict__ offsets, int32_t *__restrict__ uexp,
                                                           int32_t *__restrict__ n_union, int32_t *__restrict__ perm,
-                                                          int32_t *__restrict__ inv_perm, StatusWord *st) {
+                                                          int32_t *__restrict__ inv_perm, int32_t *__restrict__ tile_off,
+                                                          int BN, int nparts, StatusWord *st) {
     __shared__ int tot[kMaxSortE];
     __shared__ int es[1024];
     __shared__ int warp_sum[32];
@@ -142,7 +153,7 @@ __global__ void __launch_bounds__(1024) sort_small_kernel(const int32_t *__restr
     __syncthreads();
     if (e >= 0) atomicAdd(&tot[e], 1);
     __syncthreads();
-    offsets_and_union(tot, E, warp_sum, offsets, uexp, n_union);
+    offsets_and_union(tot, E, warp_sum, offsets, uexp, n_union, tile_off, BN, nparts);
     __syncthreads();  // offsets[] of this CTA's threads are visible to the others
     if (tid < P) {
         if (e < 0) {
@@ -173,18 +184,44 @@ __global__ void sort_scatter_kernel(const int32_t *__restrict__ idx, int P, int 
     inv_perm[p] = pos;
 }
 
+// Where the scale words of one activation row go: the tile-ordered block of its
+// expert's column tile (sf_tile_word), and the row's column in that tile.
+struct RowTile {
+    int tile, col;
+};
+__device__ __forceinline__ RowTile row_tile(int e, int local_row, const int32_t *tile_off, int BN) {
+    return RowTile{tile_off[e] + local_row / BN, local_row % BN};
+}
+
+// The scale words of h's padding blocks (I/32 .. Ip/32 - 1, all in the last K tile)
+// for one activation row: 0, which the gate/up epilogue overwrites for the blocks
+// below I/32.  The matching codes are zero in both operands.
+__device__ __forceinline__ void zero_h_pad(uint8_t *hs, int I, int nsfb, RowTile rt) {
+    const int ip = (I + 127) / 128 * 128;
+    if (ip != I)
+        *reinterpret_cast<uint32_t *>(hs + sf_tile_word(rt.tile, ip / 128, nsfb, ip / 128 - 1, rt.col)) = 0u;
+}
+
 // Sorted row r (one warp per row): Xs[r] = MXFP8(x[perm[r] / k]).  Shared exponent
 // X = floor(log2 amax) - 8 per 32-block (clamped to [-127, 127]); codes are
-// RNE(x / 2^X) to E4M3 with saturation.  x / 2^X is exact for bf16 input.
-__global__ void gather_quant_kernel(const uint16_t *__restrict__ x, int H, int k, int nrows,
-                                    const int32_t *__restrict__ perm, uint8_t *__restrict__ xq,
-                                    uint8_t *__restrict__ xs) {
+// RNE(x / 2^X) to E4M3 with saturation.  x / 2^X is exact for bf16 input.  Scales go
+// to the tile-ordered blocks (one 4-byte word per K tile of 128); rows at or past
+// offsets[E] (there are such rows only when a slot held an invalid expert index) are
+// left alone.
+__global__ void gather_quant_kernel(const uint16_t *__restrict__ x, int H, int I, int k, int E,
+                                    const int32_t *__restrict__ idx, const int32_t *__restrict__ perm,
+                                    const int32_t *__restrict__ offsets, const int32_t *__restrict__ tile_off, int BN,
+                                    int nsfb, uint8_t *__restrict__ xq, uint8_t *__restrict__ xs,
+                                    uint8_t *__restrict__ hs) {
     const int lane = threadIdx.x & 31;
     const int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    if (r >= nrows) return;
-    const int t = perm[r] / k;
+    if (r >= offsets[E]) return;
+    const int p = perm[r];
+    const int t = p / k, e = idx[p];
+    const RowTile rt = row_tile(e, r - offsets[e], tile_off, BN);
     const uint16_t *xr = x + (size_t)t * H;
     uint8_t *qr = xq + (size_t)r * H;
+    uint32_t word = 0;
     for (int b0 = 0; b0 < H; b0 += 32) {
         const float v = bf16_bits_to_float(xr[b0 + lane]);
         float a = fabsf(v);
@@ -199,33 +236,60 @@ __global__ void gather_quant_kernel(const uint16_t *__restrict__ x, int H, int k
         unsigned short pair;
         asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(pair) : "f"(0.f), "f"(sv));
         qr[b0 + lane] = (uint8_t)(pair & 0xFF);
-        if (lane == 0) xs[(size_t)r * (H / 32) + b0 / 32] = (uint8_t)(X + 127);
+        const int blk = b0 / 32;
+        word |= (uint32_t)(X + 127) << (8 * (blk & 3));
+        if ((blk & 3) == 3) {
+            if (lane == 0) *reinterpret_cast<uint32_t *>(xs + sf_tile_word(rt.tile, H / 128, nsfb, blk >> 2, rt.col)) = word;
+            word = 0;
+        }
     }
+    if (lane == 0) zero_h_pad(hs, I, nsfb, rt);
 }
 
 // Row r of the sorted pairs: x[perm[r] / k] as three E4M3 parts (rows 3r, 3r+1,
-// 3r+2) with one E8M0 scale per part and 32-block (split_part).  One warp per row.
-__global__ void gather_split3_kernel(const uint16_t *__restrict__ x, int H, int k, int nrows,
-                                     const int32_t *__restrict__ perm, uint8_t *__restrict__ xq,
-                                     uint8_t *__restrict__ xs) {
-    // warp = (row, group of 8 blocks of 32)
+// 3r+2) with one E8M0 scale per part and 32-block (split_part), scales in the
+// tile-ordered blocks.  One warp per (row, group of 8 blocks of 32).
+__global__ void gather_split3_kernel(const uint16_t *__restrict__ x, int H, int I, int k, int E,
+                                     const int32_t *__restrict__ idx, const int32_t *__restrict__ perm,
+                                     const int32_t *__restrict__ offsets, const int32_t *__restrict__ tile_off, int BN,
+                                     int nsfb, uint8_t *__restrict__ xq, uint8_t *__restrict__ xs,
+                                     uint8_t *__restrict__ hs) {
     const int lane = threadIdx.x & 31;
     const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int ngrp = (H / 32 + 7) / 8;
     const int r = gw / ngrp, grp = gw % ngrp;
-    if (r >= nrows) return;
-    const int t = perm[r] / k;
+    if (r >= offsets[E]) return;
+    const int p = perm[r];
+    const int t = p / k, e = idx[p];
+    RowTile rt[3];
+#pragma unroll
+    for (int q = 0; q < 3; q++) rt[q] = row_tile(e, 3 * (r - offsets[e]) + q, tile_off, BN);
     const uint16_t *xr = x + (size_t)t * H;
+    uint32_t word[3] = {0u, 0u, 0u};
     for (int b0 = grp * 256; b0 < min(H, grp * 256 + 256); b0 += 32) {
         float v = bf16_bits_to_float(xr[b0 + lane]);
+        const int blk = b0 / 32;
 #pragma unroll
         for (int q = 0; q < 3; q++) {
             float a = fabsf(v);
             for (int off = 16; off > 0; off >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, off));
             const int X = split_exp(a);
             xq[((size_t)3 * r + q) * H + b0 + lane] = split_part(v, X);
-            if (lane == 0) xs[((size_t)3 * r + q) * (H / 32) + b0 / 32] = (uint8_t)(X + 127);
+            word[q] |= (uint32_t)(X + 127) << (8 * (blk & 3));
         }
+        if ((blk & 3) == 3) {
+#pragma unroll
+            for (int q = 0; q < 3; q++) {
+                if (lane == 0)
+                    *reinterpret_cast<uint32_t *>(xs + sf_tile_word(rt[q].tile, H / 128, nsfb, blk >> 2, rt[q].col)) =
+                        word[q];
+                word[q] = 0;
+            }
+        }
+    }
+    if (lane == 0 && grp == 0) {
+#pragma unroll
+        for (int q = 0; q < 3; q++) zero_h_pad(hs, I, nsfb, rt[q]);
     }
 }
 
@@ -287,7 +351,8 @@ cudaError_t launch_grouped(const PoolView &v, const uint16_t *x, int T, const in
     }
     {
         TraceScope trace_scope("sort_scan", st);
-        sort_scan_kernel<<<1, 1024, 0, st>>>(nblocks, v.E, g.cnt, g.prior, offsets, g.uexp, g.n_union);
+        sort_scan_kernel<<<1, 1024, 0, st>>>(nblocks, v.E, g.cnt, g.prior, offsets, g.uexp, g.n_union, g.tile_off, g.BN,
+                                             1);
     }
     {
         TraceScope trace_scope("sort_scatter", st);
@@ -295,7 +360,8 @@ cudaError_t launch_grouped(const PoolView &v, const uint16_t *x, int T, const in
     }
     {
         TraceScope trace_scope("gather_quant", st);
-        gather_quant_kernel<<<(P * 32 + 255) / 256, 256, 0, st>>>(x, v.H, k, P, perm, g.xq, g.xs);
+        gather_quant_kernel<<<(P * 32 + 255) / 256, 256, 0, st>>>(x, v.H, v.I, k, v.E, idx, perm, offsets, g.tile_off,
+                                                                  g.BN, g.nsfb, g.xq, g.xs, g.hs);
     }
     cudaError_t e = launch_grouped_gemms(v, T, k, offsets, g, partial, partial_dtype, stw, st);
     if (e != cudaSuccess) return e;
@@ -315,12 +381,15 @@ cudaError_t launch_decode_multi(const PoolView &v, const uint16_t *x, int M, con
     if (P > 1024) return cudaErrorNotSupported;
     {
         TraceScope trace_scope("sort_small", st);
-        sort_small_kernel<<<1, 1024, 0, st>>>(idx, P, v.E, d.offsets, d.g.uexp, d.g.n_union, d.perm, d.inv_perm, stw);
+        sort_small_kernel<<<1, 1024, 0, st>>>(idx, P, v.E, d.offsets, d.g.uexp, d.g.n_union, d.perm, d.inv_perm,
+                                              d.g.tile_off, d.g.BN, 3, stw);
     }
     {
         TraceScope trace_scope("gather_split", st);
         const int ngrp = (v.H / 32 + 7) / 8;
-        gather_split3_kernel<<<(P * ngrp * 32 + 255) / 256, 256, 0, st>>>(x, v.H, k, P, d.perm, d.g.xq, d.g.xs);
+        gather_split3_kernel<<<(P * ngrp * 32 + 255) / 256, 256, 0, st>>>(x, v.H, v.I, k, v.E, idx, d.perm, d.offsets,
+                                                                           d.g.tile_off, d.g.BN, d.g.nsfb, d.g.xq,
+                                                                           d.g.xs, d.g.hs);
     }
     cudaError_t e = launch_grouped_gemms(v, M, k, d.offsets, d.g, d.partial, MOE_PARTIAL_F32, stw, st, 3);
     if (e != cudaSuccess) return e;

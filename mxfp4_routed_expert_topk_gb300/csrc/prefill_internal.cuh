@@ -9,6 +9,35 @@ namespace moe {
 
 constexpr int kMaxSortE = 4096;  // experts supported by the grouped path
 
+constexpr int kMaxBN = 192;      // accumulator columns of a grouped-GEMM tile
+
+// Accumulator columns per tile (BN) of the grouped GEMMs for P pairs over E experts,
+// T rows, nparts activation rows per pair; 0 when the shape is not supported.
+// nparts = 1: about twice the mean rows per expert, 32..192.  nparts = 3: all of an
+// expert's rows (at most 3T) in one tile, in whole groups of 16 pairs.
+__host__ __device__ inline int grouped_bn(int P, int E, int T, int nparts) {
+    if (nparts == 3) {
+        const int bn = (3 * T + 47) / 48 * 48;
+        return bn > kMaxBN ? 0 : bn;
+    }
+    const int mean = (P + E - 1) / E;
+    int bn = (2 * mean + 16 + 31) / 32 * 32;
+    return bn < 32 ? 32 : (bn > kMaxBN ? kMaxBN : bn);
+}
+
+// Scale factors of the activation operand (B) in the layout the MMA consumes, one
+// block per (expert, column tile): tile T_e + t of expert e (T_e = tile_off[e]) holds,
+// for each K tile kt of 128 elements, nsfb = ceil(BN / 128) atoms of 512 bytes; column
+// c of the tile (activation row nparts * offsets[e] + t * BN + c) keeps the 4 scale
+// bytes of its K tile at byte (c / 128) * 512 + (c % 32) * 16 + ((c / 32) % 4) * 4 of
+// the atoms (the 32 x 16-byte layout tcgen05.cp copies into TMEM), scale block 4kt+j
+// at byte j of the word.  Bytes of columns past the tile's rows are never read by a
+// result that is kept.  Byte offset of the word of (tile, kt, c):
+__host__ __device__ inline size_t sf_tile_word(int tile, int nkt, int nsfb, int kt, int c) {
+    return ((size_t)tile * nkt + kt) * (size_t)nsfb * 512 + (size_t)(c >> 7) * 512 + (size_t)(c & 31) * 16 +
+           (size_t)((c >> 5) & 3) * 4;
+}
+
 // Activation rows of the grouped GEMMs.  nparts = 1: one MXFP8 row per pair (OCP
 // rule, the prefill path).  nparts = 3: the value is the sum of three E4M3 parts
 // with their own E8M0 scales (see split_exp), which represents a bf16 row exactly
@@ -20,10 +49,14 @@ struct GroupedWs {
     int *prior;       // [nblocks][E]
     int32_t *uexp;    // [E] the experts with at least one pair, ascending
     int32_t *n_union; // [1] their number
+    int32_t *tile_off;// [E+1] first column tile of each expert (exclusive scan of its tiles)
+    int BN, nsfb;     // columns per tile, 512-byte scale atoms per tile and K tile
+    int max_tiles;    // bound on the column tiles of all experts
     uint8_t *xq;      // [nparts*P][H]    E4M3 rows of x in sorted order
-    uint8_t *xs;      // [nparts*P][H/32] their E8M0 scales
+    uint8_t *xs;      // [max_tiles][H/128][nsfb][512]  their E8M0 scales (sf_tile_word)
     uint8_t *hq;      // [nparts*P][I]    E4M3 rows of h in sorted order
-    uint8_t *hs;      // [nparts*P][Ip/32], Ip = I rounded up to 128 (tail bytes unused)
+    uint8_t *hs;      // [max_tiles][Ip/128][nsfb][512] Ip = I rounded up to 128; the
+                      //                   scale bytes of blocks I/32.. are 0 (2^-127)
     size_t end;       // total bytes
 };
 
@@ -32,6 +65,12 @@ __host__ __device__ inline GroupedWs grouped_ws_layout(void *ws, int E, int H, i
     const size_t P = (size_t)T * k;
     const size_t R = P * (size_t)nparts;
     const size_t nblocks = (P + 1023) / 1024;
+    const int bn = grouped_bn((int)P, E, T, nparts);
+    g.BN = bn > 0 ? bn : 48;  // (an unsupported shape is refused at launch)
+    g.nsfb = (g.BN + 127) / 128;
+    // sum over experts of ceil(rows_e / BN) <= R / BN + (experts with rows)
+    g.max_tiles = (int)((R + g.BN - 1) / g.BN + (P < (size_t)E ? P : (size_t)E));
+    const size_t ip = ((size_t)I + 127) / 128 * 128;
     char *base = (char *)ws;
     size_t o = 256;
     g.local_rank = (int *)(base + o);  o += align_up(P * 4, 1024);
@@ -39,10 +78,11 @@ __host__ __device__ inline GroupedWs grouped_ws_layout(void *ws, int E, int H, i
     g.prior = (int *)(base + o);       o += align_up(nblocks * E * 4, 1024);
     g.uexp = (int32_t *)(base + o);    o += align_up((size_t)E * 4, 256);
     g.n_union = (int32_t *)(base + o); o += 256;
+    g.tile_off = (int32_t *)(base + o); o += align_up(((size_t)E + 1) * 4, 256);
     g.xq = (uint8_t *)(base + o);      o += align_up(R * H, 1024);
-    g.xs = (uint8_t *)(base + o);      o += align_up(R * (H / 32), 1024);
+    g.xs = (uint8_t *)(base + o);      o += align_up((size_t)g.max_tiles * (H / 128) * g.nsfb * 512, 1024);
     g.hq = (uint8_t *)(base + o);      o += align_up(R * I, 1024);
-    g.hs = (uint8_t *)(base + o);      o += align_up(R * (((size_t)I + 127) / 128 * 4), 1024);
+    g.hs = (uint8_t *)(base + o);      o += align_up((size_t)g.max_tiles * (ip / 128) * g.nsfb * 512, 1024);
     g.end = o;
     return g;
 }

@@ -36,10 +36,13 @@ def test_exports_every_declared_symbol(L):
 def test_pool_sizes():
     full = moe.moe_pool_record_bytes(7168, 1600)
     # 18,278,400 B of MXFP4 data + zero padding of W_d rows to 1664 elements
-    assert full == 18_522_112
+    # (243,712 B) + the scale bytes once more in tensor-core order: W_gu 56 K tiles x
+    # 25 row tiles x 512 B, W_d 13 x 56 x 512 B
     data = synth.expert_code_bytes(7168, 1600) + synth.expert_scale_bytes(7168, 1600)
     assert data == 18_278_400
-    assert moe.moe_pool_record_bytes(1024, 512) == 835_584
+    assert full == data + 243_712 + 56 * 25 * 512 + 13 * 56 * 512 == 19_611_648
+    # 835,584 B of data (no padding), 8 x 8 x 512 + 4 x 8 x 512 B of reordered scales
+    assert moe.moe_pool_record_bytes(1024, 512) == 835_584 + 8 * 8 * 512 + 4 * 8 * 512
     assert moe.moe_pool_bytes(896, 7168, 1600) == 896 * full
     assert moe.moe_pool_bytes(896, 7100, 1600) == 0      # H not a multiple of 128
     assert moe.moe_pool_bytes(896, 7168, 1601) == 0

@@ -248,13 +248,16 @@ def test_zero_and_closed_form_experts():
     check_close(bf16_to_f64(y1), np.full((1, H), want))
 
 
-def test_bad_index_sets_status(tiny):
+@pytest.mark.parametrize("M", [1, 3])
+def test_bad_index_sets_status(tiny, M):
+    # M = 1: the fused single-token kernel; M = 3: sort, gather and grouped GEMMs
     s, pool, _, _ = tiny
-    x = to_dev_bf16(synth.tokens_bf16(0, 0, 1, s.H))
-    idx = torch.arange(s.k, dtype=torch.int32, device="cuda").view(1, -1).clone()
+    x = to_dev_bf16(synth.tokens_bf16(0, 0, M, s.H))
+    idx = torch.stack([torch.arange(s.k, dtype=torch.int32) + 5 * m for m in range(M)]).cuda()
     idx[0, 3] = 10_000
-    w = torch.full((1, s.k), 1.0 / s.k, dtype=torch.float32, device="cuda")
-    ws = moe.workspace(moe.moe_workspace_size(moe.MOE_OP_DECODE, s.E, s.H, s.I, 1, s.k))
+    idx[M - 1, 0] = -1
+    w = torch.full((M, s.k), 1.0 / s.k, dtype=torch.float32, device="cuda")
+    ws = moe.workspace(moe.moe_workspace_size(moe.MOE_OP_DECODE, s.E, s.H, s.I, M, s.k))
     y = moe.moe_expert_forward_decode(pool, x, idx, w, ws=ws)
     assert moe.moe_check_status(ws) == moe.MOE_ERR_BAD_INDEX
     assert torch.isfinite(y.float()).all()

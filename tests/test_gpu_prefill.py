@@ -87,3 +87,83 @@ def test_prefill_deterministic_after_other_shapes():
     out2, y2, _, _ = _run(s, 128, 564, sample=np.array([0]))
     assert torch.equal(out1["partial"], out2["partial"])
     assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
+
+
+def _align(v, a):
+    return (v + a - 1) // a * a
+
+
+def _tensor_core_planes(rec, H, I):
+    """The record's two scale planes in the tensor-core order, derived on the host from
+    its row-major planes by the layout's definition: block (kt, mt) byte 16l + 4q + j =
+    scale block 4kt + j of row 128mt + 32q + l, rows past the matrix 0."""
+    Ip = _align(I, 128)
+    gu_codes, d_codes = 2 * I * H // 2, H * Ip // 2
+    off_sgu = gu_codes + d_codes
+    off_sd = off_sgu + 2 * I * H // 32
+    want = []
+    for off, rows, nblk in ((off_sgu, 2 * I, H // 32), (off_sd, H, Ip // 32)):
+        S = rec[off:off + rows * nblk].reshape(rows, nblk)
+        nmt = -(-rows // 128)
+        Sp = np.zeros((nmt * 128, nblk), dtype=np.uint8)
+        Sp[:rows] = S
+        # [mt][q][l][kt][j] -> [kt][mt][l][q][j]
+        want.append(Sp.reshape(nmt, 4, 32, nblk // 4, 4).transpose(3, 0, 2, 1, 4).reshape(-1))
+    off_sgu_mma = _align(off_sd + H * Ip // 32, 1024)
+    off_sd_mma = off_sgu_mma + _align(want[0].size, 1024)
+    got = [rec[off_sgu_mma:off_sgu_mma + want[0].size], rec[off_sd_mma:off_sd_mma + want[1].size]]
+    return want, got, _align(off_sd_mma + want[1].size, 1024)
+
+
+@pytest.mark.parametrize("H,I", [(256, 96), (384, 192), (1024, 512)])
+def test_pool_tensor_core_scale_planes(H, I):
+    """The derived scale planes hold exactly the row-major scale bytes, permuted, for a
+    synthetic fill and for an uploaded expert (odd row-tile counts and padded W_d rows
+    included)."""
+    E = 3
+    pool = moe.Pool(E, H, I)
+    moe.moe_pool_fill_synthetic(pool, 41)
+    g = torch.Generator().manual_seed(H + I)
+    codes = torch.randint(0, 256, (3 * H * I // 2,), dtype=torch.uint8, generator=g).cuda()
+    scales = torch.randint(0, 256, (3 * H * I // 32,), dtype=torch.uint8, generator=g).cuda()
+    moe.moe_pool_upload_expert(pool, 1, codes, scales)
+    torch.cuda.synchronize()
+    rb = moe.moe_pool_record_bytes(H, I)
+    mem = pool.mem.cpu().numpy()
+    for e in range(E):
+        want, got, rec_bytes = _tensor_core_planes(mem[e * rb:(e + 1) * rb], H, I)
+        assert rec_bytes == rb
+        for w_, g_ in zip(want, got):
+            assert np.array_equal(w_, g_), e
+
+
+def test_prefill_bad_index_sets_status():
+    """Slots with an expert index out of range: the status word says so, those pairs are
+    left out of the sort (inv_perm -1), and every other pair's output is still right."""
+    s = synth.Shape(E=16, H=256, I=128, k=4)
+    T, seed = 64, 531
+    pool = moe.Pool(s.E, s.H, s.I)
+    moe.moe_pool_fill_synthetic(pool, seed)
+    xb = synth.tokens_bf16(seed + 2, 0, T, s.H)
+    x = to_dev_bf16(xb)
+    idx, w = moe.moe_route_topk(x, to_dev_bf16(synth.router_bf16(seed + 1, s.E, s.H)), s.k)
+    idx[5, 2] = 10_000
+    idx[7, 0] = -3
+    ws = moe.workspace(moe.moe_workspace_size(moe.MOE_OP_GROUPED, s.E, s.H, s.I, T, s.k))
+    out = moe.moe_expert_forward_grouped(pool, x, idx, ws=ws)
+    y = moe.moe_combine(out["partial"], out["inv_perm"], w)
+    assert moe.moe_check_status(ws) == moe.MOE_ERR_BAD_INDEX
+    inv = out["inv_perm"].cpu().numpy().reshape(T, s.k)
+    assert inv[5, 2] == -1 and inv[7, 0] == -1
+    assert out["offsets"].cpu().numpy()[-1] == T * s.k - 2
+    assert torch.isfinite(y.float()).all()
+    idx_ok = idx.cpu().numpy().copy()
+    idx_ok[5, 2] = 0
+    idx_ok[7, 0] = 0
+    opool = oracle.SyntheticPool(seed, s.E, s.H, s.I)
+    xq = oracle.quant_rows_mxfp8(synth.bf16_bits_to_f64(xb))
+    o_ref = oracle.pair_outputs(opool, s.H, s.I, xq, idx_ok, h_mode=1)
+    amb = oracle.pair_ambiguity(opool, s.H, s.I, xq, idx_ok)
+    valid = inv >= 0
+    part = out["partial"].float().cpu().numpy().astype(np.float64)[np.where(valid, inv, 0)]
+    check_close(part[valid], o_ref[valid], "partial", amb=amb[valid])
