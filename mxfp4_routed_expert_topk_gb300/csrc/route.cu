@@ -13,6 +13,11 @@
 //   |l~ - l| <= gamma_d * (sum_h |x_h W_r[e,h]| + |skew_e|),  gamma_d = d u / (1 - d u),
 // plus at most 2^-150 per product lost to underflow.
 //
+// For many tokens (route_tiled_kernel) the logits are a register-tiled fp32 FMA
+// product with a longer (but still bounded) summation tree, and the sum of
+// |x_h W_r[e,h]| is replaced by its Cauchy-Schwarz upper bound ||x|| ||W_r[e]||,
+// so each product costs one FMA.
+//
 // route_select_kernel (one CTA per token) sorts by (l~ desc, index asc) and
 // certifies the order with the intervals [l~ - b, l~ + b]: an outsider can only
 // enter the top k if its interval reaches the lowest lower bound of the winners,
@@ -31,17 +36,25 @@ constexpr int kMaxCand = 256;      // experts that may still enter the top k
 constexpr int kMaxExact = 64;      // experts evaluated exactly per token
 constexpr int kLimbs = 20;         // base-2^32 digits of an exact logit, unit 2^-268
 constexpr int kBins = 512;         // exponent bins of the exact evaluation
+constexpr int kTiledMinTokens = 64;  // tokens from which the logits take the tiled kernel
 
 struct RouteWs {
     float *logit;  // [M][E]
     float *bound;  // [M][E]
+    float *xnorm;  // [M] ||x_m|| (tiled path)
+    float *wnorm;  // [E] ||W_r[e]|| (tiled path)
+    size_t end;
 };
 
 __host__ __device__ inline RouteWs route_ws(void *ws, int M, int E) {
     RouteWs r;
-    char *p = (char *)ws + 256;
-    r.logit = (float *)p;
-    r.bound = (float *)(p + align_up((size_t)M * E * sizeof(float), 256));
+    char *p = (char *)ws;
+    size_t o = 256;
+    r.logit = (float *)(p + o); o += align_up((size_t)M * E * sizeof(float), 256);
+    r.bound = (float *)(p + o); o += align_up((size_t)M * E * sizeof(float), 256);
+    r.xnorm = (float *)(p + o); o += align_up((size_t)M * sizeof(float), 256);
+    r.wnorm = (float *)(p + o); o += align_up((size_t)E * sizeof(float), 256);
+    r.end = o;
     return r;
 }
 
@@ -160,6 +173,174 @@ __global__ void __launch_bounds__(256) route_logits_kernel(const uint16_t *__res
                                                            const float *__restrict__ skew,
                                                            float *__restrict__ logit, float *__restrict__ bound) {
     logits_block<8>(x, M, H, Wr, E, skew, logit, bound);
+}
+
+// ------------------------------------------------------- tiled logits (many tokens)
+//
+// CTA: 64 tokens x 64 experts over one half of H (grid z); 256 threads in four
+// K groups of 64, each thread an 8 x 8 block of (token, expert).  Per step of 64
+// elements of K the CTA stages x and W_r (bf16 -> fp32, K-major) in shared memory
+// and group g takes elements 16g .. 16g+15 of the step.  A thread's products pass
+// through at most 31 roundings of an inner FMA chain (two steps, 32 products; the
+// first FMA onto 0 is exact), then one addition per 32 products into an outer
+// running sum (H/256 of them), then the tree of the four groups (2), the sum of
+// the two halves (1) and the skew (1).
+constexpr int kTileT = 64, kTileE = 64, kTileKStep = 64, kTiledThreads = 256;
+constexpr size_t kTiledSmem = 2 * 2 * 4 * 16 * 64 * sizeof(float);  // x and W_r, two buffers (64 KB)
+
+__host__ __device__ inline int tiled_tree_depth(int H) { return 31 + (H + 255) / 256 + 2 + 1 + 1; }
+
+// ||row|| for the M rows of x and the E rows of W_r, one warp per row.  Squares of
+// bf16 values are exact in fp32; the computed sum of squares is within a relative
+// (H/256 + 8) u of the true one, far inside the 2^-10 margin of the bound that uses
+// it, and underflowed squares (at most 2^-149 each) are added back as H 2^-149.
+__global__ void route_norms_kernel(const uint16_t *__restrict__ x, int M, int H, const uint16_t *__restrict__ Wr,
+                                   int E, float *__restrict__ xnorm, float *__restrict__ wnorm) {
+    const int lane = threadIdx.x & 31;
+    const int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    if (r >= M + E) return;
+    const uint16_t *row = r < M ? x + (size_t)r * H : Wr + (size_t)(r - M) * H;
+    float ss = 0.f;
+    for (int h = lane * 8; h < H; h += 256) {
+        float f[8];
+        unpack_bf16x8(*reinterpret_cast<const uint4 *>(row + h), f);
+#pragma unroll
+        for (int i = 0; i < 8; i++) ss = __fmaf_rn(f[i], f[i], ss);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+    if (lane == 0) {
+        const float n = sqrtf(ss + (float)H * 1.4012985e-45f);
+        if (r < M)
+            xnorm[r] = n;
+        else
+            wnorm[r - M] = n;
+    }
+}
+
+// Partial logits of one half of H: half 0 into logit[], half 1 into bound[] (the
+// finish kernel combines them in place).  Rows past M or E are computed on zeros and
+// not stored.
+__global__ void __launch_bounds__(kTiledThreads, 1)
+    route_tiled_kernel(const uint16_t *__restrict__ x, int M, int H, const uint16_t *__restrict__ Wr, int E,
+                       float *__restrict__ part0, float *__restrict__ part1) {
+    extern __shared__ __align__(16) float tiled_smem[];  // kTiledSmem bytes
+    auto xs = reinterpret_cast<float(*)[4][16][kTileT]>(tiled_smem);                        // [buffer][group][k][token]
+    auto wsm = reinterpret_cast<float(*)[4][16][kTileE]>(tiled_smem + 2 * 4 * 16 * kTileT);  // [buffer][group][k][expert]
+    const int tid = threadIdx.x;
+    const int t0 = blockIdx.y * kTileT, e0 = blockIdx.x * kTileE;
+    const int half = blockIdx.z;
+    const int hlen = H / 2, hbase = half * hlen;
+    const int nsteps = hlen / kTileKStep;
+    // staging: thread (row = tid % 64, group = tid / 64) loads 16 consecutive K
+    // elements of its token row and of its expert row per step
+    const int lrow = tid & 63, lgrp = tid >> 6;
+    const bool tv = t0 + lrow < M, ev = e0 + lrow < E;
+    const uint16_t *xrow = x + (size_t)(tv ? t0 + lrow : 0) * H + hbase + 16 * lgrp;
+    const uint16_t *wrow = Wr + (size_t)(ev ? e0 + lrow : 0) * H + hbase + 16 * lgrp;
+    uint4 px[2], pw[2];
+    auto fetch = [&](int step) {
+        const uint4 *xp = reinterpret_cast<const uint4 *>(xrow + step * kTileKStep);
+        const uint4 *wp = reinterpret_cast<const uint4 *>(wrow + step * kTileKStep);
+        px[0] = tv ? __ldg(xp) : make_uint4(0u, 0u, 0u, 0u);
+        px[1] = tv ? __ldg(xp + 1) : make_uint4(0u, 0u, 0u, 0u);
+        pw[0] = ev ? __ldg(wp) : make_uint4(0u, 0u, 0u, 0u);
+        pw[1] = ev ? __ldg(wp + 1) : make_uint4(0u, 0u, 0u, 0u);
+    };
+    auto stash = [&](int buf) {
+        float f[8];
+#pragma unroll
+        for (int q = 0; q < 2; q++) {
+            unpack_bf16x8(px[q], f);
+#pragma unroll
+            for (int j = 0; j < 8; j++) xs[buf][lgrp][8 * q + j][lrow] = f[j];
+            unpack_bf16x8(pw[q], f);
+#pragma unroll
+            for (int j = 0; j < 8; j++) wsm[buf][lgrp][8 * q + j][lrow] = f[j];
+        }
+    };
+    // compute: group g = tid / 64; within it ty = (tid % 64) / 8, tx = tid % 8; tokens
+    // 4ty..4ty+3 and 32+4ty.., experts 4tx..4tx+3 and 32+4tx..
+    const int g = tid >> 6, ty = (tid & 63) >> 3, tx = tid & 7;
+    float inner[8][8], outer[8][8];
+#pragma unroll
+    for (int i = 0; i < 8; i++)
+#pragma unroll
+        for (int j = 0; j < 8; j++) inner[i][j] = outer[i][j] = 0.f;
+    fetch(0);
+    stash(0);
+    __syncthreads();
+    for (int step = 0; step < nsteps; step++) {
+        const int buf = step & 1;
+        if (step + 1 < nsteps) fetch(step + 1);
+#pragma unroll
+        for (int k = 0; k < 16; k++) {
+            const float4 a0 = *reinterpret_cast<const float4 *>(&xs[buf][g][k][4 * ty]);
+            const float4 a1 = *reinterpret_cast<const float4 *>(&xs[buf][g][k][32 + 4 * ty]);
+            const float4 b0 = *reinterpret_cast<const float4 *>(&wsm[buf][g][k][4 * tx]);
+            const float4 b1 = *reinterpret_cast<const float4 *>(&wsm[buf][g][k][32 + 4 * tx]);
+            const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+            const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+            for (int i = 0; i < 8; i++)
+#pragma unroll
+                for (int j = 0; j < 8; j++) inner[i][j] = __fmaf_rn(av[i], bv[j], inner[i][j]);
+        }
+        if ((step & 1) || step + 1 == nsteps) {
+#pragma unroll
+            for (int i = 0; i < 8; i++)
+#pragma unroll
+                for (int j = 0; j < 8; j++) {
+                    outer[i][j] = __fadd_rn(outer[i][j], inner[i][j]);
+                    inner[i][j] = 0.f;
+                }
+        }
+        if (step + 1 < nsteps) stash(buf ^ 1);
+        __syncthreads();
+    }
+    // the four groups' sums: ((g0 + g1) + (g2 + g3)), through shared memory
+    float *red = tiled_smem;  // both staging buffers: 4 x [64][64] floats
+#pragma unroll
+    for (int i = 0; i < 8; i++)
+#pragma unroll
+        for (int j = 0; j < 8; j++) {
+            const int tt = (i < 4 ? 4 * ty + i : 32 + 4 * ty + i - 4);
+            const int ee = (j < 4 ? 4 * tx + j : 32 + 4 * tx + j - 4);
+            red[(size_t)g * 4096 + tt * 64 + ee] = outer[i][j];
+        }
+    __syncthreads();
+    float *part = half == 0 ? part0 : part1;
+    for (int o = tid; o < kTileT * kTileE; o += kTiledThreads) {
+        const int tt = o / kTileE, ee = o % kTileE;
+        if (t0 + tt < M && e0 + ee < E) {
+            const float v = __fadd_rn(__fadd_rn(red[o], red[4096 + o]), __fadd_rn(red[8192 + o], red[12288 + o]));
+            part[(size_t)(t0 + tt) * E + e0 + ee] = v;
+        }
+    }
+}
+
+// logit = half0 + half1 (+ skew), bound from the tree depth and ||x|| ||W_r[e]||
+// (+ |skew|), in place over the two halves.
+__global__ void route_finish_kernel(int M, int H, int E, const float *__restrict__ skew,
+                                    const float *__restrict__ xnorm, const float *__restrict__ wnorm,
+                                    float *__restrict__ logit, float *__restrict__ bound) {
+    const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= (size_t)M * E) return;
+    const int m = (int)(i / E), e = (int)(i % E);
+    float l = __fadd_rn(logit[i], bound[i]);
+    float S = xnorm[m] * wnorm[e];
+    if (skew != nullptr) {
+        const float sk = skew[e];
+        l = __fadd_rn(l, sk);
+        S = S + fabsf(sk);
+    }
+    const int d = tiled_tree_depth(H);
+    // as in logits_block: (d+1) u S with the factor 1 + 2^-10 for the roundings of S
+    // and of the norms; 2^-148 per product for underflow
+    float b = (float)(d + 1) * 5.9604645e-8f * S * (1.0f + 9.765625e-4f);
+    b = b + (float)H * 2.8025969e-45f;
+    logit[i] = l;
+    bound[i] = b;
 }
 
 // ------------------------------------------------------------ exact logits
@@ -760,7 +941,19 @@ cudaError_t launch_route_j(const uint16_t *x, int M, int H, const uint16_t *Wr, 
         route_single_kernel<J><<<g1.x, kRouteThreads, smem1, st>>>(x, H, Wr, E, skew, k, r.logit, r.bound, idx, w, stw);
         return cudaGetLastError();
     }
-    {
+    if (M >= kTiledMinTokens && H % 128 == 0) {
+        static int smem_tiled = 0;
+        cudaError_t e = ensure_dynamic_smem(route_tiled_kernel, kTiledSmem, smem_tiled);
+        if (e != cudaSuccess) return e;
+        TraceScope trace_scope("route_logits", st);
+        route_norms_kernel<<<(M + E + 7) / 8, 256, 0, st>>>(x, M, H, Wr, E, r.xnorm, r.wnorm);
+        route_tiled_kernel<<<dim3((E + kTileE - 1) / kTileE, (M + kTileT - 1) / kTileT, 2), kTiledThreads, kTiledSmem,
+                             st>>>(
+            x, M, H, Wr, E, r.logit, r.bound);
+        const size_t n = (size_t)M * E;
+        route_finish_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(M, H, E, skew, r.xnorm, r.wnorm, r.logit,
+                                                                        r.bound);
+    } else {
         TraceScope trace_scope("route_logits", st);
         route_logits_kernel<<<g1, 256, smem1, st>>>(x, M, H, Wr, E, skew, r.logit, r.bound);
     }
@@ -775,7 +968,7 @@ cudaError_t launch_route_j(const uint16_t *x, int M, int H, const uint16_t *Wr, 
 
 size_t route_workspace_bytes(int E, int M, int k) {
     (void)k;
-    return 256 + 2 * align_up((size_t)M * E * sizeof(float), 256);
+    return route_ws(nullptr, M, E).end;
 }
 
 cudaError_t launch_route(const uint16_t *x, int M, int H, const uint16_t *Wr, int E, const float *skew, int k,

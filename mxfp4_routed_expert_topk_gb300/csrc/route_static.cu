@@ -15,7 +15,9 @@ namespace {
 
 // Largest M * E this entry point accepts (1 MiB of logits and bounds).
 constexpr size_t kStaticRouteMaxME = 131072;
-constexpr size_t kStaticScratchBytes = 256 + 2 * kStaticRouteMaxME * sizeof(float);
+// logits and bounds, plus the row norms of x and W_r (at most kStaticRouteMaxME + 4096)
+constexpr size_t kStaticScratchBytes = 256 + 2 * kStaticRouteMaxME * sizeof(float) +
+                                       (kStaticRouteMaxME + 4096) * sizeof(float) + 1024;
 constexpr int kMaxDevices = 64;
 
 // Every GPU that loads this library holds this array until the process exits.

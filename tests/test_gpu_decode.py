@@ -99,15 +99,19 @@ def test_route_tiny_bit_exact(tiny):
     _route_check(xb, Wrb, Wr, s.k)
 
 
-def test_route_full_bit_exact(full):
+# M >= 64 takes the tiled logit kernel (longer summation tree, Cauchy-Schwarz bound);
+# 130 rows leave a ragged last tile of 2 tokens
+@pytest.mark.parametrize("M", [48, 130])
+def test_route_full_bit_exact(full, M):
     s, _, Wrb, Wr = full
-    xb = synth.tokens_bf16(synth.TOKENS_SEED["full"], 0, 48, s.H)
+    xb = synth.tokens_bf16(synth.TOKENS_SEED["full"], 0, M, s.H)
     _route_check(xb, Wrb, Wr, s.k)
 
 
-def test_route_with_zipf_skew(full):
+@pytest.mark.parametrize("M", [24, 70])
+def test_route_with_zipf_skew(full, M):
     s, _, Wrb, Wr = full
-    xb = synth.tokens_bf16(synth.TOKENS_SEED["stacked"], 0, 24, s.H)
+    xb = synth.tokens_bf16(synth.TOKENS_SEED["stacked"], 0, M, s.H)
     _route_check(xb, Wrb, Wr, s.k, synth.zipf_skew_f32(synth.skew_seed(0), s.E))
 
 
@@ -118,10 +122,11 @@ def test_route_k_values(tiny, k):
     _route_check(xb, Wrb, Wr, k)
 
 
-def test_route_planted_ties_take_exact_path(tiny):
+@pytest.mark.parametrize("M", [16, 80])
+def test_route_planted_ties_take_exact_path(tiny, M):
     s, _, Wrb0, _ = tiny
     Wrb = Wrb0.copy()
-    xb = synth.tokens_bf16(7, 0, 16, s.H)
+    xb = synth.tokens_bf16(7, 0, M, s.H)
     # exact duplicates (ties -> lower index), and one-ulp near ties of a strong row
     strong = synth.bf16_bits_from_f64(np.sign(synth.bf16_bits_to_f64(xb[0])) * 0.05)
     for e in (3, 20, 41):
@@ -152,10 +157,11 @@ def test_route_threshold_fallback(full, M):
     _route_check(xb, Wrb, to_dev_bf16(Wrb), s.k)
 
 
-def test_route_large_dynamic_range(tiny):
+@pytest.mark.parametrize("M", [8, 72])
+def test_route_large_dynamic_range(tiny, M):
     s, _, Wrb0, _ = tiny
     rng = np.random.default_rng(11)
-    xb = synth.bf16_bits_from_f64(rng.standard_normal((8, s.H)) * np.exp2(rng.integers(-60, 60, size=(8, s.H))))
+    xb = synth.bf16_bits_from_f64(rng.standard_normal((M, s.H)) * np.exp2(rng.integers(-60, 60, size=(M, s.H))))
     Wrb = synth.bf16_bits_from_f64(rng.standard_normal((s.E, s.H)) * np.exp2(rng.integers(-40, 30, size=(s.E, s.H))))
     _route_check(xb, Wrb, to_dev_bf16(Wrb), s.k)
 
