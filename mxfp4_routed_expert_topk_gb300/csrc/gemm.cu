@@ -36,8 +36,10 @@ constexpr int kMaxStages = 12;
 constexpr int kTileM = 128;
 constexpr int kTileK = 128;   // elements (bytes in shared memory for both operands)
 
-constexpr int kGemmThreads = 256;  // warps: 0 copies, 2 MMA, 4-7 epilogue (1 and 3 idle)
-constexpr int kEpiThreads = 128;
+// warps: 0 copies, 2 MMA, 4-7 and 8-11 epilogue (two warpgroups taking alternate
+// column groups; warp w reads TMEM lanes 32 (w % 4) ..), 1 and 3 idle
+constexpr int kGemmThreads = 384;
+constexpr int kEpiWarps = 8;
 
 struct GemmArgs {
     int mode;            // 1: gate/up + SwiGLU + MXFP8, 2: down
@@ -166,15 +168,18 @@ __device__ __forceinline__ void tc_commit(uint64_t *bar) {
                  : "memory");
 }
 
+// 16 accumulator columns of this warp's 32 TMEM lanes; the wait is in the same
+// statement, so no use of the registers can be scheduled before the data is there.
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
     uint32_t r[16];
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
-        "%15}, [%16];"
+        "%15}, [%16];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
         : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
           "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-        : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+        : "r"(taddr)
+        : "memory");
 #pragma unroll
     for (int i = 0; i < 16; i++) v[i] = __uint_as_float(r[i]);
 }
@@ -184,8 +189,9 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
 // h = silu(g) * u, written as three E4M3 parts per 32-block along I (split_part);
 // down: the unweighted expert output row in fp32.
 __device__ __forceinline__ void epilogue_split3(const GemmArgs &a, uint32_t lane_base, bool ok, int nn, int nmma, int mt,
-                                                int row0, int n0, int tile, int warp, int lane, float *amax_x) {
-    for (int c0 = 0; c0 < nmma; c0 += 48) {
+                                                int row0, int n0, int tile, int warp, int wg, int lane, float *amax_x) {
+    const int bar = 2 + 2 * wg + (warp >> 1);  // the warp pair's barrier
+    for (int c0 = 48 * wg; c0 < nmma; c0 += 96) {
         float v0[16], v1[16], v2[16];
 #pragma unroll
         for (int j = 0; j < 16; j++) v0[j] = v1[j] = v2[j] = 0.f;
@@ -208,7 +214,7 @@ __device__ __forceinline__ void epilogue_split3(const GemmArgs &a, uint32_t lane
 #pragma unroll
             for (int j = 0; j < 16; j++) {
                 const float u = __shfl_down_sync(0xffffffffu, pv[j], 16);
-                hv[j] = (lane < 16) ? pv[j] / (1.f + expf(-pv[j])) * u : 0.f;
+                hv[j] = (lane < 16) ? __fdividef(pv[j], 1.f + __expf(-pv[j])) * u : 0.f;
             }
 #pragma unroll 1
             for (int q = 0; q < 3; q++) {
@@ -225,7 +231,7 @@ __device__ __forceinline__ void epilogue_split3(const GemmArgs &a, uint32_t lane
 #pragma unroll
                     for (int j = 0; j < 16; j++) amax_x[warp * 16 + j] = am[j];
                 }
-                named_barrier(2, kEpiThreads);
+                named_barrier(bar, 64);
 #pragma unroll
                 for (int j = 0; j < 16; j++) {
                     const int X = split_exp(fmaxf(amax_x[warp * 16 + j], amax_x[(warp ^ 1) * 16 + j]));
@@ -239,7 +245,7 @@ __device__ __forceinline__ void epilogue_split3(const GemmArgs &a, uint32_t lane
                                 (uint8_t)(X + 127);
                     }
                 }
-                named_barrier(2, kEpiThreads);
+                named_barrier(bar, 64);
             }
         } else {
             const int o = mt * kTileM + 32 * warp + lane;
@@ -253,12 +259,25 @@ __device__ __forceinline__ void epilogue_split3(const GemmArgs &a, uint32_t lane
 
 // ------------------------------------------------------------------- kernel
 
+// MXFP8 shared exponent of a 32-block from the bits of its max |h| (a finite
+// non-negative float): floor(log2 amax) - 8, or -127 for zero and values below
+// 2^-119 (the clamp; subnormals have exponent field 0).  Equal to the frexp form.
+__device__ __forceinline__ int mx_exp_from_bits(uint32_t amax_bits) { return max(-127, (int)(amax_bits >> 23) - 135); }
+
+// 2^-X as a float for X in [-127, 119] (always a normal number).
+__device__ __forceinline__ float pow2_neg(int X) { return __uint_as_float((uint32_t)(127 - X) << 23); }
+
 // One-part (MXFP8) epilogue of a tile's 16-column groups: gate/up -> h = silu(g) * u
 // quantised to MXFP8 along I (OCP rule); down -> expert output rows.  ew = warp
-// index within the epilogue warpgroup (TMEM lanes 32ew..32ew+31).
+// index within the epilogue warpgroup (TMEM lanes 32ew..32ew+31); warpgroup wg takes
+// the column groups c0 = 16 wg, 16 wg + 32, ...  Warps 2p and 2p+1 of a warpgroup
+// hold the two halves of the same 32-blocks of I and exchange their maxima through
+// shared memory under a 64-thread barrier of their own (id 2 + 2 wg + p).
 __device__ __forceinline__ void epilogue_mx1(const GemmArgs &a, uint32_t lane_base, bool ok, int nn, int nmma, int mt,
-                                             int row0, int n0, int tile, int ew, int lane, float *amax_x) {
-    for (int c0 = 0; c0 < nmma; c0 += 16) {
+                                             int row0, int n0, int tile, int ew, int wg, int lane, float *amax_x) {
+    uint32_t *amax_u = reinterpret_cast<uint32_t *>(amax_x);
+    const int bar = 2 + 2 * wg + (ew >> 1);  // the warp pair's barrier
+    for (int c0 = 16 * wg; c0 < nmma; c0 += 32) {
         float v[16];
 #pragma unroll
         for (int j = 0; j < 16; j++) v[j] = 0.f;
@@ -267,42 +286,37 @@ __device__ __forceinline__ void epilogue_mx1(const GemmArgs &a, uint32_t lane_ba
             // lanes 0-15: gate rows, 16-31: up rows of the same 16 intermediate indices
             const int i = (4 * mt + ew) * 16 + (lane & 15);
             float hv[16];
-            float am[16];
+            uint32_t am[16];
 #pragma unroll
             for (int j = 0; j < 16; j++) {
                 const float u = __shfl_down_sync(0xffffffffu, v[j], 16);
                 const float g = v[j];
-                hv[j] = (lane < 16) ? g / (1.f + expf(-g)) * u : 0.f;
-                float m = fabsf(hv[j]);
-#pragma unroll
-                for (int off = 8; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-                am[j] = m;
+                // fast exp and divide: a few ulps, far inside the tolerance of h
+                hv[j] = (lane < 16) ? __fdividef(g, 1.f + __expf(-g)) * u : 0.f;
+                // the bits of non-negative floats order as their values
+                am[j] = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(hv[j])));
             }
             if (lane == 0) {
 #pragma unroll
-                for (int j = 0; j < 16; j++) amax_x[ew * 16 + j] = am[j];
+                for (int j = 0; j < 16; j++) amax_u[ew * 16 + j] = am[j];
             }
-            named_barrier(2, kEpiThreads);
+            named_barrier(bar, 64);
 #pragma unroll
             for (int j = 0; j < 16; j++) {
                 const int n = c0 + j;
-                const float amax = fmaxf(amax_x[ew * 16 + j], amax_x[(ew ^ 1) * 16 + j]);
-                int X = -127;
-                if (amax > 0.f) {
-                    int ex;
-                    frexpf(amax, &ex);
-                    X = max(-127, min(127, ex - 1 - 8));
-                }
+                const int X = mx_exp_from_bits(max(am[j], amax_u[(ew ^ 1) * 16 + j]));
                 if (ok && n < nn && lane < 16) {
                     const uint64_t r = (uint64_t)(row0 + n0 + n);
                     unsigned short pair;
-                    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(pair) : "f"(0.f), "f"(ldexpf(hv[j], -X)));
+                    // h * 2^-X is exact (a power-of-two scaling that stays normal or
+                    // rounds as ldexp does)
+                    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(pair) : "f"(0.f), "f"(hv[j] * pow2_neg(X)));
                     a.hq[r * a.I + i] = (uint8_t)(pair & 0xFF);
                     if (lane == 0 && (ew & 1) == 0)
                         a.hs[sf_tile_word(tile, a.nkt_h, a.nsfb, i >> 7, n) + ((i >> 5) & 3)] = (uint8_t)(X + 127);
                 }
             }
-            named_barrier(2, kEpiThreads);
+            named_barrier(bar, 64);
         } else {
             const int o = mt * kTileM + 32 * ew + lane;
 #pragma unroll
@@ -331,7 +345,7 @@ struct GemmSmemLayout {
         sfb = sfa + (uint32_t)(ns * tpi) * 512;           // ns x nsfb*512
         bars = sfb + (uint32_t)ns * 512 * nsfb;           // full[], empty[], acc_full[2], acc_empty[2]
         misc = bars + (2 * kMaxStages + 4) * 8;           // tmem addr, abort, amax[4][16]
-        total = misc + 16 + 4 * 16 * 4;
+        total = misc + 16 + kEpiWarps * 16 * 4;
     }
 };
 
@@ -386,7 +400,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     uint64_t *acc_empty = acc_full + 2;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L.misc);
     int *abort_flag = reinterpret_cast<int *>(smem + L.misc + 4);
-    float *amax_x = reinterpret_cast<float *>(smem + L.misc + 16);  // [4 epilogue warps][16 columns]
+    float *amax_x = reinterpret_cast<float *>(smem + L.misc + 16);  // [8 epilogue warps][16 columns]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nu = *a.n_union;
@@ -409,7 +423,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
         for (int b = 0; b < 2; b++) {
             mbar_init(&acc_full[b], 1);   // MMA commit after a tile's last K step
-            mbar_init(&acc_empty[b], 4);  // the four epilogue warps
+            mbar_init(&acc_empty[b], kEpiWarps);  // the epilogue warps
         }
         *abort_flag = 0;
         fence_mbar_init();
@@ -529,7 +543,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
     } else if (warp >= 4) {
         // ------------------------------------------------------- epilogue
-        const int ew = warp - 4;
+        const int ew = warp & 3, wg = (warp - 4) >> 2;
+        float *amax_g = amax_x + 64 * wg;
         int jb = 0;
         for (JobIter J(a, nu); J.valid(); J.next(), jb++) {
             const int buf = jb & 1;
@@ -544,15 +559,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 const uint32_t lane_base =
                     tmem + (uint32_t)((buf * tpi + t) * a.BN) + ((uint32_t)(32 * ew) << 16);
                 if (a.nparts == 3)
-                    epilogue_split3(a, lane_base, ok, nn, nmma, J.mt + t, J.row0, J.n0(), J.tile(), ew, lane, amax_x);
+                    epilogue_split3(a, lane_base, ok, nn, nmma, J.mt + t, J.row0, J.n0(), J.tile(), ew, wg, lane,
+                                    amax_g);
                 else
-                    epilogue_mx1(a, lane_base, ok, nn, nmma, J.mt + t, J.row0, J.n0(), J.tile(), ew, lane, amax_x);
+                    epilogue_mx1(a, lane_base, ok, nn, nmma, J.mt + t, J.row0, J.n0(), J.tile(), ew, wg, lane, amax_g);
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&acc_empty[buf]);
-            // no early exit: after an abort the waits are skipped, and all four warps
-            // run the same sequence of named barriers to the end
+            // no early exit: after an abort the waits are skipped, and both warps of
+            // each pair run the same sequence of named barriers to the end
         }
     }
     // nothing may still be in flight when TMEM is released and the CTA exits

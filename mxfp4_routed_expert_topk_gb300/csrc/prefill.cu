@@ -204,10 +204,11 @@ __device__ __forceinline__ void zero_h_pad(uint8_t *hs, int I, int nsfb, RowTile
 
 // Sorted row r (one warp per row): Xs[r] = MXFP8(x[perm[r] / k]).  Shared exponent
 // X = floor(log2 amax) - 8 per 32-block (clamped to [-127, 127]); codes are
-// RNE(x / 2^X) to E4M3 with saturation.  x / 2^X is exact for bf16 input.  Scales go
-// to the tile-ordered blocks (one 4-byte word per K tile of 128); rows at or past
-// offsets[E] (there are such rows only when a slot held an invalid expert index) are
-// left alone.
+// RNE(x / 2^X) to E4M3 with saturation.  x / 2^X is exact for bf16 input.  Each lane
+// takes 8 consecutive elements (a 32-block is 4 lanes, a 128-element K tile 16), so
+// a warp step covers 256 elements; scales go to the tile-ordered blocks, one 4-byte
+// word per K tile.  Rows at or past offsets[E] (there are such rows only when a slot
+// held an invalid expert index) are left alone.
 __global__ void gather_quant_kernel(const uint16_t *__restrict__ x, int H, int I, int k, int E,
                                     const int32_t *__restrict__ idx, const int32_t *__restrict__ perm,
                                     const int32_t *__restrict__ offsets, const int32_t *__restrict__ tile_off, int BN,
@@ -221,26 +222,52 @@ __global__ void gather_quant_kernel(const uint16_t *__restrict__ x, int H, int I
     const RowTile rt = row_tile(e, r - offsets[e], tile_off, BN);
     const uint16_t *xr = x + (size_t)t * H;
     uint8_t *qr = xq + (size_t)r * H;
-    uint32_t word = 0;
-    for (int b0 = 0; b0 < H; b0 += 32) {
-        const float v = bf16_bits_to_float(xr[b0 + lane]);
-        float a = fabsf(v);
-        for (int off = 16; off > 0; off >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, off));
+    for (int b0 = 0; b0 < H; b0 += 256) {
+        // H is a multiple of 128: the upper half-warp may have nothing in the last step
+        const bool on = b0 + lane * 8 < H;
+        float f[8];
+        if (on) {
+            const uint4 v = *reinterpret_cast<const uint4 *>(xr + b0 + lane * 8);
+            const unsigned int u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int i = 0; i < 4; i++) {
+                f[2 * i] = __uint_as_float(u[i] << 16);
+                f[2 * i + 1] = __uint_as_float(u[i] & 0xffff0000u);
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; i++) f[i] = 0.f;
+        }
+        float a = 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; i++) a = fmaxf(a, fabsf(f[i]));
+        a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
+        a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
         int X = -127;
         if (a > 0.f) {
             int ex;
             frexpf(a, &ex);
             X = max(-127, min(127, ex - 1 - 8));
         }
-        const float sv = ldexpf(v, -X);
-        unsigned short pair;
-        asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(pair) : "f"(0.f), "f"(sv));
-        qr[b0 + lane] = (uint8_t)(pair & 0xFF);
-        const int blk = b0 / 32;
-        word |= (uint32_t)(X + 127) << (8 * (blk & 3));
-        if ((blk & 3) == 3) {
-            if (lane == 0) *reinterpret_cast<uint32_t *>(xs + sf_tile_word(rt.tile, H / 128, nsfb, blk >> 2, rt.col)) = word;
-            word = 0;
+        uint32_t q[2] = {0u, 0u};
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            unsigned short pair;
+            asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;"
+                : "=h"(pair)
+                : "f"(ldexpf(f[2 * i + 1], -X)), "f"(ldexpf(f[2 * i], -X)));
+            q[i >> 1] |= (uint32_t)pair << (16 * (i & 1));
+        }
+        if (on) *reinterpret_cast<uint2 *>(qr + b0 + lane * 8) = make_uint2(q[0], q[1]);
+        // scale word of each K tile: the bytes of lanes 16h, 16h+4, 16h+8, 16h+12
+        const uint32_t sb = (uint32_t)(X + 127);
+        const uint32_t b1 = __shfl_down_sync(0xffffffffu, sb, 4);
+        const uint32_t b2 = __shfl_down_sync(0xffffffffu, sb, 8);
+        const uint32_t b3 = __shfl_down_sync(0xffffffffu, sb, 12);
+        if ((lane & 15) == 0 && on) {
+            const int kt = (b0 + lane * 8) >> 7;
+            *reinterpret_cast<uint32_t *>(xs + sf_tile_word(rt.tile, H / 128, nsfb, kt, rt.col)) =
+                sb | (b1 << 8) | (b2 << 16) | (b3 << 24);
         }
     }
     if (lane == 0) zero_h_pad(hs, I, nsfb, rt);
