@@ -424,7 +424,7 @@ def run_ours(args):
             "vs_baseline": None, "dtype": "mxfp4(e2m1)xbf16, f16x2 block MAC, fp32 accumulate",
             "data": "synthetic",
             "config": {"workload": WORKLOAD, "parallelism": f"replicas x{world}",
-                       "l2": "inputs larger than L2: 16.6 GB resident pool, 16 fresh experts per token",
+                       "l2": "inputs larger than L2: 17.6 GB resident pool, 16 fresh experts per token",
                        "graph": "one CUDA graph per step (1000 tokens)"},
             "expert_weight_hbm_gbs": layer_gbs, "hbm_frac_layer": layer_gbs / hbm,
             "roofline": {"bound": "hbm", "kernel": "decode_fused", "achieved": achieved, "peak": hbm,
