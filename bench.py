@@ -235,8 +235,8 @@ def measure_verify(moe, torch, pool, Wr, dev, M, nbatch=50, iters=3):
 
 def measure_stacked(moe, torch, pool0, dev, ntok=64, L=8, iters=2):
     """Eight stacked layers (each its own pool, router and Zipf skew), one token at a
-    time: per layer x_hat = prescale(x), route(x_hat), x = x + MoE(x_hat).  Reports
-    layer-tokens/s.  Allocates L - 1 more full-size pools."""
+    time: per layer x_hat = prescale(x) and route(x_hat) in one router launch, then
+    x = x + MoE(x_hat).  Reports layer-tokens/s.  Allocates L - 1 more full-size pools."""
     s = synth.FULL
     pools = [pool0]
     for l in range(1, L):
@@ -259,8 +259,8 @@ def measure_stacked(moe, torch, pool0, dev, ntok=64, L=8, iters=2):
     def step():
         for t in range(ntok):
             for l in range(L):
-                moe.moe_prescale(xs[l][t:t + 1], out=xh)
-                moe.moe_route_topk(xh, Wrs[l], s.k, skews[l], ws=ws_r, idx=idx, w=w)
+                # pre-scale folded into the single-token router, which writes x_hat
+                moe.moe_route_topk_prescaled(xs[l][t:t + 1], Wrs[l], s.k, skews[l], ws=ws_r, idx=idx, w=w, xhat=xh)
                 moe.moe_expert_forward_decode(pools[l], xh, idx, w, residual=xs[l][t:t + 1], ws=ws_d,
                                               y=xs[l + 1][t:t + 1])
 

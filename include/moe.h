@@ -158,6 +158,15 @@ moe_status moe_route_topk_static(const uint16_t *x, int M, int H, const uint16_t
                                  const float *skew, int k, int32_t *idx, float *w,
                                  moe_stream_t stream);
 
+/* Pre-scaled routing for stacked layers: x_hat = moe_prescale(x) is written to
+ * xhat [M][H] bf16 (16-byte aligned) and the rows are routed as moe_route_topk
+ * routes x_hat (same idx, w and status).  For M = 1 the pre-scale is folded into
+ * the router's own staging of the token (one launch); for M > 1 it runs first.
+ * ws: MOE_OP_ROUTE bytes. */
+moe_status moe_route_topk_prescaled(const uint16_t *x, int M, int H, const uint16_t *Wr, int E,
+                                    const float *skew, int k, int32_t *idx, float *w, uint16_t *xhat,
+                                    void *ws, size_t ws_bytes, moe_stream_t stream);
+
 /* ------------------------------------------------------- decode / verify
  * Expert forward for M (1..32) rows that were routed by moe_route_topk: each
  * distinct selected expert is read from the pool once and applied to every row

@@ -32,7 +32,8 @@ EXPORTED = [
     "moe_pool_bytes", "moe_pool_record_bytes", "moe_pool_create", "moe_pool_destroy",
     "moe_pool_fill_synthetic", "moe_pool_upload_expert", "moe_pool_download_expert",
     "moe_workspace_size", "moe_clear_status", "moe_check_status", "moe_status_string",
-    "moe_route_topk", "moe_route_topk_static", "moe_expert_forward_decode", "moe_prescale",
+    "moe_route_topk", "moe_route_topk_static", "moe_route_topk_prescaled", "moe_expert_forward_decode",
+    "moe_prescale",
     "moe_expert_forward_grouped", "moe_combine", "moe_trace_begin", "moe_trace_end",
 ]
 
@@ -68,6 +69,7 @@ def lib() -> ctypes.CDLL:
             "moe_status_string": (ctypes.c_char_p, [_i]),
             "moe_route_topk": (_i, [_vp, _i, _i, _vp, _i, _vp, _i, _vp, _vp, _vp, _sz, _vp]),
             "moe_route_topk_static": (_i, [_vp, _i, _i, _vp, _i, _vp, _i, _vp, _vp, _vp]),
+            "moe_route_topk_prescaled": (_i, [_vp, _i, _i, _vp, _i, _vp, _i, _vp, _vp, _vp, _vp, _sz, _vp]),
             "moe_expert_forward_decode": (_i, [_vp, _vp, _i, _vp, _vp, _i, _vp, _vp, _vp, _sz, _vp]),
             "moe_prescale": (_i, [_vp, _i, _i, _vp, _vp]),
             "moe_expert_forward_grouped": (_i, [_vp, _vp, _i, _vp, _i, _i, _vp, _vp, _vp, _vp, _i, _vp, _sz,
@@ -211,6 +213,27 @@ def moe_route_topk(x: torch.Tensor, Wr: torch.Tensor, k: int, skew: torch.Tensor
     _check(lib().moe_route_topk(_ptr(x), M, H, _ptr(Wr), E, _ptr(skew), k, _ptr(idx), _ptr(w), _ptr(ws),
                                 ws.numel(), _stream(stream)), "moe_route_topk")
     return idx, w
+
+
+def moe_route_topk_prescaled(x: torch.Tensor, Wr: torch.Tensor, k: int, skew: torch.Tensor | None = None,
+                             ws: torch.Tensor | None = None, idx: torch.Tensor | None = None,
+                             w: torch.Tensor | None = None, xhat: torch.Tensor | None = None, stream=None):
+    """Route x_hat = moe_prescale(x); returns (idx, w, x_hat)."""
+    _need(x, torch.bfloat16, "x")
+    _need(Wr, torch.bfloat16, "Wr")
+    M, H = x.shape
+    E = Wr.shape[0]
+    if skew is not None:
+        _need(skew, torch.float32, "skew")
+    if ws is None:
+        ws = workspace(moe_workspace_size(MOE_OP_ROUTE, E, H, 32, M, k), x.device)
+    idx = torch.empty((M, k), dtype=torch.int32, device=x.device) if idx is None else idx
+    w = torch.empty((M, k), dtype=torch.float32, device=x.device) if w is None else w
+    xhat = torch.empty_like(x) if xhat is None else xhat
+    _need(xhat, torch.bfloat16, "xhat")
+    _check(lib().moe_route_topk_prescaled(_ptr(x), M, H, _ptr(Wr), E, _ptr(skew), k, _ptr(idx), _ptr(w), _ptr(xhat),
+                                          _ptr(ws), ws.numel(), _stream(stream)), "moe_route_topk_prescaled")
+    return idx, w, xhat
 
 
 def moe_route_topk_static(x: torch.Tensor, Wr: torch.Tensor, k: int, skew: torch.Tensor | None = None,

@@ -216,6 +216,18 @@ moe_status moe_route_topk(const uint16_t *x, int M, int H, const uint16_t *Wr, i
     return cuda_status(launch_route(x, M, H, Wr, E, skew, k, idx, w, ws, (cudaStream_t)stream));
 }
 
+moe_status moe_route_topk_prescaled(const uint16_t *x, int M, int H, const uint16_t *Wr, int E, const float *skew,
+                                    int k, int32_t *idx, float *w, uint16_t *xhat, void *ws, size_t ws_bytes,
+                                    moe_stream_t stream) {
+    if (M < 0 || x == nullptr || Wr == nullptr || idx == nullptr || w == nullptr || xhat == nullptr || ws == nullptr)
+        return MOE_ERR_INVALID_ARG;
+    if (k < 1 || k > kMaxK || k > E) return MOE_ERR_INVALID_ARG;
+    if (E > 4096 || H < 8 || H % 8 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned(x, 16) || !aligned(xhat, 16) || !aligned(Wr, 16) || !aligned(ws, 256)) return MOE_ERR_INVALID_ARG;
+    if (ws_bytes < route_workspace_bytes(E, M, k)) return MOE_ERR_WORKSPACE;
+    return cuda_status(launch_route(x, M, H, Wr, E, skew, k, idx, w, ws, (cudaStream_t)stream, xhat));
+}
+
 moe_status moe_expert_forward_decode(const moe_pool *pool, const uint16_t *x, int M, const int32_t *idx,
                                      const float *w, int k, const uint16_t *residual, uint16_t *y, void *ws,
                                      size_t ws_bytes, moe_stream_t stream) {

@@ -148,8 +148,10 @@ cudaError_t launch_pool_kernel(const PoolView &v, int mode, uint64_t seed, int e
                                uint8_t *out_scales, cudaStream_t st);
 
 size_t route_workspace_bytes(int E, int M, int k);
+// xhat != nullptr: route x_hat = prescale(x) (the exact power-of-two pre-scale of
+// launch_prescale) and write it to xhat.
 cudaError_t launch_route(const uint16_t *x, int M, int H, const uint16_t *Wr, int E, const float *skew,
-                         int k, int32_t *idx, float *w, void *ws, cudaStream_t st);
+                         int k, int32_t *idx, float *w, void *ws, cudaStream_t st, uint16_t *xhat = nullptr);
 
 size_t decode_workspace_bytes(int E, int H, int I, int M, int k);
 // The single-token fused decode runs at most this many CTAs; its workspace holds

@@ -79,10 +79,14 @@ __device__ __forceinline__ void unpack_bf16x8(const uint4 &v, float f[8]) {
 // expert 4*bx + w/2 over one half of H; lanes take 8 consecutive elements per step.
 // Used with 256 threads; x rows staged in dynamic shared memory.  NB chunks of
 // W_r are loaded per batch (one batch covers H/2 = 4096 with NB = 16).
+// With `prescale` (one token): the staged row is replaced by x_hat = x * 2^-p, p =
+// floor(log2 max|x|) - 2, rounded to bf16 element by element exactly as
+// prescale_kernel does, and the logits are those of x_hat; CTA 0 writes x_hat to
+// xhat_out (when not null).
 template <int NB>
 __device__ void logits_block(const uint16_t *__restrict__ x, int M, int H, const uint16_t *__restrict__ Wr, int E,
                              const float *__restrict__ skew, float *__restrict__ logit,
-                             float *__restrict__ bound) {
+                             float *__restrict__ bound, bool prescale = false, uint16_t *xhat_out = nullptr) {
     extern __shared__ __align__(16) uint16_t xs[];  // [nt][H]
     __shared__ float red_l[8][kLogitTokens], red_s[8][kLogitTokens];
     const int m0 = blockIdx.y * kLogitTokens;
@@ -91,6 +95,44 @@ __device__ void logits_block(const uint16_t *__restrict__ x, int M, int H, const
     const uint4 *xg = reinterpret_cast<const uint4 *>(x + (size_t)m0 * H);
     for (int i = threadIdx.x; i < nvec; i += blockDim.x) reinterpret_cast<uint4 *>(xs)[i] = xg[i];
     __syncthreads();
+    if (prescale) {
+        __shared__ float pmax[32];
+        float am = 0.f;
+        for (int i = threadIdx.x; i < nvec; i += blockDim.x) {
+            float f[8];
+            unpack_bf16x8(reinterpret_cast<const uint4 *>(xs)[i], f);
+#pragma unroll
+            for (int j = 0; j < 8; j++) am = fmaxf(am, fabsf(f[j]));
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, off));
+        if ((threadIdx.x & 31) == 0) pmax[threadIdx.x >> 5] = am;
+        __syncthreads();
+        float amax = 0.f;
+        for (int w = 0; w < (int)(blockDim.x >> 5); w++) amax = fmaxf(amax, pmax[w]);
+        int p = 0;
+        if (amax > 0.f) {
+            int ex;
+            frexpf(amax, &ex);
+            p = ex - 1 - 2;
+        }
+        for (int i = threadIdx.x; i < nvec; i += blockDim.x) {
+            float f[8];
+            unpack_bf16x8(reinterpret_cast<const uint4 *>(xs)[i], f);
+            uint32_t u[4];
+#pragma unroll
+            for (int j = 0; j < 4; j++) {
+                const __nv_bfloat16 lo = __float2bfloat16_rn(ldexpf(f[2 * j], -p));
+                const __nv_bfloat16 hi = __float2bfloat16_rn(ldexpf(f[2 * j + 1], -p));
+                u[j] = (uint32_t)(*reinterpret_cast<const uint16_t *>(&lo)) |
+                       ((uint32_t)(*reinterpret_cast<const uint16_t *>(&hi)) << 16);
+            }
+            const uint4 v = make_uint4(u[0], u[1], u[2], u[3]);
+            reinterpret_cast<uint4 *>(xs)[i] = v;
+            if (xhat_out != nullptr && blockIdx.x == 0) reinterpret_cast<uint4 *>(xhat_out)[i] = v;
+        }
+        __syncthreads();
+    }
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int e = blockIdx.x * kLogitExperts + (warp >> 1);
@@ -186,7 +228,9 @@ __global__ void __launch_bounds__(256) route_logits_kernel(const uint16_t *__res
 // running sum (H/256 of them), then the tree of the four groups (2), the sum of
 // the two halves (1) and the skew (1).
 constexpr int kTileT = 64, kTileE = 64, kTileKStep = 64, kTiledThreads = 256;
-constexpr size_t kTiledSmem = 2 * 2 * 4 * 16 * 64 * sizeof(float);  // x and W_r, two buffers (64 KB)
+constexpr int kTiledStages = 3;  // bf16 staging buffers in flight
+// x and W_r: two fp32 compute buffers (64 KB) and the bf16 staging ring (3 x 16 KB)
+constexpr size_t kTiledSmem = 2 * 2 * 4 * 16 * 64 * sizeof(float) + (size_t)kTiledStages * 2 * 64 * 64 * sizeof(uint16_t);
 
 __host__ __device__ inline int tiled_tree_depth(int H) { return 31 + (H + 255) / 256 + 2 + 1 + 1; }
 
@@ -218,45 +262,78 @@ __global__ void route_norms_kernel(const uint16_t *__restrict__ x, int M, int H,
     }
 }
 
+// 16-byte asynchronous copy global -> shared (both 16-byte aligned); src_bytes 0
+// writes zeros without reading.
+__device__ __forceinline__ void cp_async16(void *dst, const void *src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)),
+                 "l"(src), "r"(src_bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
 // Partial logits of one half of H: half 0 into logit[], half 1 into bound[] (the
 // finish kernel combines them in place).  Rows past M or E are computed on zeros and
 // not stored.
+//
+// Each step of 64 K elements: x and W_r rows arrive as raw bf16 by cp.async in a ring
+// of kTiledStages staging buffers ([row][64] with the 16-byte chunks of row r at
+// position chunk ^ (r % 8), so the conversion reads are free of bank conflicts),
+// then every thread converts 2 x 16 elements into the fp32 K-major buffer of the
+// step (two buffers alternate), and the four K groups compute from it.
 __global__ void __launch_bounds__(kTiledThreads, 1)
     route_tiled_kernel(const uint16_t *__restrict__ x, int M, int H, const uint16_t *__restrict__ Wr, int E,
                        float *__restrict__ part0, float *__restrict__ part1) {
     extern __shared__ __align__(16) float tiled_smem[];  // kTiledSmem bytes
-    auto xs = reinterpret_cast<float(*)[4][16][kTileT]>(tiled_smem);                        // [buffer][group][k][token]
-    auto wsm = reinterpret_cast<float(*)[4][16][kTileE]>(tiled_smem + 2 * 4 * 16 * kTileT);  // [buffer][group][k][expert]
+    // fp32 compute buffers [2][group][k][64] for x and W_r, then the bf16 staging ring
+    auto xs = reinterpret_cast<float(*)[4][16][kTileT]>(tiled_smem);
+    auto wsm = reinterpret_cast<float(*)[4][16][kTileE]>(tiled_smem + 2 * 4 * 16 * kTileT);
+    uint16_t *stage = reinterpret_cast<uint16_t *>(tiled_smem + 2 * 4 * 16 * (kTileT + kTileE));
+    constexpr int kStageElems = 2 * 64 * kTileKStep;  // x rows then W_r rows, bf16
     const int tid = threadIdx.x;
     const int t0 = blockIdx.y * kTileT, e0 = blockIdx.x * kTileE;
     const int half = blockIdx.z;
     const int hlen = H / 2, hbase = half * hlen;
     const int nsteps = hlen / kTileKStep;
-    // staging: thread (row = tid % 64, group = tid / 64) loads 16 consecutive K
-    // elements of its token row and of its expert row per step
-    const int lrow = tid & 63, lgrp = tid >> 6;
-    const bool tv = t0 + lrow < M, ev = e0 + lrow < E;
-    const uint16_t *xrow = x + (size_t)(tv ? t0 + lrow : 0) * H + hbase + 16 * lgrp;
-    const uint16_t *wrow = Wr + (size_t)(ev ? e0 + lrow : 0) * H + hbase + 16 * lgrp;
-    uint4 px[2], pw[2];
-    auto fetch = [&](int step) {
-        const uint4 *xp = reinterpret_cast<const uint4 *>(xrow + step * kTileKStep);
-        const uint4 *wp = reinterpret_cast<const uint4 *>(wrow + step * kTileKStep);
-        px[0] = tv ? __ldg(xp) : make_uint4(0u, 0u, 0u, 0u);
-        px[1] = tv ? __ldg(xp + 1) : make_uint4(0u, 0u, 0u, 0u);
-        pw[0] = ev ? __ldg(wp) : make_uint4(0u, 0u, 0u, 0u);
-        pw[1] = ev ? __ldg(wp + 1) : make_uint4(0u, 0u, 0u, 0u);
+    // copies: 2 operands x 64 rows x 8 chunks of 16 bytes, four per thread
+    auto issue = [&](int step) {
+        uint16_t *st = stage + (size_t)(step % kTiledStages) * kStageElems;
+#pragma unroll
+        for (int q = 0; q < 4; q++) {
+            const int c = tid + q * kTiledThreads;  // 0..1023
+            const int op = c >> 9, row = (c >> 3) & 63, ch = c & 7;
+            const int grow = (op == 0 ? t0 : e0) + row;
+            const bool valid = grow < (op == 0 ? M : E);
+            const uint16_t *src = (op == 0 ? x : Wr) + (size_t)(valid ? grow : 0) * H + hbase + step * kTileKStep + ch * 8;
+            cp_async16(st + (size_t)op * 64 * kTileKStep + row * kTileKStep + ((ch ^ (row & 7)) * 8), src,
+                       valid ? 16u : 0u);
+        }
+        cp_async_commit();
     };
-    auto stash = [&](int buf) {
-        float f[8];
+    // conversion: thread (row = tid % 64, group g = tid / 64) takes elements 16g..16g+15
+    // of its x row and its W_r row
+    const int crow = tid & 63, cg = tid >> 6;
+    auto convert = [&](int step) {
+        const uint16_t *st = stage + (size_t)(step % kTiledStages) * kStageElems;
+        const int buf = step & 1;
 #pragma unroll
-        for (int q = 0; q < 2; q++) {
-            unpack_bf16x8(px[q], f);
+        for (int op = 0; op < 2; op++) {
 #pragma unroll
-            for (int j = 0; j < 8; j++) xs[buf][lgrp][8 * q + j][lrow] = f[j];
-            unpack_bf16x8(pw[q], f);
+            for (int hq = 0; hq < 2; hq++) {
+                const int ch = 2 * cg + hq;
+                const uint4 v = *reinterpret_cast<const uint4 *>(st + (size_t)op * 64 * kTileKStep + crow * kTileKStep +
+                                                                 ((ch ^ (crow & 7)) * 8));
+                float f[8];
+                unpack_bf16x8(v, f);
 #pragma unroll
-            for (int j = 0; j < 8; j++) wsm[buf][lgrp][8 * q + j][lrow] = f[j];
+                for (int j = 0; j < 8; j++) {
+                    if (op == 0)
+                        xs[buf][cg][8 * hq + j][crow] = f[j];
+                    else
+                        wsm[buf][cg][8 * hq + j][crow] = f[j];
+                }
+            }
         }
     };
     // compute: group g = tid / 64; within it ty = (tid % 64) / 8, tx = tid % 8; tokens
@@ -267,12 +344,24 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
     for (int i = 0; i < 8; i++)
 #pragma unroll
         for (int j = 0; j < 8; j++) inner[i][j] = outer[i][j] = 0.f;
-    fetch(0);
-    stash(0);
-    __syncthreads();
+#pragma unroll
+    for (int p = 0; p < kTiledStages - 1; p++) {
+        if (p < nsteps)
+            issue(p);
+        else
+            cp_async_commit();  // empty group: the wait counts stay uniform
+    }
     for (int step = 0; step < nsteps; step++) {
+        cp_async_wait<kTiledStages - 2>();  // this thread's copies of `step` have landed
+        __syncthreads();                     // everyone's; and everyone is done with step - 1's
+                                             // compute buffer and step - 1's staging slot
+        if (step + kTiledStages - 1 < nsteps)
+            issue(step + kTiledStages - 1);
+        else
+            cp_async_commit();
+        convert(step);
+        __syncthreads();
         const int buf = step & 1;
-        if (step + 1 < nsteps) fetch(step + 1);
 #pragma unroll
         for (int k = 0; k < 16; k++) {
             const float4 a0 = *reinterpret_cast<const float4 *>(&xs[buf][g][k][4 * ty]);
@@ -295,11 +384,11 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
                     inner[i][j] = 0.f;
                 }
         }
-        if (step + 1 < nsteps) stash(buf ^ 1);
-        __syncthreads();
     }
+    cp_async_wait<0>();
+    __syncthreads();
     // the four groups' sums: ((g0 + g1) + (g2 + g3)), through shared memory
-    float *red = tiled_smem;  // both staging buffers: 4 x [64][64] floats
+    float *red = tiled_smem;  // the two compute buffers: 4 x [64][64] floats
 #pragma unroll
     for (int i = 0; i < 8; i++)
 #pragma unroll
@@ -911,10 +1000,11 @@ template <int J>
 __global__ void __launch_bounds__(kRouteThreads) route_single_kernel(
     const uint16_t *__restrict__ x, int H, const uint16_t *__restrict__ Wr, int E, const float *__restrict__ skew,
     int k, float *__restrict__ logit, float *__restrict__ bound, int32_t *__restrict__ idx_out,
-    float *__restrict__ w_out, StatusWord *st) {
+    float *__restrict__ w_out, StatusWord *st, uint16_t *xhat) {
     __shared__ SelectShared s;
     __shared__ int last;
-    logits_block<16>(x, 1, H, Wr, E, skew, logit, bound);
+    extern __shared__ __align__(16) uint16_t xrow[];  // the (pre-scaled) token staged by logits_block
+    logits_block<16>(x, 1, H, Wr, E, skew, logit, bound, xhat != nullptr, xhat);
     __syncthreads();
     if (threadIdx.x == 0) {
         // release: this CTA's logits (ordered by the CTA barrier) before the
@@ -925,20 +1015,23 @@ __global__ void __launch_bounds__(kRouteThreads) route_single_kernel(
     }
     __syncthreads();
     if (!last) return;
-    select_token<J>(0, x, H, Wr, E, skew, k, logit, bound, idx_out, w_out, st, s);
+    // the exact fallback reads the token this CTA staged (x_hat when pre-scaled)
+    select_token<J>(0, xhat != nullptr ? xrow : x, H, Wr, E, skew, k, logit, bound, idx_out, w_out, st, s);
     if (threadIdx.x == 0) st->pad[kStRouteTicket] = 0u;
 }
 
 template <int J>
 cudaError_t launch_route_j(const uint16_t *x, int M, int H, const uint16_t *Wr, int E, const float *skew, int k,
-                           int32_t *idx, float *w, const RouteWs &r, size_t smem1, StatusWord *stw, cudaStream_t st) {
+                           int32_t *idx, float *w, const RouteWs &r, size_t smem1, StatusWord *stw, cudaStream_t st,
+                           uint16_t *xhat) {
     static int smem_single = 0;
     dim3 g1((E + kLogitExperts - 1) / kLogitExperts, (M + kLogitTokens - 1) / kLogitTokens);
     if (M == 1) {
         cudaError_t e = ensure_dynamic_smem(route_single_kernel<J>, smem1, smem_single);
         if (e != cudaSuccess) return e;
         TraceScope trace_scope("route_single", st);
-        route_single_kernel<J><<<g1.x, kRouteThreads, smem1, st>>>(x, H, Wr, E, skew, k, r.logit, r.bound, idx, w, stw);
+        route_single_kernel<J><<<g1.x, kRouteThreads, smem1, st>>>(x, H, Wr, E, skew, k, r.logit, r.bound, idx, w, stw,
+                                                                  xhat);
         return cudaGetLastError();
     }
     if (M >= kTiledMinTokens && H % 128 == 0) {
@@ -972,7 +1065,7 @@ size_t route_workspace_bytes(int E, int M, int k) {
 }
 
 cudaError_t launch_route(const uint16_t *x, int M, int H, const uint16_t *Wr, int E, const float *skew, int k,
-                         int32_t *idx, float *w, void *ws, cudaStream_t st) {
+                         int32_t *idx, float *w, void *ws, cudaStream_t st, uint16_t *xhat) {
     if (M == 0) return cudaSuccess;
     RouteWs r = route_ws(ws, M, E);
     const int nt = M < kLogitTokens ? M : kLogitTokens;
@@ -982,9 +1075,22 @@ cudaError_t launch_route(const uint16_t *x, int M, int H, const uint16_t *Wr, in
     cudaError_t e = ensure_dynamic_smem(route_logits_kernel, smem1, smem_logits);
     if (e != cudaSuccess) return e;
     StatusWord *stw = reinterpret_cast<StatusWord *>(ws);
-    if (E <= 4 * kRouteThreads) return launch_route_j<4>(x, M, H, Wr, E, skew, k, idx, w, r, smem1, stw, st);
-    if (E <= 8 * kRouteThreads) return launch_route_j<8>(x, M, H, Wr, E, skew, k, idx, w, r, smem1, stw, st);
-    return launch_route_j<16>(x, M, H, Wr, E, skew, k, idx, w, r, smem1, stw, st);
+    // pre-scaled routing: one token folds the pre-scale into the router's own staging
+    // of x; several tokens pre-scale first and route x_hat
+    uint16_t *fused_xhat = nullptr;
+    if (xhat != nullptr) {
+        if (M == 1) {
+            fused_xhat = xhat;
+        } else {
+            if ((e = launch_prescale(x, M, H, xhat, st)) != cudaSuccess) return e;
+            x = xhat;
+        }
+    }
+    if (E <= 4 * kRouteThreads)
+        return launch_route_j<4>(x, M, H, Wr, E, skew, k, idx, w, r, smem1, stw, st, fused_xhat);
+    if (E <= 8 * kRouteThreads)
+        return launch_route_j<8>(x, M, H, Wr, E, skew, k, idx, w, r, smem1, stw, st, fused_xhat);
+    return launch_route_j<16>(x, M, H, Wr, E, skew, k, idx, w, r, smem1, stw, st, fused_xhat);
 }
 
 }  // namespace moe

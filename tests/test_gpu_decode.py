@@ -270,6 +270,49 @@ def test_bad_index_sets_status(tiny, M):
     assert moe.moe_check_status(ws) == moe.MOE_OK      # cleared by the first check
 
 
+@pytest.mark.parametrize("M", [1, 3])
+def test_route_prescaled_matches_prescale_then_route(full, M):
+    """moe_route_topk_prescaled writes x_hat = moe_prescale(x) bit for bit and routes it
+    exactly as moe_route_topk routes x_hat (M = 1 folds the pre-scale into the router)."""
+    s, _, _, Wr = full
+    rng = np.random.default_rng(M)
+    xb = synth.bf16_bits_from_f64(synth.bf16_bits_to_f64(synth.tokens_bf16(synth.TOKENS_SEED["stacked"], 0, M, s.H))
+                                  * np.exp2(rng.integers(-20, 20, size=(M, 1))))
+    x = to_dev_bf16(xb)
+    skew = torch.from_numpy(synth.zipf_skew_f32(synth.skew_seed(0), s.E)).cuda()
+    idx_p, w_p, xh_p = moe.moe_route_topk_prescaled(x, Wr, s.k, skew)
+    xh = moe.moe_prescale(x)
+    idx_r, w_r = moe.moe_route_topk(xh, Wr, s.k, skew)
+    torch.cuda.synchronize()
+    assert torch.equal(xh_p.view(torch.int16), xh.view(torch.int16))
+    assert np.array_equal(bf16_to_bits(xh_p), np.stack([oracle.prescale(xb[m]) for m in range(M)]))
+    assert torch.equal(idx_p, idx_r)
+    assert torch.equal(w_p, w_r)
+
+
+def test_route_prescaled_exact_path(tiny):
+    """Planted ties after the pre-scale: the single-token router's exact fallback reads
+    the pre-scaled token it staged, and the indices match the oracle's on x_hat."""
+    s, _, Wrb0, _ = tiny
+    Wrb = Wrb0.copy()
+    xb = synth.bf16_bits_from_f64(synth.bf16_bits_to_f64(synth.tokens_bf16(7, 0, 1, s.H)) * 1024.0)
+    Wrb[50] = Wrb[17]
+    Wrb[63] = Wrb[17]
+    strong = synth.bf16_bits_from_f64(np.sign(synth.bf16_bits_to_f64(xb[0])) * 0.05)
+    for e in (3, 20, 41):
+        Wrb[e] = strong
+    ws = moe.workspace(moe.moe_workspace_size(moe.MOE_OP_ROUTE, s.E, s.H, 32, 1, s.k))
+    idx, w, xh = moe.moe_route_topk_prescaled(to_dev_bf16(xb), to_dev_bf16(Wrb), s.k, ws=ws)
+    torch.cuda.synchronize()
+    assert moe.exact_fallbacks(ws) > 0
+    assert moe.moe_check_status(ws) == moe.MOE_OK
+    xhb = oracle.prescale(xb[0])[None, :]
+    assert np.array_equal(bf16_to_bits(xh), xhb)
+    ridx, rw, _ = oracle.route(xhb, Wrb, s.k, None)
+    assert np.array_equal(idx.cpu().numpy(), ridx)
+    assert np.max(np.abs(w.cpu().numpy() - rw)) < 2e-6
+
+
 def test_stacked_layers_oracle_forced(tiny):
     """Per layer on the oracle's own layer input: pre-scale bit-exact, routing bit-exact,
     layer output within tolerance."""
