@@ -41,6 +41,14 @@ def peaks():
     return 6800.0, "fallback"
 
 
+def tensor_peak_tflops():
+    """Dense bf16 tensor peak (measured burst, else the fallback) and its source."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        return float(json.load(open(p))["bf16_tflops"]), "measured"
+    return 1900.0, "fallback"
+
+
 def expert_bytes(H, I):
     return synth.expert_code_bytes(H, I) + synth.expert_scale_bytes(H, I)
 
@@ -170,9 +178,15 @@ def measure_prefill(moe, torch, pool, Wr, dev, T, iters=3):
         kern[name] = tot / max(n, 1)
     wbytes = s.E * expert_bytes(s.H, s.I)
     flops = 2.0 * 3 * s.H * s.I * T * s.k
+    tflops = flops / ((kern["gemm_gateup"] + kern["gemm_down"]) / 1000.0) / 1e12
+    bf16, bf16_kind = tensor_peak_tflops()
     return {"tok_s": T / (ms / 1000.0), "ms": ms, "kernel_ms": kern,
             "gemm_weight_gbs": wbytes / ((kern["gemm_gateup"] + kern["gemm_down"]) / 1000.0) / 1e9,
-            "gemm_tflops": flops / ((kern["gemm_gateup"] + kern["gemm_down"]) / 1000.0) / 1e12}
+            "gemm_tflops": tflops,
+            # the MMA kind issued (mxf8f6f4: E2M1 x E4M3) runs at the FP8 rate; the FP4 rate
+            # needs both operands in FP4.  Peaks: bf16 (measured burst) x the nominal 2x / 6x
+            "tensor_frac": {"of_fp8_rate": tflops / (2.0 * bf16), "of_fp4_rate": tflops / (6.0 * bf16),
+                            "bf16_peak_tflops": bf16, "peak_kind": bf16_kind}}
 
 
 def measure_verify(moe, torch, pool, Wr, dev, M, nbatch=50, iters=3):
