@@ -138,6 +138,9 @@ __global__ void __launch_bounds__(kThreadsF, 1) decode_fused_kernel(const FusedA
         *abort_flag = 0;
         fence_mbar_init();
     }
+    // launched early (programmatic dependent launch): nothing global is read before the
+    // previous kernel of the stream (typically the router) has completed
+    griddep_wait();
     if (threadIdx.x < kMaxKF) samax[threadIdx.x] = 0u;
     if (threadIdx.x < k) {
         const int e = a.idx[threadIdx.x];
@@ -553,11 +556,13 @@ cudaError_t launch_decode_fused(const PoolView &v, const uint16_t *x, const int3
     cfg.blockDim = dim3(kThreadsF);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeCooperative;  // all CTAs co-resident: the grid barrier needs it
     attr[0].val.cooperative = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // overlap the launch with the
+    attr[1].val.programmaticStreamSerializationAllowed = 1;          // previous kernel's tail
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     TraceScope trace_scope("decode_fused", st);
     e = cudaLaunchKernelEx(&cfg, decode_fused_kernel, fa);
     if (e != cudaSuccess) return e;

@@ -25,6 +25,7 @@
 // intervals that touch the top k are re-evaluated with exact integer arithmetic
 // (every term is an integer multiple of 2^-268) and ordered by exact value.
 #include "moe_internal.cuh"
+#include "sm100_async.cuh"
 
 namespace moe {
 namespace {
@@ -1004,6 +1005,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_single_kernel(
     __shared__ SelectShared s;
     __shared__ int last;
     extern __shared__ __align__(16) uint16_t xrow[];  // the (pre-scaled) token staged by logits_block
+    griddep_wait();  // launched early: the previous kernel (e.g. the layer below) has completed
     logits_block<16>(x, 1, H, Wr, E, skew, logit, bound, xhat != nullptr, xhat);
     __syncthreads();
     if (threadIdx.x == 0) {
@@ -1030,8 +1032,20 @@ cudaError_t launch_route_j(const uint16_t *x, int M, int H, const uint16_t *Wr, 
         cudaError_t e = ensure_dynamic_smem(route_single_kernel<J>, smem1, smem_single);
         if (e != cudaSuccess) return e;
         TraceScope trace_scope("route_single", st);
-        route_single_kernel<J><<<g1.x, kRouteThreads, smem1, st>>>(x, H, Wr, E, skew, k, r.logit, r.bound, idx, w, stw,
-                                                                  xhat);
+        // programmatic dependent launch: the CTAs start while the previous kernel of the
+        // stream finishes and wait for it before reading anything
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(g1.x);
+        cfg.blockDim = dim3(kRouteThreads);
+        cfg.dynamicSmemBytes = smem1;
+        cfg.stream = st;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, route_single_kernel<J>, x, H, Wr, E, skew, k, r.logit, r.bound, idx, w, stw, xhat);
+        if (e != cudaSuccess) return e;
         return cudaGetLastError();
     }
     if (M >= kTiledMinTokens && H % 128 == 0) {
