@@ -165,5 +165,51 @@ def test_prefill_bad_index_sets_status():
     o_ref = oracle.pair_outputs(opool, s.H, s.I, xq, idx_ok, h_mode=1)
     amb = oracle.pair_ambiguity(opool, s.H, s.I, xq, idx_ok)
     valid = inv >= 0
-    part = out["partial"].float().cpu().numpy().astype(np.float64)[np.where(valid, inv, 0)]
+    # rows past offsets[E] were never written: select the valid pairs' rows before casting
+    part = out["partial"].float().cpu().numpy()[np.where(valid, inv, 0)].astype(np.float64)
     check_close(part[valid], o_ref[valid], "partial", amb=amb[valid])
+
+
+@pytest.mark.parametrize("T,nsample", [(2048, 5), (8192, 4)])
+def test_prefill_full_size_sweep_sampled(T, nsample):
+    """The 2048- and 8192-token prefill at the full shape, in the launch configuration the
+    benchmark times (96-column tiles with two row tiles per item; 192-column tiles with
+    two scale atoms per tile): exact routing of sampled tokens, the pair permutation of
+    the oracle's stable sort, and the sampled tokens' outputs."""
+    s = synth.FULL
+    seed = 720 + T
+    pool = moe.Pool(s.E, s.H, s.I)
+    moe.moe_pool_fill_synthetic(pool, seed)
+    Wrb = synth.router_bf16(seed + 1, s.E, s.H)
+    xb = synth.tokens_bf16(seed + 2, 0, T, s.H)
+    x = to_dev_bf16(xb)
+    idx, w = moe.moe_route_topk(x, to_dev_bf16(Wrb), s.k)
+    ws = moe.workspace(moe.moe_workspace_size(moe.MOE_OP_GROUPED, s.E, s.H, s.I, T, s.k))
+    out = moe.moe_expert_forward_grouped(pool, x, idx, ws=ws)
+    y = moe.moe_combine(out["partial"], out["inv_perm"], w)
+    assert moe.moe_check_status(ws) == moe.MOE_OK
+    idx_g = idx.cpu().numpy()
+    toks = np.linspace(0, T - 1, nsample).astype(np.int64)
+    ridx, rw, _ = oracle.route(xb[toks], Wrb, s.k)
+    assert np.array_equal(idx_g[toks], ridx)
+    assert np.max(np.abs(w.cpu().numpy()[toks] - rw)) < 2e-6
+    perm, inv, offsets = oracle.sort_pairs(idx_g, s.E)
+    assert np.array_equal(out["perm"].cpu().numpy(), perm)
+    assert np.array_equal(out["inv_perm"].cpu().numpy(), inv)
+    assert np.array_equal(out["offsets"].cpu().numpy(), offsets)
+    opool = oracle.SyntheticPool(seed, s.E, s.H, s.I)
+    xq = oracle.quant_rows_mxfp8(synth.bf16_bits_to_f64(xb[toks]))
+    yref = oracle.combine_rows(opool, s.H, s.I, xq, ridx, rw, h_mode=1)
+    amb = oracle.combine_ambiguity(opool, s.H, s.I, xq, ridx, rw)
+    check_close(bf16_to_f64(y)[toks], yref, "y", amb=amb)
+
+
+@pytest.mark.parametrize("T", [1, 3])
+def test_prefill_fewer_pairs_than_experts(T):
+    """16 or 48 pairs over 64 experts: most experts have no rows (the union list, empty
+    tiles and a grid smaller than the SM count)."""
+    s = synth.TINY
+    out, y, ref, xb = _run(s, T, 540 + T)
+    assert np.array_equal(out["perm"].cpu().numpy(), ref["perm"])
+    assert np.array_equal(out["offsets"].cpu().numpy(), ref["offsets"])
+    check_close(bf16_to_f64(y), ref["y"], "y", amb=ref["y_amb"])
