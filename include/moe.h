@@ -145,9 +145,9 @@ moe_status moe_route_topk(const uint16_t *x, int M, int H, const uint16_t *Wr, i
  * scratch buffers, and latency-critical threads that must not risk the
  * device-wide synchronisation cudaMalloc/cudaFree can cause.
  * Same arguments, kernels and results as moe_route_topk, but the scratch (status
- * word, fp32 logits and their bounds) lives in one static device array of the
- * library, 1 MiB + 256 B, that every GPU which loads the library keeps until the
- * process exits.  Limit: M * E <= 131072 (else MOE_ERR_UNSUPPORTED_SHAPE).
+ * word, fp32 logits and their bounds, the row norms of the many-token logit
+ * kernel) lives in one static device array of the library, about 1.5 MiB, that
+ * every GPU which loads the library keeps until the process exits.  Limit: M * E <= 131072 (else MOE_ERR_UNSUPPORTED_SHAPE).
  * The first call on a device looks up the array's device address (with that
  * device current), so make that first call before any stream capture.  All calls
  * share the array: calls that overlap on the GPU (other streams, other threads)
