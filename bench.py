@@ -139,6 +139,23 @@ def run_reference(args):
 # ---------------------------------------------------------------------- ours
 
 
+def max_over_ranks(ms, dist, device):
+    """The slowest rank's time (each rank runs an independent replica): an all-reduce
+    MAX over the process group, or ms itself without one."""
+    if dist is None:
+        return ms
+    import torch
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_value(world, tokens_per_rank, ms_per_step):
+    """Layer-tokens/s of the whole job: the tokens all ranks processed per step divided
+    by the (max-over-ranks) step time."""
+    return world * tokens_per_rank / (ms_per_step / 1000.0)
+
+
 def measure_prefill(moe, torch, pool, Wr, dev, T, iters=3):
     """Expert-major prefill of T tokens on the full-size layer: route, sort,
     MXFP8 gather, grouped gate/up and down GEMMs, combine.  Returns timings."""
@@ -363,13 +380,9 @@ def run_ours(args):
                 graph.replay()
             e1.record(stream)
         barrier()
-    ms = e0.elapsed_time(e1)
-    if dist is not None:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(e0.elapsed_time(e1), dist, dev)
     ms_step = ms / args.steps
-    value = world * NTOK / (ms_step / 1000.0)
+    value = whole_job_value(world, NTOK, ms_step)
 
     # end to end through the public API: pinned host x in, host y out, every step
     with torch.cuda.stream(stream):
