@@ -36,10 +36,21 @@ constexpr int kMaxStages = 12;
 constexpr int kTileM = 128;
 constexpr int kTileK = 128;   // elements (bytes in shared memory for both operands)
 
-// warps: 0 copies, 2 MMA, 4-7 and 8-11 epilogue (two warpgroups taking alternate
-// column groups; warp w reads TMEM lanes 32 (w % 4) ..), 1 and 3 idle
-constexpr int kGemmThreads = 384;
-constexpr int kEpiWarps = 8;
+// Two shapes of the kernel (template parameter NT = threads per CTA):
+//   NT = 384, one CTA per SM: warp 0 copies, warp 1 MMAs, warps 4-7 and 8-11 two
+//             epilogue warpgroups taking alternate column groups (2, 3 idle);
+//   NT = 192, two CTAs per SM: warp 0 copies, warp 1 MMAs, warps 2-5 one epilogue
+//             warpgroup.  Two CTAs give each SM two independent copy and MMA streams,
+//             which overlap the fixed per-instruction time of narrow (small N) MMAs.
+// An epilogue warp w reads TMEM lanes 32 (w % 4) ...
+constexpr int kEpiWarps = 8;  // the most epilogue warps (shared-memory sizing)
+template <int NT>
+struct GemmShape {
+    static constexpr int kEpiFirst = NT == 192 ? 2 : 4;          // first epilogue warp
+    static constexpr int kEpiWarps = NT / 32 - kEpiFirst;         // 4 or 8
+    static constexpr int kWarpGroups = kEpiWarps / 4;             // 1 or 2
+    static constexpr int kCtasPerSm = NT == 192 ? 2 : 1;
+};
 
 struct GemmArgs {
     int mode;            // 1: gate/up + SwiGLU + MXFP8, 2: down
@@ -189,9 +200,10 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
 // h = silu(g) * u, written as three E4M3 parts per 32-block along I (split_part);
 // down: the unweighted expert output row in fp32.
 __device__ __forceinline__ void epilogue_split3(const GemmArgs &a, uint32_t lane_base, bool ok, int nn, int nmma, int mt,
-                                                int row0, int n0, int tile, int warp, int wg, int lane, float *amax_x) {
+                                                int row0, int n0, int tile, int warp, int wg, int nwg, int lane,
+                                                float *amax_x) {
     const int bar = 2 + 2 * wg + (warp >> 1);  // the warp pair's barrier
-    for (int c0 = 48 * wg; c0 < nmma; c0 += 96) {
+    for (int c0 = 48 * wg; c0 < nmma; c0 += 48 * nwg) {
         float v0[16], v1[16], v2[16];
 #pragma unroll
         for (int j = 0; j < 16; j++) v0[j] = v1[j] = v2[j] = 0.f;
@@ -269,15 +281,16 @@ __device__ __forceinline__ float pow2_neg(int X) { return __uint_as_float((uint3
 
 // One-part (MXFP8) epilogue of a tile's 16-column groups: gate/up -> h = silu(g) * u
 // quantised to MXFP8 along I (OCP rule); down -> expert output rows.  ew = warp
-// index within the epilogue warpgroup (TMEM lanes 32ew..32ew+31); warpgroup wg takes
-// the column groups c0 = 16 wg, 16 wg + 32, ...  Warps 2p and 2p+1 of a warpgroup
+// index within the epilogue warpgroup (TMEM lanes 32ew..32ew+31); warpgroup wg of nwg
+// takes the column groups c0 = 16 wg, 16 (wg + nwg), ...  Warps 2p and 2p+1 of a warpgroup
 // hold the two halves of the same 32-blocks of I and exchange their maxima through
 // shared memory under a 64-thread barrier of their own (id 2 + 2 wg + p).
 __device__ __forceinline__ void epilogue_mx1(const GemmArgs &a, uint32_t lane_base, bool ok, int nn, int nmma, int mt,
-                                             int row0, int n0, int tile, int ew, int wg, int lane, float *amax_x) {
+                                             int row0, int n0, int tile, int ew, int wg, int nwg, int lane,
+                                             float *amax_x) {
     uint32_t *amax_u = reinterpret_cast<uint32_t *>(amax_x);
     const int bar = 2 + 2 * wg + (ew >> 1);  // the warp pair's barrier
-    for (int c0 = 16 * wg; c0 < nmma; c0 += 32) {
+    for (int c0 = 16 * wg; c0 < nmma; c0 += 16 * nwg) {
         float v[16];
 #pragma unroll
         for (int j = 0; j < 16; j++) v[j] = 0.f;
@@ -384,7 +397,8 @@ struct JobIter {
     }
 };
 
-__global__ void __launch_bounds__(kGemmThreads, 1)
+template <int NT>
+__global__ void __launch_bounds__(NT, GemmShape<NT>::kCtasPerSm)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const GemmArgs a) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -411,9 +425,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // other 8 (which the MMA format pads with) zero for the whole kernel.  The
     // scale-factor areas start at zero too (the second tile of an item past the
     // expert's last row tile gets no copy and reads whatever is there).
-    for (int i = threadIdx.x; i < ns * tpi * kTileM * kTileK / 16; i += kGemmThreads)
+    using Shape = GemmShape<NT>;
+    for (int i = threadIdx.x; i < ns * tpi * kTileM * kTileK / 16; i += NT)
         reinterpret_cast<uint4 *>(sA)[i] = make_uint4(0u, 0u, 0u, 0u);
-    for (int i = threadIdx.x; i < ns * (tpi + nsfb) * 512 / 16; i += kGemmThreads)
+    for (int i = threadIdx.x; i < ns * (tpi + nsfb) * 512 / 16; i += NT)
         reinterpret_cast<uint4 *>(sSFA)[i] = make_uint4(0u, 0u, 0u, 0u);  // sSFB follows sSFA
     fence_proxy_async_smem();
     if (threadIdx.x == 0) {
@@ -423,12 +438,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
         for (int b = 0; b < 2; b++) {
             mbar_init(&acc_full[b], 1);   // MMA commit after a tile's last K step
-            mbar_init(&acc_empty[b], kEpiWarps);  // the epilogue warps
+            mbar_init(&acc_empty[b], Shape::kEpiWarps);  // the epilogue warps
         }
         *abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == 2) tmem_alloc(tmem_slot, a.tmem_cols);
+    if (warp == 1) tmem_alloc(tmem_slot, a.tmem_cols);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -480,7 +495,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 }
             }
         }
-    } else if (warp == 2) {
+    } else if (warp == 1) {
         // ------------------------------------------------------- MMA issue
         int jb = 0, s = 0;  // tiles; slot of the next stage
         uint32_t ph = 0;    // its phase parity
@@ -541,9 +556,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             if (elect_one()) tc_commit(&acc_full[buf]);  // the accumulator is complete (or as far as it got)
             __syncwarp();
         }
-    } else if (warp >= 4) {
+    } else if (warp >= Shape::kEpiFirst) {
         // ------------------------------------------------------- epilogue
-        const int ew = warp & 3, wg = (warp - 4) >> 2;
+        const int ew = warp & 3, wg = (warp - Shape::kEpiFirst) >> 2;
         float *amax_g = amax_x + 64 * wg;
         int jb = 0;
         for (JobIter J(a, nu); J.valid(); J.next(), jb++) {
@@ -559,10 +574,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 const uint32_t lane_base =
                     tmem + (uint32_t)((buf * tpi + t) * a.BN) + ((uint32_t)(32 * ew) << 16);
                 if (a.nparts == 3)
-                    epilogue_split3(a, lane_base, ok, nn, nmma, J.mt + t, J.row0, J.n0(), J.tile(), ew, wg, lane,
-                                    amax_g);
+                    epilogue_split3(a, lane_base, ok, nn, nmma, J.mt + t, J.row0, J.n0(), J.tile(), ew, wg,
+                                    Shape::kWarpGroups, lane, amax_g);
                 else
-                    epilogue_mx1(a, lane_base, ok, nn, nmma, J.mt + t, J.row0, J.n0(), J.tile(), ew, wg, lane, amax_g);
+                    epilogue_mx1(a, lane_base, ok, nn, nmma, J.mt + t, J.row0, J.n0(), J.tile(), ew, wg,
+                                 Shape::kWarpGroups, lane, amax_g);
             }
             tc_fence_before();
             __syncwarp();
@@ -578,7 +594,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
     __syncthreads();
     tc_fence_after();
-    if (warp == 2) tmem_dealloc(tmem, a.tmem_cols);
+    if (warp == 1) tmem_dealloc(tmem, a.tmem_cols);
 }
 
 // ------------------------------------------------------------- tensor maps
@@ -627,9 +643,50 @@ uint32_t pow2_at_least(uint32_t v) {
     return p;
 }
 
-int g_gemm_smem = 0;
 int g_smem_max = 0;
 int g_sms = 0;
+
+int g_smem_set_384 = 0;
+int g_smem_set_192 = 0;
+
+// One grouped GEMM launch (args complete but for the shape fields set here).  The
+// kernel's shape: narrow tiles (BN <= 64, and the gate/up GEMM at BN <= 96) run two
+// CTAs of 6 warps per SM with one 128-row tile per item and at most 256 TMEM columns
+// each; wider tiles run one CTA of 12 warps per SM, with two 128-row tiles per item
+// (one 256-row tensor copy) while their four accumulators fit in TMEM.  Measured on the
+// full-size layer: two CTAs per SM took the 512-token GEMMs from 3.84 to 3.03 ms; the
+// down GEMM at BN = 96 and all GEMMs at BN >= 128 are faster with one.
+cudaError_t launch_one(GemmArgs ga, const uint8_t *a_base, int a_k, int a_rows, uint64_t a_ld, int E, const uint8_t *b_base,
+                       int b_k, int b_rows, int nexp, const char *trace_name, cudaStream_t stream) {
+    const int BN = ga.BN, nsfb = ga.nsfb;
+    const bool two = BN <= 64 || (BN <= 96 && ga.mode == 1);
+    const int tpi = two ? 1 : (BN <= 96 ? 2 : 1);
+    const uint32_t smem_cap = two ? (uint32_t)(g_smem_max / 2 - 1024) : (uint32_t)g_smem_max;
+    const uint32_t tmem_cap = two ? 256u : 512u;
+    // as many pipeline stages as fit the CTA's share of shared memory and TMEM
+    int ns = kMaxStages;
+    auto tmem_need = [&](int n) { return (uint32_t)(2 * tpi * BN + n * (4 * tpi + 4 * nsfb)); };
+    while (ns > 2 && (GemmSmemLayout(BN, ns, tpi).total + 1024 > smem_cap || tmem_need(ns) > tmem_cap)) ns--;
+    const uint32_t tmem_cols = pow2_at_least(tmem_need(ns));
+    if (tmem_cols > tmem_cap || GemmSmemLayout(BN, ns, tpi).total + 1024 > smem_cap) return cudaErrorNotSupported;
+    const size_t smem = GemmSmemLayout(BN, ns, tpi).total + 1024;  // alignment slack
+    cudaError_t e = two ? ensure_dynamic_smem(grouped_gemm_kernel<192>, smem, g_smem_set_192)
+                        : ensure_dynamic_smem(grouped_gemm_kernel<384>, smem, g_smem_set_384);
+    if (e != cudaSuccess) return e;
+    ga.ns = ns;
+    ga.tpi = tpi;
+    ga.tmem_cols = tmem_cols;
+    CUtensorMap mA, mB;
+    if ((e = make_map_a(&mA, a_base, a_k, a_rows, E, a_ld, ga.rec, tpi * kTileM)) != cudaSuccess) return e;
+    if ((e = make_map_b(&mB, b_base, b_k, b_rows, BN)) != cudaSuccess) return e;
+    const int items = nexp * ((ga.nmt + tpi - 1) / tpi);
+    TraceScope trace_scope(trace_name, stream);
+    if (two)
+        grouped_gemm_kernel<192><<<std::min(2 * g_sms, items), 192, smem, stream>>>(mA, mB, ga);
+    else
+        grouped_gemm_kernel<384><<<std::min(g_sms, items), 384, smem, stream>>>(mA, mB, ga);
+    return cudaGetLastError();
+}
 
 }  // namespace
 
@@ -653,20 +710,6 @@ cudaError_t launch_grouped_gemms(const PoolView &v, int T, int k, const int32_t 
         cudaDeviceGetAttribute(&g_smem_max, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
         cudaDeviceGetAttribute(&g_sms, cudaDevAttrMultiProcessorCount, dev);
     }
-    // Work items of two 128-row tiles (one 256-row tensor copy of A, 16 KB, which the
-    // copy engine streams at about twice the rate of 8 KB copies) while their four
-    // accumulators fit in TMEM, else single tiles.
-    const int tpi = BN <= 96 ? 2 : 1;
-    // as many pipeline stages as fit (one CTA per SM)
-    int ns = kMaxStages;
-    while (ns > 2 && GemmSmemLayout(BN, ns, tpi).total + 1024 > (uint32_t)g_smem_max) ns--;
-    const uint32_t tmem_cols = pow2_at_least((uint32_t)(2 * tpi * BN + ns * (4 * tpi + 4 * nsfb)));
-    if (tmem_cols > 512) return cudaErrorNotSupported;
-    const GemmSmemLayout L(BN, ns, tpi);
-    const size_t smem = L.total + 1024;  // alignment slack
-    e = ensure_dynamic_smem(grouped_gemm_kernel, smem, g_gemm_smem);
-    if (e != cudaSuccess) return e;
-
     GemmArgs ga;
     ga.E = v.E;
     ga.pool = v.base;
@@ -675,12 +718,8 @@ cudaError_t launch_grouped_gemms(const PoolView &v, int T, int k, const int32_t 
     ga.tile_off = g.tile_off;
     ga.uexp = g.uexp;
     ga.n_union = g.n_union;
-    const int nexp = P < v.E ? P : v.E;  // at most this many experts have pairs
     ga.BN = BN;
     ga.nsfb = nsfb;
-    ga.ns = ns;
-    ga.tpi = tpi;
-    ga.tmem_cols = tmem_cols;
     ga.I = v.I;
     ga.H = v.H;
     ga.hq = g.hq;
@@ -690,38 +729,25 @@ cudaError_t launch_grouped_gemms(const PoolView &v, int T, int k, const int32_t 
     ga.partial_dtype = partial_dtype;
     ga.nparts = nparts;
     ga.st = st;
+    const int nexp = P < v.E ? P : v.E;  // at most this many experts have pairs
 
     // GEMM 1: gate/up
-    CUtensorMap mA, mB;
-    if ((e = make_map_a(&mA, v.base, v.H, 2 * v.I, v.E, (uint64_t)v.ld_gu, v.rec, tpi * kTileM)) != cudaSuccess) return e;
-    if ((e = make_map_b(&mB, g.xq, v.H, nparts * P, BN)) != cudaSuccess) return e;
     ga.mode = 1;
     ga.nkt = v.H / kTileK;
     ga.a_sf_off = v.off_sgu_mma;
     ga.bscale = g.xs;
-    {
-        TraceScope trace_scope("gemm_gateup", stream);
-        ga.nmt = v.nmt_gu;
-        grouped_gemm_kernel<<<std::min(g_sms, nexp * ((ga.nmt + tpi - 1) / tpi)), kGemmThreads, smem, stream>>>(mA, mB,
-                                                                                                            ga);
-    }
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    ga.nmt = v.nmt_gu;
+    e = launch_one(ga, v.base, v.H, 2 * v.I, (uint64_t)v.ld_gu, v.E, g.xq, v.H, nparts * P, nexp, "gemm_gateup", stream);
+    if (e != cudaSuccess) return e;
 
     // GEMM 2: down
-    if ((e = make_map_a(&mA, v.base + v.off_d, v.Ip, v.H, v.E, (uint64_t)v.ld_d, v.rec, tpi * kTileM)) != cudaSuccess)
-        return e;
-    if ((e = make_map_b(&mB, g.hq, v.I, nparts * P, BN)) != cudaSuccess) return e;
     ga.mode = 2;
     ga.nkt = v.Ip / kTileK;
     ga.a_sf_off = v.off_sd_mma;
     ga.bscale = g.hs;
-    {
-        TraceScope trace_scope("gemm_down", stream);
-        ga.nmt = v.nmt_d;
-        grouped_gemm_kernel<<<std::min(g_sms, nexp * ((ga.nmt + tpi - 1) / tpi)), kGemmThreads, smem, stream>>>(mA, mB,
-                                                                                                            ga);
-    }
-    return cudaGetLastError();
+    ga.nmt = v.nmt_d;
+    return launch_one(ga, v.base + v.off_d, v.Ip, v.H, (uint64_t)v.ld_d, v.E, g.hq, v.I, nparts * P, nexp, "gemm_down",
+                      stream);
 }
 
 }  // namespace moe
