@@ -13,15 +13,17 @@ constexpr int kMaxBN = 192;      // accumulator columns of a grouped-GEMM tile
 
 // Accumulator columns per tile (BN) of the grouped GEMMs for P pairs over E experts,
 // T rows, nparts activation rows per pair; 0 when the shape is not supported.
-// nparts = 1: about twice the mean rows per expert, 32..192.  nparts = 3: all of an
-// expert's rows (at most 3T) in one tile, in whole groups of 16 pairs.
+// nparts = 1: 1.5 times the mean rows per expert rounded up to 32, 32..192 (an expert
+// with more rows takes several tiles; narrow tiles let the GEMMs run two CTAs per SM).
+// nparts = 3: all of an expert's rows (at most 3T) in one tile, in whole groups of 16
+// pairs.
 __host__ __device__ inline int grouped_bn(int P, int E, int T, int nparts) {
     if (nparts == 3) {
         const int bn = (3 * T + 47) / 48 * 48;
         return bn > kMaxBN ? 0 : bn;
     }
     const int mean = (P + E - 1) / E;
-    int bn = (2 * mean + 16 + 31) / 32 * 32;
+    int bn = (3 * mean / 2 + 31) / 32 * 32;
     return bn < 32 ? 32 : (bn > kMaxBN ? kMaxBN : bn);
 }
 
