@@ -213,3 +213,31 @@ def test_prefill_fewer_pairs_than_experts(T):
     assert np.array_equal(out["perm"].cpu().numpy(), ref["perm"])
     assert np.array_equal(out["offsets"].cpu().numpy(), ref["offsets"])
     check_close(bf16_to_f64(y), ref["y"], "y", amb=ref["y_amb"])
+
+
+@pytest.mark.parametrize("E,H,I,k,T", [(16, 256, 128, 4, 64), (64, 1024, 512, 16, 96)])
+def test_prefill_hot_expert_spans_column_tiles(E, H, I, k, T):
+    """Planted routing: every token sends slot 0 to expert 0, so that expert has T rows
+    while the tiles are sized for the mean (2 or 3 column tiles on the two-CTAs-per-SM
+    shape); each pair's output must match the oracle's."""
+    s = synth.Shape(E=E, H=H, I=I, k=k)
+    seed = 860 + E
+    pool = moe.Pool(E, H, I)
+    moe.moe_pool_fill_synthetic(pool, seed)
+    xb = synth.tokens_bf16(seed + 2, 0, T, H)
+    rng = np.random.default_rng(seed)
+    idx_h = np.stack([np.concatenate([[0], 1 + rng.choice(E - 1, k - 1, replace=False)]) for _ in range(T)])
+    idx = torch.from_numpy(idx_h.astype(np.int32)).cuda()
+    x = to_dev_bf16(xb)
+    ws = moe.workspace(moe.moe_workspace_size(moe.MOE_OP_GROUPED, E, H, I, T, k))
+    out = moe.moe_expert_forward_grouped(pool, x, idx, ws=ws)
+    assert moe.moe_check_status(ws) == moe.MOE_OK
+    perm, inv, offsets = oracle.sort_pairs(idx_h, E)
+    assert np.array_equal(out["perm"].cpu().numpy(), perm)
+    assert offsets[1] - offsets[0] == T
+    opool = oracle.SyntheticPool(seed, E, H, I)
+    xq = oracle.quant_rows_mxfp8(synth.bf16_bits_to_f64(xb))
+    o_ref = oracle.pair_outputs(opool, H, I, xq, idx_h, h_mode=1)
+    amb = oracle.pair_ambiguity(opool, H, I, xq, idx_h)
+    part = out["partial"].float().cpu().numpy().astype(np.float64)[out["inv_perm"].cpu().numpy()]
+    check_close(part.reshape(T, k, H), o_ref, "partial", amb=amb)
