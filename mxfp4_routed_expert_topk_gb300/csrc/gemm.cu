@@ -9,18 +9,19 @@
 //   GEMM 2 (down):    A = W_d (H rows, K = I, zero padded to 128), B = MXFP8 h rows;
 //            epilogue writes the unweighted expert output rows (fp32 or bf16)
 //
-// Persistent: one CTA per SM walks the (expert with pairs, 128-row tile of A) items
-// with a stride of the grid, with as many pipeline stages as shared memory holds
-// (the stream of K steps runs on across items).  8 warps: warp 0 issues a stage's
-// four copies (the tensor copies of A and B, and one bulk copy each of their scale
-// factors, which both operands keep in memory already in the 32x16-byte layout
-// tcgen05.cp expects: the pool's tensor-core scale planes and the tile-ordered
-// activation scales), warp 2 owns TMEM and issues the MMAs into one of two
-// accumulators, and warps 4-7 run the epilogue of the other accumulator (warp 4+w
-// reads TMEM lanes 32w..32w+31), so a tile's epilogue overlaps the next tile's MMAs.  With three-part activations (nparts = 3, the
-// multi-token decode) each sorted pair has three B rows whose columns the
-// epilogue sums.  Every wait is bounded (MOE_ERR_TIMEOUT), and nothing exits with
-// copies or MMAs in flight.
+// Persistent: CTAs walk the (expert with pairs, row tiles of A) items with a stride of
+// the grid, with as many pipeline stages as their share of shared memory holds (the
+// stream of K steps runs on across items).  Warp 0 issues a stage's four copies (the
+// tensor copies of A and B, and one bulk copy each of their scale factors, which both
+// operands keep in memory already in the 32x16-byte layout tcgen05.cp expects: the
+// pool's tensor-core scale planes and the tile-ordered activation scales); warp 1 owns
+// TMEM and issues the scale copies and MMAs into one of two accumulators; the epilogue
+// warps drain the other accumulator, so a tile's epilogue overlaps the next tile's
+// MMAs.  Two shapes (GemmShape): one CTA of 12 warps per SM (two epilogue warpgroups)
+// or two CTAs of 6 warps per SM (one), chosen per launch by the tile width.  With
+// three-part activations (nparts = 3, the multi-token decode) each sorted pair has
+// three B rows whose columns the epilogue sums.  Every wait is bounded
+// (MOE_ERR_TIMEOUT), and nothing exits with copies or MMAs in flight.
 #include <algorithm>
 
 #include <cuda.h>
