@@ -1,8 +1,11 @@
 // Decode / verify path: 1..32 rows, memory-bound.
 //
-// Each distinct expert selected by the rows is read from the pool once (the
+// One row runs the fused cooperative kernel (decode_fused.cu).  Several rows (the
 // verify batch of the four-SSD page, "可选的 Qwen 扩展": one forward pass checks
-// several rows) and its packed 4-bit weights are dequantised in registers:
+// several rows) run on the tensor cores through the grouped GEMMs with three-part
+// E4M3 activations (launch_decode_multi in prefill.cu) when I is a multiple of 64;
+// otherwise the kernels below read each distinct selected expert from the pool once
+// and dequantise its packed 4-bit weights in registers:
 //   decode_prep_kernel    union of selected experts, per-expert row lists,
 //                         bf16 rows -> f16 with a per-row power-of-two scale
 //   decode_gateup_kernel  g = W_g x, u = W_u x, h = silu(g) * u       (fp32 out)

@@ -4,10 +4,13 @@
 //   sort_rank_kernel / sort_scan_kernel / sort_scatter_kernel
 //        stable counting sort of the pairs p = t*k + j by expert (bit-exact perm)
 //   gather_quant_kernel
-//        rows of x in sorted order, quantised to MXFP8 (E4M3 + E8M0 per 32)
+//        rows of x in sorted order, quantised to MXFP8 (E4M3 + E8M0 per 32), the
+//        scales written in the tile order of the GEMMs
 //   grouped GEMMs (tcgen05, block-scaled)               -- gemm.cu
 //   combine_kernel
 //        y[t] = sum_j w[t,j] partial[inv_perm[t*k+j]] (+ residual), slot order
+// The multi-token decode (launch_decode_multi) uses the same pieces with a one-CTA
+// sort (sort_small_kernel) and three-part activations (gather_split3_kernel).
 #include "moe_internal.cuh"
 #include "prefill_internal.cuh"
 
