@@ -164,6 +164,12 @@ __device__ __forceinline__ void tc_cp_sf(uint32_t taddr, uint64_t sdesc) {
     asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
 }
 
+// 128 lanes x 32 bytes (8 columns) from shared memory: the two interleaved scale atoms
+// of a 256-column B tile, already replicated per lane quadrant in shared memory.
+__device__ __forceinline__ void tc_cp_sf2(uint32_t taddr, uint64_t sdesc) {
+    asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
 __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t sfa,
                                        uint32_t sfb, uint32_t accumulate) {
     asm volatile(
@@ -356,8 +362,8 @@ struct GemmSmemLayout {
         a = 0;                                            // ns x tpi x 16 KB (1024-aligned)
         b = a + (uint32_t)(ns * tpi) * kTileM * kTileK;   // ns x BN*128
         sfa = b + (uint32_t)ns * (uint32_t)BN * kTileK;   // ns x tpi x 512
-        sfb = sfa + (uint32_t)(ns * tpi) * 512;           // ns x nsfb*512
-        bars = sfb + (uint32_t)ns * 512 * nsfb;           // full[], empty[], acc_full[2], acc_empty[2]
+        sfb = sfa + (uint32_t)(ns * tpi) * 512;           // ns x sfb_stage_bytes(nsfb)
+        bars = sfb + (uint32_t)ns * sfb_stage_bytes((int)nsfb);  // full[], empty[], acc_full[2], acc_empty[2]
         misc = bars + (2 * kMaxStages + 4) * 8;           // tmem addr, abort, amax[4][16]
         total = misc + 16 + kEpiWarps * 16 * 4;
     }
@@ -429,7 +435,7 @@ __global__ void __launch_bounds__(NT, GemmShape<NT>::kCtasPerSm)
     using Shape = GemmShape<NT>;
     for (int i = threadIdx.x; i < ns * tpi * kTileM * kTileK / 16; i += NT)
         reinterpret_cast<uint4 *>(sA)[i] = make_uint4(0u, 0u, 0u, 0u);
-    for (int i = threadIdx.x; i < ns * (tpi + nsfb) * 512 / 16; i += NT)
+    for (int i = threadIdx.x; i < ns * (tpi * 512 + (int)sfb_stage_bytes(nsfb)) / 16; i += NT)
         reinterpret_cast<uint4 *>(sSFA)[i] = make_uint4(0u, 0u, 0u, 0u);  // sSFB follows sSFA
     fence_proxy_async_smem();
     if (threadIdx.x == 0) {
@@ -477,7 +483,8 @@ __global__ void __launch_bounds__(NT, GemmShape<NT>::kCtasPerSm)
                 // scale factors: the item's row tiles of A (adjacent in the plane) and
                 // the column tile's atoms of B, each one contiguous block
                 const uint32_t a_tiles = (uint32_t)min(tpi, a.nmt - J.mt);
-                const uint32_t tx = (uint32_t)(tpi * kTileM * kTileK / 2 + a.BN * kTileK) + (a_tiles + (uint32_t)nsfb) * 512u;
+                const uint32_t tx =
+                    (uint32_t)(tpi * kTileM * kTileK / 2 + a.BN * kTileK) + a_tiles * 512u + sfb_stage_bytes(nsfb);
                 const uint8_t *sfa_src = a.pool + (uint64_t)J.e * a.rec + a.a_sf_off + ((uint64_t)kt * a.nmt + J.mt) * 512;
                 const uint8_t *sfb_src = a.bscale + sf_tile_word(J.tile(), a.nkt, nsfb, kt, 0);
                 const int brow = J.row0 + J.n0();
@@ -486,7 +493,12 @@ __global__ void __launch_bounds__(NT, GemmShape<NT>::kCtasPerSm)
                     tma_load_3d(sA + (size_t)s * tpi * kTileM * kTileK, &tmA, kt * kTileK, J.mt * kTileM, J.e, &full[s]);
                     tma_load_2d(sB + (size_t)s * a.BN * kTileK, &tmB, kt * kTileK, brow, &full[s]);
                     bulk_g2s_l2(sSFA + (size_t)s * tpi * 512, sfa_src, a_tiles * 512u, &full[s]);
-                    bulk_g2s_l2(sSFB + (size_t)s * nsfb * 512, sfb_src, (uint32_t)nsfb * 512u, &full[s]);
+                    if (nsfb == 1) {
+                        bulk_g2s_l2(sSFB + (size_t)s * 512, sfb_src, 512u, &full[s]);
+                    } else {
+                        // the interleaved 1 KB block once per TMEM lane quadrant
+                        for (int q = 0; q < 4; q++) bulk_g2s_l2(sSFB + (size_t)s * 4096 + q * 1024, sfb_src, 1024u, &full[s]);
+                    }
                 }
                 __syncwarp();
                 it_issued = it + 1;
@@ -527,14 +539,17 @@ __global__ void __launch_bounds__(NT, GemmShape<NT>::kCtasPerSm)
                 const uint32_t sfa_t = tmem + sf_col0 + (uint32_t)s * sf_stage;  // + 4t for tile t
                 const uint32_t sfb_t = sfa_t + 4u * (uint32_t)tpi;
                 const uint32_t sfa_s = smem_u32(sSFA + (size_t)s * tpi * 512);
-                const uint32_t sfb_s = smem_u32(sSFB + (size_t)s * nsfb * 512);
+                const uint32_t sfb_s = smem_u32(sSFB + (size_t)s * sfb_stage_bytes(nsfb));
                 const uint32_t a_base = smem_u32(sA + (size_t)s * tpi * kTileM * kTileK);
                 const uint32_t b_base = smem_u32(sB + (size_t)s * a.BN * kTileK);
                 if (elect_one()) {
                     for (int t = 0; t < tpi; t++)
                         tc_cp_sf(sfa_t + 4u * t, smem_desc(sfa_s + 512u * t, 128, 128, kSwizzleNone));
-                    for (int at = 0; at < nsfb; at++)
-                        tc_cp_sf(sfb_t + 4u * at, smem_desc(sfb_s + 512u * at, 128, 128, kSwizzleNone));
+                    if (nsfb == 1)
+                        tc_cp_sf(sfb_t, smem_desc(sfb_s, 128, 128, kSwizzleNone));
+                    else  // core matrices of 8 rows x 16 bytes: the two 16-byte halves 128 bytes
+                          // apart, row groups 256 bytes apart
+                        tc_cp_sf2(sfb_t, smem_desc(sfb_s, 128, 256, kSwizzleNone));
                     for (int t = 0; t < tpi; t++) {
                         // tile t: rows 128t.. of the stage's A (16 KB apart), accumulator columns t*BN..
 #pragma unroll

@@ -29,16 +29,25 @@ __host__ __device__ inline int grouped_bn(int P, int E, int T, int nparts) {
 
 // Scale factors of the activation operand (B) in the layout the MMA consumes, one
 // block per (expert, column tile): tile T_e + t of expert e (T_e = tile_off[e]) holds,
-// for each K tile kt of 128 elements, nsfb = ceil(BN / 128) atoms of 512 bytes; column
-// c of the tile (activation row nparts * offsets[e] + t * BN + c) keeps the 4 scale
-// bytes of its K tile at byte (c / 128) * 512 + (c % 32) * 16 + ((c / 32) % 4) * 4 of
-// the atoms (the 32 x 16-byte layout tcgen05.cp copies into TMEM), scale block 4kt+j
-// at byte j of the word.  Bytes of columns past the tile's rows are never read by a
-// result that is kept.  Byte offset of the word of (tile, kt, c):
+// for each K tile kt of 128 elements, nsfb = ceil(BN / 128) atoms of 512 bytes.  Column
+// c of the tile (activation row nparts * offsets[e] + t * BN + c) belongs to atom c / 128
+// and keeps the 4 scale bytes of its K tile (scale block 4kt+j at byte j of the word)
+// in row c % 32 of the atom (16 bytes, word (c / 32) % 4): the 32 x 16-byte layout that
+// tcgen05.cp copies into TMEM.  With two atoms, their rows are interleaved by groups of
+// 8 (row group g of atom a at byte g * 256 + a * 128), so that the 1 KB block is one
+// lane quadrant of the 128 x 32-byte matrix a single 128x256b tcgen05.cp takes (in the
+// core-matrix order of its descriptor); with one atom this is the plain atom.  Bytes of
+// columns past the tile's rows are never read by a result that is kept.  Byte offset of
+// the word of (tile, kt, c):
 __host__ __device__ inline size_t sf_tile_word(int tile, int nkt, int nsfb, int kt, int c) {
-    return ((size_t)tile * nkt + kt) * (size_t)nsfb * 512 + (size_t)(c >> 7) * 512 + (size_t)(c & 31) * 16 +
-           (size_t)((c >> 5) & 3) * 4;
+    return ((size_t)tile * nkt + kt) * (size_t)nsfb * 512 + (size_t)((c & 31) >> 3) * (size_t)nsfb * 128 +
+           (size_t)(c >> 7) * 128 + (size_t)(c & 7) * 16 + (size_t)((c >> 5) & 3) * 4;
 }
+
+// Bytes of B's scale factors in one pipeline stage in shared memory: the atom, or for
+// two atoms the interleaved 1 KB block four times over (one copy per TMEM lane
+// quadrant, the replication the MMA's scale layout needs).
+__host__ __device__ inline uint32_t sfb_stage_bytes(int nsfb) { return nsfb == 1 ? 512u : 4096u; }
 
 // Activation rows of the grouped GEMMs.  nparts = 1: one MXFP8 row per pair (OCP
 // rule, the prefill path).  nparts = 3: the value is the sum of three E4M3 parts
