@@ -333,3 +333,13 @@ def test_stacked_layers_oracle_forced(tiny):
         y = moe.moe_expert_forward_decode(gpools[l], xh, idx, w, residual=x)
         # the layer output is x + MoE(x_hat); compare it whole (bf16-rounded on the GPU)
         check_close(bf16_to_f64(y), synth.bf16_bits_to_f64(ly["x"]) + ly["y"])
+
+
+@pytest.mark.parametrize("E,H,M,k", [(100, 512, 70, 8), (1100, 256, 64, 16), (33, 384, 65, 4)])
+def test_route_tiled_ragged_shapes(E, H, M, k):
+    """The many-token logit kernel with expert counts that leave a partial 64-expert tile
+    (and, for E > 1024, the selection with 8 keys per thread), bit-exact indices."""
+    rng = np.random.default_rng(E + H + M)
+    Wrb = synth.bf16_bits_from_f64(rng.standard_normal((E, H)) / np.sqrt(H))
+    xb = synth.bf16_bits_from_f64(rng.standard_normal((M, H)))
+    _route_check(xb, Wrb, to_dev_bf16(Wrb), k)
