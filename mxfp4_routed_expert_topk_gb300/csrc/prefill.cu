@@ -18,6 +18,7 @@ namespace moe {
 namespace {
 
 constexpr int kSortBlock = 1024;  // pairs per block of the counting sort
+constexpr int kGatherChunk = 1024; // elements of a token row per gather warp (a multiple of 256)
 
 // Block b: local rank of each of its pairs among the block's pairs of the same
 // expert (in pair order), and the block's per-expert counts cnt[b][e].
@@ -205,29 +206,40 @@ __device__ __forceinline__ void zero_h_pad(uint8_t *hs, int I, int nsfb, RowTile
         *reinterpret_cast<uint32_t *>(hs + sf_tile_word(rt.tile, ip / 128, nsfb, ip / 128 - 1, rt.col)) = 0u;
 }
 
-// Sorted row r (one warp per row): Xs[r] = MXFP8(x[perm[r] / k]).  Shared exponent
-// X = floor(log2 amax) - 8 per 32-block (clamped to [-127, 127]); codes are
+// Token t, a chunk of kGatherChunk elements per warp: MXFP8(x[t]) once, written to the
+// sorted row of each of its k pairs (inv_perm; a pair whose expert index was invalid
+// has none).  Shared
+// exponent X = floor(log2 amax) - 8 per 32-block (clamped to [-127, 127]); codes are
 // RNE(x / 2^X) to E4M3 with saturation.  x / 2^X is exact for bf16 input.  Each lane
-// takes 8 consecutive elements (a 32-block is 4 lanes, a 128-element K tile 16), so
-// a warp step covers 256 elements; scales go to the tile-ordered blocks, one 4-byte
-// word per K tile.  Rows at or past offsets[E] (there are such rows only when a slot
-// held an invalid expert index) are left alone.
-__global__ void gather_quant_kernel(const uint16_t *__restrict__ x, int H, int I, int k, int E,
-                                    const int32_t *__restrict__ idx, const int32_t *__restrict__ perm,
+// takes 8 consecutive elements (a 32-block is 4 lanes, a 128-element K tile 16), so a
+// warp step covers 256 elements; scales go to the tile-ordered blocks, one 4-byte word
+// per K tile.
+__global__ void gather_quant_kernel(const uint16_t *__restrict__ x, int T, int H, int I, int k,
+                                    const int32_t *__restrict__ idx, const int32_t *__restrict__ inv_perm,
                                     const int32_t *__restrict__ offsets, const int32_t *__restrict__ tile_off, int BN,
                                     int nsfb, uint8_t *__restrict__ xq, uint8_t *__restrict__ xs,
                                     uint8_t *__restrict__ hs) {
     const int lane = threadIdx.x & 31;
-    const int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    if (r >= offsets[E]) return;
-    const int p = perm[r];
-    const int t = p / k, e = idx[p];
-    const RowTile rt = row_tile(e, r - offsets[e], tile_off, BN);
+    const int nchunk = (H + kGatherChunk - 1) / kGatherChunk;
+    const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int t = gw / nchunk, chunk = gw % nchunk;
+    if (t >= T) return;
+    // lane j < k: slot j's sorted row and its place in the tile-ordered scales
+    int myrow = -1;
+    RowTile myrt{0, 0};
+    if (lane < k) {
+        const int p = t * k + lane;
+        myrow = inv_perm[p];
+        if (myrow >= 0) {
+            const int e = idx[p];
+            myrt = row_tile(e, myrow - offsets[e], tile_off, BN);
+        }
+    }
     const uint16_t *xr = x + (size_t)t * H;
-    uint8_t *qr = xq + (size_t)r * H;
-    for (int b0 = 0; b0 < H; b0 += 256) {
+    const int b_end = min(H, (chunk + 1) * kGatherChunk);
+    for (int b0 = chunk * kGatherChunk; b0 < b_end; b0 += 256) {
         // H is a multiple of 128: the upper half-warp may have nothing in the last step
-        const bool on = b0 + lane * 8 < H;
+        const bool on = b0 + lane * 8 < b_end;
         float f[8];
         if (on) {
             const uint4 v = *reinterpret_cast<const uint4 *>(xr + b0 + lane * 8);
@@ -261,19 +273,26 @@ __global__ void gather_quant_kernel(const uint16_t *__restrict__ x, int H, int I
                 : "f"(ldexpf(f[2 * i + 1], -X)), "f"(ldexpf(f[2 * i], -X)));
             q[i >> 1] |= (uint32_t)pair << (16 * (i & 1));
         }
-        if (on) *reinterpret_cast<uint2 *>(qr + b0 + lane * 8) = make_uint2(q[0], q[1]);
         // scale word of each K tile: the bytes of lanes 16h, 16h+4, 16h+8, 16h+12
         const uint32_t sb = (uint32_t)(X + 127);
         const uint32_t b1 = __shfl_down_sync(0xffffffffu, sb, 4);
         const uint32_t b2 = __shfl_down_sync(0xffffffffu, sb, 8);
         const uint32_t b3 = __shfl_down_sync(0xffffffffu, sb, 12);
-        if ((lane & 15) == 0 && on) {
-            const int kt = (b0 + lane * 8) >> 7;
-            *reinterpret_cast<uint32_t *>(xs + sf_tile_word(rt.tile, H / 128, nsfb, kt, rt.col)) =
-                sb | (b1 << 8) | (b2 << 16) | (b3 << 24);
+        const uint32_t word = sb | (b1 << 8) | (b2 << 16) | (b3 << 24);
+        const int kt = (b0 + lane * 8) >> 7;
+        for (int j = 0; j < k; j++) {
+            const int r = __shfl_sync(0xffffffffu, myrow, j);
+            if (r < 0) continue;  // warp-uniform
+            const int tile = __shfl_sync(0xffffffffu, myrt.tile, j);
+            const int col = __shfl_sync(0xffffffffu, myrt.col, j);
+            if (on) {
+                *reinterpret_cast<uint2 *>(xq + (size_t)r * H + b0 + lane * 8) = make_uint2(q[0], q[1]);
+                if ((lane & 15) == 0)
+                    *reinterpret_cast<uint32_t *>(xs + sf_tile_word(tile, H / 128, nsfb, kt, col)) = word;
+            }
         }
     }
-    if (lane == 0) zero_h_pad(hs, I, nsfb, rt);
+    if (chunk == 0 && myrow >= 0) zero_h_pad(hs, I, nsfb, myrt);
 }
 
 // Row r of the sorted pairs: x[perm[r] / k] as three E4M3 parts (rows 3r, 3r+1,
@@ -390,8 +409,9 @@ cudaError_t launch_grouped(const PoolView &v, const uint16_t *x, int T, const in
     }
     {
         TraceScope trace_scope("gather_quant", st);
-        gather_quant_kernel<<<(P * 32 + 255) / 256, 256, 0, st>>>(x, v.H, v.I, k, v.E, idx, perm, offsets, g.tile_off,
-                                                                  g.BN, g.nsfb, g.xq, g.xs, g.hs);
+        const int nchunk = (v.H + kGatherChunk - 1) / kGatherChunk;
+        gather_quant_kernel<<<(unsigned)(((size_t)T * nchunk * 32 + 255) / 256), 256, 0, st>>>(
+            x, T, v.H, v.I, k, idx, inv_perm, offsets, g.tile_off, g.BN, g.nsfb, g.xq, g.xs, g.hs);
     }
     cudaError_t e = launch_grouped_gemms(v, T, k, offsets, g, partial, partial_dtype, stw, st);
     if (e != cudaSuccess) return e;
