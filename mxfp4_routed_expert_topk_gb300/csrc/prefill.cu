@@ -375,6 +375,74 @@ __global__ void combine_kernel(const PT *__restrict__ partial, const int32_t *__
     }
 }
 
+// Four consecutive partial elements as fp32 (16-byte or 8-byte loads).
+__device__ __forceinline__ void load_partial4(const float *p, float (&v)[4]) {
+    const float4 q = *reinterpret_cast<const float4 *>(p);
+    v[0] = q.x;
+    v[1] = q.y;
+    v[2] = q.z;
+    v[3] = q.w;
+}
+__device__ __forceinline__ void load_partial4(const __nv_bfloat16 *p, float (&v)[4]) {
+    const uint2 q = *reinterpret_cast<const uint2 *>(p);
+    v[0] = __uint_as_float(q.x << 16);
+    v[1] = __uint_as_float(q.x & 0xffff0000u);
+    v[2] = __uint_as_float(q.y << 16);
+    v[3] = __uint_as_float(q.y & 0xffff0000u);
+}
+
+// combine_kernel with four consecutive outputs per thread (H a multiple of 4, rows
+// 16-byte aligned): the same slot-order fp32 sums, so the same bits.
+template <typename PT>
+__global__ void combine4_kernel(const PT *__restrict__ partial, const int32_t *__restrict__ inv_perm,
+                                const float *__restrict__ w, int k, int H, const uint16_t *__restrict__ residual,
+                                uint16_t *__restrict__ y, int chunk) {
+    __shared__ int rows[kMaxK];
+    __shared__ float ws[kMaxK];
+    const int t = blockIdx.x;
+    const int o_lo = blockIdx.y * chunk, o_hi = min(H, o_lo + chunk);
+    if (threadIdx.x < k) {
+        rows[threadIdx.x] = inv_perm[(size_t)t * k + threadIdx.x];
+        ws[threadIdx.x] = w[(size_t)t * k + threadIdx.x];
+    }
+    __syncthreads();
+    for (int o = o_lo + 4 * threadIdx.x; o < o_hi; o += 4 * blockDim.x) {
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int j = 0; j < k; j++) {
+            const int r = rows[j];
+            if (r >= 0) {
+                float v[4];
+                load_partial4(partial + (size_t)r * H + o, v);
+#pragma unroll
+                for (int i = 0; i < 4; i++) acc[i] = fmaf(ws[j], v[i], acc[i]);
+            }
+        }
+        if (residual != nullptr) {
+            const uint2 rv = *reinterpret_cast<const uint2 *>(residual + (size_t)t * H + o);
+            acc[0] += __uint_as_float(rv.x << 16);
+            acc[1] += __uint_as_float(rv.x & 0xffff0000u);
+            acc[2] += __uint_as_float(rv.y << 16);
+            acc[3] += __uint_as_float(rv.y & 0xffff0000u);
+        }
+        uint16_t b[4];
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            const __nv_bfloat16 bv = __float2bfloat16_rn(acc[i]);
+            b[i] = *reinterpret_cast<const uint16_t *>(&bv);
+        }
+        *reinterpret_cast<uint2 *>(y + (size_t)t * H + o) =
+            make_uint2((uint32_t)b[0] | ((uint32_t)b[1] << 16), (uint32_t)b[2] | ((uint32_t)b[3] << 16));
+    }
+}
+
+// The four-wide combine's loads and stores are aligned: H % 4 == 0 and the row bases
+// aligned to a whole vector.
+bool combine4_ok(const void *partial, int partial_dtype, int H, const uint16_t *residual, const uint16_t *y) {
+    const size_t pv = partial_dtype == MOE_PARTIAL_F32 ? 16 : 8;
+    return H % 4 == 0 && (uintptr_t)partial % pv == 0 && (uintptr_t)y % 8 == 0 &&
+           (residual == nullptr || (uintptr_t)residual % 8 == 0);
+}
+
 }  // namespace
 
 size_t grouped_workspace_bytes(int E, int H, int I, int T, int k) {
@@ -445,9 +513,10 @@ cudaError_t launch_decode_multi(const PoolView &v, const uint16_t *x, int M, con
     if (e != cudaSuccess) return e;
     {
         TraceScope trace_scope("combine", st);
-        const int chunk = 256;  // few rows: one output per thread, (row, chunk) grid
-        combine_kernel<float><<<dim3(M, (v.H + chunk - 1) / chunk), 256, 0, st>>>(d.partial, d.inv_perm, w, k, v.H,
-                                                                                   residual, y, chunk);
+        // few rows: a (row, 256-element chunk) grid, one output per thread (more warps in
+        // flight than four outputs per thread, which is faster at this size)
+        combine_kernel<float><<<dim3(M, (v.H + 255) / 256), 256, 0, st>>>(d.partial, d.inv_perm, w, k, v.H, residual, y,
+                                                                         256);
     }
     return cudaGetLastError();
 }
@@ -456,14 +525,26 @@ cudaError_t launch_combine(const void *partial, int partial_dtype, const int32_t
                            int H, const uint16_t *residual, uint16_t *y, cudaStream_t st) {
     if (T == 0) return cudaSuccess;
     TraceScope trace_scope("combine", st);
-    // one CTA per row over all of H, or (row, chunk) CTAs when there are few rows
+    // one CTA per row over all of H, four outputs per thread when the rows are aligned
+    // for it; or, when there are few rows, (row, 256-element chunk) CTAs with one output
+    // per thread (more warps in flight)
+    const bool v4 = T >= 152 && combine4_ok(partial, partial_dtype, H, residual, y);
     const int chunk = T < 152 ? 256 : H;
     const dim3 grid(T, (H + chunk - 1) / chunk);
-    if (partial_dtype == MOE_PARTIAL_F32)
-        combine_kernel<float><<<grid, 256, 0, st>>>((const float *)partial, inv_perm, w, k, H, residual, y, chunk);
-    else
-        combine_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>((const __nv_bfloat16 *)partial, inv_perm, w, k, H, residual,
-                                                            y, chunk);
+    const int nthr = 256;
+    if (partial_dtype == MOE_PARTIAL_F32) {
+        if (v4)
+            combine4_kernel<float><<<grid, nthr, 0, st>>>((const float *)partial, inv_perm, w, k, H, residual, y, chunk);
+        else
+            combine_kernel<float><<<grid, 256, 0, st>>>((const float *)partial, inv_perm, w, k, H, residual, y, chunk);
+    } else {
+        if (v4)
+            combine4_kernel<__nv_bfloat16><<<grid, nthr, 0, st>>>((const __nv_bfloat16 *)partial, inv_perm, w, k, H,
+                                                                 residual, y, chunk);
+        else
+            combine_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>((const __nv_bfloat16 *)partial, inv_perm, w, k, H,
+                                                                residual, y, chunk);
+    }
     return cudaGetLastError();
 }
 
