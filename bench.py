@@ -474,7 +474,8 @@ def run_ours(args):
 def run_profile_case(args):
     """A small case of the same kernels for ncu captures: full H and I, a 64-expert
     pool (1.2 GB, larger than L2); a few single-token calls (decode) or one
-    64-token expert-major call (prefill)."""
+    expert-major call of --profile-tokens tokens (prefill; 585 tokens give the 146
+    rows per expert of 8192 tokens over 896 experts)."""
     import torch
     import mxfp4_routed_expert_topk_gb300 as moe
     moe.build()
@@ -495,7 +496,7 @@ def run_profile_case(args):
     moe.moe_pool_fill_synthetic(pool, synth.pool_seed(0))
     Wr = torch.from_numpy(synth.router_bf16(synth.router_seed(0), s.E, s.H).view(np.int16)).cuda().view(torch.bfloat16)
     if args.profile == "prefill":
-        xb = synth.tokens_bf16(synth.TOKENS_SEED["prefill"], 0, 64, s.H)
+        xb = synth.tokens_bf16(synth.TOKENS_SEED["prefill"], 0, args.profile_tokens, s.H)
         x = torch.from_numpy(xb.view(np.int16)).cuda().view(torch.bfloat16)
         for _ in range(2):
             idx, w = moe.moe_route_topk(x, Wr, s.k)
@@ -526,6 +527,8 @@ def main():
                     help="skip the multi-token verify and 8-layer stacked measurements")
     ap.add_argument("--profile", choices=["decode", "prefill", "route"], default=None,
                     help="run a small case of the kernels for an ncu capture (no JSON line)")
+    ap.add_argument("--profile-tokens", type=int, default=64,
+                    help="tokens of the prefill profile case (64-expert pool)")
     args = ap.parse_args()
     if args.profile:
         run_profile_case(args)

@@ -363,8 +363,8 @@ struct GemmSmemLayout {
         b = a + (uint32_t)(ns * tpi) * kTileM * kTileK;   // ns x BN*128
         sfa = b + (uint32_t)ns * (uint32_t)BN * kTileK;   // ns x tpi x 512
         sfb = sfa + (uint32_t)(ns * tpi) * 512;           // ns x sfb_stage_bytes(nsfb)
-        bars = sfb + (uint32_t)ns * sfb_stage_bytes((int)nsfb);  // full[], empty[], acc_full[2], acc_empty[2]
-        misc = bars + (2 * kMaxStages + 4) * 8;           // tmem addr, abort, amax[4][16]
+        bars = sfb + (uint32_t)ns * sfb_stage_bytes((int)nsfb);  // full[], empty[], acc_full[2], acc_empty[2], mma_done
+        misc = bars + (2 * kMaxStages + 5) * 8;           // tmem addr, abort, amax[4][16]
         total = misc + 16 + kEpiWarps * 16 * 4;
     }
 };
@@ -419,6 +419,7 @@ __global__ void __launch_bounds__(NT, GemmShape<NT>::kCtasPerSm)
     uint64_t *empty = full + kMaxStages;
     uint64_t *acc_full = empty + kMaxStages;
     uint64_t *acc_empty = acc_full + 2;
+    uint64_t *mma_done = acc_empty + 2;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L.misc);
     int *abort_flag = reinterpret_cast<int *>(smem + L.misc + 4);
     float *amax_x = reinterpret_cast<float *>(smem + L.misc + 16);  // [8 epilogue warps][16 columns]
@@ -447,6 +448,7 @@ __global__ void __launch_bounds__(NT, GemmShape<NT>::kCtasPerSm)
             mbar_init(&acc_full[b], 1);   // MMA commit after a tile's last K step
             mbar_init(&acc_empty[b], Shape::kEpiWarps);  // the epilogue warps
         }
+        mbar_init(mma_done, 1);  // the MMA warp's last commit
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -470,7 +472,7 @@ __global__ void __launch_bounds__(NT, GemmShape<NT>::kCtasPerSm)
         for (JobIter J(a, nu); run && J.valid(); J.next()) {
             for (int kt = 0; kt < a.nkt; kt++, it++) {
                 int okl = 1;
-                if (lane == 0) okl = !*(volatile int *)abort_flag && mbar_wait(&empty[s], ph ^ 1u, a.st, 0x500u + s);
+                if (lane == 0) okl = mbar_wait_or_abort(&empty[s], ph ^ 1u, a.st, 0x500u + s, abort_flag);
                 if (!__shfl_sync(0xffffffffu, okl, 0)) {
                     if (lane == 0) *abort_flag = 1;
                     run = false;
@@ -510,68 +512,99 @@ __global__ void __launch_bounds__(NT, GemmShape<NT>::kCtasPerSm)
         }
     } else if (warp == 1) {
         // ------------------------------------------------------- MMA issue
+        // The issue of a stage is a chain of dependent steps (wait, broadcast, scale
+        // copies, MMAs, commit), so the warp first asks which of the next few stages
+        // have landed (lane i polls stage kt + i, one vote) and issues all of those in
+        // one go; the abort flag is read only while a stage is still outstanding.
         int jb = 0, s = 0;  // tiles; slot of the next stage
         uint32_t ph = 0;    // its phase parity
         bool run = true;
+        const uint32_t a_stage = (uint32_t)(tpi * kTileM * kTileK), b_stage = (uint32_t)(a.BN * kTileK);
+        const uint32_t sfb_bytes = sfb_stage_bytes(nsfb);
+        const uint32_t sA0 = smem_u32(sA), sB0 = smem_u32(sB), sSFA0 = smem_u32(sSFA), sSFB0 = smem_u32(sSFB);
+        const int nlook = min(4, ns);  // stages polled at once (never past the ring)
         for (JobIter J(a, nu); run && J.valid(); J.next(), jb++) {
             const int nmma = (J.nn() + 15) / 16 * 16;
             const int buf = jb & 1;
             // the epilogue has finished with this accumulator (two tiles ago)
             int okl = 1;
-            if (lane == 0)
-                okl = !*(volatile int *)abort_flag &&
-                      mbar_wait(&acc_empty[buf], ((uint32_t)(jb >> 1) & 1u) ^ 1u, a.st, 0x680u + buf);
+            if (lane == 0) okl = mbar_wait_or_abort(&acc_empty[buf], ((uint32_t)(jb >> 1) & 1u) ^ 1u, a.st, 0x680u + buf,
+                                                    abort_flag);
             if (!__shfl_sync(0xffffffffu, okl, 0)) {
                 if (lane == 0) *abort_flag = 1;
                 break;
             }
             tc_fence_after();
             const uint32_t acc = tmem + (uint32_t)(buf * tpi * a.BN);
-            for (int kt = 0; kt < a.nkt; kt++) {
-                okl = 1;
-                if (lane == 0) okl = !*(volatile int *)abort_flag && mbar_wait(&full[s], ph, a.st, 0x700u + s);
-                if (!__shfl_sync(0xffffffffu, okl, 0)) {
-                    if (lane == 0) *abort_flag = 1;
-                    run = false;
-                    break;
+            for (int kt = 0; kt < a.nkt;) {
+                // stages kt .. kt + r - 1 have landed
+                const int want = min(nlook, a.nkt - kt);
+                bool rl = false;
+                if (lane < want) {
+                    const int q = s + lane;
+                    rl = mbar_try_wait(&full[q % ns], ph ^ ((uint32_t)(q / ns) & 1u));
+                }
+                const uint32_t ready = __ballot_sync(0xffffffffu, rl);
+                int r = min(__ffs(~ready) - 1, want);
+                if (r == 0) {
+                    okl = 1;
+                    if (lane == 0) okl = mbar_wait_or_abort(&full[s], ph, a.st, 0x700u + s, abort_flag);
+                    if (!__shfl_sync(0xffffffffu, okl, 0)) {
+                        if (lane == 0) *abort_flag = 1;
+                        run = false;
+                        break;
+                    }
+                    r = 1;
                 }
                 tc_fence_after();
-                const uint32_t sfa_t = tmem + sf_col0 + (uint32_t)s * sf_stage;  // + 4t for tile t
-                const uint32_t sfb_t = sfa_t + 4u * (uint32_t)tpi;
-                const uint32_t sfa_s = smem_u32(sSFA + (size_t)s * tpi * 512);
-                const uint32_t sfb_s = smem_u32(sSFB + (size_t)s * sfb_stage_bytes(nsfb));
-                const uint32_t a_base = smem_u32(sA + (size_t)s * tpi * kTileM * kTileK);
-                const uint32_t b_base = smem_u32(sB + (size_t)s * a.BN * kTileK);
                 if (elect_one()) {
-                    for (int t = 0; t < tpi; t++)
-                        tc_cp_sf(sfa_t + 4u * t, smem_desc(sfa_s + 512u * t, 128, 128, kSwizzleNone));
-                    if (nsfb == 1)
-                        tc_cp_sf(sfb_t, smem_desc(sfb_s, 128, 128, kSwizzleNone));
-                    else  // core matrices of 8 rows x 16 bytes: the two 16-byte halves 128 bytes
-                          // apart, row groups 256 bytes apart
-                        tc_cp_sf2(sfb_t, smem_desc(sfb_s, 128, 256, kSwizzleNone));
-                    for (int t = 0; t < tpi; t++) {
-                        // tile t: rows 128t.. of the stage's A (16 KB apart), accumulator columns t*BN..
+                    int sq = s;
+                    for (int q = 0; q < r; q++) {
+                        const uint32_t sfa_t = tmem + sf_col0 + (uint32_t)sq * sf_stage;  // + 4t for tile t
+                        const uint32_t sfb_t = sfa_t + 4u * (uint32_t)tpi;
+                        const uint32_t sfa_s = sSFA0 + (uint32_t)sq * (uint32_t)tpi * 512u;
+                        const uint32_t sfb_s = sSFB0 + (uint32_t)sq * sfb_bytes;
+                        const uint32_t a_base = sA0 + (uint32_t)sq * a_stage;
+                        const uint32_t b_base = sB0 + (uint32_t)sq * b_stage;
+                        for (int t = 0; t < tpi; t++)
+                            tc_cp_sf(sfa_t + 4u * t, smem_desc(sfa_s + 512u * t, 128, 128, kSwizzleNone));
+                        if (nsfb == 1)
+                            tc_cp_sf(sfb_t, smem_desc(sfb_s, 128, 128, kSwizzleNone));
+                        else  // core matrices of 8 rows x 16 bytes: the two 16-byte halves 128 bytes
+                              // apart, row groups 256 bytes apart
+                            tc_cp_sf2(sfb_t, smem_desc(sfb_s, 128, 256, kSwizzleNone));
+                        for (int t = 0; t < tpi; t++) {
+                            // tile t: rows 128t.. of the stage's A (16 KB apart), accumulator columns t*BN..
 #pragma unroll
-                        for (int ks = 0; ks < kTileK / 32; ks++) {
-                            const uint64_t ad = smem_desc(a_base + (uint32_t)(t * kTileM * kTileK) + 32 * ks, 16, 1024,
-                                                          kSwizzle128B);
-                            const uint64_t bd = smem_desc(b_base + 32 * ks, 16, 1024, kSwizzle128B);
-                            tc_mma(acc + (uint32_t)(t * a.BN), ad, bd, idesc_mxf8f6f4(nmma, ks), sfa_t + 4u * t, sfb_t,
-                                   (kt > 0 || ks > 0) ? 1u : 0u);
+                            for (int ks = 0; ks < kTileK / 32; ks++) {
+                                const uint64_t ad = smem_desc(a_base + (uint32_t)(t * kTileM * kTileK) + 32 * ks, 16,
+                                                              1024, kSwizzle128B);
+                                const uint64_t bd = smem_desc(b_base + 32 * ks, 16, 1024, kSwizzle128B);
+                                tc_mma(acc + (uint32_t)(t * a.BN), ad, bd, idesc_mxf8f6f4(nmma, ks), sfa_t + 4u * t,
+                                       sfb_t, (kt + q > 0 || ks > 0) ? 1u : 0u);
+                            }
                         }
+                        tc_commit(&empty[sq]);  // frees the stage when these MMAs have read it
+                        if (++sq == ns) sq = 0;
                     }
-                    tc_commit(&empty[s]);  // frees the stage when these MMAs have read it
                 }
                 __syncwarp();
-                if (++s == ns) {
-                    s = 0;
+                kt += r;
+                s += r;
+                if (s >= ns) {
+                    s -= ns;
                     ph ^= 1u;
                 }
             }
             if (elect_one()) tc_commit(&acc_full[buf]);  // the accumulator is complete (or as far as it got)
             __syncwarp();
         }
+        // every MMA this warp issued has finished before TMEM can be released (also
+        // after an abort, when the epilogue may not wait for the last accumulator)
+        if (elect_one()) tc_commit(mma_done);
+        __syncwarp();
+        if (lane == 0) mbar_wait(mma_done, 0u, a.st, 0x6c0u);
+        __syncwarp();
     } else if (warp >= Shape::kEpiFirst) {
         // ------------------------------------------------------- epilogue
         const int ew = warp & 3, wg = (warp - Shape::kEpiFirst) >> 2;

@@ -71,6 +71,23 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, Status
     }
 }
 
+// mbar_wait that also gives up (false, no status) once *abort_flag is set.  The flag
+// is read only while the phase is still open, so a phase that is already complete
+// costs one try_wait.
+__device__ __forceinline__ bool mbar_wait_or_abort(uint64_t *bar, uint32_t parity, StatusWord *st, unsigned where,
+                                                   const int *abort_flag) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t it = 0;; it++) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*(const volatile int *)abort_flag) return false;
+        if ((it & 63u) == 63u && global_timer_ns() - t0 > kWaitLimitNs) {
+            set_status(st, MOE_ERR_TIMEOUT, where);
+            return false;
+        }
+    }
+}
+
 __device__ __forceinline__ uint64_t policy_evict_first() {
     uint64_t pol;
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
