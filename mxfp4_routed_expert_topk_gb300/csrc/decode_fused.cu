@@ -164,7 +164,7 @@ __global__ void __launch_bounds__(kThreadsF, 1) decode_fused_kernel(const FusedA
             const uint32_t ph = (uint32_t)(s / kSlots) & 1u;
             int go = 1;
             if (lane == 0) {
-                if (!mbar_wait(&empty[slot], ph ^ 1u, a.st, 0x100u + slot) || *(volatile int *)abort_flag) {
+                if (!mbar_wait_or_abort(&empty[slot], ph ^ 1u, a.st, 0x100u + slot, abort_flag)) {
                     *abort_flag = 1;
                     go = 0;
                 } else {
@@ -212,12 +212,12 @@ __global__ void __launch_bounds__(kThreadsF, 1) decode_fused_kernel(const FusedA
             const bool pre = sb == spre_at;
             int go = 1;
             if (lane == 0) {
-                bool okw = mbar_wait(&empty[slot], ph ^ 1u, a.st, 0x100u + slot);
+                bool okw = mbar_wait_or_abort(&empty[slot], ph ^ 1u, a.st, 0x100u + slot, abort_flag);
                 if (okw && pre && nstageA > 0) {
                     const int sl = nstageA - 1;  // nothing has reused its slot yet
-                    okw = mbar_wait(&empty[sl % kSlots], (uint32_t)(sl / kSlots) & 1u, a.st, 0x140u);
+                    okw = mbar_wait_or_abort(&empty[sl % kSlots], (uint32_t)(sl / kSlots) & 1u, a.st, 0x140u, abort_flag);
                 }
-                if (!okw || *(volatile int *)abort_flag) {
+                if (!okw) {
                     *abort_flag = 1;
                     go = 0;
                 } else {
@@ -308,7 +308,7 @@ __global__ void __launch_bounds__(kThreadsF, 1) decode_fused_kernel(const FusedA
         const int n = (u_lo + s) * kItems + item;
         const int p = n / v.I, i = n % v.I;
         const bool valid = sidx[p] >= 0;
-        ok = !*(volatile int *)abort_flag && mbar_wait(&full[slot], ph, a.st, 0x200u + slot);
+        ok = mbar_wait_or_abort(&full[slot], ph, a.st, 0x200u + slot, abort_flag);
         if (!ok) *abort_flag = 1;
         float ag = 0.f, au = 0.f;
         if (ok && valid) {
@@ -425,7 +425,7 @@ __global__ void __launch_bounds__(kThreadsF, 1) decode_fused_kernel(const FusedA
         }
         // the preloaded scale rows (one wait per launch)
         if (a.sp_stride != 0 && nstageB > 0) {
-            ok = !*(volatile int *)abort_flag && mbar_wait(fullS, 0u, a.st, 0x3a0u);
+            ok = mbar_wait_or_abort(fullS, 0u, a.st, 0x3a0u, abort_flag);
             if (!ok) *abort_flag = 1;
         }
         const int soffP = (int)((uint64_t)o_lo * v.lds_d % 16);
@@ -434,7 +434,7 @@ __global__ void __launch_bounds__(kThreadsF, 1) decode_fused_kernel(const FusedA
             const uint32_t ph = (uint32_t)(s / kSlots) & 1u;
             const int r0 = sb * a.R, nr = min(a.R, rows - r0);
             const int soff = (int)((uint64_t)(o_lo + r0) * v.lds_d % 16);  // first scale row in the span
-            ok = !*(volatile int *)abort_flag && mbar_wait(&full[slot], ph, a.st, 0x400u + slot);
+            ok = mbar_wait_or_abort(&full[slot], ph, a.st, 0x400u + slot, abort_flag);
             if (!ok) *abort_flag = 1;
             float part[kMaxR] = {0.f, 0.f, 0.f, 0.f};
             if (ok) {
