@@ -8,15 +8,21 @@
 //
 // route_logits_kernel computes l~_e in fp32 with a rigorous bound
 // |l~_e - l_e| <= b_e.  A product of two bf16 is exact in fp32, so the only
-// errors are the roundings of the additions: every product passes through at most
-// d of them (d follows from the summation tree below), hence
-//   |l~ - l| <= gamma_d * (sum_h |x_h W_r[e,h]| + |skew_e|),  gamma_d = d u / (1 - d u),
-// plus at most 2^-150 per product lost to underflow.
+// errors are the roundings of the additions.  A rounded sum r = fl(a + b) is off
+// by at most u |r| (u = 2^-24, round to nearest) when r is normal, and by at most
+// 2^-150 when it is subnormal.  The kernel therefore carries, next to every partial
+// sum, u times the sum of the magnitudes of all the rounded additions below it (a
+// running error bound, accumulated with rounding upwards):
+//   |l~ - l| <= u * sum over the additions of |r_i|  +  2^-149 per product,
+// the last term for underflowing products and subnormal sums.  For sums of terms
+// of mixed sign this is far tighter than the a-priori bound gamma_d * sum |x W|,
+// so far fewer tokens need the exact evaluation.
 //
 // For many tokens (route_tiled_kernel) the logits are a register-tiled fp32 FMA
-// product with a longer (but still bounded) summation tree, and the sum of
-// |x_h W_r[e,h]| is replaced by its Cauchy-Schwarz upper bound ||x|| ||W_r[e]||,
-// so each product costs one FMA.
+// product with a bounded summation tree of depth d, and the a-priori bound
+//   |l~ - l| <= gamma_d * (sum_h |x_h W_r[e,h]| + |skew_e|),  gamma_d = d u / (1 - d u),
+// is used with the sum of |x_h W_r[e,h]| replaced by its Cauchy-Schwarz upper bound
+// ||x|| ||W_r[e]||, so each product costs one FMA.
 //
 // route_select_kernel (one CTA per token) sorts by (l~ desc, index asc) and
 // certifies the order with the intervals [l~ - b, l~ + b]: an outsider can only
@@ -57,14 +63,6 @@ __host__ __device__ inline RouteWs route_ws(void *ws, int M, int E) {
     r.wnorm = (float *)(p + o); o += align_up((size_t)E * sizeof(float), 256);
     r.end = o;
     return r;
-}
-
-// depth of the summation tree of route_logits_kernel for a given H
-__host__ __device__ inline int logit_tree_depth(int H) {
-    const int hmid = ((H / 2) + 7) / 8 * 8;
-    const int longest = hmid > H - hmid ? hmid : H - hmid;
-    const int chunks = (longest + 255) / 256;
-    return 3 /* pairwise 8 */ + chunks /* lane running sum */ + 5 /* warp */ + 1 /* halves */ + 1 /* skew */;
 }
 
 __device__ __forceinline__ void unpack_bf16x8(const uint4 &v, float f[8]) {
@@ -139,9 +137,12 @@ __device__ void logits_block(const uint16_t *__restrict__ x, int M, int H, const
     const int e = blockIdx.x * kLogitExperts + (warp >> 1);
     const int hmid = ((H / 2) + 7) / 8 * 8;
     const int h0 = (warp & 1) ? hmid : 0, h1 = (warp & 1) ? H : hmid;
-    float acc[kLogitTokens], accs[kLogitTokens];
+    // acc: the partial logit; ea, eb: u times the magnitudes of the additions below
+    // it (two chains, rounded upwards)
+    constexpr float u = 5.9604645e-8f;  // 2^-24
+    float acc[kLogitTokens], ea[kLogitTokens], eb[kLogitTokens];
 #pragma unroll
-    for (int t = 0; t < kLogitTokens; t++) acc[t] = accs[t] = 0.f;
+    for (int t = 0; t < kLogitTokens; t++) acc[t] = ea[t] = eb[t] = 0.f;
     if (e < E) {
         const uint16_t *wrow = Wr + (size_t)e * H;
         // batches of NB chunks: all loads of a batch issued before any arithmetic;
@@ -166,11 +167,18 @@ __device__ void logits_block(const uint16_t *__restrict__ x, int M, int H, const
                         unpack_bf16x8(*reinterpret_cast<const uint4 *>(xs + (size_t)t * H + h), xf);
 #pragma unroll
                         for (int i = 0; i < 8; i++) p[i] = xf[i] * wf[i];  // exact
-                        const float s = ((p[0] + p[1]) + (p[2] + p[3])) + ((p[4] + p[5]) + (p[6] + p[7]));
-                        const float a = ((fabsf(p[0]) + fabsf(p[1])) + (fabsf(p[2]) + fabsf(p[3]))) +
-                                        ((fabsf(p[4]) + fabsf(p[5])) + (fabsf(p[6]) + fabsf(p[7])));
+                        const float s01 = p[0] + p[1], s23 = p[2] + p[3], s45 = p[4] + p[5], s67 = p[6] + p[7];
+                        const float s03 = s01 + s23, s47 = s45 + s67;
+                        const float s = s03 + s47;
                         acc[t] += s;
-                        accs[t] += a;
+                        ea[t] = __fmaf_ru(fabsf(s01), u, ea[t]);
+                        eb[t] = __fmaf_ru(fabsf(s23), u, eb[t]);
+                        ea[t] = __fmaf_ru(fabsf(s45), u, ea[t]);
+                        eb[t] = __fmaf_ru(fabsf(s67), u, eb[t]);
+                        ea[t] = __fmaf_ru(fabsf(s03), u, ea[t]);
+                        eb[t] = __fmaf_ru(fabsf(s47), u, eb[t]);
+                        ea[t] = __fmaf_ru(fabsf(s), u, ea[t]);
+                        eb[t] = __fmaf_ru(fabsf(acc[t]), u, eb[t]);
                     }
                 }
             }
@@ -178,14 +186,19 @@ __device__ void logits_block(const uint16_t *__restrict__ x, int M, int H, const
     }
 #pragma unroll
     for (int t = 0; t < kLogitTokens; t++) {
+        float err = __fadd_ru(ea[t], eb[t]);
+        // butterfly: both partners form the same sum, and each carries the bounds of
+        // both halves plus that of the new addition
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) {
-            acc[t] += __shfl_xor_sync(0xffffffffu, acc[t], off);
-            accs[t] += __shfl_xor_sync(0xffffffffu, accs[t], off);
+            const float o = __shfl_xor_sync(0xffffffffu, acc[t], off);
+            const float oe = __shfl_xor_sync(0xffffffffu, err, off);
+            acc[t] += o;
+            err = __fmaf_ru(fabsf(acc[t]), u, __fadd_ru(err, oe));
         }
         if (lane == 0) {
             red_l[warp][t] = acc[t];
-            red_s[warp][t] = accs[t];
+            red_s[warp][t] = err;
         }
     }
     __syncthreads();
@@ -194,17 +207,14 @@ __device__ void logits_block(const uint16_t *__restrict__ x, int M, int H, const
         const int eq = blockIdx.x * kLogitExperts + q;
         if (eq < E) {
             float l = red_l[2 * q][t] + red_l[2 * q + 1][t];
-            float S = red_s[2 * q][t] + red_s[2 * q + 1][t];
+            float b = __fmaf_ru(fabsf(l), u, __fadd_ru(red_s[2 * q][t], red_s[2 * q + 1][t]));
             if (skew != nullptr) {
-                const float sk = skew[eq];
-                l = l + sk;
-                S = S + fabsf(sk);
+                l = l + skew[eq];
+                b = __fmaf_ru(fabsf(l), u, b);
             }
-            const int d = logit_tree_depth(H);
-            // (d+1) u S covers gamma_d S; the factor 1 + 2^-10 covers the rounding of S
-            // itself and of this expression; 2^-148 per product covers underflow.
-            float b = (float)(d + 1) * 5.9604645e-8f * S * (1.0f + 9.765625e-4f);
-            b = b + (float)H * 2.8025969e-45f;
+            // underflowing products and subnormal sums: at most 2^-150 each, fewer
+            // than 2H of them; 2^-148 per element of H covers both
+            b = __fmaf_ru((float)H, 2.8025969e-45f, b);
             logit[(size_t)(m0 + t) * E + eq] = l;
             bound[(size_t)(m0 + t) * E + eq] = b;
         }
