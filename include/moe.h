@@ -133,7 +133,10 @@ const char *moe_status_string(moe_status s);
  * sum_h x_h Wr[e,h] (+ skew_e) in descending order, ties to the lower index;
  * w [M][k] fp32 = softmax over those k logits.  The selection is exact: fp32
  * logits carry a rigorous error bound and any order the bound cannot decide is
- * settled with exact integer arithmetic.  ws: MOE_OP_ROUTE bytes. */
+ * settled with exact integer arithmetic.  ws: MOE_OP_ROUTE bytes; after the call
+ * it holds, for diagnostics, the status word (256 B), then the fp32 logits
+ * [M][E] and then their error bounds [M][E], each region starting on a 256-byte
+ * boundary (|logit - exact logit| <= bound). */
 moe_status moe_route_topk(const uint16_t *x, int M, int H, const uint16_t *Wr, int E,
                           const float *skew, int k, int32_t *idx, float *w,
                           void *ws, size_t ws_bytes, moe_stream_t stream);

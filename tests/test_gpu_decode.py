@@ -115,6 +115,37 @@ def test_route_with_zipf_skew(full, M):
     _route_check(xb, Wrb, Wr, s.k, synth.zipf_skew_f32(synth.skew_seed(0), s.E))
 
 
+@pytest.mark.parametrize("M, skewed", [(1, False), (1, True), (17, False), (40, True)])
+def test_route_bound_covers_error(full, M, skewed):
+    """Fewer than 64 tokens: each fp32 logit and its bound (read from the workspace
+    after the call) satisfy |logit - exact| <= bound against the oracle's exact
+    logits, and the running bound stays far below the a-priori gamma_d * sum|x w|
+    (d = 24 roundings at H = 7168, the bound these kernels used before)."""
+    s, _, Wrb, Wr = full
+    xb = synth.tokens_bf16(synth.TOKENS_SEED["full"], 200, M, s.H)
+    skew = synth.zipf_skew_f32(synth.skew_seed(0), s.E) if skewed else None
+    x = to_dev_bf16(xb)
+    sk = None if skew is None else torch.from_numpy(skew).cuda()
+    ws = moe.workspace(moe.moe_workspace_size(moe.MOE_OP_ROUTE, s.E, s.H, 32, M, s.k))
+    moe.moe_route_topk(x, Wr, s.k, sk, ws=ws)
+    torch.cuda.synchronize()
+    assert moe.moe_check_status(ws) == moe.MOE_OK
+    n = M * s.E
+    raw = ws.cpu().numpy()
+    off_b = 256 + (n * 4 + 255) // 256 * 256
+    logit = np.frombuffer(raw[256:256 + 4 * n].tobytes(), np.float32).reshape(M, s.E).astype(np.float64)
+    bound = np.frombuffer(raw[off_b:off_b + 4 * n].tobytes(), np.float32).reshape(M, s.E).astype(np.float64)
+    _, _, exact = oracle.route(xb, Wrb, s.k, skew)
+    err = np.abs(logit - exact)
+    # the oracle's logits are the exact values rounded once to fp64
+    assert np.all(err <= bound + 2.0 ** -52 * np.abs(exact)), float(np.max(err / bound))
+    S = np.abs(synth.bf16_bits_to_f64(xb)) @ np.abs(synth.bf16_bits_to_f64(Wrb)).T
+    if skew is not None:
+        S = S + np.abs(skew.astype(np.float64))[None, :]
+    apriori = 25 * 2.0 ** -24 * S
+    assert np.mean(bound) < 0.25 * np.mean(apriori)
+
+
 @pytest.mark.parametrize("k", [1, 2, 16, 32])
 def test_route_k_values(tiny, k):
     s, _, Wrb, Wr = tiny
