@@ -676,6 +676,14 @@ __device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long v)
     return ((unsigned long long)mhi << 32) | mlo;
 }
 
+__device__ __forceinline__ unsigned long long warp_min_u64(unsigned long long v) {
+    const unsigned int hi = (unsigned int)(v >> 32);
+    const unsigned int mhi = __reduce_min_sync(0xffffffffu, hi);
+    const unsigned int lo = hi == mhi ? (unsigned int)v : 0xffffffffu;
+    const unsigned int mlo = __reduce_min_sync(0xffffffffu, lo);
+    return ((unsigned long long)mhi << 32) | mlo;
+}
+
 constexpr int kMaxTopCand = 512;  // keys at or above the filter threshold ranked directly
 
 struct SelectShared {
@@ -759,31 +767,41 @@ __device__ void select_token(int m, const uint16_t *__restrict__ x, int H, const
         }
     }
     __syncthreads();
-    if (tid == 0) {
-        unsigned long long t = ~0ull;
-        for (int ww = 0; ww < kRouteWarps; ww++)
-            for (int r = 0; r < q; r++) t = s.wtop[ww][r] < t ? s.wtop[ww][r] : t;
-        s.thr = t;
-        s.nc = 0;
+    if (warp == 0) {  // the smallest of the kRouteWarps * q warp maxima (q <= 4)
+        const unsigned long long t = lane < kRouteWarps * q ? s.wtop[lane / q][lane % q] : ~0ull;
+        const unsigned long long tmin = warp_min_u64(t);
+        if (lane == 0) {
+            s.thr = tmin;
+            s.nc = 0;
+        }
     }
     __syncthreads();
-    // (2) gather every key at or above the threshold (slots by warp ballot)
+    // (2) gather every key at or above the threshold: one slot reservation per warp
+    // for all its keys, each key's slot from the ballots
     const unsigned long long thr = s.thr;
+    {
+        unsigned int bal[J];
+        int cnt = 0;
 #pragma unroll
-    for (int j = 0; j < J; j++) {
-        const int e = tid + kRouteThreads * j;
-        key[j] = e < E ? route_key(lv[j], e) : 0ull;  // restore what (1) cleared
-        const bool take = key[j] != 0ull && key[j] >= thr;
-        const unsigned int bal = __ballot_sync(0xffffffffu, take);
-        if (bal != 0u) {
+        for (int j = 0; j < J; j++) {
+            const int e = tid + kRouteThreads * j;
+            key[j] = e < E ? route_key(lv[j], e) : 0ull;  // restore what (1) cleared
+            bal[j] = __ballot_sync(0xffffffffu, key[j] != 0ull && key[j] >= thr);
+            cnt += __popc(bal[j]);
+        }
+        if (cnt != 0) {  // warp-uniform
             int base = 0;
-            if (lane == __ffs(bal) - 1) base = atomicAdd(&s.nc, __popc(bal));
-            base = __shfl_sync(0xffffffffu, base, __ffs(bal) - 1);
-            const int slot = base + __popc(bal & ((1u << lane) - 1u));
-            if (take && slot < kMaxTopCand) {
-                s.ckey[slot] = key[j];
-                s.cl[slot] = lv[j];
-                s.cb[slot] = bv[j];
+            if (lane == 0) base = atomicAdd(&s.nc, cnt);
+            base = __shfl_sync(0xffffffffu, base, 0);
+#pragma unroll
+            for (int j = 0; j < J; j++) {
+                const int slot = base + __popc(bal[j] & ((1u << lane) - 1u));
+                if (((bal[j] >> lane) & 1u) && slot < kMaxTopCand) {
+                    s.ckey[slot] = key[j];
+                    s.cl[slot] = lv[j];
+                    s.cb[slot] = bv[j];
+                }
+                base += __popc(bal[j]);
             }
         }
     }
@@ -794,6 +812,7 @@ __device__ void select_token(int m, const uint16_t *__restrict__ x, int H, const
         for (int c = tid; c < nc; c += kRouteThreads) {
             const unsigned long long kc = s.ckey[c];
             int r = 0;
+#pragma unroll 8
             for (int d = 0; d < nc; d++) r += s.ckey[d] > kc;
             if (r < k) {
                 s.top[r] = kc;
