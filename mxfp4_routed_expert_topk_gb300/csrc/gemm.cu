@@ -462,8 +462,9 @@ __global__ void __launch_bounds__(NT, GemmShape<NT>::kCtasPerSm)
 
     int it_issued = 0;  // producer: stages issued
     // The copy and MMA roles run their loops with the whole warp converged (waits
-    // polled by lane 0 and broadcast), so the addresses, coordinates and descriptors
-    // are warp-uniform values; one elected lane issues the asynchronous operations.
+    // polled by lane 0, or lanes 0-3 with a vote, and broadcast), so the addresses,
+    // coordinates and descriptors are warp-uniform values; one elected lane issues
+    // the asynchronous operations.
     if (warp == 0) {
         // ------------------------------------------------------- tensor copies
         int it = 0, s = 0;  // stages issued; slot of stage it
