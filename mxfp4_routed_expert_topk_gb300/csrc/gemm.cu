@@ -117,6 +117,9 @@ constexpr uint32_t kSwizzleNone = 0;
 
 // Instruction descriptor of kind::mxf8f6f4: A = E2M1 (5), B = E4M3 (0), both
 // K-major, M = 128, N = n, E8M0 scales, scale-factor ids for A and B.
+// idesc_mxf8f6f4(n, k) = idesc_mxf8f6f4(n, 0) + k * kIdescSfStep for k in 0..3
+constexpr uint32_t kIdescSfStep = (1u << 4) | (1u << 29);
+
 __device__ __forceinline__ uint32_t idesc_mxf8f6f4(int n, int sf_id) {
     uint32_t d = 0;
     d |= (uint32_t)(sf_id & 3) << 4;     // B scale factor id
@@ -520,12 +523,21 @@ __global__ void __launch_bounds__(NT, GemmShape<NT>::kCtasPerSm)
         int jb = 0, s = 0;  // tiles; slot of the next stage
         uint32_t ph = 0;    // its phase parity
         bool run = true;
-        const uint32_t a_stage = (uint32_t)(tpi * kTileM * kTileK), b_stage = (uint32_t)(a.BN * kTileK);
-        const uint32_t sfb_bytes = sfb_stage_bytes(nsfb);
-        const uint32_t sA0 = smem_u32(sA), sB0 = smem_u32(sB), sSFA0 = smem_u32(sSFA), sSFB0 = smem_u32(sSFB);
+        // Descriptors of slot 0, built once: a stage's descriptors add the stage's
+        // offset in 16-byte units to the start-address field (shared addresses stay
+        // below 2^18, so the 14-bit field never carries into the next one).
+        const uint32_t a_stage16 = (uint32_t)(tpi * kTileM * kTileK) >> 4, b_stage16 = (uint32_t)(a.BN * kTileK) >> 4;
+        const uint32_t sfa_stage16 = (uint32_t)tpi * 512u >> 4, sfb_stage16 = sfb_stage_bytes(nsfb) >> 4;
+        const uint64_t adesc0 = smem_desc(smem_u32(sA), 16, 1024, kSwizzle128B);
+        const uint64_t bdesc0 = smem_desc(smem_u32(sB), 16, 1024, kSwizzle128B);
+        const uint64_t sfadesc0 = smem_desc(smem_u32(sSFA), 128, 128, kSwizzleNone);
+        // core matrices of 8 rows x 16 bytes: for two atoms the 16-byte halves 128 bytes
+        // apart and the row groups 256 bytes apart
+        const uint64_t sfbdesc0 = smem_desc(smem_u32(sSFB), 128, nsfb == 1 ? 128 : 256, kSwizzleNone);
         const int nlook = min(4, ns);  // stages polled at once (never past the ring)
         for (JobIter J(a, nu); run && J.valid(); J.next(), jb++) {
             const int nmma = (J.nn() + 15) / 16 * 16;
+            const uint32_t idesc0 = idesc_mxf8f6f4(nmma, 0);  // + ks * kIdescSfStep for K step ks
             const int buf = jb & 1;
             // the epilogue has finished with this accumulator (two tiles ago)
             int okl = 1;
@@ -563,26 +575,24 @@ __global__ void __launch_bounds__(NT, GemmShape<NT>::kCtasPerSm)
                     for (int q = 0; q < r; q++) {
                         const uint32_t sfa_t = tmem + sf_col0 + (uint32_t)sq * sf_stage;  // + 4t for tile t
                         const uint32_t sfb_t = sfa_t + 4u * (uint32_t)tpi;
-                        const uint32_t sfa_s = sSFA0 + (uint32_t)sq * (uint32_t)tpi * 512u;
-                        const uint32_t sfb_s = sSFB0 + (uint32_t)sq * sfb_bytes;
-                        const uint32_t a_base = sA0 + (uint32_t)sq * a_stage;
-                        const uint32_t b_base = sB0 + (uint32_t)sq * b_stage;
-                        for (int t = 0; t < tpi; t++)
-                            tc_cp_sf(sfa_t + 4u * t, smem_desc(sfa_s + 512u * t, 128, 128, kSwizzleNone));
+                        const uint64_t sfad = sfadesc0 + (uint64_t)((uint32_t)sq * sfa_stage16);
+                        const uint64_t sfbd = sfbdesc0 + (uint64_t)((uint32_t)sq * sfb_stage16);
+                        const uint64_t ad0 = adesc0 + (uint64_t)((uint32_t)sq * a_stage16);
+                        const uint64_t bd0 = bdesc0 + (uint64_t)((uint32_t)sq * b_stage16);
+                        for (int t = 0; t < tpi; t++) tc_cp_sf(sfa_t + 4u * t, sfad + (uint64_t)(32 * t));  // 512 B apart
                         if (nsfb == 1)
-                            tc_cp_sf(sfb_t, smem_desc(sfb_s, 128, 128, kSwizzleNone));
-                        else  // core matrices of 8 rows x 16 bytes: the two 16-byte halves 128 bytes
-                              // apart, row groups 256 bytes apart
-                            tc_cp_sf2(sfb_t, smem_desc(sfb_s, 128, 256, kSwizzleNone));
+                            tc_cp_sf(sfb_t, sfbd);
+                        else
+                            tc_cp_sf2(sfb_t, sfbd);
                         for (int t = 0; t < tpi; t++) {
                             // tile t: rows 128t.. of the stage's A (16 KB apart), accumulator columns t*BN..
+                            const uint64_t adt = ad0 + (uint64_t)(1024 * t);
 #pragma unroll
                             for (int ks = 0; ks < kTileK / 32; ks++) {
-                                const uint64_t ad = smem_desc(a_base + (uint32_t)(t * kTileM * kTileK) + 32 * ks, 16,
-                                                              1024, kSwizzle128B);
-                                const uint64_t bd = smem_desc(b_base + 32 * ks, 16, 1024, kSwizzle128B);
-                                tc_mma(acc + (uint32_t)(t * a.BN), ad, bd, idesc_mxf8f6f4(nmma, ks), sfa_t + 4u * t,
-                                       sfb_t, (kt + q > 0 || ks > 0) ? 1u : 0u);
+                                // K step ks: 32 bytes further along both operands' rows
+                                tc_mma(acc + (uint32_t)(t * a.BN), adt + (uint64_t)(2 * ks), bd0 + (uint64_t)(2 * ks),
+                                       idesc0 + (uint32_t)ks * kIdescSfStep, sfa_t + 4u * t, sfb_t,
+                                       (kt + q > 0 || ks > 0) ? 1u : 0u);
                             }
                         }
                         tc_commit(&empty[sq]);  // frees the stage when these MMAs have read it
