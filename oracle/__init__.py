@@ -88,6 +88,9 @@ def lib():
         L.orc_expert_ambiguity.restype = None
         L.orc_expert_ambiguity.argtypes = [_u8p, _u8p, ctypes.c_int, ctypes.c_int, _f64p, ctypes.c_int,
                                            ctypes.c_double, _f64p]
+        L.orc_h_radius.restype = None
+        L.orc_h_radius.argtypes = [_u8p, _u8p, ctypes.c_int, ctypes.c_int, _f64p, ctypes.c_int, ctypes.c_double,
+                                   _f64p, _f64p]
         L.orc_prescale_exponent.restype = ctypes.c_int
         L.orc_prescale_exponent.argtypes = [_u16p, ctypes.c_int]
         L.orc_prescale.restype = None
@@ -187,9 +190,12 @@ def expert_forward(codes: np.ndarray, scales: np.ndarray, H: int, I: int, x: np.
     return y, h
 
 
-# Error model of the fp32 h of the tensor-core path, relative to the sums of
-# |products| of its dot products (a few fp32 ulps per term, with a wide margin).
-MXFP8_AMBIGUITY_EPS = 2.0 ** -16
+# Error model of the fp32 h of the tensor-core path (orc_h_radius): each
+# block-scaled MMA step of K = 32 adds its exact block sum S_t to the fp32
+# accumulator P_{t-1} with an error of at most this times |P_{t-1}| + |S_t| (one
+# fp32 ulp of the larger operand), so |g_gpu - g| <= MMA_STEP_REL *
+# sum_t (|P_{t-1}| + |S_t|).
+MMA_STEP_REL = 2.0 ** -23
 
 
 def mxfp8_ambiguity(v: np.ndarray, radius) -> np.ndarray:
@@ -200,6 +206,19 @@ def mxfp8_ambiguity(v: np.ndarray, radius) -> np.ndarray:
     d = np.empty_like(v)
     lib().orc_mxfp8_ambiguity(v, r, v.size, d)
     return d
+
+
+def h_radius(codes: np.ndarray, scales: np.ndarray, H: int, I: int, x: np.ndarray,
+             rel: float = MMA_STEP_REL):
+    """h [n, I] of one expert for MXFP8-exact rows x [n, H], and the error radius of
+    the fp32 h the tensor-core path computes under the step-error model `rel`."""
+    x = np.ascontiguousarray(np.atleast_2d(x), dtype=np.float64)
+    n = x.shape[0]
+    h = np.empty((n, I), dtype=np.float64)
+    r = np.empty((n, I), dtype=np.float64)
+    lib().orc_h_radius(np.ascontiguousarray(codes, dtype=np.uint8), np.ascontiguousarray(scales, dtype=np.uint8),
+                       H, I, x, n, rel, h, r)
+    return h, r
 
 
 def prescale(x_bits: np.ndarray) -> np.ndarray:
@@ -299,7 +318,7 @@ def sort_pairs(idx: np.ndarray, E: int):
 
 
 def pair_ambiguity(experts, H: int, I: int, x: np.ndarray, idx: np.ndarray,
-                   eps: float = MXFP8_AMBIGUITY_EPS) -> np.ndarray:
+                   eps: float = MMA_STEP_REL) -> np.ndarray:
     """amb[m, j, o]: the largest change of expert_{idx[m,j]}(x[m])[o] that an
     alternative (equally correct) MXFP8 rounding of its h could make."""
     M, k = idx.shape
@@ -317,7 +336,7 @@ def pair_ambiguity(experts, H: int, I: int, x: np.ndarray, idx: np.ndarray,
 
 
 def combine_ambiguity(experts, H: int, I: int, x: np.ndarray, idx: np.ndarray, w: np.ndarray,
-                      eps: float = MXFP8_AMBIGUITY_EPS) -> np.ndarray:
+                      eps: float = MMA_STEP_REL) -> np.ndarray:
     """Per output, sum_j |w_j| * pair_ambiguity: the part of the difference between
     two correct MXFP8-h layer outputs that rounding choices can explain."""
     amb = pair_ambiguity(experts, H, I, x, idx, eps)

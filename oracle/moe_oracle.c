@@ -270,33 +270,47 @@ static int exact_logit(const uint16_t *x, const uint16_t *w, int H, const float 
 int orc_route(const uint16_t *x, int M, int H, const uint16_t *Wr, int E, const float *skew, int k,
               int32_t *idx, double *w, double *logits) {
     if (M < 0 || H <= 0 || E <= 0 || k <= 0 || k > E) return -2;
-    exact_t *l = (exact_t *)malloc(sizeof(exact_t) * (size_t)E);
-    char *taken = (char *)malloc((size_t)E);
-    if (!l || !taken) { free(l); free(taken); return -2; }
     int rc = 0;
-    for (int m = 0; m < M && rc == 0; m++) {
-        const uint16_t *xm = x + (size_t)m * H;
-        for (int e = 0; e < E; e++)
-            if (exact_logit(xm, Wr + (size_t)e * H, H, skew ? skew + e : NULL, &l[e])) { rc = -1; break; }
-        if (rc) break;
-        if (logits) for (int e = 0; e < E; e++) logits[(size_t)m * E + e] = ex_to_double(&l[e]);
-        memset(taken, 0, (size_t)E);
-        for (int j = 0; j < k; j++) {              /* k passes of "largest remaining, lowest index" */
-            int best = -1;
-            for (int e = 0; e < E; e++) {
-                if (taken[e]) continue;
-                if (best < 0 || ex_cmp(&l[e], &l[best]) > 0) best = e;
-            }
-            taken[best] = 1;
-            idx[(size_t)m * k + j] = best;
+    /* tokens are independent: each thread routes whole tokens with its own buffers */
+    #pragma omp parallel
+    {
+        exact_t *l = (exact_t *)malloc(sizeof(exact_t) * (size_t)E);
+        char *taken = (char *)malloc((size_t)E);
+        if (!l || !taken) {
+            #pragma omp atomic write
+            rc = -2;
         }
-        double lmax = ex_to_double(&l[idx[(size_t)m * k]]), z = 0.0;
-        for (int j = 0; j < k; j++) z += exp(ex_to_double(&l[idx[(size_t)m * k + j]]) - lmax);
-        for (int j = 0; j < k; j++)
-            w[(size_t)m * k + j] = exp(ex_to_double(&l[idx[(size_t)m * k + j]]) - lmax) / z;
+        #pragma omp for schedule(dynamic, 1)
+        for (int m = 0; m < M; m++) {
+            if (!l || !taken) continue;
+            const uint16_t *xm = x + (size_t)m * H;
+            int bad = 0;
+            for (int e = 0; e < E && !bad; e++)
+                if (exact_logit(xm, Wr + (size_t)e * H, H, skew ? skew + e : NULL, &l[e])) bad = 1;
+            if (bad) {
+                #pragma omp atomic write
+                rc = -1;
+                continue;
+            }
+            if (logits) for (int e = 0; e < E; e++) logits[(size_t)m * E + e] = ex_to_double(&l[e]);
+            memset(taken, 0, (size_t)E);
+            for (int j = 0; j < k; j++) {              /* k passes of "largest remaining, lowest index" */
+                int best = -1;
+                for (int e = 0; e < E; e++) {
+                    if (taken[e]) continue;
+                    if (best < 0 || ex_cmp(&l[e], &l[best]) > 0) best = e;
+                }
+                taken[best] = 1;
+                idx[(size_t)m * k + j] = best;
+            }
+            double lmax = ex_to_double(&l[idx[(size_t)m * k]]), z = 0.0;
+            for (int j = 0; j < k; j++) z += exp(ex_to_double(&l[idx[(size_t)m * k + j]]) - lmax);
+            for (int j = 0; j < k; j++)
+                w[(size_t)m * k + j] = exp(ex_to_double(&l[idx[(size_t)m * k + j]]) - lmax) / z;
+        }
+        free(l);
+        free(taken);
     }
-    free(l);
-    free(taken);
     return rc;
 }
 
@@ -352,93 +366,129 @@ void orc_expert_forward(const uint8_t *codes, const uint8_t *scales, int H, int 
 }
 
 /* ------------------------------------------------- MXFP8 rounding ambiguity
- * Test support for the tensor-core prefill path, whose h is computed in fp32:
- * h_i carries an error of up to radius[i] there, so a value within radius[i] of an
- * E4M3 rounding midpoint may legitimately round to either neighbour, and a block
- * whose max |h| lies within its radius of a power of two may take either shared
- * exponent.  delta[i] = the largest change of the dequantised value such an
- * alternative choice makes (0 when the choice is clear).  The quantised values
- * themselves are those of orc_quant_mxfp8. */
+ * Test support for the tensor-core prefill path.  There h is computed in fp32, so
+ * the oracle knows the GPU's h_i only to within an error radius r_i (orc_h_radius),
+ * and an MXFP8 decision that falls inside that radius may go either way: the
+ * element may round to either E4M3 neighbour, and a block whose max |h| sits near a
+ * power of two may take either shared exponent.  Both sides apply the same OCP
+ * rule (orc_quant_mxfp8) to the value they hold. */
+
+/* Shared exponent of a block with max |v| = amax (OCP MX v1.0: floor(log2 amax) - 8,
+ * clamped to [-127, 127]; -127 for amax == 0). */
+static int mx8_exp(double amax) {
+    if (!(amax > 0.0)) return -127;
+    int ex;
+    frexp(amax, &ex);
+    int X = (ex - 1) - 8;
+    if (X < -127) X = -127;
+    if (X > 127) X = 127;
+    return X;
+}
+
+/* v quantised at shared exponent X and dequantised: E4M3(v 2^-X) 2^X. */
+static double mx8_at(double v, int X) { return ldexp(orc_e4m3_value(orc_e4m3_encode(ldexp(v, -X))), X); }
+
+/* delta[i] = the largest |alternative - nominal| of the MXFP8 value of v[i] when each
+ * element of its 32-block may be anywhere in [v - radius, v + radius]: every shared
+ * exponent a block max in its range can give is tried, and at each exponent the
+ * quantised value is monotone in the element, so its extremes over the interval are
+ * the quantised ends of the interval.  The nominal value is that of orc_quant_mxfp8. */
 void orc_mxfp8_ambiguity(const double *v, const double *radius, int n, double *delta) {
     for (int b0 = 0; b0 < n; b0 += 32) {
         int b1 = b0 + 32 < n ? b0 + 32 : n;
-        double amax = 0.0, rmax = 0.0;
+        double amax = 0.0, alo = 0.0, ahi = 0.0;
         for (int i = b0; i < b1; i++) {
-            if (fabs(v[i]) > amax) amax = fabs(v[i]);
-            if (radius[i] > rmax) rmax = radius[i];
+            double a = fabs(v[i]), lo = a - radius[i] > 0.0 ? a - radius[i] : 0.0;
+            if (a > amax) amax = a;
+            if (lo > alo) alo = lo;
+            if (a + radius[i] > ahi) ahi = a + radius[i];
         }
-        int X = -127, Xalt = 1000;
-        if (amax > 0.0) {
-            int ex;
-            frexp(amax, &ex);
-            X = (ex - 1) - 8;
-            if (X < -127) X = -127;
-            if (X > 127) X = 127;
-            if (amax + rmax >= ldexp(1.0, X + 9) && X < 127) Xalt = X + 1;
-            else if (amax - rmax < ldexp(1.0, X + 8) && X > -127) Xalt = X - 1;
-        }
+        int X = mx8_exp(amax), Xlo = mx8_exp(alo), Xhi = mx8_exp(ahi);
         for (int i = b0; i < b1; i++) {
-            double t = ldexp(v[i], -X), a = fabs(t), rt = ldexp(radius[i], -X);
-            double q = ldexp(orc_e4m3_value(orc_e4m3_encode(t)), X);
-            double d = 0.0;
-            if (a < 448.0) {
-                double lo = 0.0, hi = 448.0;           /* neighbours of a among E4M3 values */
-                for (unsigned c = 0; c < 0x7F; c++) {
-                    double vc = orc_e4m3_value(c);
-                    if (vc <= a && vc > lo) lo = vc;
-                    if (vc >= a && vc < hi) hi = vc;
-                }
-                if (fabs(a - 0.5 * (lo + hi)) <= rt) d = ldexp(hi - lo, X);
-            }
-            if (Xalt != 1000) {
-                double q2 = ldexp(orc_e4m3_value(orc_e4m3_encode(ldexp(v[i], -Xalt))), Xalt);
-                if (fabs(q2 - q) > d) d = fabs(q2 - q);
+            double q = mx8_at(v[i], X), d = 0.0;
+            for (int Xa = Xlo; Xa <= Xhi; Xa++) {
+                double e1 = fabs(mx8_at(v[i] - radius[i], Xa) - q);
+                double e2 = fabs(mx8_at(v[i] + radius[i], Xa) - q);
+                if (e1 > d) d = e1;
+                if (e2 > d) d = e2;
             }
             delta[i] = d;
         }
     }
 }
 
-/* |dot| of an MXFP4 row with v: sum_j |w_j v_j| (the scale of fp32 rounding error). */
-static double mx_row_absdot(const uint8_t *codes, const uint8_t *scales, size_t row, int K, const double *v) {
+/* Dot product as mx_row_dot, also returning sum_t (|P_{t-1}| + |S_t|) over the
+ * 32-element blocks t in ascending K, with S_t the block's scaled sum and P_t the
+ * running sum after it (P_0 = 0). */
+static double mx_row_dot_steps(const uint8_t *codes, const uint8_t *scales, size_t row, int K, const double *v,
+                               double *step_mag) {
     const uint8_t *c = codes + row * (size_t)(K / 2);
     const uint8_t *s = scales + row * (size_t)(K / 32);
-    double acc = 0.0;
+    double acc = 0.0, sp = 0.0;
     for (int b = 0; b < K / 32; b++) {
         double sc = orc_e8m0_value(s[b]), part = 0.0;
         for (int j = 32 * b; j < 32 * b + 32; j++) {
             unsigned code = (j & 1) ? (c[j / 2] >> 4) : (c[j / 2] & 15);
-            part += fabs(orc_e2m1_value(code) * v[j]);
+            part += orc_e2m1_value(code) * v[j];
         }
+        sp += fabs(acc) + fabs(sc * part);
         acc += sc * part;
     }
+    *step_mag = sp;
     return acc;
 }
 
-/* Per output row o of one expert applied to the rows x [n][H] with MXFP8 h:
- * yamb[o] = sum_i |W_d[o][i]| * delta_i (orc_mxfp8_ambiguity).  The error radius
- * of h_i = silu(g) u is modelled as rel * (S_g |u| + |g| S_u) + rel * |h|, with
- * S = the sum of |products| of each dot product (fp32 accumulation with some
- * ulps per term; rel = 2^-16 leaves a wide margin). */
-void orc_expert_ambiguity(const uint8_t *codes, const uint8_t *scales, int H, int I,
-                          const double *x, int n, double rel, double *yamb) {
-    const uint8_t *cg = codes, *cu = codes + (size_t)I * H / 2, *cd = codes + (size_t)I * H;
-    const uint8_t *sg = scales, *su = scales + (size_t)I * H / 32, *sd = scales + (size_t)I * H / 16;
-    double *hv = (double *)malloc(sizeof(double) * (size_t)I);
-    double *rd = (double *)malloc(sizeof(double) * (size_t)I);
-    double *dl = (double *)malloc(sizeof(double) * (size_t)I);
+/* h = silu(W_g x) * (W_u x) of one expert for rows x [n][H] (x already MXFP8-exact),
+ * and the error radius of the fp32 h the tensor-core path computes, per element.
+ * The error model:
+ *  (1) each block-scaled MMA step of K = 32 (one E8M0 block of both operands) adds
+ *      its block sum S_t, exact, to the fp32 accumulator P_{t-1} with an error of at
+ *      most rel * (|P_{t-1}| + |S_t|) (rel = 2^-23, one fp32 ulp of the larger
+ *      operand: covers round-to-nearest or truncation of the sum, and truncation of
+ *      the smaller operand when it is aligned to the larger), so |g_gpu - g| <=
+ *      dg = rel * sum_t (|P_{t-1}| + |S_t|), the steps taken in ascending K, the
+ *      order the MMAs run in; likewise du;
+ *  (2) silu(g) * u is then evaluated in fp32 with a fast exponential (whose
+ *      documented error grows linearly in |g|) and a fast division: relative error
+ *      at most (8 + 2|g|) 2^-23;
+ *  so, with |silu'| <= 1.1,
+ *      r = 1.1 dg (|u| + du) + |silu(g)| du + (8 + 2|g|) 2^-23 |h|.
+ * h, radius [n][I]. */
+void orc_h_radius(const uint8_t *codes, const uint8_t *scales, int H, int I, const double *x, int n, double rel,
+                  double *h, double *radius) {
+    const uint8_t *cg = codes, *cu = codes + (size_t)I * H / 2;
+    const uint8_t *sg = scales, *su = scales + (size_t)I * H / 32;
     for (int r = 0; r < n; r++) {
         const double *xr = x + (size_t)r * H;
         #pragma omp parallel for schedule(static)
         for (int i = 0; i < I; i++) {
-            double g = mx_row_dot(cg, sg, (size_t)i, H, xr);
-            double u = mx_row_dot(cu, su, (size_t)i, H, xr);
-            double Sg = mx_row_absdot(cg, sg, (size_t)i, H, xr);
-            double Su = mx_row_absdot(cu, su, (size_t)i, H, xr);
-            hv[i] = silu(g) * u;
-            rd[i] = rel * (Sg * fabs(u) + fabs(g) * Su) + rel * fabs(hv[i]);
+            double Pg, Pu;
+            double g = mx_row_dot_steps(cg, sg, (size_t)i, H, xr, &Pg);
+            double u = mx_row_dot_steps(cu, su, (size_t)i, H, xr, &Pu);
+            /* the fp64 running sums stand in for the exact ones: 1e-9 of margin */
+            double dg = rel * Pg * (1.0 + 1e-9), du = rel * Pu * (1.0 + 1e-9);
+            double sg_ = silu(g), hv = sg_ * u;
+            h[(size_t)r * I + i] = hv;
+            radius[(size_t)r * I + i] =
+                1.1 * dg * (fabs(u) + du) + fabs(sg_) * du + (8.0 + 2.0 * fabs(g)) * ldexp(1.0, -23) * fabs(hv);
         }
-        orc_mxfp8_ambiguity(hv, rd, I, dl);
+    }
+}
+
+/* Per output row o of one expert applied to the rows x [n][H] with MXFP8 h:
+ * yamb[o] = sum_i |W_d[o][i]| * delta_i, with delta from orc_mxfp8_ambiguity on the
+ * radii of orc_h_radius (step error `rel`): the largest change of o that equally
+ * valid MXFP8 decisions on the GPU's h can make. */
+void orc_expert_ambiguity(const uint8_t *codes, const uint8_t *scales, int H, int I,
+                          const double *x, int n, double rel, double *yamb) {
+    const uint8_t *cd = codes + (size_t)I * H;
+    const uint8_t *sd = scales + (size_t)I * H / 16;
+    double *hv = (double *)malloc(sizeof(double) * (size_t)n * I);
+    double *rd = (double *)malloc(sizeof(double) * (size_t)n * I);
+    double *dl = (double *)malloc(sizeof(double) * (size_t)I);
+    orc_h_radius(codes, scales, H, I, x, n, rel, hv, rd);
+    for (int r = 0; r < n; r++) {
+        orc_mxfp8_ambiguity(hv + (size_t)r * I, rd + (size_t)r * I, I, dl);
         #pragma omp parallel for schedule(static)
         for (int o = 0; o < H; o++) {
             const uint8_t *c = cd + (size_t)o * (I / 2);

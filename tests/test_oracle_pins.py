@@ -14,6 +14,7 @@ import torch
 
 import oracle
 import synth
+from tests._util import dequant_mxfp4 as _dequant, split_expert as _split
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
@@ -235,25 +236,6 @@ def test_route_weights_sum_to_one_and_are_monotone():
 # ------------------------------------------------------------------ the expert
 
 
-def _dequant(codes, scales, rows, K):
-    """Dense matrix from logical MXFP4 bytes, by the OCP bit-field definition."""
-    c = np.asarray(codes, dtype=np.uint8).reshape(rows, K // 2)
-    nib = np.empty((rows, K), dtype=np.int64)
-    nib[:, 0::2] = c & 15
-    nib[:, 1::2] = c >> 4
-    s, e, m = nib >> 3, (nib >> 1) & 3, nib & 1
-    mag = np.where(e == 0, m * 0.5, np.exp2(e - 1.0) * (1 + m / 2))
-    val = np.where(s == 1, -mag, mag)
-    sc = np.exp2(np.asarray(scales, dtype=np.float64).reshape(rows, K // 32) - 127)
-    return val * np.repeat(sc, 32, axis=1)
-
-
-def _split(codes, scales, H, I):
-    n1, n2 = I * H // 2, 2 * I * H // 2
-    s1, s2 = I * H // 32, 2 * I * H // 32
-    return ((codes[:n1], scales[:s1]), (codes[n1:n2], scales[s1:s2]), (codes[n2:], scales[s2:]))
-
-
 def test_zero_code_expert_contributes_zero():
     H, I = 256, 128
     codes = np.zeros(3 * H * I // 2, dtype=np.uint8)
@@ -388,3 +370,139 @@ def test_mxfp8_ambiguity_marks_only_near_decisions():
     assert d[32] > 0.0                # scale alternative 2^1 changes 511.99 -> 512 vs 448
     q = oracle.quant_mxfp8(v)[2]
     assert q[3] == 1.0 and q[1] == 1.0  # midpoint rounds to even (1.0)
+
+
+# ------------------------------------------- MXFP8 h of the tensor-core path
+# The prefill path quantises h = silu(g) * u to MXFP8 before W_d.  The GPU holds g
+# and u as fp32 sums of block-scaled MMA steps (K = 32 each), so near an E4M3
+# rounding midpoint or a power-of-two block max either MXFP8 choice is correct.  The
+# oracle bounds the GPU's error in h (orc_h_radius) and the output change the open
+# choices can make (orc_mxfp8_ambiguity, orc_expert_ambiguity); the pins below fix
+# those pieces against an independent composition, an fp32 emulation of the step
+# model and brute force.
+
+
+def _one_expert(codes, scales):
+    return lambda e: (codes, scales)
+
+
+def test_expert_mxfp8_h_matches_independent_composition():
+    """orc_expert_forward with h_mode 1 = dense dequantised W_g, W_u (bit-field
+    definition) -> SwiGLU -> MXFP8 of h (the pinned block rule) -> dense W_d."""
+    H, I = 256, 128
+    codes, scales = oracle.gen_expert(17, 3, H, I)
+    (cg, sg), (cu, su), (cd, sd) = _split(codes, scales, H, I)
+    Wg, Wu, Wd = _dequant(cg, sg, I, H), _dequant(cu, su, I, H), _dequant(cd, sd, H, I)
+    xq = oracle.quant_rows_mxfp8(synth.bf16_bits_to_f64(synth.tokens_bf16(13, 0, 3, H)))
+    y, h = oracle.expert_forward(codes, scales, H, I, xq, h_mode=1)
+    for m in range(3):
+        g, u = Wg @ xq[m], Wu @ xq[m]
+        hq = oracle.quant_mxfp8(g / (1 + np.exp(-g)) * u)[2]
+        assert np.array_equal(h[m], hq)
+        assert np.allclose(y[m], Wd @ hq, rtol=1e-13, atol=1e-13 * np.abs(y[m]).max())
+    y0, _ = oracle.expert_forward(codes, scales, H, I, xq, h_mode=0)
+    assert not np.array_equal(y, y0)          # the quantisation step is really applied
+
+
+def _round_f32(v, mode):
+    """fp64 values rounded once to fp32: nearest-even, toward zero, up or down."""
+    r = v.astype(np.float32)
+    rd = r.astype(np.float64)
+    if mode == "ru":
+        r = np.where(rd < v, np.nextafter(r, np.float32(np.inf)), r)
+    elif mode == "rd":
+        r = np.where(rd > v, np.nextafter(r, np.float32(-np.inf)), r)
+    elif mode == "rz":
+        r = np.where(np.abs(rd) > np.abs(v), np.nextafter(r, np.float32(0)), r)
+    return r
+
+
+def _fp32_steps(W, x, mode):
+    """The fp32 accumulation of the step model: the exact sums of each 32-column block
+    (in order) added to an fp32 running sum, one rounding per step."""
+    blocks = (W * x[None, :]).reshape(W.shape[0], -1, 32).sum(axis=2)   # exact in fp64
+    acc = _round_f32(blocks[:, 0], mode)
+    for t in range(1, blocks.shape[1]):
+        acc = _round_f32(acc.astype(np.float64) + blocks[:, t], mode)
+    return acc
+
+
+@pytest.mark.parametrize("mode", ["rn", "rz", "ru", "rd"])
+def test_h_radius_covers_fp32_step_accumulation(mode):
+    """The radius covers the error of an fp32 h built under the step model with any of
+    the four rounding modes (and an fp32 epilogue), and is not far above the error that
+    directed rounding actually reaches: a widened model constant fails here."""
+    H, I = 1024, 256
+    codes, scales = oracle.gen_expert(31, 4, H, I)
+    (cg, sg), (cu, su), _ = _split(codes, scales, H, I)
+    Wg, Wu = _dequant(cg, sg, I, H), _dequant(cu, su, I, H)
+    # MXFP8 rows (as on the GPU: their short block sums often add up exactly in fp32)
+    # and rows of full fp32 precision (every step rounds)
+    xq = np.concatenate([oracle.quant_rows_mxfp8(synth.bf16_bits_to_f64(synth.tokens_bf16(12, 0, 2, H))),
+                         np.random.default_rng(12).standard_normal((2, H)).astype(np.float32).astype(np.float64)])
+    h, r = oracle.h_radius(codes, scales, H, I, xq)
+    ratios = []
+    for m in range(4):
+        g, u = Wg @ xq[m], Wu @ xq[m]
+        assert np.allclose(h[m], g / (1 + np.exp(-g)) * u, rtol=1e-12, atol=1e-12 * np.abs(h[m]).max())
+        g32, u32 = _fp32_steps(Wg, xq[m], mode), _fp32_steps(Wu, xq[m], mode)
+        h32 = (g32 / (np.float32(1) + np.exp(-g32)) * u32).astype(np.float64)
+        err = np.abs(h32 - h[m])
+        assert np.all(err <= r[m]), float(np.max(err / r[m]))
+        if m >= 2:
+            ratios.append(err / r[m])
+    if mode in ("ru", "rd"):
+        assert np.median(np.concatenate(ratios)) > 0.04
+
+
+def test_mxfp8_ambiguity_bounds_every_choice_in_the_radius():
+    """Brute force: values drawn anywhere in [v - r, v + r] (and at the ends) quantise
+    to within delta of the nominal MXFP8 value, elements with delta 0 never change, and
+    delta is reached for many of the open elements."""
+    rng = np.random.default_rng(5)
+    n = 32 * 48
+    v = rng.standard_normal(n) * np.exp2(rng.integers(-3, 3, size=n))
+    # planted decisions: E4M3 midpoints, and block maxima at a power of two
+    v[3] = 1.0625 * 2.0 ** -6
+    v[40] = 2.0 ** 3
+    v[96:128] *= 0.1                  # element 100 the clear max of its block, just below 2
+    v[100] = -(2.0 ** 1) * (1 - 1e-7)
+    r = np.abs(v) * 10.0 ** rng.uniform(-7, -2, size=n)
+    r[100] = 1e-6
+    d = oracle.mxfp8_ambiguity(v, r)
+    q0 = oracle.quant_mxfp8(v)[2]
+    worst = np.zeros(n)
+    for trial in range(400):
+        pick = rng.integers(0, 3, size=n)
+        vv = np.where(pick == 0, v - r, np.where(pick == 1, v + r, v + rng.uniform(-1, 1, size=n) * r))
+        dq = np.abs(oracle.quant_mxfp8(vv)[2] - q0)
+        assert np.all(dq <= d)
+        worst = np.maximum(worst, dq)
+    assert np.all(worst[d == 0] == 0)
+    openi = d > 0
+    assert openi.sum() > 20 and d[3] > 0 and d[40] > 0 and d[100] > 0
+    assert np.mean(worst[openi] == d[openi]) > 0.25
+
+
+def test_expert_ambiguity_bounds_the_output_change():
+    """Brute force on a tiny expert with a large step error (so that many decisions
+    are open): every h inside the radius gives an output within the per-output
+    ambiguity of the nominal MXFP8-h output."""
+    H, I = 256, 128
+    rel = 2.0 ** -12
+    codes, scales = oracle.gen_expert(19, 2, H, I)
+    _, _, (cd, sd) = _split(codes, scales, H, I)
+    Wd = _dequant(cd, sd, H, I)
+    xq = oracle.quant_rows_mxfp8(synth.bf16_bits_to_f64(synth.tokens_bf16(14, 0, 2, H)))
+    h, r = oracle.h_radius(codes, scales, H, I, xq, rel)
+    amb = oracle.pair_ambiguity(_one_expert(codes, scales), H, I, xq, np.zeros((2, 1), np.int32), rel)[:, 0]
+    y, _ = oracle.expert_forward(codes, scales, H, I, xq, h_mode=1)
+    rng = np.random.default_rng(6)
+    for m in range(2):
+        o0 = Wd @ oracle.quant_mxfp8(h[m])[2]
+        assert np.allclose(o0, y[m], rtol=1e-13, atol=1e-13 * np.abs(o0).max())
+        for trial in range(150):
+            hh = h[m] + r[m] * rng.choice([-1.0, 1.0, 0.0], size=I) * rng.uniform(0.5, 1.0, size=I)
+            dq = np.abs(Wd @ oracle.quant_mxfp8(hh)[2] - o0)
+            assert np.all(dq <= amb[m] * (1 + 1e-12) + 1e-14 * np.abs(o0).max())
+        assert np.mean(amb[m] > 0) > 0.5
