@@ -152,9 +152,10 @@ moe_status moe_route_topk(const uint16_t *x, int M, int H, const uint16_t *Wr, i
  * kernel) lives in one static device array of the library, about 1.5 MiB, that
  * every GPU which loads the library keeps until the process exits.  Limit: M * E <= 131072 (else MOE_ERR_UNSUPPORTED_SHAPE).
  * The first call on a device looks up the array's device address (with that
- * device current), so make that first call before any stream capture.  All calls
- * share the array: calls that overlap on the GPU (other streams, other threads)
- * race and must be serialised by the caller.  The status word is cleared at the
+ * device current), so make that first call before any stream capture; host threads
+ * that make their first calls at the same time look it up alike (the per-device
+ * entries are atomic).  All calls share the array: calls that overlap on the GPU
+ * (other streams, other threads) race and must be serialised by the caller.  The status word is cleared at the
  * start of every call; device-detected errors are recorded there but not
  * returned -- use moe_route_topk with a workspace to read them. */
 moe_status moe_route_topk_static(const uint16_t *x, int M, int H, const uint16_t *Wr, int E,
@@ -210,12 +211,42 @@ moe_status moe_expert_forward_grouped(const moe_pool *pool, const uint16_t *x, i
                                       void *partial, int partial_dtype,
                                       void *ws, size_t ws_bytes, moe_stream_t stream);
 
+/* Diagnostics of the expert-major path: after moe_expert_forward_grouped(T, k) with
+ * workspace `ws` and its `offsets` output, copy the MXFP8 h that the gate/up GEMM
+ * wrote for W_d, in sorted row order: hq [T*k][I] E4M3 codes (16-byte aligned) and
+ * hs [T*k][I/32] E8M0 scale bytes; h[r][i] = E4M3(hq[r][i]) * 2^(hs[r][i/32] - 127).
+ * Rows past offsets[E] (pairs with an invalid expert index) are left untouched.  It
+ * lets a caller check each MXFP8 decision on h against a reference; the workspace
+ * must not have been reused since the grouped call. */
+moe_status moe_grouped_read_h(const moe_pool *pool, int T, int k, const int32_t *offsets, const void *ws,
+                              size_t ws_bytes, uint8_t *hq, uint8_t *hs, moe_stream_t stream);
+
 /* Weighted combine of the grouped path: y[t] = sum_{j<k} w[t,j] *
  * partial[inv_perm[t*k+j]] (+ residual[t]), summed in slot order j in fp32 and
  * rounded to bf16.  No atomics: the result is deterministic. */
 moe_status moe_combine(const void *partial, int partial_dtype, const int32_t *inv_perm,
                        const float *w, int T, int k, int H, const uint16_t *residual,
                        uint16_t *y, moe_stream_t stream);
+
+/* ------------------------------------------------------------- test support
+ * Failure detection without a GPU fault.  Every device wait of the library (the
+ * mbarrier waits of the copy/MMA pipelines, the grid barrier of the single-token
+ * decode kernel) is bounded; on expiry the kernel records MOE_ERR_TIMEOUT in the
+ * status word, stops issuing work, waits (bounded) for its own copies in flight,
+ * frees any TMEM it holds and returns.  These two calls let a test make one such
+ * wait run out.  Both are process-wide; call them with no work of the library in
+ * flight (the wait limit is written to the current device with a synchronous copy).
+ *
+ * moe_debug_set_wait_limit: bound every wait by `ns` nanoseconds (0 restores the
+ * default of 1 s).  MOE_ERR_CUDA if the copy fails. */
+moe_status moe_debug_set_wait_limit(uint64_t ns);
+
+/* moe_debug_set_barrier_extra: make the grid barrier of the single-token decode
+ * kernel wait for `extra` (0..1024) arrivals beyond its grid, which never come, so
+ * that the barrier's bounded wait runs out (0 turns the hook off).  The call then
+ * writes no y, records MOE_ERR_TIMEOUT, and leaves the workspace's counters zero, so
+ * the next call on the same workspace (after moe_check_status) runs normally. */
+moe_status moe_debug_set_barrier_extra(int extra);
 
 /* ----------------------------------------------------------------- tracing
  * Between moe_trace_begin(name) and moe_trace_end(), every launch of the named

@@ -34,7 +34,8 @@ EXPORTED = [
     "moe_workspace_size", "moe_clear_status", "moe_check_status", "moe_status_string",
     "moe_route_topk", "moe_route_topk_static", "moe_route_topk_prescaled", "moe_expert_forward_decode",
     "moe_prescale",
-    "moe_expert_forward_grouped", "moe_combine", "moe_trace_begin", "moe_trace_end",
+    "moe_expert_forward_grouped", "moe_grouped_read_h", "moe_combine", "moe_trace_begin", "moe_trace_end",
+    "moe_debug_set_wait_limit", "moe_debug_set_barrier_extra",
 ]
 
 
@@ -74,7 +75,10 @@ def lib() -> ctypes.CDLL:
             "moe_prescale": (_i, [_vp, _i, _i, _vp, _vp]),
             "moe_expert_forward_grouped": (_i, [_vp, _vp, _i, _vp, _i, _i, _vp, _vp, _vp, _vp, _i, _vp, _sz,
                                                 _vp]),
+            "moe_grouped_read_h": (_i, [_vp, _i, _i, _vp, _vp, _sz, _vp, _vp, _vp]),
             "moe_combine": (_i, [_vp, _i, _vp, _vp, _i, _i, _i, _vp, _vp, _vp]),
+            "moe_debug_set_wait_limit": (_i, [_u64]),
+            "moe_debug_set_barrier_extra": (_i, [_i]),
             "moe_trace_begin": (_i, [ctypes.c_char_p]),
             "moe_trace_end": (_i, [ctypes.POINTER(_i), ctypes.POINTER(ctypes.c_double)]),
         }
@@ -298,6 +302,17 @@ def moe_expert_forward_grouped(pool: Pool, x: torch.Tensor, idx: torch.Tensor, a
     return out
 
 
+def moe_grouped_read_h(pool: Pool, T: int, k: int, offsets: torch.Tensor, ws: torch.Tensor, stream=None):
+    """The MXFP8 h of the last grouped call on `ws`, in sorted row order:
+    (codes uint8 [T*k, I], scale bytes uint8 [T*k, I/32])."""
+    _need(offsets, torch.int32, "offsets")
+    hq = torch.zeros((T * k, pool.I), dtype=torch.uint8, device=ws.device)
+    hs = torch.zeros((T * k, pool.I // 32), dtype=torch.uint8, device=ws.device)
+    _check(lib().moe_grouped_read_h(pool.handle, T, k, _ptr(offsets), _ptr(ws), ws.numel(), _ptr(hq), _ptr(hs),
+                                    _stream(stream)), "moe_grouped_read_h")
+    return hq, hs
+
+
 def moe_combine(partial: torch.Tensor, inv_perm: torch.Tensor, w: torch.Tensor, residual: torch.Tensor | None = None,
                 y: torch.Tensor | None = None, stream=None):
     _need(inv_perm, torch.int32, "inv_perm")
@@ -309,6 +324,20 @@ def moe_combine(partial: torch.Tensor, inv_perm: torch.Tensor, w: torch.Tensor, 
     _check(lib().moe_combine(_ptr(partial), pdt, _ptr(inv_perm), _ptr(w), T, k, H, _ptr(residual), _ptr(y),
                              _stream(stream)), "moe_combine")
     return y
+
+
+# ---------------------------------------------------------- test support
+
+
+def moe_debug_set_wait_limit(ns: int):
+    """Bound every device wait of the library by `ns` nanoseconds (0: the 1 s default)."""
+    _check(lib().moe_debug_set_wait_limit(ns), "moe_debug_set_wait_limit")
+
+
+def moe_debug_set_barrier_extra(extra: int):
+    """Make the single-token decode kernel's grid barrier wait for `extra` arrivals
+    that never come (0 turns the hook off)."""
+    _check(lib().moe_debug_set_barrier_extra(extra), "moe_debug_set_barrier_extra")
 
 
 # --------------------------------------------------------------- tracing

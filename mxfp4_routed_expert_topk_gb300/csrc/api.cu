@@ -270,4 +270,28 @@ moe_status moe_combine(const void *partial, int partial_dtype, const int32_t *in
     return cuda_status(launch_combine(partial, partial_dtype, inv_perm, w, T, k, H, residual, y, (cudaStream_t)stream));
 }
 
+moe_status moe_grouped_read_h(const moe_pool *pool, int T, int k, const int32_t *offsets, const void *ws,
+                              size_t ws_bytes, uint8_t *hq, uint8_t *hs, moe_stream_t stream) {
+    if (pool == nullptr || offsets == nullptr || ws == nullptr || hq == nullptr || hs == nullptr)
+        return MOE_ERR_INVALID_ARG;
+    if (T < 0 || k < 1 || k > kMaxK || k > pool->v.E) return MOE_ERR_INVALID_ARG;
+    if (pool->v.I % 64 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned(ws, 256) || !aligned(hq, 16)) return MOE_ERR_INVALID_ARG;
+    if (ws_bytes < grouped_workspace_bytes(pool->v.E, pool->v.H, pool->v.I, T, k)) return MOE_ERR_WORKSPACE;
+    return cuda_status(launch_read_h(pool->v, T, k, offsets, ws, hq, hs, (cudaStream_t)stream));
+}
+
+moe_status moe_debug_set_wait_limit(uint64_t ns) {
+    const uint64_t lim = ns == 0 ? 1000ull * 1000ull * 1000ull : ns;
+    if (set_wait_limit_decode_fused(lim) != cudaSuccess) return MOE_ERR_CUDA;
+    if (set_wait_limit_gemm(lim) != cudaSuccess) return MOE_ERR_CUDA;
+    return MOE_OK;
+}
+
+moe_status moe_debug_set_barrier_extra(int extra) {
+    if (extra < 0 || extra > 1024) return MOE_ERR_INVALID_ARG;
+    set_barrier_extra((unsigned int)extra);
+    return MOE_OK;
+}
+
 }  // extern "C"

@@ -301,7 +301,7 @@ __global__ void prescale_kernel(const uint16_t *__restrict__ x, int H, uint16_t 
     }
 }
 
-int g_num_sms = 0;
+PerDevice g_num_sms(0);
 
 }  // namespace
 
@@ -315,10 +315,10 @@ size_t decode_workspace_bytes(int E, int H, int I, int M, int k) {
 cudaError_t launch_decode(const PoolView &v, const uint16_t *x, int M, const int32_t *idx, const float *w, int k,
                           const uint16_t *residual, uint16_t *y, void *ws, cudaStream_t st) {
     if (M == 0) return cudaSuccess;
-    if (g_num_sms == 0) {
-        int dev = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev);
+    int num_sms = 0;
+    {
+        const cudaError_t e = device_attr(cudaDevAttrMultiProcessorCount, g_num_sms, &num_sms);
+        if (e != cudaSuccess) return e;
     }
     if (M == 1) {
         const cudaError_t e = launch_decode_fused(v, x, idx, w, k, residual, y, ws, st);
@@ -337,14 +337,14 @@ cudaError_t launch_decode(const PoolView &v, const uint16_t *x, int M, const int
     const int umax = P < v.E ? P : v.E;
     const long long tasks = (long long)umax * (v.I / 2);
     long long blocks = (tasks + 7) / 8;
-    const long long cap = (long long)g_num_sms * 4;
+    const long long cap = (long long)num_sms * 4;
     if (blocks > cap) blocks = cap;
     {
         TraceScope trace_scope("decode_gateup", st);
         decode_gateup_kernel<<<(unsigned)blocks, kThreads, 0, st>>>(v, M, k, d);
     }
     // two CTAs per SM, each a block of consecutive output rows (a multiple of 8)
-    int rows = (v.H + 2 * g_num_sms - 1) / (2 * g_num_sms);
+    int rows = (v.H + 2 * num_sms - 1) / (2 * num_sms);
     rows = (rows + 7) / 8 * 8;
     // pairs staged per pass: at most 32, and at most ~200 KB of f16 rows
     int group = P < kDownPairGroup ? P : kDownPairGroup;
@@ -352,7 +352,7 @@ cudaError_t launch_decode(const PoolView &v, const uint16_t *x, int M, const int
     if (group > fit) group = fit;
     if (group < 1) return cudaErrorInvalidValue;
     const size_t smem = (size_t)group * v.Ip * 2 + (size_t)M * rows * 4;
-    static int smem_down = 0;
+    static PerDevice smem_down(0);
     cudaError_t e = ensure_dynamic_smem(decode_down_kernel, smem, smem_down);
     if (e != cudaSuccess) return e;
     {

@@ -45,6 +45,8 @@ struct FusedArgs {
     float *h;            // [k][8][I/32] float4 workspace (see h_slot)
     float *hmax;         // [kMaxKF][G] workspace: each CTA's max |h| per pair
     StatusWord *st;      // grid barrier and exit counters
+    unsigned int barrier_count;  // arrivals the grid barrier waits for: G (more only under
+                                 // moe_debug_set_barrier_extra, to make the wait run out)
     uint32_t slot_bytes;
     int R;
     uint32_t sb_stride;  // bytes per pair of phase-B scale rows in a slot
@@ -354,7 +356,7 @@ __global__ void __launch_bounds__(kThreadsF, 1) decode_fused_kernel(const FusedA
     named_barrier(1, kCW * 32);
     if (threadIdx.x < kMaxKF) a.hmax[threadIdx.x * G + b] = __uint_as_float(samax[threadIdx.x]);
     // every consumer warp takes part, aborted or not, so the named barriers match
-    ok = grid_barrier(&a.st->pad[kStGridBarrier], (unsigned)G, 1, kCW * 32, a.st, 0x300u, abort_flag);
+    ok = grid_barrier(&a.st->pad[kStGridBarrier], a.barrier_count, 1, kCW * 32, a.st, 0x300u, abort_flag);
 
     // ---- phase B: each lane owns up to two (pair, 32-block) combinations of h, in
     // registers as f16 scaled by a per-pair power of two (from the max |h| of the
@@ -486,12 +488,17 @@ __global__ void __launch_bounds__(kThreadsF, 1) decode_fused_kernel(const FusedA
     }
 }
 
-int g_sms = 0;
-int g_smem_max = 0;
-int g_grid = -1;   // co-resident CTAs of the fused kernel (0: unusable)
-int g_smem_set = 0;
+PerDevice g_sms(0);
+PerDevice g_smem_max(0);
+PerDevice g_grid(-1);  // co-resident CTAs of the fused kernel (0: unusable), per device
+PerDevice g_smem_set(0);
+unsigned int g_barrier_extra = 0;  // test hook: arrivals the grid barrier waits for beyond G
 
 }  // namespace
+
+cudaError_t set_wait_limit_decode_fused(uint64_t ns) { return set_wait_limit_here(ns); }
+
+void set_barrier_extra(unsigned int extra) { g_barrier_extra = extra; }
 
 // Launch the fused kernel if the shape allows it; cudaErrorNotSupported otherwise
 // (the caller then uses the general decode kernels).
@@ -499,11 +506,11 @@ cudaError_t launch_decode_fused(const PoolView &v, const uint16_t *x, const int3
                                 const uint16_t *residual, uint16_t *y, void *ws, cudaStream_t st) {
     if (!(k <= kMaxKF && v.H <= 32 * 32 * kMaxJ && v.H % 512 == 0 && v.I <= 64 * 32))
         return cudaErrorNotSupported;
-    if (g_sms == 0) {
-        int dev = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&g_sms, cudaDevAttrMultiProcessorCount, dev);
-    }
+    int dev = 0, sms = 0, smem_max = 0;
+    cudaError_t e = current_device(&dev);
+    if (e != cudaSuccess) return e;
+    if ((e = device_attr(cudaDevAttrMultiProcessorCount, g_sms, &sms)) != cudaSuccess) return e;
+    if ((e = device_attr(cudaDevAttrMaxSharedMemoryPerBlockOptin, g_smem_max, &smem_max)) != cudaSuccess) return e;
     FusedArgs fa;
     fa.v = v;
     fa.k = k;
@@ -525,31 +532,29 @@ cudaError_t launch_decode_fused(const PoolView &v, const uint16_t *x, const int3
     fa.sb_stride = sb_of(R);
     const uint32_t slot_need = slotA > stageB(R) ? slotA : stageB(R);
     fa.slot_bytes = (slot_need + 127) / 128 * 128;
-    if (g_smem_max == 0) {
-        int dev = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&g_smem_max, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-    }
     // everything but the token / preloaded-scale region
     const size_t head = (size_t)kSlots * fa.slot_bytes + 8 * sizeof(uint64_t) + (size_t)kCW * kMaxRowsCta * sizeof(float) +
                         2 * kItems * 2 * sizeof(float2) + (4 * kMaxKF + 4) * sizeof(int);
     // the W_d scale rows of a CTA's output rows (at most ceil(H / SMs) of them), one
     // 16-byte aligned span per pair, if they fit in shared memory
-    const int rows_max = (v.H + g_sms - 1) / g_sms;
+    const int rows_max = (v.H + sms - 1) / sms;
     const uint32_t sp = (uint32_t)((rows_max * v.lds_d + 15) / 16 * 16 + 32);
     const size_t tok = (size_t)v.H * 2;
-    fa.sp_stride = head + std::max(tok, (size_t)k * sp) <= (size_t)g_smem_max ? sp : 0u;
+    fa.sp_stride = head + std::max(tok, (size_t)k * sp) <= (size_t)smem_max ? sp : 0u;
     fa.tail_bytes = (uint32_t)std::max(tok, (size_t)k * fa.sp_stride);
     const size_t smem = head + fa.tail_bytes;
-    cudaError_t e = ensure_dynamic_smem(decode_fused_kernel, smem, g_smem_set);
+    e = ensure_dynamic_smem(decode_fused_kernel, smem, g_smem_set);
     if (e != cudaSuccess) return e;
-    if (g_grid < 0) {
+    int grid = g_grid.v[dev].load(std::memory_order_relaxed);
+    if (grid < 0) {
         int per_sm = 0;
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_fused_kernel, kThreadsF, smem);
         if (e != cudaSuccess) return e;
-        g_grid = per_sm >= 1 ? g_sms : 0;
+        grid = per_sm >= 1 ? sms : 0;
+        g_grid.v[dev].store(grid, std::memory_order_relaxed);
     }
-    fa.G = g_grid;
+    fa.G = grid;
+    fa.barrier_count = (unsigned int)grid + g_barrier_extra;
     if (fa.G <= 0 || fa.G > kMaxFusedGrid || (v.H + fa.G - 1) / fa.G > kMaxRowsCta) return cudaErrorNotSupported;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(fa.G);

@@ -703,11 +703,11 @@ uint32_t pow2_at_least(uint32_t v) {
     return p;
 }
 
-int g_smem_max = 0;
-int g_sms = 0;
+PerDevice g_smem_max(0);
+PerDevice g_sms(0);
 
-int g_smem_set_384 = 0;
-int g_smem_set_192 = 0;
+PerDevice g_smem_set_384(0);
+PerDevice g_smem_set_192(0);
 
 // One grouped GEMM launch (args complete but for the shape fields set here).  The
 // kernel's shape: narrow tiles (BN <= 64, and the gate/up GEMM at BN <= 96) run two
@@ -719,9 +719,13 @@ int g_smem_set_192 = 0;
 cudaError_t launch_one(GemmArgs ga, const uint8_t *a_base, int a_k, int a_rows, uint64_t a_ld, int E, const uint8_t *b_base,
                        int b_k, int b_rows, int nexp, const char *trace_name, cudaStream_t stream) {
     const int BN = ga.BN, nsfb = ga.nsfb;
+    int smem_max = 0, sms = 0;
+    cudaError_t e = device_attr(cudaDevAttrMaxSharedMemoryPerBlockOptin, g_smem_max, &smem_max);
+    if (e != cudaSuccess) return e;
+    if ((e = device_attr(cudaDevAttrMultiProcessorCount, g_sms, &sms)) != cudaSuccess) return e;
     const bool two = BN <= 64 || (BN <= 96 && ga.mode == 1);
     const int tpi = two ? 1 : (BN <= 96 ? 2 : 1);
-    const uint32_t smem_cap = two ? (uint32_t)(g_smem_max / 2 - 1024) : (uint32_t)g_smem_max;
+    const uint32_t smem_cap = two ? (uint32_t)(smem_max / 2 - 1024) : (uint32_t)smem_max;
     const uint32_t tmem_cap = two ? 256u : 512u;
     // as many pipeline stages as fit the CTA's share of shared memory and TMEM
     int ns = kMaxStages;
@@ -730,8 +734,8 @@ cudaError_t launch_one(GemmArgs ga, const uint8_t *a_base, int a_k, int a_rows, 
     const uint32_t tmem_cols = pow2_at_least(tmem_need(ns));
     if (tmem_cols > tmem_cap || GemmSmemLayout(BN, ns, tpi).total + 1024 > smem_cap) return cudaErrorNotSupported;
     const size_t smem = GemmSmemLayout(BN, ns, tpi).total + 1024;  // alignment slack
-    cudaError_t e = two ? ensure_dynamic_smem(grouped_gemm_kernel<192>, smem, g_smem_set_192)
-                        : ensure_dynamic_smem(grouped_gemm_kernel<384>, smem, g_smem_set_384);
+    e = two ? ensure_dynamic_smem(grouped_gemm_kernel<192>, smem, g_smem_set_192)
+            : ensure_dynamic_smem(grouped_gemm_kernel<384>, smem, g_smem_set_384);
     if (e != cudaSuccess) return e;
     ga.ns = ns;
     ga.tpi = tpi;
@@ -742,13 +746,15 @@ cudaError_t launch_one(GemmArgs ga, const uint8_t *a_base, int a_k, int a_rows, 
     const int items = nexp * ((ga.nmt + tpi - 1) / tpi);
     TraceScope trace_scope(trace_name, stream);
     if (two)
-        grouped_gemm_kernel<192><<<std::min(2 * g_sms, items), 192, smem, stream>>>(mA, mB, ga);
+        grouped_gemm_kernel<192><<<std::min(2 * sms, items), 192, smem, stream>>>(mA, mB, ga);
     else
-        grouped_gemm_kernel<384><<<std::min(g_sms, items), 384, smem, stream>>>(mA, mB, ga);
+        grouped_gemm_kernel<384><<<std::min(sms, items), 384, smem, stream>>>(mA, mB, ga);
     return cudaGetLastError();
 }
 
 }  // namespace
+
+cudaError_t set_wait_limit_gemm(uint64_t ns) { return set_wait_limit_here(ns); }
 
 cudaError_t launch_grouped_gemms(const PoolView &v, int T, int k, const int32_t *offsets, const GroupedWs &g,
                                  void *partial, int partial_dtype, StatusWord *st, cudaStream_t stream, int nparts) {
@@ -764,12 +770,6 @@ cudaError_t launch_grouped_gemms(const PoolView &v, int T, int k, const int32_t 
     if (BN == 0) return cudaErrorNotSupported;
     if (BN != g.BN) return cudaErrorInvalidValue;
     const int nsfb = g.nsfb;
-    if (g_smem_max == 0) {
-        int dev = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&g_smem_max, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-        cudaDeviceGetAttribute(&g_sms, cudaDevAttrMultiProcessorCount, dev);
-    }
     GemmArgs ga;
     ga.E = v.E;
     ga.pool = v.base;

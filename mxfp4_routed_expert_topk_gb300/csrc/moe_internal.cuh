@@ -7,6 +7,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "../../include/moe.h"
 
 namespace moe {
@@ -132,13 +134,55 @@ struct TraceScope {
     ~TraceScope() { trace_post(name, st); }
 };
 
-// Raise a kernel's dynamic shared memory limit to `bytes` if needed (per kernel,
-// remembered in `cur`).  Returns the error of the attribute call.
+// Values the library caches per device: device attributes and each kernel's raised
+// dynamic shared-memory limit (a function attribute belongs to one device), so that
+// one process may use several devices.  Entries are atomics: host threads making
+// their first calls on a device at the same time store the same value.
+constexpr int kMaxDevices = 64;
+struct PerDevice {
+    std::atomic<int> v[kMaxDevices];
+    explicit PerDevice(int init) {
+        for (auto &a : v) a.store(init, std::memory_order_relaxed);
+    }
+};
+
+inline cudaError_t current_device(int *dev) {
+    cudaError_t e = cudaGetDevice(dev);
+    if (e != cudaSuccess) return e;
+    return (*dev >= 0 && *dev < kMaxDevices) ? cudaSuccess : cudaErrorInvalidDevice;
+}
+
+// Attribute `attr` of the current device, read once per device (cache: init 0).
+inline cudaError_t device_attr(cudaDeviceAttr attr, PerDevice &cache, int *out) {
+    int dev = 0;
+    cudaError_t e = current_device(&dev);
+    if (e != cudaSuccess) return e;
+    int v = cache.v[dev].load(std::memory_order_relaxed);
+    if (v == 0) {
+        e = cudaDeviceGetAttribute(&v, attr, dev);
+        if (e != cudaSuccess) return e;
+        cache.v[dev].store(v, std::memory_order_relaxed);
+    }
+    *out = v;
+    return cudaSuccess;
+}
+
+// Raise a kernel's dynamic shared memory limit on the current device to `bytes` if
+// needed (per kernel and device, remembered in `cur`, init 0).  Returns the error of
+// the attribute call.
 template <typename K>
-inline cudaError_t ensure_dynamic_smem(K kernel, size_t bytes, int &cur) {
-    if ((int)bytes <= cur || bytes <= 48 * 1024) return cudaSuccess;
-    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
-    if (e == cudaSuccess) cur = (int)bytes;
+inline cudaError_t ensure_dynamic_smem(K kernel, size_t bytes, PerDevice &cur) {
+    if (bytes <= 48 * 1024) return cudaSuccess;
+    int dev = 0;
+    cudaError_t e = current_device(&dev);
+    if (e != cudaSuccess) return e;
+    if ((int)bytes <= cur.v[dev].load(std::memory_order_relaxed)) return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    if (e == cudaSuccess) {
+        int old = cur.v[dev].load(std::memory_order_relaxed);
+        while (old < (int)bytes && !cur.v[dev].compare_exchange_weak(old, (int)bytes, std::memory_order_relaxed)) {
+        }
+    }
     return e;
 }
 
@@ -169,11 +213,20 @@ cudaError_t launch_decode_fused(const PoolView &v, const uint16_t *x, const int3
 
 cudaError_t launch_prescale(const uint16_t *x, int M, int H, uint16_t *out, cudaStream_t st);
 
+// Test support (moe_debug_*): the wait limit of the translation units whose kernels
+// wait, and extra arrivals the fused decode kernel's grid barrier waits for.
+cudaError_t set_wait_limit_decode_fused(uint64_t ns);
+cudaError_t set_wait_limit_gemm(uint64_t ns);
+void set_barrier_extra(unsigned int extra);
+
 size_t grouped_workspace_bytes(int E, int H, int I, int T, int k);
 cudaError_t launch_grouped(const PoolView &v, const uint16_t *x, int T, const int32_t *idx, int k,
                            int act_mode, int32_t *perm, int32_t *inv_perm, int32_t *offsets,
                            void *partial, int partial_dtype, void *ws, cudaStream_t st);
 cudaError_t launch_combine(const void *partial, int partial_dtype, const int32_t *inv_perm, const float *w,
                            int T, int k, int H, const uint16_t *residual, uint16_t *y, cudaStream_t st);
+// Diagnostics: the MXFP8 h of the last grouped call on `ws`, in sorted row order.
+cudaError_t launch_read_h(const PoolView &v, int T, int k, const int32_t *offsets, const void *ws, uint8_t *hq,
+                          uint8_t *hs, cudaStream_t st);
 
 }  // namespace moe

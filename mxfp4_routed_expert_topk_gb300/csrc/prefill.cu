@@ -443,7 +443,43 @@ bool combine4_ok(const void *partial, int partial_dtype, int H, const uint16_t *
            (residual == nullptr || (uintptr_t)residual % 8 == 0);
 }
 
+// Diagnostics: MXFP8 h of sorted row r and 32-block b as the gate/up epilogue wrote
+// it (codes [P][I], and the scale byte from the tile-ordered blocks).  One thread
+// per (row, block); the row's expert is the last e with offsets[e] <= r.
+__global__ void read_h_kernel(int E, int I, const int32_t *__restrict__ offsets, const int32_t *__restrict__ tile_off,
+                              int BN, int nsfb, const uint8_t *__restrict__ hq_ws, const uint8_t *__restrict__ hs_ws,
+                              uint8_t *__restrict__ hq, uint8_t *__restrict__ hs) {
+    const int nb = I / 32;
+    const size_t gid = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int P = offsets[E];
+    if (gid >= (size_t)P * nb) return;
+    const int r = (int)(gid / nb), b = (int)(gid % nb);
+    int lo = 0, hi = E - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) / 2;
+        if (offsets[mid] <= r) lo = mid;
+        else hi = mid - 1;
+    }
+    const RowTile rt = row_tile(lo, r - offsets[lo], tile_off, BN);
+    const int ip = (I + 127) / 128 * 128;
+    hs[(size_t)r * nb + b] = hs_ws[sf_tile_word(rt.tile, ip / 128, nsfb, b >> 2, rt.col) + (b & 3)];
+    const uint4 *src = reinterpret_cast<const uint4 *>(hq_ws + (size_t)r * I + 32 * b);
+    uint4 *dst = reinterpret_cast<uint4 *>(hq + (size_t)r * I + 32 * b);
+    dst[0] = src[0];
+    dst[1] = src[1];
+}
+
 }  // namespace
+
+cudaError_t launch_read_h(const PoolView &v, int T, int k, const int32_t *offsets, const void *ws, uint8_t *hq,
+                          uint8_t *hs, cudaStream_t st) {
+    const GroupedWs g = grouped_ws_layout(const_cast<void *>(ws), v.E, v.H, v.I, T, k);
+    const size_t n = (size_t)T * k * (v.I / 32);
+    if (n == 0) return cudaSuccess;
+    read_h_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(v.E, v.I, offsets, g.tile_off, g.BN, g.nsfb, g.hq, g.hs,
+                                                               hq, hs);
+    return cudaGetLastError();
+}
 
 size_t grouped_workspace_bytes(int E, int H, int I, int T, int k) {
     return grouped_ws_layout(nullptr, E, H, I, T, k).end;

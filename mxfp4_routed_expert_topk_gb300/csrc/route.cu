@@ -1055,7 +1055,7 @@ template <int J>
 cudaError_t launch_route_j(const uint16_t *x, int M, int H, const uint16_t *Wr, int E, const float *skew, int k,
                            int32_t *idx, float *w, const RouteWs &r, size_t smem1, StatusWord *stw, cudaStream_t st,
                            uint16_t *xhat) {
-    static int smem_single = 0;
+    static PerDevice smem_single(0);
     dim3 g1((E + kLogitExperts - 1) / kLogitExperts, (M + kLogitTokens - 1) / kLogitTokens);
     if (M == 1) {
         cudaError_t e = ensure_dynamic_smem(route_single_kernel<J>, smem1, smem_single);
@@ -1078,7 +1078,7 @@ cudaError_t launch_route_j(const uint16_t *x, int M, int H, const uint16_t *Wr, 
         return cudaGetLastError();
     }
     if (M >= kTiledMinTokens && H % 128 == 0) {
-        static int smem_tiled = 0;
+        static PerDevice smem_tiled(0);
         cudaError_t e = ensure_dynamic_smem(route_tiled_kernel, kTiledSmem, smem_tiled);
         if (e != cudaSuccess) return e;
         TraceScope trace_scope("route_logits", st);
@@ -1114,7 +1114,7 @@ cudaError_t launch_route(const uint16_t *x, int M, int H, const uint16_t *Wr, in
     const int nt = M < kLogitTokens ? M : kLogitTokens;
     if ((size_t)nt * H * sizeof(uint16_t) > 200 * 1024) return cudaErrorInvalidValue;
     const size_t smem1 = (size_t)nt * H * sizeof(uint16_t);
-    static int smem_logits = 0;
+    static PerDevice smem_logits(0);
     cudaError_t e = ensure_dynamic_smem(route_logits_kernel, smem1, smem_logits);
     if (e != cudaSuccess) return e;
     StatusWord *stw = reinterpret_cast<StatusWord *>(ws);

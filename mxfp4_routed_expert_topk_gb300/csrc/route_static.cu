@@ -18,28 +18,27 @@ constexpr size_t kStaticRouteMaxME = 131072;
 // logits and bounds, plus the row norms of x and W_r (at most kStaticRouteMaxME + 4096)
 constexpr size_t kStaticScratchBytes = 256 + 2 * kStaticRouteMaxME * sizeof(float) +
                                        (kStaticRouteMaxME + 4096) * sizeof(float) + 1024;
-constexpr int kMaxDevices = 64;
-
 // Every GPU that loads this library holds this array until the process exits.
 __device__ __align__(256) unsigned char g_route_scratch[kStaticScratchBytes];
 
-// Device address of g_route_scratch per device, looked up once per device.
-void *g_scratch_ptr[kMaxDevices] = {nullptr};
+// Device address of g_route_scratch per device, looked up once per device.  Atomic
+// entries: two host threads making their first call on one device at the same time
+// both look the address up and store the same value.
+std::atomic<void *> g_scratch_ptr[moe::kMaxDevices];
 
 cudaError_t scratch_for_current_device(void **out) {
     int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    cudaError_t e = moe::current_device(&dev);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-    if (g_scratch_ptr[dev] == nullptr) {
+    void *p = g_scratch_ptr[dev].load(std::memory_order_relaxed);
+    if (p == nullptr) {
         // The symbol's host-side name is only a stand-in; the kernels need the
         // device address, valid for the current device.
-        void *p = nullptr;
         e = cudaGetSymbolAddress(&p, g_route_scratch);
         if (e != cudaSuccess) return e;
-        g_scratch_ptr[dev] = p;
+        g_scratch_ptr[dev].store(p, std::memory_order_relaxed);
     }
-    *out = g_scratch_ptr[dev];
+    *out = p;
     return cudaSuccess;
 }
 

@@ -8,8 +8,16 @@
 
 namespace moe {
 
-// Every wait in the library gives up after this long and reports MOE_ERR_TIMEOUT.
-constexpr uint64_t kWaitLimitNs = 1000ull * 1000ull * 1000ull;  // 1 s
+// Every wait in the library gives up after g_wait_limit_ns nanoseconds and reports
+// MOE_ERR_TIMEOUT: 1 s unless moe_debug_set_wait_limit changed it.  Without relocatable
+// device code each translation unit that waits holds its own copy of the variable,
+// set through set_wait_limit_here() from a wrapper in that unit.
+constexpr uint64_t kDefaultWaitLimitNs = 1000ull * 1000ull * 1000ull;  // 1 s
+static __device__ uint64_t g_wait_limit_ns = kDefaultWaitLimitNs;
+
+static inline cudaError_t set_wait_limit_here(uint64_t ns) {
+    return cudaMemcpyToSymbol(g_wait_limit_ns, &ns, sizeof(ns));
+}
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -58,13 +66,13 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
 }
 
 // Wait for the phase of parity `parity` to complete; false (and the status word
-// set to MOE_ERR_TIMEOUT with `where`) if it does not within kWaitLimitNs.
+// set to MOE_ERR_TIMEOUT with `where`) if it does not within the wait limit.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, StatusWord *st, unsigned where) {
     if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = global_timer_ns();
+    const uint64_t t0 = global_timer_ns(), lim = g_wait_limit_ns;
     for (uint32_t it = 0;; it++) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 63u) == 63u && global_timer_ns() - t0 > kWaitLimitNs) {
+        if ((it & 63u) == 63u && global_timer_ns() - t0 > lim) {
             set_status(st, MOE_ERR_TIMEOUT, where);
             return false;
         }
@@ -77,11 +85,11 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, Status
 __device__ __forceinline__ bool mbar_wait_or_abort(uint64_t *bar, uint32_t parity, StatusWord *st, unsigned where,
                                                    const int *abort_flag) {
     if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = global_timer_ns();
+    const uint64_t t0 = global_timer_ns(), lim = g_wait_limit_ns;
     for (uint32_t it = 0;; it++) {
         if (mbar_try_wait(bar, parity)) return true;
         if (*(const volatile int *)abort_flag) return false;
-        if ((it & 63u) == 63u && global_timer_ns() - t0 > kWaitLimitNs) {
+        if ((it & 63u) == 63u && global_timer_ns() - t0 > lim) {
             set_status(st, MOE_ERR_TIMEOUT, where);
             return false;
         }
@@ -129,7 +137,7 @@ __device__ __forceinline__ void red_release_gpu_add(unsigned int *p, unsigned in
 // threads of the calling CTA that take part (named barrier `bar_id`; thread 0 of
 // the CTA must be one of them).  The counter is zero before the launch; each of
 // the G CTAs adds 1.  A CTA that has aborted does not arrive; the others then give
-// up after kWaitLimitNs.  Returns false if this CTA aborted or timed out.
+// up after the wait limit.  Returns false if this CTA aborted or timed out.
 //
 // Ordering: the CTA's writes before the barrier precede thread 0's release add
 // (CTA barrier, then release at GPU scope); thread 0's acquire load that sees the
@@ -141,9 +149,9 @@ __device__ __forceinline__ bool grid_barrier(unsigned int *counter, unsigned int
     named_barrier(bar_id, nthreads);
     if (threadIdx.x == 0 && *(volatile int *)abort_flag == 0) {
         red_release_gpu_add(counter, 1u);
-        const uint64_t t0 = global_timer_ns();
+        const uint64_t t0 = global_timer_ns(), lim = g_wait_limit_ns;
         while (ld_acquire_gpu(counter) < G) {
-            if (global_timer_ns() - t0 > kWaitLimitNs) {
+            if (global_timer_ns() - t0 > lim) {
                 set_status(st, MOE_ERR_TIMEOUT, where);
                 *abort_flag = 1;
                 break;

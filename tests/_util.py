@@ -50,25 +50,55 @@ def bf16_to_f64(t: torch.Tensor) -> np.ndarray:
     return t.float().cpu().numpy().astype(np.float64)
 
 
-def check_close(y: np.ndarray, ref: np.ndarray, what: str = "y", amb=None):
-    """The float tolerance.  `amb` (optional, per element; tensor-core prefill path)
-    is the largest change that equally valid MXFP8 roundings of h can make to each
-    output (the oracle's error model of the GPU's fp32 h): an element may exceed
-    2e-2 * RMS by at most its amb, and such elements must be rare."""
+def bf16_half_ulp(v: np.ndarray) -> np.ndarray:
+    """Half the bf16 spacing at |v| (8 significant bits; subnormal spacing 2^-133):
+    the largest error of rounding v to bf16."""
+    a = np.abs(np.asarray(v, dtype=np.float64))
+    e = np.floor(np.log2(np.maximum(a, 2.0 ** -126)))
+    return np.exp2(np.maximum(e, -126.0) - 8)
+
+
+def check_close(y: np.ndarray, ref: np.ndarray, what: str = "y", amb=None, bf16_at=None):
+    """The float tolerance: max|y - ref| <= 2e-2 * RMS(ref), relative L1 <= 5e-3, with
+    two per-element allowances that name a stated rounding step:
+      - `amb` (tensor-core prefill path): the largest change that equally valid MXFP8
+        roundings of h can make (the oracle's error model of the GPU's fp32 h); the
+        elements that need it must be rare;
+      - `bf16_at`: the values that were rounded to the stated bf16 output format (the
+        GPU output itself, or the residual stream it was fused with); each element may
+        also differ by the half-ulp of that rounding, which at |y| beyond about
+        10 * RMS exceeds 2e-2 * RMS by itself."""
     err = np.abs(y - ref)
     rms = float(np.sqrt(np.mean(ref * ref)))
     rel = float(err.sum() / max(np.abs(ref).sum(), 1e-300))
     tol = MAX_ERR_RMS * rms
+    allow = np.zeros_like(err) if bf16_at is None else bf16_half_ulp(np.abs(bf16_at) + tol)
+    over = err - allow
     need, slack = 0.0, 0.0
     if amb is not None:
-        over = err - amb
-        assert over.max() <= tol, f"{what}: max(|err| - ambiguity) {over.max():.3e} > {MAX_ERR_RMS} * rms {rms:.3e}"
-        need = float(np.mean(err > tol))
+        assert (over - amb).max() <= tol, (
+            f"{what}: max(|err| - allowances) {(over - amb).max():.3e} > {MAX_ERR_RMS} * rms {rms:.3e}")
+        need = float(np.mean(over > tol))
         slack = float(np.max(amb) / rms) if rms > 0 else 0.0
         assert need <= SLACK_FRAC, f"{what}: {need:.2e} of the elements need the ambiguity slack"
     else:
-        assert err.max() <= tol, f"{what}: max|err| {err.max():.3e} > {MAX_ERR_RMS} * rms {rms:.3e}"
+        assert over.max() <= tol, f"{what}: max(|err| - bf16 allowance) {over.max():.3e} > {MAX_ERR_RMS} * rms {rms:.3e}"
     assert rel <= REL_L1, f"{what}: relative L1 {rel:.3e} > {REL_L1}"
     MARGINS.append({"what": what, "max_err_rms": float(err.max() / rms) if rms > 0 else 0.0, "rel_l1": rel,
-                    "max_slack_rms": slack, "slack_frac": need, "n": int(err.size)})
+                    "max_slack_rms": slack, "slack_frac": need,
+                    "bf16_frac": float(np.mean(err > tol)) if bf16_at is not None else 0.0, "n": int(err.size)})
+    return float(err.max() / rms) if rms > 0 else 0.0, rel
+
+
+def report_close(y: np.ndarray, ref: np.ndarray, what: str):
+    """Record max|err|/RMS and relative L1 of a comparison whose per-element bound does
+    not apply as such (an end-to-end pass in which each side feeds its own rounded
+    outputs forward), and assert the relative L1 bound only."""
+    err = np.abs(y - ref)
+    rms = float(np.sqrt(np.mean(ref * ref)))
+    rel = float(err.sum() / max(np.abs(ref).sum(), 1e-300))
+    MARGINS.append({"what": what, "max_err_rms": float(err.max() / rms) if rms > 0 else 0.0, "rel_l1": rel,
+                    "max_slack_rms": 0.0, "slack_frac": 0.0, "bf16_frac": float(np.mean(err > MAX_ERR_RMS * rms)),
+                    "n": int(err.size)})
+    assert rel <= REL_L1, f"{what}: relative L1 {rel:.3e} > {REL_L1}"
     return float(err.max() / rms) if rms > 0 else 0.0, rel

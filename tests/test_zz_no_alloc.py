@@ -42,9 +42,17 @@ def test_static_router_matches_workspace_router():
     s = synth.FULL
     Wr = to_dev_bf16(synth.router_bf16(synth.router_seed(0), s.E, s.H))
     skew = torch.from_numpy(synth.zipf_skew_f32(synth.skew_seed(0), s.E)).cuda()
+    # calls in a row share the array: M = 17 and 5 (the few-token logit kernel), then
+    # M = 1 (the single-kernel router with its ticket counter in the status word) and
+    # M = 128 (the many-token tiled router, whose row norms also live in the array;
+    # 128 x 896 = 114,688 <= 131,072)
     calls = [(synth.tokens_bf16(synth.TOKENS_SEED["full"], 0, 17, s.H), None),
-             (synth.tokens_bf16(synth.TOKENS_SEED["stacked"], 0, 5, s.H), skew)]
-    for xb, sk in calls:                      # two calls in a row share the array
+             (synth.tokens_bf16(synth.TOKENS_SEED["stacked"], 0, 5, s.H), skew),
+             (synth.tokens_bf16(synth.TOKENS_SEED["full"], 40, 1, s.H), None),
+             (synth.tokens_bf16(synth.TOKENS_SEED["full"], 41, 1, s.H), skew),
+             (synth.tokens_bf16(synth.TOKENS_SEED["full"], 100, 128, s.H), None),
+             (synth.tokens_bf16(synth.TOKENS_SEED["stacked"], 100, 128, s.H), skew)]
+    for xb, sk in calls:
         x = to_dev_bf16(xb)
         idx_s, w_s = _static_route(L, x, Wr, s.k, sk)
         idx_r, w_r = moe.moe_route_topk(x, Wr, s.k, sk)
