@@ -193,17 +193,35 @@ def measure_prefill(moe, torch, pool, Wr, dev, T, iters=3):
         once()
         n, tot = moe.moe_trace_end()
         kern[name] = tot / max(n, 1)
-    wbytes = s.E * expert_bytes(s.H, s.I)
-    flops = 2.0 * 3 * s.H * s.I * T * s.k
-    tflops = flops / ((kern["gemm_gateup"] + kern["gemm_down"]) / 1000.0) / 1e12
+    off = out["offsets"].cpu().numpy()
+    nexp = int(np.count_nonzero(np.diff(off)))       # experts with at least one pair
+    P = T * s.k
+    wbytes = nexp * expert_bytes(s.H, s.I)
+    flops = 2.0 * 3 * s.H * s.I * P
+    gemm_ms = kern["gemm_gateup"] + kern["gemm_down"]
+    tflops = flops / (gemm_ms / 1000.0) / 1e12
     bf16, bf16_kind = tensor_peak_tflops()
+    hbm, hbm_kind = peaks()
+    # Roofline of the two grouped GEMMs together: the MXFP4 weights of every expert with
+    # pairs, the MXFP8 rows of x read (codes + one scale byte per 32), the MXFP8 h written
+    # and read again, and the fp32 expert outputs written.  The MMA kind issued
+    # (mxf8f6f4: E2M1 x E4M3) runs at the FP8 rate, taken as the nominal 2x of the
+    # measured bf16 peak; the FP4 rate (6x) needs both operands in FP4.
+    act_bytes = P * s.H * (1 + 1 / 32) + 2 * P * s.I * (1 + 1 / 32) + P * s.H * 4
+    gbytes = wbytes + act_bytes
+    t_bytes = gbytes / (hbm * 1e9) * 1e3
+    t_flops = flops / (2.0 * bf16 * 1e12) * 1e3
+    attainable = max(t_bytes, t_flops)
     return {"tok_s": T / (ms / 1000.0), "ms": ms, "kernel_ms": kern,
-            "gemm_weight_gbs": wbytes / ((kern["gemm_gateup"] + kern["gemm_down"]) / 1000.0) / 1e9,
+            "gemm_weight_gbs": wbytes / (gemm_ms / 1000.0) / 1e9,
             "gemm_tflops": tflops,
-            # the MMA kind issued (mxf8f6f4: E2M1 x E4M3) runs at the FP8 rate; the FP4 rate
-            # needs both operands in FP4.  Peaks: bf16 (measured burst) x the nominal 2x / 6x
             "tensor_frac": {"of_fp8_rate": tflops / (2.0 * bf16), "of_fp4_rate": tflops / (6.0 * bf16),
-                            "bf16_peak_tflops": bf16, "peak_kind": bf16_kind}}
+                            "bf16_peak_tflops": bf16, "peak_kind": bf16_kind},
+            "roofline": {"kernels": "gemm_gateup + gemm_down", "bound": "hbm" if t_bytes >= t_flops else "tensor",
+                         "algorithmic_bytes": gbytes, "weight_bytes": wbytes, "flops": flops,
+                         "peak_hbm_gbs": hbm, "peak_tflops_fp8": 2.0 * bf16, "peak_kind": f"{hbm_kind} hbm, "
+                         f"{bf16_kind} bf16 x 2 (nominal fp8 ratio)", "attainable_ms": attainable,
+                         "measured_ms": gemm_ms, "frac": attainable / gemm_ms}}
 
 
 def measure_verify(moe, torch, pool, Wr, dev, M, nbatch=50, iters=3):
@@ -430,10 +448,17 @@ def run_ours(args):
         import oracle
         oracle.build()
         cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+        prev = oracle.set_threads(cores)
         secs = oracle_sample(args.ref_tokens)
+        oracle.set_threads(1)
+        n1 = max(1, args.ref_tokens // 8)
+        secs1 = oracle_sample(n1)
+        oracle.set_threads(prev)
         cpu = {"value": args.ref_tokens / secs, "unit": "layer-tokens/s", "cores": cores, "kind": "oracle",
                "sample": f"{args.ref_tokens} tokens of the workload (exact route + 16 experts, fp64), "
-                         "experts pre-generated outside the timing"}
+                         "experts pre-generated outside the timing",
+               "single_thread": {"value": n1 / secs1, "unit": "layer-tokens/s", "cores": 1,
+                                 "sample": f"{n1} tokens of the same workload on one thread"}}
     launches = 2 * NTOK * args.steps      # route_single + decode_fused per token
     prefill = {}
     if not args.no_prefill:

@@ -87,10 +87,18 @@ def lib():
         L.orc_mxfp8_ambiguity.argtypes = [_f64p, _f64p, ctypes.c_int, _f64p]
         L.orc_expert_ambiguity.restype = None
         L.orc_expert_ambiguity.argtypes = [_u8p, _u8p, ctypes.c_int, ctypes.c_int, _f64p, ctypes.c_int,
-                                           ctypes.c_double, _f64p]
+                                           ctypes.c_double, ctypes.c_int, _f64p]
+        L.orc_mx_ambiguity.restype = None
+        L.orc_mx_ambiguity.argtypes = [_f64p, _f64p, ctypes.c_int, ctypes.c_int, _f64p]
+        L.orc_e2m1_encode.restype = ctypes.c_uint
+        L.orc_e2m1_encode.argtypes = [ctypes.c_double]
+        L.orc_quant_mxfp4.restype = None
+        L.orc_quant_mxfp4.argtypes = [_f64p, ctypes.c_int, _u8p, _u8p, _f64p]
         L.orc_h_radius.restype = None
         L.orc_h_radius.argtypes = [_u8p, _u8p, ctypes.c_int, ctypes.c_int, _f64p, ctypes.c_int, ctypes.c_double,
                                    _f64p, _f64p]
+        L.orc_set_threads.restype = ctypes.c_int
+        L.orc_set_threads.argtypes = [ctypes.c_int]
         L.orc_prescale_exponent.restype = ctypes.c_int
         L.orc_prescale_exponent.argtypes = [_u16p, ctypes.c_int]
         L.orc_prescale.restype = None
@@ -100,6 +108,11 @@ def lib():
 
 
 # ------------------------------------------------------------------ primitives
+
+
+def set_threads(n: int) -> int:
+    """Threads of the oracle's OpenMP loops (n <= 0 leaves it); returns the previous count."""
+    return int(lib().orc_set_threads(n))
 
 
 def splitmix64_at(state: int, i: int) -> int:
@@ -142,6 +155,21 @@ def quant_mxfp8(v: np.ndarray):
     sb = np.empty((n + 31) // 32, dtype=np.uint8)
     deq = np.empty(n, dtype=np.float64)
     lib().orc_quant_mxfp8(v, n, codes, sb, deq)
+    return codes, sb, deq
+
+
+def e2m1_encode(v: float) -> int:
+    return int(lib().orc_e2m1_encode(float(v)))
+
+
+def quant_mxfp4(v: np.ndarray):
+    """MXFP4 (E2M1 + E8M0 per 32) of a 1-D vector: (codes, scale bytes, dequantised)."""
+    v = np.ascontiguousarray(v, dtype=np.float64)
+    n = v.size
+    codes = np.empty(n, dtype=np.uint8)
+    sb = np.empty((n + 31) // 32, dtype=np.uint8)
+    deq = np.empty(n, dtype=np.float64)
+    lib().orc_quant_mxfp4(v, n, codes, sb, deq)
     return codes, sb, deq
 
 
@@ -201,10 +229,15 @@ MMA_STEP_REL = 2.0 ** -23
 def mxfp8_ambiguity(v: np.ndarray, radius) -> np.ndarray:
     """delta[i]: change an alternative MXFP8 rounding may make when v[i] is known
     only to within radius[i] (absolute)."""
+    return mx_ambiguity(v, radius, 8)
+
+
+def mx_ambiguity(v: np.ndarray, radius, fmt: int) -> np.ndarray:
+    """As mxfp8_ambiguity for fmt 8 (MXFP8) or 4 (MXFP4)."""
     v = np.ascontiguousarray(v, dtype=np.float64)
     r = np.ascontiguousarray(np.broadcast_to(radius, v.shape), dtype=np.float64)
     d = np.empty_like(v)
-    lib().orc_mxfp8_ambiguity(v, r, v.size, d)
+    lib().orc_mx_ambiguity(v, r, v.size, fmt, d)
     return d
 
 
@@ -318,9 +351,10 @@ def sort_pairs(idx: np.ndarray, E: int):
 
 
 def pair_ambiguity(experts, H: int, I: int, x: np.ndarray, idx: np.ndarray,
-                   eps: float = MMA_STEP_REL) -> np.ndarray:
+                   eps: float = MMA_STEP_REL, fmt: int = 8) -> np.ndarray:
     """amb[m, j, o]: the largest change of expert_{idx[m,j]}(x[m])[o] that an
-    alternative (equally correct) MXFP8 rounding of its h could make."""
+    alternative (equally correct) MX rounding of its h could make (fmt 8: MXFP8,
+    4: MXFP4)."""
     M, k = idx.shape
     amb = np.zeros((M, k, H), dtype=np.float64)
     for e in sorted(set(int(v) for v in idx.ravel())):
@@ -329,17 +363,17 @@ def pair_ambiguity(experts, H: int, I: int, x: np.ndarray, idx: np.ndarray,
         xe = np.ascontiguousarray(np.stack([x[m] for m, _ in rows]), dtype=np.float64)
         ya = np.empty((len(rows), H), dtype=np.float64)
         lib().orc_expert_ambiguity(np.ascontiguousarray(codes), np.ascontiguousarray(scales), H, I, xe, len(rows),
-                                   eps, ya)
+                                   eps, fmt, ya)
         for r, (m, j) in enumerate(rows):
             amb[m, j] = ya[r]
     return amb
 
 
 def combine_ambiguity(experts, H: int, I: int, x: np.ndarray, idx: np.ndarray, w: np.ndarray,
-                      eps: float = MMA_STEP_REL) -> np.ndarray:
+                      eps: float = MMA_STEP_REL, fmt: int = 8) -> np.ndarray:
     """Per output, sum_j |w_j| * pair_ambiguity: the part of the difference between
-    two correct MXFP8-h layer outputs that rounding choices can explain."""
-    amb = pair_ambiguity(experts, H, I, x, idx, eps)
+    two correct MX-h layer outputs that rounding choices can explain."""
+    amb = pair_ambiguity(experts, H, I, x, idx, eps, fmt)
     return np.einsum("mj,mjh->mh", np.abs(w), amb)
 
 
@@ -351,21 +385,39 @@ def quant_rows_mxfp8(x: np.ndarray) -> np.ndarray:
     return out
 
 
+def quant_rows_mxfp4(x: np.ndarray) -> np.ndarray:
+    """Rows of x (fp64) replaced by their MXFP4-dequantised values."""
+    out = np.empty_like(x, dtype=np.float64)
+    for r in range(x.shape[0]):
+        out[r] = quant_mxfp4(x[r])[2]
+    return out
+
+
+def quant_rows(x: np.ndarray, act_mode: int) -> np.ndarray:
+    """The activation rows as the prefill path quantises them: act_mode 1 MXFP8,
+    2 MXFP4, 0 unquantised."""
+    if act_mode == 1:
+        return quant_rows_mxfp8(x)
+    if act_mode == 2:
+        return quant_rows_mxfp4(x)
+    return np.asarray(x, dtype=np.float64)
+
+
 def prefill_layer(experts, x_bits: np.ndarray, Wr_bits: np.ndarray, k: int, act_mode: int = 1,
                   sample_tokens=None):
     """Expert-major prefill: routing and the pair permutation for all T tokens, and
     the output y for the tokens in `sample_tokens` (all when None).
 
-    act_mode 1: activations MXFP8 (x before W_g/W_u, h before W_d); 0: fp64."""
+    act_mode 1: activations MXFP8 (x before W_g/W_u, h before W_d); 2: MXFP4 (the
+    same two steps with E2M1 elements); 0: fp64."""
     T, H = x_bits.shape
     idx, w, _ = route(x_bits, Wr_bits, k)
     perm, inv, offsets = sort_pairs(idx, experts.E)
     toks = np.arange(T) if sample_tokens is None else np.asarray(sample_tokens)
-    xs = bf16_value(x_bits[toks])
-    if act_mode == 1:
-        xs = quant_rows_mxfp8(xs)
+    xs = quant_rows(bf16_value(x_bits[toks]), act_mode)
     y = combine_rows(experts, H, experts.I, xs, idx[toks], w[toks], h_mode=act_mode)
-    amb = combine_ambiguity(experts, H, experts.I, xs, idx[toks], w[toks]) if act_mode == 1 else np.zeros_like(y)
+    amb = (combine_ambiguity(experts, H, experts.I, xs, idx[toks], w[toks], fmt=8 if act_mode == 1 else 4)
+           if act_mode in (1, 2) else np.zeros_like(y))
     return {"idx": idx, "w": w, "perm": perm, "inv_perm": inv, "offsets": offsets,
             "tokens": toks, "y": y, "y_amb": amb}
 

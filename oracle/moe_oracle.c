@@ -24,9 +24,18 @@
  * marked "parity unpinned" below (none at present).
  */
 #include <math.h>
+#include <omp.h>
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
+
+/* Threads of the OpenMP loops (rows and tokens are independent; the arithmetic of
+ * each result does not depend on the thread count).  Returns the previous value. */
+int orc_set_threads(int n) {
+    int prev = omp_get_max_threads();
+    if (n > 0) omp_set_num_threads(n);
+    return prev;
+}
 
 /* ------------------------------------------------------------------ SplitMix64
  * Steele, Lea & Flood, "Fast Splittable Pseudorandom Number Generators" (2014),
@@ -131,6 +140,48 @@ void orc_quant_mxfp8(const double *v, int n, uint8_t *codes, uint8_t *sbytes, do
             unsigned c = orc_e4m3_encode(ldexp(v[i], -X));
             codes[i] = (uint8_t)c;
             if (deq) deq[i] = ldexp(orc_e4m3_value(c), X);
+        }
+    }
+}
+
+/* Round v to E2M1: nearest of the 8 magnitudes {0, 0.5, 1, 1.5, 2, 3, 4, 6}, ties to
+ * the even code (mantissa bit 0), |v| beyond 6 saturates to +-6; the sign bit is
+ * that of v (so small negatives give -0, code 8). */
+unsigned orc_e2m1_encode(double v) {
+    unsigned sign = (v < 0 || (v == 0 && signbit(v))) ? 8u : 0u;
+    double a = fabs(v);
+    if (a >= 6.0) return sign | 7u;                 /* saturation (also where |v - m| loses m) */
+    unsigned best = 0;
+    double bestd = INFINITY;
+    for (unsigned c = 0; c < 8; c++) {
+        double d = fabs(E2M1_MAG[c] - a);
+        if (d < bestd || (d == bestd && (c & 1u) == 0u)) { best = c; bestd = d; }
+    }
+    return sign | best;
+}
+
+/* MXFP4 quantisation of n values in blocks of 32 (OCP MX v1.0): shared exponent
+ * X = floor(log2(amax)) - 2 (2 = E2M1 emax), clamped to [-127, 127]; element code =
+ * E2M1(v / 2^X) with saturation.  amax == 0 gives X = -127.
+ * codes[n] (one code per byte), sbytes[ceil(n/32)], deq[n] (nullable). */
+void orc_quant_mxfp4(const double *v, int n, uint8_t *codes, uint8_t *sbytes, double *deq) {
+    for (int b0 = 0; b0 < n; b0 += 32) {
+        int b1 = b0 + 32 < n ? b0 + 32 : n;
+        double amax = 0.0;
+        for (int i = b0; i < b1; i++) if (fabs(v[i]) > amax) amax = fabs(v[i]);
+        int X = -127;
+        if (amax > 0.0) {
+            int ex;
+            frexp(amax, &ex);
+            X = (ex - 1) - 2;
+            if (X < -127) X = -127;
+            if (X > 127) X = 127;
+        }
+        sbytes[b0 / 32] = (uint8_t)(X + 127);
+        for (int i = b0; i < b1; i++) {
+            unsigned c = orc_e2m1_encode(ldexp(v[i], -X));
+            codes[i] = (uint8_t)c;
+            if (deq) deq[i] = ldexp(orc_e2m1_value(c), X);
         }
     }
 }
@@ -337,7 +388,8 @@ static double silu(double g) { return g / (1.0 + exp(-g)); }
 
 /* Apply one expert (logical layout, see orc_gen_expert) to n rows x [n][H]:
  * y [n][H] = W_d (silu(W_g x) * (W_u x)); h [n][I] (nullable) receives h.
- * h_mode 1: h is MXFP8-quantised along I (orc_quant_mxfp8) before W_d.
+ * h_mode 1: h is MXFP8-quantised along I (orc_quant_mxfp8) before W_d;
+ * h_mode 2: h is MXFP4-quantised along I (orc_quant_mxfp4) before W_d.
  * Rows are independent; the loop over rows is the outer one for clarity. */
 void orc_expert_forward(const uint8_t *codes, const uint8_t *scales, int H, int I,
                         const double *x, int n, double *y, double *h, int h_mode) {
@@ -354,6 +406,7 @@ void orc_expert_forward(const uint8_t *codes, const uint8_t *scales, int H, int 
             hv[i] = silu(g) * u;
         }
         if (h_mode == 1) orc_quant_mxfp8(hv, I, qc, qs, hv);
+        if (h_mode == 2) orc_quant_mxfp4(hv, I, qc, qs, hv);
         if (h) memcpy(h + (size_t)r * I, hv, sizeof(double) * (size_t)I);
         #pragma omp parallel for schedule(static)
         for (int o = 0; o < H; o++) {
@@ -373,27 +426,32 @@ void orc_expert_forward(const uint8_t *codes, const uint8_t *scales, int H, int 
  * power of two may take either shared exponent.  Both sides apply the same OCP
  * rule (orc_quant_mxfp8) to the value they hold. */
 
-/* Shared exponent of a block with max |v| = amax (OCP MX v1.0: floor(log2 amax) - 8,
- * clamped to [-127, 127]; -127 for amax == 0). */
-static int mx8_exp(double amax) {
+/* Shared exponent of a block with max |v| = amax (OCP MX v1.0: floor(log2 amax) - emax,
+ * clamped to [-127, 127]; -127 for amax == 0), emax = 8 for E4M3, 2 for E2M1. */
+static int mx_block_exp(double amax, int emax) {
     if (!(amax > 0.0)) return -127;
     int ex;
     frexp(amax, &ex);
-    int X = (ex - 1) - 8;
+    int X = (ex - 1) - emax;
     if (X < -127) X = -127;
     if (X > 127) X = 127;
     return X;
 }
 
-/* v quantised at shared exponent X and dequantised: E4M3(v 2^-X) 2^X. */
-static double mx8_at(double v, int X) { return ldexp(orc_e4m3_value(orc_e4m3_encode(ldexp(v, -X))), X); }
+/* v quantised at shared exponent X and dequantised: E4M3 (fmt 8) or E2M1 (fmt 4). */
+static double mx_at(double v, int X, int fmt) {
+    if (fmt == 4) return ldexp(orc_e2m1_value(orc_e2m1_encode(ldexp(v, -X))), X);
+    return ldexp(orc_e4m3_value(orc_e4m3_encode(ldexp(v, -X))), X);
+}
 
-/* delta[i] = the largest |alternative - nominal| of the MXFP8 value of v[i] when each
- * element of its 32-block may be anywhere in [v - radius, v + radius]: every shared
- * exponent a block max in its range can give is tried, and at each exponent the
- * quantised value is monotone in the element, so its extremes over the interval are
- * the quantised ends of the interval.  The nominal value is that of orc_quant_mxfp8. */
-void orc_mxfp8_ambiguity(const double *v, const double *radius, int n, double *delta) {
+/* delta[i] = the largest |alternative - nominal| of the MX value (fmt 8: MXFP8, 4:
+ * MXFP4) of v[i] when each element of its 32-block may be anywhere in
+ * [v - radius, v + radius]: every shared exponent a block max in its range can give
+ * is tried, and at each exponent the quantised value is monotone in the element, so
+ * its extremes over the interval are the quantised ends of the interval.  The
+ * nominal value is that of orc_quant_mxfp8 / orc_quant_mxfp4. */
+void orc_mx_ambiguity(const double *v, const double *radius, int n, int fmt, double *delta) {
+    const int emax = fmt == 4 ? 2 : 8;
     for (int b0 = 0; b0 < n; b0 += 32) {
         int b1 = b0 + 32 < n ? b0 + 32 : n;
         double amax = 0.0, alo = 0.0, ahi = 0.0;
@@ -403,18 +461,22 @@ void orc_mxfp8_ambiguity(const double *v, const double *radius, int n, double *d
             if (lo > alo) alo = lo;
             if (a + radius[i] > ahi) ahi = a + radius[i];
         }
-        int X = mx8_exp(amax), Xlo = mx8_exp(alo), Xhi = mx8_exp(ahi);
+        int X = mx_block_exp(amax, emax), Xlo = mx_block_exp(alo, emax), Xhi = mx_block_exp(ahi, emax);
         for (int i = b0; i < b1; i++) {
-            double q = mx8_at(v[i], X), d = 0.0;
+            double q = mx_at(v[i], X, fmt), d = 0.0;
             for (int Xa = Xlo; Xa <= Xhi; Xa++) {
-                double e1 = fabs(mx8_at(v[i] - radius[i], Xa) - q);
-                double e2 = fabs(mx8_at(v[i] + radius[i], Xa) - q);
+                double e1 = fabs(mx_at(v[i] - radius[i], Xa, fmt) - q);
+                double e2 = fabs(mx_at(v[i] + radius[i], Xa, fmt) - q);
                 if (e1 > d) d = e1;
                 if (e2 > d) d = e2;
             }
             delta[i] = d;
         }
     }
+}
+
+void orc_mxfp8_ambiguity(const double *v, const double *radius, int n, double *delta) {
+    orc_mx_ambiguity(v, radius, n, 8, delta);
 }
 
 /* Dot product as mx_row_dot, also returning sum_t (|P_{t-1}| + |S_t|) over the
@@ -475,12 +537,12 @@ void orc_h_radius(const uint8_t *codes, const uint8_t *scales, int H, int I, con
     }
 }
 
-/* Per output row o of one expert applied to the rows x [n][H] with MXFP8 h:
- * yamb[o] = sum_i |W_d[o][i]| * delta_i, with delta from orc_mxfp8_ambiguity on the
- * radii of orc_h_radius (step error `rel`): the largest change of o that equally
- * valid MXFP8 decisions on the GPU's h can make. */
+/* Per output row o of one expert applied to the rows x [n][H] with MX-quantised h
+ * (fmt 8: MXFP8, 4: MXFP4): yamb[o] = sum_i |W_d[o][i]| * delta_i, with delta from
+ * orc_mx_ambiguity on the radii of orc_h_radius (step error `rel`): the largest
+ * change of o that equally valid decisions on the GPU's h can make. */
 void orc_expert_ambiguity(const uint8_t *codes, const uint8_t *scales, int H, int I,
-                          const double *x, int n, double rel, double *yamb) {
+                          const double *x, int n, double rel, int fmt, double *yamb) {
     const uint8_t *cd = codes + (size_t)I * H;
     const uint8_t *sd = scales + (size_t)I * H / 16;
     double *hv = (double *)malloc(sizeof(double) * (size_t)n * I);
@@ -488,7 +550,7 @@ void orc_expert_ambiguity(const uint8_t *codes, const uint8_t *scales, int H, in
     double *dl = (double *)malloc(sizeof(double) * (size_t)I);
     orc_h_radius(codes, scales, H, I, x, n, rel, hv, rd);
     for (int r = 0; r < n; r++) {
-        orc_mxfp8_ambiguity(hv + (size_t)r * I, rd + (size_t)r * I, I, dl);
+        orc_mx_ambiguity(hv + (size_t)r * I, rd + (size_t)r * I, I, fmt, dl);
         #pragma omp parallel for schedule(static)
         for (int o = 0; o < H; o++) {
             const uint8_t *c = cd + (size_t)o * (I / 2);

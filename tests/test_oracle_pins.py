@@ -506,3 +506,95 @@ def test_expert_ambiguity_bounds_the_output_change():
             dq = np.abs(Wd @ oracle.quant_mxfp8(hh)[2] - o0)
             assert np.all(dq <= amb[m] * (1 + 1e-12) + 1e-14 * np.abs(o0).max())
         assert np.mean(amb[m] > 0) > 0.5
+
+
+# ------------------------------------------------------- MXFP4 activations
+# The prefill variant with FP4 activations quantises x and h to MXFP4 (OCP MX v1.0:
+# E2M1 elements, one E8M0 scale per 32, shared exponent floor(log2 amax) - 2).
+
+
+def test_e2m1_encode_round_trip_midpoints_and_saturation():
+    mags = [oracle.e2m1_value(c) for c in range(8)]
+    assert mags == [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+    for c in range(8):
+        assert oracle.e2m1_encode(mags[c]) == c
+        assert oracle.e2m1_encode(-mags[c]) == (c | 8)
+    for c in range(7):                          # exact midpoints go to the even code
+        mid = (mags[c] + mags[c + 1]) / 2
+        assert oracle.e2m1_encode(mid) == (c if c % 2 == 0 else c + 1)
+        eps = (mags[c + 1] - mags[c]) * 1e-9
+        assert oracle.e2m1_encode(mid - eps) == c
+        assert oracle.e2m1_encode(mid + eps) == c + 1
+    for big in [6.0, 6.5, 7.0, 100.0, 1e300]:
+        assert oracle.e2m1_encode(big) == 7 and oracle.e2m1_encode(-big) == 15
+
+
+def test_e2m1_encode_is_the_nearest_value():
+    rng = np.random.default_rng(9)
+    mags = np.array([oracle.e2m1_value(c) for c in range(8)])
+    for v in rng.uniform(-7, 7, size=2000):
+        c = oracle.e2m1_encode(v)
+        got = oracle.e2m1_value(c)
+        assert abs(abs(got) - min(abs(v), 6.0)) == np.min(np.abs(mags - min(abs(v), 6.0)))
+        assert math.copysign(1, got) == math.copysign(1, v)
+
+
+def test_mxfp4_block_rule():
+    v = np.zeros(96)
+    v[0] = 1.0          # amax 1 -> X = 0 - 2 = -2 (byte 125); 1 * 4 = 4 exact
+    v[1] = -0.3         # 0.3 * 4 = 1.2 -> 1.0 -> -0.25
+    v[32] = 7.0         # amax 7 -> X = 2 - 2 = 0; 7 saturates to 6
+    v[33] = 2.5         # tie between 2 and 3 -> 2 (even)
+    codes, sb, deq = oracle.quant_mxfp4(v)
+    assert list(sb) == [125, 127, 0]
+    assert deq[0] == 1.0 and deq[1] == -0.25
+    assert deq[32] == 6.0 and deq[33] == 2.0
+    assert np.all(deq[64:] == 0) and np.all(codes[2:32] == 0)
+
+
+def test_mxfp4_error_bound_on_bf16_inputs():
+    # the block max lies in [4, 8) * 2^X; every element is within half a step of its
+    # value, the step being 2^(X + e - 1) for element exponent e >= 0, 2^(X-1) below
+    x = synth.bf16_bits_to_f64(synth.tokens_bf16(0, 0, 4, 1024)).ravel()
+    _, sb, deq = oracle.quant_mxfp4(x)
+    for b in range(0, x.size, 32):
+        X = int(sb[b // 32]) - 127
+        blk = x[b:b + 32]
+        assert 4 <= np.max(np.abs(blk)) / 2.0 ** X < 8
+        t = np.abs(blk) / 2.0 ** X
+        step = np.where(t >= 1, 2.0 ** (np.floor(np.log2(np.maximum(t, 1))) - 1), 0.5) * 2.0 ** X
+        small = t <= 6
+        assert np.all(np.abs(deq[b:b + 32] - blk)[small] <= step[small] / 2)
+
+
+def test_expert_mxfp4_h_matches_independent_composition():
+    H, I = 256, 128
+    codes, scales = oracle.gen_expert(23, 1, H, I)
+    (cg, sg), (cu, su), (cd, sd) = _split(codes, scales, H, I)
+    Wg, Wu, Wd = _dequant(cg, sg, I, H), _dequant(cu, su, I, H), _dequant(cd, sd, H, I)
+    xq = oracle.quant_rows_mxfp4(synth.bf16_bits_to_f64(synth.tokens_bf16(15, 0, 3, H)))
+    y, h = oracle.expert_forward(codes, scales, H, I, xq, h_mode=2)
+    for m in range(3):
+        g, u = Wg @ xq[m], Wu @ xq[m]
+        hq = oracle.quant_mxfp4(g / (1 + np.exp(-g)) * u)[2]
+        assert np.array_equal(h[m], hq)
+        assert np.allclose(y[m], Wd @ hq, rtol=1e-13, atol=1e-13 * np.abs(y[m]).max())
+
+
+def test_mxfp4_ambiguity_bounds_every_choice_in_the_radius():
+    rng = np.random.default_rng(8)
+    n = 32 * 48
+    v = rng.standard_normal(n) * np.exp2(rng.integers(-3, 3, size=n))
+    v[3] = 1.25 * 2.0 ** -3           # an E2M1 midpoint at the block's scale
+    r = np.abs(v) * 10.0 ** rng.uniform(-4, -0.7, size=n)
+    d = oracle.mx_ambiguity(v, r, 4)
+    q0 = oracle.quant_mxfp4(v)[2]
+    worst = np.zeros(n)
+    for trial in range(400):
+        pick = rng.integers(0, 3, size=n)
+        vv = np.where(pick == 0, v - r, np.where(pick == 1, v + r, v + rng.uniform(-1, 1, size=n) * r))
+        dq = np.abs(oracle.quant_mxfp4(vv)[2] - q0)
+        assert np.all(dq <= d)
+        worst = np.maximum(worst, dq)
+    assert np.all(worst[d == 0] == 0)
+    assert (d > 0).sum() > 20 and np.mean(worst[d > 0] == d[d > 0]) > 0.25
