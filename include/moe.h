@@ -56,7 +56,7 @@ typedef struct moe_pool moe_pool;  /* host-side view of a resident expert pool *
 enum { MOE_OP_ROUTE = 0, MOE_OP_DECODE = 1, MOE_OP_GROUPED = 2 };
 
 /* Activation formats of the expert-major (grouped) path. */
-enum { MOE_ACT_MXFP8 = 1 };
+enum { MOE_ACT_MXFP8 = 1, MOE_ACT_MXFP4 = 2 };
 
 /* Element types of the grouped path's partial outputs. */
 enum { MOE_PARTIAL_F32 = 0, MOE_PARTIAL_BF16 = 1 };
@@ -202,7 +202,10 @@ moe_status moe_prescale(const uint16_t *x, int M, int H, uint16_t *out, moe_stre
  * expert).  With act_mode MOE_ACT_MXFP8 the rows are quantised to MXFP8 (E4M3
  * elements, one E8M0 scale per 32, shared exponent floor(log2 amax) - 8,
  * round-to-nearest-even with saturation) before W_g/W_u, and h likewise before
- * W_d; the contractions run on the tensor cores as block-scaled MMAs.
+ * W_d; the contractions run on the tensor cores as block-scaled MMAs of
+ * kind::mxf8f6f4 (the FP8 rate).  With MOE_ACT_MXFP4 the rows and h are quantised
+ * to MXFP4 instead (E2M1 elements, shared exponent floor(log2 amax) - 2, RNE with
+ * saturation at 6) and the MMAs are kind::mxf4 (both operands FP4: the FP4 rate).
  * Out: partial [T*k][H] (partial_dtype MOE_PARTIAL_*), row r = o of pair perm[r]
  * (unweighted).  ws: MOE_OP_GROUPED bytes. */
 moe_status moe_expert_forward_grouped(const moe_pool *pool, const uint16_t *x, int T,
@@ -211,15 +214,17 @@ moe_status moe_expert_forward_grouped(const moe_pool *pool, const uint16_t *x, i
                                       void *partial, int partial_dtype,
                                       void *ws, size_t ws_bytes, moe_stream_t stream);
 
-/* Diagnostics of the expert-major path: after moe_expert_forward_grouped(T, k) with
- * workspace `ws` and its `offsets` output, copy the MXFP8 h that the gate/up GEMM
- * wrote for W_d, in sorted row order: hq [T*k][I] E4M3 codes (16-byte aligned) and
- * hs [T*k][I/32] E8M0 scale bytes; h[r][i] = E4M3(hq[r][i]) * 2^(hs[r][i/32] - 127).
- * Rows past offsets[E] (pairs with an invalid expert index) are left untouched.  It
- * lets a caller check each MXFP8 decision on h against a reference; the workspace
- * must not have been reused since the grouped call. */
-moe_status moe_grouped_read_h(const moe_pool *pool, int T, int k, const int32_t *offsets, const void *ws,
-                              size_t ws_bytes, uint8_t *hq, uint8_t *hs, moe_stream_t stream);
+/* Diagnostics of the expert-major path: after moe_expert_forward_grouped(T, k,
+ * act_mode) with workspace `ws` and its `offsets` output, copy the MX-quantised h
+ * that the gate/up GEMM wrote for W_d, in sorted row order: hq [T*k][I] element
+ * codes, one per byte (E4M3 for MOE_ACT_MXFP8, E2M1 in the low nibble for
+ * MOE_ACT_MXFP4; 16-byte aligned) and hs [T*k][I/32] E8M0 scale bytes;
+ * h[r][i] = code value * 2^(hs[r][i/32] - 127).  Rows past offsets[E] (pairs with
+ * an invalid expert index) are left untouched.  It lets a caller check each
+ * quantisation decision on h against a reference; the workspace must not have been
+ * reused since the grouped call. */
+moe_status moe_grouped_read_h(const moe_pool *pool, int T, int k, int act_mode, const int32_t *offsets,
+                              const void *ws, size_t ws_bytes, uint8_t *hq, uint8_t *hs, moe_stream_t stream);
 
 /* Weighted combine of the grouped path: y[t] = sum_{j<k} w[t,j] *
  * partial[inv_perm[t*k+j]] (+ residual[t]), summed in slot order j in fp32 and

@@ -25,7 +25,7 @@ MOE_ERR_TIMEOUT = 6
 MOE_ERR_NONFINITE = 7
 
 MOE_OP_ROUTE, MOE_OP_DECODE, MOE_OP_GROUPED = 0, 1, 2
-MOE_ACT_MXFP8 = 1
+MOE_ACT_MXFP8, MOE_ACT_MXFP4 = 1, 2
 MOE_PARTIAL_F32, MOE_PARTIAL_BF16 = 0, 1
 
 EXPORTED = [
@@ -75,7 +75,7 @@ def lib() -> ctypes.CDLL:
             "moe_prescale": (_i, [_vp, _i, _i, _vp, _vp]),
             "moe_expert_forward_grouped": (_i, [_vp, _vp, _i, _vp, _i, _i, _vp, _vp, _vp, _vp, _i, _vp, _sz,
                                                 _vp]),
-            "moe_grouped_read_h": (_i, [_vp, _i, _i, _vp, _vp, _sz, _vp, _vp, _vp]),
+            "moe_grouped_read_h": (_i, [_vp, _i, _i, _i, _vp, _vp, _sz, _vp, _vp, _vp]),
             "moe_combine": (_i, [_vp, _i, _vp, _vp, _i, _i, _i, _vp, _vp, _vp]),
             "moe_debug_set_wait_limit": (_i, [_u64]),
             "moe_debug_set_barrier_extra": (_i, [_i]),
@@ -302,14 +302,15 @@ def moe_expert_forward_grouped(pool: Pool, x: torch.Tensor, idx: torch.Tensor, a
     return out
 
 
-def moe_grouped_read_h(pool: Pool, T: int, k: int, offsets: torch.Tensor, ws: torch.Tensor, stream=None):
-    """The MXFP8 h of the last grouped call on `ws`, in sorted row order:
-    (codes uint8 [T*k, I], scale bytes uint8 [T*k, I/32])."""
+def moe_grouped_read_h(pool: Pool, T: int, k: int, offsets: torch.Tensor, ws: torch.Tensor,
+                       act_mode: int = MOE_ACT_MXFP8, stream=None):
+    """The MX-quantised h of the last grouped call on `ws`, in sorted row order:
+    (codes uint8 [T*k, I] (E4M3, or E2M1 with MOE_ACT_MXFP4), scale bytes [T*k, I/32])."""
     _need(offsets, torch.int32, "offsets")
     hq = torch.zeros((T * k, pool.I), dtype=torch.uint8, device=ws.device)
     hs = torch.zeros((T * k, pool.I // 32), dtype=torch.uint8, device=ws.device)
-    _check(lib().moe_grouped_read_h(pool.handle, T, k, _ptr(offsets), _ptr(ws), ws.numel(), _ptr(hq), _ptr(hs),
-                                    _stream(stream)), "moe_grouped_read_h")
+    _check(lib().moe_grouped_read_h(pool.handle, T, k, act_mode, _ptr(offsets), _ptr(ws), ws.numel(), _ptr(hq),
+                                    _ptr(hs), _stream(stream)), "moe_grouped_read_h")
     return hq, hs
 
 

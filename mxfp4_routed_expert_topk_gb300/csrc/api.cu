@@ -253,7 +253,7 @@ moe_status moe_expert_forward_grouped(const moe_pool *pool, const uint16_t *x, i
         offsets == nullptr || partial == nullptr || ws == nullptr)
         return MOE_ERR_INVALID_ARG;
     if (T < 0 || k < 1 || k > kMaxK || k > pool->v.E) return MOE_ERR_INVALID_ARG;
-    if (act_mode != MOE_ACT_MXFP8) return MOE_ERR_INVALID_ARG;
+    if (act_mode != MOE_ACT_MXFP8 && act_mode != MOE_ACT_MXFP4) return MOE_ERR_INVALID_ARG;
     if (partial_dtype != MOE_PARTIAL_F32 && partial_dtype != MOE_PARTIAL_BF16) return MOE_ERR_INVALID_ARG;
     if (pool->v.I % 64 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
     if (!aligned(ws, 256) || !aligned(x, 16) || !aligned(partial, 16)) return MOE_ERR_INVALID_ARG;
@@ -270,15 +270,16 @@ moe_status moe_combine(const void *partial, int partial_dtype, const int32_t *in
     return cuda_status(launch_combine(partial, partial_dtype, inv_perm, w, T, k, H, residual, y, (cudaStream_t)stream));
 }
 
-moe_status moe_grouped_read_h(const moe_pool *pool, int T, int k, const int32_t *offsets, const void *ws,
-                              size_t ws_bytes, uint8_t *hq, uint8_t *hs, moe_stream_t stream) {
+moe_status moe_grouped_read_h(const moe_pool *pool, int T, int k, int act_mode, const int32_t *offsets,
+                              const void *ws, size_t ws_bytes, uint8_t *hq, uint8_t *hs, moe_stream_t stream) {
     if (pool == nullptr || offsets == nullptr || ws == nullptr || hq == nullptr || hs == nullptr)
         return MOE_ERR_INVALID_ARG;
     if (T < 0 || k < 1 || k > kMaxK || k > pool->v.E) return MOE_ERR_INVALID_ARG;
+    if (act_mode != MOE_ACT_MXFP8 && act_mode != MOE_ACT_MXFP4) return MOE_ERR_INVALID_ARG;
     if (pool->v.I % 64 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
     if (!aligned(ws, 256) || !aligned(hq, 16)) return MOE_ERR_INVALID_ARG;
     if (ws_bytes < grouped_workspace_bytes(pool->v.E, pool->v.H, pool->v.I, T, k)) return MOE_ERR_WORKSPACE;
-    return cuda_status(launch_read_h(pool->v, T, k, offsets, ws, hq, hs, (cudaStream_t)stream));
+    return cuda_status(launch_read_h(pool->v, T, k, act_mode, offsets, ws, hq, hs, (cudaStream_t)stream));
 }
 
 moe_status moe_debug_set_wait_limit(uint64_t ns) {

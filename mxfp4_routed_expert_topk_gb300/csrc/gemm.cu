@@ -1,7 +1,12 @@
 // Grouped block-scaled GEMMs of the expert-major prefill path on the 5th-generation
-// tensor cores (tcgen05, kind::mxf8f6f4): weights are the MMA's A operand (E2M1,
-// one E8M0 scale per 32 along K, 128 rows per tile), the expert's sorted token rows
-// are B (E4M3 with E8M0 scales, up to BN rows per tile), fp32 accumulators in TMEM.
+// tensor cores (tcgen05): weights are the MMA's A operand (E2M1, one E8M0 scale per
+// 32 along K, 128 rows per tile), the expert's sorted token rows are B (up to BN rows
+// per tile), fp32 accumulators in TMEM.  Two activation formats:
+//   MXFP8 rows: kind::mxf8f6f4 (E2M1 x E4M3, the FP8 rate), K = 32 per MMA; A arrives
+//          unpacked by the tensor copy (16 E2M1 values per 16 bytes), 128 K per stage;
+//   MXFP4 rows (FP4 template): kind::mxf4, scale_vec::2X (E2M1 x E2M1, the FP4 rate),
+//          K = 64 per MMA; both operands stay packed (two codes per byte), 256 K per
+//          stage, two scale atoms per operand and stage.
 //
 //   GEMM 1 (gate/up): A = W_gu (2I rows, K = H), B = MXFP8 x rows; epilogue
 //            h = silu(g) * u from the interleaved gate/up rows, quantised to MXFP8
@@ -54,9 +59,10 @@ struct GemmShape {
 };
 
 struct GemmArgs {
-    int mode;            // 1: gate/up + SwiGLU + MXFP8, 2: down
+    int mode;            // 1: gate/up + SwiGLU + MX quantisation of h, 2: down
     int E;
-    int nkt;             // K tiles of 128
+    int nkt;             // pipeline stages along K (128 K each, 256 with FP4 rows)
+    int nkt_sf;          // K tiles of 128 (the unit of the scale-factor blocks)
     uint64_t a_sf_off;   // offset in a record of A's scale factors in tensor-core order [nkt][nmt][512]
     const uint8_t *pool;
     uint64_t rec;
@@ -184,6 +190,33 @@ __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t
         : "memory");
 }
 
+// Instruction descriptor of kind::mxf4: A and B E2M1 (format 1 of this kind), both
+// K-major, M = 128, N = n, E8M0 scales.  With scale_vec::2X an MMA (K = 64) takes the
+// scale bytes sf_id, sf_id + 1 (sf_id 0 or 2) of a 32-bit TMEM column: add
+// kIdescSf2 for sf_id 2 (A and B alike).
+constexpr uint32_t kIdescSf2 = (2u << 4) | (2u << 29);
+
+__device__ __forceinline__ uint32_t idesc_mxf4(int n) {
+    uint32_t d = 0;
+    d |= 1u << 7;                        // A format: E2M1
+    d |= 1u << 10;                       // B format: E2M1
+    d |= (uint32_t)(n >> 3) << 17;       // N / 8
+    d |= 1u << 23;                       // scale format: UE8M0
+    d |= (uint32_t)(kTileM >> 4) << 24;  // M / 16
+    return d;
+}
+
+__device__ __forceinline__ void tc_mma_f4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                          uint32_t sfa, uint32_t sfb, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+            d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+        : "memory");
+}
+
 __device__ __forceinline__ void tc_commit(uint64_t *bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
                  : "memory");
@@ -286,7 +319,11 @@ __device__ __forceinline__ void epilogue_split3(const GemmArgs &a, uint32_t lane
 // 2^-119 (the clamp; subnormals have exponent field 0).  Equal to the frexp form.
 __device__ __forceinline__ int mx_exp_from_bits(uint32_t amax_bits) { return max(-127, (int)(amax_bits >> 23) - 135); }
 
-// 2^-X as a float for X in [-127, 119] (always a normal number).
+// MXFP4 shared exponent from the bits of the block's max |h|: floor(log2 amax) - 2,
+// or -127 for zero and values below 2^-125.
+__device__ __forceinline__ int mx4_exp_from_bits(uint32_t amax_bits) { return max(-127, (int)(amax_bits >> 23) - 129); }
+
+// 2^-X as a float for X in [-127, 125] (always a normal number).
 __device__ __forceinline__ float pow2_neg(int X) { return __uint_as_float((uint32_t)(127 - X) << 23); }
 
 // One-part (MXFP8) epilogue of a tile's 16-column groups: gate/up -> h = silu(g) * u
@@ -295,6 +332,7 @@ __device__ __forceinline__ float pow2_neg(int X) { return __uint_as_float((uint3
 // takes the column groups c0 = 16 wg, 16 (wg + nwg), ...  Warps 2p and 2p+1 of a warpgroup
 // hold the two halves of the same 32-blocks of I and exchange their maxima through
 // shared memory under a 64-thread barrier of their own (id 2 + 2 wg + p).
+template <bool FP4>
 __device__ __forceinline__ void epilogue_mx1(const GemmArgs &a, uint32_t lane_base, bool ok, int nn, int nmma, int mt,
                                              int row0, int n0, int tile, int ew, int wg, int nwg, int lane,
                                              float *amax_x) {
@@ -327,13 +365,24 @@ __device__ __forceinline__ void epilogue_mx1(const GemmArgs &a, uint32_t lane_ba
 #pragma unroll
             for (int j = 0; j < 16; j++) {
                 const int n = c0 + j;
-                const int X = mx_exp_from_bits(max(am[j], amax_u[(ew ^ 1) * 16 + j]));
-                if (ok && n < nn && lane < 16) {
+                const uint32_t amb = max(am[j], amax_u[(ew ^ 1) * 16 + j]);
+                const int X = FP4 ? mx4_exp_from_bits(amb) : mx_exp_from_bits(amb);
+                // h * 2^-X is exact (a power-of-two scaling that stays normal or rounds
+                // as ldexp does)
+                const float hsc = hv[j] * pow2_neg(X);
+                if (FP4) {
+                    // lanes 2m and 2m+1 hold intermediate indices i, i+1: one byte
+                    const float hnext = __shfl_down_sync(0xffffffffu, hsc, 1);
+                    if (ok && n < nn && lane < 16 && (lane & 1) == 0) {
+                        const uint64_t r = (uint64_t)(row0 + n0 + n);
+                        a.hq[r * (a.I / 2) + (i >> 1)] = e2m1x2_rn(hsc, hnext);
+                        if (lane == 0 && (ew & 1) == 0)
+                            a.hs[sf_tile_word(tile, a.nkt_h, a.nsfb, i >> 7, n) + ((i >> 5) & 3)] = (uint8_t)(X + 127);
+                    }
+                } else if (ok && n < nn && lane < 16) {
                     const uint64_t r = (uint64_t)(row0 + n0 + n);
                     unsigned short pair;
-                    // h * 2^-X is exact (a power-of-two scaling that stays normal or
-                    // rounds as ldexp does)
-                    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(pair) : "f"(0.f), "f"(hv[j] * pow2_neg(X)));
+                    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(pair) : "f"(0.f), "f"(hsc));
                     a.hq[r * a.I + i] = (uint8_t)(pair & 0xFF);
                     if (lane == 0 && (ew & 1) == 0)
                         a.hs[sf_tile_word(tile, a.nkt_h, a.nsfb, i >> 7, n) + ((i >> 5) & 3)] = (uint8_t)(X + 127);
@@ -358,15 +407,18 @@ __device__ __forceinline__ void epilogue_mx1(const GemmArgs &a, uint32_t lane_ba
 }
 
 // Shared memory of the persistent kernel for BN accumulator columns and ns stages.
+// With FP4 rows a stage holds two scale atoms per operand (K = 256, one B atom).
 struct GemmSmemLayout {
-    uint32_t a, b, sfa, sfb, bars, misc, total;
-    __host__ __device__ GemmSmemLayout(int BN, int ns, int tpi) {
+    uint32_t a, b, sfa, sfb, bars, misc, total, sfa_stage, sfb_stage;
+    __host__ __device__ GemmSmemLayout(int BN, int ns, int tpi, bool fp4 = false) {
         const uint32_t nsfb = (uint32_t)((BN + 127) / 128);
+        sfa_stage = (uint32_t)tpi * (fp4 ? 1024u : 512u);
+        sfb_stage = fp4 ? 1024u : sfb_stage_bytes((int)nsfb);
         a = 0;                                            // ns x tpi x 16 KB (1024-aligned)
         b = a + (uint32_t)(ns * tpi) * kTileM * kTileK;   // ns x BN*128
-        sfa = b + (uint32_t)ns * (uint32_t)BN * kTileK;   // ns x tpi x 512
-        sfb = sfa + (uint32_t)(ns * tpi) * 512;           // ns x sfb_stage_bytes(nsfb)
-        bars = sfb + (uint32_t)ns * sfb_stage_bytes((int)nsfb);  // full[], empty[], acc_full[2], acc_empty[2], mma_done
+        sfa = b + (uint32_t)ns * (uint32_t)BN * kTileK;   // ns x sfa_stage
+        sfb = sfa + (uint32_t)ns * sfa_stage;             // ns x sfb_stage
+        bars = sfb + (uint32_t)ns * sfb_stage;            // full[], empty[], acc_full[2], acc_empty[2], mma_done
         misc = bars + (2 * kMaxStages + 5) * 8;           // tmem addr, abort, amax[4][16]
         total = misc + 16 + kEpiWarps * 16 * 4;
     }
@@ -407,7 +459,7 @@ struct JobIter {
     }
 };
 
-template <int NT>
+template <int NT, bool FP4>
 __global__ void __launch_bounds__(NT, GemmShape<NT>::kCtasPerSm)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const GemmArgs a) {
@@ -416,7 +468,7 @@ __global__ void __launch_bounds__(NT, GemmShape<NT>::kCtasPerSm)
     unsigned char *smem = (unsigned char *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     const int ns = a.ns;
     const int tpi = a.tpi;
-    const GemmSmemLayout L(a.BN, ns, tpi);
+    const GemmSmemLayout L(a.BN, ns, tpi, FP4);
     uint8_t *sA = smem + L.a, *sB = smem + L.b, *sSFA = smem + L.sfa, *sSFB = smem + L.sfb;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.bars);
     uint64_t *empty = full + kMaxStages;
@@ -439,7 +491,7 @@ __global__ void __launch_bounds__(NT, GemmShape<NT>::kCtasPerSm)
     using Shape = GemmShape<NT>;
     for (int i = threadIdx.x; i < ns * tpi * kTileM * kTileK / 16; i += NT)
         reinterpret_cast<uint4 *>(sA)[i] = make_uint4(0u, 0u, 0u, 0u);
-    for (int i = threadIdx.x; i < ns * (tpi * 512 + (int)sfb_stage_bytes(nsfb)) / 16; i += NT)
+    for (int i = threadIdx.x; i < ns * (int)(L.sfa_stage + L.sfb_stage) / 16; i += NT)
         reinterpret_cast<uint4 *>(sSFA)[i] = make_uint4(0u, 0u, 0u, 0u);  // sSFB follows sSFA
     fence_proxy_async_smem();
     if (threadIdx.x == 0) {
@@ -461,7 +513,8 @@ __global__ void __launch_bounds__(NT, GemmShape<NT>::kCtasPerSm)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const uint32_t sf_col0 = 2u * (uint32_t)(tpi * a.BN);  // scale factors after the two accumulators
-    const uint32_t sf_stage = 4u * (uint32_t)tpi + 4u * (uint32_t)nsfb;  // TMEM columns per stage
+    // TMEM columns per stage: 4 per 512-byte scale atom (two atoms per operand with FP4)
+    const uint32_t sf_stage = FP4 ? 8u * (uint32_t)tpi + 8u : 4u * (uint32_t)tpi + 4u * (uint32_t)nsfb;
 
     int it_issued = 0;  // producer: stages issued
     // The copy and MMA roles run their loops with the whole warp converged (waits
@@ -489,21 +542,44 @@ __global__ void __launch_bounds__(NT, GemmShape<NT>::kCtasPerSm)
                 // scale factors: the item's row tiles of A (adjacent in the plane) and
                 // the column tile's atoms of B, each one contiguous block
                 const uint32_t a_tiles = (uint32_t)min(tpi, a.nmt - J.mt);
-                const uint32_t tx =
-                    (uint32_t)(tpi * kTileM * kTileK / 2 + a.BN * kTileK) + a_tiles * 512u + sfb_stage_bytes(nsfb);
-                const uint8_t *sfa_src = a.pool + (uint64_t)J.e * a.rec + a.a_sf_off + ((uint64_t)kt * a.nmt + J.mt) * 512;
-                const uint8_t *sfb_src = a.bscale + sf_tile_word(J.tile(), a.nkt, nsfb, kt, 0);
                 const int brow = J.row0 + J.n0();
-                if (elect_one()) {
-                    mbar_arrive_expect_tx(&full[s], tx);
-                    tma_load_3d(sA + (size_t)s * tpi * kTileM * kTileK, &tmA, kt * kTileK, J.mt * kTileM, J.e, &full[s]);
-                    tma_load_2d(sB + (size_t)s * a.BN * kTileK, &tmB, kt * kTileK, brow, &full[s]);
-                    bulk_g2s_l2(sSFA + (size_t)s * tpi * 512, sfa_src, a_tiles * 512u, &full[s]);
-                    if (nsfb == 1) {
-                        bulk_g2s_l2(sSFB + (size_t)s * 512, sfb_src, 512u, &full[s]);
-                    } else {
-                        // the interleaved 1 KB block once per TMEM lane quadrant
-                        for (int q = 0; q < 4; q++) bulk_g2s_l2(sSFB + (size_t)s * 4096 + q * 1024, sfb_src, 1024u, &full[s]);
+                if (FP4) {
+                    // packed operands, 256 K (128 bytes) per stage: both boxes arrive whole
+                    // (parts past the end of K are zero-filled and counted); one or two
+                    // 128-K scale tiles (the last stage of an odd count has one)
+                    const int n2 = min(2, a.nkt_sf - 2 * kt);
+                    const uint32_t tx = (uint32_t)(tpi * kTileM * kTileK + a.BN * kTileK) + (uint32_t)n2 * 1024u;
+                    const uint8_t *sfa_src =
+                        a.pool + (uint64_t)J.e * a.rec + a.a_sf_off + ((uint64_t)(2 * kt) * a.nmt + J.mt) * 512;
+                    const uint8_t *sfb_src = a.bscale + sf_tile_word(J.tile(), a.nkt_sf, 1, 2 * kt, 0);
+                    if (elect_one()) {
+                        mbar_arrive_expect_tx(&full[s], tx);
+                        tma_load_3d(sA + (size_t)s * kTileM * kTileK, &tmA, kt * kTileK, J.mt * kTileM, J.e, &full[s]);
+                        tma_load_2d(sB + (size_t)s * a.BN * kTileK, &tmB, kt * kTileK, brow, &full[s]);
+                        for (int j = 0; j < n2; j++)  // the two K tiles' A blocks are nmt blocks apart
+                            bulk_g2s_l2(sSFA + (size_t)s * 1024 + 512 * j, sfa_src + (size_t)j * a.nmt * 512, 512u,
+                                        &full[s]);
+                        bulk_g2s_l2(sSFB + (size_t)s * 1024, sfb_src, (uint32_t)n2 * 512u, &full[s]);  // adjacent
+                    }
+                } else {
+                    const uint32_t tx =
+                        (uint32_t)(tpi * kTileM * kTileK / 2 + a.BN * kTileK) + a_tiles * 512u + sfb_stage_bytes(nsfb);
+                    const uint8_t *sfa_src =
+                        a.pool + (uint64_t)J.e * a.rec + a.a_sf_off + ((uint64_t)kt * a.nmt + J.mt) * 512;
+                    const uint8_t *sfb_src = a.bscale + sf_tile_word(J.tile(), a.nkt, nsfb, kt, 0);
+                    if (elect_one()) {
+                        mbar_arrive_expect_tx(&full[s], tx);
+                        tma_load_3d(sA + (size_t)s * tpi * kTileM * kTileK, &tmA, kt * kTileK, J.mt * kTileM, J.e,
+                                    &full[s]);
+                        tma_load_2d(sB + (size_t)s * a.BN * kTileK, &tmB, kt * kTileK, brow, &full[s]);
+                        bulk_g2s_l2(sSFA + (size_t)s * tpi * 512, sfa_src, a_tiles * 512u, &full[s]);
+                        if (nsfb == 1) {
+                            bulk_g2s_l2(sSFB + (size_t)s * 512, sfb_src, 512u, &full[s]);
+                        } else {
+                            // the interleaved 1 KB block once per TMEM lane quadrant
+                            for (int q = 0; q < 4; q++)
+                                bulk_g2s_l2(sSFB + (size_t)s * 4096 + q * 1024, sfb_src, 1024u, &full[s]);
+                        }
                     }
                 }
                 __syncwarp();
@@ -527,7 +603,7 @@ __global__ void __launch_bounds__(NT, GemmShape<NT>::kCtasPerSm)
         // offset in 16-byte units to the start-address field (shared addresses stay
         // below 2^18, so the 14-bit field never carries into the next one).
         const uint32_t a_stage16 = (uint32_t)(tpi * kTileM * kTileK) >> 4, b_stage16 = (uint32_t)(a.BN * kTileK) >> 4;
-        const uint32_t sfa_stage16 = (uint32_t)tpi * 512u >> 4, sfb_stage16 = sfb_stage_bytes(nsfb) >> 4;
+        const uint32_t sfa_stage16 = L.sfa_stage >> 4, sfb_stage16 = L.sfb_stage >> 4;
         const uint64_t adesc0 = smem_desc(smem_u32(sA), 16, 1024, kSwizzle128B);
         const uint64_t bdesc0 = smem_desc(smem_u32(sB), 16, 1024, kSwizzle128B);
         const uint64_t sfadesc0 = smem_desc(smem_u32(sSFA), 128, 128, kSwizzleNone);
@@ -537,7 +613,8 @@ __global__ void __launch_bounds__(NT, GemmShape<NT>::kCtasPerSm)
         const int nlook = min(4, ns);  // stages polled at once (never past the ring)
         for (JobIter J(a, nu); run && J.valid(); J.next(), jb++) {
             const int nmma = (J.nn() + 15) / 16 * 16;
-            const uint32_t idesc0 = idesc_mxf8f6f4(nmma, 0);  // + ks * kIdescSfStep for K step ks
+            // mxf8f6f4: + ks * kIdescSfStep for K step ks; mxf4: + kIdescSf2 for odd ks
+            const uint32_t idesc0 = FP4 ? idesc_mxf4(nmma) : idesc_mxf8f6f4(nmma, 0);
             const int buf = jb & 1;
             // the epilogue has finished with this accumulator (two tiles ago)
             int okl = 1;
@@ -579,20 +656,36 @@ __global__ void __launch_bounds__(NT, GemmShape<NT>::kCtasPerSm)
                         const uint64_t sfbd = sfbdesc0 + (uint64_t)((uint32_t)sq * sfb_stage16);
                         const uint64_t ad0 = adesc0 + (uint64_t)((uint32_t)sq * a_stage16);
                         const uint64_t bd0 = bdesc0 + (uint64_t)((uint32_t)sq * b_stage16);
-                        for (int t = 0; t < tpi; t++) tc_cp_sf(sfa_t + 4u * t, sfad + (uint64_t)(32 * t));  // 512 B apart
-                        if (nsfb == 1)
-                            tc_cp_sf(sfb_t, sfbd);
-                        else
-                            tc_cp_sf2(sfb_t, sfbd);
-                        for (int t = 0; t < tpi; t++) {
-                            // tile t: rows 128t.. of the stage's A (16 KB apart), accumulator columns t*BN..
-                            const uint64_t adt = ad0 + (uint64_t)(1024 * t);
+                        if constexpr (FP4) {
+                            // two 128-K scale atoms per operand (one in the last stage of an
+                            // odd count): K step ks (64 K) reads atom ks / 2, bytes 2 (ks % 2)..
+                            const int n2 = min(2, a.nkt_sf - 2 * (kt + q));
+                            const uint32_t sfb_t4 = sfa_t + 8u;
+                            for (int j = 0; j < n2; j++) {
+                                tc_cp_sf(sfa_t + 4u * j, sfad + (uint64_t)(32 * j));
+                                tc_cp_sf(sfb_t4 + 4u * j, sfbd + (uint64_t)(32 * j));
+                            }
+                            for (int ks = 0; ks < 2 * n2; ks++)
+                                tc_mma_f4(acc, ad0 + (uint64_t)(2 * ks), bd0 + (uint64_t)(2 * ks),
+                                          idesc0 + ((ks & 1) ? kIdescSf2 : 0u), sfa_t + 4u * (ks >> 1),
+                                          sfb_t4 + 4u * (ks >> 1), (kt + q > 0 || ks > 0) ? 1u : 0u);
+                        } else {
+                            for (int t = 0; t < tpi; t++)
+                                tc_cp_sf(sfa_t + 4u * t, sfad + (uint64_t)(32 * t));  // 512 B apart
+                            if (nsfb == 1)
+                                tc_cp_sf(sfb_t, sfbd);
+                            else
+                                tc_cp_sf2(sfb_t, sfbd);
+                            for (int t = 0; t < tpi; t++) {
+                                // tile t: rows 128t.. of the stage's A (16 KB apart), accumulator columns t*BN..
+                                const uint64_t adt = ad0 + (uint64_t)(1024 * t);
 #pragma unroll
-                            for (int ks = 0; ks < kTileK / 32; ks++) {
-                                // K step ks: 32 bytes further along both operands' rows
-                                tc_mma(acc + (uint32_t)(t * a.BN), adt + (uint64_t)(2 * ks), bd0 + (uint64_t)(2 * ks),
-                                       idesc0 + (uint32_t)ks * kIdescSfStep, sfa_t + 4u * t, sfb_t,
-                                       (kt + q > 0 || ks > 0) ? 1u : 0u);
+                                for (int ks = 0; ks < kTileK / 32; ks++) {
+                                    // K step ks: 32 bytes further along both operands' rows
+                                    tc_mma(acc + (uint32_t)(t * a.BN), adt + (uint64_t)(2 * ks),
+                                           bd0 + (uint64_t)(2 * ks), idesc0 + (uint32_t)ks * kIdescSfStep,
+                                           sfa_t + 4u * t, sfb_t, (kt + q > 0 || ks > 0) ? 1u : 0u);
+                                }
                             }
                         }
                         tc_commit(&empty[sq]);  // frees the stage when these MMAs have read it
@@ -637,8 +730,8 @@ __global__ void __launch_bounds__(NT, GemmShape<NT>::kCtasPerSm)
                     epilogue_split3(a, lane_base, ok, nn, nmma, J.mt + t, J.row0, J.n0(), J.tile(), ew, wg,
                                     Shape::kWarpGroups, lane, amax_g);
                 else
-                    epilogue_mx1(a, lane_base, ok, nn, nmma, J.mt + t, J.row0, J.n0(), J.tile(), ew, wg,
-                                 Shape::kWarpGroups, lane, amax_g);
+                    epilogue_mx1<FP4>(a, lane_base, ok, nn, nmma, J.mt + t, J.row0, J.n0(), J.tile(), ew, wg,
+                                      Shape::kWarpGroups, lane, amax_g);
             }
             tc_fence_before();
             __syncwarp();
@@ -685,7 +778,22 @@ cudaError_t make_map_a(CUtensorMap *m, const void *base, int K, int rows, int E,
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-// B: E4M3 rows [P][K] (one byte per element), boxes of box_rows rows.
+// A with FP4 rows: the same weights as plain bytes (two E2M1 codes per byte, the
+// packed operand format of kind::mxf4), K_bytes = K / 2 per row, boxes of 128 bytes.
+cudaError_t make_map_a4(CUtensorMap *m, const void *base, int K_bytes, int rows, int E, uint64_t row_stride,
+                        uint64_t rec, int box_rows) {
+    cuuint64_t dims[3] = {(cuuint64_t)K_bytes, (cuuint64_t)rows, (cuuint64_t)E};
+    cuuint64_t strides[2] = {row_stride, rec};
+    cuuint32_t box[3] = {kTileK, (cuuint32_t)box_rows, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(base), dims, strides, box, es,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+// B: activation rows [P][K] bytes (E4M3, one per element; or E2M1 pairs, K = row
+// bytes), boxes of 128 bytes x box_rows rows.
 cudaError_t make_map_b(CUtensorMap *m, const void *base, int K, int P, int box_rows) {
     cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)P};
     cuuint64_t strides[1] = {(cuuint64_t)K};
@@ -708,6 +816,8 @@ PerDevice g_sms(0);
 
 PerDevice g_smem_set_384(0);
 PerDevice g_smem_set_192(0);
+PerDevice g_smem_set_384f4(0);
+PerDevice g_smem_set_192f4(0);
 
 // One grouped GEMM launch (args complete but for the shape fields set here).  The
 // kernel's shape: narrow tiles (BN <= 64, and the gate/up GEMM at BN <= 96) run two
@@ -715,40 +825,63 @@ PerDevice g_smem_set_192(0);
 // each; wider tiles run one CTA of 12 warps per SM, with two 128-row tiles per item
 // (one 256-row tensor copy) while their four accumulators fit in TMEM.  Measured on the
 // full-size layer: two CTAs per SM took the 512-token GEMMs from 3.84 to 3.03 ms; the
-// down GEMM at BN = 96 and all GEMMs at BN >= 128 are faster with one.
+// down GEMM at BN = 96 and all GEMMs at BN >= 128 are faster with one.  With FP4 rows
+// (BN <= 128, one B scale atom) every item is one 128-row tile, and a stage holds two
+// scale atoms per operand (16 TMEM columns).  a_k and b_k are K in elements.
 cudaError_t launch_one(GemmArgs ga, const uint8_t *a_base, int a_k, int a_rows, uint64_t a_ld, int E, const uint8_t *b_base,
-                       int b_k, int b_rows, int nexp, const char *trace_name, cudaStream_t stream) {
+                       int b_k, int b_rows, int nexp, const char *trace_name, cudaStream_t stream, bool fp4) {
     const int BN = ga.BN, nsfb = ga.nsfb;
+    if (fp4 && nsfb != 1) return cudaErrorNotSupported;
     int smem_max = 0, sms = 0;
     cudaError_t e = device_attr(cudaDevAttrMaxSharedMemoryPerBlockOptin, g_smem_max, &smem_max);
     if (e != cudaSuccess) return e;
     if ((e = device_attr(cudaDevAttrMultiProcessorCount, g_sms, &sms)) != cudaSuccess) return e;
     const bool two = BN <= 64 || (BN <= 96 && ga.mode == 1);
-    const int tpi = two ? 1 : (BN <= 96 ? 2 : 1);
+    const int tpi = fp4 || two ? 1 : (BN <= 96 ? 2 : 1);
     const uint32_t smem_cap = two ? (uint32_t)(smem_max / 2 - 1024) : (uint32_t)smem_max;
     const uint32_t tmem_cap = two ? 256u : 512u;
     // as many pipeline stages as fit the CTA's share of shared memory and TMEM
     int ns = kMaxStages;
-    auto tmem_need = [&](int n) { return (uint32_t)(2 * tpi * BN + n * (4 * tpi + 4 * nsfb)); };
-    while (ns > 2 && (GemmSmemLayout(BN, ns, tpi).total + 1024 > smem_cap || tmem_need(ns) > tmem_cap)) ns--;
+    const uint32_t sf_cols = fp4 ? 8u * tpi + 8u : 4u * tpi + 4u * nsfb;
+    auto tmem_need = [&](int n) { return (uint32_t)(2 * tpi * BN) + (uint32_t)n * sf_cols; };
+    auto smem_need = [&](int n) { return GemmSmemLayout(BN, n, tpi, fp4).total + 1024; };  // + alignment slack
+    while (ns > 2 && (smem_need(ns) > smem_cap || tmem_need(ns) > tmem_cap)) ns--;
     const uint32_t tmem_cols = pow2_at_least(tmem_need(ns));
-    if (tmem_cols > tmem_cap || GemmSmemLayout(BN, ns, tpi).total + 1024 > smem_cap) return cudaErrorNotSupported;
-    const size_t smem = GemmSmemLayout(BN, ns, tpi).total + 1024;  // alignment slack
-    e = two ? ensure_dynamic_smem(grouped_gemm_kernel<192>, smem, g_smem_set_192)
-            : ensure_dynamic_smem(grouped_gemm_kernel<384>, smem, g_smem_set_384);
+    if (tmem_cols > tmem_cap || smem_need(ns) > smem_cap) return cudaErrorNotSupported;
+    const size_t smem = smem_need(ns);
+    if (fp4)
+        e = two ? ensure_dynamic_smem(grouped_gemm_kernel<192, true>, smem, g_smem_set_192f4)
+                : ensure_dynamic_smem(grouped_gemm_kernel<384, true>, smem, g_smem_set_384f4);
+    else
+        e = two ? ensure_dynamic_smem(grouped_gemm_kernel<192, false>, smem, g_smem_set_192)
+                : ensure_dynamic_smem(grouped_gemm_kernel<384, false>, smem, g_smem_set_384);
     if (e != cudaSuccess) return e;
     ga.ns = ns;
     ga.tpi = tpi;
     ga.tmem_cols = tmem_cols;
+    ga.nkt_sf = a_k / kTileK;
+    ga.nkt = fp4 ? (ga.nkt_sf + 1) / 2 : ga.nkt_sf;
     CUtensorMap mA, mB;
-    if ((e = make_map_a(&mA, a_base, a_k, a_rows, E, a_ld, ga.rec, tpi * kTileM)) != cudaSuccess) return e;
-    if ((e = make_map_b(&mB, b_base, b_k, b_rows, BN)) != cudaSuccess) return e;
+    if (fp4) {
+        if ((e = make_map_a4(&mA, a_base, a_k / 2, a_rows, E, a_ld, ga.rec, kTileM)) != cudaSuccess) return e;
+        if ((e = make_map_b(&mB, b_base, b_k / 2, b_rows, BN)) != cudaSuccess) return e;
+    } else {
+        if ((e = make_map_a(&mA, a_base, a_k, a_rows, E, a_ld, ga.rec, tpi * kTileM)) != cudaSuccess) return e;
+        if ((e = make_map_b(&mB, b_base, b_k, b_rows, BN)) != cudaSuccess) return e;
+    }
     const int items = nexp * ((ga.nmt + tpi - 1) / tpi);
     TraceScope trace_scope(trace_name, stream);
-    if (two)
-        grouped_gemm_kernel<192><<<std::min(2 * sms, items), 192, smem, stream>>>(mA, mB, ga);
-    else
-        grouped_gemm_kernel<384><<<std::min(sms, items), 384, smem, stream>>>(mA, mB, ga);
+    if (fp4) {
+        if (two)
+            grouped_gemm_kernel<192, true><<<std::min(2 * sms, items), 192, smem, stream>>>(mA, mB, ga);
+        else
+            grouped_gemm_kernel<384, true><<<std::min(sms, items), 384, smem, stream>>>(mA, mB, ga);
+    } else {
+        if (two)
+            grouped_gemm_kernel<192, false><<<std::min(2 * sms, items), 192, smem, stream>>>(mA, mB, ga);
+        else
+            grouped_gemm_kernel<384, false><<<std::min(sms, items), 384, smem, stream>>>(mA, mB, ga);
+    }
     return cudaGetLastError();
 }
 
@@ -757,16 +890,18 @@ cudaError_t launch_one(GemmArgs ga, const uint8_t *a_base, int a_k, int a_rows, 
 cudaError_t set_wait_limit_gemm(uint64_t ns) { return set_wait_limit_here(ns); }
 
 cudaError_t launch_grouped_gemms(const PoolView &v, int T, int k, const int32_t *offsets, const GroupedWs &g,
-                                 void *partial, int partial_dtype, StatusWord *st, cudaStream_t stream, int nparts) {
+                                 void *partial, int partial_dtype, StatusWord *st, cudaStream_t stream, int nparts,
+                                 bool fp4) {
     const int P = T * k;
     if (P == 0) return cudaSuccess;
     if (nparts != 1 && nparts != 3) return cudaErrorInvalidValue;
+    if (fp4 && nparts != 1) return cudaErrorInvalidValue;
     cudaError_t e = get_encoder();
     if (e != cudaSuccess) return e;
     // one expert has at most T pairs (distinct slots of a row), so with three parts
     // all of its 3T columns fit one tile; the sort laid out the activation scales
     // for this BN
-    const int BN = grouped_bn(P, v.E, T, nparts);
+    const int BN = grouped_bn(P, v.E, T, nparts, fp4);
     if (BN == 0) return cudaErrorNotSupported;
     if (BN != g.BN) return cudaErrorInvalidValue;
     const int nsfb = g.nsfb;
@@ -793,21 +928,21 @@ cudaError_t launch_grouped_gemms(const PoolView &v, int T, int k, const int32_t 
 
     // GEMM 1: gate/up
     ga.mode = 1;
-    ga.nkt = v.H / kTileK;
     ga.a_sf_off = v.off_sgu_mma;
     ga.bscale = g.xs;
     ga.nmt = v.nmt_gu;
-    e = launch_one(ga, v.base, v.H, 2 * v.I, (uint64_t)v.ld_gu, v.E, g.xq, v.H, nparts * P, nexp, "gemm_gateup", stream);
+    e = launch_one(ga, v.base, v.H, 2 * v.I, (uint64_t)v.ld_gu, v.E, g.xq, v.H, nparts * P, nexp, "gemm_gateup", stream,
+                   fp4);
     if (e != cudaSuccess) return e;
 
-    // GEMM 2: down
+    // GEMM 2: down (K = Ip, the W_d rows padded with zero codes; h has I columns, the
+    // rest of its last box is zero-filled)
     ga.mode = 2;
-    ga.nkt = v.Ip / kTileK;
     ga.a_sf_off = v.off_sd_mma;
     ga.bscale = g.hs;
     ga.nmt = v.nmt_d;
     return launch_one(ga, v.base + v.off_d, v.Ip, v.H, (uint64_t)v.ld_d, v.E, g.hq, v.I, nparts * P, nexp, "gemm_down",
-                      stream);
+                      stream, fp4);
 }
 
 }  // namespace moe

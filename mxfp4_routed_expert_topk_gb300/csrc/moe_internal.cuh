@@ -226,7 +226,7 @@ cudaError_t launch_grouped(const PoolView &v, const uint16_t *x, int T, const in
 cudaError_t launch_combine(const void *partial, int partial_dtype, const int32_t *inv_perm, const float *w,
                            int T, int k, int H, const uint16_t *residual, uint16_t *y, cudaStream_t st);
 // Diagnostics: the MXFP8 h of the last grouped call on `ws`, in sorted row order.
-cudaError_t launch_read_h(const PoolView &v, int T, int k, const int32_t *offsets, const void *ws, uint8_t *hq,
-                          uint8_t *hs, cudaStream_t st);
+cudaError_t launch_read_h(const PoolView &v, int T, int k, int act_mode, const int32_t *offsets, const void *ws,
+                          uint8_t *hq, uint8_t *hs, cudaStream_t st);
 
 }  // namespace moe

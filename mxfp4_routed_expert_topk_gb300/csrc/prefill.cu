@@ -11,6 +11,8 @@
 //        y[t] = sum_j w[t,j] partial[inv_perm[t*k+j]] (+ residual), slot order
 // The multi-token decode (launch_decode_multi) uses the same pieces with a one-CTA
 // sort (sort_small_kernel) and three-part activations (gather_split3_kernel).
+#include <algorithm>
+
 #include "moe_internal.cuh"
 #include "prefill_internal.cuh"
 
@@ -295,6 +297,82 @@ __global__ void gather_quant_kernel(const uint16_t *__restrict__ x, int T, int H
     if (chunk == 0 && myrow >= 0) zero_h_pad(hs, I, nsfb, myrt);
 }
 
+// gather_quant_kernel with MXFP4 rows: shared exponent X = floor(log2 amax) - 2 per
+// 32-block (E2M1 emax 2), codes RNE(x / 2^X) to E2M1 with saturation, two per byte
+// (rows of H/2 bytes: a lane's 8 elements are one 4-byte word).  The scale words go
+// to the same tile-ordered blocks.
+__global__ void gather_quant4_kernel(const uint16_t *__restrict__ x, int T, int H, int I, int k,
+                                     const int32_t *__restrict__ idx, const int32_t *__restrict__ inv_perm,
+                                     const int32_t *__restrict__ offsets, const int32_t *__restrict__ tile_off, int BN,
+                                     int nsfb, uint8_t *__restrict__ xq, uint8_t *__restrict__ xs,
+                                     uint8_t *__restrict__ hs) {
+    const int lane = threadIdx.x & 31;
+    const int nchunk = (H + kGatherChunk - 1) / kGatherChunk;
+    const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int t = gw / nchunk, chunk = gw % nchunk;
+    if (t >= T) return;
+    int myrow = -1;
+    RowTile myrt{0, 0};
+    if (lane < k) {
+        const int p = t * k + lane;
+        myrow = inv_perm[p];
+        if (myrow >= 0) {
+            const int e = idx[p];
+            myrt = row_tile(e, myrow - offsets[e], tile_off, BN);
+        }
+    }
+    const uint16_t *xr = x + (size_t)t * H;
+    const int b_end = min(H, (chunk + 1) * kGatherChunk);
+    for (int b0 = chunk * kGatherChunk; b0 < b_end; b0 += 256) {
+        const bool on = b0 + lane * 8 < b_end;
+        float f[8];
+        if (on) {
+            const uint4 v = *reinterpret_cast<const uint4 *>(xr + b0 + lane * 8);
+            const unsigned int u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int i = 0; i < 4; i++) {
+                f[2 * i] = __uint_as_float(u[i] << 16);
+                f[2 * i + 1] = __uint_as_float(u[i] & 0xffff0000u);
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; i++) f[i] = 0.f;
+        }
+        float a = 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; i++) a = fmaxf(a, fabsf(f[i]));
+        a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
+        a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
+        int X = -127;
+        if (a > 0.f) {
+            int ex;
+            frexpf(a, &ex);
+            X = max(-127, min(127, ex - 1 - 2));
+        }
+#pragma unroll
+        for (int i = 0; i < 8; i++) f[i] = ldexpf(f[i], -X);
+        const uint32_t q = e2m1x8_rn(f);
+        const uint32_t sb = (uint32_t)(X + 127);
+        const uint32_t b1 = __shfl_down_sync(0xffffffffu, sb, 4);
+        const uint32_t b2 = __shfl_down_sync(0xffffffffu, sb, 8);
+        const uint32_t b3 = __shfl_down_sync(0xffffffffu, sb, 12);
+        const uint32_t word = sb | (b1 << 8) | (b2 << 16) | (b3 << 24);
+        const int kt = (b0 + lane * 8) >> 7;
+        for (int j = 0; j < k; j++) {
+            const int r = __shfl_sync(0xffffffffu, myrow, j);
+            if (r < 0) continue;  // warp-uniform
+            const int tile = __shfl_sync(0xffffffffu, myrt.tile, j);
+            const int col = __shfl_sync(0xffffffffu, myrt.col, j);
+            if (on) {
+                *reinterpret_cast<uint32_t *>(xq + (size_t)r * (H / 2) + (b0 + lane * 8) / 2) = q;
+                if ((lane & 15) == 0)
+                    *reinterpret_cast<uint32_t *>(xs + sf_tile_word(tile, H / 128, nsfb, kt, col)) = word;
+            }
+        }
+    }
+    if (chunk == 0 && myrow >= 0) zero_h_pad(hs, I, nsfb, myrt);
+}
+
 // Row r of the sorted pairs: x[perm[r] / k] as three E4M3 parts (rows 3r, 3r+1,
 // 3r+2) with one E8M0 scale per part and 32-block (split_part), scales in the
 // tile-ordered blocks.  One warp per (row, group of 8 blocks of 32).
@@ -443,12 +521,13 @@ bool combine4_ok(const void *partial, int partial_dtype, int H, const uint16_t *
            (residual == nullptr || (uintptr_t)residual % 8 == 0);
 }
 
-// Diagnostics: MXFP8 h of sorted row r and 32-block b as the gate/up epilogue wrote
-// it (codes [P][I], and the scale byte from the tile-ordered blocks).  One thread
-// per (row, block); the row's expert is the last e with offsets[e] <= r.
+// Diagnostics: the MX-quantised h of sorted row r and 32-block b as the gate/up
+// epilogue wrote it (codes, one per byte of the output, and the scale byte from the
+// tile-ordered blocks).  One thread per (row, block); the row's expert is the last e
+// with offsets[e] <= r.
 __global__ void read_h_kernel(int E, int I, const int32_t *__restrict__ offsets, const int32_t *__restrict__ tile_off,
-                              int BN, int nsfb, const uint8_t *__restrict__ hq_ws, const uint8_t *__restrict__ hs_ws,
-                              uint8_t *__restrict__ hq, uint8_t *__restrict__ hs) {
+                              int BN, int nsfb, bool fp4, const uint8_t *__restrict__ hq_ws,
+                              const uint8_t *__restrict__ hs_ws, uint8_t *__restrict__ hq, uint8_t *__restrict__ hs) {
     const int nb = I / 32;
     const size_t gid = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int P = offsets[E];
@@ -463,6 +542,14 @@ __global__ void read_h_kernel(int E, int I, const int32_t *__restrict__ offsets,
     const RowTile rt = row_tile(lo, r - offsets[lo], tile_off, BN);
     const int ip = (I + 127) / 128 * 128;
     hs[(size_t)r * nb + b] = hs_ws[sf_tile_word(rt.tile, ip / 128, nsfb, b >> 2, rt.col) + (b & 3)];
+    if (fp4) {
+        const uint8_t *src = hq_ws + (size_t)r * (I / 2) + 16 * b;
+        for (int j = 0; j < 16; j++) {
+            hq[(size_t)r * I + 32 * b + 2 * j] = src[j] & 15;
+            hq[(size_t)r * I + 32 * b + 2 * j + 1] = src[j] >> 4;
+        }
+        return;
+    }
     const uint4 *src = reinterpret_cast<const uint4 *>(hq_ws + (size_t)r * I + 32 * b);
     uint4 *dst = reinterpret_cast<uint4 *>(hq + (size_t)r * I + 32 * b);
     dst[0] = src[0];
@@ -471,26 +558,29 @@ __global__ void read_h_kernel(int E, int I, const int32_t *__restrict__ offsets,
 
 }  // namespace
 
-cudaError_t launch_read_h(const PoolView &v, int T, int k, const int32_t *offsets, const void *ws, uint8_t *hq,
-                          uint8_t *hs, cudaStream_t st) {
-    const GroupedWs g = grouped_ws_layout(const_cast<void *>(ws), v.E, v.H, v.I, T, k);
+cudaError_t launch_read_h(const PoolView &v, int T, int k, int act_mode, const int32_t *offsets, const void *ws,
+                          uint8_t *hq, uint8_t *hs, cudaStream_t st) {
+    const bool fp4 = act_mode == MOE_ACT_MXFP4;
+    const GroupedWs g = grouped_ws_layout(const_cast<void *>(ws), v.E, v.H, v.I, T, k, 1, fp4);
     const size_t n = (size_t)T * k * (v.I / 32);
     if (n == 0) return cudaSuccess;
-    read_h_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(v.E, v.I, offsets, g.tile_off, g.BN, g.nsfb, g.hq, g.hs,
-                                                               hq, hs);
+    read_h_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(v.E, v.I, offsets, g.tile_off, g.BN, g.nsfb, fp4, g.hq,
+                                                               g.hs, hq, hs);
     return cudaGetLastError();
 }
 
 size_t grouped_workspace_bytes(int E, int H, int I, int T, int k) {
-    return grouped_ws_layout(nullptr, E, H, I, T, k).end;
+    // either activation format (MXFP4 tiles are narrower, so more of them)
+    return std::max(grouped_ws_layout(nullptr, E, H, I, T, k, 1, false).end,
+                    grouped_ws_layout(nullptr, E, H, I, T, k, 1, true).end);
 }
 
 cudaError_t launch_grouped(const PoolView &v, const uint16_t *x, int T, const int32_t *idx, int k, int act_mode,
                            int32_t *perm, int32_t *inv_perm, int32_t *offsets, void *partial, int partial_dtype,
                            void *ws, cudaStream_t st) {
-    (void)act_mode;
     if (v.E > kMaxSortE) return cudaErrorNotSupported;
-    const GroupedWs g = grouped_ws_layout(ws, v.E, v.H, v.I, T, k);
+    const bool fp4 = act_mode == MOE_ACT_MXFP4;
+    const GroupedWs g = grouped_ws_layout(ws, v.E, v.H, v.I, T, k, 1, fp4);
     StatusWord *stw = reinterpret_cast<StatusWord *>(ws);
     const int P = T * k;
     if (P == 0) {
@@ -514,10 +604,15 @@ cudaError_t launch_grouped(const PoolView &v, const uint16_t *x, int T, const in
     {
         TraceScope trace_scope("gather_quant", st);
         const int nchunk = (v.H + kGatherChunk - 1) / kGatherChunk;
-        gather_quant_kernel<<<(unsigned)(((size_t)T * nchunk * 32 + 255) / 256), 256, 0, st>>>(
-            x, T, v.H, v.I, k, idx, inv_perm, offsets, g.tile_off, g.BN, g.nsfb, g.xq, g.xs, g.hs);
+        const unsigned nblk = (unsigned)(((size_t)T * nchunk * 32 + 255) / 256);
+        if (fp4)
+            gather_quant4_kernel<<<nblk, 256, 0, st>>>(x, T, v.H, v.I, k, idx, inv_perm, offsets, g.tile_off, g.BN,
+                                                       g.nsfb, g.xq, g.xs, g.hs);
+        else
+            gather_quant_kernel<<<nblk, 256, 0, st>>>(x, T, v.H, v.I, k, idx, inv_perm, offsets, g.tile_off, g.BN,
+                                                      g.nsfb, g.xq, g.xs, g.hs);
     }
-    cudaError_t e = launch_grouped_gemms(v, T, k, offsets, g, partial, partial_dtype, stw, st);
+    cudaError_t e = launch_grouped_gemms(v, T, k, offsets, g, partial, partial_dtype, stw, st, 1, fp4);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }

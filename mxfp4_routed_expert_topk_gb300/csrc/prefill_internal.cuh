@@ -10,21 +10,24 @@ namespace moe {
 constexpr int kMaxSortE = 4096;  // experts supported by the grouped path
 
 constexpr int kMaxBN = 192;      // accumulator columns of a grouped-GEMM tile
+constexpr int kMaxBN4 = 128;     // ... with MXFP4 activations (one scale atom per K tile)
 
 // Accumulator columns per tile (BN) of the grouped GEMMs for P pairs over E experts,
 // T rows, nparts activation rows per pair; 0 when the shape is not supported.
 // nparts = 1: 1.5 times the mean rows per expert rounded up to 32, 32..192 (an expert
-// with more rows takes several tiles; narrow tiles let the GEMMs run two CTAs per SM).
+// with more rows takes several tiles; narrow tiles let the GEMMs run two CTAs per SM),
+// at most 128 with MXFP4 activations (fp4).
 // nparts = 3: all of an expert's rows (at most 3T) in one tile, in whole groups of 16
 // pairs.
-__host__ __device__ inline int grouped_bn(int P, int E, int T, int nparts) {
+__host__ __device__ inline int grouped_bn(int P, int E, int T, int nparts, bool fp4 = false) {
     if (nparts == 3) {
         const int bn = (3 * T + 47) / 48 * 48;
         return bn > kMaxBN ? 0 : bn;
     }
+    const int cap = fp4 ? kMaxBN4 : kMaxBN;
     const int mean = (P + E - 1) / E;
     int bn = (3 * mean / 2 + 31) / 32 * 32;
-    return bn < 32 ? 32 : (bn > kMaxBN ? kMaxBN : bn);
+    return bn < 32 ? 32 : (bn > cap ? cap : bn);
 }
 
 // Scale factors of the activation operand (B) in the layout the MMA consumes, one
@@ -50,10 +53,11 @@ __host__ __device__ inline size_t sf_tile_word(int tile, int nkt, int nsfb, int 
 __host__ __device__ inline uint32_t sfb_stage_bytes(int nsfb) { return nsfb == 1 ? 512u : 4096u; }
 
 // Activation rows of the grouped GEMMs.  nparts = 1: one MXFP8 row per pair (OCP
-// rule, the prefill path).  nparts = 3: the value is the sum of three E4M3 parts
-// with their own E8M0 scales (see split_exp), which represents a bf16 row exactly
-// for elements within about 20 binades of their 32-block's max (the multi-token
-// decode path); row 3r+q holds part q of sorted pair r.
+// rule, the prefill path), or with fp4 one MXFP4 row (two E2M1 codes per byte,
+// element 2j in the low nibble: rows of H/2 and I/2 bytes).  nparts = 3: the value
+// is the sum of three E4M3 parts with their own E8M0 scales (see split_exp), which
+// represents a bf16 row exactly for elements within about 20 binades of their
+// 32-block's max (the multi-token decode path); row 3r+q holds part q of pair r.
 struct GroupedWs {
     int *local_rank;  // [P]
     int *cnt;         // [nblocks][E]
@@ -63,20 +67,21 @@ struct GroupedWs {
     int32_t *tile_off;// [E+1] first column tile of each expert (exclusive scan of its tiles)
     int BN, nsfb;     // columns per tile, 512-byte scale atoms per tile and K tile
     int max_tiles;    // bound on the column tiles of all experts
-    uint8_t *xq;      // [nparts*P][H]    E4M3 rows of x in sorted order
+    uint8_t *xq;      // [nparts*P][H]    E4M3 rows of x in sorted order ([P][H/2] E2M1 pairs with fp4)
     uint8_t *xs;      // [max_tiles][H/128][nsfb][512]  their E8M0 scales (sf_tile_word)
-    uint8_t *hq;      // [nparts*P][I]    E4M3 rows of h in sorted order
+    uint8_t *hq;      // [nparts*P][I]    E4M3 rows of h in sorted order ([P][I/2] with fp4)
     uint8_t *hs;      // [max_tiles][Ip/128][nsfb][512] Ip = I rounded up to 128; the
                       //                   scale bytes of blocks I/32.. are 0 (2^-127)
     size_t end;       // total bytes
 };
 
-__host__ __device__ inline GroupedWs grouped_ws_layout(void *ws, int E, int H, int I, int T, int k, int nparts = 1) {
+__host__ __device__ inline GroupedWs grouped_ws_layout(void *ws, int E, int H, int I, int T, int k, int nparts = 1,
+                                                       bool fp4 = false) {
     GroupedWs g;
     const size_t P = (size_t)T * k;
     const size_t R = P * (size_t)nparts;
     const size_t nblocks = (P + 1023) / 1024;
-    const int bn = grouped_bn((int)P, E, T, nparts);
+    const int bn = grouped_bn((int)P, E, T, nparts, fp4);
     g.BN = bn > 0 ? bn : 48;  // (an unsupported shape is refused at launch)
     g.nsfb = (g.BN + 127) / 128;
     // sum over experts of ceil(rows_e / BN) <= R / BN + (experts with rows)
@@ -133,6 +138,32 @@ __device__ __forceinline__ int split_exp(float amax) {
     return max(-127, min(127, ex - 1 - 7));
 }
 
+// Eight values -> eight E2M1 codes (round to nearest even, saturating at +-6), two
+// per byte with element 2j in the low nibble: bytes 0..3 of the result.
+__device__ __forceinline__ uint32_t e2m1x8_rn(const float (&f)[8]) {
+    uint32_t r;
+    asm("{\n\t.reg .b8 q0, q1, q2, q3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 q0, %2, %1;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 q1, %4, %3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 q2, %6, %5;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 q3, %8, %7;\n\t"
+        "mov.b32 %0, {q0, q1, q2, q3};\n\t}"
+        : "=r"(r)
+        : "f"(f[0]), "f"(f[1]), "f"(f[2]), "f"(f[3]), "f"(f[4]), "f"(f[5]), "f"(f[6]), "f"(f[7]));
+    return r;
+}
+
+// Two values -> one byte of E2M1 codes (lo in the low nibble).
+__device__ __forceinline__ uint8_t e2m1x2_rn(float lo, float hi) {
+    uint32_t r;
+    asm("{\n\t.reg .b8 q;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 q, %1, %2;\n\t"
+        "mov.b32 %0, {q, q, q, q};\n\t}"
+        : "=r"(r)
+        : "f"(hi), "f"(lo));
+    return (uint8_t)(r & 0xFFu);
+}
+
 __device__ __forceinline__ uint8_t e4m3_rn(float v) {
     unsigned short pair;
     asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(pair) : "f"(0.f), "f"(v));
@@ -157,7 +188,7 @@ __device__ __forceinline__ uint8_t split_part(float &r, int X) {
 // then down), over the sorted rows.
 cudaError_t launch_grouped_gemms(const PoolView &v, int T, int k, const int32_t *offsets, const GroupedWs &g,
                                  void *partial, int partial_dtype, StatusWord *st, cudaStream_t stream,
-                                 int nparts = 1);
+                                 int nparts = 1, bool fp4 = false);
 
 // Multi-token decode (M > 1) through the grouped GEMMs with three-part activations;
 // cudaErrorNotSupported for shapes the GEMMs do not take.

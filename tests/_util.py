@@ -58,7 +58,7 @@ def bf16_half_ulp(v: np.ndarray) -> np.ndarray:
     return np.exp2(np.maximum(e, -126.0) - 8)
 
 
-def check_close(y: np.ndarray, ref: np.ndarray, what: str = "y", amb=None, bf16_at=None):
+def check_close(y: np.ndarray, ref: np.ndarray, what: str = "y", amb=None, bf16_at=None, l1_on=None):
     """The float tolerance: max|y - ref| <= 2e-2 * RMS(ref), relative L1 <= 5e-3, with
     two per-element allowances that name a stated rounding step:
       - `amb` (tensor-core prefill path): the largest change that equally valid MXFP8
@@ -67,10 +67,14 @@ def check_close(y: np.ndarray, ref: np.ndarray, what: str = "y", amb=None, bf16_
       - `bf16_at`: the values that were rounded to the stated bf16 output format (the
         GPU output itself, or the residual stream it was fused with); each element may
         also differ by the half-ulp of that rounding, which at |y| beyond about
-        10 * RMS exceeds 2e-2 * RMS by itself."""
+        10 * RMS exceeds 2e-2 * RMS by itself.
+    `l1_on` = (output, reference) on which the relative L1 error is taken when that
+    is not (y, ref): for a layer fused with its residual, the max error is judged on
+    the MoE part and the relative L1 on the layer's output, the residual stream."""
     err = np.abs(y - ref)
     rms = float(np.sqrt(np.mean(ref * ref)))
-    rel = float(err.sum() / max(np.abs(ref).sum(), 1e-300))
+    yl, rl = (y, ref) if l1_on is None else l1_on
+    rel = float(np.abs(yl - rl).sum() / max(np.abs(rl).sum(), 1e-300))
     tol = MAX_ERR_RMS * rms
     allow = np.zeros_like(err) if bf16_at is None else bf16_half_ulp(np.abs(bf16_at) + tol)
     over = err - allow

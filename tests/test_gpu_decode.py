@@ -407,9 +407,9 @@ def test_stacked_layers_oracle_forced(tiny):
         assert np.array_equal(idx.cpu().numpy(), ly["idx"])
         y = moe.moe_expert_forward_decode(gpools[l], xh, idx, w, residual=x)
         # the layer output is bf16(x + MoE(x_hat)): its MoE part against the oracle's,
-        # with the half-ulp of the bf16 residual stream
-        xl = synth.bf16_bits_to_f64(ly["x"])
-        check_close(bf16_to_f64(y) - xl, ly["y"], "stacked tiny, oracle-forced", bf16_at=bf16_to_f64(y))
+        # with the half-ulp of the bf16 residual stream; relative L1 on the output
+        xl, xn = synth.bf16_bits_to_f64(ly["x"]), bf16_to_f64(y)
+        check_close(xn - xl, ly["y"], "stacked tiny, oracle-forced", bf16_at=xn, l1_on=(xn, xl + ly["y"]))
 
 
 def test_stacked_layers_full_size():
@@ -456,9 +456,10 @@ def test_stacked_layers_full_size():
         d = oracle.decode_layer(opools[l], xh_ref, routers[l], s.k, skews[l])
         assert np.array_equal(idxs[l], d["idx"]), l
         # x_{l+1} = bf16(x_l + MoE(x_hat_l)): the MoE part against the oracle's, with the
-        # half-ulp of the bf16 residual stream
+        # half-ulp of the bf16 residual stream; relative L1 on x_{l+1}
         xn, xl = synth.bf16_bits_to_f64(xs[l + 1]), synth.bf16_bits_to_f64(xs[l])
-        check_close(xn - xl, d["y"], "config 2: 8 full layers, teacher-forced per layer", bf16_at=xn)
+        check_close(xn - xl, d["y"], "config 2: 8 full layers, teacher-forced per layer", bf16_at=xn,
+                    l1_on=(xn, xl + d["y"]))
     # free-running
     diverged, ys, refs = [], [], []
     for t in range(ntok):

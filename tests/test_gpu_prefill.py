@@ -23,7 +23,7 @@ def _built():
     oracle.build()
 
 
-def _run(s, T, seed, sample=None, partial_dtype=0):
+def _run(s, T, seed, sample=None, partial_dtype=0, act_mode=1):
     pool = moe.Pool(s.E, s.H, s.I)
     moe.moe_pool_fill_synthetic(pool, seed)
     Wrb = synth.router_bf16(seed + 1, s.E, s.H)
@@ -31,11 +31,12 @@ def _run(s, T, seed, sample=None, partial_dtype=0):
     x = to_dev_bf16(xb)
     idx, w = moe.moe_route_topk(x, to_dev_bf16(Wrb), s.k)
     ws = moe.workspace(moe.moe_workspace_size(moe.MOE_OP_GROUPED, s.E, s.H, s.I, T, s.k))
-    out = moe.moe_expert_forward_grouped(pool, x, idx, partial_dtype=partial_dtype, ws=ws)
+    out = moe.moe_expert_forward_grouped(pool, x, idx, act_mode=act_mode, partial_dtype=partial_dtype, ws=ws)
     y = moe.moe_combine(out["partial"], out["inv_perm"], w)
     assert moe.moe_check_status(ws) == moe.MOE_OK
-    ref = oracle.prefill_layer(oracle.SyntheticPool(seed, s.E, s.H, s.I), xb, Wrb, s.k, act_mode=1,
+    ref = oracle.prefill_layer(oracle.SyntheticPool(seed, s.E, s.H, s.I), xb, Wrb, s.k, act_mode=act_mode,
                                sample_tokens=sample)
+    out["ws"], out["pool"] = ws, pool
     return out, y, ref, xb
 
 
@@ -92,7 +93,7 @@ def test_prefill_full_size_all_tokens():
     check_close(yg, ref["y"], "config 4: prefill T=512, all tokens", amb=ref["y_amb"], bf16_at=yg)
 
 
-def _h_decisions_and_down_sums(pool, s, T, xb, idx_np, out, ws, seed, tokens, label):
+def _h_decisions_and_down_sums(pool, s, T, xb, idx_np, out, ws, seed, tokens, label, act_mode=1):
     """Checks on the GPU's MXFP8 h (read back from the workspace) for the pairs of
     `tokens`:
       - every element equals the oracle's MXFP8(h), or differs only where the oracle's
@@ -103,8 +104,10 @@ def _h_decisions_and_down_sums(pool, s, T, xb, idx_np, out, ws, seed, tokens, la
         32-element K steps in ascending order (this measures the tensor pipe's
         accumulation, the premise of the h model, on the hardware itself).
     Returns (elements compared, mismatches, elements the model leaves open)."""
-    hq, hs = moe.moe_grouped_read_h(pool, T, s.k, out["offsets"], ws)
+    hq, hs = moe.moe_grouped_read_h(pool, T, s.k, out["offsets"], ws, act_mode=act_mode)
     hq, hs = hq.cpu(), hs.cpu().numpy()
+    fmt = 8 if act_mode == 1 else 4
+    e2m1 = np.array([oracle.e2m1_value(c) for c in range(16)])
     inv = out["inv_perm"].cpu().numpy()
     part = out["partial"].float().cpu().numpy()
     opool = oracle.SyntheticPool(seed, s.E, s.H, s.I)
@@ -112,15 +115,18 @@ def _h_decisions_and_down_sums(pool, s, T, xb, idx_np, out, ws, seed, tokens, la
     n = mism = nopen = 0
     worst_step = 0.0
     for t in tokens:
-        xq = oracle.quant_rows_mxfp8(synth.bf16_bits_to_f64(xb[t:t + 1]))
+        xq = oracle.quant_rows(synth.bf16_bits_to_f64(xb[t:t + 1]), act_mode)
         for j in range(s.k):
             e, r = int(idx_np[t, j]), int(inv[t * s.k + j])
             codes, scales = opool(e)
             h, rad = oracle.h_radius(codes, scales, s.H, s.I, xq)
-            d = oracle.mxfp8_ambiguity(h[0], rad[0])
-            q_or = oracle.quant_mxfp8(h[0])[2]
-            q_gpu = hq[r].view(torch.float8_e4m3fn).to(torch.float64).numpy() * np.repeat(
-                np.exp2(hs[r].astype(np.float64) - 127), 32)
+            d = oracle.mx_ambiguity(h[0], rad[0], fmt)
+            q_or = (oracle.quant_mxfp8 if act_mode == 1 else oracle.quant_mxfp4)(h[0])[2]
+            if act_mode == 1:
+                vals = hq[r].view(torch.float8_e4m3fn).to(torch.float64).numpy()
+            else:
+                vals = e2m1[hq[r].numpy() & 15]
+            q_gpu = vals * np.repeat(np.exp2(hs[r].astype(np.float64) - 127), 32)
             diff = np.abs(q_gpu - q_or)
             assert np.all(diff <= d), f"{label}: pair ({t},{j}) h outside the open decisions"
             n += diff.size
@@ -322,3 +328,48 @@ def test_prefill_hot_expert_spans_column_tiles(E, H, I, k, T):
     amb = oracle.pair_ambiguity(opool, H, I, xq, idx_h)
     part = out["partial"].float().cpu().numpy().astype(np.float64)[out["inv_perm"].cpu().numpy()]
     check_close(part.reshape(T, k, H), o_ref, "prefill hot expert: per-pair outputs", amb=amb)
+
+
+# ------------------------------------------------------- MXFP4 activations
+# act_mode MOE_ACT_MXFP4: x and h quantised to MXFP4 (the oracle applies the same
+# step), contractions as kind::mxf4 MMAs (E2M1 x E2M1).
+
+
+@pytest.mark.parametrize("E,H,I,k,T", [(16, 256, 128, 4, 64), (24, 384, 192, 8, 96), (64, 1024, 512, 16, 128)])
+def test_prefill_mxfp4_small_shapes(E, H, I, k, T):
+    s = synth.Shape(E=E, H=H, I=I, k=k)
+    seed = 940 + E
+    out, y, ref, xb = _run(s, T, seed, act_mode=2)
+    assert np.array_equal(out["perm"].cpu().numpy(), ref["perm"])
+    assert np.array_equal(out["offsets"].cpu().numpy(), ref["offsets"])
+    pool = oracle.SyntheticPool(seed, s.E, s.H, s.I)
+    xq = oracle.quant_rows_mxfp4(synth.bf16_bits_to_f64(xb))
+    o_ref = oracle.pair_outputs(pool, s.H, s.I, xq, ref["idx"], h_mode=2)
+    part = out["partial"].float().cpu().numpy().astype(np.float64)[out["inv_perm"].cpu().numpy()]
+    p_amb = oracle.pair_ambiguity(pool, s.H, s.I, xq, ref["idx"], fmt=4)
+    check_close(part.reshape(T, s.k, s.H), o_ref, "prefill MXFP4 small shapes: per-pair outputs", amb=p_amb)
+    yg = bf16_to_f64(y)
+    check_close(yg, ref["y"], "prefill MXFP4 small shapes: y", amb=ref["y_amb"], bf16_at=yg)
+
+
+@pytest.mark.parametrize("shape,T,tokens", [("tiny", 128, None), ("full", 512, (0, 255, 511))])
+def test_prefill_mxfp4_h_decisions_follow_the_error_model(shape, T, tokens):
+    s = synth.TINY if shape == "tiny" else synth.FULL
+    seed = 960 + T
+    out, _, ref, xb = _run(s, T, seed, sample=np.array([0]), act_mode=2)
+    assert np.array_equal(out["perm"].cpu().numpy(), ref["perm"])    # so the routing is the oracle's
+    toks = range(T) if tokens is None else tokens
+    n, mism, nopen = _h_decisions_and_down_sums(out["pool"], s, T, xb, ref["idx"], out, out["ws"], seed, toks,
+                                                f"MXFP4 h decisions {shape} T={T}", act_mode=2)
+    assert mism <= nopen
+
+
+@pytest.mark.parametrize("T,nsample", [(512, 32), (2048, 16), (8192, 16)])
+def test_prefill_mxfp4_full_size(T, nsample):
+    s = synth.FULL
+    out, y, ref, _ = _run(s, T, 980 + T, sample=np.linspace(0, T - 1, nsample).astype(np.int64), act_mode=2)
+    assert np.array_equal(out["perm"].cpu().numpy(), ref["perm"])
+    assert np.array_equal(out["offsets"].cpu().numpy(), ref["offsets"])
+    yg = bf16_to_f64(y)[ref["tokens"]]
+    check_close(yg, ref["y"], f"config 4 MXFP4: prefill T={T}, {nsample} sampled tokens", amb=ref["y_amb"],
+                bf16_at=yg)
