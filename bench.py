@@ -156,9 +156,10 @@ def whole_job_value(world, tokens_per_rank, ms_per_step):
     return world * tokens_per_rank / (ms_per_step / 1000.0)
 
 
-def measure_prefill(moe, torch, pool, Wr, dev, T, iters=3):
+def measure_prefill(moe, torch, pool, Wr, dev, T, iters=3, act_mode=1):
     """Expert-major prefill of T tokens on the full-size layer: route, sort,
-    MXFP8 gather, grouped gate/up and down GEMMs, combine.  Returns timings."""
+    MXFP8 (act_mode 1) or MXFP4 (2) gather, grouped gate/up and down GEMMs, combine.
+    Returns timings."""
     s = synth.FULL
     xb = synth.tokens_bf16(synth.TOKENS_SEED["prefill"], 0, T, s.H)
     x = torch.from_numpy(xb.view(np.int16)).to(dev).view(torch.bfloat16)
@@ -174,7 +175,7 @@ def measure_prefill(moe, torch, pool, Wr, dev, T, iters=3):
 
     def once():
         moe.moe_route_topk(x, Wr, s.k, ws=ws_r, idx=idx, w=w)
-        moe.moe_expert_forward_grouped(pool, x, idx, ws=ws_g, out=out)
+        moe.moe_expert_forward_grouped(pool, x, idx, act_mode=act_mode, ws=ws_g, out=out)
         moe.moe_combine(out["partial"], out["inv_perm"], w, y=y)
 
     once()
@@ -203,14 +204,16 @@ def measure_prefill(moe, torch, pool, Wr, dev, T, iters=3):
     bf16, bf16_kind = tensor_peak_tflops()
     hbm, hbm_kind = peaks()
     # Roofline of the two grouped GEMMs together: the MXFP4 weights of every expert with
-    # pairs, the MXFP8 rows of x read (codes + one scale byte per 32), the MXFP8 h written
-    # and read again, and the fp32 expert outputs written.  The MMA kind issued
-    # (mxf8f6f4: E2M1 x E4M3) runs at the FP8 rate, taken as the nominal 2x of the
-    # measured bf16 peak; the FP4 rate (6x) needs both operands in FP4.
-    act_bytes = P * s.H * (1 + 1 / 32) + 2 * P * s.I * (1 + 1 / 32) + P * s.H * 4
+    # pairs, the activation rows of x read (codes + one scale byte per 32), h written and
+    # read again, and the fp32 expert outputs written.  MXFP8 rows: the MMA kind issued
+    # (mxf8f6f4: E2M1 x E4M3) runs at the FP8 rate, the nominal 2x of the measured bf16
+    # peak; MXFP4 rows: kind::mxf4 at the FP4 rate, the nominal 6x.
+    eb = 1.0 if act_mode == 1 else 0.5           # bytes per activation element
+    act_bytes = P * s.H * (eb + 1 / 32) + 2 * P * s.I * (eb + 1 / 32) + P * s.H * 4
     gbytes = wbytes + act_bytes
+    kind_ratio = 2.0 if act_mode == 1 else 6.0
     t_bytes = gbytes / (hbm * 1e9) * 1e3
-    t_flops = flops / (2.0 * bf16 * 1e12) * 1e3
+    t_flops = flops / (kind_ratio * bf16 * 1e12) * 1e3
     attainable = max(t_bytes, t_flops)
     return {"tok_s": T / (ms / 1000.0), "ms": ms, "kernel_ms": kern,
             "gemm_weight_gbs": wbytes / (gemm_ms / 1000.0) / 1e9,
@@ -218,9 +221,11 @@ def measure_prefill(moe, torch, pool, Wr, dev, T, iters=3):
             "tensor_frac": {"of_fp8_rate": tflops / (2.0 * bf16), "of_fp4_rate": tflops / (6.0 * bf16),
                             "bf16_peak_tflops": bf16, "peak_kind": bf16_kind},
             "roofline": {"kernels": "gemm_gateup + gemm_down", "bound": "hbm" if t_bytes >= t_flops else "tensor",
+                         "mma_kind": "mxf8f6f4" if act_mode == 1 else "mxf4",
                          "algorithmic_bytes": gbytes, "weight_bytes": wbytes, "flops": flops,
-                         "peak_hbm_gbs": hbm, "peak_tflops_fp8": 2.0 * bf16, "peak_kind": f"{hbm_kind} hbm, "
-                         f"{bf16_kind} bf16 x 2 (nominal fp8 ratio)", "attainable_ms": attainable,
+                         "peak_hbm_gbs": hbm, "peak_tflops": kind_ratio * bf16,
+                         "peak_kind": f"{hbm_kind} hbm; {bf16_kind} bf16 x {kind_ratio:g} (nominal "
+                         f"{'fp8' if act_mode == 1 else 'fp4'} ratio)", "attainable_ms": attainable,
                          "measured_ms": gemm_ms, "frac": attainable / gemm_ms}}
 
 
@@ -460,10 +465,13 @@ def run_ours(args):
                "single_thread": {"value": n1 / secs1, "unit": "layer-tokens/s", "cores": 1,
                                  "sample": f"{n1} tokens of the same workload on one thread"}}
     launches = 2 * NTOK * args.steps      # route_single + decode_fused per token
-    prefill = {}
+    prefill, prefill4 = {}, {}
     if not args.no_prefill:
         for T in synth.PREFILL_T:
             prefill[str(T)] = measure_prefill(moe, torch, pool, Wr, dev, T)
+        for T in synth.PREFILL_T + synth.PREFILL_T_LARGE:
+            prefill4[str(T)] = measure_prefill(moe, torch, pool, Wr, dev, T, act_mode=2)
+            torch.cuda.empty_cache()
     verify, stacked = {}, None
     if not args.no_extra:
         for M in synth.VERIFY_M:
@@ -488,6 +496,7 @@ def run_ours(args):
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": launches,
             "prefill": prefill,
+            "prefill_mxfp4": prefill4,
             "verify": verify,
             "stacked_8_layers": stacked,
             "clocks": clk.summary(),

@@ -132,6 +132,7 @@ FULL = Shape(E=896, H=7168, I=1600, k=16)
 
 VERIFY_M = (2, 5, 9, 17)
 PREFILL_T = (512, 2048, 8192)
+PREFILL_T_LARGE = (16384, 32768)    # the large-T sweep of the MXFP4-activation prefill
 STACKED_LAYERS = 8
 ZIPF_S = 1.1
 VERIFY_MIX = 0.7
