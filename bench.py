@@ -342,6 +342,67 @@ def measure_stacked(moe, torch, pool0, dev, ntok=64, L=8, iters=2):
             "us_per_layer_token": sec * 1e6 / (ntok * L), "hbm_gbs": ntok * L * per_layer / sec / 1e9}
 
 
+def measure_streamed(moe, torch, pool0, dev, ntok=48, warm=16, L=8, slots=128):
+    """Eight stacked layers decoded one token at a time with the experts streamed: the
+    records live in pinned host memory (one host copy of the pool shared by the
+    layers, each layer with its own router, Zipf skew and HBM cache of `slots`
+    records), and per layer-token the router's indices are read back, the missing
+    records copied over NVLink-C2C (one cudaMemcpyAsync each) and the layer run on the
+    cache.  Reports layer-tokens/s, the cache hit rate and the copy rate."""
+    s = synth.FULL
+    rec = moe.moe_pool_record_bytes(s.H, s.I)
+    host = torch.empty(s.E * rec, dtype=torch.uint8).pin_memory()
+    host.copy_(pool0.mem)
+    sps = [moe.StreamPool(host, s.E, s.H, s.I, slots, device=dev) for _ in range(L)]
+    Wrs = [torch.from_numpy(synth.router_bf16(synth.router_seed(l), s.E, s.H).view(np.int16)).to(dev)
+           .view(torch.bfloat16) for l in range(L)]
+    skews = [torch.from_numpy(synth.zipf_skew_f32(synth.skew_seed(l), s.E)).to(dev) for l in range(L)]
+    xb = synth.tokens_bf16(synth.TOKENS_SEED["stacked"], 0, warm + ntok, s.H)
+    x_all = torch.from_numpy(xb.view(np.int16)).to(dev).view(torch.bfloat16)
+    xs = [torch.empty((1, s.H), dtype=torch.bfloat16, device=dev) for _ in range(L + 1)]
+    xh = torch.empty((1, s.H), dtype=torch.bfloat16, device=dev)
+    idx = torch.empty((1, s.k), dtype=torch.int32, device=dev)
+    w = torch.empty((1, s.k), dtype=torch.float32, device=dev)
+    idx_h = torch.empty((1, s.k), dtype=torch.int32).pin_memory()
+    slot_h = torch.empty((1, s.k), dtype=torch.int32).pin_memory()
+    slot_d = torch.empty((1, s.k), dtype=torch.int32, device=dev)
+    ws_r = moe.workspace(moe.moe_workspace_size(moe.MOE_OP_ROUTE, s.E, s.H, s.I, 1, s.k), dev)
+    ws_d = moe.workspace(moe.moe_workspace_size(moe.MOE_OP_DECODE, slots, s.H, s.I, 1, s.k), dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def token(t):
+        xs[0].copy_(x_all[t:t + 1])
+        for l in range(L):
+            moe.moe_route_topk_prescaled(xs[l], Wrs[l], s.k, skews[l], ws=ws_r, idx=idx, w=w, xhat=xh)
+            idx_h.copy_(idx, non_blocking=True)
+            stream.synchronize()
+            slot_h.numpy()[:] = sps[l].map(idx_h.numpy(), stream)
+            slot_d.copy_(slot_h, non_blocking=True)
+            moe.moe_expert_forward_decode(sps[l].cache, xh, slot_d, w, residual=xs[l], ws=ws_d, y=xs[l + 1])
+
+    for t in range(warm):
+        token(t)
+    torch.cuda.synchronize()
+    st0 = [sp.stats() for sp in sps]
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for t in range(warm, warm + ntok):
+        token(t)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    assert moe.moe_check_status(ws_d) == 0 and moe.moe_check_status(ws_r) == 0
+    sec = e0.elapsed_time(e1) / 1000.0
+    st1 = [sp.stats() for sp in sps]
+    hits = sum(b[0] - a[0] for a, b in zip(st0, st1))
+    misses = sum(b[1] - a[1] for a, b in zip(st0, st1))
+    copied = sum(b[2] - a[2] for a, b in zip(st0, st1))
+    del sps, host
+    return {"tokens": ntok, "layers": L, "slots_per_layer": slots, "slot_fraction": slots / s.E,
+            "layer_tokens_per_s": ntok * L / sec, "us_per_layer_token": sec * 1e6 / (ntok * L),
+            "hit_rate": hits / max(hits + misses, 1), "misses_per_layer_token": misses / (ntok * L),
+            "copy_gbs": copied / sec / 1e9, "note": "one pinned host copy of the pool shared by the layers"}
+
+
 def run_ours(args):
     import torch
     import mxfp4_routed_expert_topk_gb300 as moe
@@ -472,11 +533,13 @@ def run_ours(args):
         for T in synth.PREFILL_T + synth.PREFILL_T_LARGE:
             prefill4[str(T)] = measure_prefill(moe, torch, pool, Wr, dev, T, act_mode=2)
             torch.cuda.empty_cache()
-    verify, stacked = {}, None
+    verify, stacked, streamed = {}, None, None
     if not args.no_extra:
         for M in synth.VERIFY_M:
             verify[str(M)] = measure_verify(moe, torch, pool, Wr, dev, M)
         stacked = measure_stacked(moe, torch, pool, dev)
+        torch.cuda.empty_cache()
+        streamed = {str(c): measure_streamed(moe, torch, pool, dev, slots=c) for c in (128, 256)}
     if rank == 0:
         print(json.dumps({
             "metric": METRIC, "value": value, "unit": "layer-tokens/s", "n_gpus": world, "steps": args.steps,
@@ -499,6 +562,7 @@ def run_ours(args):
             "prefill_mxfp4": prefill4,
             "verify": verify,
             "stacked_8_layers": stacked,
+            "streamed_8_layers": streamed,
             "clocks": clk.summary(),
         }))
     if dist is not None:

@@ -106,6 +106,45 @@ moe_status moe_pool_upload_expert(moe_pool *pool, int e, const uint8_t *codes_de
 moe_status moe_pool_download_expert(const moe_pool *pool, int e, uint8_t *codes_dev,
                                     uint8_t *scales_dev, moe_stream_t stream);
 
+/* ------------------------------------------------------ streamed expert pool
+ * The pages' streamed experts ("技术亮点" on the hn page: experts read on demand,
+ * with a cache; "存储子系统" on the four-SSD page: demand reads of one unit per
+ * (layer, expert)) in GB300 form.  The E records of a layer (the pool record layout
+ * above) live in caller-owned host memory, pinned so that the copy engines read
+ * them over NVLink-C2C; a cache of C = cache_bytes / moe_pool_record_bytes(H, I)
+ * record slots lives in caller-owned device memory.  The cache is an ordinary pool
+ * view of C records (moe_stream_pool_cache), so moe_expert_forward_decode and
+ * moe_expert_forward_grouped run on it with slot indices in place of expert indices.
+ *
+ * moe_stream_pool_create: host_records >= E records (host_bytes), dev_cache
+ * 1024-byte aligned with room for C >= 1 records (C <= E).  dev_cache may be NULL:
+ * the object then only plans (assigns slots, counts hits and misses) and copies
+ * nothing, which tests the replacement policy without a GPU. */
+typedef struct moe_stream_pool moe_stream_pool;
+moe_status moe_stream_pool_create(moe_stream_pool **out, const void *host_records, size_t host_bytes, int E, int H,
+                                  int I, void *dev_cache, size_t cache_bytes);
+void moe_stream_pool_destroy(moe_stream_pool *sp);
+
+/* The cache as a pool of C records (slot s is "expert" s); NULL when planning only. */
+const moe_pool *moe_stream_pool_cache(const moe_stream_pool *sp);
+int moe_stream_pool_slots(const moe_stream_pool *sp);
+
+/* Make the experts idx_host[0..n) (host memory; n = M*k of a decode or grouped call)
+ * resident and write their slots to slot_host[0..n) (host memory; copy them to the
+ * device for the kernels).  A missing expert takes the least recently used slot that
+ * this call does not use, and its record is copied with one cudaMemcpyAsync
+ * (host -> device) on `stream`: after every earlier use of the slot on that stream
+ * and before every later one, so all work that uses the cache must be issued on
+ * `stream` (or ordered with it).  An index outside [0, E) gets slot -1 (the kernels
+ * report MOE_ERR_BAD_INDEX and add nothing for it).  MOE_ERR_UNSUPPORTED_SHAPE if the
+ * call names more distinct experts than C.  Not thread-safe per object. */
+moe_status moe_stream_pool_map(moe_stream_pool *sp, const int32_t *idx_host, int n, int32_t *slot_host,
+                               moe_stream_t stream);
+
+/* Counters since creation: distinct experts per call found resident (hits) and
+ * copied (misses), and the bytes copied. */
+moe_status moe_stream_pool_stats(const moe_stream_pool *sp, uint64_t *hits, uint64_t *misses, uint64_t *bytes);
+
 /* ------------------------------------------------------------- workspace */
 
 /* Workspace bytes of operation `op` (MOE_OP_*) for M (decode) or T (prefill)

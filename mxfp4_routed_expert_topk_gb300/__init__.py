@@ -5,7 +5,7 @@ include/moe.h); this package is its thin Python binding.  PyTorch supplies devic
 memory and streams only.
 """
 from ._lib import *  # noqa: F401,F403
-from ._lib import Pool, MoeError, lib, workspace, exact_fallbacks, status_string  # noqa: F401
+from ._lib import Pool, StreamPool, MoeError, lib, workspace, exact_fallbacks, status_string  # noqa: F401
 from ._lib import moe_trace_begin, moe_trace_end  # noqa: F401
 
 

@@ -36,6 +36,8 @@ EXPORTED = [
     "moe_prescale",
     "moe_expert_forward_grouped", "moe_grouped_read_h", "moe_combine", "moe_trace_begin", "moe_trace_end",
     "moe_debug_set_wait_limit", "moe_debug_set_barrier_extra",
+    "moe_stream_pool_create", "moe_stream_pool_destroy", "moe_stream_pool_cache", "moe_stream_pool_slots",
+    "moe_stream_pool_map", "moe_stream_pool_stats",
 ]
 
 
@@ -78,6 +80,12 @@ def lib() -> ctypes.CDLL:
             "moe_grouped_read_h": (_i, [_vp, _i, _i, _i, _vp, _vp, _sz, _vp, _vp, _vp]),
             "moe_combine": (_i, [_vp, _i, _vp, _vp, _i, _i, _i, _vp, _vp, _vp]),
             "moe_debug_set_wait_limit": (_i, [_u64]),
+            "moe_stream_pool_create": (_i, [ctypes.POINTER(_vp), _vp, _sz, _i, _i, _i, _vp, _sz]),
+            "moe_stream_pool_destroy": (None, [_vp]),
+            "moe_stream_pool_cache": (_vp, [_vp]),
+            "moe_stream_pool_slots": (_i, [_vp]),
+            "moe_stream_pool_map": (_i, [_vp, _vp, _i, _vp, _vp]),
+            "moe_stream_pool_stats": (_i, [_vp, ctypes.POINTER(_u64), ctypes.POINTER(_u64), ctypes.POINTER(_u64)]),
             "moe_debug_set_barrier_extra": (_i, [_i]),
             "moe_trace_begin": (_i, [ctypes.c_char_p]),
             "moe_trace_end": (_i, [ctypes.POINTER(_i), ctypes.POINTER(ctypes.c_double)]),
@@ -325,6 +333,69 @@ def moe_combine(partial: torch.Tensor, inv_perm: torch.Tensor, w: torch.Tensor, 
     _check(lib().moe_combine(_ptr(partial), pdt, _ptr(inv_perm), _ptr(w), T, k, H, _ptr(residual), _ptr(y),
                              _stream(stream)), "moe_combine")
     return y
+
+
+# ------------------------------------------------------ streamed expert pool
+
+
+class _CacheView:
+    """The device cache of a StreamPool, usable wherever a Pool is (slot indices)."""
+
+    def __init__(self, handle, E, H, I, mem):
+        self.handle, self.E, self.H, self.I, self.mem = handle, E, H, I, mem
+
+
+class StreamPool:
+    """Expert records in pinned host memory (`host`, a CPU uint8 tensor holding E
+    records), an HBM cache of `slots` records; `cache` is the pool view the kernels use
+    with the slot indices that `map` returns."""
+
+    def __init__(self, host: torch.Tensor, E: int, H: int, I: int, slots: int, device="cuda", plan_only=False):
+        if host.is_cuda or host.dtype != torch.uint8 or not host.is_contiguous():
+            raise ValueError("host: expected a contiguous CPU uint8 tensor")
+        self.E, self.H, self.I = E, H, I
+        rec = moe_pool_record_bytes(H, I)
+        self.host = host
+        self.rec = rec
+        if plan_only:
+            self.buffer, mem, cache_ptr = None, None, None
+        else:
+            self.buffer = torch.empty(slots * rec + 1024, dtype=torch.uint8, device=device)
+            off = (-self.buffer.data_ptr()) % 1024
+            mem = self.buffer[off:off + slots * rec]
+            cache_ptr = _ptr(mem)
+        h = ctypes.c_void_p()
+        _check(lib().moe_stream_pool_create(ctypes.byref(h), ctypes.c_void_p(host.data_ptr()), host.numel(), E, H, I,
+                                            cache_ptr, slots * rec), "moe_stream_pool_create")
+        self.handle = h
+        self.slots = int(lib().moe_stream_pool_slots(h))
+        c = lib().moe_stream_pool_cache(h)
+        self.cache = None if c is None else _CacheView(ctypes.c_void_p(c), self.slots, H, I, mem)
+        self._idx = torch.empty(32 * 32, dtype=torch.int32).pin_memory() if not plan_only else None
+
+    def map(self, idx_host, stream=None):
+        """Slots (int32 numpy array, same shape) for the expert indices `idx_host`
+        (numpy int32); misses are copied on `stream` (the current stream if None)."""
+        import numpy as np
+        a = np.ascontiguousarray(idx_host, dtype=np.int32)
+        out = np.empty_like(a)
+        st = None if self.cache is None else _stream(stream)
+        _check(lib().moe_stream_pool_map(self.handle, a.ctypes.data_as(ctypes.c_void_p), a.size,
+                                         out.ctypes.data_as(ctypes.c_void_p), st), "moe_stream_pool_map")
+        return out
+
+    def stats(self):
+        """(hits, misses, bytes copied) since creation."""
+        h, m, b = _u64(), _u64(), _u64()
+        _check(lib().moe_stream_pool_stats(self.handle, ctypes.byref(h), ctypes.byref(m), ctypes.byref(b)),
+               "moe_stream_pool_stats")
+        return int(h.value), int(m.value), int(b.value)
+
+    def __del__(self):
+        h = getattr(self, "handle", None)
+        if h is not None and _lib is not None:
+            _lib.moe_stream_pool_destroy(h)
+            self.handle = None
 
 
 # ---------------------------------------------------------- test support

@@ -16,7 +16,7 @@ OUT = os.path.join(HERE, "libmoe.so")
 OBJDIR = os.path.join(HERE, "_build")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC"]
-SOURCES = ["api.cu", "pool.cu", "route.cu", "route_static.cu", "decode.cu", "decode_fused.cu", "prefill.cu", "gemm.cu"]
+SOURCES = ["api.cu", "pool.cu", "route.cu", "route_static.cu", "decode.cu", "decode_fused.cu", "prefill.cu", "gemm.cu", "stream_pool.cu"]
 
 
 def _nvcc() -> str:
