@@ -598,7 +598,7 @@ def run_profile_case(args):
         x = torch.from_numpy(xb.view(np.int16)).cuda().view(torch.bfloat16)
         for _ in range(2):
             idx, w = moe.moe_route_topk(x, Wr, s.k)
-            out = moe.moe_expert_forward_grouped(pool, x, idx)
+            out = moe.moe_expert_forward_grouped(pool, x, idx, act_mode=args.profile_act)
             moe.moe_combine(out["partial"], out["inv_perm"], w)
         torch.cuda.synchronize()
         print("profile case done")
@@ -627,6 +627,8 @@ def main():
                     help="run a small case of the kernels for an ncu capture (no JSON line)")
     ap.add_argument("--profile-tokens", type=int, default=64,
                     help="tokens of the prefill profile case (64-expert pool)")
+    ap.add_argument("--profile-act", type=int, default=1, choices=[1, 2],
+                    help="activation format of the prefill profile case: 1 MXFP8, 2 MXFP4")
     args = ap.parse_args()
     if args.profile:
         run_profile_case(args)

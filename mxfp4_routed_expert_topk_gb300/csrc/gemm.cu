@@ -76,6 +76,8 @@ struct GemmArgs {
     int ns;              // pipeline stages
     int nmt;             // 128-row tiles of A per expert
     int tpi;             // 128-row tiles per work item (1, or 2: one 256-row tensor copy of A)
+    int nacc;            // accumulator buffers in TMEM: 2 (a tile's epilogue overlaps the next
+                         // tile's MMAs) or 1 (when TMEM is short; two CTAs per SM overlap instead)
     uint32_t tmem_cols;
     // epilogue outputs
     int I;               // intermediate size (gate/up epilogue)
@@ -407,13 +409,13 @@ __device__ __forceinline__ void epilogue_mx1(const GemmArgs &a, uint32_t lane_ba
 }
 
 // Shared memory of the persistent kernel for BN accumulator columns and ns stages.
-// With FP4 rows a stage holds two scale atoms per operand (K = 256, one B atom).
+// With FP4 rows a stage holds the scale factors of two 128-K tiles (K = 256).
 struct GemmSmemLayout {
     uint32_t a, b, sfa, sfb, bars, misc, total, sfa_stage, sfb_stage;
     __host__ __device__ GemmSmemLayout(int BN, int ns, int tpi, bool fp4 = false) {
         const uint32_t nsfb = (uint32_t)((BN + 127) / 128);
         sfa_stage = (uint32_t)tpi * (fp4 ? 1024u : 512u);
-        sfb_stage = fp4 ? 1024u : sfb_stage_bytes((int)nsfb);
+        sfb_stage = fp4 ? 2u * sfb_stage_bytes((int)nsfb) : sfb_stage_bytes((int)nsfb);
         a = 0;                                            // ns x tpi x 16 KB (1024-aligned)
         b = a + (uint32_t)(ns * tpi) * kTileM * kTileK;   // ns x BN*128
         sfa = b + (uint32_t)ns * (uint32_t)BN * kTileK;   // ns x sfa_stage
@@ -512,9 +514,9 @@ __global__ void __launch_bounds__(NT, GemmShape<NT>::kCtasPerSm)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t sf_col0 = 2u * (uint32_t)(tpi * a.BN);  // scale factors after the two accumulators
+    const uint32_t sf_col0 = (uint32_t)(a.nacc * tpi * a.BN);  // scale factors after the accumulators
     // TMEM columns per stage: 4 per 512-byte scale atom (two atoms per operand with FP4)
-    const uint32_t sf_stage = FP4 ? 8u * (uint32_t)tpi + 8u : 4u * (uint32_t)tpi + 4u * (uint32_t)nsfb;
+    const uint32_t sf_stage = FP4 ? 8u * (uint32_t)tpi + 8u * (uint32_t)nsfb : 4u * (uint32_t)tpi + 4u * (uint32_t)nsfb;
 
     int it_issued = 0;  // producer: stages issued
     // The copy and MMA roles run their loops with the whole warp converged (waits
@@ -548,10 +550,12 @@ __global__ void __launch_bounds__(NT, GemmShape<NT>::kCtasPerSm)
                     // (parts past the end of K are zero-filled and counted); one or two
                     // 128-K scale tiles (the last stage of an odd count has one)
                     const int n2 = min(2, a.nkt_sf - 2 * kt);
-                    const uint32_t tx = (uint32_t)(tpi * kTileM * kTileK + a.BN * kTileK) + (uint32_t)n2 * 1024u;
+                    const uint32_t sfbk = sfb_stage_bytes(nsfb);  // per 128-K tile
+                    const uint32_t tx =
+                        (uint32_t)(tpi * kTileM * kTileK + a.BN * kTileK) + (uint32_t)n2 * (512u + sfbk);
                     const uint8_t *sfa_src =
                         a.pool + (uint64_t)J.e * a.rec + a.a_sf_off + ((uint64_t)(2 * kt) * a.nmt + J.mt) * 512;
-                    const uint8_t *sfb_src = a.bscale + sf_tile_word(J.tile(), a.nkt_sf, 1, 2 * kt, 0);
+                    const uint8_t *sfb_src = a.bscale + sf_tile_word(J.tile(), a.nkt_sf, nsfb, 2 * kt, 0);
                     if (elect_one()) {
                         mbar_arrive_expect_tx(&full[s], tx);
                         tma_load_3d(sA + (size_t)s * kTileM * kTileK, &tmA, kt * kTileK, J.mt * kTileM, J.e, &full[s]);
@@ -559,7 +563,15 @@ __global__ void __launch_bounds__(NT, GemmShape<NT>::kCtasPerSm)
                         for (int j = 0; j < n2; j++)  // the two K tiles' A blocks are nmt blocks apart
                             bulk_g2s_l2(sSFA + (size_t)s * 1024 + 512 * j, sfa_src + (size_t)j * a.nmt * 512, 512u,
                                         &full[s]);
-                        bulk_g2s_l2(sSFB + (size_t)s * 1024, sfb_src, (uint32_t)n2 * 512u, &full[s]);  // adjacent
+                        if (nsfb == 1) {
+                            bulk_g2s_l2(sSFB + (size_t)s * 1024, sfb_src, (uint32_t)n2 * 512u, &full[s]);  // adjacent
+                        } else {
+                            // per K tile the interleaved 1 KB block once per TMEM lane quadrant
+                            for (int j = 0; j < n2; j++)
+                                for (int q = 0; q < 4; q++)
+                                    bulk_g2s_l2(sSFB + (size_t)s * 8192 + (size_t)j * 4096 + q * 1024,
+                                                sfb_src + (size_t)j * 1024, 1024u, &full[s]);
+                        }
                     }
                 } else {
                     const uint32_t tx =
@@ -615,10 +627,12 @@ __global__ void __launch_bounds__(NT, GemmShape<NT>::kCtasPerSm)
             const int nmma = (J.nn() + 15) / 16 * 16;
             // mxf8f6f4: + ks * kIdescSfStep for K step ks; mxf4: + kIdescSf2 for odd ks
             const uint32_t idesc0 = FP4 ? idesc_mxf4(nmma) : idesc_mxf8f6f4(nmma, 0);
-            const int buf = jb & 1;
-            // the epilogue has finished with this accumulator (two tiles ago)
+            // accumulator buffer of tile jb and its use count
+            const int buf = a.nacc == 2 ? (jb & 1) : 0;
+            const uint32_t use = a.nacc == 2 ? (uint32_t)(jb >> 1) : (uint32_t)jb;
+            // the epilogue has finished with this accumulator (nacc tiles ago)
             int okl = 1;
-            if (lane == 0) okl = mbar_wait_or_abort(&acc_empty[buf], ((uint32_t)(jb >> 1) & 1u) ^ 1u, a.st, 0x680u + buf,
+            if (lane == 0) okl = mbar_wait_or_abort(&acc_empty[buf], (use & 1u) ^ 1u, a.st, 0x680u + buf,
                                                     abort_flag);
             if (!__shfl_sync(0xffffffffu, okl, 0)) {
                 if (lane == 0) *abort_flag = 1;
@@ -659,16 +673,20 @@ __global__ void __launch_bounds__(NT, GemmShape<NT>::kCtasPerSm)
                         if constexpr (FP4) {
                             // two 128-K scale atoms per operand (one in the last stage of an
                             // odd count): K step ks (64 K) reads atom ks / 2, bytes 2 (ks % 2)..
+                            // B: one atom (4 columns) or one two-atom block (8 columns) per K tile
                             const int n2 = min(2, a.nkt_sf - 2 * (kt + q));
-                            const uint32_t sfb_t4 = sfa_t + 8u;
+                            const uint32_t sfb_t4 = sfa_t + 8u, bw = 4u * (uint32_t)nsfb;
                             for (int j = 0; j < n2; j++) {
                                 tc_cp_sf(sfa_t + 4u * j, sfad + (uint64_t)(32 * j));
-                                tc_cp_sf(sfb_t4 + 4u * j, sfbd + (uint64_t)(32 * j));
+                                if (nsfb == 1)
+                                    tc_cp_sf(sfb_t4 + 4u * j, sfbd + (uint64_t)(32 * j));
+                                else
+                                    tc_cp_sf2(sfb_t4 + 8u * j, sfbd + (uint64_t)(256 * j));  // 4 KB apart
                             }
                             for (int ks = 0; ks < 2 * n2; ks++)
                                 tc_mma_f4(acc, ad0 + (uint64_t)(2 * ks), bd0 + (uint64_t)(2 * ks),
                                           idesc0 + ((ks & 1) ? kIdescSf2 : 0u), sfa_t + 4u * (ks >> 1),
-                                          sfb_t4 + 4u * (ks >> 1), (kt + q > 0 || ks > 0) ? 1u : 0u);
+                                          sfb_t4 + bw * (ks >> 1), (kt + q > 0 || ks > 0) ? 1u : 0u);
                         } else {
                             for (int t = 0; t < tpi; t++)
                                 tc_cp_sf(sfa_t + 4u * t, sfad + (uint64_t)(32 * t));  // 512 B apart
@@ -715,10 +733,10 @@ __global__ void __launch_bounds__(NT, GemmShape<NT>::kCtasPerSm)
         float *amax_g = amax_x + 64 * wg;
         int jb = 0;
         for (JobIter J(a, nu); J.valid(); J.next(), jb++) {
-            const int buf = jb & 1;
+            const int buf = a.nacc == 2 ? (jb & 1) : 0;
+            const uint32_t use = a.nacc == 2 ? (uint32_t)(jb >> 1) : (uint32_t)jb;
             const int nn = J.nn(), nmma = (nn + 15) / 16 * 16;
-            bool okl = !*(volatile int *)abort_flag &&
-                       mbar_wait(&acc_full[buf], (uint32_t)(jb >> 1) & 1u, a.st, 0x800u + buf);
+            bool okl = !*(volatile int *)abort_flag && mbar_wait(&acc_full[buf], use & 1u, a.st, 0x800u + buf);
             if (!okl) *abort_flag = 1;
             const bool ok = __all_sync(0xffffffffu, okl);  // warp-uniform for the .sync.aligned loads
             tc_fence_after();
@@ -826,12 +844,15 @@ PerDevice g_smem_set_192f4(0);
 // (one 256-row tensor copy) while their four accumulators fit in TMEM.  Measured on the
 // full-size layer: two CTAs per SM took the 512-token GEMMs from 3.84 to 3.03 ms; the
 // down GEMM at BN = 96 and all GEMMs at BN >= 128 are faster with one.  With FP4 rows
-// (BN <= 128, one B scale atom) every item is one 128-row tile, and a stage holds two
-// scale atoms per operand (16 TMEM columns).  a_k and b_k are K in elements.
+// every item is one 128-row tile and a stage covers two 128-K scale tiles: two A atoms
+// (8 TMEM columns) and two B atoms or, for BN > 128, two interleaved two-atom blocks
+// (16 columns).  (Two CTAs of one accumulator each per SM, tried for BN = 128, left
+// only three stages per CTA and made the 32768-token GEMMs 1.34x slower.)  a_k and b_k
+// are K in elements.
 cudaError_t launch_one(GemmArgs ga, const uint8_t *a_base, int a_k, int a_rows, uint64_t a_ld, int E, const uint8_t *b_base,
                        int b_k, int b_rows, int nexp, const char *trace_name, cudaStream_t stream, bool fp4) {
     const int BN = ga.BN, nsfb = ga.nsfb;
-    if (fp4 && nsfb != 1) return cudaErrorNotSupported;
+    if (fp4 && nsfb > 2) return cudaErrorNotSupported;
     int smem_max = 0, sms = 0;
     cudaError_t e = device_attr(cudaDevAttrMaxSharedMemoryPerBlockOptin, g_smem_max, &smem_max);
     if (e != cudaSuccess) return e;
@@ -840,10 +861,12 @@ cudaError_t launch_one(GemmArgs ga, const uint8_t *a_base, int a_k, int a_rows, 
     const int tpi = fp4 || two ? 1 : (BN <= 96 ? 2 : 1);
     const uint32_t smem_cap = two ? (uint32_t)(smem_max / 2 - 1024) : (uint32_t)smem_max;
     const uint32_t tmem_cap = two ? 256u : 512u;
+    const uint32_t sf_cols = fp4 ? 8u * tpi + 8u * nsfb : 4u * tpi + 4u * nsfb;
+    // two accumulators if they leave room for at least 4 stages of scale columns
+    const int nacc = (uint32_t)(2 * tpi * BN) + 4u * sf_cols <= tmem_cap ? 2 : 1;
     // as many pipeline stages as fit the CTA's share of shared memory and TMEM
     int ns = kMaxStages;
-    const uint32_t sf_cols = fp4 ? 8u * tpi + 8u : 4u * tpi + 4u * nsfb;
-    auto tmem_need = [&](int n) { return (uint32_t)(2 * tpi * BN) + (uint32_t)n * sf_cols; };
+    auto tmem_need = [&](int n) { return (uint32_t)(nacc * tpi * BN) + (uint32_t)n * sf_cols; };
     auto smem_need = [&](int n) { return GemmSmemLayout(BN, n, tpi, fp4).total + 1024; };  // + alignment slack
     while (ns > 2 && (smem_need(ns) > smem_cap || tmem_need(ns) > tmem_cap)) ns--;
     const uint32_t tmem_cols = pow2_at_least(tmem_need(ns));
@@ -858,6 +881,7 @@ cudaError_t launch_one(GemmArgs ga, const uint8_t *a_base, int a_k, int a_rows, 
     if (e != cudaSuccess) return e;
     ga.ns = ns;
     ga.tpi = tpi;
+    ga.nacc = nacc;
     ga.tmem_cols = tmem_cols;
     ga.nkt_sf = a_k / kTileK;
     ga.nkt = fp4 ? (ga.nkt_sf + 1) / 2 : ga.nkt_sf;

@@ -10,13 +10,13 @@ namespace moe {
 constexpr int kMaxSortE = 4096;  // experts supported by the grouped path
 
 constexpr int kMaxBN = 192;      // accumulator columns of a grouped-GEMM tile
-constexpr int kMaxBN4 = 128;     // ... with MXFP4 activations (one scale atom per K tile)
+constexpr int kMaxBN4 = 192;     // ... with MXFP4 activations
 
 // Accumulator columns per tile (BN) of the grouped GEMMs for P pairs over E experts,
 // T rows, nparts activation rows per pair; 0 when the shape is not supported.
 // nparts = 1: 1.5 times the mean rows per expert rounded up to 32, 32..192 (an expert
-// with more rows takes several tiles; narrow tiles let the GEMMs run two CTAs per SM),
-// at most 128 with MXFP4 activations (fp4).
+// with more rows takes several tiles; narrow tiles let the GEMMs run two CTAs per SM);
+// the same rule with MXFP4 activations (fp4).
 // nparts = 3: all of an expert's rows (at most 3T) in one tile, in whole groups of 16
 // pairs.
 __host__ __device__ inline int grouped_bn(int P, int E, int T, int nparts, bool fp4 = false) {
