@@ -578,14 +578,21 @@ def run_profile_case(args):
     import mxfp4_routed_expert_topk_gb300 as moe
     moe.build()
     if args.profile == "route":
-        # the router alone at the full shape (E=896, H=7168): 12.8 MB of W_r
+        # the router alone at the full shape (E=896, H=7168): 12.8 MB of W_r; four
+        # single-token calls, or (--profile-tokens > 64) one call on that many tokens,
+        # which takes the tiled logit kernel
         s = synth.FULL
         Wr = torch.from_numpy(synth.router_bf16(synth.router_seed(0), s.E, s.H).view(np.int16)).cuda()
         Wr = Wr.view(torch.bfloat16)
-        xb = synth.tokens_bf16(synth.TOKENS_SEED["full"], 0, 4, s.H)
+        n = args.profile_tokens if args.profile_tokens > 64 else 4
+        xb = synth.tokens_bf16(synth.TOKENS_SEED["full"], 0, n, s.H)
         x = torch.from_numpy(xb.view(np.int16)).cuda().view(torch.bfloat16)
-        for t in range(4):
-            moe.moe_route_topk(x[t:t + 1], Wr, s.k)
+        if n > 64:
+            for _ in range(2):
+                moe.moe_route_topk(x, Wr, s.k)
+        else:
+            for t in range(4):
+                moe.moe_route_topk(x[t:t + 1], Wr, s.k)
         torch.cuda.synchronize()
         print("profile case done")
         return

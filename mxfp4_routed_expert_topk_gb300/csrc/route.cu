@@ -273,6 +273,28 @@ __global__ void route_norms_kernel(const uint16_t *__restrict__ x, int M, int H,
     }
 }
 
+// Two fp32 values in one 64-bit register (lo in the low half, as in memory), and the
+// packed fp32 arithmetic of sm_100-family cores on such pairs: each half is an
+// ordinary, correctly rounded fp32 operation.
+__device__ __forceinline__ unsigned long long dup_f32x2(float v) {
+    unsigned long long r;
+    asm("mov.b64 %0, {%1, %1};" : "=l"(r) : "f"(v));
+    return r;
+}
+__device__ __forceinline__ float unpack_f32x2(unsigned long long v, int hi) {
+    float lo_f, hi_f;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo_f), "=f"(hi_f) : "l"(v));
+    return hi ? hi_f : lo_f;
+}
+// d = a * b + d (round to nearest, no flush), halfwise
+__device__ __forceinline__ void fma_f32x2(unsigned long long &d, unsigned long long a, unsigned long long b) {
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(d) : "l"(a), "l"(b));
+}
+// d = d + a (round to nearest), halfwise
+__device__ __forceinline__ void add_f32x2(unsigned long long &d, unsigned long long a) {
+    asm("add.rn.f32x2 %0, %0, %1;" : "+l"(d) : "l"(a));
+}
+
 // 16-byte asynchronous copy global -> shared (both 16-byte aligned); src_bytes 0
 // writes zeros without reading.
 __device__ __forceinline__ void cp_async16(void *dst, const void *src, uint32_t src_bytes) {
@@ -348,13 +370,16 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
         }
     };
     // compute: group g = tid / 64; within it ty = (tid % 64) / 8, tx = tid % 8; tokens
-    // 4ty..4ty+3 and 32+4ty.., experts 4tx..4tx+3 and 32+4tx..
+    // 4ty..4ty+3 and 32+4ty.., experts 4tx..4tx+3 and 32+4tx..  The accumulators are
+    // packed in pairs of adjacent experts (fma.rn.f32x2 / add.rn.f32x2: two independent,
+    // correctly rounded fp32 operations per instruction, so every (token, expert) sum
+    // takes the same roundings in the same order as scalar fp32 code).
     const int g = tid >> 6, ty = (tid & 63) >> 3, tx = tid & 7;
-    float inner[8][8], outer[8][8];
+    unsigned long long inner[8][4], outer[8][4];
 #pragma unroll
     for (int i = 0; i < 8; i++)
 #pragma unroll
-        for (int j = 0; j < 8; j++) inner[i][j] = outer[i][j] = 0.f;
+        for (int p = 0; p < 4; p++) inner[i][p] = outer[i][p] = 0ull;  // +0.0f in both halves
 #pragma unroll
     for (int p = 0; p < kTiledStages - 1; p++) {
         if (p < nsteps)
@@ -377,22 +402,25 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
         for (int k = 0; k < 16; k++) {
             const float4 a0 = *reinterpret_cast<const float4 *>(&xs[buf][g][k][4 * ty]);
             const float4 a1 = *reinterpret_cast<const float4 *>(&xs[buf][g][k][32 + 4 * ty]);
-            const float4 b0 = *reinterpret_cast<const float4 *>(&wsm[buf][g][k][4 * tx]);
-            const float4 b1 = *reinterpret_cast<const float4 *>(&wsm[buf][g][k][32 + 4 * tx]);
+            // experts 4tx.. and 32+4tx.. as pairs (adjacent floats: lo = the lower expert)
+            const ulonglong2 b01 = *reinterpret_cast<const ulonglong2 *>(&wsm[buf][g][k][4 * tx]);
+            const ulonglong2 b23 = *reinterpret_cast<const ulonglong2 *>(&wsm[buf][g][k][32 + 4 * tx]);
             const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-            const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+            const unsigned long long bp[4] = {b01.x, b01.y, b23.x, b23.y};
 #pragma unroll
-            for (int i = 0; i < 8; i++)
+            for (int i = 0; i < 8; i++) {
+                const unsigned long long ap = dup_f32x2(av[i]);
 #pragma unroll
-                for (int j = 0; j < 8; j++) inner[i][j] = __fmaf_rn(av[i], bv[j], inner[i][j]);
+                for (int p = 0; p < 4; p++) fma_f32x2(inner[i][p], ap, bp[p]);
+            }
         }
         if ((step & 1) || step + 1 == nsteps) {
 #pragma unroll
             for (int i = 0; i < 8; i++)
 #pragma unroll
-                for (int j = 0; j < 8; j++) {
-                    outer[i][j] = __fadd_rn(outer[i][j], inner[i][j]);
-                    inner[i][j] = 0.f;
+                for (int p = 0; p < 4; p++) {
+                    add_f32x2(outer[i][p], inner[i][p]);
+                    inner[i][p] = 0ull;
                 }
         }
     }
@@ -406,7 +434,7 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
         for (int j = 0; j < 8; j++) {
             const int tt = (i < 4 ? 4 * ty + i : 32 + 4 * ty + i - 4);
             const int ee = (j < 4 ? 4 * tx + j : 32 + 4 * tx + j - 4);
-            red[(size_t)g * 4096 + tt * 64 + ee] = outer[i][j];
+            red[(size_t)g * 4096 + tt * 64 + ee] = unpack_f32x2(outer[i][j >> 1], j & 1);
         }
     __syncthreads();
     float *part = half == 0 ? part0 : part1;
