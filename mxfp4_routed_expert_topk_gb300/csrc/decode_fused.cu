@@ -357,6 +357,9 @@ __global__ void __launch_bounds__(kThreadsF, 1) decode_fused_kernel(const FusedA
     if (threadIdx.x < kMaxKF) a.hmax[threadIdx.x * G + b] = __uint_as_float(samax[threadIdx.x]);
     // every consumer warp takes part, aborted or not, so the named barriers match
     ok = grid_barrier(&a.st->pad[kStGridBarrier], a.barrier_count, 1, kCW * 32, a.st, 0x300u, abort_flag);
+    // phase B remains: the next kernel of the stream (the next router) may launch; it
+    // waits for this grid to complete before it reads anything
+    if (threadIdx.x == 0) griddep_launch_dependents();
 
     // ---- phase B: each lane owns up to two (pair, 32-block) combinations of h, in
     // registers as f16 scaled by a per-pair power of two (from the max |h| of the

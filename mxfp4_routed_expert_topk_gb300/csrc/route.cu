@@ -1074,6 +1074,10 @@ __global__ void __launch_bounds__(kRouteThreads) route_single_kernel(
     }
     __syncthreads();
     if (!last) return;
+    // every other CTA has exited: the next kernel (the expert forward) may launch and
+    // set itself up while this CTA selects; it reads idx and w only after this grid
+    // has completed
+    griddep_launch_dependents();
     // the exact fallback reads the token this CTA staged (x_hat when pre-scaled)
     select_token<J>(0, xhat != nullptr ? xrow : x, H, Wr, E, skew, k, logit, bound, idx_out, w_out, st, s);
     if (threadIdx.x == 0) st->pad[kStRouteTicket] = 0u;

@@ -425,7 +425,8 @@ def test_stacked_layers_full_size():
         3e-3 against a typical gap of about 0.04 between the 16th and 17th, so the
         routing of a token eventually diverges.  Per token the first layer whose
         routing differs is reported, and the streams entering it (x_8 if none) are
-        compared: max|err|/RMS recorded, relative L1 held to 5e-3."""
+        compared: max|err|/RMS recorded, relative L1 held to the streams' own rounding,
+        8 x 2^-9 (a bf16 half-ulp per layer)."""
     s = synth.FULL
     L, ntok = 8, 16
     pools = [make_pool(s, synth.pool_seed(l)) for l in range(L)]
@@ -472,7 +473,10 @@ def test_stacked_layers_full_size():
         ys.append(synth.bf16_bits_to_f64(xs[f, t]))
         refs.append(synth.bf16_bits_to_f64(layers[f]["x"][0] if f < L else x_fin[0]))
     print(f"config 2 free-running: first layer whose routing diverged, per token (8 = none): {first}")
-    report_close(np.stack(ys), np.stack(refs), "config 2: free-running stream at first divergence")
+    # each side rounds its own stream to bf16 after every layer: at most a half-ulp
+    # (2^-9 relative) per layer apart, over at most 8 layers
+    report_close(np.stack(ys), np.stack(refs), "config 2: free-running stream at first divergence",
+                 rel_l1=L * 2.0 ** -9)
     assert min(first) >= 1          # layer 0 sees the same x_0 on both sides
     del pools
     torch.cuda.empty_cache()
