@@ -600,6 +600,21 @@ def run_profile_case(args):
     pool = moe.Pool(s.E, s.H, s.I)
     moe.moe_pool_fill_synthetic(pool, synth.pool_seed(0))
     Wr = torch.from_numpy(synth.router_bf16(synth.router_seed(0), s.E, s.H).view(np.int16)).cuda().view(torch.bfloat16)
+    if args.profile == "verify":
+        # four verify batches of --profile-tokens correlated rows (router, sort, split,
+        # grouped GEMMs, combine); the router at the full E = 896
+        Wr_full = torch.from_numpy(synth.router_bf16(synth.router_seed(0), synth.FULL.E, s.H).view(np.int16)).cuda()
+        Wr_full = Wr_full.view(torch.bfloat16)
+        M = args.profile_tokens
+        for b in range(4):
+            xb = synth.verify_batch_bf16(synth.TOKENS_SEED["verify"], b, M, s.H)
+            x = torch.from_numpy(xb.view(np.int16)).cuda().view(torch.bfloat16)
+            moe.moe_route_topk(x, Wr_full, s.k)
+            idx, w = moe.moe_route_topk(x, Wr, s.k)
+            moe.moe_expert_forward_decode(pool, x, idx, w)
+        torch.cuda.synchronize()
+        print("profile case done")
+        return
     if args.profile == "prefill":
         xb = synth.tokens_bf16(synth.TOKENS_SEED["prefill"], 0, args.profile_tokens, s.H)
         x = torch.from_numpy(xb.view(np.int16)).cuda().view(torch.bfloat16)
@@ -630,7 +645,7 @@ def main():
     ap.add_argument("--no-prefill", action="store_true", help="skip the expert-major prefill measurements")
     ap.add_argument("--no-extra", action="store_true",
                     help="skip the multi-token verify and 8-layer stacked measurements")
-    ap.add_argument("--profile", choices=["decode", "prefill", "route"], default=None,
+    ap.add_argument("--profile", choices=["decode", "prefill", "route", "verify"], default=None,
                     help="run a small case of the kernels for an ncu capture (no JSON line)")
     ap.add_argument("--profile-tokens", type=int, default=64,
                     help="tokens of the prefill profile case (64-expert pool)")

@@ -375,16 +375,18 @@ __global__ void gather_quant4_kernel(const uint16_t *__restrict__ x, int T, int 
 
 // Row r of the sorted pairs: x[perm[r] / k] as three E4M3 parts (rows 3r, 3r+1,
 // 3r+2) with one E8M0 scale per part and 32-block (split_part), scales in the
-// tile-ordered blocks.  One warp per (row, group of 8 blocks of 32).
+// tile-ordered blocks.  One warp per (row, chunk of kGatherChunk elements); per step of
+// 256 elements a lane takes 8 consecutive ones (16-byte loads), so a 32-block is 4
+// lanes and a 128-element K tile 16.
 __global__ void gather_split3_kernel(const uint16_t *__restrict__ x, int H, int I, int k, int E,
                                      const int32_t *__restrict__ idx, const int32_t *__restrict__ perm,
                                      const int32_t *__restrict__ offsets, const int32_t *__restrict__ tile_off, int BN,
                                      int nsfb, uint8_t *__restrict__ xq, uint8_t *__restrict__ xs,
                                      uint8_t *__restrict__ hs) {
     const int lane = threadIdx.x & 31;
+    const int nchunk = (H + kGatherChunk - 1) / kGatherChunk;
     const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const int ngrp = (H / 32 + 7) / 8;
-    const int r = gw / ngrp, grp = gw % ngrp;
+    const int r = gw / nchunk, chunk = gw % nchunk;
     if (r >= offsets[E]) return;
     const int p = perm[r];
     const int t = p / k, e = idx[p];
@@ -392,29 +394,50 @@ __global__ void gather_split3_kernel(const uint16_t *__restrict__ x, int H, int 
 #pragma unroll
     for (int q = 0; q < 3; q++) rt[q] = row_tile(e, 3 * (r - offsets[e]) + q, tile_off, BN);
     const uint16_t *xr = x + (size_t)t * H;
-    uint32_t word[3] = {0u, 0u, 0u};
-    for (int b0 = grp * 256; b0 < min(H, grp * 256 + 256); b0 += 32) {
-        float v = bf16_bits_to_float(xr[b0 + lane]);
-        const int blk = b0 / 32;
+    const int b_end = min(H, (chunk + 1) * kGatherChunk);
+    for (int b0 = chunk * kGatherChunk; b0 < b_end; b0 += 256) {
+        // H is a multiple of 128: the upper half-warp may have nothing in the last step
+        const bool on = b0 + lane * 8 < b_end;
+        float v[8];
+        if (on) {
+            const uint4 u4 = *reinterpret_cast<const uint4 *>(xr + b0 + lane * 8);
+            const unsigned int u[4] = {u4.x, u4.y, u4.z, u4.w};
+#pragma unroll
+            for (int i = 0; i < 4; i++) {
+                v[2 * i] = __uint_as_float(u[i] << 16);
+                v[2 * i + 1] = __uint_as_float(u[i] & 0xffff0000u);
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; i++) v[i] = 0.f;
+        }
+        const int kt = (b0 + lane * 8) >> 7;
 #pragma unroll
         for (int q = 0; q < 3; q++) {
-            float a = fabsf(v);
-            for (int off = 16; off > 0; off >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, off));
-            const int X = split_exp(a);
-            xq[((size_t)3 * r + q) * H + b0 + lane] = split_part(v, X);
-            word[q] |= (uint32_t)(X + 127) << (8 * (blk & 3));
-        }
-        if ((blk & 3) == 3) {
+            // max |remainder| of the 32-block (the 4 lanes that hold it)
+            float a = 0.f;
 #pragma unroll
-            for (int q = 0; q < 3; q++) {
-                if (lane == 0)
-                    *reinterpret_cast<uint32_t *>(xs + sf_tile_word(rt[q].tile, H / 128, nsfb, blk >> 2, rt[q].col)) =
-                        word[q];
-                word[q] = 0;
+            for (int i = 0; i < 8; i++) a = fmaxf(a, fabsf(v[i]));
+            a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
+            a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
+            const int X = split_exp(a);
+            uint32_t c[2] = {0u, 0u};
+#pragma unroll
+            for (int i = 0; i < 8; i++) c[i >> 2] |= (uint32_t)split_part(v[i], X) << (8 * (i & 3));
+            // scale word of each K tile: the bytes of lanes 16h, 16h+4, 16h+8, 16h+12
+            const uint32_t sb = (uint32_t)(X + 127);
+            const uint32_t b1 = __shfl_down_sync(0xffffffffu, sb, 4);
+            const uint32_t b2 = __shfl_down_sync(0xffffffffu, sb, 8);
+            const uint32_t b3 = __shfl_down_sync(0xffffffffu, sb, 12);
+            if (on) {
+                *reinterpret_cast<uint2 *>(xq + ((size_t)3 * r + q) * H + b0 + lane * 8) = make_uint2(c[0], c[1]);
+                if ((lane & 15) == 0)
+                    *reinterpret_cast<uint32_t *>(xs + sf_tile_word(rt[q].tile, H / 128, nsfb, kt, rt[q].col)) =
+                        sb | (b1 << 8) | (b2 << 16) | (b3 << 24);
             }
         }
     }
-    if (lane == 0 && grp == 0) {
+    if (lane == 0 && chunk == 0) {
 #pragma unroll
         for (int q = 0; q < 3; q++) zero_h_pad(hs, I, nsfb, rt[q]);
     }
@@ -635,10 +658,10 @@ cudaError_t launch_decode_multi(const PoolView &v, const uint16_t *x, int M, con
     }
     {
         TraceScope trace_scope("gather_split", st);
-        const int ngrp = (v.H / 32 + 7) / 8;
-        gather_split3_kernel<<<(P * ngrp * 32 + 255) / 256, 256, 0, st>>>(x, v.H, v.I, k, v.E, idx, d.perm, d.offsets,
-                                                                           d.g.tile_off, d.g.BN, d.g.nsfb, d.g.xq,
-                                                                           d.g.xs, d.g.hs);
+        const int nchunk = (v.H + kGatherChunk - 1) / kGatherChunk;
+        gather_split3_kernel<<<(P * nchunk * 32 + 255) / 256, 256, 0, st>>>(x, v.H, v.I, k, v.E, idx, d.perm,
+                                                                             d.offsets, d.g.tile_off, d.g.BN, d.g.nsfb,
+                                                                             d.g.xq, d.g.xs, d.g.hs);
     }
     cudaError_t e = launch_grouped_gemms(v, M, k, d.offsets, d.g, d.partial, MOE_PARTIAL_F32, stw, st, 3);
     if (e != cudaSuccess) return e;

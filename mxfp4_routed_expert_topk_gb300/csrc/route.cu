@@ -91,6 +91,19 @@ __device__ void logits_block(const uint16_t *__restrict__ x, int M, int H, const
     const int m0 = blockIdx.y * kLogitTokens;
     const int nt = min(kLogitTokens, M - m0);
     const int nvec = nt * H / 8;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int e = blockIdx.x * kLogitExperts + (warp >> 1);
+    const int hmid = ((H / 2) + 7) / 8 * 8;
+    const int h0 = (warp & 1) ? hmid : 0, h1 = (warp & 1) ? H : hmid;
+    const uint16_t *wrow = Wr + (size_t)(e < E ? e : 0) * H;
+    // this warp's first batch of W_r chunks is requested before x is staged, so the
+    // two latencies overlap
+    uint4 wv[NB];
+#pragma unroll
+    for (int c = 0; c < NB; c++) {
+        const int h = h0 + lane * 8 + 256 * c;
+        wv[c] = (e < E && h < h1) ? __ldg(reinterpret_cast<const uint4 *>(wrow + h)) : make_uint4(0u, 0u, 0u, 0u);
+    }
     const uint4 *xg = reinterpret_cast<const uint4 *>(x + (size_t)m0 * H);
     for (int i = threadIdx.x; i < nvec; i += blockDim.x) reinterpret_cast<uint4 *>(xs)[i] = xg[i];
     __syncthreads();
@@ -133,10 +146,6 @@ __device__ void logits_block(const uint16_t *__restrict__ x, int M, int H, const
         __syncthreads();
     }
 
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int e = blockIdx.x * kLogitExperts + (warp >> 1);
-    const int hmid = ((H / 2) + 7) / 8 * 8;
-    const int h0 = (warp & 1) ? hmid : 0, h1 = (warp & 1) ? H : hmid;
     // acc: the partial logit; ea, eb: u times the magnitudes of the additions below
     // it (two chains, rounded upwards)
     constexpr float u = 5.9604645e-8f;  // 2^-24
@@ -144,15 +153,16 @@ __device__ void logits_block(const uint16_t *__restrict__ x, int M, int H, const
 #pragma unroll
     for (int t = 0; t < kLogitTokens; t++) acc[t] = ea[t] = eb[t] = 0.f;
     if (e < E) {
-        const uint16_t *wrow = Wr + (size_t)e * H;
-        // batches of NB chunks: all loads of a batch issued before any arithmetic;
-        // chunks are still summed in increasing h (the order the bound assumes)
+        // batches of NB chunks: all loads of a batch issued before any arithmetic (the
+        // first before x was staged); chunks are summed in increasing h (the order the
+        // bound assumes)
         for (int hb = h0 + lane * 8; hb < h1; hb += 256 * NB) {
-            uint4 wv[NB];
+            if (hb != h0 + lane * 8) {
 #pragma unroll
-            for (int c = 0; c < NB; c++) {
-                const int h = hb + 256 * c;
-                wv[c] = h < h1 ? __ldg(reinterpret_cast<const uint4 *>(wrow + h)) : make_uint4(0u, 0u, 0u, 0u);
+                for (int c = 0; c < NB; c++) {
+                    const int h = hb + 256 * c;
+                    wv[c] = h < h1 ? __ldg(reinterpret_cast<const uint4 *>(wrow + h)) : make_uint4(0u, 0u, 0u, 0u);
+                }
             }
 #pragma unroll
             for (int c = 0; c < NB; c++) {
@@ -225,7 +235,7 @@ __global__ void __launch_bounds__(256) route_logits_kernel(const uint16_t *__res
                                                            const uint16_t *__restrict__ Wr, int E,
                                                            const float *__restrict__ skew,
                                                            float *__restrict__ logit, float *__restrict__ bound) {
-    logits_block<8>(x, M, H, Wr, E, skew, logit, bound);
+    logits_block<16>(x, M, H, Wr, E, skew, logit, bound);
 }
 
 // ------------------------------------------------------- tiled logits (many tokens)
