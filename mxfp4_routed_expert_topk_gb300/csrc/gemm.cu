@@ -72,6 +72,8 @@ struct GemmArgs {
     const int32_t *n_union;
     const uint8_t *bscale;    // xs or hs in tile order (sf_tile_word), nkt K tiles
     int BN;              // columns of the accumulator tile (multiple of 16)
+    int bbox;            // rows per tensor copy of B: BN (one copy per stage), or 16 (as many
+                         // copies as the tile's MMA width needs: narrow tiles)
     int nsfb;            // 512-byte scale atoms of B per K tile = ceil(BN / 128)
     int ns;              // pipeline stages
     int nmt;             // 128-row tiles of A per expert
@@ -328,6 +330,91 @@ __device__ __forceinline__ int mx4_exp_from_bits(uint32_t amax_bits) { return ma
 // 2^-X as a float for X in [-127, 125] (always a normal number).
 __device__ __forceinline__ float pow2_neg(int X) { return __uint_as_float((uint32_t)(127 - X) << 23); }
 
+// Epilogue of the five-part MXFP4 activations (the multi-token decode on kind::mxf4):
+// 16 pairs (80 accumulator columns) at a time, each pair's value the sum of its five
+// columns in part order.  Gate/up: h = silu(g) * u, written as five MXFP4 parts per
+// 32-block along I (the split of gather_split5_f4_kernel; lanes 2m and 2m+1 pack one
+// byte); down: the unweighted expert output row in fp32.
+__device__ __forceinline__ void epilogue_split5_f4(const GemmArgs &a, uint32_t lane_base, bool ok, int nn, int nmma,
+                                                   int mt, int row0, int n0, int tile, int warp, int wg, int nwg,
+                                                   int lane, float *amax_x) {
+    constexpr int NP = 5;
+    const int bar = 2 + 2 * wg + (warp >> 1);  // the warp pair's barrier
+    for (int c0 = 16 * NP * wg; c0 < nmma; c0 += 16 * NP * nwg) {
+        float v[NP][16];
+#pragma unroll
+        for (int q = 0; q < NP; q++)
+#pragma unroll
+            for (int j = 0; j < 16; j++) v[q][j] = 0.f;
+        if (ok) {
+#pragma unroll
+            for (int q = 0; q < NP; q++) tmem_ld16(lane_base + (uint32_t)(c0 + 16 * q), v[q]);
+        }
+        float pv[16];
+#pragma unroll
+        for (int j = 0; j < 16; j++) {
+            float acc = 0.f;
+#pragma unroll
+            for (int q = 0; q < NP; q++) {
+                const int c = NP * j + q;  // column c of the group: register c % 16 of load c / 16
+                acc = q == 0 ? v[c >> 4][c & 15] : acc + v[c >> 4][c & 15];
+            }
+            pv[j] = acc;
+        }
+        const int pair0 = (row0 + n0 + c0) / NP;
+        const int npair = min(16, (nn - c0) / NP);  // pairs of this group with all their columns
+        if (a.mode == 1) {
+            // lanes 0-15: gate rows, 16-31: up rows of the same 16 intermediate indices
+            const int i = (4 * mt + warp) * 16 + (lane & 15);
+            float hv[16];
+#pragma unroll
+            for (int j = 0; j < 16; j++) {
+                const float u = __shfl_down_sync(0xffffffffu, pv[j], 16);
+                hv[j] = (lane < 16) ? __fdividef(pv[j], 1.f + __expf(-pv[j])) * u : 0.f;
+            }
+#pragma unroll 1
+            for (int q = 0; q < NP; q++) {
+                // max |remainder| of each pair's 32-block along I (warps 2w and 2w+1)
+                float am[16];
+#pragma unroll
+                for (int j = 0; j < 16; j++) {
+                    float m = fabsf(hv[j]);
+#pragma unroll
+                    for (int off = 8; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+                    am[j] = m;
+                }
+                if (lane == 0) {
+#pragma unroll
+                    for (int j = 0; j < 16; j++) amax_x[warp * 16 + j] = am[j];
+                }
+                named_barrier(bar, 64);
+#pragma unroll
+                for (int j = 0; j < 16; j++) {
+                    const int X = mx4_exp(fmaxf(amax_x[warp * 16 + j], amax_x[(warp ^ 1) * 16 + j]));
+                    const float hs = hv[j] * pow2_neg(X);
+                    const float hn = __shfl_down_sync(0xffffffffu, hs, 1);
+                    const uint8_t byte = e2m1x2_rn(hs, hn);  // this lane's code in the low nibble
+                    hv[j] -= e2m1_nibble_value(byte) * __uint_as_float((uint32_t)(X + 127) << 23);
+                    if (ok && j < npair && lane < 16 && (lane & 1) == 0) {
+                        const uint64_t r = (uint64_t)NP * (pair0 + j) + q;
+                        a.hq[r * (a.I / 2) + (i >> 1)] = byte;
+                        if (lane == 0 && (warp & 1) == 0)
+                            a.hs[sf_tile_word(tile, a.nkt_h, a.nsfb, i >> 7, c0 + NP * j + q) + ((i >> 5) & 3)] =
+                                (uint8_t)(X + 127);
+                    }
+                }
+                named_barrier(bar, 64);
+            }
+        } else {
+            const int o = mt * kTileM + 32 * warp + lane;
+#pragma unroll
+            for (int j = 0; j < 16; j++)
+                if (ok && j < npair && o < a.H)
+                    reinterpret_cast<float *>(a.partial)[(uint64_t)(pair0 + j) * a.H + o] = pv[j];
+        }
+    }
+}
+
 // One-part (MXFP8) epilogue of a tile's 16-column groups: gate/up -> h = silu(g) * u
 // quantised to MXFP8 along I (OCP rule); down -> expert output rows.  ew = warp
 // index within the epilogue warpgroup (TMEM lanes 32ew..32ew+31); warpgroup wg of nwg
@@ -551,15 +638,18 @@ __global__ void __launch_bounds__(NT, GemmShape<NT>::kCtasPerSm)
                     // 128-K scale tiles (the last stage of an odd count has one)
                     const int n2 = min(2, a.nkt_sf - 2 * kt);
                     const uint32_t sfbk = sfb_stage_bytes(nsfb);  // per 128-K tile
+                    const int brows = a.bbox == a.BN ? a.BN : (J.nn() + 15) / 16 * 16;  // B rows copied
                     const uint32_t tx =
-                        (uint32_t)(tpi * kTileM * kTileK + a.BN * kTileK) + (uint32_t)n2 * (512u + sfbk);
+                        (uint32_t)(tpi * kTileM * kTileK + brows * kTileK) + (uint32_t)n2 * (512u + sfbk);
                     const uint8_t *sfa_src =
                         a.pool + (uint64_t)J.e * a.rec + a.a_sf_off + ((uint64_t)(2 * kt) * a.nmt + J.mt) * 512;
                     const uint8_t *sfb_src = a.bscale + sf_tile_word(J.tile(), a.nkt_sf, nsfb, 2 * kt, 0);
                     if (elect_one()) {
                         mbar_arrive_expect_tx(&full[s], tx);
                         tma_load_3d(sA + (size_t)s * kTileM * kTileK, &tmA, kt * kTileK, J.mt * kTileM, J.e, &full[s]);
-                        tma_load_2d(sB + (size_t)s * a.BN * kTileK, &tmB, kt * kTileK, brow, &full[s]);
+                        for (int c = 0; c < brows; c += a.bbox)
+                            tma_load_2d(sB + (size_t)s * a.BN * kTileK + (size_t)c * kTileK, &tmB, kt * kTileK,
+                                        brow + c, &full[s]);
                         for (int j = 0; j < n2; j++)  // the two K tiles' A blocks are nmt blocks apart
                             bulk_g2s_l2(sSFA + (size_t)s * 1024 + 512 * j, sfa_src + (size_t)j * a.nmt * 512, 512u,
                                         &full[s]);
@@ -574,8 +664,9 @@ __global__ void __launch_bounds__(NT, GemmShape<NT>::kCtasPerSm)
                         }
                     }
                 } else {
+                    const int brows = a.bbox == a.BN ? a.BN : (J.nn() + 15) / 16 * 16;  // B rows copied
                     const uint32_t tx =
-                        (uint32_t)(tpi * kTileM * kTileK / 2 + a.BN * kTileK) + a_tiles * 512u + sfb_stage_bytes(nsfb);
+                        (uint32_t)(tpi * kTileM * kTileK / 2 + brows * kTileK) + a_tiles * 512u + sfb_stage_bytes(nsfb);
                     const uint8_t *sfa_src =
                         a.pool + (uint64_t)J.e * a.rec + a.a_sf_off + ((uint64_t)kt * a.nmt + J.mt) * 512;
                     const uint8_t *sfb_src = a.bscale + sf_tile_word(J.tile(), a.nkt, nsfb, kt, 0);
@@ -583,7 +674,9 @@ __global__ void __launch_bounds__(NT, GemmShape<NT>::kCtasPerSm)
                         mbar_arrive_expect_tx(&full[s], tx);
                         tma_load_3d(sA + (size_t)s * tpi * kTileM * kTileK, &tmA, kt * kTileK, J.mt * kTileM, J.e,
                                     &full[s]);
-                        tma_load_2d(sB + (size_t)s * a.BN * kTileK, &tmB, kt * kTileK, brow, &full[s]);
+                        for (int c = 0; c < brows; c += a.bbox)
+                            tma_load_2d(sB + (size_t)s * a.BN * kTileK + (size_t)c * kTileK, &tmB, kt * kTileK,
+                                        brow + c, &full[s]);
                         bulk_g2s_l2(sSFA + (size_t)s * tpi * 512, sfa_src, a_tiles * 512u, &full[s]);
                         if (nsfb == 1) {
                             bulk_g2s_l2(sSFB + (size_t)s * 512, sfb_src, 512u, &full[s]);
@@ -747,6 +840,9 @@ __global__ void __launch_bounds__(NT, GemmShape<NT>::kCtasPerSm)
                 if (a.nparts == 3)
                     epilogue_split3(a, lane_base, ok, nn, nmma, J.mt + t, J.row0, J.n0(), J.tile(), ew, wg,
                                     Shape::kWarpGroups, lane, amax_g);
+                else if (FP4 && a.nparts == 5)
+                    epilogue_split5_f4(a, lane_base, ok, nn, nmma, J.mt + t, J.row0, J.n0(), J.tile(), ew, wg,
+                                       Shape::kWarpGroups, lane, amax_g);
                 else
                     epilogue_mx1<FP4>(a, lane_base, ok, nn, nmma, J.mt + t, J.row0, J.n0(), J.tile(), ew, wg,
                                       Shape::kWarpGroups, lane, amax_g);
@@ -857,7 +953,8 @@ cudaError_t launch_one(GemmArgs ga, const uint8_t *a_base, int a_k, int a_rows, 
     cudaError_t e = device_attr(cudaDevAttrMaxSharedMemoryPerBlockOptin, g_smem_max, &smem_max);
     if (e != cudaSuccess) return e;
     if ((e = device_attr(cudaDevAttrMultiProcessorCount, g_sms, &sms)) != cudaSuccess) return e;
-    const bool two = BN <= 64 || (BN <= 96 && ga.mode == 1);
+    // (FP4: the down GEMM too at BN <= 96, where its K loop is short: 7 stages at I = 1600)
+    const bool two = BN <= 64 || (BN <= 96 && (ga.mode == 1 || fp4));
     const int tpi = fp4 || two ? 1 : (BN <= 96 ? 2 : 1);
     const uint32_t smem_cap = two ? (uint32_t)(smem_max / 2 - 1024) : (uint32_t)smem_max;
     const uint32_t tmem_cap = two ? 256u : 512u;
@@ -882,16 +979,20 @@ cudaError_t launch_one(GemmArgs ga, const uint8_t *a_base, int a_k, int a_rows, 
     ga.ns = ns;
     ga.tpi = tpi;
     ga.nacc = nacc;
+    // narrow tiles copy B in 16-row boxes, only the rows the tile's MMAs read: verify
+    // tiles (several parts per row) hold a few rows in a box sized for 32, and prefill
+    // tiles up to 64 columns are sized for the expert rows' spread
+    ga.bbox = (ga.nparts > 1 || BN <= 64) ? 16 : BN;
     ga.tmem_cols = tmem_cols;
     ga.nkt_sf = a_k / kTileK;
     ga.nkt = fp4 ? (ga.nkt_sf + 1) / 2 : ga.nkt_sf;
     CUtensorMap mA, mB;
     if (fp4) {
         if ((e = make_map_a4(&mA, a_base, a_k / 2, a_rows, E, a_ld, ga.rec, kTileM)) != cudaSuccess) return e;
-        if ((e = make_map_b(&mB, b_base, b_k / 2, b_rows, BN)) != cudaSuccess) return e;
+        if ((e = make_map_b(&mB, b_base, b_k / 2, b_rows, ga.bbox)) != cudaSuccess) return e;
     } else {
         if ((e = make_map_a(&mA, a_base, a_k, a_rows, E, a_ld, ga.rec, tpi * kTileM)) != cudaSuccess) return e;
-        if ((e = make_map_b(&mB, b_base, b_k, b_rows, BN)) != cudaSuccess) return e;
+        if ((e = make_map_b(&mB, b_base, b_k, b_rows, ga.bbox)) != cudaSuccess) return e;
     }
     const int items = nexp * ((ga.nmt + tpi - 1) / tpi);
     TraceScope trace_scope(trace_name, stream);
@@ -918,8 +1019,8 @@ cudaError_t launch_grouped_gemms(const PoolView &v, int T, int k, const int32_t 
                                  bool fp4) {
     const int P = T * k;
     if (P == 0) return cudaSuccess;
-    if (nparts != 1 && nparts != 3) return cudaErrorInvalidValue;
-    if (fp4 && nparts != 1) return cudaErrorInvalidValue;
+    // one MXFP8 or MXFP4 row per pair, three E4M3 parts (mxf8f6f4) or five MXFP4 parts (mxf4)
+    if (!(nparts == 1 || (nparts == 3 && !fp4) || (nparts == 5 && fp4))) return cudaErrorInvalidValue;
     cudaError_t e = get_encoder();
     if (e != cudaSuccess) return e;
     // one expert has at most T pairs (distinct slots of a row), so with three parts

@@ -443,6 +443,79 @@ __global__ void gather_split3_kernel(const uint16_t *__restrict__ x, int H, int 
     }
 }
 
+// gather_split3_kernel with five MXFP4 parts (rows 5r .. 5r+4, two codes per byte, H/2
+// bytes per row) for the kind::mxf4 multi-token decode: part q takes the remainder's
+// shared exponent floor(log2 amax) - 2 and its E2M1 codes (RNE, saturating), and the
+// remainder drops what the codes represent (exact in fp32: a code keeps the leading
+// bits of the remainder, and a saturated code lies below it within a factor of two).
+// Each part shrinks the block's largest remainder about fourfold; five keep the layer's
+// outputs within about 3e-4 of RMS of the unquantised result.
+__global__ void gather_split5_f4_kernel(const uint16_t *__restrict__ x, int H, int I, int k, int E,
+                                        const int32_t *__restrict__ idx, const int32_t *__restrict__ perm,
+                                        const int32_t *__restrict__ offsets, const int32_t *__restrict__ tile_off,
+                                        int BN, int nsfb, uint8_t *__restrict__ xq, uint8_t *__restrict__ xs,
+                                        uint8_t *__restrict__ hs) {
+    constexpr int NP = kDecodeParts;
+    const int lane = threadIdx.x & 31;
+    const int nchunk = (H + kGatherChunk - 1) / kGatherChunk;
+    const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int r = gw / nchunk, chunk = gw % nchunk;
+    if (r >= offsets[E]) return;
+    const int p = perm[r];
+    const int t = p / k, e = idx[p];
+    RowTile rt[NP];
+#pragma unroll
+    for (int q = 0; q < NP; q++) rt[q] = row_tile(e, NP * (r - offsets[e]) + q, tile_off, BN);
+    const uint16_t *xr = x + (size_t)t * H;
+    const int b_end = min(H, (chunk + 1) * kGatherChunk);
+    for (int b0 = chunk * kGatherChunk; b0 < b_end; b0 += 256) {
+        const bool on = b0 + lane * 8 < b_end;
+        float v[8];
+        if (on) {
+            const uint4 u4 = *reinterpret_cast<const uint4 *>(xr + b0 + lane * 8);
+            const unsigned int u[4] = {u4.x, u4.y, u4.z, u4.w};
+#pragma unroll
+            for (int i = 0; i < 4; i++) {
+                v[2 * i] = __uint_as_float(u[i] << 16);
+                v[2 * i + 1] = __uint_as_float(u[i] & 0xffff0000u);
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; i++) v[i] = 0.f;
+        }
+        const int kt = (b0 + lane * 8) >> 7;
+#pragma unroll
+        for (int q = 0; q < NP; q++) {
+            float a = 0.f;
+#pragma unroll
+            for (int i = 0; i < 8; i++) a = fmaxf(a, fabsf(v[i]));
+            a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
+            a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
+            const int X = mx4_exp(a);
+            float sc[8];
+#pragma unroll
+            for (int i = 0; i < 8; i++) sc[i] = ldexpf(v[i], -X);
+            const uint32_t c = e2m1x8_rn(sc);
+#pragma unroll
+            for (int i = 0; i < 8; i++) v[i] -= ldexpf(e2m1_nibble_value(c >> (4 * i)), X);
+            const uint32_t sb = (uint32_t)(X + 127);
+            const uint32_t b1 = __shfl_down_sync(0xffffffffu, sb, 4);
+            const uint32_t b2 = __shfl_down_sync(0xffffffffu, sb, 8);
+            const uint32_t b3 = __shfl_down_sync(0xffffffffu, sb, 12);
+            if (on) {
+                *reinterpret_cast<uint32_t *>(xq + ((size_t)NP * r + q) * (H / 2) + (b0 + lane * 8) / 2) = c;
+                if ((lane & 15) == 0)
+                    *reinterpret_cast<uint32_t *>(xs + sf_tile_word(rt[q].tile, H / 128, nsfb, kt, rt[q].col)) =
+                        sb | (b1 << 8) | (b2 << 16) | (b3 << 24);
+            }
+        }
+    }
+    if (lane == 0 && chunk == 0) {
+#pragma unroll
+        for (int q = 0; q < NP; q++) zero_h_pad(hs, I, nsfb, rt[q]);
+    }
+}
+
 template <typename PT>
 __device__ __forceinline__ float load_partial(const PT *p);
 template <>
@@ -646,7 +719,7 @@ size_t decode_multi_workspace_bytes(int E, int H, int I, int M, int k) {
 
 cudaError_t launch_decode_multi(const PoolView &v, const uint16_t *x, int M, const int32_t *idx, const float *w, int k,
                                 const uint16_t *residual, uint16_t *y, void *ws, cudaStream_t st) {
-    if (v.E > kMaxSortE || v.I % 64 != 0 || v.H % 128 != 0 || 3 * M > 96) return cudaErrorNotSupported;
+    if (v.E > kMaxSortE || v.I % 64 != 0 || v.H % 128 != 0 || M > kMaxDecodeRows) return cudaErrorNotSupported;
     const DecodeMultiWs d = decode_multi_ws_layout(ws, v.E, v.H, v.I, M, k);
     StatusWord *stw = reinterpret_cast<StatusWord *>(ws);
     const int P = M * k;
@@ -654,16 +727,16 @@ cudaError_t launch_decode_multi(const PoolView &v, const uint16_t *x, int M, con
     {
         TraceScope trace_scope("sort_small", st);
         sort_small_kernel<<<1, 1024, 0, st>>>(idx, P, v.E, d.offsets, d.g.uexp, d.g.n_union, d.perm, d.inv_perm,
-                                              d.g.tile_off, d.g.BN, 3, stw);
+                                              d.g.tile_off, d.g.BN, kDecodeParts, stw);
     }
     {
         TraceScope trace_scope("gather_split", st);
         const int nchunk = (v.H + kGatherChunk - 1) / kGatherChunk;
-        gather_split3_kernel<<<(P * nchunk * 32 + 255) / 256, 256, 0, st>>>(x, v.H, v.I, k, v.E, idx, d.perm,
-                                                                             d.offsets, d.g.tile_off, d.g.BN, d.g.nsfb,
-                                                                             d.g.xq, d.g.xs, d.g.hs);
+        gather_split5_f4_kernel<<<(P * nchunk * 32 + 255) / 256, 256, 0, st>>>(
+            x, v.H, v.I, k, v.E, idx, d.perm, d.offsets, d.g.tile_off, d.g.BN, d.g.nsfb, d.g.xq, d.g.xs, d.g.hs);
     }
-    cudaError_t e = launch_grouped_gemms(v, M, k, d.offsets, d.g, d.partial, MOE_PARTIAL_F32, stw, st, 3);
+    cudaError_t e = launch_grouped_gemms(v, M, k, d.offsets, d.g, d.partial, MOE_PARTIAL_F32, stw, st, kDecodeParts,
+                                         true);
     if (e != cudaSuccess) return e;
     {
         TraceScope trace_scope("combine", st);

@@ -18,12 +18,14 @@ constexpr int kMaxBN4 = 192;     // ... with MXFP4 activations
 // with more rows takes several tiles; narrow tiles let the GEMMs run two CTAs per SM);
 // the same rule with MXFP4 activations (fp4).
 // nparts = 3: all of an expert's rows (at most 3T) in one tile, in whole groups of 16
-// pairs.
+// pairs; nparts = 5: tiles of 16 pairs.
 __host__ __device__ inline int grouped_bn(int P, int E, int T, int nparts, bool fp4 = false) {
     if (nparts == 3) {
         const int bn = (3 * T + 47) / 48 * 48;
         return bn > kMaxBN ? 0 : bn;
     }
+    if (nparts == 5) return 80;  // five MXFP4 parts: one group of 16 pairs per tile (an expert
+                                 // with more rows takes further tiles); one scale atom
     const int cap = fp4 ? kMaxBN4 : kMaxBN;
     const int mean = (P + E - 1) / E;
     int bn = (3 * mean / 2 + 31) / 32 * 32;
@@ -114,9 +116,12 @@ struct DecodeMultiWs {
     size_t end;
 };
 
+// The multi-token decode writes each row and h as five MXFP4 parts (kind::mxf4).
+constexpr int kDecodeParts = 5;
+
 __host__ __device__ inline DecodeMultiWs decode_multi_ws_layout(void *ws, int E, int H, int I, int M, int k) {
     DecodeMultiWs d;
-    d.g = grouped_ws_layout(ws, E, H, I, M, k, 3);
+    d.g = grouped_ws_layout(ws, E, H, I, M, k, kDecodeParts, true);
     const size_t P = (size_t)M * k;
     char *base = (char *)ws;
     size_t o = d.g.end;
@@ -126,6 +131,18 @@ __host__ __device__ inline DecodeMultiWs decode_multi_ws_layout(void *ws, int E,
     d.partial = (float *)(base + o);    o += align_up(P * H * 4, 1024);
     d.end = o;
     return d;
+}
+
+// MXFP4 shared exponent of a block with max |v| = amax (finite, non-negative):
+// floor(log2 amax) - 2, or -127 for zero and values below 2^-125 (OCP MX rule).
+__device__ __forceinline__ int mx4_exp(float amax) { return max(-127, (int)(__float_as_uint(amax) >> 23) - 129); }
+
+// Value of an E2M1 code (the low 4 bits of `nib`): sign bit 3, exponent bits 2..1
+// (bias 1), mantissa bit 0.
+__device__ __forceinline__ float e2m1_nibble_value(uint32_t nib) {
+    const uint32_t m = nib & 7u, e = m >> 1, f = m & 1u;
+    const float mag = e == 0u ? 0.5f * (float)f : __uint_as_float((126u + e) << 23) * (1.f + 0.5f * (float)f);
+    return (nib & 8u) ? -mag : mag;
 }
 
 // E8M0 exponent of one E4M3 part of a 32-element block with max |v| = amax: the

@@ -283,6 +283,27 @@ def test_decode_full_verify_batches(full, M):
                       opool=opool)
 
 
+@pytest.mark.parametrize("M", [20, 32])
+def test_decode_verify_hot_expert_spans_tiles(tiny, M):
+    """Planted routing for a verify batch: every row sends slot 0 to expert 0, so that
+    expert has M rows (more than the 16 pairs of one tile of the five-part path); each
+    row's output must match the oracle's on the same indices and weights."""
+    s, pool, _, _ = tiny
+    rng = np.random.default_rng(M)
+    xb = synth.verify_batch_bf16(synth.TOKENS_SEED["verify"], 50 + M, M, s.H)
+    idx_h = np.stack([np.concatenate([[0], 1 + rng.choice(s.E - 1, s.k - 1, replace=False)]) for _ in range(M)])
+    w_h = rng.dirichlet(np.ones(s.k), size=M)
+    idx = torch.from_numpy(idx_h.astype(np.int32)).cuda()
+    w = torch.from_numpy(w_h.astype(np.float32)).cuda()
+    ws = moe.workspace(moe.moe_workspace_size(moe.MOE_OP_DECODE, s.E, s.H, s.I, M, s.k))
+    y = moe.moe_expert_forward_decode(pool, to_dev_bf16(xb), idx, w, ws=ws)
+    assert moe.moe_check_status(ws) == moe.MOE_OK
+    opool = oracle.SyntheticPool(synth.pool_seed(0), s.E, s.H, s.I, cache=s.E)
+    ref = oracle.combine_rows(opool, s.H, s.I, synth.bf16_bits_to_f64(xb), idx_h, w_h.astype(np.float32).astype(np.float64))
+    yg = bf16_to_f64(y)
+    check_close(yg, ref, "verify with a hot expert (M rows)", bf16_at=yg)
+
+
 @pytest.mark.parametrize("E,H,I,k,M", [(40, 384, 96, 8, 3), (20, 256, 160, 4, 7), (33, 640, 224, 32, 2)])
 def test_decode_ragged_shapes(E, H, I, k, M):
     s = synth.Shape(E=E, H=H, I=I, k=k)
