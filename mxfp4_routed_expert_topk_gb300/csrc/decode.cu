@@ -2,8 +2,8 @@
 //
 // One row runs the fused cooperative kernel (decode_fused.cu).  Several rows (the
 // verify batch of the four-SSD page, "可选的 Qwen 扩展": one forward pass checks
-// several rows) run on the tensor cores through the grouped GEMMs with three-part
-// E4M3 activations (launch_decode_multi in prefill.cu) when I is a multiple of 64;
+// several rows) run on the tensor cores through the grouped GEMMs with five-part
+// MXFP4 activations (launch_decode_multi in prefill.cu) when I is a multiple of 64;
 // otherwise the kernels below read each distinct selected expert from the pool once
 // and dequantise its packed 4-bit weights in registers:
 //   decode_prep_kernel    union of selected experts, per-expert row lists,

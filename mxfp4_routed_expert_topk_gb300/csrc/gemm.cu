@@ -24,8 +24,8 @@
 // warps drain the other accumulator, so a tile's epilogue overlaps the next tile's
 // MMAs.  Two shapes (GemmShape): one CTA of 12 warps per SM (two epilogue warpgroups)
 // or two CTAs of 6 warps per SM (one), chosen per launch by the tile width.  With
-// three-part activations (nparts = 3, the multi-token decode) each sorted pair has
-// three B rows whose columns the epilogue sums.  Every wait is bounded
+// five-part MXFP4 activations (nparts = 5, the multi-token decode) each sorted pair
+// has five B rows whose columns the epilogue sums.  Every wait is bounded
 // (MOE_ERR_TIMEOUT), and nothing exits with copies or MMAs in flight.
 #include <algorithm>
 
@@ -240,80 +240,6 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
         : "memory");
 #pragma unroll
     for (int i = 0; i < 16; i++) v[i] = __uint_as_float(r[i]);
-}
-
-// Epilogue of the three-part activations: 16 pairs (48 accumulator columns) at a
-// time, each pair's value the sum of its three columns in part order.  Gate/up:
-// h = silu(g) * u, written as three E4M3 parts per 32-block along I (split_part);
-// down: the unweighted expert output row in fp32.
-__device__ __forceinline__ void epilogue_split3(const GemmArgs &a, uint32_t lane_base, bool ok, int nn, int nmma, int mt,
-                                                int row0, int n0, int tile, int warp, int wg, int nwg, int lane,
-                                                float *amax_x) {
-    const int bar = 2 + 2 * wg + (warp >> 1);  // the warp pair's barrier
-    for (int c0 = 48 * wg; c0 < nmma; c0 += 48 * nwg) {
-        float v0[16], v1[16], v2[16];
-#pragma unroll
-        for (int j = 0; j < 16; j++) v0[j] = v1[j] = v2[j] = 0.f;
-        if (ok) {
-            tmem_ld16(lane_base + (uint32_t)c0, v0);
-            tmem_ld16(lane_base + (uint32_t)c0 + 16, v1);
-            tmem_ld16(lane_base + (uint32_t)c0 + 32, v2);
-        }
-        auto col = [&](int c) { return c < 16 ? v0[c] : (c < 32 ? v1[c - 16] : v2[c - 32]); };
-        float pv[16];
-#pragma unroll
-        for (int j = 0; j < 16; j++) pv[j] = (col(3 * j) + col(3 * j + 1)) + col(3 * j + 2);
-        // sorted pair of column group j: (row0 + n0 + c0) / 3 + j
-        const int pair0 = (row0 + n0 + c0) / 3;
-        const int npair = min(16, (nn - c0) / 3);  // pairs of this group with all three columns
-        if (a.mode == 1) {
-            // lanes 0-15: gate rows, 16-31: up rows of the same 16 intermediate indices
-            const int i = (4 * mt + warp) * 16 + (lane & 15);
-            float hv[16];
-#pragma unroll
-            for (int j = 0; j < 16; j++) {
-                const float u = __shfl_down_sync(0xffffffffu, pv[j], 16);
-                hv[j] = (lane < 16) ? __fdividef(pv[j], 1.f + __expf(-pv[j])) * u : 0.f;
-            }
-#pragma unroll 1
-            for (int q = 0; q < 3; q++) {
-                // max |remainder| of each pair's 32-block along I (warps 2w and 2w+1)
-                float am[16];
-#pragma unroll
-                for (int j = 0; j < 16; j++) {
-                    float m = fabsf(hv[j]);
-#pragma unroll
-                    for (int off = 8; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-                    am[j] = m;
-                }
-                if (lane == 0) {
-#pragma unroll
-                    for (int j = 0; j < 16; j++) amax_x[warp * 16 + j] = am[j];
-                }
-                named_barrier(bar, 64);
-#pragma unroll
-                for (int j = 0; j < 16; j++) {
-                    const int X = split_exp(fmaxf(amax_x[warp * 16 + j], amax_x[(warp ^ 1) * 16 + j]));
-                    const uint8_t code = split_part(hv[j], X);
-                    if (ok && j < npair && lane < 16) {
-                        const uint64_t r = (uint64_t)3 * (pair0 + j) + q;
-                        a.hq[r * a.I + i] = code;
-                        // column of row r in the tile: c0 + 3j + q (row0 + n0 is a multiple of 3)
-                        if (lane == 0 && (warp & 1) == 0)
-                            a.hs[sf_tile_word(tile, a.nkt_h, a.nsfb, i >> 7, c0 + 3 * j + q) + ((i >> 5) & 3)] =
-                                (uint8_t)(X + 127);
-                    }
-                }
-                named_barrier(bar, 64);
-            }
-        } else {
-            const int o = mt * kTileM + 32 * warp + lane;
-#pragma unroll
-            for (int j = 0; j < 16; j++)
-                if (ok && j < npair && o < a.H)
-                    reinterpret_cast<float *>(a.partial)[(uint64_t)(pair0 + j) * a.H + o] = pv[j];
-        }
-    }
 }
 
 // ------------------------------------------------------------------- kernel
@@ -837,10 +763,7 @@ __global__ void __launch_bounds__(NT, GemmShape<NT>::kCtasPerSm)
                 if (J.mt + t >= a.nmt) break;  // a half item past the expert's A rows (uniform)
                 const uint32_t lane_base =
                     tmem + (uint32_t)((buf * tpi + t) * a.BN) + ((uint32_t)(32 * ew) << 16);
-                if (a.nparts == 3)
-                    epilogue_split3(a, lane_base, ok, nn, nmma, J.mt + t, J.row0, J.n0(), J.tile(), ew, wg,
-                                    Shape::kWarpGroups, lane, amax_g);
-                else if (FP4 && a.nparts == 5)
+                if (FP4 && a.nparts == 5)
                     epilogue_split5_f4(a, lane_base, ok, nn, nmma, J.mt + t, J.row0, J.n0(), J.tile(), ew, wg,
                                        Shape::kWarpGroups, lane, amax_g);
                 else
@@ -1019,13 +942,11 @@ cudaError_t launch_grouped_gemms(const PoolView &v, int T, int k, const int32_t 
                                  bool fp4) {
     const int P = T * k;
     if (P == 0) return cudaSuccess;
-    // one MXFP8 or MXFP4 row per pair, three E4M3 parts (mxf8f6f4) or five MXFP4 parts (mxf4)
-    if (!(nparts == 1 || (nparts == 3 && !fp4) || (nparts == 5 && fp4))) return cudaErrorInvalidValue;
+    // one MXFP8 or MXFP4 row per pair, or five MXFP4 parts (mxf4)
+    if (!(nparts == 1 || (nparts == 5 && fp4))) return cudaErrorInvalidValue;
     cudaError_t e = get_encoder();
     if (e != cudaSuccess) return e;
-    // one expert has at most T pairs (distinct slots of a row), so with three parts
-    // all of its 3T columns fit one tile; the sort laid out the activation scales
-    // for this BN
+    // the sort laid out the activation scales for this BN
     const int BN = grouped_bn(P, v.E, T, nparts, fp4);
     if (BN == 0) return cudaErrorNotSupported;
     if (BN != g.BN) return cudaErrorInvalidValue;

@@ -10,7 +10,7 @@
 //   combine_kernel
 //        y[t] = sum_j w[t,j] partial[inv_perm[t*k+j]] (+ residual), slot order
 // The multi-token decode (launch_decode_multi) uses the same pieces with a one-CTA
-// sort (sort_small_kernel) and three-part activations (gather_split3_kernel).
+// sort (sort_small_kernel) and five-part MXFP4 activations (gather_split5_f4_kernel).
 #include <algorithm>
 
 #include "moe_internal.cuh"
@@ -373,78 +373,11 @@ __global__ void gather_quant4_kernel(const uint16_t *__restrict__ x, int T, int 
     if (chunk == 0 && myrow >= 0) zero_h_pad(hs, I, nsfb, myrt);
 }
 
-// Row r of the sorted pairs: x[perm[r] / k] as three E4M3 parts (rows 3r, 3r+1,
-// 3r+2) with one E8M0 scale per part and 32-block (split_part), scales in the
-// tile-ordered blocks.  One warp per (row, chunk of kGatherChunk elements); per step of
-// 256 elements a lane takes 8 consecutive ones (16-byte loads), so a 32-block is 4
-// lanes and a 128-element K tile 16.
-__global__ void gather_split3_kernel(const uint16_t *__restrict__ x, int H, int I, int k, int E,
-                                     const int32_t *__restrict__ idx, const int32_t *__restrict__ perm,
-                                     const int32_t *__restrict__ offsets, const int32_t *__restrict__ tile_off, int BN,
-                                     int nsfb, uint8_t *__restrict__ xq, uint8_t *__restrict__ xs,
-                                     uint8_t *__restrict__ hs) {
-    const int lane = threadIdx.x & 31;
-    const int nchunk = (H + kGatherChunk - 1) / kGatherChunk;
-    const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const int r = gw / nchunk, chunk = gw % nchunk;
-    if (r >= offsets[E]) return;
-    const int p = perm[r];
-    const int t = p / k, e = idx[p];
-    RowTile rt[3];
-#pragma unroll
-    for (int q = 0; q < 3; q++) rt[q] = row_tile(e, 3 * (r - offsets[e]) + q, tile_off, BN);
-    const uint16_t *xr = x + (size_t)t * H;
-    const int b_end = min(H, (chunk + 1) * kGatherChunk);
-    for (int b0 = chunk * kGatherChunk; b0 < b_end; b0 += 256) {
-        // H is a multiple of 128: the upper half-warp may have nothing in the last step
-        const bool on = b0 + lane * 8 < b_end;
-        float v[8];
-        if (on) {
-            const uint4 u4 = *reinterpret_cast<const uint4 *>(xr + b0 + lane * 8);
-            const unsigned int u[4] = {u4.x, u4.y, u4.z, u4.w};
-#pragma unroll
-            for (int i = 0; i < 4; i++) {
-                v[2 * i] = __uint_as_float(u[i] << 16);
-                v[2 * i + 1] = __uint_as_float(u[i] & 0xffff0000u);
-            }
-        } else {
-#pragma unroll
-            for (int i = 0; i < 8; i++) v[i] = 0.f;
-        }
-        const int kt = (b0 + lane * 8) >> 7;
-#pragma unroll
-        for (int q = 0; q < 3; q++) {
-            // max |remainder| of the 32-block (the 4 lanes that hold it)
-            float a = 0.f;
-#pragma unroll
-            for (int i = 0; i < 8; i++) a = fmaxf(a, fabsf(v[i]));
-            a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
-            a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
-            const int X = split_exp(a);
-            uint32_t c[2] = {0u, 0u};
-#pragma unroll
-            for (int i = 0; i < 8; i++) c[i >> 2] |= (uint32_t)split_part(v[i], X) << (8 * (i & 3));
-            // scale word of each K tile: the bytes of lanes 16h, 16h+4, 16h+8, 16h+12
-            const uint32_t sb = (uint32_t)(X + 127);
-            const uint32_t b1 = __shfl_down_sync(0xffffffffu, sb, 4);
-            const uint32_t b2 = __shfl_down_sync(0xffffffffu, sb, 8);
-            const uint32_t b3 = __shfl_down_sync(0xffffffffu, sb, 12);
-            if (on) {
-                *reinterpret_cast<uint2 *>(xq + ((size_t)3 * r + q) * H + b0 + lane * 8) = make_uint2(c[0], c[1]);
-                if ((lane & 15) == 0)
-                    *reinterpret_cast<uint32_t *>(xs + sf_tile_word(rt[q].tile, H / 128, nsfb, kt, rt[q].col)) =
-                        sb | (b1 << 8) | (b2 << 16) | (b3 << 24);
-            }
-        }
-    }
-    if (lane == 0 && chunk == 0) {
-#pragma unroll
-        for (int q = 0; q < 3; q++) zero_h_pad(hs, I, nsfb, rt[q]);
-    }
-}
-
-// gather_split3_kernel with five MXFP4 parts (rows 5r .. 5r+4, two codes per byte, H/2
-// bytes per row) for the kind::mxf4 multi-token decode: part q takes the remainder's
+// Row r of the sorted pairs: x[perm[r] / k] as five MXFP4 parts (rows 5r .. 5r+4, two
+// codes per byte, H/2 bytes per row) for the kind::mxf4 multi-token decode, with one
+// E8M0 scale per part and 32-block in the tile-ordered blocks.  One warp per (row,
+// 256-element step): a lane takes 8 consecutive elements (16-byte loads), a 32-block is
+// 4 lanes and a 128-element K tile 16.  Part q takes the remainder's
 // shared exponent floor(log2 amax) - 2 and its E2M1 codes (RNE, saturating), and the
 // remainder drops what the codes represent (exact in fp32: a code keeps the leading
 // bits of the remainder, and a saturated code lies below it within a factor of two).
@@ -456,8 +389,9 @@ __global__ void gather_split5_f4_kernel(const uint16_t *__restrict__ x, int H, i
                                         int BN, int nsfb, uint8_t *__restrict__ xq, uint8_t *__restrict__ xs,
                                         uint8_t *__restrict__ hs) {
     constexpr int NP = kDecodeParts;
+    constexpr int kChunk = 256;  // elements per warp: one step (few rows, so many warps)
     const int lane = threadIdx.x & 31;
-    const int nchunk = (H + kGatherChunk - 1) / kGatherChunk;
+    const int nchunk = (H + kChunk - 1) / kChunk;
     const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int r = gw / nchunk, chunk = gw % nchunk;
     if (r >= offsets[E]) return;
@@ -467,9 +401,9 @@ __global__ void gather_split5_f4_kernel(const uint16_t *__restrict__ x, int H, i
 #pragma unroll
     for (int q = 0; q < NP; q++) rt[q] = row_tile(e, NP * (r - offsets[e]) + q, tile_off, BN);
     const uint16_t *xr = x + (size_t)t * H;
-    const int b_end = min(H, (chunk + 1) * kGatherChunk);
-    for (int b0 = chunk * kGatherChunk; b0 < b_end; b0 += 256) {
-        const bool on = b0 + lane * 8 < b_end;
+    {
+        const int b0 = chunk * kChunk;
+        const bool on = b0 + lane * 8 < H;  // H is a multiple of 128: the upper half-warp may be off
         float v[8];
         if (on) {
             const uint4 u4 = *reinterpret_cast<const uint4 *>(xr + b0 + lane * 8);
@@ -492,12 +426,15 @@ __global__ void gather_split5_f4_kernel(const uint16_t *__restrict__ x, int H, i
             a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
             a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
             const int X = mx4_exp(a);
+            // 2^-X and 2^X as floats (exact scalings; 2^-127 for X = -127 is subnormal)
+            const float down = __uint_as_float((uint32_t)(127 - X) << 23);
+            const float up = X > -127 ? __uint_as_float((uint32_t)(X + 127) << 23) : 5.877471754e-39f;
             float sc[8];
 #pragma unroll
-            for (int i = 0; i < 8; i++) sc[i] = ldexpf(v[i], -X);
+            for (int i = 0; i < 8; i++) sc[i] = v[i] * down;
             const uint32_t c = e2m1x8_rn(sc);
 #pragma unroll
-            for (int i = 0; i < 8; i++) v[i] -= ldexpf(e2m1_nibble_value(c >> (4 * i)), X);
+            for (int i = 0; i < 8; i++) v[i] -= e2m1_nibble_value(c >> (4 * i)) * up;
             const uint32_t sb = (uint32_t)(X + 127);
             const uint32_t b1 = __shfl_down_sync(0xffffffffu, sb, 4);
             const uint32_t b2 = __shfl_down_sync(0xffffffffu, sb, 8);
@@ -731,8 +668,8 @@ cudaError_t launch_decode_multi(const PoolView &v, const uint16_t *x, int M, con
     }
     {
         TraceScope trace_scope("gather_split", st);
-        const int nchunk = (v.H + kGatherChunk - 1) / kGatherChunk;
-        gather_split5_f4_kernel<<<(P * nchunk * 32 + 255) / 256, 256, 0, st>>>(
+        const int nchunk5 = (v.H + 255) / 256;  // the five-part split takes one 256-element step per warp
+        gather_split5_f4_kernel<<<(P * nchunk5 * 32 + 255) / 256, 256, 0, st>>>(
             x, v.H, v.I, k, v.E, idx, d.perm, d.offsets, d.g.tile_off, d.g.BN, d.g.nsfb, d.g.xq, d.g.xs, d.g.hs);
     }
     cudaError_t e = launch_grouped_gemms(v, M, k, d.offsets, d.g, d.partial, MOE_PARTIAL_F32, stw, st, kDecodeParts,

@@ -17,13 +17,8 @@ constexpr int kMaxBN4 = 192;     // ... with MXFP4 activations
 // nparts = 1: 1.5 times the mean rows per expert rounded up to 32, 32..192 (an expert
 // with more rows takes several tiles; narrow tiles let the GEMMs run two CTAs per SM);
 // the same rule with MXFP4 activations (fp4).
-// nparts = 3: all of an expert's rows (at most 3T) in one tile, in whole groups of 16
-// pairs; nparts = 5: tiles of 16 pairs.
+// nparts = 5: tiles of 16 pairs.
 __host__ __device__ inline int grouped_bn(int P, int E, int T, int nparts, bool fp4 = false) {
-    if (nparts == 3) {
-        const int bn = (3 * T + 47) / 48 * 48;
-        return bn > kMaxBN ? 0 : bn;
-    }
     if (nparts == 5) return 80;  // five MXFP4 parts: one group of 16 pairs per tile (an expert
                                  // with more rows takes further tiles); one scale atom
     const int cap = fp4 ? kMaxBN4 : kMaxBN;
@@ -56,10 +51,9 @@ __host__ __device__ inline uint32_t sfb_stage_bytes(int nsfb) { return nsfb == 1
 
 // Activation rows of the grouped GEMMs.  nparts = 1: one MXFP8 row per pair (OCP
 // rule, the prefill path), or with fp4 one MXFP4 row (two E2M1 codes per byte,
-// element 2j in the low nibble: rows of H/2 and I/2 bytes).  nparts = 3: the value
-// is the sum of three E4M3 parts with their own E8M0 scales (see split_exp), which
-// represents a bf16 row exactly for elements within about 20 binades of their
-// 32-block's max (the multi-token decode path); row 3r+q holds part q of pair r.
+// element 2j in the low nibble: rows of H/2 and I/2 bytes).  nparts = 5: the value
+// is the sum of five MXFP4 parts, each with its own E8M0 scales (the multi-token
+// decode path); row 5r+q holds part q of pair r.
 struct GroupedWs {
     int *local_rank;  // [P]
     int *cnt;         // [nblocks][E]
@@ -105,8 +99,8 @@ __host__ __device__ inline GroupedWs grouped_ws_layout(void *ws, int E, int H, i
     return g;
 }
 
-// The multi-token decode through the grouped GEMMs: the grouped workspace with three
-// activation parts, then the sort's outputs and the fp32 expert output rows.
+// The multi-token decode through the grouped GEMMs: the grouped workspace with five
+// MXFP4 activation parts, then the sort's outputs and the fp32 expert output rows.
 struct DecodeMultiWs {
     GroupedWs g;
     int32_t *perm;      // [P]
@@ -145,16 +139,6 @@ __device__ __forceinline__ float e2m1_nibble_value(uint32_t nib) {
     return (nib & 8u) ? -mag : mag;
 }
 
-// E8M0 exponent of one E4M3 part of a 32-element block with max |v| = amax: the
-// block's largest value scales into [128, 256), below E4M3's 448, so nothing
-// saturates and the part is v rounded (RNE) to E4M3 precision.
-__device__ __forceinline__ int split_exp(float amax) {
-    if (!(amax > 0.f) || !isfinite(amax)) return -127;
-    int ex;
-    frexpf(amax, &ex);  // amax in [2^(ex-1), 2^ex)
-    return max(-127, min(127, ex - 1 - 7));
-}
-
 // Eight values -> eight E2M1 codes (round to nearest even, saturating at +-6), two
 // per byte with element 2j in the low nibble: bytes 0..3 of the result.
 __device__ __forceinline__ uint32_t e2m1x8_rn(const float (&f)[8]) {
@@ -181,34 +165,14 @@ __device__ __forceinline__ uint8_t e2m1x2_rn(float lo, float hi) {
     return (uint8_t)(r & 0xFFu);
 }
 
-__device__ __forceinline__ uint8_t e4m3_rn(float v) {
-    unsigned short pair;
-    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(pair) : "f"(0.f), "f"(v));
-    return (uint8_t)(pair & 0xFF);
-}
-
-__device__ __forceinline__ float e4m3_value(uint8_t q) {
-    unsigned int h2;
-    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"((unsigned short)q));
-    return __half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFFu)));
-}
-
-// One part of the split: the E4M3 code of r at exponent X, and r less what the
-// code represents (exact in fp32: the code keeps the leading bits of r).
-__device__ __forceinline__ uint8_t split_part(float &r, int X) {
-    const uint8_t q = e4m3_rn(ldexpf(r, -X));
-    r -= ldexpf(e4m3_value(q), X);
-    return q;
-}
-
-// The two grouped block-scaled GEMMs (gate/up with SwiGLU and MXFP8 epilogue,
-// then down), over the sorted rows.
+// The two grouped block-scaled GEMMs (gate/up with SwiGLU and the MX quantisation of
+// h, then down), over the sorted rows.
 cudaError_t launch_grouped_gemms(const PoolView &v, int T, int k, const int32_t *offsets, const GroupedWs &g,
                                  void *partial, int partial_dtype, StatusWord *st, cudaStream_t stream,
                                  int nparts = 1, bool fp4 = false);
 
-// Multi-token decode (M > 1) through the grouped GEMMs with three-part activations;
-// cudaErrorNotSupported for shapes the GEMMs do not take.
+// Multi-token decode (M > 1) through the grouped GEMMs with five-part MXFP4
+// activations; cudaErrorNotSupported for shapes the GEMMs do not take.
 cudaError_t launch_decode_multi(const PoolView &v, const uint16_t *x, int M, const int32_t *idx, const float *w, int k,
                                 const uint16_t *residual, uint16_t *y, void *ws, cudaStream_t st);
 size_t decode_multi_workspace_bytes(int E, int H, int I, int M, int k);
