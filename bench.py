@@ -351,7 +351,8 @@ def measure_streamed(moe, torch, pool0, dev, ntok=48, warm=16, L=8, slots=128):
     cache.  Reports layer-tokens/s, the cache hit rate and the copy rate."""
     s = synth.FULL
     rec = moe.moe_pool_record_bytes(s.H, s.I)
-    host = torch.empty(s.E * rec, dtype=torch.uint8).pin_memory()
+    hb = moe.HostBuffer(s.E * rec, dev)  # pinned, on the GPU's own host NUMA node
+    host = hb.tensor
     host.copy_(pool0.mem)
     sps = [moe.StreamPool(host, s.E, s.H, s.I, slots, device=dev) for _ in range(L)]
     Wrs = [torch.from_numpy(synth.router_bf16(synth.router_seed(l), s.E, s.H).view(np.int16)).to(dev)
@@ -396,11 +397,15 @@ def measure_streamed(moe, torch, pool0, dev, ntok=48, warm=16, L=8, slots=128):
     hits = sum(b[0] - a[0] for a, b in zip(st0, st1))
     misses = sum(b[1] - a[1] for a, b in zip(st0, st1))
     copied = sum(b[2] - a[2] for a, b in zip(st0, st1))
+    node = hb.numa_node
     del sps, host
+    hb.close()
     return {"tokens": ntok, "layers": L, "slots_per_layer": slots, "slot_fraction": slots / s.E,
+            "host_numa_node": node, "gpu_host_numa_node": moe.moe_host_numa_node(dev),
             "layer_tokens_per_s": ntok * L / sec, "us_per_layer_token": sec * 1e6 / (ntok * L),
             "hit_rate": hits / max(hits + misses, 1), "misses_per_layer_token": misses / (ntok * L),
-            "copy_gbs": copied / sec / 1e9, "note": "one pinned host copy of the pool shared by the layers"}
+            "copy_gbs": copied / sec / 1e9,
+            "note": "one pinned host copy of the pool, on the GPU's own NUMA node, shared by the layers"}
 
 
 def run_ours(args):

@@ -145,6 +145,22 @@ moe_status moe_stream_pool_map(moe_stream_pool *sp, const int32_t *idx_host, int
  * copied (misses), and the bytes copied. */
 moe_status moe_stream_pool_stats(const moe_stream_pool *sp, uint64_t *hits, uint64_t *misses, uint64_t *bytes);
 
+/* Pinned host memory for the records, placed on the host NUMA node closest to GPU
+ * `device` (cudaDevAttrHostNumaId).  On a Grace host each CPU die is a NUMA node and
+ * the GPU's copy engines read their own die's memory over NVLink-C2C, the other
+ * die's only through the CPU-to-CPU link, several times slower; ordinary pinned
+ * memory lands on the node of whichever CPU the allocating thread runs on.
+ * *out: page-aligned, `bytes` rounded up to whole pages, readable and writable by
+ * the host and registered with CUDA (cudaHostRegister).  *numa_node (may be NULL):
+ * the node the first page actually lies on, -1 if unknown (placement is a
+ * preference: a full node falls back to another).  MOE_ERR_CUDA if the registration
+ * fails; free with moe_host_free(p, bytes) using the same `bytes`. */
+moe_status moe_host_alloc(int device, size_t bytes, void **out, int *numa_node);
+moe_status moe_host_free(void *p, size_t bytes);
+
+/* The host NUMA node closest to GPU `device`, or -1 (no NUMA, or unknown). */
+int moe_host_numa_node(int device);
+
 /* ------------------------------------------------------------- workspace */
 
 /* Workspace bytes of operation `op` (MOE_OP_*) for M (decode) or T (prefill)

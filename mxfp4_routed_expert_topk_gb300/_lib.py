@@ -37,7 +37,7 @@ EXPORTED = [
     "moe_expert_forward_grouped", "moe_grouped_read_h", "moe_combine", "moe_trace_begin", "moe_trace_end",
     "moe_debug_set_wait_limit", "moe_debug_set_barrier_extra",
     "moe_stream_pool_create", "moe_stream_pool_destroy", "moe_stream_pool_cache", "moe_stream_pool_slots",
-    "moe_stream_pool_map", "moe_stream_pool_stats",
+    "moe_stream_pool_map", "moe_stream_pool_stats", "moe_host_alloc", "moe_host_free", "moe_host_numa_node",
 ]
 
 
@@ -86,6 +86,9 @@ def lib() -> ctypes.CDLL:
             "moe_stream_pool_slots": (_i, [_vp]),
             "moe_stream_pool_map": (_i, [_vp, _vp, _i, _vp, _vp]),
             "moe_stream_pool_stats": (_i, [_vp, ctypes.POINTER(_u64), ctypes.POINTER(_u64), ctypes.POINTER(_u64)]),
+            "moe_host_alloc": (_i, [_i, _sz, ctypes.POINTER(_vp), ctypes.POINTER(_i)]),
+            "moe_host_free": (_i, [_vp, _sz]),
+            "moe_host_numa_node": (_i, [_i]),
             "moe_debug_set_barrier_extra": (_i, [_i]),
             "moe_trace_begin": (_i, [ctypes.c_char_p]),
             "moe_trace_end": (_i, [ctypes.POINTER(_i), ctypes.POINTER(ctypes.c_double)]),
@@ -396,6 +399,42 @@ class StreamPool:
         if h is not None and _lib is not None:
             _lib.moe_stream_pool_destroy(h)
             self.handle = None
+
+
+class HostBuffer:
+    """`nbytes` of pinned host memory on the NUMA node closest to `device`
+    (moe_host_alloc); `tensor` is a CPU uint8 view of it, `numa_node` the node its
+    first page lies on (-1 if unknown).  Freed by close() or when collected; the
+    tensor must not be used after that."""
+
+    def __init__(self, nbytes: int, device=None):
+        dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+        self.nbytes = int(nbytes)
+        p, node = _vp(), _i()
+        _check(lib().moe_host_alloc(dev.index or 0, self.nbytes, ctypes.byref(p), ctypes.byref(node)),
+               "moe_host_alloc")
+        self._p = p
+        self.numa_node = int(node.value)
+        arr = (ctypes.c_uint8 * self.nbytes).from_address(p.value)
+        self.tensor = torch.frombuffer(arr, dtype=torch.uint8)
+
+    def close(self):
+        if getattr(self, "_p", None) is not None and _lib is not None:
+            self.tensor = None
+            _check(_lib.moe_host_free(self._p, self.nbytes), "moe_host_free")
+            self._p = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except MoeError:
+            pass
+
+
+def moe_host_numa_node(device=None) -> int:
+    """The host NUMA node closest to `device` (-1: no NUMA or unknown)."""
+    dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+    return int(lib().moe_host_numa_node(dev.index or 0))
 
 
 # ---------------------------------------------------------- test support

@@ -8,9 +8,13 @@
 // in place of expert indices.
 //
 // Host code only: a least-recently-used slot map with the slots of the current call
-// pinned.
+// pinned, and the allocation of the host records on the GPU's own NUMA node.
+#include <linux/mempolicy.h>
 #include <stdlib.h>
 #include <string.h>
+#include <sys/mman.h>
+#include <sys/syscall.h>
+#include <unistd.h>
 
 #include <new>
 #include <vector>
@@ -132,6 +136,69 @@ moe_status moe_stream_pool_map(moe_stream_pool *sp, const int32_t *idx_host, int
         slot_host[i] = s;
     }
     return MOE_OK;
+}
+
+// A Grace host has one NUMA node per CPU die, and a GPU's copy engines reach the
+// memory of their own die over NVLink-C2C but the other die's only through the
+// CPU-to-CPU link, several times slower.  The pages are given a preferred node
+// before they exist (mbind on the fresh mapping), then faulted in and pinned by
+// cudaHostRegister; MPOL_PREFERRED rather than MPOL_BIND, so that a full node falls
+// back to another instead of failing the allocation.
+static size_t host_map_len(size_t bytes) {
+    const long pg = sysconf(_SC_PAGESIZE);
+    const size_t page = pg > 0 ? (size_t)pg : 4096;
+    return (bytes + page - 1) / page * page;
+}
+
+moe_status moe_host_alloc(int device, size_t bytes, void **out, int *numa_node) {
+    if (out == nullptr || bytes == 0) return MOE_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (numa_node != nullptr) *numa_node = -1;
+    int want = -1;
+    if (cudaDeviceGetAttribute(&want, cudaDevAttrHostNumaId, device) != cudaSuccess) {
+        (void)cudaGetLastError();
+        want = -1;
+    }
+    const size_t len = host_map_len(bytes);
+    void *p = mmap(nullptr, len, PROT_READ | PROT_WRITE, MAP_PRIVATE | MAP_ANONYMOUS, -1, 0);
+    if (p == MAP_FAILED) return MOE_ERR_INVALID_ARG;
+    constexpr int kMaskBits = 1024;
+    if (want >= 0 && want < kMaskBits) {
+        unsigned long mask[kMaskBits / (8 * sizeof(unsigned long))] = {};
+        mask[(size_t)want / (8 * sizeof(unsigned long))] |= 1ul << ((size_t)want % (8 * sizeof(unsigned long)));
+        // failure (a node outside this process's cpuset) leaves the kernel's default
+        (void)syscall(SYS_mbind, p, len, (unsigned long)MPOL_PREFERRED, mask, (unsigned long)kMaskBits + 1, 0ul);
+    }
+    if (cudaHostRegister(p, len, cudaHostRegisterDefault) != cudaSuccess) {
+        (void)cudaGetLastError();
+        munmap(p, len);
+        return MOE_ERR_CUDA;
+    }
+    if (numa_node != nullptr) {
+        int node = -1;
+        if (syscall(SYS_get_mempolicy, &node, nullptr, 0ul, p, (unsigned long)(MPOL_F_NODE | MPOL_F_ADDR)) == 0)
+            *numa_node = node;
+    }
+    *out = p;
+    return MOE_OK;
+}
+
+moe_status moe_host_free(void *p, size_t bytes) {
+    if (p == nullptr) return MOE_OK;
+    if (bytes == 0) return MOE_ERR_INVALID_ARG;
+    const cudaError_t e = cudaHostUnregister(p);
+    if (e != cudaSuccess) (void)cudaGetLastError();
+    munmap(p, host_map_len(bytes));
+    return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+int moe_host_numa_node(int device) {
+    int n = -1;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrHostNumaId, device) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return -1;
+    }
+    return n;
 }
 
 moe_status moe_stream_pool_stats(const moe_stream_pool *sp, uint64_t *hits, uint64_t *misses, uint64_t *bytes) {

@@ -27,7 +27,8 @@ def test_streamed_decode_matches_resident(shape, slots, ntok):
     pool = moe.Pool(s.E, s.H, s.I)
     moe.moe_pool_fill_synthetic(pool, synth.pool_seed(3))
     rec = moe.moe_pool_record_bytes(s.H, s.I)
-    host = torch.empty(s.E * rec, dtype=torch.uint8).pin_memory()
+    hb = moe.HostBuffer(s.E * rec)
+    host = hb.tensor
     host.copy_(pool.mem)
     torch.cuda.synchronize()
     sp = moe.StreamPool(host, s.E, s.H, s.I, slots)
@@ -49,3 +50,22 @@ def test_streamed_decode_matches_resident(shape, slots, ntok):
     assert torch.equal(y.view(torch.int16), y_ref.view(torch.int16))
     hits, misses, nbytes = sp.stats()
     assert hits > 0 and misses > slots and nbytes == misses * rec   # it evicted and refetched
+
+
+def test_host_alloc_near_gpu():
+    """moe_host_alloc: page-rounded pinned memory that host and device both reach, on
+    the GPU's own host NUMA node when the system reports one."""
+    want = moe.moe_host_numa_node()
+    nbytes = (64 << 20) + 3
+    hb = moe.HostBuffer(nbytes)
+    if want >= 0:
+        assert hb.numa_node == want
+    pat = torch.arange(nbytes, dtype=torch.int64).remainder_(251).to(torch.uint8)
+    hb.tensor.copy_(pat)
+    d = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    d.copy_(hb.tensor, non_blocking=True)
+    back = torch.empty(nbytes, dtype=torch.uint8)
+    back.copy_(d)
+    assert torch.equal(back, pat)
+    hb.close()
+    hb.close()  # a second close is a no-op
