@@ -235,10 +235,12 @@ moe_status moe_route_topk_prescaled(const uint16_t *x, int M, int H, const uint1
  * fp32 accumulation, rounded to nearest-even.  ws: MOE_OP_DECODE bytes.
  * M = 1 runs on the CUDA cores (E2M1 -> f16 dequantisation, f16 products summed
  * per 32-element block, then fp32).  M > 1 runs on the tensor cores when I is a
- * multiple of 64: each activation block is written as the sum of three E4M3
- * parts with their own E8M0 scales (exact for bf16 elements within about 20
- * binades of their block's max), multiplied with the E2M1 weights in
- * block-scaled MMAs with fp32 accumulation; h is split the same way for W_d. */
+ * multiple of 64: each 32-element block of a row is written as the sum of five
+ * MXFP4 parts (each the OCP rule applied to what the earlier parts left; the
+ * block's largest remainder shrinks at least threefold per part), multiplied with
+ * the E2M1 weights in kind::mxf4 block-scaled MMAs with fp32 accumulation; h is
+ * split the same way for W_d.  What the five parts leave out is below 3^-5 of each
+ * block's max |value| (about 3e-4 of RMS on the outputs of full-size layers). */
 moe_status moe_expert_forward_decode(const moe_pool *pool, const uint16_t *x, int M,
                                      const int32_t *idx, const float *w, int k,
                                      const uint16_t *residual, uint16_t *y,
