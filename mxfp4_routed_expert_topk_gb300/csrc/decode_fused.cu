@@ -347,7 +347,9 @@ __global__ void __launch_bounds__(kThreadsF, 1) decode_fused_kernel(const FusedA
         if (ok && valid && half == 0 && lane == 0) {
             const float2 lo = ps[item * 2], hi = ps[item * 2 + 1];
             const float gv = ldexpf(lo.x + hi.x, sx), uv = ldexpf(lo.y + hi.y, sx);
-            const float hval = gv / (1.f + expf(-gv)) * uv;
+            // fast exponential and division (a few ulp): the accurate forms cost this
+            // lane's warp, and the warp pair waiting for it, about 15 % of a stage
+            const float hval = __fdividef(gv, 1.f + __expf(-gv)) * uv;
             a.h[h_slot(p, i, nkbd)] = hval;
             atomicMax(&samax[p], __float_as_uint(fabsf(hval)));
         }
