@@ -43,7 +43,6 @@ struct FusedArgs {
     const uint16_t *residual;
     uint16_t *y;
     float *h;            // [k][8][I/32] float4 workspace (see h_slot)
-    float *hmax;         // [kMaxKF][G] workspace: each CTA's max |h| per pair
     StatusWord *st;      // grid barrier and exit counters
     unsigned int barrier_count;  // arrivals the grid barrier waits for: G (more only under
                                  // moe_debug_set_barrier_extra, to make the wait run out)
@@ -117,9 +116,6 @@ __global__ void __launch_bounds__(kThreadsF, 1) decode_fused_kernel(const FusedA
     float2 *pairsum = reinterpret_cast<float2 *>(tail + a.tail_bytes);  // [2][kItems][2] half sums
     int *sidx = reinterpret_cast<int *>(pairsum + 2 * kItems * 2);      // [kMaxKF]
     int *abort_flag = sidx + kMaxKF;
-    unsigned int *samax = reinterpret_cast<unsigned int *>(abort_flag + 1);  // [kMaxKF] max |h| per pair
-    int *s_sp = reinterpret_cast<int *>(samax + kMaxKF);                     // [kMaxKF] h scale exponent per pair
-    float *s_wsc = reinterpret_cast<float *>(s_sp + kMaxKF);                 // [kMaxKF] w_p * 2^sp
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int b = blockIdx.x, G = a.G, k = a.k;
     // I % 32 == 0: a unit of 8 items never straddles a pair or a 16-row group
@@ -143,7 +139,6 @@ __global__ void __launch_bounds__(kThreadsF, 1) decode_fused_kernel(const FusedA
     // launched early (programmatic dependent launch): nothing global is read before the
     // previous kernel of the stream (typically the router) has completed
     griddep_wait();
-    if (threadIdx.x < kMaxKF) samax[threadIdx.x] = 0u;
     if (threadIdx.x < k) {
         const int e = a.idx[threadIdx.x];
         const bool ok = e >= 0 && e < v.E;
@@ -351,12 +346,8 @@ __global__ void __launch_bounds__(kThreadsF, 1) decode_fused_kernel(const FusedA
             // lane's warp, and the warp pair waiting for it, about 15 % of a stage
             const float hval = __fdividef(gv, 1.f + __expf(-gv)) * uv;
             a.h[h_slot(p, i, nkbd)] = hval;
-            atomicMax(&samax[p], __float_as_uint(fabsf(hval)));
         }
     }
-    // this CTA's max |h| per pair (plain stores: one column of the [pair][CTA] table)
-    named_barrier(1, kCW * 32);
-    if (threadIdx.x < kMaxKF) a.hmax[threadIdx.x * G + b] = __uint_as_float(samax[threadIdx.x]);
     // every consumer warp takes part, aborted or not, so the named barriers match
     ok = grid_barrier(&a.st->pad[kStGridBarrier], a.barrier_count, 1, kCW * 32, a.st, 0x300u, abort_flag);
     // phase B remains: the next kernel of the stream (the next router) may launch; it
@@ -364,8 +355,8 @@ __global__ void __launch_bounds__(kThreadsF, 1) decode_fused_kernel(const FusedA
     if (threadIdx.x == 0) griddep_launch_dependents();
 
     // ---- phase B: each lane owns up to two (pair, 32-block) combinations of h, in
-    // registers as f16 scaled by a per-pair power of two (from the max |h| of the
-    // pair gathered in phase A), and for every output row of a stage adds
+    // registers as f16 scaled by a power of two per combination (from the max |h| of
+    // its 32 elements), and for every output row of a stage adds
     //   w_pair * (W_d,pair row block . h block) * scale
     // for each.  Combination 0: pair = warp, block = lane (blocks 0..31).
     // Combination 1: the tail blocks 32..I/32-1 of every pair, packed densely into
@@ -395,39 +386,28 @@ __global__ void __launch_bounds__(kThreadsF, 1) decode_fused_kernel(const FusedA
             }
         }
     }
-    // warp p: max |h| of pair p over its row of the [pair][CTA] table, then the
-    // pair's f16 scale exponent and scaled routing weight for all warps
-    {
-        if (ok && warp < k) {
-            float ha = 0.f;
-            for (int c = lane; c < G; c += 32) ha = fmaxf(ha, __ldcg(a.hmax + warp * G + c));
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) ha = fmaxf(ha, __shfl_xor_sync(0xffffffffu, ha, off));
-            int sp = 0;
-            if (ha > 0.f && isfinite(ha)) {
-                int ex;
-                frexpf(ha, &ex);
-                sp = ex - 1 - 7;
-            }
-            if (lane == 0) {
-                s_sp[warp] = sp;
-                s_wsc[warp] = sidx[warp] >= 0 ? ldexpf(__ldg(a.w + warp), sp) : 0.f;
-            }
-        }
-    }
-    named_barrier(1, kCW * 32);  // every consumer warp, aborted or not
     if (ok) {
 #pragma unroll
         for (int u = 0; u < 2; u++) {
-            const int sp = pv[u] ? s_sp[pb[u]] : 0;
-            if (pv[u]) wsc[u] = s_wsc[pb[u]];
+            float hm = 0.f;
+#pragma unroll
+            for (int q = 0; q < 4; q++)
+#pragma unroll
+                for (int h2 = 0; h2 < 2; h2++) {
+                    const float4 f = hv[u][q][h2];
+                    hm = fmaxf(hm, fmaxf(fmaxf(fabsf(f.x), fabsf(f.y)), fmaxf(fabsf(f.z), fabsf(f.w))));
+                }
+            // max |h 2^-sp| in [128, 256); sp in [-126, 120], so 2^-sp and 2^sp are
+            // normal floats and the scaling is exact
+            int sp = 0;
+            if (hm > 0.f && isfinite(hm)) sp = max((int)((__float_as_uint(hm) >> 23) & 0xffu) - 127 - 7, -126);
+            const float dn = __uint_as_float((uint32_t)(127 - sp) << 23);
+            if (pv[u]) wsc[u] = __ldg(a.w + pb[u]) * __uint_as_float((uint32_t)(127 + sp) << 23);
 #pragma unroll
             for (int q = 0; q < 4; q++) {
                 const float4 f0 = hv[u][q][0], f1 = hv[u][q][1];
-                hr[u][q] = make_uint4(pack_half2(mul_pow2(f0.x, -sp), mul_pow2(f0.y, -sp)),
-                                      pack_half2(mul_pow2(f0.z, -sp), mul_pow2(f0.w, -sp)),
-                                      pack_half2(mul_pow2(f1.x, -sp), mul_pow2(f1.y, -sp)),
-                                      pack_half2(mul_pow2(f1.z, -sp), mul_pow2(f1.w, -sp)));
+                hr[u][q] = make_uint4(pack_half2(f0.x * dn, f0.y * dn), pack_half2(f0.z * dn, f0.w * dn),
+                                      pack_half2(f1.x * dn, f1.y * dn), pack_half2(f1.z * dn, f1.w * dn));
             }
         }
         // the preloaded scale rows (one wait per launch)
@@ -525,7 +505,6 @@ cudaError_t launch_decode_fused(const PoolView &v, const uint16_t *x, const int3
     fa.residual = residual;
     fa.y = y;
     fa.h = reinterpret_cast<float *>((char *)ws + 256);
-    fa.hmax = reinterpret_cast<float *>((char *)ws + 256 + align_up((size_t)k * v.I * sizeof(float), 256));
     fa.st = reinterpret_cast<StatusWord *>(ws);
     const uint32_t slotA = (uint32_t)(2 * kItems * (v.ld_gu + v.lds_gu));
     // phase-B stage: R rows of W_d per pair plus a 16-byte aligned span of their scale rows
@@ -539,7 +518,7 @@ cudaError_t launch_decode_fused(const PoolView &v, const uint16_t *x, const int3
     fa.slot_bytes = (slot_need + 127) / 128 * 128;
     // everything but the token / preloaded-scale region
     const size_t head = (size_t)kSlots * fa.slot_bytes + 8 * sizeof(uint64_t) + (size_t)kCW * kMaxRowsCta * sizeof(float) +
-                        2 * kItems * 2 * sizeof(float2) + (4 * kMaxKF + 4) * sizeof(int);
+                        2 * kItems * 2 * sizeof(float2) + (kMaxKF + 4) * sizeof(int);
     // the W_d scale rows of a CTA's output rows (at most ceil(H / SMs) of them), one
     // 16-byte aligned span per pair, if they fit in shared memory
     const int rows_max = (v.H + sms - 1) / sms;

@@ -199,11 +199,9 @@ cudaError_t launch_route(const uint16_t *x, int M, int H, const uint16_t *Wr, in
 
 size_t decode_workspace_bytes(int E, int H, int I, int M, int k);
 // The single-token fused decode runs at most this many CTAs; its workspace holds
-// h [k][I] and a [16][grid] table of per-CTA max |h| after the status word.
+// h [k][I] after the status word.
 constexpr int kMaxFusedGrid = 1024;
-inline size_t decode_fused_workspace_bytes(int I, int k) {
-    return 256 + align_up((size_t)k * I * sizeof(float), 256) + (size_t)16 * kMaxFusedGrid * sizeof(float);
-}
+inline size_t decode_fused_workspace_bytes(int I, int k) { return 256 + align_up((size_t)k * I * sizeof(float), 256); }
 cudaError_t launch_decode(const PoolView &v, const uint16_t *x, int M, const int32_t *idx, const float *w,
                           int k, const uint16_t *residual, uint16_t *y, void *ws, cudaStream_t st);
 
