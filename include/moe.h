@@ -44,7 +44,8 @@ typedef enum {
     MOE_ERR_UNSUPPORTED_SHAPE = 2, /* shape outside the supported set above */
     MOE_ERR_WORKSPACE = 3,         /* ws smaller than moe_workspace_size() */
     MOE_ERR_CUDA = 4,              /* a CUDA runtime call or launch failed */
-    MOE_ERR_BAD_INDEX = 5,         /* device: an expert index outside [0, E) */
+    MOE_ERR_BAD_INDEX = 5,         /* device: an expert index outside [0, E), or named too
+                                      often in one multi-row decode call */
     MOE_ERR_TIMEOUT = 6,           /* device: a bounded wait gave up */
     MOE_ERR_NONFINITE = 7          /* device: non-finite router input or logit */
 } moe_status;
@@ -240,7 +241,12 @@ moe_status moe_route_topk_prescaled(const uint16_t *x, int M, int H, const uint1
  * block's largest remainder shrinks at least threefold per part), multiplied with
  * the E2M1 weights in kind::mxf4 block-scaled MMAs with fp32 accumulation; h is
  * split the same way for W_d.  What the five parts leave out is below 3^-5 of each
- * block's max |value| (about 3e-4 of RMS on the outputs of full-size layers). */
+ * block's max |value| (about 3e-4 of RMS on the outputs of full-size layers).
+ * On that path the k indices of each row should be distinct (moe_route_topk gives
+ * them so): for M <= 15 the GEMM stages reserve room for ceil16(5 M) activation
+ * rows per expert, and an expert named more than ceil16(5 M) / 5 times in all is
+ * reported as MOE_ERR_BAD_INDEX (y is then not valid).  A row may repeat an index
+ * as long as no expert exceeds that count. */
 moe_status moe_expert_forward_decode(const moe_pool *pool, const uint16_t *x, int M,
                                      const int32_t *idx, const float *w, int k,
                                      const uint16_t *residual, uint16_t *y,

@@ -74,6 +74,8 @@ struct GemmArgs {
     int BN;              // columns of the accumulator tile (multiple of 16)
     int bbox;            // rows per tensor copy of B: BN (one copy per stage), or 16 (as many
                          // copies as the tile's MMA width needs: narrow tiles)
+    int bsr;             // B rows reserved per pipeline stage in shared memory: BN, or fewer
+                         // (a multiple of 16, with bbox = 16) when no tile has more columns
     int nsfb;            // 512-byte scale atoms of B per K tile = ceil(BN / 128)
     int ns;              // pipeline stages
     int nmt;             // 128-row tiles of A per expert
@@ -89,7 +91,7 @@ struct GemmArgs {
     int nkt_h;           // Ip / 128
     void *partial;       // [P][H]
     int partial_dtype;
-    int nparts;          // activation rows per pair (1, or 3 for the exact split)
+    int nparts;          // activation rows per pair (1, or 5: the MXFP4 parts of the multi-token decode)
     StatusWord *st;
 };
 
@@ -425,13 +427,13 @@ __device__ __forceinline__ void epilogue_mx1(const GemmArgs &a, uint32_t lane_ba
 // With FP4 rows a stage holds the scale factors of two 128-K tiles (K = 256).
 struct GemmSmemLayout {
     uint32_t a, b, sfa, sfb, bars, misc, total, sfa_stage, sfb_stage;
-    __host__ __device__ GemmSmemLayout(int BN, int ns, int tpi, bool fp4 = false) {
+    __host__ __device__ GemmSmemLayout(int BN, int ns, int tpi, bool fp4, int bsr) {
         const uint32_t nsfb = (uint32_t)((BN + 127) / 128);
         sfa_stage = (uint32_t)tpi * (fp4 ? 1024u : 512u);
         sfb_stage = fp4 ? 2u * sfb_stage_bytes((int)nsfb) : sfb_stage_bytes((int)nsfb);
         a = 0;                                            // ns x tpi x 16 KB (1024-aligned)
-        b = a + (uint32_t)(ns * tpi) * kTileM * kTileK;   // ns x BN*128
-        sfa = b + (uint32_t)ns * (uint32_t)BN * kTileK;   // ns x sfa_stage
+        b = a + (uint32_t)(ns * tpi) * kTileM * kTileK;   // ns x bsr*128
+        sfa = b + (uint32_t)ns * (uint32_t)bsr * kTileK;  // ns x sfa_stage
         sfb = sfa + (uint32_t)ns * sfa_stage;             // ns x sfb_stage
         bars = sfb + (uint32_t)ns * sfb_stage;            // full[], empty[], acc_full[2], acc_empty[2], mma_done
         misc = bars + (2 * kMaxStages + 5) * 8;           // tmem addr, abort, amax[4][16]
@@ -465,7 +467,9 @@ struct JobIter {
     __device__ bool valid() const { return i < nu * ((a.nmt + a.tpi - 1) / a.tpi) && ntile > 0; }
     __device__ int n0() const { return nt * a.BN; }
     __device__ int tile() const { return tile0 + nt; }
-    __device__ int nn() const { return min(a.BN, nrows - nt * a.BN); }
+    // columns of the current tile (at most bsr: a tile with more is reported by the
+    // sort as a bad index and computed only in part)
+    __device__ int nn() const { return min(a.bsr, nrows - nt * a.BN); }
     __device__ void next() {
         if (++nt >= ntile) {
             i += (int)gridDim.x;
@@ -483,7 +487,7 @@ __global__ void __launch_bounds__(NT, GemmShape<NT>::kCtasPerSm)
     unsigned char *smem = (unsigned char *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     const int ns = a.ns;
     const int tpi = a.tpi;
-    const GemmSmemLayout L(a.BN, ns, tpi, FP4);
+    const GemmSmemLayout L(a.BN, ns, tpi, FP4, a.bsr);
     uint8_t *sA = smem + L.a, *sB = smem + L.b, *sSFA = smem + L.sfa, *sSFB = smem + L.sfb;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.bars);
     uint64_t *empty = full + kMaxStages;
@@ -574,7 +578,7 @@ __global__ void __launch_bounds__(NT, GemmShape<NT>::kCtasPerSm)
                         mbar_arrive_expect_tx(&full[s], tx);
                         tma_load_3d(sA + (size_t)s * kTileM * kTileK, &tmA, kt * kTileK, J.mt * kTileM, J.e, &full[s]);
                         for (int c = 0; c < brows; c += a.bbox)
-                            tma_load_2d(sB + (size_t)s * a.BN * kTileK + (size_t)c * kTileK, &tmB, kt * kTileK,
+                            tma_load_2d(sB + (size_t)s * a.bsr * kTileK + (size_t)c * kTileK, &tmB, kt * kTileK,
                                         brow + c, &full[s]);
                         for (int j = 0; j < n2; j++)  // the two K tiles' A blocks are nmt blocks apart
                             bulk_g2s_l2(sSFA + (size_t)s * 1024 + 512 * j, sfa_src + (size_t)j * a.nmt * 512, 512u,
@@ -601,7 +605,7 @@ __global__ void __launch_bounds__(NT, GemmShape<NT>::kCtasPerSm)
                         tma_load_3d(sA + (size_t)s * tpi * kTileM * kTileK, &tmA, kt * kTileK, J.mt * kTileM, J.e,
                                     &full[s]);
                         for (int c = 0; c < brows; c += a.bbox)
-                            tma_load_2d(sB + (size_t)s * a.BN * kTileK + (size_t)c * kTileK, &tmB, kt * kTileK,
+                            tma_load_2d(sB + (size_t)s * a.bsr * kTileK + (size_t)c * kTileK, &tmB, kt * kTileK,
                                         brow + c, &full[s]);
                         bulk_g2s_l2(sSFA + (size_t)s * tpi * 512, sfa_src, a_tiles * 512u, &full[s]);
                         if (nsfb == 1) {
@@ -633,7 +637,7 @@ __global__ void __launch_bounds__(NT, GemmShape<NT>::kCtasPerSm)
         // Descriptors of slot 0, built once: a stage's descriptors add the stage's
         // offset in 16-byte units to the start-address field (shared addresses stay
         // below 2^18, so the 14-bit field never carries into the next one).
-        const uint32_t a_stage16 = (uint32_t)(tpi * kTileM * kTileK) >> 4, b_stage16 = (uint32_t)(a.BN * kTileK) >> 4;
+        const uint32_t a_stage16 = (uint32_t)(tpi * kTileM * kTileK) >> 4, b_stage16 = (uint32_t)(a.bsr * kTileK) >> 4;
         const uint32_t sfa_stage16 = L.sfa_stage >> 4, sfb_stage16 = L.sfb_stage >> 4;
         const uint64_t adesc0 = smem_desc(smem_u32(sA), 16, 1024, kSwizzle128B);
         const uint64_t bdesc0 = smem_desc(smem_u32(sB), 16, 1024, kSwizzle128B);
@@ -887,7 +891,7 @@ cudaError_t launch_one(GemmArgs ga, const uint8_t *a_base, int a_k, int a_rows, 
     // as many pipeline stages as fit the CTA's share of shared memory and TMEM
     int ns = kMaxStages;
     auto tmem_need = [&](int n) { return (uint32_t)(nacc * tpi * BN) + (uint32_t)n * sf_cols; };
-    auto smem_need = [&](int n) { return GemmSmemLayout(BN, n, tpi, fp4).total + 1024; };  // + alignment slack
+    auto smem_need = [&](int n) { return GemmSmemLayout(BN, n, tpi, fp4, ga.bsr).total + 1024; };  // + alignment slack
     while (ns > 2 && (smem_need(ns) > smem_cap || tmem_need(ns) > tmem_cap)) ns--;
     const uint32_t tmem_cols = pow2_at_least(tmem_need(ns));
     if (tmem_cols > tmem_cap || smem_need(ns) > smem_cap) return cudaErrorNotSupported;
@@ -906,6 +910,7 @@ cudaError_t launch_one(GemmArgs ga, const uint8_t *a_base, int a_k, int a_rows, 
     // tiles (several parts per row) hold a few rows in a box sized for 32, and prefill
     // tiles up to 64 columns are sized for the expert rows' spread
     ga.bbox = (ga.nparts > 1 || BN <= 64) ? 16 : BN;
+    if (ga.bsr != BN && ga.bbox != 16) return cudaErrorInvalidValue;
     ga.tmem_cols = tmem_cols;
     ga.nkt_sf = a_k / kTileK;
     ga.nkt = fp4 ? (ga.nkt_sf + 1) / 2 : ga.nkt_sf;
@@ -939,7 +944,7 @@ cudaError_t set_wait_limit_gemm(uint64_t ns) { return set_wait_limit_here(ns); }
 
 cudaError_t launch_grouped_gemms(const PoolView &v, int T, int k, const int32_t *offsets, const GroupedWs &g,
                                  void *partial, int partial_dtype, StatusWord *st, cudaStream_t stream, int nparts,
-                                 bool fp4) {
+                                 bool fp4, int max_cols) {
     const int P = T * k;
     if (P == 0) return cudaSuccess;
     // one MXFP8 or MXFP4 row per pair, or five MXFP4 parts (mxf4)
@@ -970,6 +975,9 @@ cudaError_t launch_grouped_gemms(const PoolView &v, int T, int k, const int32_t 
     ga.partial_dtype = partial_dtype;
     ga.nparts = nparts;
     ga.st = st;
+    // B rows a stage reserves: all BN, or (five-part rows, known bound) just the columns
+    // any tile has, rounded to the 16-row boxes: more pipeline stages fit
+    ga.bsr = (nparts > 1 && max_cols > 0 && max_cols < BN) ? (max_cols + 15) / 16 * 16 : BN;
     const int nexp = P < v.E ? P : v.E;  // at most this many experts have pairs
 
     // GEMM 1: gate/up

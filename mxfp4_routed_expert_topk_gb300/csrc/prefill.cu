@@ -141,7 +141,7 @@ __global__ void __launch_bounds__(1024) sort_small_kernel(const int32_t *__restr
                                                           int32_t *__restrict__ offsets, int32_t *__restrict__ uexp,
                                                           int32_t *__restrict__ n_union, int32_t *__restrict__ perm,
                                                           int32_t *__restrict__ inv_perm, int32_t *__restrict__ tile_off,
-                                                          int BN, int nparts, StatusWord *st) {
+                                                          int BN, int nparts, int maxcnt, StatusWord *st) {
     __shared__ int tot[kMaxSortE];
     __shared__ int es[1024];
     __shared__ int warp_sum[32];
@@ -159,6 +159,9 @@ __global__ void __launch_bounds__(1024) sort_small_kernel(const int32_t *__restr
     __syncthreads();
     if (e >= 0) atomicAdd(&tot[e], 1);
     __syncthreads();
+    // (maxcnt > 0) an expert named more than maxcnt times, which distinct indices per
+    // row cannot give, is reported: the GEMMs reserve room for that many pairs only
+    if (maxcnt > 0 && e >= 0 && tot[e] > maxcnt) set_status(st, MOE_ERR_BAD_INDEX, (unsigned)tid);
     offsets_and_union(tot, E, warp_sum, offsets, uexp, n_union, tile_off, BN, nparts);
     __syncthreads();  // offsets[] of this CTA's threads are visible to the others
     if (tid < P) {
@@ -661,10 +664,15 @@ cudaError_t launch_decode_multi(const PoolView &v, const uint16_t *x, int M, con
     StatusWord *stw = reinterpret_cast<StatusWord *>(ws);
     const int P = M * k;
     if (P > 1024) return cudaErrorNotSupported;
+    // with the k indices of a row distinct, an expert has at most M pairs, 5 M columns:
+    // when that is below a tile, the GEMM stages reserve only those B rows (more stages
+    // fit), and the sort reports an expert with more pairs than fit
+    int bsr = (kDecodeParts * M + 15) / 16 * 16;
+    if (bsr >= d.g.BN) bsr = 0;  // whole tiles (an expert with more pairs takes further tiles)
     {
         TraceScope trace_scope("sort_small", st);
         sort_small_kernel<<<1, 1024, 0, st>>>(idx, P, v.E, d.offsets, d.g.uexp, d.g.n_union, d.perm, d.inv_perm,
-                                              d.g.tile_off, d.g.BN, kDecodeParts, stw);
+                                              d.g.tile_off, d.g.BN, kDecodeParts, bsr / kDecodeParts, stw);
     }
     {
         TraceScope trace_scope("gather_split", st);
@@ -673,7 +681,7 @@ cudaError_t launch_decode_multi(const PoolView &v, const uint16_t *x, int M, con
             x, v.H, v.I, k, v.E, idx, d.perm, d.offsets, d.g.tile_off, d.g.BN, d.g.nsfb, d.g.xq, d.g.xs, d.g.hs);
     }
     cudaError_t e = launch_grouped_gemms(v, M, k, d.offsets, d.g, d.partial, MOE_PARTIAL_F32, stw, st, kDecodeParts,
-                                         true);
+                                         true, bsr);
     if (e != cudaSuccess) return e;
     {
         TraceScope trace_scope("combine", st);

@@ -166,10 +166,12 @@ __device__ __forceinline__ uint8_t e2m1x2_rn(float lo, float hi) {
 }
 
 // The two grouped block-scaled GEMMs (gate/up with SwiGLU and the MX quantisation of
-// h, then down), over the sorted rows.
+// h, then down), over the sorted rows.  max_cols > 0 (five-part rows only): no tile
+// has more columns than this (the sort reports an expert with more pairs as a bad
+// index), so each pipeline stage reserves only that many B rows.
 cudaError_t launch_grouped_gemms(const PoolView &v, int T, int k, const int32_t *offsets, const GroupedWs &g,
                                  void *partial, int partial_dtype, StatusWord *st, cudaStream_t stream,
-                                 int nparts = 1, bool fp4 = false);
+                                 int nparts = 1, bool fp4 = false, int max_cols = 0);
 
 // Multi-token decode (M > 1) through the grouped GEMMs with five-part MXFP4
 // activations; cudaErrorNotSupported for shapes the GEMMs do not take.

@@ -304,6 +304,50 @@ def test_decode_verify_hot_expert_spans_tiles(tiny, M):
     check_close(yg, ref, "verify with a hot expert (M rows)", bf16_at=yg)
 
 
+@pytest.mark.parametrize("M", [2, 5])
+def test_decode_verify_repeated_index_within_bound(tiny, M):
+    """A verify batch whose rows repeat an index: with an expert named at most
+    ceil16(5 M) / 5 times in all (3 for M = 2, 6 for M = 5) the narrow GEMM stages
+    hold all its rows, and every output matches the oracle on the same indices."""
+    s, pool, _, _ = tiny
+    rng = np.random.default_rng(100 + M)
+    limit = ((5 * M + 15) // 16 * 16) // 5
+    xb = synth.verify_batch_bf16(synth.TOKENS_SEED["verify"], 70 + M, M, s.H)
+    idx_h = np.stack([rng.choice(np.arange(1, s.E), s.k, replace=False) for _ in range(M)])
+    # expert 0: twice in row 0, once in each other row, up to the limit
+    idx_h[0, :2] = 0
+    for m in range(1, min(M, limit - 1)):
+        idx_h[m, 0] = 0
+    assert (idx_h == 0).sum() <= limit
+    w_h = rng.dirichlet(np.ones(s.k), size=M)
+    idx = torch.from_numpy(idx_h.astype(np.int32)).cuda()
+    w = torch.from_numpy(w_h.astype(np.float32)).cuda()
+    ws = moe.workspace(moe.moe_workspace_size(moe.MOE_OP_DECODE, s.E, s.H, s.I, M, s.k))
+    y = moe.moe_expert_forward_decode(pool, to_dev_bf16(xb), idx, w, ws=ws)
+    assert moe.moe_check_status(ws) == moe.MOE_OK
+    opool = oracle.SyntheticPool(synth.pool_seed(0), s.E, s.H, s.I, cache=s.E)
+    ref = oracle.combine_rows(opool, s.H, s.I, synth.bf16_bits_to_f64(xb), idx_h, w_h.astype(np.float32).astype(np.float64))
+    yg = bf16_to_f64(y)
+    check_close(yg, ref, "verify with a repeated index", bf16_at=yg)
+
+
+def test_decode_verify_expert_named_too_often(tiny):
+    """M = 2: an expert named 4 times (more than the 3 that 16 reserved B rows hold)
+    is reported as MOE_ERR_BAD_INDEX (y is then not valid); the status word clears on
+    the first check."""
+    s, pool, _, _ = tiny
+    M = 2
+    xb = synth.verify_batch_bf16(synth.TOKENS_SEED["verify"], 90, M, s.H)
+    idx_h = np.stack([np.arange(s.k) + 1, np.arange(s.k) + 1 + s.k]).astype(np.int32)
+    idx_h[0, :2] = 0
+    idx_h[1, :2] = 0
+    w = torch.full((M, s.k), 1.0 / s.k, dtype=torch.float32, device="cuda")
+    ws = moe.workspace(moe.moe_workspace_size(moe.MOE_OP_DECODE, s.E, s.H, s.I, M, s.k))
+    moe.moe_expert_forward_decode(pool, to_dev_bf16(xb), torch.from_numpy(idx_h).cuda(), w, ws=ws)
+    assert moe.moe_check_status(ws) == moe.MOE_ERR_BAD_INDEX
+    assert moe.moe_check_status(ws) == moe.MOE_OK
+
+
 @pytest.mark.parametrize("E,H,I,k,M", [(40, 384, 96, 8, 3), (20, 256, 160, 4, 7), (33, 640, 224, 32, 2)])
 def test_decode_ragged_shapes(E, H, I, k, M):
     s = synth.Shape(E=E, H=H, I=I, k=k)
