@@ -482,6 +482,10 @@ template <int NT, bool FP4>
 __global__ void __launch_bounds__(NT, GemmShape<NT>::kCtasPerSm)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const GemmArgs a) {
+    // launched early (programmatic dependent launch) on the multi-row decode path:
+    // wait for the previous kernel, then let the next one launch
+    griddep_wait();
+    griddep_launch_dependents();
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     // the tensor copies with 128-byte swizzling need 1024-byte aligned tiles
     unsigned char *smem = (unsigned char *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -925,10 +929,18 @@ cudaError_t launch_one(GemmArgs ga, const uint8_t *a_base, int a_k, int a_rows, 
     const int items = nexp * ((ga.nmt + tpi - 1) / tpi);
     TraceScope trace_scope(trace_name, stream);
     if (fp4) {
-        if (two)
+        // (the multi-token decode's chain of kernels launches each one early)
+        if (two && ga.nparts > 1)
+            e = launch_pdl(grouped_gemm_kernel<192, true>, dim3(std::min(2 * sms, items)), dim3(192), smem, stream,
+                           mA, mB, ga);
+        else if (two)
             grouped_gemm_kernel<192, true><<<std::min(2 * sms, items), 192, smem, stream>>>(mA, mB, ga);
+        else if (ga.nparts > 1)
+            e = launch_pdl(grouped_gemm_kernel<384, true>, dim3(std::min(sms, items)), dim3(384), smem, stream, mA,
+                           mB, ga);
         else
             grouped_gemm_kernel<384, true><<<std::min(sms, items), 384, smem, stream>>>(mA, mB, ga);
+        if (e != cudaSuccess) return e;
     } else {
         if (two)
             grouped_gemm_kernel<192, false><<<std::min(2 * sms, items), 192, smem, stream>>>(mA, mB, ga);

@@ -8,6 +8,7 @@
 #include <stdint.h>
 
 #include <atomic>
+#include <utility>
 
 #include "../../include/moe.h"
 
@@ -126,6 +127,41 @@ __device__ __forceinline__ unsigned char ldg_stream_u8(const void *p) {
 // Kernel tracing (api.cu): bracket one launch of kernel `name` with events.
 void trace_pre(const char *name, cudaStream_t st);
 void trace_post(const char *name, cudaStream_t st);
+
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialization may start while the previous kernel in the stream finishes; this
+// waits until that kernel has completed and its memory is visible (a no-op for a
+// kernel launched without the attribute).
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Let the next kernel of the stream (launched with programmatic stream serialization)
+// start once every CTA of this grid has called this or exited; it still waits, in
+// griddep_wait, for this grid to complete before it reads what this grid writes.
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Launch `kernel` on `st` with programmatic stream serialization: its CTAs may be
+// scheduled once every CTA of the previous kernel of the stream has let them
+// (griddepcontrol.launch_dependents) or exited, and it must execute
+// griddepcontrol.wait before it reads anything that kernel writes.  (Dependents start
+// only after all of the previous grid's CTAs are running, so they never keep it from
+// finishing.)
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                              Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 struct TraceScope {
     const char *name;

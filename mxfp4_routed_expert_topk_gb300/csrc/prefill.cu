@@ -142,6 +142,10 @@ __global__ void __launch_bounds__(1024) sort_small_kernel(const int32_t *__restr
                                                           int32_t *__restrict__ n_union, int32_t *__restrict__ perm,
                                                           int32_t *__restrict__ inv_perm, int32_t *__restrict__ tile_off,
                                                           int BN, int nparts, int maxcnt, StatusWord *st) {
+    // launched early (programmatic dependent launch) on the multi-row decode path:
+    // wait for the previous kernel, then let the next one launch
+    griddep_wait();
+    griddep_launch_dependents();
     __shared__ int tot[kMaxSortE];
     __shared__ int es[1024];
     __shared__ int warp_sum[32];
@@ -391,6 +395,10 @@ __global__ void gather_split5_f4_kernel(const uint16_t *__restrict__ x, int H, i
                                         const int32_t *__restrict__ offsets, const int32_t *__restrict__ tile_off,
                                         int BN, int nsfb, uint8_t *__restrict__ xq, uint8_t *__restrict__ xs,
                                         uint8_t *__restrict__ hs) {
+    // launched early (programmatic dependent launch) on the multi-row decode path:
+    // wait for the previous kernel, then let the next one launch
+    griddep_wait();
+    griddep_launch_dependents();
     constexpr int NP = kDecodeParts;
     constexpr int kChunk = 256;  // elements per warp: one step (few rows, so many warps)
     const int lane = threadIdx.x & 31;
@@ -468,6 +476,10 @@ template <typename PT>
 __global__ void combine_kernel(const PT *__restrict__ partial, const int32_t *__restrict__ inv_perm,
                                const float *__restrict__ w, int k, int H, const uint16_t *__restrict__ residual,
                                uint16_t *__restrict__ y, int chunk) {
+    // launched early (programmatic dependent launch) on the multi-row decode path:
+    // wait for the previous kernel, then let the next one launch
+    griddep_wait();
+    griddep_launch_dependents();
     __shared__ int rows[kMaxK];
     __shared__ float ws[kMaxK];
     const int t = blockIdx.x;
@@ -671,14 +683,18 @@ cudaError_t launch_decode_multi(const PoolView &v, const uint16_t *x, int M, con
     if (bsr >= d.g.BN) bsr = 0;  // whole tiles (an expert with more pairs takes further tiles)
     {
         TraceScope trace_scope("sort_small", st);
-        sort_small_kernel<<<1, 1024, 0, st>>>(idx, P, v.E, d.offsets, d.g.uexp, d.g.n_union, d.perm, d.inv_perm,
-                                              d.g.tile_off, d.g.BN, kDecodeParts, bsr / kDecodeParts, stw);
+        const cudaError_t e = launch_pdl(sort_small_kernel, dim3(1), dim3(1024), 0, st, idx, P, v.E, d.offsets, d.g.uexp,
+                                         d.g.n_union, d.perm, d.inv_perm, d.g.tile_off, d.g.BN, kDecodeParts,
+                                         bsr / kDecodeParts, stw);
+        if (e != cudaSuccess) return e;
     }
     {
         TraceScope trace_scope("gather_split", st);
         const int nchunk5 = (v.H + 255) / 256;  // the five-part split takes one 256-element step per warp
-        gather_split5_f4_kernel<<<(P * nchunk5 * 32 + 255) / 256, 256, 0, st>>>(
-            x, v.H, v.I, k, v.E, idx, d.perm, d.offsets, d.g.tile_off, d.g.BN, d.g.nsfb, d.g.xq, d.g.xs, d.g.hs);
+        const cudaError_t e = launch_pdl(gather_split5_f4_kernel, dim3((P * nchunk5 * 32 + 255) / 256), dim3(256), 0, st,
+                                         x, v.H, v.I, k, v.E, idx, d.perm, d.offsets, d.g.tile_off, d.g.BN, d.g.nsfb,
+                                         d.g.xq, d.g.xs, d.g.hs);
+        if (e != cudaSuccess) return e;
     }
     cudaError_t e = launch_grouped_gemms(v, M, k, d.offsets, d.g, d.partial, MOE_PARTIAL_F32, stw, st, kDecodeParts,
                                          true, bsr);
@@ -687,8 +703,9 @@ cudaError_t launch_decode_multi(const PoolView &v, const uint16_t *x, int M, con
         TraceScope trace_scope("combine", st);
         // few rows: a (row, 256-element chunk) grid, one output per thread (more warps in
         // flight than four outputs per thread, which is faster at this size)
-        combine_kernel<float><<<dim3(M, (v.H + 255) / 256), 256, 0, st>>>(d.partial, d.inv_perm, w, k, v.H, residual, y,
-                                                                         256);
+        e = launch_pdl(combine_kernel<float>, dim3(M, (v.H + 255) / 256), dim3(256), 0, st, (const float *)d.partial,
+                       (const int32_t *)d.inv_perm, w, k, v.H, residual, y, 256);
+        if (e != cudaSuccess) return e;
     }
     return cudaGetLastError();
 }

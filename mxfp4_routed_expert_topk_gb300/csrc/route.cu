@@ -235,6 +235,10 @@ __global__ void __launch_bounds__(256) route_logits_kernel(const uint16_t *__res
                                                            const uint16_t *__restrict__ Wr, int E,
                                                            const float *__restrict__ skew,
                                                            float *__restrict__ logit, float *__restrict__ bound) {
+    // launched early (programmatic dependent launch): wait for the previous kernel,
+    // then let the next one launch
+    griddep_wait();
+    griddep_launch_dependents();
     logits_block<16>(x, M, H, Wr, E, skew, logit, bound);
 }
 
@@ -1057,6 +1061,10 @@ __global__ void __launch_bounds__(kRouteThreads) route_select_kernel(
     const uint16_t *__restrict__ x, int H, const uint16_t *__restrict__ Wr, int E, const float *__restrict__ skew,
     int k, const float *__restrict__ logit, const float *__restrict__ bound, int32_t *__restrict__ idx_out,
     float *__restrict__ w_out, StatusWord *st) {
+    // launched early (programmatic dependent launch): wait for the previous kernel,
+    // then let the next one launch
+    griddep_wait();
+    griddep_launch_dependents();
     __shared__ SelectShared s;
     const int m = blockIdx.x;
     select_token<J>(m, x, H, Wr, E, skew, k, logit + (size_t)m * E, bound + (size_t)m * E, idx_out, w_out, st, s);
@@ -1133,11 +1141,14 @@ cudaError_t launch_route_j(const uint16_t *x, int M, int H, const uint16_t *Wr, 
                                                                         r.bound);
     } else {
         TraceScope trace_scope("route_logits", st);
-        route_logits_kernel<<<g1, 256, smem1, st>>>(x, M, H, Wr, E, skew, r.logit, r.bound);
+        cudaError_t e = launch_pdl(route_logits_kernel, g1, dim3(256), smem1, st, x, M, H, Wr, E, skew, r.logit, r.bound);
+        if (e != cudaSuccess) return e;
     }
     {
         TraceScope trace_scope("route_select", st);
-        route_select_kernel<J><<<M, kRouteThreads, 0, st>>>(x, H, Wr, E, skew, k, r.logit, r.bound, idx, w, stw);
+        cudaError_t e = launch_pdl(route_select_kernel<J>, dim3(M), dim3(kRouteThreads), 0, st, x, H, Wr, E, skew, k,
+                                   r.logit, r.bound, idx, w, stw);
+        if (e != cudaSuccess) return e;
     }
     return cudaGetLastError();
 }

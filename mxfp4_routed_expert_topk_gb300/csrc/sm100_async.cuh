@@ -112,19 +112,6 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
         : "memory");
 }
 
-// Programmatic dependent launch: a kernel launched with programmatic stream
-// serialization may start while the previous kernel in the stream finishes; this
-// waits until that kernel has completed and its memory is visible (a no-op for a
-// kernel launched without the attribute).
-__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-
-// Let the next kernel of the stream (launched with programmatic stream serialization)
-// start once every CTA of this grid has called this or exited; it still waits, in
-// griddep_wait, for this grid to complete before it reads what this grid writes.
-__device__ __forceinline__ void griddep_launch_dependents() {
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-
 // Named barrier over `count` threads (a multiple of 32) with id `id` (1..15).
 __device__ __forceinline__ void named_barrier(int id, int count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
