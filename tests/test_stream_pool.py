@@ -81,3 +81,16 @@ def test_matches_reference_lru_on_zipf_requests():
         assert len(set(got)) == k                    # distinct experts, distinct slots
     assert sp.stats()[:2] == (ref.hits, ref.misses)
     assert ref.hits > ref.misses                     # the skew makes the cache useful
+
+
+def test_host_alloc_argument_checks():
+    """moe_host_alloc / moe_host_free reject bad arguments before any CUDA call (so this
+    runs without a GPU): a null out pointer or zero bytes is MOE_ERR_INVALID_ARG, and
+    freeing a null pointer is a no-op."""
+    import ctypes
+    L = moe.lib()
+    p = ctypes.c_void_p()
+    node = ctypes.c_int(7)
+    assert L.moe_host_alloc(0, 0, ctypes.byref(p), ctypes.byref(node)) == moe.MOE_ERR_INVALID_ARG
+    assert L.moe_host_alloc(0, 4096, None, None) == moe.MOE_ERR_INVALID_ARG
+    assert L.moe_host_free(None, 4096) == moe.MOE_OK
