@@ -120,6 +120,31 @@ def test_e4m3_encode_matches_torch_in_range():
         assert oracle.e4m3_encode(a) == c
 
 
+def test_e4m3_encode_every_bf16_pattern_by_brute_force():
+    """E4M3 encoding (round to nearest, ties to the even code, saturating at 448) of
+    every finite bf16 value, against a nearest-value search over the 127 magnitudes
+    written out from the format's definition (bias 7, 3 mantissa bits, subnormals at
+    exponent field 0, magnitude code 0x7F reserved for NaN)."""
+    mags = np.array([(m & 7) / 8.0 * 2.0 ** -6 if (m >> 3) == 0 else (1 + (m & 7) / 8.0) * 2.0 ** ((m >> 3) - 7)
+                     for m in range(127)])
+    assert mags[-1] == 448.0 and np.all(np.diff(mags) > 0)
+    bits = np.arange(65536, dtype=np.uint32)
+    f32 = (bits << 16).view(np.float32)
+    finite = np.isfinite(f32)
+    vals = np.where(finite, f32, 0).astype(np.float64)
+    for b, v in zip(bits[finite], vals[finite]):
+        a = abs(v)
+        if a >= 448.0:
+            m = 126
+        else:
+            hi = int(np.searchsorted(mags, a))          # first magnitude >= a
+            lo = max(hi - 1, 0)
+            dl, dh = a - mags[lo], mags[hi] - a
+            m = lo if dl < dh else hi if dh < dl else (lo if lo % 2 == 0 else hi)
+        want = m | (0x80 if (b >> 15) & 1 else 0)
+        assert oracle.e4m3_encode(v) == want, (hex(int(b)), v)
+
+
 def test_mxfp8_block_rule():
     # amax 1.0 -> X = floor(log2 1) - 8 = -8 (byte 119); 1.0 -> 256 -> code exact
     v = np.zeros(64)
