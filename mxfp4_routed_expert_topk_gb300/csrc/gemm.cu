@@ -175,14 +175,11 @@ __device__ __forceinline__ bool elect_one() {
     return p != 0;
 }
 
+// One 512-byte scale atom (32 rows x 16 bytes) into 4 TMEM columns of all four lane
+// quadrants.  Each copy occupies the tensor pipe for about 100 clocks whatever its size
+// (a 4 KB 128x256b copy costs the same), in order with the MMAs.
 __device__ __forceinline__ void tc_cp_sf(uint32_t taddr, uint64_t sdesc) {
     asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
-}
-
-// 128 lanes x 32 bytes (8 columns) from shared memory: the two interleaved scale atoms
-// of a 256-column B tile, already replicated per lane quadrant in shared memory.
-__device__ __forceinline__ void tc_cp_sf2(uint32_t taddr, uint64_t sdesc) {
-    asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
 }
 
 __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t sfa,
@@ -587,15 +584,8 @@ __global__ void __launch_bounds__(NT, GemmShape<NT>::kCtasPerSm)
                         for (int j = 0; j < n2; j++)  // the two K tiles' A blocks are nmt blocks apart
                             bulk_g2s_l2(sSFA + (size_t)s * 1024 + 512 * j, sfa_src + (size_t)j * a.nmt * 512, 512u,
                                         &full[s]);
-                        if (nsfb == 1) {
-                            bulk_g2s_l2(sSFB + (size_t)s * 1024, sfb_src, (uint32_t)n2 * 512u, &full[s]);  // adjacent
-                        } else {
-                            // per K tile the interleaved 1 KB block once per TMEM lane quadrant
-                            for (int j = 0; j < n2; j++)
-                                for (int q = 0; q < 4; q++)
-                                    bulk_g2s_l2(sSFB + (size_t)s * 8192 + (size_t)j * 4096 + q * 1024,
-                                                sfb_src + (size_t)j * 1024, 1024u, &full[s]);
-                        }
+                        // the n2 K tiles' atoms (or interleaved 1 KB two-atom blocks) are adjacent
+                        bulk_g2s_l2(sSFB + (size_t)s * 2 * sfbk, sfb_src, (uint32_t)n2 * sfbk, &full[s]);
                     }
                 } else {
                     const int brows = a.bbox == a.BN ? a.BN : (J.nn() + 15) / 16 * 16;  // B rows copied
@@ -612,13 +602,7 @@ __global__ void __launch_bounds__(NT, GemmShape<NT>::kCtasPerSm)
                             tma_load_2d(sB + (size_t)s * a.bsr * kTileK + (size_t)c * kTileK, &tmB, kt * kTileK,
                                         brow + c, &full[s]);
                         bulk_g2s_l2(sSFA + (size_t)s * tpi * 512, sfa_src, a_tiles * 512u, &full[s]);
-                        if (nsfb == 1) {
-                            bulk_g2s_l2(sSFB + (size_t)s * 512, sfb_src, 512u, &full[s]);
-                        } else {
-                            // the interleaved 1 KB block once per TMEM lane quadrant
-                            for (int q = 0; q < 4; q++)
-                                bulk_g2s_l2(sSFB + (size_t)s * 4096 + q * 1024, sfb_src, 1024u, &full[s]);
-                        }
+                        bulk_g2s_l2(sSFB + (size_t)s * sfb_stage_bytes(nsfb), sfb_src, sfb_stage_bytes(nsfb), &full[s]);
                     }
                 }
                 __syncwarp();
@@ -646,9 +630,10 @@ __global__ void __launch_bounds__(NT, GemmShape<NT>::kCtasPerSm)
         const uint64_t adesc0 = smem_desc(smem_u32(sA), 16, 1024, kSwizzle128B);
         const uint64_t bdesc0 = smem_desc(smem_u32(sB), 16, 1024, kSwizzle128B);
         const uint64_t sfadesc0 = smem_desc(smem_u32(sSFA), 128, 128, kSwizzleNone);
-        // core matrices of 8 rows x 16 bytes: for two atoms the 16-byte halves 128 bytes
-        // apart and the row groups 256 bytes apart
-        const uint64_t sfbdesc0 = smem_desc(smem_u32(sSFB), 128, nsfb == 1 ? 128 : 256, kSwizzleNone);
+        // core matrices of 8 rows x 16 bytes: an atom's row groups are 128 bytes apart, or
+        // 256 in a two-atom block (the other atom's rows in between)
+        const uint32_t sfb_rg = nsfb == 1 ? 128u : 256u;
+        const uint64_t sfbdesc0 = smem_desc(smem_u32(sSFB), sfb_rg, sfb_rg, kSwizzleNone);
         const int nlook = min(4, ns);  // stages polled at once (never past the ring)
         for (JobIter J(a, nu); run && J.valid(); J.next(), jb++) {
             const int nmma = (J.nn() + 15) / 16 * 16;
@@ -705,10 +690,13 @@ __global__ void __launch_bounds__(NT, GemmShape<NT>::kCtasPerSm)
                             const uint32_t sfb_t4 = sfa_t + 8u, bw = 4u * (uint32_t)nsfb;
                             for (int j = 0; j < n2; j++) {
                                 tc_cp_sf(sfa_t + 4u * j, sfad + (uint64_t)(32 * j));
-                                if (nsfb == 1)
+                                if (nsfb == 1) {
                                     tc_cp_sf(sfb_t4 + 4u * j, sfbd + (uint64_t)(32 * j));
-                                else
-                                    tc_cp_sf2(sfb_t4 + 8u * j, sfbd + (uint64_t)(256 * j));  // 4 KB apart
+                                } else {
+                                    // the two atoms of the 1 KB block: rows 128 bytes apart in it
+                                    tc_cp_sf(sfb_t4 + 8u * j, sfbd + (uint64_t)(64 * j));
+                                    tc_cp_sf(sfb_t4 + 8u * j + 4u, sfbd + (uint64_t)(64 * j + 8));
+                                }
                             }
                             for (int ks = 0; ks < 2 * n2; ks++)
                                 tc_mma_f4(acc, ad0 + (uint64_t)(2 * ks), bd0 + (uint64_t)(2 * ks),
@@ -717,10 +705,8 @@ __global__ void __launch_bounds__(NT, GemmShape<NT>::kCtasPerSm)
                         } else {
                             for (int t = 0; t < tpi; t++)
                                 tc_cp_sf(sfa_t + 4u * t, sfad + (uint64_t)(32 * t));  // 512 B apart
-                            if (nsfb == 1)
-                                tc_cp_sf(sfb_t, sfbd);
-                            else
-                                tc_cp_sf2(sfb_t, sfbd);
+                            tc_cp_sf(sfb_t, sfbd);
+                            if (nsfb == 2) tc_cp_sf(sfb_t + 4u, sfbd + 8u);  // the block's second atom
                             for (int t = 0; t < tpi; t++) {
                                 // tile t: rows 128t.. of the stage's A (16 KB apart), accumulator columns t*BN..
                                 const uint64_t adt = ad0 + (uint64_t)(1024 * t);

@@ -34,20 +34,19 @@ __host__ __device__ inline int grouped_bn(int P, int E, int T, int nparts, bool 
 // and keeps the 4 scale bytes of its K tile (scale block 4kt+j at byte j of the word)
 // in row c % 32 of the atom (16 bytes, word (c / 32) % 4): the 32 x 16-byte layout that
 // tcgen05.cp copies into TMEM.  With two atoms, their rows are interleaved by groups of
-// 8 (row group g of atom a at byte g * 256 + a * 128), so that the 1 KB block is one
-// lane quadrant of the 128 x 32-byte matrix a single 128x256b tcgen05.cp takes (in the
-// core-matrix order of its descriptor); with one atom this is the plain atom.  Bytes of
-// columns past the tile's rows are never read by a result that is kept.  Byte offset of
-// the word of (tile, kt, c):
+// 8 (row group g of atom a at byte g * 256 + a * 128): each atom is then one 32x128b
+// copy whose row groups are 256 bytes apart; with one atom this is the plain atom.
+// Bytes of columns past the tile's rows are never read by a result that is kept.  Byte
+// offset of the word of (tile, kt, c):
 __host__ __device__ inline size_t sf_tile_word(int tile, int nkt, int nsfb, int kt, int c) {
     return ((size_t)tile * nkt + kt) * (size_t)nsfb * 512 + (size_t)((c & 31) >> 3) * (size_t)nsfb * 128 +
            (size_t)(c >> 7) * 128 + (size_t)(c & 7) * 16 + (size_t)((c >> 5) & 3) * 4;
 }
 
-// Bytes of B's scale factors in one pipeline stage in shared memory: the atom, or for
-// two atoms the interleaved 1 KB block four times over (one copy per TMEM lane
-// quadrant, the replication the MMA's scale layout needs).
-__host__ __device__ inline uint32_t sfb_stage_bytes(int nsfb) { return nsfb == 1 ? 512u : 4096u; }
+// Bytes of B's scale factors per 128-K tile in shared memory: the atom, or the
+// interleaved 1 KB two-atom block (each atom reaches all four TMEM lane quadrants
+// through its own .warpx4 copy, so nothing is replicated in shared memory).
+__host__ __device__ inline uint32_t sfb_stage_bytes(int nsfb) { return nsfb == 1 ? 512u : 1024u; }
 
 // Activation rows of the grouped GEMMs.  nparts = 1: one MXFP8 row per pair (OCP
 // rule, the prefill path), or with fp4 one MXFP4 row (two E2M1 codes per byte,
