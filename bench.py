@@ -579,13 +579,24 @@ def run_ours(args):
                "single_thread": {"value": n1 / secs1, "unit": "layer-tokens/s", "cores": 1,
                                  "sample": f"{n1} tokens of the same workload on one thread"}}
     launches = 2 * NTOK * args.steps      # route_single + decode_fused per token
-    prefill, prefill4 = {}, {}
+    prefill, prefill4, pairs = {}, {}, {}
     if not args.no_prefill:
         for T in synth.PREFILL_T:
             prefill[str(T)] = measure_prefill(moe, torch, pool, Wr, dev, T)
         for T in synth.PREFILL_T + synth.PREFILL_T_LARGE:
             prefill4[str(T)] = measure_prefill(moe, torch, pool, Wr, dev, T, act_mode=2)
             torch.cuda.empty_cache()
+        # the other tile shape of each row format: MXFP8 on one CTA per tile (the default
+        # runs it on paired-SM tiles, tcgen05 cta_group::2), MXFP4 on paired-SM tiles
+        for mode, cases in ((moe.CTA_PAIRS_NEVER, ((8192, 1),)), (moe.CTA_PAIRS_ALWAYS, ((8192, 2), (32768, 2)))):
+            moe.moe_grouped_set_cta_pairs(mode)
+            try:
+                for T, act in cases:
+                    key = f"{T}_{'mxfp8' if act == 1 else 'mxfp4'}_{'one_cta' if mode == moe.CTA_PAIRS_NEVER else 'pairs'}"
+                    pairs[key] = measure_prefill(moe, torch, pool, Wr, dev, T, act_mode=act)["kernel_ms"]
+            finally:
+                moe.moe_grouped_set_cta_pairs(moe.CTA_PAIRS_MXFP8)
+        torch.cuda.empty_cache()
     verify, stacked, streamed, tiny = {}, None, None, None
     if not args.no_extra:
         tiny = measure_tiny_l2(moe, torch, dev)
@@ -614,6 +625,7 @@ def run_ours(args):
             "gpu_launches": launches,
             "prefill": prefill,
             "prefill_mxfp4": prefill4,
+            "prefill_other_tile_shape": pairs,
             "verify": verify,
             "stacked_8_layers": stacked,
             "tiny_l2": tiny,

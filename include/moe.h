@@ -296,6 +296,19 @@ moe_status moe_combine(const void *partial, int partial_dtype, const int32_t *in
                        const float *w, int T, int k, int H, const uint16_t *residual,
                        uint16_t *y, moe_stream_t stream);
 
+/* Tile shape of moe_expert_forward_grouped's tensor-core GEMMs (process-wide, for
+ * calls that start after it returns).  One-part tiles of 128 or more columns can run
+ * on pairs of SMs: a cluster of two CTAs issuing tcgen05 MMAs of cta_group::2, M = 256,
+ * each CTA holding 128 weight rows and half of the tile's activation rows (so each SM
+ * copies half of B), the odd CTA's tensor copies counted on the even CTA's barrier.
+ * mode 0: never (one CTA per 128-row tile); 1: always where the tile allows it;
+ * 2 (the default): with MXFP8 rows only.  Measured on a GB300 at 8192 tokens the
+ * pairs took the MXFP8 GEMMs 5.78 -> 5.10 ms and the MXFP4 GEMMs 4.57 -> 4.70 ms
+ * (32768 tokens: 16.9 -> 17.2 ms), hence the default.  Results agree up to the fp32
+ * accumulation order of the tensor pipe, which neither shape fixes.
+ * MOE_ERR_INVALID_ARG for other modes. */
+moe_status moe_grouped_set_cta_pairs(int mode);
+
 /* ------------------------------------------------------------- test support
  * Failure detection without a GPU fault.  Every device wait of the library (the
  * mbarrier waits of the copy/MMA pipelines, the grid barrier of the single-token

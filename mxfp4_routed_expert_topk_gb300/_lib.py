@@ -34,7 +34,8 @@ EXPORTED = [
     "moe_workspace_size", "moe_clear_status", "moe_check_status", "moe_status_string",
     "moe_route_topk", "moe_route_topk_static", "moe_route_topk_prescaled", "moe_expert_forward_decode",
     "moe_prescale",
-    "moe_expert_forward_grouped", "moe_grouped_read_h", "moe_combine", "moe_trace_begin", "moe_trace_end",
+    "moe_expert_forward_grouped", "moe_grouped_read_h", "moe_combine", "moe_grouped_set_cta_pairs",
+    "moe_trace_begin", "moe_trace_end",
     "moe_debug_set_wait_limit", "moe_debug_set_barrier_extra",
     "moe_stream_pool_create", "moe_stream_pool_destroy", "moe_stream_pool_cache", "moe_stream_pool_slots",
     "moe_stream_pool_map", "moe_stream_pool_stats", "moe_host_alloc", "moe_host_free", "moe_host_numa_node",
@@ -90,6 +91,7 @@ def lib() -> ctypes.CDLL:
             "moe_host_free": (_i, [_vp, _sz]),
             "moe_host_numa_node": (_i, [_i]),
             "moe_debug_set_barrier_extra": (_i, [_i]),
+            "moe_grouped_set_cta_pairs": (_i, [_i]),
             "moe_trace_begin": (_i, [ctypes.c_char_p]),
             "moe_trace_end": (_i, [ctypes.POINTER(_i), ctypes.POINTER(ctypes.c_double)]),
         }
@@ -435,6 +437,16 @@ def moe_host_numa_node(device=None) -> int:
     """The host NUMA node closest to `device` (-1: no NUMA or unknown)."""
     dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
     return int(lib().moe_host_numa_node(dev.index or 0))
+
+
+CTA_PAIRS_NEVER, CTA_PAIRS_ALWAYS, CTA_PAIRS_MXFP8 = 0, 1, 2
+
+
+def moe_grouped_set_cta_pairs(mode: int):
+    """Tile shape of the grouped GEMMs for later calls: one-part tiles of 128+ columns on
+    pairs of SMs (tcgen05 cta_group::2) never (0), always (1), or with MXFP8 rows only
+    (2, the default)."""
+    _check(lib().moe_grouped_set_cta_pairs(int(mode)), "moe_grouped_set_cta_pairs")
 
 
 # ---------------------------------------------------------- test support

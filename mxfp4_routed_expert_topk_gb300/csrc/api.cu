@@ -289,6 +289,12 @@ moe_status moe_debug_set_wait_limit(uint64_t ns) {
     return MOE_OK;
 }
 
+moe_status moe_grouped_set_cta_pairs(int mode) {
+    if (mode < 0 || mode > 2) return MOE_ERR_INVALID_ARG;
+    set_cta_pairs(mode);
+    return MOE_OK;
+}
+
 moe_status moe_debug_set_barrier_extra(int extra) {
     if (extra < 0 || extra > 1024) return MOE_ERR_INVALID_ARG;
     set_barrier_extra((unsigned int)extra);

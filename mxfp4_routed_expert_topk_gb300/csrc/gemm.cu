@@ -23,10 +23,14 @@
 // TMEM and issues the scale copies and MMAs into one of two accumulators; the epilogue
 // warps drain the other accumulator, so a tile's epilogue overlaps the next tile's
 // MMAs.  Two shapes (GemmShape): one CTA of 12 warps per SM (two epilogue warpgroups)
-// or two CTAs of 6 warps per SM (one), chosen per launch by the tile width.  With
-// five-part MXFP4 activations (nparts = 5, the multi-token decode) each sorted pair
-// has five B rows whose columns the epilogue sums.  Every wait is bounded
-// (MOE_ERR_TIMEOUT), and nothing exits with copies or MMAs in flight.
+// or two CTAs of 6 warps per SM (one), chosen per launch by the tile width.  Wide
+// one-part tiles can also run on CTA pairs (PAIR: a cluster of two CTAs on two SMs,
+// tcgen05 MMAs of cta_group::2 with M = 256 issued by the even CTA; each CTA copies its
+// 128 weight rows and half of the tile's activation rows, and its tensor copies count
+// on the even CTA's barrier).  With five-part MXFP4 activations (nparts = 5, the
+// multi-token decode) each sorted pair has five B rows whose columns the epilogue sums.
+// Every wait is bounded (MOE_ERR_TIMEOUT), and nothing exits with copies or MMAs in
+// flight.
 #include <algorithm>
 
 #include <cuda.h>
@@ -92,6 +96,8 @@ struct GemmArgs {
     void *partial;       // [P][H]
     int partial_dtype;
     int nparts;          // activation rows per pair (1, or 5: the MXFP4 parts of the multi-token decode)
+    int pair;            // 1: CTA pairs (cta_group::2), an item is two 128-row tiles of A, one per CTA,
+                         // and each CTA holds bsr = BN / 2 rows of B per stage
     StatusWord *st;
 };
 
@@ -113,6 +119,26 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, i
         : "memory");
 }
 
+// A pair's tensor copies: into this CTA's shared memory, completion counted on the even
+// CTA's barrier (`mbar`, its address in the cluster window), so that barrier's phase
+// covers the copies of both CTAs.
+__device__ __forceinline__ void tma_load_3d_pair(void *dst, const CUtensorMap *map, int c0, int c1, int c2,
+                                                 uint32_t mbar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cta.global.tile.mbarrier::complete_tx::bytes.cta_group::2 [%0], [%1, {%2, %3, "
+        "%4}], [%5];" ::"r"(smem_u32(dst)),
+        "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(mbar)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d_pair(void *dst, const CUtensorMap *map, int c0, int c1, uint32_t mbar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cta.global.tile.mbarrier::complete_tx::bytes.cta_group::2 [%0], [%1, {%2, "
+        "%3}], [%4];" ::"r"(smem_u32(dst)),
+        "l"(map), "r"(c0), "r"(c1), "r"(mbar)
+        : "memory");
+}
+
 // Shared-memory matrix descriptor of tcgen05: start address, leading / stride
 // byte offsets (16-byte units), fixed version bits 46..48 = 0b001, swizzle mode.
 __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo, uint32_t swizzle) {
@@ -128,18 +154,19 @@ constexpr uint32_t kSwizzle128B = 2;
 constexpr uint32_t kSwizzleNone = 0;
 
 // Instruction descriptor of kind::mxf8f6f4: A = E2M1 (5), B = E4M3 (0), both
-// K-major, M = 128, N = n, E8M0 scales, scale-factor ids for A and B.
+// K-major, M = m (128, or 256 for a CTA pair), N = n, E8M0 scales, scale-factor ids
+// for A and B.
 // idesc_mxf8f6f4(n, k) = idesc_mxf8f6f4(n, 0) + k * kIdescSfStep for k in 0..3
 constexpr uint32_t kIdescSfStep = (1u << 4) | (1u << 29);
 
-__device__ __forceinline__ uint32_t idesc_mxf8f6f4(int n, int sf_id) {
+__device__ __forceinline__ uint32_t idesc_mxf8f6f4(int n, int sf_id, int m = kTileM) {
     uint32_t d = 0;
     d |= (uint32_t)(sf_id & 3) << 4;     // B scale factor id
     d |= 5u << 7;                        // A format: E2M1
     d |= 0u << 10;                       // B format: E4M3
     d |= (uint32_t)(n >> 3) << 17;       // N / 8
     d |= 1u << 23;                       // scale format: UE8M0
-    d |= (uint32_t)(kTileM >> 4) << 24;  // M / 16
+    d |= (uint32_t)(m >> 4) << 24;       // M / 16
     d |= (uint32_t)(sf_id & 3) << 29;    // A scale factor id
     return d;
 }
@@ -194,18 +221,18 @@ __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t
 }
 
 // Instruction descriptor of kind::mxf4: A and B E2M1 (format 1 of this kind), both
-// K-major, M = 128, N = n, E8M0 scales.  With scale_vec::2X an MMA (K = 64) takes the
+// K-major, M = m (128, or 256 for a CTA pair), N = n, E8M0 scales.  With scale_vec::2X an MMA (K = 64) takes the
 // scale bytes sf_id, sf_id + 1 (sf_id 0 or 2) of a 32-bit TMEM column: add
 // kIdescSf2 for sf_id 2 (A and B alike).
 constexpr uint32_t kIdescSf2 = (2u << 4) | (2u << 29);
 
-__device__ __forceinline__ uint32_t idesc_mxf4(int n) {
+__device__ __forceinline__ uint32_t idesc_mxf4(int n, int m = kTileM) {
     uint32_t d = 0;
     d |= 1u << 7;                        // A format: E2M1
     d |= 1u << 10;                       // B format: E2M1
     d |= (uint32_t)(n >> 3) << 17;       // N / 8
     d |= 1u << 23;                       // scale format: UE8M0
-    d |= (uint32_t)(kTileM >> 4) << 24;  // M / 16
+    d |= (uint32_t)(m >> 4) << 24;       // M / 16
     return d;
 }
 
@@ -223,6 +250,110 @@ __device__ __forceinline__ void tc_mma_f4(uint32_t d_tmem, uint64_t adesc, uint6
 __device__ __forceinline__ void tc_commit(uint64_t *bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
                  : "memory");
+}
+
+// ---- CTA pairs (cta_group::2).  A cluster of two CTAs on two SMs: the even CTA issues
+// MMAs of M = 256 whose A rows (128 per CTA) and B columns (N / 2 per CTA, the even CTA
+// the first half) come from both CTAs' shared memory at the same offsets; each CTA's
+// TMEM holds its own 128 accumulator rows, and the scale factors of its A rows and of
+// all N columns of B.  Scale copies, MMAs and commits are issued by the even CTA and act
+// on both; a commit arrives on the barrier at the same offset in both CTAs.
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// All threads of both CTAs (release / acquire at cluster scope).
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Address in the cluster's shared window of the object at the same offset in CTA `rank`.
+__device__ __forceinline__ uint32_t mapa_shared(const void *p, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+    return r;
+}
+
+// Arrive on a barrier of the other CTA (release at cluster scope).
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
+// try_wait with acquire at cluster scope: for phases completed by the other CTA's arrivals.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// mbar_wait_or_abort for such phases.
+__device__ __forceinline__ bool mbar_wait_cluster_or_abort(uint64_t *bar, uint32_t parity, StatusWord *st,
+                                                           unsigned where, const int *abort_flag) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns(), lim = g_wait_limit_ns;
+    for (uint32_t it = 0;; it++) {
+        if (mbar_try_wait_cluster(bar, parity)) return true;
+        if (*(const volatile int *)abort_flag) return false;
+        if ((it & 63u) == 63u && global_timer_ns() - t0 > lim) {
+            set_status(st, MOE_ERR_TIMEOUT, where);
+            return false;
+        }
+    }
+}
+
+// TMEM of both CTAs: one warp of each CTA takes part.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t *dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+__device__ __forceinline__ void tc_cp_sf_pair(uint32_t taddr, uint64_t sdesc) {
+    asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
+__device__ __forceinline__ void tc_mma_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t sfa, uint32_t sfb, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+            d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_mma_f4_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                               uint32_t sfa, uint32_t sfb, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+            d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+        : "memory");
+}
+
+// Commit of the pair's MMAs: arrives on `bar` in both CTAs.
+__device__ __forceinline__ void tc_commit_pair(uint64_t *bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            smem_u32(bar)),
+        "h"((uint16_t)3)
+        : "memory");
 }
 
 // 16 accumulator columns of this warp's 32 TMEM lanes; the wait is in the same
@@ -438,51 +569,60 @@ struct GemmSmemLayout {
     }
 };
 
-// The work of a CTA: items i = blockIdx.x, +gridDim.x, ... of the n_union * nmt
-// (expert of the union, 128-row tile of A) items; each item's columns in tiles of
-// BN.  Every role walks this same sequence.
+// The work of a CTA (or CTA pair): items i = first, first + stride, ... of the
+// (expert of the union, span 128-row tiles of A) items, span = tpi, or 2 for a pair
+// (first = the pair's index, stride = the number of pairs); each item's columns in
+// tiles of BN.  Every role of both CTAs walks this same sequence.
 struct JobIter {
     const GemmArgs &a;
-    int nu, i, nt, ntile, e, mt, row0, nrows, tile0;
-    __device__ JobIter(const GemmArgs &args, int nu_) : a(args), nu(nu_), i((int)blockIdx.x), nt(0), ntile(0) { load(); }
+    int nu, i, stride, span, nt, ntile, e, mt, row0, nrows, tile0;
+    __device__ JobIter(const GemmArgs &args, int nu_, int first, int stride_)
+        : a(args), nu(nu_), i(first), stride(stride_), span(args.pair ? 2 : args.tpi), nt(0), ntile(0) {
+        load();
+    }
     __device__ void load() {
         ntile = 0;
-        const int nwi = (a.nmt + a.tpi - 1) / a.tpi;  // items per expert
+        const int nwi = (a.nmt + span - 1) / span;  // items per expert
         while (i < nu * nwi) {
             const int u = i / nwi;
-            mt = (i % nwi) * a.tpi;  // first 128-row tile of the item
+            mt = (i % nwi) * span;  // first 128-row tile of the item
             e = a.uexp[u];
             row0 = a.nparts * a.offsets[e];
             nrows = a.nparts * (a.offsets[e + 1] - a.offsets[e]);
             ntile = (nrows + a.BN - 1) / a.BN;
             tile0 = a.tile_off[e];
             if (ntile > 0) break;
-            i += (int)gridDim.x;
+            i += stride;
         }
         nt = 0;
     }
-    __device__ bool valid() const { return i < nu * ((a.nmt + a.tpi - 1) / a.tpi) && ntile > 0; }
+    __device__ bool valid() const { return i < nu * ((a.nmt + span - 1) / span) && ntile > 0; }
     __device__ int n0() const { return nt * a.BN; }
     __device__ int tile() const { return tile0 + nt; }
     // columns of the current tile (at most bsr: a tile with more is reported by the
-    // sort as a bad index and computed only in part)
-    __device__ int nn() const { return min(a.bsr, nrows - nt * a.BN); }
+    // sort as a bad index and computed only in part; a pair's CTAs hold BN / 2 each)
+    __device__ int nn() const { return min(a.pair ? a.BN : a.bsr, nrows - nt * a.BN); }
+    // MMA width: the columns rounded up to 16
+    __device__ int nmma() const { return (nn() + 15) / 16 * 16; }
     __device__ void next() {
         if (++nt >= ntile) {
-            i += (int)gridDim.x;
+            i += stride;
             load();
         }
     }
 };
 
-template <int NT, bool FP4>
+template <int NT, bool FP4, bool PAIR>
 __global__ void __launch_bounds__(NT, GemmShape<NT>::kCtasPerSm)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                        const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
                         const GemmArgs a) {
+    // (tmSA, tmSB: the scale factors of A and B as tensors, used by CTA pairs)
     // launched early (programmatic dependent launch) on the multi-row decode path:
     // wait for the previous kernel, then let the next one launch
     griddep_wait();
     griddep_launch_dependents();
+    static_assert(!PAIR || NT == 384, "CTA pairs use the one-CTA-per-SM shape");
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     // the tensor copies with 128-byte swizzling need 1024-byte aligned tiles
     unsigned char *smem = (unsigned char *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -500,8 +640,14 @@ __global__ void __launch_bounds__(NT, GemmShape<NT>::kCtasPerSm)
     float *amax_x = reinterpret_cast<float *>(smem + L.misc + 16);  // [8 epilogue warps][16 columns]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // a pair's CTAs: rank 0 issues the MMAs, rank 1 holds the second 128 A rows and the
+    // second half of the columns of each item
+    const int rank = PAIR ? (int)cluster_ctarank() : 0;
+    const int first = PAIR ? (int)blockIdx.x / 2 : (int)blockIdx.x;
+    const int stride = PAIR ? (int)gridDim.x / 2 : (int)gridDim.x;
     const int nu = *a.n_union;
-    if ((int)blockIdx.x >= nu * ((a.nmt + tpi - 1) / tpi)) return;  // the whole CTA, before any barrier
+    // the whole CTA (both CTAs of a pair alike), before any barrier
+    if (first >= nu * ((a.nmt + (PAIR ? 2 : tpi) - 1) / (PAIR ? 2 : tpi))) return;
     const int nsfb = a.nsfb;
 
     // The unpacked E2M1 copies write 8 of every 16 bytes of an A tile; keep the
@@ -520,16 +666,23 @@ __global__ void __launch_bounds__(NT, GemmShape<NT>::kCtasPerSm)
             mbar_init(&empty[s], 1);  // MMA commit
         }
         for (int b = 0; b < 2; b++) {
-            mbar_init(&acc_full[b], 1);   // MMA commit after a tile's last K step
-            mbar_init(&acc_empty[b], Shape::kEpiWarps);  // the epilogue warps
+            mbar_init(&acc_full[b], 1);  // MMA commit after a tile's last K step
+            // the epilogue warps (of both CTAs of a pair)
+            mbar_init(&acc_empty[b], (PAIR ? 2 : 1) * Shape::kEpiWarps);
         }
         mbar_init(mma_done, 1);  // the MMA warp's last commit
         *abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == 1) tmem_alloc(tmem_slot, a.tmem_cols);
+    if (warp == 1) {
+        if (PAIR)
+            tmem_alloc_pair(tmem_slot, a.tmem_cols);
+        else
+            tmem_alloc(tmem_slot, a.tmem_cols);
+    }
     tc_fence_before();
     __syncthreads();
+    if (PAIR) cluster_sync();  // the other CTA's barriers exist before anything arrives on them
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const uint32_t sf_col0 = (uint32_t)(a.nacc * tpi * a.BN);  // scale factors after the accumulators
@@ -543,10 +696,16 @@ __global__ void __launch_bounds__(NT, GemmShape<NT>::kCtasPerSm)
     // the asynchronous operations.
     if (warp == 0) {
         // ------------------------------------------------------- tensor copies
+        const uint32_t full_lead = PAIR ? mapa_shared(full, 0u) : 0u;  // the even CTA's full[0]
         int it = 0, s = 0;  // stages issued; slot of stage it
         uint32_t ph = 0;    // phase parity of slot s's use by stage it
         bool run = true;
-        for (JobIter J(a, nu); run && J.valid(); J.next()) {
+        for (JobIter J(a, nu, first, stride); run && J.valid(); J.next()) {
+            // this CTA's A row tile, and (pairs) whether it exists
+            const int mta = J.mt + rank;
+            const bool has_a = !PAIR || mta < a.nmt;
+            // B: a pair's CTAs take the first and second half of the tile's MMA columns
+            const int brow = J.row0 + J.n0() + (PAIR ? rank * (J.nmma() / 2) : 0);
             for (int kt = 0; kt < a.nkt; kt++, it++) {
                 int okl = 1;
                 if (lane == 0) okl = mbar_wait_or_abort(&empty[s], ph ^ 1u, a.st, 0x500u + s, abort_flag);
@@ -561,47 +720,72 @@ __global__ void __launch_bounds__(NT, GemmShape<NT>::kCtasPerSm)
                 // experts or are out of range and zero; the MMA does not read them)
                 // scale factors: the item's row tiles of A (adjacent in the plane) and
                 // the column tile's atoms of B, each one contiguous block
-                const uint32_t a_tiles = (uint32_t)min(tpi, a.nmt - J.mt);
-                const int brow = J.row0 + J.n0();
-                if (FP4) {
+                const uint32_t a_tiles = PAIR ? (has_a ? 1u : 0u) : (uint32_t)min(tpi, a.nmt - J.mt);
+                if (PAIR) {
+                    // A pair: both CTAs copy the same boxes (A rows, their half of B's
+                    // rows, A's scale atoms, all of B's scales) as tensors, counted on the
+                    // even CTA's barrier, which expects the bytes of both.  Boxes past the
+                    // end of a tensor (the odd CTA's A tile beyond the expert's last, the
+                    // scales of the next K tile) arrive zero-filled and are counted whole.
+                    const uint32_t fbar = full_lead + 8u * (uint32_t)s;
+                    const uint32_t sfbk = sfb_stage_bytes(nsfb);  // per 128-K tile
+                    const int n2 = FP4 ? min(2, a.nkt_sf - 2 * kt) : 1;
+                    const uint32_t tx = FP4 ? (uint32_t)(kTileM * kTileK + a.bbox * kTileK) + (uint32_t)n2 * 512u + 2u * sfbk
+                                            : (uint32_t)(kTileM * kTileK / 2 + a.bbox * kTileK) + 512u + sfbk;
+                    if (elect_one()) {
+                        if (rank == 0) mbar_arrive_expect_tx(&full[s], 2u * tx);
+                        tma_load_3d_pair(sA + (size_t)s * kTileM * kTileK, &tmA, kt * kTileK, mta * kTileM, J.e, fbar);
+                        tma_load_2d_pair(sB + (size_t)s * a.bsr * kTileK, &tmB, kt * kTileK, brow, fbar);
+                        const int kt0 = FP4 ? 2 * kt : kt;  // first 128-K tile of the stage
+                        for (int j = 0; j < n2; j++)
+                            tma_load_3d_pair(sSFA + (size_t)s * (FP4 ? 1024 : 512) + 512 * j, &tmSA, 0,
+                                             (kt0 + j) * a.nmt + mta, J.e, fbar);
+                        // one box of B's scale rows: both 128-K tiles of the stage with FP4 rows
+                        tma_load_2d_pair(sSFB + (size_t)s * (FP4 ? 2 : 1) * sfbk, &tmSB, 0, J.tile() * a.nkt_sf + kt0,
+                                         fbar);
+                    }
+                } else if (FP4) {
                     // packed operands, 256 K (128 bytes) per stage: both boxes arrive whole
                     // (parts past the end of K are zero-filled and counted); one or two
                     // 128-K scale tiles (the last stage of an odd count has one)
                     const int n2 = min(2, a.nkt_sf - 2 * kt);
                     const uint32_t sfbk = sfb_stage_bytes(nsfb);  // per 128-K tile
-                    const int brows = a.bbox == a.BN ? a.BN : (J.nn() + 15) / 16 * 16;  // B rows copied
-                    const uint32_t tx =
-                        (uint32_t)(tpi * kTileM * kTileK + brows * kTileK) + (uint32_t)n2 * (512u + sfbk);
+                    const int brows =
+                        PAIR ? a.bbox : (a.bbox == a.BN ? a.BN : (J.nn() + 15) / 16 * 16);  // B rows copied
+                    const uint32_t tx = (uint32_t)(tpi * kTileM * kTileK + brows * kTileK) +
+                                        (uint32_t)n2 * ((has_a ? 512u : 0u) + sfbk);
                     const uint8_t *sfa_src =
-                        a.pool + (uint64_t)J.e * a.rec + a.a_sf_off + ((uint64_t)(2 * kt) * a.nmt + J.mt) * 512;
+                        a.pool + (uint64_t)J.e * a.rec + a.a_sf_off + ((uint64_t)(2 * kt) * a.nmt + mta) * 512;
                     const uint8_t *sfb_src = a.bscale + sf_tile_word(J.tile(), a.nkt_sf, nsfb, 2 * kt, 0);
                     if (elect_one()) {
                         mbar_arrive_expect_tx(&full[s], tx);
-                        tma_load_3d(sA + (size_t)s * kTileM * kTileK, &tmA, kt * kTileK, J.mt * kTileM, J.e, &full[s]);
+                        tma_load_3d(sA + (size_t)s * kTileM * kTileK, &tmA, kt * kTileK, mta * kTileM, J.e, &full[s]);
                         for (int c = 0; c < brows; c += a.bbox)
                             tma_load_2d(sB + (size_t)s * a.bsr * kTileK + (size_t)c * kTileK, &tmB, kt * kTileK,
                                         brow + c, &full[s]);
-                        for (int j = 0; j < n2; j++)  // the two K tiles' A blocks are nmt blocks apart
-                            bulk_g2s_l2(sSFA + (size_t)s * 1024 + 512 * j, sfa_src + (size_t)j * a.nmt * 512, 512u,
-                                        &full[s]);
+                        if (has_a)
+                            for (int j = 0; j < n2; j++)  // the two K tiles' A blocks are nmt blocks apart
+                                bulk_g2s_l2(sSFA + (size_t)s * 1024 + 512 * j, sfa_src + (size_t)j * a.nmt * 512,
+                                            512u, &full[s]);
                         // the n2 K tiles' atoms (or interleaved 1 KB two-atom blocks) are adjacent
                         bulk_g2s_l2(sSFB + (size_t)s * 2 * sfbk, sfb_src, (uint32_t)n2 * sfbk, &full[s]);
                     }
                 } else {
-                    const int brows = a.bbox == a.BN ? a.BN : (J.nn() + 15) / 16 * 16;  // B rows copied
+                    const int brows =
+                        PAIR ? a.bbox : (a.bbox == a.BN ? a.BN : (J.nn() + 15) / 16 * 16);  // B rows copied
                     const uint32_t tx =
                         (uint32_t)(tpi * kTileM * kTileK / 2 + brows * kTileK) + a_tiles * 512u + sfb_stage_bytes(nsfb);
                     const uint8_t *sfa_src =
-                        a.pool + (uint64_t)J.e * a.rec + a.a_sf_off + ((uint64_t)kt * a.nmt + J.mt) * 512;
+                        a.pool + (uint64_t)J.e * a.rec + a.a_sf_off + ((uint64_t)kt * a.nmt + mta) * 512;
                     const uint8_t *sfb_src = a.bscale + sf_tile_word(J.tile(), a.nkt, nsfb, kt, 0);
                     if (elect_one()) {
                         mbar_arrive_expect_tx(&full[s], tx);
-                        tma_load_3d(sA + (size_t)s * tpi * kTileM * kTileK, &tmA, kt * kTileK, J.mt * kTileM, J.e,
+                        tma_load_3d(sA + (size_t)s * tpi * kTileM * kTileK, &tmA, kt * kTileK, mta * kTileM, J.e,
                                     &full[s]);
                         for (int c = 0; c < brows; c += a.bbox)
                             tma_load_2d(sB + (size_t)s * a.bsr * kTileK + (size_t)c * kTileK, &tmB, kt * kTileK,
                                         brow + c, &full[s]);
-                        bulk_g2s_l2(sSFA + (size_t)s * tpi * 512, sfa_src, a_tiles * 512u, &full[s]);
+                        if (a_tiles > 0) bulk_g2s_l2(sSFA + (size_t)s * tpi * 512, sfa_src, a_tiles * 512u, &full[s]);
                         bulk_g2s_l2(sSFB + (size_t)s * sfb_stage_bytes(nsfb), sfb_src, sfb_stage_bytes(nsfb), &full[s]);
                     }
                 }
@@ -618,10 +802,12 @@ __global__ void __launch_bounds__(NT, GemmShape<NT>::kCtasPerSm)
         // The issue of a stage is a chain of dependent steps (wait, broadcast, scale
         // copies, MMAs, commit), so the warp first asks which of the next few stages
         // have landed (lane i polls stage kt + i, one vote) and issues all of those in
-        // one go; the abort flag is read only while a stage is still outstanding.
+        // one go; the abort flag is read only while a stage is still outstanding.  In a
+        // pair the even CTA issues for both (its barrier counts both CTAs' copies); the
+        // odd CTA's MMA warp only waits for the last commit.
         int jb = 0, s = 0;  // tiles; slot of the next stage
         uint32_t ph = 0;    // its phase parity
-        bool run = true;
+        bool run = !PAIR || rank == 0;
         // Descriptors of slot 0, built once: a stage's descriptors add the stage's
         // offset in 16-byte units to the start-address field (shared addresses stay
         // below 2^18, so the 14-bit field never carries into the next one).
@@ -635,17 +821,21 @@ __global__ void __launch_bounds__(NT, GemmShape<NT>::kCtasPerSm)
         const uint32_t sfb_rg = nsfb == 1 ? 128u : 256u;
         const uint64_t sfbdesc0 = smem_desc(smem_u32(sSFB), sfb_rg, sfb_rg, kSwizzleNone);
         const int nlook = min(4, ns);  // stages polled at once (never past the ring)
-        for (JobIter J(a, nu); run && J.valid(); J.next(), jb++) {
-            const int nmma = (J.nn() + 15) / 16 * 16;
+        const int mma_m = PAIR ? 2 * kTileM : kTileM;
+        for (JobIter J(a, nu, first, stride); run && J.valid(); J.next(), jb++) {
+            const int nmma = J.nmma();
             // mxf8f6f4: + ks * kIdescSfStep for K step ks; mxf4: + kIdescSf2 for odd ks
-            const uint32_t idesc0 = FP4 ? idesc_mxf4(nmma) : idesc_mxf8f6f4(nmma, 0);
+            const uint32_t idesc0 = FP4 ? idesc_mxf4(nmma, mma_m) : idesc_mxf8f6f4(nmma, 0, mma_m);
             // accumulator buffer of tile jb and its use count
             const int buf = a.nacc == 2 ? (jb & 1) : 0;
             const uint32_t use = a.nacc == 2 ? (uint32_t)(jb >> 1) : (uint32_t)jb;
-            // the epilogue has finished with this accumulator (nacc tiles ago)
+            // the epilogue has finished with this accumulator (nacc tiles ago; in a pair,
+            // the epilogues of both CTAs)
             int okl = 1;
-            if (lane == 0) okl = mbar_wait_or_abort(&acc_empty[buf], (use & 1u) ^ 1u, a.st, 0x680u + buf,
-                                                    abort_flag);
+            if (lane == 0)
+                okl = PAIR ? mbar_wait_cluster_or_abort(&acc_empty[buf], (use & 1u) ^ 1u, a.st, 0x680u + buf,
+                                                        abort_flag)
+                           : mbar_wait_or_abort(&acc_empty[buf], (use & 1u) ^ 1u, a.st, 0x680u + buf, abort_flag);
             if (!__shfl_sync(0xffffffffu, okl, 0)) {
                 if (lane == 0) *abort_flag = 1;
                 break;
@@ -689,37 +879,66 @@ __global__ void __launch_bounds__(NT, GemmShape<NT>::kCtasPerSm)
                             const int n2 = min(2, a.nkt_sf - 2 * (kt + q));
                             const uint32_t sfb_t4 = sfa_t + 8u, bw = 4u * (uint32_t)nsfb;
                             for (int j = 0; j < n2; j++) {
-                                tc_cp_sf(sfa_t + 4u * j, sfad + (uint64_t)(32 * j));
-                                if (nsfb == 1) {
-                                    tc_cp_sf(sfb_t4 + 4u * j, sfbd + (uint64_t)(32 * j));
-                                } else {
-                                    // the two atoms of the 1 KB block: rows 128 bytes apart in it
-                                    tc_cp_sf(sfb_t4 + 8u * j, sfbd + (uint64_t)(64 * j));
-                                    tc_cp_sf(sfb_t4 + 8u * j + 4u, sfbd + (uint64_t)(64 * j + 8));
+                                if (PAIR)
+                                    tc_cp_sf_pair(sfa_t + 4u * j, sfad + (uint64_t)(32 * j));
+                                else
+                                    tc_cp_sf(sfa_t + 4u * j, sfad + (uint64_t)(32 * j));
+                                for (int b = 0; b < nsfb; b++) {
+                                    // one atom, or the two atoms of the 1 KB block (rows 128 bytes apart)
+                                    const uint64_t d = nsfb == 1 ? sfbd + (uint64_t)(32 * j)
+                                                                 : sfbd + (uint64_t)(64 * j + 8 * b);
+                                    if (PAIR)
+                                        tc_cp_sf_pair(sfb_t4 + bw * j + 4u * b, d);
+                                    else
+                                        tc_cp_sf(sfb_t4 + bw * j + 4u * b, d);
                                 }
                             }
-                            for (int ks = 0; ks < 2 * n2; ks++)
-                                tc_mma_f4(acc, ad0 + (uint64_t)(2 * ks), bd0 + (uint64_t)(2 * ks),
-                                          idesc0 + ((ks & 1) ? kIdescSf2 : 0u), sfa_t + 4u * (ks >> 1),
-                                          sfb_t4 + bw * (ks >> 1), (kt + q > 0 || ks > 0) ? 1u : 0u);
+                            for (int ks = 0; ks < 2 * n2; ks++) {
+                                const uint32_t id = idesc0 + ((ks & 1) ? kIdescSf2 : 0u);
+                                const uint32_t accum = (kt + q > 0 || ks > 0) ? 1u : 0u;
+                                if (PAIR)
+                                    tc_mma_f4_pair(acc, ad0 + (uint64_t)(2 * ks), bd0 + (uint64_t)(2 * ks), id,
+                                                   sfa_t + 4u * (ks >> 1), sfb_t4 + bw * (ks >> 1), accum);
+                                else
+                                    tc_mma_f4(acc, ad0 + (uint64_t)(2 * ks), bd0 + (uint64_t)(2 * ks), id,
+                                              sfa_t + 4u * (ks >> 1), sfb_t4 + bw * (ks >> 1), accum);
+                            }
                         } else {
-                            for (int t = 0; t < tpi; t++)
-                                tc_cp_sf(sfa_t + 4u * t, sfad + (uint64_t)(32 * t));  // 512 B apart
-                            tc_cp_sf(sfb_t, sfbd);
-                            if (nsfb == 2) tc_cp_sf(sfb_t + 4u, sfbd + 8u);  // the block's second atom
+                            for (int t = 0; t < tpi; t++) {
+                                if (PAIR)
+                                    tc_cp_sf_pair(sfa_t + 4u * t, sfad + (uint64_t)(32 * t));
+                                else
+                                    tc_cp_sf(sfa_t + 4u * t, sfad + (uint64_t)(32 * t));  // 512 B apart
+                            }
+                            for (int b = 0; b < nsfb; b++) {
+                                // one atom, or the two atoms of the 1 KB block (rows 128 bytes apart)
+                                if (PAIR)
+                                    tc_cp_sf_pair(sfb_t + 4u * b, sfbd + (uint64_t)(8 * b));
+                                else
+                                    tc_cp_sf(sfb_t + 4u * b, sfbd + (uint64_t)(8 * b));
+                            }
                             for (int t = 0; t < tpi; t++) {
                                 // tile t: rows 128t.. of the stage's A (16 KB apart), accumulator columns t*BN..
                                 const uint64_t adt = ad0 + (uint64_t)(1024 * t);
 #pragma unroll
                                 for (int ks = 0; ks < kTileK / 32; ks++) {
                                     // K step ks: 32 bytes further along both operands' rows
-                                    tc_mma(acc + (uint32_t)(t * a.BN), adt + (uint64_t)(2 * ks),
-                                           bd0 + (uint64_t)(2 * ks), idesc0 + (uint32_t)ks * kIdescSfStep,
-                                           sfa_t + 4u * t, sfb_t, (kt + q > 0 || ks > 0) ? 1u : 0u);
+                                    const uint32_t id = idesc0 + (uint32_t)ks * kIdescSfStep;
+                                    const uint32_t accum = (kt + q > 0 || ks > 0) ? 1u : 0u;
+                                    if (PAIR)
+                                        tc_mma_pair(acc + (uint32_t)(t * a.BN), adt + (uint64_t)(2 * ks),
+                                                    bd0 + (uint64_t)(2 * ks), id, sfa_t + 4u * t, sfb_t, accum);
+                                    else
+                                        tc_mma(acc + (uint32_t)(t * a.BN), adt + (uint64_t)(2 * ks),
+                                               bd0 + (uint64_t)(2 * ks), id, sfa_t + 4u * t, sfb_t, accum);
                                 }
                             }
                         }
-                        tc_commit(&empty[sq]);  // frees the stage when these MMAs have read it
+                        // frees the stage (in both CTAs of a pair) when these MMAs have read it
+                        if (PAIR)
+                            tc_commit_pair(&empty[sq]);
+                        else
+                            tc_commit(&empty[sq]);
                         if (++sq == ns) sq = 0;
                     }
                 }
@@ -731,12 +950,25 @@ __global__ void __launch_bounds__(NT, GemmShape<NT>::kCtasPerSm)
                     ph ^= 1u;
                 }
             }
-            if (elect_one()) tc_commit(&acc_full[buf]);  // the accumulator is complete (or as far as it got)
+            // the accumulator is complete (or as far as it got)
+            if (elect_one()) {
+                if (PAIR)
+                    tc_commit_pair(&acc_full[buf]);
+                else
+                    tc_commit(&acc_full[buf]);
+            }
             __syncwarp();
         }
         // every MMA this warp issued has finished before TMEM can be released (also
         // after an abort, when the epilogue may not wait for the last accumulator)
-        if (elect_one()) tc_commit(mma_done);
+        if (!PAIR || rank == 0) {
+            if (elect_one()) {
+                if (PAIR)
+                    tc_commit_pair(mma_done);
+                else
+                    tc_commit(mma_done);
+            }
+        }
         __syncwarp();
         if (lane == 0) mbar_wait(mma_done, 0u, a.st, 0x6c0u);
         __syncwarp();
@@ -744,41 +976,62 @@ __global__ void __launch_bounds__(NT, GemmShape<NT>::kCtasPerSm)
         // ------------------------------------------------------- epilogue
         const int ew = warp & 3, wg = (warp - Shape::kEpiFirst) >> 2;
         float *amax_g = amax_x + 64 * wg;
+        // a pair's odd CTA reports a drained accumulator to the even CTA's barrier
+        const uint32_t acc_empty_r = PAIR ? mapa_shared(acc_empty, 0u) : 0u;
         int jb = 0;
-        for (JobIter J(a, nu); J.valid(); J.next(), jb++) {
+        for (JobIter J(a, nu, first, stride); J.valid(); J.next(), jb++) {
             const int buf = a.nacc == 2 ? (jb & 1) : 0;
             const uint32_t use = a.nacc == 2 ? (uint32_t)(jb >> 1) : (uint32_t)jb;
-            const int nn = J.nn(), nmma = (nn + 15) / 16 * 16;
+            const int nn = J.nn(), nmma = J.nmma();
             bool okl = !*(volatile int *)abort_flag && mbar_wait(&acc_full[buf], use & 1u, a.st, 0x800u + buf);
             if (!okl) *abort_flag = 1;
             const bool ok = __all_sync(0xffffffffu, okl);  // warp-uniform for the .sync.aligned loads
             tc_fence_after();
-            for (int t = 0; t < tpi; t++) {
-                if (J.mt + t >= a.nmt) break;  // a half item past the expert's A rows (uniform)
+            for (int t = 0; t < (PAIR ? 1 : tpi); t++) {
+                const int mt = J.mt + (PAIR ? rank : t);
+                if (mt >= a.nmt) break;  // a half item past the expert's A rows (uniform)
                 const uint32_t lane_base =
                     tmem + (uint32_t)((buf * tpi + t) * a.BN) + ((uint32_t)(32 * ew) << 16);
                 if (FP4 && a.nparts == 5)
-                    epilogue_split5_f4(a, lane_base, ok, nn, nmma, J.mt + t, J.row0, J.n0(), J.tile(), ew, wg,
+                    epilogue_split5_f4(a, lane_base, ok, nn, nmma, mt, J.row0, J.n0(), J.tile(), ew, wg,
                                        Shape::kWarpGroups, lane, amax_g);
                 else
-                    epilogue_mx1<FP4>(a, lane_base, ok, nn, nmma, J.mt + t, J.row0, J.n0(), J.tile(), ew, wg,
+                    epilogue_mx1<FP4>(a, lane_base, ok, nn, nmma, mt, J.row0, J.n0(), J.tile(), ew, wg,
                                       Shape::kWarpGroups, lane, amax_g);
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&acc_empty[buf]);
+            if (lane == 0) {
+                if (PAIR && rank == 1)
+                    mbar_arrive_cluster(acc_empty_r + (uint32_t)(8 * buf));
+                else
+                    mbar_arrive(&acc_empty[buf]);
+            }
             // no early exit: after an abort the waits are skipped, and both warps of
             // each pair run the same sequence of named barriers to the end
         }
     }
-    // nothing may still be in flight when TMEM is released and the CTA exits
+    // nothing may still be in flight when TMEM is released and the CTA exits: this
+    // CTA's copies (a pair's odd CTA counts its copies on the even CTA's barrier; they
+    // have landed once the MMAs that read them have committed onto its own stages)
     if (warp == 0 && lane == 0) {
-        for (int it = max(0, it_issued - ns); it < it_issued; it++)
-            mbar_wait(&full[it % ns], (uint32_t)(it / ns) & 1u, a.st, 0x900u);
+        if (!PAIR || rank == 0)
+            for (int it = max(0, it_issued - ns); it < it_issued; it++)
+                mbar_wait(&full[it % ns], (uint32_t)(it / ns) & 1u, a.st, 0x900u);
+        if (PAIR)
+            for (int it = max(0, it_issued - ns); it < it_issued; it++)
+                mbar_wait(&empty[it % ns], (uint32_t)(it / ns) & 1u, a.st, 0x940u);
     }
+    tc_fence_before();
     __syncthreads();
+    if (PAIR) cluster_sync();  // both CTAs are done with TMEM and with each other's barriers
     tc_fence_after();
-    if (warp == 1) tmem_dealloc(tmem, a.tmem_cols);
+    if (warp == 1) {
+        if (PAIR)
+            tmem_dealloc_pair(tmem, a.tmem_cols);
+        else
+            tmem_dealloc(tmem, a.tmem_cols);
+    }
 }
 
 // ------------------------------------------------------------- tensor maps
@@ -836,6 +1089,22 @@ cudaError_t make_map_b(CUtensorMap *m, const void *base, int K, int P, int box_r
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// Scale factors as 32-bit words for a pair's tensor copies.  A: the pool's tensor-core
+// scale plane of each expert record, [E][rows][128 words] (rows = K tiles x row tiles,
+// one 512-byte atom each); B: the tile-ordered activation scales, [rows][words] (rows
+// = column tiles x K tiles, words = 128 per atom).  Boxes of box_rows whole rows.
+cudaError_t make_map_sf(CUtensorMap *m, const void *base, int words, int rows, int E, uint64_t rec, int box_rows) {
+    const int rank = E > 1 ? 3 : 2;
+    cuuint64_t dims[3] = {(cuuint64_t)words, (cuuint64_t)rows, (cuuint64_t)(E > 1 ? E : 1)};
+    cuuint64_t strides[2] = {(cuuint64_t)words * 4u, rec};
+    cuuint32_t box[3] = {(cuuint32_t)words, (cuuint32_t)box_rows, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, rank, const_cast<void *>(base), dims, strides, box, es,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 uint32_t pow2_at_least(uint32_t v) {
     uint32_t p = 32;
     while (p < v) p <<= 1;
@@ -849,6 +1118,60 @@ PerDevice g_smem_set_384(0);
 PerDevice g_smem_set_192(0);
 PerDevice g_smem_set_384f4(0);
 PerDevice g_smem_set_192f4(0);
+PerDevice g_smem_set_pair(0);
+PerDevice g_smem_set_pairf4(0);
+std::atomic<int> g_cta_pairs{2};  // moe_grouped_set_cta_pairs: 0 never, 1 always, 2 MXFP8 rows only
+PerDevice g_pair_clusters(0);    // co-resident CTA pairs of the paired kernel, MXFP8 rows (-1: none)
+PerDevice g_pair_clusters_f4(0); // ... MXFP4 rows
+
+// Launch configuration of the paired kernel: clusters of two CTAs of 384 threads.
+inline cudaLaunchConfig_t pair_config(cudaLaunchAttribute *attr, int pairs, size_t smem, cudaStream_t stream) {
+    cudaLaunchConfig_t cfg = {};
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(2 * pairs);
+    cfg.blockDim = dim3(384);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cfg;
+}
+
+// CTA pairs of the paired kernel that can be resident at once with `smem` bytes each
+// (one CTA per SM at the sizes used), 0 if none; the persistent grid takes at most
+// this many.  The kernel's dynamic shared-memory attribute must already allow `smem`.
+template <bool FP4>
+int pair_capacity(size_t smem) {
+    int dev = 0;
+    if (current_device(&dev) != cudaSuccess) return 0;
+    PerDevice &cache = FP4 ? g_pair_clusters_f4 : g_pair_clusters;
+    int pairs = cache.v[dev].load(std::memory_order_relaxed);
+    if (pairs == 0) {
+        int sms = 0;
+        if (device_attr(cudaDevAttrMultiProcessorCount, g_sms, &sms) != cudaSuccess) return 0;
+        cudaLaunchAttribute attr[1];
+        const cudaLaunchConfig_t cfg = pair_config(attr, sms / 2, smem, nullptr);
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, grouped_gemm_kernel<384, FP4, true>, &cfg) != cudaSuccess || n <= 0) {
+            (void)cudaGetLastError();
+            n = -1;
+        }
+        pairs = n;
+        cache.v[dev].store(pairs, std::memory_order_relaxed);
+    }
+    return pairs > 0 ? pairs : 0;
+}
+
+template <bool FP4>
+cudaError_t launch_pair(const CUtensorMap &mA, const CUtensorMap &mB, const CUtensorMap &mSA, const CUtensorMap &mSB,
+                        const GemmArgs &ga, int pairs, size_t smem, cudaStream_t stream) {
+    cudaLaunchAttribute attr[1];
+    const cudaLaunchConfig_t cfg = pair_config(attr, pairs, smem, stream);
+    return cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<384, FP4, true>, mA, mB, mSA, mSB, ga);
+}
 
 // One grouped GEMM launch (args complete but for the shape fields set here).  The
 // kernel's shape: narrow tiles (BN <= 64, and the gate/up GEMM at BN <= 96) run two
@@ -863,7 +1186,8 @@ PerDevice g_smem_set_192f4(0);
 // only three stages per CTA and made the 32768-token GEMMs 1.34x slower.)  a_k and b_k
 // are K in elements.
 cudaError_t launch_one(GemmArgs ga, const uint8_t *a_base, int a_k, int a_rows, uint64_t a_ld, int E, const uint8_t *b_base,
-                       int b_k, int b_rows, int nexp, const char *trace_name, cudaStream_t stream, bool fp4) {
+                       int b_k, int b_rows, int nexp, int max_tiles, const char *trace_name, cudaStream_t stream,
+                       bool fp4) {
     const int BN = ga.BN, nsfb = ga.nsfb;
     if (fp4 && nsfb > 2) return cudaErrorNotSupported;
     int smem_max = 0, sms = 0;
@@ -873,6 +1197,9 @@ cudaError_t launch_one(GemmArgs ga, const uint8_t *a_base, int a_k, int a_rows, 
     // (FP4: the down GEMM too at BN <= 96, where its K loop is short: 7 stages at I = 1600)
     const bool two = BN <= 64 || (BN <= 96 && (ga.mode == 1 || fp4));
     const int tpi = fp4 || two ? 1 : (BN <= 96 ? 2 : 1);
+    // wide one-part tiles run on CTA pairs (cta_group::2): each SM copies half of B
+    if (ga.pair && (two || tpi != 1 || ga.nparts != 1 || BN < 128 || BN % 32 != 0)) ga.pair = 0;
+    if (ga.pair) ga.bsr = BN / 2;
     const uint32_t smem_cap = two ? (uint32_t)(smem_max / 2 - 1024) : (uint32_t)smem_max;
     const uint32_t tmem_cap = two ? 256u : 512u;
     const uint32_t sf_cols = fp4 ? 8u * tpi + 8u * nsfb : 4u * tpi + 4u * nsfb;
@@ -886,12 +1213,25 @@ cudaError_t launch_one(GemmArgs ga, const uint8_t *a_base, int a_k, int a_rows, 
     const uint32_t tmem_cols = pow2_at_least(tmem_need(ns));
     if (tmem_cols > tmem_cap || smem_need(ns) > smem_cap) return cudaErrorNotSupported;
     const size_t smem = smem_need(ns);
-    if (fp4)
-        e = two ? ensure_dynamic_smem(grouped_gemm_kernel<192, true>, smem, g_smem_set_192f4)
-                : ensure_dynamic_smem(grouped_gemm_kernel<384, true>, smem, g_smem_set_384f4);
+    int pairs = 0;
+    if (ga.pair) {
+        e = fp4 ? ensure_dynamic_smem(grouped_gemm_kernel<384, true, true>, smem, g_smem_set_pairf4)
+                : ensure_dynamic_smem(grouped_gemm_kernel<384, false, true>, smem, g_smem_set_pair);
+        if (e != cudaSuccess) return e;
+        pairs = fp4 ? pair_capacity<true>(smem) : pair_capacity<false>(smem);
+        if (pairs == 0) {
+            // no two SMs can hold a pair: the one-CTA tiles instead
+            ga.pair = 0;
+            ga.bsr = BN;
+            return launch_one(ga, a_base, a_k, a_rows, a_ld, E, b_base, b_k, b_rows, nexp, max_tiles, trace_name, stream,
+                              fp4);
+        }
+    } else if (fp4)
+        e = two ? ensure_dynamic_smem(grouped_gemm_kernel<192, true, false>, smem, g_smem_set_192f4)
+                : ensure_dynamic_smem(grouped_gemm_kernel<384, true, false>, smem, g_smem_set_384f4);
     else
-        e = two ? ensure_dynamic_smem(grouped_gemm_kernel<192, false>, smem, g_smem_set_192)
-                : ensure_dynamic_smem(grouped_gemm_kernel<384, false>, smem, g_smem_set_384);
+        e = two ? ensure_dynamic_smem(grouped_gemm_kernel<192, false, false>, smem, g_smem_set_192)
+                : ensure_dynamic_smem(grouped_gemm_kernel<384, false, false>, smem, g_smem_set_384);
     if (e != cudaSuccess) return e;
     ga.ns = ns;
     ga.tpi = tpi;
@@ -899,12 +1239,19 @@ cudaError_t launch_one(GemmArgs ga, const uint8_t *a_base, int a_k, int a_rows, 
     // narrow tiles copy B in 16-row boxes, only the rows the tile's MMAs read: verify
     // tiles (several parts per row) hold a few rows in a box sized for 32, and prefill
     // tiles up to 64 columns are sized for the expert rows' spread
-    ga.bbox = (ga.nparts > 1 || BN <= 64) ? 16 : BN;
-    if (ga.bsr != BN && ga.bbox != 16) return cudaErrorInvalidValue;
+    ga.bbox = ga.pair ? BN / 2 : ((ga.nparts > 1 || BN <= 64) ? 16 : BN);
+    if (!ga.pair && ga.bsr != BN && ga.bbox != 16) return cudaErrorInvalidValue;
     ga.tmem_cols = tmem_cols;
     ga.nkt_sf = a_k / kTileK;
     ga.nkt = fp4 ? (ga.nkt_sf + 1) / 2 : ga.nkt_sf;
-    CUtensorMap mA, mB;
+    CUtensorMap mA, mB, mSA = {}, mSB = {};
+    if (ga.pair) {
+        // the scales as tensors: A's plane in each record, B's tile-ordered blocks
+        if ((e = make_map_sf(&mSA, ga.pool + ga.a_sf_off, 128, ga.nkt_sf * ga.nmt, E, ga.rec, 1)) != cudaSuccess)
+            return e;
+        if ((e = make_map_sf(&mSB, ga.bscale, 128 * nsfb, max_tiles * ga.nkt_sf, 1, 0, fp4 ? 2 : 1)) != cudaSuccess)
+            return e;
+    }
     if (fp4) {
         if ((e = make_map_a4(&mA, a_base, a_k / 2, a_rows, E, a_ld, ga.rec, kTileM)) != cudaSuccess) return e;
         if ((e = make_map_b(&mB, b_base, b_k / 2, b_rows, ga.bbox)) != cudaSuccess) return e;
@@ -912,26 +1259,31 @@ cudaError_t launch_one(GemmArgs ga, const uint8_t *a_base, int a_k, int a_rows, 
         if ((e = make_map_a(&mA, a_base, a_k, a_rows, E, a_ld, ga.rec, tpi * kTileM)) != cudaSuccess) return e;
         if ((e = make_map_b(&mB, b_base, b_k, b_rows, ga.bbox)) != cudaSuccess) return e;
     }
-    const int items = nexp * ((ga.nmt + tpi - 1) / tpi);
+    const int items = nexp * ((ga.nmt + (ga.pair ? 2 : tpi) - 1) / (ga.pair ? 2 : tpi));
     TraceScope trace_scope(trace_name, stream);
-    if (fp4) {
+    if (ga.pair) {
+        pairs = std::min(pairs, items);
+        e = fp4 ? launch_pair<true>(mA, mB, mSA, mSB, ga, pairs, smem, stream)
+                : launch_pair<false>(mA, mB, mSA, mSB, ga, pairs, smem, stream);
+        if (e != cudaSuccess) return e;
+    } else if (fp4) {
         // (the multi-token decode's chain of kernels launches each one early)
         if (two && ga.nparts > 1)
-            e = launch_pdl(grouped_gemm_kernel<192, true>, dim3(std::min(2 * sms, items)), dim3(192), smem, stream,
-                           mA, mB, ga);
+            e = launch_pdl(grouped_gemm_kernel<192, true, false>, dim3(std::min(2 * sms, items)), dim3(192), smem, stream,
+                           mA, mB, mSA, mSB, ga);
         else if (two)
-            grouped_gemm_kernel<192, true><<<std::min(2 * sms, items), 192, smem, stream>>>(mA, mB, ga);
+            grouped_gemm_kernel<192, true, false><<<std::min(2 * sms, items), 192, smem, stream>>>(mA, mB, mSA, mSB, ga);
         else if (ga.nparts > 1)
-            e = launch_pdl(grouped_gemm_kernel<384, true>, dim3(std::min(sms, items)), dim3(384), smem, stream, mA,
-                           mB, ga);
+            e = launch_pdl(grouped_gemm_kernel<384, true, false>, dim3(std::min(sms, items)), dim3(384), smem, stream, mA,
+                           mB, mSA, mSB, ga);
         else
-            grouped_gemm_kernel<384, true><<<std::min(sms, items), 384, smem, stream>>>(mA, mB, ga);
+            grouped_gemm_kernel<384, true, false><<<std::min(sms, items), 384, smem, stream>>>(mA, mB, mSA, mSB, ga);
         if (e != cudaSuccess) return e;
     } else {
         if (two)
-            grouped_gemm_kernel<192, false><<<std::min(2 * sms, items), 192, smem, stream>>>(mA, mB, ga);
+            grouped_gemm_kernel<192, false, false><<<std::min(2 * sms, items), 192, smem, stream>>>(mA, mB, mSA, mSB, ga);
         else
-            grouped_gemm_kernel<384, false><<<std::min(sms, items), 384, smem, stream>>>(mA, mB, ga);
+            grouped_gemm_kernel<384, false, false><<<std::min(sms, items), 384, smem, stream>>>(mA, mB, mSA, mSB, ga);
     }
     return cudaGetLastError();
 }
@@ -939,6 +1291,8 @@ cudaError_t launch_one(GemmArgs ga, const uint8_t *a_base, int a_k, int a_rows, 
 }  // namespace
 
 cudaError_t set_wait_limit_gemm(uint64_t ns) { return set_wait_limit_here(ns); }
+
+void set_cta_pairs(int mode) { g_cta_pairs.store(mode, std::memory_order_relaxed); }
 
 cudaError_t launch_grouped_gemms(const PoolView &v, int T, int k, const int32_t *offsets, const GroupedWs &g,
                                  void *partial, int partial_dtype, StatusWord *st, cudaStream_t stream, int nparts,
@@ -972,6 +1326,10 @@ cudaError_t launch_grouped_gemms(const PoolView &v, int T, int k, const int32_t 
     ga.partial = partial;
     ga.partial_dtype = partial_dtype;
     ga.nparts = nparts;
+    // CTA pairs where they measured faster (MXFP8 rows), or as set; launch_one decides per
+    // GEMM whether the tile shape allows them
+    const int pairs_mode = g_cta_pairs.load(std::memory_order_relaxed);
+    ga.pair = pairs_mode == 1 || (pairs_mode == 2 && !fp4) ? 1 : 0;
     ga.st = st;
     // B rows a stage reserves: all BN, or (five-part rows, known bound) just the columns
     // any tile has, rounded to the 16-row boxes: more pipeline stages fit
@@ -983,8 +1341,8 @@ cudaError_t launch_grouped_gemms(const PoolView &v, int T, int k, const int32_t 
     ga.a_sf_off = v.off_sgu_mma;
     ga.bscale = g.xs;
     ga.nmt = v.nmt_gu;
-    e = launch_one(ga, v.base, v.H, 2 * v.I, (uint64_t)v.ld_gu, v.E, g.xq, v.H, nparts * P, nexp, "gemm_gateup", stream,
-                   fp4);
+    e = launch_one(ga, v.base, v.H, 2 * v.I, (uint64_t)v.ld_gu, v.E, g.xq, v.H, nparts * P, nexp, g.max_tiles,
+                   "gemm_gateup", stream, fp4);
     if (e != cudaSuccess) return e;
 
     // GEMM 2: down (K = Ip, the W_d rows padded with zero codes; h has I columns, the
@@ -993,8 +1351,8 @@ cudaError_t launch_grouped_gemms(const PoolView &v, int T, int k, const int32_t 
     ga.a_sf_off = v.off_sd_mma;
     ga.bscale = g.hs;
     ga.nmt = v.nmt_d;
-    return launch_one(ga, v.base + v.off_d, v.Ip, v.H, (uint64_t)v.ld_d, v.E, g.hq, v.I, nparts * P, nexp, "gemm_down",
-                      stream, fp4);
+    return launch_one(ga, v.base + v.off_d, v.Ip, v.H, (uint64_t)v.ld_d, v.E, g.hq, v.I, nparts * P, nexp, g.max_tiles,
+                      "gemm_down", stream, fp4);
 }
 
 }  // namespace moe

@@ -252,6 +252,7 @@ cudaError_t launch_prescale(const uint16_t *x, int M, int H, uint16_t *out, cuda
 cudaError_t set_wait_limit_decode_fused(uint64_t ns);
 cudaError_t set_wait_limit_gemm(uint64_t ns);
 void set_barrier_extra(unsigned int extra);
+void set_cta_pairs(int mode);  // grouped GEMMs on CTA pairs: 0 never, 1 always, 2 MXFP8 rows only
 
 size_t grouped_workspace_bytes(int E, int H, int I, int T, int k);
 cudaError_t launch_grouped(const PoolView &v, const uint16_t *x, int T, const int32_t *idx, int k,

@@ -79,5 +79,8 @@ def test_host_validation_without_gpu(L):
     assert L.moe_pool_create(ctypes.byref(h), vp((1 << 20) + 8), 1 << 30, 64, 1024, 512) == 1   # alignment
     assert L.moe_pool_create(ctypes.byref(h), vp(1 << 20), 1000, 64, 1024, 512) == 1           # too small
     assert L.moe_combine(None, 0, fake, fake, 1, 16, 1024, None, fake, None) == 1
+    # the grouped GEMMs' tile-shape switch: modes 0..2, anything else rejected; 2 restored
+    assert L.moe_grouped_set_cta_pairs(3) == 1 and L.moe_grouped_set_cta_pairs(-1) == 1
+    assert L.moe_grouped_set_cta_pairs(0) == 0 and L.moe_grouped_set_cta_pairs(2) == 0
     for code in range(8):
         assert moe.status_string(code) not in ("", "unknown status")

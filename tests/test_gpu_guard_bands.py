@@ -109,12 +109,24 @@ def test_decode_writes_stay_inside(shape, M):
     g.check(f"moe_expert_forward_decode {shape} M={M}, second call")
 
 
-@pytest.mark.parametrize("act_mode,partial_dtype", [(moe.MOE_ACT_MXFP8, moe.MOE_PARTIAL_F32),
-                                                    (moe.MOE_ACT_MXFP8, moe.MOE_PARTIAL_BF16),
-                                                    (moe.MOE_ACT_MXFP4, moe.MOE_PARTIAL_F32)])
-def test_grouped_and_combine_writes_stay_inside(act_mode, partial_dtype):
-    s = synth.TINY
-    T = 48
+@pytest.mark.parametrize("act_mode,partial_dtype,pairs", [(moe.MOE_ACT_MXFP8, moe.MOE_PARTIAL_F32, False),
+                                                          (moe.MOE_ACT_MXFP8, moe.MOE_PARTIAL_BF16, False),
+                                                          (moe.MOE_ACT_MXFP4, moe.MOE_PARTIAL_F32, False),
+                                                          (moe.MOE_ACT_MXFP8, moe.MOE_PARTIAL_F32, True),
+                                                          (moe.MOE_ACT_MXFP4, moe.MOE_PARTIAL_BF16, True)])
+def test_grouped_and_combine_writes_stay_inside(act_mode, partial_dtype, pairs):
+    # pairs: 192-column tiles on CTA pairs (16 experts, 1024 tokens x 4 slots)
+    s = synth.Shape(E=16, H=384, I=192, k=4) if pairs else synth.TINY
+    T = 1024 if pairs else 48
+    if pairs:
+        moe.moe_grouped_set_cta_pairs(moe.CTA_PAIRS_ALWAYS)
+    try:
+        _grouped_and_combine(s, T, act_mode, partial_dtype)
+    finally:
+        moe.moe_grouped_set_cta_pairs(moe.CTA_PAIRS_MXFP8)
+
+
+def _grouped_and_combine(s, T, act_mode, partial_dtype):
     pool = moe.Pool(s.E, s.H, s.I)
     moe.moe_pool_fill_synthetic(pool, synth.pool_seed(0))
     Wr = _router(s, synth.router_seed(0))

@@ -40,7 +40,10 @@ def _run(s, T, seed, sample=None, partial_dtype=0, act_mode=1):
     return out, y, ref, xb
 
 
-@pytest.mark.parametrize("E,H,I,k,T", [(16, 256, 128, 4, 64), (24, 384, 192, 8, 96), (64, 1024, 512, 16, 128)])
+# (16, 384, 192, 4, 1024): 256 rows per expert on 192-column tiles (two column tiles per
+# expert), with an odd number of 128-row A tiles in both GEMMs (3 and 3)
+@pytest.mark.parametrize("E,H,I,k,T", [(16, 256, 128, 4, 64), (24, 384, 192, 8, 96), (64, 1024, 512, 16, 128),
+                                       (16, 384, 192, 4, 1024)])
 def test_prefill_small_shapes(E, H, I, k, T):
     s = synth.Shape(E=E, H=H, I=I, k=k)
     out, y, ref, xb = _run(s, T, 500 + E)
@@ -335,7 +338,8 @@ def test_prefill_hot_expert_spans_column_tiles(E, H, I, k, T):
 # step), contractions as kind::mxf4 MMAs (E2M1 x E2M1).
 
 
-@pytest.mark.parametrize("E,H,I,k,T", [(16, 256, 128, 4, 64), (24, 384, 192, 8, 96), (64, 1024, 512, 16, 128)])
+@pytest.mark.parametrize("E,H,I,k,T", [(16, 256, 128, 4, 64), (24, 384, 192, 8, 96), (64, 1024, 512, 16, 128),
+                                       (16, 384, 192, 4, 1024)])
 def test_prefill_mxfp4_small_shapes(E, H, I, k, T):
     s = synth.Shape(E=E, H=H, I=I, k=k)
     seed = 940 + E
@@ -373,3 +377,57 @@ def test_prefill_mxfp4_full_size(T, nsample):
     yg = bf16_to_f64(y)[ref["tokens"]]
     check_close(yg, ref["y"], f"config 4 MXFP4: prefill T={T}, {nsample} sampled tokens", amb=ref["y_amb"],
                 bf16_at=yg)
+
+
+# ------------------------------------------------------- paired-SM tiles
+# moe_grouped_set_cta_pairs(CTA_PAIRS_ALWAYS): one-part tiles of 128+ columns on CTA
+# pairs (tcgen05 cta_group::2, M = 256, each CTA half of the tile's activation rows)
+# with MXFP4 rows too (the default pairs MXFP8 rows only).
+
+
+@pytest.fixture
+def cta_pairs():
+    moe.moe_grouped_set_cta_pairs(moe.CTA_PAIRS_ALWAYS)
+    try:
+        yield
+    finally:
+        moe.moe_grouped_set_cta_pairs(moe.CTA_PAIRS_MXFP8)
+
+
+@pytest.mark.parametrize("act_mode", [1, 2])
+def test_prefill_cta_pairs_small_shape(cta_pairs, act_mode):
+    # 192-column tiles, two per expert; 3 row tiles of A in both GEMMs, so each expert's
+    # last pair has no second tile
+    s = synth.Shape(E=16, H=384, I=192, k=4)
+    T, seed = 1024, 1010 + act_mode
+    out, y, ref, xb = _run(s, T, seed, act_mode=act_mode)
+    assert np.array_equal(out["perm"].cpu().numpy(), ref["perm"])
+    assert np.array_equal(out["offsets"].cpu().numpy(), ref["offsets"])
+    pool = oracle.SyntheticPool(seed, s.E, s.H, s.I)
+    xf = synth.bf16_bits_to_f64(xb)
+    xq = oracle.quant_rows_mxfp8(xf) if act_mode == 1 else oracle.quant_rows_mxfp4(xf)
+    o_ref = oracle.pair_outputs(pool, s.H, s.I, xq, ref["idx"], h_mode=act_mode)
+    part = out["partial"].float().cpu().numpy().astype(np.float64)[out["inv_perm"].cpu().numpy()]
+    p_amb = oracle.pair_ambiguity(pool, s.H, s.I, xq, ref["idx"], fmt=8 if act_mode == 1 else 4)
+    check_close(part.reshape(T, s.k, s.H), o_ref, f"CTA pairs, act_mode {act_mode}: per-pair outputs", amb=p_amb)
+    yg = bf16_to_f64(y)
+    check_close(yg, ref["y"], f"CTA pairs, act_mode {act_mode}: y", amb=ref["y_amb"], bf16_at=yg)
+
+
+def test_prefill_cta_pairs_multiple_column_tiles(cta_pairs):
+    s = synth.TINY
+    out, y, ref, _ = _run(s, 2048, 1020, sample=np.arange(0, 2048, 97))
+    assert np.array_equal(out["perm"].cpu().numpy(), ref["perm"])
+    yg = bf16_to_f64(y)[ref["tokens"]]
+    check_close(yg, ref["y"], "CTA pairs: tiny T=2048, y (sampled)", amb=ref["y_amb"], bf16_at=yg)
+
+
+@pytest.mark.parametrize("act_mode", [1, 2])
+def test_prefill_cta_pairs_full_size(cta_pairs, act_mode):
+    s = synth.FULL
+    T = 8192
+    out, y, ref, _ = _run(s, T, 1030 + act_mode, sample=np.linspace(0, T - 1, 8).astype(np.int64), act_mode=act_mode)
+    assert np.array_equal(out["perm"].cpu().numpy(), ref["perm"])
+    yg = bf16_to_f64(y)[ref["tokens"]]
+    check_close(yg, ref["y"], f"CTA pairs, act_mode {act_mode}: prefill T=8192, 8 sampled tokens",
+                amb=ref["y_amb"], bf16_at=yg)
