@@ -303,8 +303,8 @@ moe_status moe_combine(const void *partial, int partial_dtype, const int32_t *in
  * copies half of B), the odd CTA's tensor copies counted on the even CTA's barrier.
  * mode 0: never (one CTA per 128-row tile); 1: always where the tile allows it;
  * 2 (the default): with MXFP8 rows only.  Measured on a GB300 at 8192 tokens the
- * pairs took the MXFP8 GEMMs 5.78 -> 5.10 ms and the MXFP4 GEMMs 4.57 -> 4.70 ms
- * (32768 tokens: 16.9 -> 17.2 ms), hence the default.  Results agree up to the fp32
+ * pairs took the MXFP8 GEMMs 5.35 -> 4.69 ms and the MXFP4 GEMMs 4.52 -> 4.62 ms
+ * (32768 tokens: 16.4 -> 17.0 ms), hence the default.  Results agree up to the fp32
  * accumulation order of the tensor pipe, which neither shape fixes.
  * MOE_ERR_INVALID_ARG for other modes. */
 moe_status moe_grouped_set_cta_pairs(int mode);

@@ -24,10 +24,10 @@
 // warps drain the other accumulator, so a tile's epilogue overlaps the next tile's
 // MMAs.  Two shapes (GemmShape): one CTA of 12 warps per SM (two epilogue warpgroups)
 // or two CTAs of 6 warps per SM (one), chosen per launch by the tile width.  Wide
-// one-part tiles can also run on CTA pairs (PAIR: a cluster of two CTAs on two SMs,
-// tcgen05 MMAs of cta_group::2 with M = 256 issued by the even CTA; each CTA copies its
-// 128 weight rows and half of the tile's activation rows, and its tensor copies count
-// on the even CTA's barrier).  With five-part MXFP4 activations (nparts = 5, the
+// one-part tiles can also run on CTA pairs (grouped_gemm_pair_kernel: a cluster of two
+// CTAs on two SMs, tcgen05 MMAs of cta_group::2 with M = 256 issued by the even CTA;
+// each CTA copies its 128 weight rows and half of the tile's activation rows, and its
+// tensor copies count on the even CTA's barrier).  With five-part MXFP4 activations (nparts = 5, the
 // multi-token decode) each sorted pair has five B rows whose columns the epilogue sums.
 // Every wait is bounded (MOE_ERR_TIMEOUT), and nothing exits with copies or MMAs in
 // flight.
@@ -569,60 +569,51 @@ struct GemmSmemLayout {
     }
 };
 
-// The work of a CTA (or CTA pair): items i = first, first + stride, ... of the
-// (expert of the union, span 128-row tiles of A) items, span = tpi, or 2 for a pair
-// (first = the pair's index, stride = the number of pairs); each item's columns in
-// tiles of BN.  Every role of both CTAs walks this same sequence.
+// The work of a CTA: items i = blockIdx.x, +gridDim.x, ... of the n_union * nmt
+// (expert of the union, 128-row tile of A) items; each item's columns in tiles of
+// BN.  Every role walks this same sequence.
 struct JobIter {
     const GemmArgs &a;
-    int nu, i, stride, span, nt, ntile, e, mt, row0, nrows, tile0;
-    __device__ JobIter(const GemmArgs &args, int nu_, int first, int stride_)
-        : a(args), nu(nu_), i(first), stride(stride_), span(args.pair ? 2 : args.tpi), nt(0), ntile(0) {
-        load();
-    }
+    int nu, i, nt, ntile, e, mt, row0, nrows, tile0;
+    __device__ JobIter(const GemmArgs &args, int nu_) : a(args), nu(nu_), i((int)blockIdx.x), nt(0), ntile(0) { load(); }
     __device__ void load() {
         ntile = 0;
-        const int nwi = (a.nmt + span - 1) / span;  // items per expert
+        const int nwi = (a.nmt + a.tpi - 1) / a.tpi;  // items per expert
         while (i < nu * nwi) {
             const int u = i / nwi;
-            mt = (i % nwi) * span;  // first 128-row tile of the item
+            mt = (i % nwi) * a.tpi;  // first 128-row tile of the item
             e = a.uexp[u];
             row0 = a.nparts * a.offsets[e];
             nrows = a.nparts * (a.offsets[e + 1] - a.offsets[e]);
             ntile = (nrows + a.BN - 1) / a.BN;
             tile0 = a.tile_off[e];
             if (ntile > 0) break;
-            i += stride;
+            i += (int)gridDim.x;
         }
         nt = 0;
     }
-    __device__ bool valid() const { return i < nu * ((a.nmt + span - 1) / span) && ntile > 0; }
+    __device__ bool valid() const { return i < nu * ((a.nmt + a.tpi - 1) / a.tpi) && ntile > 0; }
     __device__ int n0() const { return nt * a.BN; }
     __device__ int tile() const { return tile0 + nt; }
     // columns of the current tile (at most bsr: a tile with more is reported by the
-    // sort as a bad index and computed only in part; a pair's CTAs hold BN / 2 each)
-    __device__ int nn() const { return min(a.pair ? a.BN : a.bsr, nrows - nt * a.BN); }
-    // MMA width: the columns rounded up to 16
-    __device__ int nmma() const { return (nn() + 15) / 16 * 16; }
+    // sort as a bad index and computed only in part)
+    __device__ int nn() const { return min(a.bsr, nrows - nt * a.BN); }
     __device__ void next() {
         if (++nt >= ntile) {
-            i += stride;
+            i += (int)gridDim.x;
             load();
         }
     }
 };
 
-template <int NT, bool FP4, bool PAIR>
+template <int NT, bool FP4>
 __global__ void __launch_bounds__(NT, GemmShape<NT>::kCtasPerSm)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                        const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
                         const GemmArgs a) {
-    // (tmSA, tmSB: the scale factors of A and B as tensors, used by CTA pairs)
     // launched early (programmatic dependent launch) on the multi-row decode path:
     // wait for the previous kernel, then let the next one launch
     griddep_wait();
     griddep_launch_dependents();
-    static_assert(!PAIR || NT == 384, "CTA pairs use the one-CTA-per-SM shape");
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     // the tensor copies with 128-byte swizzling need 1024-byte aligned tiles
     unsigned char *smem = (unsigned char *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -640,14 +631,8 @@ __global__ void __launch_bounds__(NT, GemmShape<NT>::kCtasPerSm)
     float *amax_x = reinterpret_cast<float *>(smem + L.misc + 16);  // [8 epilogue warps][16 columns]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // a pair's CTAs: rank 0 issues the MMAs, rank 1 holds the second 128 A rows and the
-    // second half of the columns of each item
-    const int rank = PAIR ? (int)cluster_ctarank() : 0;
-    const int first = PAIR ? (int)blockIdx.x / 2 : (int)blockIdx.x;
-    const int stride = PAIR ? (int)gridDim.x / 2 : (int)gridDim.x;
     const int nu = *a.n_union;
-    // the whole CTA (both CTAs of a pair alike), before any barrier
-    if (first >= nu * ((a.nmt + (PAIR ? 2 : tpi) - 1) / (PAIR ? 2 : tpi))) return;
+    if ((int)blockIdx.x >= nu * ((a.nmt + tpi - 1) / tpi)) return;  // the whole CTA, before any barrier
     const int nsfb = a.nsfb;
 
     // The unpacked E2M1 copies write 8 of every 16 bytes of an A tile; keep the
@@ -666,23 +651,16 @@ __global__ void __launch_bounds__(NT, GemmShape<NT>::kCtasPerSm)
             mbar_init(&empty[s], 1);  // MMA commit
         }
         for (int b = 0; b < 2; b++) {
-            mbar_init(&acc_full[b], 1);  // MMA commit after a tile's last K step
-            // the epilogue warps (of both CTAs of a pair)
-            mbar_init(&acc_empty[b], (PAIR ? 2 : 1) * Shape::kEpiWarps);
+            mbar_init(&acc_full[b], 1);   // MMA commit after a tile's last K step
+            mbar_init(&acc_empty[b], Shape::kEpiWarps);  // the epilogue warps
         }
         mbar_init(mma_done, 1);  // the MMA warp's last commit
         *abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == 1) {
-        if (PAIR)
-            tmem_alloc_pair(tmem_slot, a.tmem_cols);
-        else
-            tmem_alloc(tmem_slot, a.tmem_cols);
-    }
+    if (warp == 1) tmem_alloc(tmem_slot, a.tmem_cols);
     tc_fence_before();
     __syncthreads();
-    if (PAIR) cluster_sync();  // the other CTA's barriers exist before anything arrives on them
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const uint32_t sf_col0 = (uint32_t)(a.nacc * tpi * a.BN);  // scale factors after the accumulators
@@ -696,16 +674,10 @@ __global__ void __launch_bounds__(NT, GemmShape<NT>::kCtasPerSm)
     // the asynchronous operations.
     if (warp == 0) {
         // ------------------------------------------------------- tensor copies
-        const uint32_t full_lead = PAIR ? mapa_shared(full, 0u) : 0u;  // the even CTA's full[0]
         int it = 0, s = 0;  // stages issued; slot of stage it
         uint32_t ph = 0;    // phase parity of slot s's use by stage it
         bool run = true;
-        for (JobIter J(a, nu, first, stride); run && J.valid(); J.next()) {
-            // this CTA's A row tile, and (pairs) whether it exists
-            const int mta = J.mt + rank;
-            const bool has_a = !PAIR || mta < a.nmt;
-            // B: a pair's CTAs take the first and second half of the tile's MMA columns
-            const int brow = J.row0 + J.n0() + (PAIR ? rank * (J.nmma() / 2) : 0);
+        for (JobIter J(a, nu); run && J.valid(); J.next()) {
             for (int kt = 0; kt < a.nkt; kt++, it++) {
                 int okl = 1;
                 if (lane == 0) okl = mbar_wait_or_abort(&empty[s], ph ^ 1u, a.st, 0x500u + s, abort_flag);
@@ -720,72 +692,47 @@ __global__ void __launch_bounds__(NT, GemmShape<NT>::kCtasPerSm)
                 // experts or are out of range and zero; the MMA does not read them)
                 // scale factors: the item's row tiles of A (adjacent in the plane) and
                 // the column tile's atoms of B, each one contiguous block
-                const uint32_t a_tiles = PAIR ? (has_a ? 1u : 0u) : (uint32_t)min(tpi, a.nmt - J.mt);
-                if (PAIR) {
-                    // A pair: both CTAs copy the same boxes (A rows, their half of B's
-                    // rows, A's scale atoms, all of B's scales) as tensors, counted on the
-                    // even CTA's barrier, which expects the bytes of both.  Boxes past the
-                    // end of a tensor (the odd CTA's A tile beyond the expert's last, the
-                    // scales of the next K tile) arrive zero-filled and are counted whole.
-                    const uint32_t fbar = full_lead + 8u * (uint32_t)s;
-                    const uint32_t sfbk = sfb_stage_bytes(nsfb);  // per 128-K tile
-                    const int n2 = FP4 ? min(2, a.nkt_sf - 2 * kt) : 1;
-                    const uint32_t tx = FP4 ? (uint32_t)(kTileM * kTileK + a.bbox * kTileK) + (uint32_t)n2 * 512u + 2u * sfbk
-                                            : (uint32_t)(kTileM * kTileK / 2 + a.bbox * kTileK) + 512u + sfbk;
-                    if (elect_one()) {
-                        if (rank == 0) mbar_arrive_expect_tx(&full[s], 2u * tx);
-                        tma_load_3d_pair(sA + (size_t)s * kTileM * kTileK, &tmA, kt * kTileK, mta * kTileM, J.e, fbar);
-                        tma_load_2d_pair(sB + (size_t)s * a.bsr * kTileK, &tmB, kt * kTileK, brow, fbar);
-                        const int kt0 = FP4 ? 2 * kt : kt;  // first 128-K tile of the stage
-                        for (int j = 0; j < n2; j++)
-                            tma_load_3d_pair(sSFA + (size_t)s * (FP4 ? 1024 : 512) + 512 * j, &tmSA, 0,
-                                             (kt0 + j) * a.nmt + mta, J.e, fbar);
-                        // one box of B's scale rows: both 128-K tiles of the stage with FP4 rows
-                        tma_load_2d_pair(sSFB + (size_t)s * (FP4 ? 2 : 1) * sfbk, &tmSB, 0, J.tile() * a.nkt_sf + kt0,
-                                         fbar);
-                    }
-                } else if (FP4) {
+                const uint32_t a_tiles = (uint32_t)min(tpi, a.nmt - J.mt);
+                const int brow = J.row0 + J.n0();
+                if (FP4) {
                     // packed operands, 256 K (128 bytes) per stage: both boxes arrive whole
                     // (parts past the end of K are zero-filled and counted); one or two
                     // 128-K scale tiles (the last stage of an odd count has one)
                     const int n2 = min(2, a.nkt_sf - 2 * kt);
                     const uint32_t sfbk = sfb_stage_bytes(nsfb);  // per 128-K tile
-                    const int brows =
-                        PAIR ? a.bbox : (a.bbox == a.BN ? a.BN : (J.nn() + 15) / 16 * 16);  // B rows copied
-                    const uint32_t tx = (uint32_t)(tpi * kTileM * kTileK + brows * kTileK) +
-                                        (uint32_t)n2 * ((has_a ? 512u : 0u) + sfbk);
+                    const int brows = a.bbox == a.BN ? a.BN : (J.nn() + 15) / 16 * 16;  // B rows copied
+                    const uint32_t tx =
+                        (uint32_t)(tpi * kTileM * kTileK + brows * kTileK) + (uint32_t)n2 * (512u + sfbk);
                     const uint8_t *sfa_src =
-                        a.pool + (uint64_t)J.e * a.rec + a.a_sf_off + ((uint64_t)(2 * kt) * a.nmt + mta) * 512;
+                        a.pool + (uint64_t)J.e * a.rec + a.a_sf_off + ((uint64_t)(2 * kt) * a.nmt + J.mt) * 512;
                     const uint8_t *sfb_src = a.bscale + sf_tile_word(J.tile(), a.nkt_sf, nsfb, 2 * kt, 0);
                     if (elect_one()) {
                         mbar_arrive_expect_tx(&full[s], tx);
-                        tma_load_3d(sA + (size_t)s * kTileM * kTileK, &tmA, kt * kTileK, mta * kTileM, J.e, &full[s]);
+                        tma_load_3d(sA + (size_t)s * kTileM * kTileK, &tmA, kt * kTileK, J.mt * kTileM, J.e, &full[s]);
                         for (int c = 0; c < brows; c += a.bbox)
                             tma_load_2d(sB + (size_t)s * a.bsr * kTileK + (size_t)c * kTileK, &tmB, kt * kTileK,
                                         brow + c, &full[s]);
-                        if (has_a)
-                            for (int j = 0; j < n2; j++)  // the two K tiles' A blocks are nmt blocks apart
-                                bulk_g2s_l2(sSFA + (size_t)s * 1024 + 512 * j, sfa_src + (size_t)j * a.nmt * 512,
-                                            512u, &full[s]);
+                        for (int j = 0; j < n2; j++)  // the two K tiles' A blocks are nmt blocks apart
+                            bulk_g2s_l2(sSFA + (size_t)s * 1024 + 512 * j, sfa_src + (size_t)j * a.nmt * 512, 512u,
+                                        &full[s]);
                         // the n2 K tiles' atoms (or interleaved 1 KB two-atom blocks) are adjacent
                         bulk_g2s_l2(sSFB + (size_t)s * 2 * sfbk, sfb_src, (uint32_t)n2 * sfbk, &full[s]);
                     }
                 } else {
-                    const int brows =
-                        PAIR ? a.bbox : (a.bbox == a.BN ? a.BN : (J.nn() + 15) / 16 * 16);  // B rows copied
+                    const int brows = a.bbox == a.BN ? a.BN : (J.nn() + 15) / 16 * 16;  // B rows copied
                     const uint32_t tx =
                         (uint32_t)(tpi * kTileM * kTileK / 2 + brows * kTileK) + a_tiles * 512u + sfb_stage_bytes(nsfb);
                     const uint8_t *sfa_src =
-                        a.pool + (uint64_t)J.e * a.rec + a.a_sf_off + ((uint64_t)kt * a.nmt + mta) * 512;
+                        a.pool + (uint64_t)J.e * a.rec + a.a_sf_off + ((uint64_t)kt * a.nmt + J.mt) * 512;
                     const uint8_t *sfb_src = a.bscale + sf_tile_word(J.tile(), a.nkt, nsfb, kt, 0);
                     if (elect_one()) {
                         mbar_arrive_expect_tx(&full[s], tx);
-                        tma_load_3d(sA + (size_t)s * tpi * kTileM * kTileK, &tmA, kt * kTileK, mta * kTileM, J.e,
+                        tma_load_3d(sA + (size_t)s * tpi * kTileM * kTileK, &tmA, kt * kTileK, J.mt * kTileM, J.e,
                                     &full[s]);
                         for (int c = 0; c < brows; c += a.bbox)
                             tma_load_2d(sB + (size_t)s * a.bsr * kTileK + (size_t)c * kTileK, &tmB, kt * kTileK,
                                         brow + c, &full[s]);
-                        if (a_tiles > 0) bulk_g2s_l2(sSFA + (size_t)s * tpi * 512, sfa_src, a_tiles * 512u, &full[s]);
+                        bulk_g2s_l2(sSFA + (size_t)s * tpi * 512, sfa_src, a_tiles * 512u, &full[s]);
                         bulk_g2s_l2(sSFB + (size_t)s * sfb_stage_bytes(nsfb), sfb_src, sfb_stage_bytes(nsfb), &full[s]);
                     }
                 }
@@ -802,12 +749,10 @@ __global__ void __launch_bounds__(NT, GemmShape<NT>::kCtasPerSm)
         // The issue of a stage is a chain of dependent steps (wait, broadcast, scale
         // copies, MMAs, commit), so the warp first asks which of the next few stages
         // have landed (lane i polls stage kt + i, one vote) and issues all of those in
-        // one go; the abort flag is read only while a stage is still outstanding.  In a
-        // pair the even CTA issues for both (its barrier counts both CTAs' copies); the
-        // odd CTA's MMA warp only waits for the last commit.
+        // one go; the abort flag is read only while a stage is still outstanding.
         int jb = 0, s = 0;  // tiles; slot of the next stage
         uint32_t ph = 0;    // its phase parity
-        bool run = !PAIR || rank == 0;
+        bool run = true;
         // Descriptors of slot 0, built once: a stage's descriptors add the stage's
         // offset in 16-byte units to the start-address field (shared addresses stay
         // below 2^18, so the 14-bit field never carries into the next one).
@@ -821,21 +766,17 @@ __global__ void __launch_bounds__(NT, GemmShape<NT>::kCtasPerSm)
         const uint32_t sfb_rg = nsfb == 1 ? 128u : 256u;
         const uint64_t sfbdesc0 = smem_desc(smem_u32(sSFB), sfb_rg, sfb_rg, kSwizzleNone);
         const int nlook = min(4, ns);  // stages polled at once (never past the ring)
-        const int mma_m = PAIR ? 2 * kTileM : kTileM;
-        for (JobIter J(a, nu, first, stride); run && J.valid(); J.next(), jb++) {
-            const int nmma = J.nmma();
+        for (JobIter J(a, nu); run && J.valid(); J.next(), jb++) {
+            const int nmma = (J.nn() + 15) / 16 * 16;
             // mxf8f6f4: + ks * kIdescSfStep for K step ks; mxf4: + kIdescSf2 for odd ks
-            const uint32_t idesc0 = FP4 ? idesc_mxf4(nmma, mma_m) : idesc_mxf8f6f4(nmma, 0, mma_m);
+            const uint32_t idesc0 = FP4 ? idesc_mxf4(nmma) : idesc_mxf8f6f4(nmma, 0);
             // accumulator buffer of tile jb and its use count
             const int buf = a.nacc == 2 ? (jb & 1) : 0;
             const uint32_t use = a.nacc == 2 ? (uint32_t)(jb >> 1) : (uint32_t)jb;
-            // the epilogue has finished with this accumulator (nacc tiles ago; in a pair,
-            // the epilogues of both CTAs)
+            // the epilogue has finished with this accumulator (nacc tiles ago)
             int okl = 1;
-            if (lane == 0)
-                okl = PAIR ? mbar_wait_cluster_or_abort(&acc_empty[buf], (use & 1u) ^ 1u, a.st, 0x680u + buf,
-                                                        abort_flag)
-                           : mbar_wait_or_abort(&acc_empty[buf], (use & 1u) ^ 1u, a.st, 0x680u + buf, abort_flag);
+            if (lane == 0) okl = mbar_wait_or_abort(&acc_empty[buf], (use & 1u) ^ 1u, a.st, 0x680u + buf,
+                                                    abort_flag);
             if (!__shfl_sync(0xffffffffu, okl, 0)) {
                 if (lane == 0) *abort_flag = 1;
                 break;
@@ -879,66 +820,37 @@ __global__ void __launch_bounds__(NT, GemmShape<NT>::kCtasPerSm)
                             const int n2 = min(2, a.nkt_sf - 2 * (kt + q));
                             const uint32_t sfb_t4 = sfa_t + 8u, bw = 4u * (uint32_t)nsfb;
                             for (int j = 0; j < n2; j++) {
-                                if (PAIR)
-                                    tc_cp_sf_pair(sfa_t + 4u * j, sfad + (uint64_t)(32 * j));
-                                else
-                                    tc_cp_sf(sfa_t + 4u * j, sfad + (uint64_t)(32 * j));
-                                for (int b = 0; b < nsfb; b++) {
-                                    // one atom, or the two atoms of the 1 KB block (rows 128 bytes apart)
-                                    const uint64_t d = nsfb == 1 ? sfbd + (uint64_t)(32 * j)
-                                                                 : sfbd + (uint64_t)(64 * j + 8 * b);
-                                    if (PAIR)
-                                        tc_cp_sf_pair(sfb_t4 + bw * j + 4u * b, d);
-                                    else
-                                        tc_cp_sf(sfb_t4 + bw * j + 4u * b, d);
+                                tc_cp_sf(sfa_t + 4u * j, sfad + (uint64_t)(32 * j));
+                                if (nsfb == 1) {
+                                    tc_cp_sf(sfb_t4 + 4u * j, sfbd + (uint64_t)(32 * j));
+                                } else {
+                                    // the two atoms of the 1 KB block: rows 128 bytes apart in it
+                                    tc_cp_sf(sfb_t4 + 8u * j, sfbd + (uint64_t)(64 * j));
+                                    tc_cp_sf(sfb_t4 + 8u * j + 4u, sfbd + (uint64_t)(64 * j + 8));
                                 }
                             }
-                            for (int ks = 0; ks < 2 * n2; ks++) {
-                                const uint32_t id = idesc0 + ((ks & 1) ? kIdescSf2 : 0u);
-                                const uint32_t accum = (kt + q > 0 || ks > 0) ? 1u : 0u;
-                                if (PAIR)
-                                    tc_mma_f4_pair(acc, ad0 + (uint64_t)(2 * ks), bd0 + (uint64_t)(2 * ks), id,
-                                                   sfa_t + 4u * (ks >> 1), sfb_t4 + bw * (ks >> 1), accum);
-                                else
-                                    tc_mma_f4(acc, ad0 + (uint64_t)(2 * ks), bd0 + (uint64_t)(2 * ks), id,
-                                              sfa_t + 4u * (ks >> 1), sfb_t4 + bw * (ks >> 1), accum);
-                            }
+                            for (int ks = 0; ks < 2 * n2; ks++)
+                                tc_mma_f4(acc, ad0 + (uint64_t)(2 * ks), bd0 + (uint64_t)(2 * ks),
+                                          idesc0 + ((ks & 1) ? kIdescSf2 : 0u), sfa_t + 4u * (ks >> 1),
+                                          sfb_t4 + bw * (ks >> 1), (kt + q > 0 || ks > 0) ? 1u : 0u);
                         } else {
-                            for (int t = 0; t < tpi; t++) {
-                                if (PAIR)
-                                    tc_cp_sf_pair(sfa_t + 4u * t, sfad + (uint64_t)(32 * t));
-                                else
-                                    tc_cp_sf(sfa_t + 4u * t, sfad + (uint64_t)(32 * t));  // 512 B apart
-                            }
-                            for (int b = 0; b < nsfb; b++) {
-                                // one atom, or the two atoms of the 1 KB block (rows 128 bytes apart)
-                                if (PAIR)
-                                    tc_cp_sf_pair(sfb_t + 4u * b, sfbd + (uint64_t)(8 * b));
-                                else
-                                    tc_cp_sf(sfb_t + 4u * b, sfbd + (uint64_t)(8 * b));
-                            }
+                            for (int t = 0; t < tpi; t++)
+                                tc_cp_sf(sfa_t + 4u * t, sfad + (uint64_t)(32 * t));  // 512 B apart
+                            tc_cp_sf(sfb_t, sfbd);
+                            if (nsfb == 2) tc_cp_sf(sfb_t + 4u, sfbd + 8u);  // the block's second atom
                             for (int t = 0; t < tpi; t++) {
                                 // tile t: rows 128t.. of the stage's A (16 KB apart), accumulator columns t*BN..
                                 const uint64_t adt = ad0 + (uint64_t)(1024 * t);
 #pragma unroll
                                 for (int ks = 0; ks < kTileK / 32; ks++) {
                                     // K step ks: 32 bytes further along both operands' rows
-                                    const uint32_t id = idesc0 + (uint32_t)ks * kIdescSfStep;
-                                    const uint32_t accum = (kt + q > 0 || ks > 0) ? 1u : 0u;
-                                    if (PAIR)
-                                        tc_mma_pair(acc + (uint32_t)(t * a.BN), adt + (uint64_t)(2 * ks),
-                                                    bd0 + (uint64_t)(2 * ks), id, sfa_t + 4u * t, sfb_t, accum);
-                                    else
-                                        tc_mma(acc + (uint32_t)(t * a.BN), adt + (uint64_t)(2 * ks),
-                                               bd0 + (uint64_t)(2 * ks), id, sfa_t + 4u * t, sfb_t, accum);
+                                    tc_mma(acc + (uint32_t)(t * a.BN), adt + (uint64_t)(2 * ks),
+                                           bd0 + (uint64_t)(2 * ks), idesc0 + (uint32_t)ks * kIdescSfStep,
+                                           sfa_t + 4u * t, sfb_t, (kt + q > 0 || ks > 0) ? 1u : 0u);
                                 }
                             }
                         }
-                        // frees the stage (in both CTAs of a pair) when these MMAs have read it
-                        if (PAIR)
-                            tc_commit_pair(&empty[sq]);
-                        else
-                            tc_commit(&empty[sq]);
+                        tc_commit(&empty[sq]);  // frees the stage when these MMAs have read it
                         if (++sq == ns) sq = 0;
                     }
                 }
@@ -950,25 +862,12 @@ __global__ void __launch_bounds__(NT, GemmShape<NT>::kCtasPerSm)
                     ph ^= 1u;
                 }
             }
-            // the accumulator is complete (or as far as it got)
-            if (elect_one()) {
-                if (PAIR)
-                    tc_commit_pair(&acc_full[buf]);
-                else
-                    tc_commit(&acc_full[buf]);
-            }
+            if (elect_one()) tc_commit(&acc_full[buf]);  // the accumulator is complete (or as far as it got)
             __syncwarp();
         }
         // every MMA this warp issued has finished before TMEM can be released (also
         // after an abort, when the epilogue may not wait for the last accumulator)
-        if (!PAIR || rank == 0) {
-            if (elect_one()) {
-                if (PAIR)
-                    tc_commit_pair(mma_done);
-                else
-                    tc_commit(mma_done);
-            }
-        }
+        if (elect_one()) tc_commit(mma_done);
         __syncwarp();
         if (lane == 0) mbar_wait(mma_done, 0u, a.st, 0x6c0u);
         __syncwarp();
@@ -976,10 +875,297 @@ __global__ void __launch_bounds__(NT, GemmShape<NT>::kCtasPerSm)
         // ------------------------------------------------------- epilogue
         const int ew = warp & 3, wg = (warp - Shape::kEpiFirst) >> 2;
         float *amax_g = amax_x + 64 * wg;
-        // a pair's odd CTA reports a drained accumulator to the even CTA's barrier
-        const uint32_t acc_empty_r = PAIR ? mapa_shared(acc_empty, 0u) : 0u;
         int jb = 0;
-        for (JobIter J(a, nu, first, stride); J.valid(); J.next(), jb++) {
+        for (JobIter J(a, nu); J.valid(); J.next(), jb++) {
+            const int buf = a.nacc == 2 ? (jb & 1) : 0;
+            const uint32_t use = a.nacc == 2 ? (uint32_t)(jb >> 1) : (uint32_t)jb;
+            const int nn = J.nn(), nmma = (nn + 15) / 16 * 16;
+            bool okl = !*(volatile int *)abort_flag && mbar_wait(&acc_full[buf], use & 1u, a.st, 0x800u + buf);
+            if (!okl) *abort_flag = 1;
+            const bool ok = __all_sync(0xffffffffu, okl);  // warp-uniform for the .sync.aligned loads
+            tc_fence_after();
+            for (int t = 0; t < tpi; t++) {
+                if (J.mt + t >= a.nmt) break;  // a half item past the expert's A rows (uniform)
+                const uint32_t lane_base =
+                    tmem + (uint32_t)((buf * tpi + t) * a.BN) + ((uint32_t)(32 * ew) << 16);
+                if (FP4 && a.nparts == 5)
+                    epilogue_split5_f4(a, lane_base, ok, nn, nmma, J.mt + t, J.row0, J.n0(), J.tile(), ew, wg,
+                                       Shape::kWarpGroups, lane, amax_g);
+                else
+                    epilogue_mx1<FP4>(a, lane_base, ok, nn, nmma, J.mt + t, J.row0, J.n0(), J.tile(), ew, wg,
+                                      Shape::kWarpGroups, lane, amax_g);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acc_empty[buf]);
+            // no early exit: after an abort the waits are skipped, and both warps of
+            // each pair run the same sequence of named barriers to the end
+        }
+    }
+    // nothing may still be in flight when TMEM is released and the CTA exits
+    if (warp == 0 && lane == 0) {
+        for (int it = max(0, it_issued - ns); it < it_issued; it++)
+            mbar_wait(&full[it % ns], (uint32_t)(it / ns) & 1u, a.st, 0x900u);
+    }
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem, a.tmem_cols);
+}
+
+// The work of a CTA pair: items i = pair, pair + pairs, ... of the (expert of the union,
+// two 128-row tiles of A) items, one tile per CTA; each item's columns in tiles of BN.
+// Both CTAs walk this same sequence with all their roles.
+struct PairJobIter {
+    const GemmArgs &a;
+    int nu, i, nt, ntile, e, mt, row0, nrows, tile0;
+    __device__ PairJobIter(const GemmArgs &args, int nu_) : a(args), nu(nu_), i((int)blockIdx.x / 2), nt(0), ntile(0) {
+        load();
+    }
+    __device__ int items_per_expert() const { return (a.nmt + 1) / 2; }
+    __device__ void load() {
+        ntile = 0;
+        const int nwi = items_per_expert();
+        while (i < nu * nwi) {
+            const int u = i / nwi;
+            mt = (i % nwi) * 2;  // the even CTA's 128-row tile of the item
+            e = a.uexp[u];
+            row0 = a.offsets[e];
+            nrows = a.offsets[e + 1] - a.offsets[e];
+            ntile = (nrows + a.BN - 1) / a.BN;
+            tile0 = a.tile_off[e];
+            if (ntile > 0) break;
+            i += (int)gridDim.x / 2;
+        }
+        nt = 0;
+    }
+    __device__ bool valid() const { return i < nu * items_per_expert() && ntile > 0; }
+    __device__ int n0() const { return nt * a.BN; }
+    __device__ int tile() const { return tile0 + nt; }
+    __device__ int nn() const { return min(a.BN, nrows - nt * a.BN); }  // columns of the tile
+    __device__ int nmma() const { return (nn() + 15) / 16 * 16; }       // MMA width
+    __device__ void next() {
+        if (++nt >= ntile) {
+            i += (int)gridDim.x / 2;
+            load();
+        }
+    }
+};
+
+// The grouped GEMM on CTA pairs (one-part rows, tiles of 128+ columns): clusters of two
+// CTAs of 384 threads, one per SM, the same roles as grouped_gemm_kernel<384>.  The even
+// CTA (rank 0) issues MMAs of M = 256 for both: A's rows 256 i.. (128 per CTA), B's
+// columns split in halves (the even CTA the first nmma / 2).  Each CTA copies its own
+// operands (its A tile, its half of B's rows, its A scale atoms and all of B's scale
+// factors) with tensor copies whose completion counts on the even CTA's barrier, which
+// expects the bytes of both; the even CTA's commits arrive in both CTAs; the odd CTA's
+// epilogue reports a drained accumulator to the even CTA's barrier.  Boxes past the end
+// of a tensor (the odd CTA's A tile beyond the expert's last, the scales of the next K
+// tile) arrive zero-filled and count whole.
+template <bool FP4>
+__global__ void __launch_bounds__(384, 1)
+    grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                             const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
+                             const GemmArgs a) {
+    using Shape = GemmShape<384>;
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    // the tensor copies with 128-byte swizzling need 1024-byte aligned tiles
+    unsigned char *smem = (unsigned char *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    const int ns = a.ns;
+    const GemmSmemLayout L(a.BN, ns, 1, FP4, a.bsr);
+    uint8_t *sA = smem + L.a, *sB = smem + L.b, *sSFA = smem + L.sfa, *sSFB = smem + L.sfb;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.bars);
+    uint64_t *empty = full + kMaxStages;
+    uint64_t *acc_full = empty + kMaxStages;
+    uint64_t *acc_empty = acc_full + 2;
+    uint64_t *mma_done = acc_empty + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L.misc);
+    int *abort_flag = reinterpret_cast<int *>(smem + L.misc + 4);
+    float *amax_x = reinterpret_cast<float *>(smem + L.misc + 16);  // [8 epilogue warps][16 columns]
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int rank = (int)cluster_ctarank();
+    const int nu = *a.n_union;
+    if ((int)blockIdx.x / 2 >= nu * ((a.nmt + 1) / 2)) return;  // both CTAs of the pair, before any barrier
+    const int nsfb = a.nsfb;
+
+    // the unpacked E2M1 copies (MXFP8 rows) write 8 of every 16 bytes of an A tile: keep
+    // the other 8 zero
+    for (int i = threadIdx.x; i < ns * kTileM * kTileK / 16; i += 384)
+        reinterpret_cast<uint4 *>(sA)[i] = make_uint4(0u, 0u, 0u, 0u);
+    fence_proxy_async_smem();
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < ns; s++) {
+            mbar_init(&full[s], 1);   // the even CTA's producer's expect-tx arrival
+            mbar_init(&empty[s], 1);  // the even CTA's MMA commit
+        }
+        for (int b = 0; b < 2; b++) {
+            mbar_init(&acc_full[b], 1);                        // MMA commit after a tile's last K step
+            mbar_init(&acc_empty[b], 2 * Shape::kEpiWarps);  // the epilogue warps of both CTAs
+        }
+        mbar_init(mma_done, 1);  // the last commit
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) tmem_alloc_pair(tmem_slot, a.tmem_cols);
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();  // the other CTA's barriers exist before anything arrives on them
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t sf_col0 = (uint32_t)(a.nacc * a.BN);  // scale factors after the accumulators
+    // TMEM columns per stage: 4 per 512-byte scale atom (two atoms per operand with FP4)
+    const uint32_t sf_stage = FP4 ? 8u + 8u * (uint32_t)nsfb : 4u + 4u * (uint32_t)nsfb;
+    const uint32_t sfbk = sfb_stage_bytes(nsfb);  // B scale bytes per 128-K tile
+
+    int it_issued = 0;  // producer: stages issued
+    if (warp == 0) {
+        // ------------------------------------------------------- tensor copies
+        const uint32_t full_lead = mapa_shared(full, 0u);  // the even CTA's full[0]
+        int it = 0, s = 0;  // stages issued; slot of stage it
+        uint32_t ph = 0;    // phase parity of slot s's use by stage it
+        bool run = true;
+        for (PairJobIter J(a, nu); run && J.valid(); J.next()) {
+            const int mta = J.mt + rank;                           // this CTA's A row tile
+            const int brow = J.row0 + J.n0() + rank * (J.nmma() / 2);  // and its first B row
+            for (int kt = 0; kt < a.nkt; kt++, it++) {
+                int okl = 1;
+                if (lane == 0) okl = mbar_wait_or_abort(&empty[s], ph ^ 1u, a.st, 0x500u + s, abort_flag);
+                if (!__shfl_sync(0xffffffffu, okl, 0)) {
+                    if (lane == 0) *abort_flag = 1;
+                    run = false;
+                    break;
+                }
+                // A: 128 rows (MXFP8 rows: unpacked by the copy, counted packed); B: this
+                // CTA's half of the rows; A's scale atoms of the stage's 128-K tiles (nmt
+                // atoms apart); one box of B's scale rows (both K tiles with FP4 rows)
+                const int n2 = FP4 ? min(2, a.nkt_sf - 2 * kt) : 1;
+                const int kt0 = FP4 ? 2 * kt : kt;  // first 128-K tile of the stage
+                const uint32_t tx = (uint32_t)(FP4 ? kTileM * kTileK : kTileM * kTileK / 2) +
+                                    (uint32_t)(a.bbox * kTileK) + (uint32_t)n2 * 512u + (FP4 ? 2u : 1u) * sfbk;
+                const uint32_t fbar = full_lead + 8u * (uint32_t)s;
+                if (elect_one()) {
+                    if (rank == 0) mbar_arrive_expect_tx(&full[s], 2u * tx);  // both CTAs' bytes
+                    tma_load_3d_pair(sA + (size_t)s * kTileM * kTileK, &tmA, kt * kTileK, mta * kTileM, J.e, fbar);
+                    tma_load_2d_pair(sB + (size_t)s * a.bsr * kTileK, &tmB, kt * kTileK, brow, fbar);
+                    for (int j = 0; j < n2; j++)
+                        tma_load_3d_pair(sSFA + (size_t)s * L.sfa_stage + 512 * j, &tmSA, 0, (kt0 + j) * a.nmt + mta,
+                                         J.e, fbar);
+                    tma_load_2d_pair(sSFB + (size_t)s * L.sfb_stage, &tmSB, 0, J.tile() * a.nkt_sf + kt0, fbar);
+                }
+                __syncwarp();
+                it_issued = it + 1;
+                if (++s == ns) {
+                    s = 0;
+                    ph ^= 1u;
+                }
+            }
+        }
+    } else if (warp == 1 && rank == 0) {
+        // ------------------------------------------------------- MMA issue (even CTA)
+        // as in grouped_gemm_kernel: poll the next few stages at once and issue every
+        // landed one; the scale copies, MMAs and commits act on both CTAs
+        int jb = 0, s = 0;  // tiles; slot of the next stage
+        uint32_t ph = 0;    // its phase parity
+        bool run = true;
+        const uint32_t a_stage16 = (uint32_t)(kTileM * kTileK) >> 4, b_stage16 = (uint32_t)(a.bsr * kTileK) >> 4;
+        const uint32_t sfa_stage16 = L.sfa_stage >> 4, sfb_stage16 = L.sfb_stage >> 4;
+        const uint64_t adesc0 = smem_desc(smem_u32(sA), 16, 1024, kSwizzle128B);
+        const uint64_t bdesc0 = smem_desc(smem_u32(sB), 16, 1024, kSwizzle128B);
+        const uint64_t sfadesc0 = smem_desc(smem_u32(sSFA), 128, 128, kSwizzleNone);
+        const uint32_t sfb_rg = nsfb == 1 ? 128u : 256u;  // row groups of a B atom (256: two-atom block)
+        const uint64_t sfbdesc0 = smem_desc(smem_u32(sSFB), sfb_rg, sfb_rg, kSwizzleNone);
+        const int nlook = min(4, ns);
+        for (PairJobIter J(a, nu); run && J.valid(); J.next(), jb++) {
+            const int nmma = J.nmma();
+            const uint32_t idesc0 = FP4 ? idesc_mxf4(nmma, 2 * kTileM) : idesc_mxf8f6f4(nmma, 0, 2 * kTileM);
+            const int buf = a.nacc == 2 ? (jb & 1) : 0;
+            const uint32_t use = a.nacc == 2 ? (uint32_t)(jb >> 1) : (uint32_t)jb;
+            // both CTAs' epilogues have finished with this accumulator
+            int okl = 1;
+            if (lane == 0)
+                okl = mbar_wait_cluster_or_abort(&acc_empty[buf], (use & 1u) ^ 1u, a.st, 0x680u + buf, abort_flag);
+            if (!__shfl_sync(0xffffffffu, okl, 0)) {
+                if (lane == 0) *abort_flag = 1;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t acc = tmem + (uint32_t)(buf * a.BN);
+            for (int kt = 0; kt < a.nkt;) {
+                const int want = min(nlook, a.nkt - kt);
+                bool rl = false;
+                if (lane < want) {
+                    const int q = s + lane;
+                    rl = mbar_try_wait(&full[q % ns], ph ^ ((uint32_t)(q / ns) & 1u));
+                }
+                const uint32_t ready = __ballot_sync(0xffffffffu, rl);
+                int r = min(__ffs(~ready) - 1, want);
+                if (r == 0) {
+                    okl = 1;
+                    if (lane == 0) okl = mbar_wait_or_abort(&full[s], ph, a.st, 0x700u + s, abort_flag);
+                    if (!__shfl_sync(0xffffffffu, okl, 0)) {
+                        if (lane == 0) *abort_flag = 1;
+                        run = false;
+                        break;
+                    }
+                    r = 1;
+                }
+                tc_fence_after();
+                if (elect_one()) {
+                    int sq = s;
+                    for (int q = 0; q < r; q++) {
+                        const uint32_t sfa_t = tmem + sf_col0 + (uint32_t)sq * sf_stage;
+                        const uint64_t sfad = sfadesc0 + (uint64_t)((uint32_t)sq * sfa_stage16);
+                        const uint64_t sfbd = sfbdesc0 + (uint64_t)((uint32_t)sq * sfb_stage16);
+                        const uint64_t ad0 = adesc0 + (uint64_t)((uint32_t)sq * a_stage16);
+                        const uint64_t bd0 = bdesc0 + (uint64_t)((uint32_t)sq * b_stage16);
+                        if constexpr (FP4) {
+                            const int n2 = min(2, a.nkt_sf - 2 * (kt + q));
+                            const uint32_t sfb_t4 = sfa_t + 8u, bw = 4u * (uint32_t)nsfb;
+                            for (int j = 0; j < n2; j++) {
+                                tc_cp_sf_pair(sfa_t + 4u * j, sfad + (uint64_t)(32 * j));
+                                for (int b = 0; b < nsfb; b++)  // one atom, or the two of the 1 KB block
+                                    tc_cp_sf_pair(sfb_t4 + bw * j + 4u * b,
+                                                  sfbd + (uint64_t)(nsfb == 1 ? 32 * j : 64 * j + 8 * b));
+                            }
+                            for (int ks = 0; ks < 2 * n2; ks++)
+                                tc_mma_f4_pair(acc, ad0 + (uint64_t)(2 * ks), bd0 + (uint64_t)(2 * ks),
+                                               idesc0 + ((ks & 1) ? kIdescSf2 : 0u), sfa_t + 4u * (ks >> 1),
+                                               sfb_t4 + bw * (ks >> 1), (kt + q > 0 || ks > 0) ? 1u : 0u);
+                        } else {
+                            const uint32_t sfb_t = sfa_t + 4u;
+                            tc_cp_sf_pair(sfa_t, sfad);
+                            for (int b = 0; b < nsfb; b++) tc_cp_sf_pair(sfb_t + 4u * b, sfbd + (uint64_t)(8 * b));
+#pragma unroll
+                            for (int ks = 0; ks < kTileK / 32; ks++)
+                                tc_mma_pair(acc, ad0 + (uint64_t)(2 * ks), bd0 + (uint64_t)(2 * ks),
+                                            idesc0 + (uint32_t)ks * kIdescSfStep, sfa_t, sfb_t,
+                                            (kt + q > 0 || ks > 0) ? 1u : 0u);
+                        }
+                        tc_commit_pair(&empty[sq]);  // frees the stage in both CTAs
+                        if (++sq == ns) sq = 0;
+                    }
+                }
+                __syncwarp();
+                kt += r;
+                s += r;
+                if (s >= ns) {
+                    s -= ns;
+                    ph ^= 1u;
+                }
+            }
+            if (elect_one()) tc_commit_pair(&acc_full[buf]);  // the accumulator is complete (or as far as it got)
+            __syncwarp();
+        }
+        // every MMA has finished before TMEM is released (in both CTAs)
+        if (elect_one()) tc_commit_pair(mma_done);
+        __syncwarp();
+    } else if (warp >= Shape::kEpiFirst) {
+        // ------------------------------------------------------- epilogue
+        const int ew = warp & 3, wg = (warp - Shape::kEpiFirst) >> 2;
+        float *amax_g = amax_x + 64 * wg;
+        const uint32_t acc_empty_lead = mapa_shared(acc_empty, 0u);  // the even CTA's acc_empty[0]
+        int jb = 0;
+        for (PairJobIter J(a, nu); J.valid(); J.next(), jb++) {
             const int buf = a.nacc == 2 ? (jb & 1) : 0;
             const uint32_t use = a.nacc == 2 ? (uint32_t)(jb >> 1) : (uint32_t)jb;
             const int nn = J.nn(), nmma = J.nmma();
@@ -987,51 +1173,38 @@ __global__ void __launch_bounds__(NT, GemmShape<NT>::kCtasPerSm)
             if (!okl) *abort_flag = 1;
             const bool ok = __all_sync(0xffffffffu, okl);  // warp-uniform for the .sync.aligned loads
             tc_fence_after();
-            for (int t = 0; t < (PAIR ? 1 : tpi); t++) {
-                const int mt = J.mt + (PAIR ? rank : t);
-                if (mt >= a.nmt) break;  // a half item past the expert's A rows (uniform)
-                const uint32_t lane_base =
-                    tmem + (uint32_t)((buf * tpi + t) * a.BN) + ((uint32_t)(32 * ew) << 16);
-                if (FP4 && a.nparts == 5)
-                    epilogue_split5_f4(a, lane_base, ok, nn, nmma, mt, J.row0, J.n0(), J.tile(), ew, wg,
-                                       Shape::kWarpGroups, lane, amax_g);
-                else
-                    epilogue_mx1<FP4>(a, lane_base, ok, nn, nmma, mt, J.row0, J.n0(), J.tile(), ew, wg,
-                                      Shape::kWarpGroups, lane, amax_g);
+            const int mt = J.mt + rank;  // this CTA's 128 rows of the tile
+            if (mt < a.nmt) {            // (uniform) the odd CTA's tile may lie past the expert's rows
+                const uint32_t lane_base = tmem + (uint32_t)(buf * a.BN) + ((uint32_t)(32 * ew) << 16);
+                epilogue_mx1<FP4>(a, lane_base, ok, nn, nmma, mt, J.row0, J.n0(), J.tile(), ew, wg,
+                                  Shape::kWarpGroups, lane, amax_g);
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) {
-                if (PAIR && rank == 1)
-                    mbar_arrive_cluster(acc_empty_r + (uint32_t)(8 * buf));
+                if (rank == 1)
+                    mbar_arrive_cluster(acc_empty_lead + (uint32_t)(8 * buf));
                 else
                     mbar_arrive(&acc_empty[buf]);
             }
-            // no early exit: after an abort the waits are skipped, and both warps of
-            // each pair run the same sequence of named barriers to the end
         }
     }
-    // nothing may still be in flight when TMEM is released and the CTA exits: this
-    // CTA's copies (a pair's odd CTA counts its copies on the even CTA's barrier; they
-    // have landed once the MMAs that read them have committed onto its own stages)
+    // Nothing may still be in flight when TMEM is released and the CTA exits: the even
+    // CTA waits for the last stages' copies (of both CTAs) and both wait for the last
+    // commit (and with it every commit onto their stages) before the final cluster barrier.
     if (warp == 0 && lane == 0) {
-        if (!PAIR || rank == 0)
+        if (rank == 0)
             for (int it = max(0, it_issued - ns); it < it_issued; it++)
                 mbar_wait(&full[it % ns], (uint32_t)(it / ns) & 1u, a.st, 0x900u);
-        if (PAIR)
-            for (int it = max(0, it_issued - ns); it < it_issued; it++)
-                mbar_wait(&empty[it % ns], (uint32_t)(it / ns) & 1u, a.st, 0x940u);
+        for (int it = max(0, it_issued - ns); it < it_issued; it++)
+            mbar_wait(&empty[it % ns], (uint32_t)(it / ns) & 1u, a.st, 0x940u);
     }
+    if (warp == 1 && lane == 0) mbar_wait(mma_done, 0u, a.st, 0x6c0u);
     tc_fence_before();
     __syncthreads();
-    if (PAIR) cluster_sync();  // both CTAs are done with TMEM and with each other's barriers
+    cluster_sync();  // both CTAs are done with TMEM and with each other's barriers
     tc_fence_after();
-    if (warp == 1) {
-        if (PAIR)
-            tmem_dealloc_pair(tmem, a.tmem_cols);
-        else
-            tmem_dealloc(tmem, a.tmem_cols);
-    }
+    if (warp == 1) tmem_dealloc_pair(tmem, a.tmem_cols);
 }
 
 // ------------------------------------------------------------- tensor maps
@@ -1155,7 +1328,7 @@ int pair_capacity(size_t smem) {
         cudaLaunchAttribute attr[1];
         const cudaLaunchConfig_t cfg = pair_config(attr, sms / 2, smem, nullptr);
         int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, grouped_gemm_kernel<384, FP4, true>, &cfg) != cudaSuccess || n <= 0) {
+        if (cudaOccupancyMaxActiveClusters(&n, grouped_gemm_pair_kernel<FP4>, &cfg) != cudaSuccess || n <= 0) {
             (void)cudaGetLastError();
             n = -1;
         }
@@ -1170,7 +1343,7 @@ cudaError_t launch_pair(const CUtensorMap &mA, const CUtensorMap &mB, const CUte
                         const GemmArgs &ga, int pairs, size_t smem, cudaStream_t stream) {
     cudaLaunchAttribute attr[1];
     const cudaLaunchConfig_t cfg = pair_config(attr, pairs, smem, stream);
-    return cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<384, FP4, true>, mA, mB, mSA, mSB, ga);
+    return cudaLaunchKernelEx(&cfg, grouped_gemm_pair_kernel<FP4>, mA, mB, mSA, mSB, ga);
 }
 
 // One grouped GEMM launch (args complete but for the shape fields set here).  The
@@ -1215,8 +1388,8 @@ cudaError_t launch_one(GemmArgs ga, const uint8_t *a_base, int a_k, int a_rows, 
     const size_t smem = smem_need(ns);
     int pairs = 0;
     if (ga.pair) {
-        e = fp4 ? ensure_dynamic_smem(grouped_gemm_kernel<384, true, true>, smem, g_smem_set_pairf4)
-                : ensure_dynamic_smem(grouped_gemm_kernel<384, false, true>, smem, g_smem_set_pair);
+        e = fp4 ? ensure_dynamic_smem(grouped_gemm_pair_kernel<true>, smem, g_smem_set_pairf4)
+                : ensure_dynamic_smem(grouped_gemm_pair_kernel<false>, smem, g_smem_set_pair);
         if (e != cudaSuccess) return e;
         pairs = fp4 ? pair_capacity<true>(smem) : pair_capacity<false>(smem);
         if (pairs == 0) {
@@ -1227,11 +1400,11 @@ cudaError_t launch_one(GemmArgs ga, const uint8_t *a_base, int a_k, int a_rows, 
                               fp4);
         }
     } else if (fp4)
-        e = two ? ensure_dynamic_smem(grouped_gemm_kernel<192, true, false>, smem, g_smem_set_192f4)
-                : ensure_dynamic_smem(grouped_gemm_kernel<384, true, false>, smem, g_smem_set_384f4);
+        e = two ? ensure_dynamic_smem(grouped_gemm_kernel<192, true>, smem, g_smem_set_192f4)
+                : ensure_dynamic_smem(grouped_gemm_kernel<384, true>, smem, g_smem_set_384f4);
     else
-        e = two ? ensure_dynamic_smem(grouped_gemm_kernel<192, false, false>, smem, g_smem_set_192)
-                : ensure_dynamic_smem(grouped_gemm_kernel<384, false, false>, smem, g_smem_set_384);
+        e = two ? ensure_dynamic_smem(grouped_gemm_kernel<192, false>, smem, g_smem_set_192)
+                : ensure_dynamic_smem(grouped_gemm_kernel<384, false>, smem, g_smem_set_384);
     if (e != cudaSuccess) return e;
     ga.ns = ns;
     ga.tpi = tpi;
@@ -1269,21 +1442,21 @@ cudaError_t launch_one(GemmArgs ga, const uint8_t *a_base, int a_k, int a_rows, 
     } else if (fp4) {
         // (the multi-token decode's chain of kernels launches each one early)
         if (two && ga.nparts > 1)
-            e = launch_pdl(grouped_gemm_kernel<192, true, false>, dim3(std::min(2 * sms, items)), dim3(192), smem, stream,
-                           mA, mB, mSA, mSB, ga);
+            e = launch_pdl(grouped_gemm_kernel<192, true>, dim3(std::min(2 * sms, items)), dim3(192), smem, stream,
+                           mA, mB, ga);
         else if (two)
-            grouped_gemm_kernel<192, true, false><<<std::min(2 * sms, items), 192, smem, stream>>>(mA, mB, mSA, mSB, ga);
+            grouped_gemm_kernel<192, true><<<std::min(2 * sms, items), 192, smem, stream>>>(mA, mB, ga);
         else if (ga.nparts > 1)
-            e = launch_pdl(grouped_gemm_kernel<384, true, false>, dim3(std::min(sms, items)), dim3(384), smem, stream, mA,
-                           mB, mSA, mSB, ga);
+            e = launch_pdl(grouped_gemm_kernel<384, true>, dim3(std::min(sms, items)), dim3(384), smem, stream, mA,
+                           mB, ga);
         else
-            grouped_gemm_kernel<384, true, false><<<std::min(sms, items), 384, smem, stream>>>(mA, mB, mSA, mSB, ga);
+            grouped_gemm_kernel<384, true><<<std::min(sms, items), 384, smem, stream>>>(mA, mB, ga);
         if (e != cudaSuccess) return e;
     } else {
         if (two)
-            grouped_gemm_kernel<192, false, false><<<std::min(2 * sms, items), 192, smem, stream>>>(mA, mB, mSA, mSB, ga);
+            grouped_gemm_kernel<192, false><<<std::min(2 * sms, items), 192, smem, stream>>>(mA, mB, ga);
         else
-            grouped_gemm_kernel<384, false, false><<<std::min(sms, items), 384, smem, stream>>>(mA, mB, mSA, mSB, ga);
+            grouped_gemm_kernel<384, false><<<std::min(sms, items), 384, smem, stream>>>(mA, mB, ga);
     }
     return cudaGetLastError();
 }
