@@ -27,10 +27,10 @@
 // one-part tiles can also run on CTA pairs (grouped_gemm_pair_kernel: a cluster of two
 // CTAs on two SMs, tcgen05 MMAs of cta_group::2 with M = 256 issued by the even CTA;
 // each CTA copies its 128 weight rows and half of the tile's activation rows, and its
-// tensor copies count on the even CTA's barrier).  With five-part MXFP4 activations (nparts = 5, the
-// multi-token decode) each sorted pair has five B rows whose columns the epilogue sums.
-// Every wait is bounded (MOE_ERR_TIMEOUT), and nothing exits with copies or MMAs in
-// flight.
+// tensor copies count on the even CTA's barrier).  With five-part MXFP4 activations
+// (nparts = 5, the multi-token decode) each sorted pair has five B rows whose columns
+// the epilogue sums.  Every wait is bounded (MOE_ERR_TIMEOUT), and nothing exits with
+// copies or MMAs in flight.
 #include <algorithm>
 
 #include <cuda.h>
@@ -221,9 +221,9 @@ __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t
 }
 
 // Instruction descriptor of kind::mxf4: A and B E2M1 (format 1 of this kind), both
-// K-major, M = m (128, or 256 for a CTA pair), N = n, E8M0 scales.  With scale_vec::2X an MMA (K = 64) takes the
-// scale bytes sf_id, sf_id + 1 (sf_id 0 or 2) of a 32-bit TMEM column: add
-// kIdescSf2 for sf_id 2 (A and B alike).
+// K-major, M = m (128, or 256 for a CTA pair), N = n, E8M0 scales.  With
+// scale_vec::2X an MMA (K = 64) takes the scale bytes sf_id, sf_id + 1 (sf_id 0 or 2)
+// of a 32-bit TMEM column: add kIdescSf2 for sf_id 2 (A and B alike).
 constexpr uint32_t kIdescSf2 = (2u << 4) | (2u << 29);
 
 __device__ __forceinline__ uint32_t idesc_mxf4(int n, int m = kTileM) {
