@@ -276,9 +276,10 @@ __device__ __forceinline__ uint32_t mapa_shared(const void *p, uint32_t rank) {
     return r;
 }
 
-// Arrive on a barrier of the other CTA (release at cluster scope).
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+// `count` arrivals on a barrier of the other CTA (release at cluster scope).
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr, uint32_t count) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(cluster_addr), "r"(count)
+                 : "memory");
 }
 
 // try_wait with acquire at cluster scope: for phases completed by the other CTA's arrivals.
@@ -958,7 +959,8 @@ struct PairJobIter {
 // operands (its A tile, its half of B's rows, its A scale atoms and all of B's scale
 // factors) with tensor copies whose completion counts on the even CTA's barrier, which
 // expects the bytes of both; the even CTA's commits arrive in both CTAs; the odd CTA's
-// epilogue reports a drained accumulator to the even CTA's barrier.  Boxes past the end
+// epilogue reports a drained accumulator to the even CTA's barrier (one arrival per tile
+// for all its epilogue warps).  Boxes past the end
 // of a tensor (the odd CTA's A tile beyond the expert's last, the scales of the next K
 // tile) arrive zero-filled and count whole.
 template <bool FP4>
@@ -1180,12 +1182,15 @@ __global__ void __launch_bounds__(384, 1)
                                   Shape::kWarpGroups, lane, amax_g);
             }
             tc_fence_before();
-            __syncwarp();
-            if (lane == 0) {
-                if (rank == 1)
-                    mbar_arrive_cluster(acc_empty_lead + (uint32_t)(8 * buf));
-                else
-                    mbar_arrive(&acc_empty[buf]);
+            if (rank == 1) {
+                // the odd CTA: its epilogue warps meet, and one arrival of all of them
+                // (one cluster-scope release per tile, not one per warp)
+                named_barrier(6, Shape::kEpiWarps * 32);
+                if (warp == Shape::kEpiFirst && lane == 0)
+                    mbar_arrive_cluster(acc_empty_lead + (uint32_t)(8 * buf), (uint32_t)Shape::kEpiWarps);
+            } else {
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&acc_empty[buf]);
             }
         }
     }
