@@ -269,6 +269,8 @@ moe_status moe_prescale(const uint16_t *x, int M, int H, uint16_t *out, moe_stre
  * kind::mxf8f6f4 (the FP8 rate).  With MOE_ACT_MXFP4 the rows and h are quantised
  * to MXFP4 instead (E2M1 elements, shared exponent floor(log2 amax) - 2, RNE with
  * saturation at 6) and the MMAs are kind::mxf4 (both operands FP4: the FP4 rate).
+ * The tile shape (one CTA per 128 weight rows, or pairs of SMs for wide tiles) is set
+ * by moe_grouped_set_cta_pairs.
  * Out: partial [T*k][H] (partial_dtype MOE_PARTIAL_*), row r = o of pair perm[r]
  * (unweighted).  ws: MOE_OP_GROUPED bytes. */
 moe_status moe_expert_forward_grouped(const moe_pool *pool, const uint16_t *x, int T,
